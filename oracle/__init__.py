@@ -1,0 +1,238 @@
+"""ORACLE — test infrastructure, not part of the product.
+
+Python binding of ``ck_oracle.c``, the plain CPU restatement of curta-core's integer
+forward pass (page "The inference core", curta.chat docs).  Only ``tests/``,
+``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg may import this package.
+It imports nothing from the GPU library and the library imports nothing from it.
+
+Pin status (each function is checked in ``tests/test_oracle_pins.py`` against values the
+page fixes, closed forms, textbook routines or brute force):
+  isqrt, embed, rmsnorm, matrow, fits32, rotate, attention_head, silu, silu_gate, argmax,
+  page_state_size: pinned.
+  Whole-model token streams: parity unpinned against curta-core itself (the page prints no
+  tokens or logits for a model); pinned only through the per-step pins and invariants.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ck_oracle.c")
+_LIB = os.path.join(_HERE, "_oracle.so")
+_lib = None
+
+EVENT_NAMES = ("matrow_acc", "matrow_scale", "norm_squares", "norm_product", "rotary",
+               "score_dot", "score_scale", "silu_product", "residual")
+LAYOUT_NAMES = ("prompt", "out", "x", "xb", "q", "o", "y", "h", "logits", "scores", "k", "v", "size")
+
+# header offsets of the ids-mode state (format "CKSTATE1")
+H_PHASE, H_POSITION, H_NPROMPT, H_MAXTOK, H_CACHE, H_GENERATED = 8, 12, 16, 20, 24, 28
+H_FLAGS, H_TEMP, H_ERROR, H_LASTTOK, H_SEED, H_TURNS, H_ERRKEY, H_MAXLOGIT = 32, 36, 40, 44, 48, 56, 64, 72
+PHASE_RUNNING, PHASE_DONE, PHASE_FAILED = 3, 20, 21
+FLAG_STOP_TOKENS = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile ``ck_oracle.c`` into ``_oracle.so`` (gcc -O2, OpenMP over independent rows)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-o", tmp, _SRC])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+class TurnResult(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint32) for n in (
+        "complete", "generated", "generated_this_turn", "token", "work",
+        "err_position", "err_layer", "err_phase", "err_element")]
+
+    def as_dict(self) -> dict:
+        return {n: int(getattr(self, n)) for n, _ in self._fields_}
+
+
+def _lib_():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        vp, u32, u64, i64, i32 = ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int64, ctypes.c_int32
+        sig = {
+            "orc_isqrt": ([u64], u64),
+            "orc_embed": ([vp, u32, u32, vp], None),
+            "orc_rmsnorm": ([vp, vp, u32, vp], None),
+            "orc_matrow": ([vp, u64, vp, u32, u32, vp, vp], None),
+            "orc_fits32": ([i64], ctypes.c_int),
+            "orc_rotate": ([i64, i64, i32, i32, vp, vp], None),
+            "orc_attention_head": ([vp, vp, vp, u64, u32, u32, u32, vp, vp, vp], None),
+            "orc_silu": ([i64, vp], i64),
+            "orc_silu_gate": ([vp, vp, u32, vp, vp], None),
+            "orc_argmax": ([vp, u32], u32),
+            "orc_page_state_size": ([vp, u32, u32], u64),
+            "orc_model_open": ([vp, u64, ctypes.POINTER(vp)], ctypes.c_int),
+            "orc_model_close": ([vp], None),
+            "orc_state_size": ([vp, u32, u32], u64),
+            "orc_init_state": ([vp, vp, u64, vp, u32, u32, u32, u64, u32], ctypes.c_int),
+            "orc_turn": ([vp, vp, u64, u32, ctypes.POINTER(TurnResult)], ctypes.c_int),
+            "orc_state_layout": ([vp, u32, u32, vp], None),
+            "orc_events_reset": ([ctypes.c_int], None),
+            "orc_events_get": ([vp], None),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = lib
+    return _lib
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ------------------------------------------------------------------ single steps
+
+def isqrt(v: int) -> int:
+    return int(_lib_().orc_isqrt(v))
+
+
+def embed(row: np.ndarray, scale: int) -> np.ndarray:
+    row = _c(row, np.uint8)
+    out = np.zeros(row.size, dtype=np.int64)
+    _lib_().orc_embed(row.ctypes.data, scale, row.size, out.ctypes.data)
+    return out
+
+
+def rmsnorm(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    x, w = _c(x, np.int64), _c(w, np.int32)
+    assert x.size == w.size and x.size > 0
+    out = np.zeros(x.size, dtype=np.int64)
+    _lib_().orc_rmsnorm(x.ctypes.data, w.ctypes.data, x.size, out.ctypes.data)
+    return out
+
+
+def matrow(W: np.ndarray, scale: np.ndarray, x: np.ndarray, cols: int | None = None) -> np.ndarray:
+    """W is [rows][pitch] uint8; the first ``cols`` (default pitch) columns are used."""
+    W, scale, x = _c(W, np.uint8), _c(scale, np.uint32), _c(x, np.int64)
+    rows, pitch = W.shape
+    cols = pitch if cols is None else cols
+    assert x.size >= cols and scale.size >= rows
+    out = np.zeros(rows, dtype=np.int64)
+    _lib_().orc_matrow(W.ctypes.data, pitch, scale.ctypes.data, rows, cols, x.ctypes.data, out.ctypes.data)
+    return out
+
+
+def fits32(v: int) -> bool:
+    return bool(_lib_().orc_fits32(v))
+
+
+def rotate(a: int, b: int, c: int, s: int) -> tuple[int, int]:
+    a2, b2 = ctypes.c_int64(), ctypes.c_int64()
+    _lib_().orc_rotate(a, b, c, s, ctypes.byref(a2), ctypes.byref(b2))
+    return a2.value, b2.value
+
+
+def attention_head(q: np.ndarray, K: np.ndarray, V: np.ndarray, inv: int, exp_tab: np.ndarray):
+    """q i64[hd]; K, V i32[p][hd].  Returns (out i64[hd], probabilities i64[p])."""
+    q, K, V, e = _c(q, np.int64), _c(K, np.int32), _c(V, np.int32), _c(exp_tab, np.uint32)
+    p, hd = K.shape
+    scores = np.zeros(p, dtype=np.int64)
+    out = np.zeros(hd, dtype=np.int64)
+    _lib_().orc_attention_head(q.ctypes.data, K.ctypes.data, V.ctypes.data, hd, p, hd, inv,
+                               e.ctypes.data, scores.ctypes.data, out.ctypes.data)
+    return out, scores
+
+
+def silu(g: int, tab: np.ndarray) -> int:
+    tab = _c(tab, np.int32)
+    return int(_lib_().orc_silu(g, tab.ctypes.data))
+
+
+def silu_gate(g: np.ndarray, u: np.ndarray, tab: np.ndarray) -> np.ndarray:
+    g, u, tab = _c(g, np.int64), _c(u, np.int64), _c(tab, np.int32)
+    out = np.zeros(g.size, dtype=np.int64)
+    _lib_().orc_silu_gate(g.ctypes.data, u.ctypes.data, g.size, tab.ctypes.data, out.ctypes.data)
+    return out
+
+
+def argmax(logits: np.ndarray) -> int:
+    logits = _c(logits, np.int64)
+    return int(_lib_().orc_argmax(logits.ctypes.data, logits.size))
+
+
+def page_state_size(config, prompt_bytes: int, max_tokens: int) -> int:
+    cfg = np.array(config, dtype=np.uint32)
+    return int(_lib_().orc_page_state_size(cfg.ctypes.data, prompt_bytes, max_tokens))
+
+
+def events_reset(enable: bool = True) -> None:
+    _lib_().orc_events_reset(1 if enable else 0)
+
+
+def events() -> dict:
+    out = np.zeros(len(EVENT_NAMES), dtype=np.uint64)
+    _lib_().orc_events_get(out.ctypes.data)
+    return {n: int(v) for n, v in zip(EVENT_NAMES, out)}
+
+
+# ------------------------------------------------------------------ whole model
+
+class Model:
+    """A parsed artifact; the array must stay alive (the oracle aliases it)."""
+
+    def __init__(self, artifact: np.ndarray):
+        self.artifact = _c(artifact, np.uint8)
+        h = ctypes.c_void_p()
+        rc = _lib_().orc_model_open(self.artifact.ctypes.data, self.artifact.size, ctypes.byref(h))
+        if rc:
+            raise ValueError(f"oracle: artifact rejected with error {rc}")
+        self._h = h
+        self.config = tuple(int(v) for v in self.artifact[8:36].view("<u4"))
+
+    def close(self):
+        if self._h:
+            _lib_().orc_model_close(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def state_size(self, n_prompt: int, max_tokens: int) -> int:
+        return int(_lib_().orc_state_size(self._h, n_prompt, max_tokens))
+
+    def layout(self, n_prompt: int, max_tokens: int) -> dict:
+        out = np.zeros(13, dtype=np.uint64)
+        _lib_().orc_state_layout(self._h, n_prompt, max_tokens, out.ctypes.data)
+        return {n: int(v) for n, v in zip(LAYOUT_NAMES, out)}
+
+    def init_state(self, ids, max_tokens: int, temperature_q16: int = 0, seed: int = 0,
+                   flags: int = 0, length: int | None = None):
+        """Returns (rc, state bytes)."""
+        ids = _c(np.asarray(ids), np.uint32)
+        n = self.state_size(max(ids.size, 1), max(max_tokens, 1)) if length is None else length
+        st = np.zeros(max(n, 256), dtype=np.uint8)
+        rc = _lib_().orc_init_state(self._h, st.ctypes.data, n, ids.ctypes.data, ids.size,
+                                    max_tokens, temperature_q16, seed, flags)
+        return rc, st
+
+    def turn(self, state: np.ndarray, n_positions: int):
+        """Runs up to n_positions positions in place.  Returns (rc, result dict)."""
+        assert state.dtype == np.uint8 and state.flags.c_contiguous
+        res = TurnResult()
+        rc = _lib_().orc_turn(self._h, state.ctypes.data, state.size, n_positions, ctypes.byref(res))
+        return rc, res.as_dict()
+
+
+def header(state: np.ndarray) -> dict:
+    u32 = lambda o: int(state[o:o + 4].view("<u4")[0])
+    u64 = lambda o: int(state[o:o + 8].view("<u8")[0])
+    return {"phase": u32(H_PHASE), "position": u32(H_POSITION), "n_prompt": u32(H_NPROMPT),
+            "max_tokens": u32(H_MAXTOK), "cache": u32(H_CACHE), "generated": u32(H_GENERATED),
+            "flags": u32(H_FLAGS), "error": u32(H_ERROR), "last_token": u32(H_LASTTOK),
+            "turns": u64(H_TURNS), "err_key": u64(H_ERRKEY),
+            "max_logit": int(state[H_MAXLOGIT:H_MAXLOGIT + 8].view("<i8")[0])}

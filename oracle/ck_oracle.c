@@ -1,0 +1,584 @@
+/* ORACLE — test infrastructure, not part of the product.
+ *
+ * A plain, slow, obviously correct CPU restatement of curta-core's integer forward pass
+ * (phases 3 to 19 at temperature zero), written from the page "The inference core"
+ * (curta.chat docs).  Only the tests, the smoke check and the benchmark's CPU-baseline leg
+ * may load it.  It shares no code with the GPU library: it parses the model artifact and
+ * the state layout itself, from the format description.
+ *
+ * Every function cites the section of that page it follows.  Wrapping arithmetic is done
+ * on uint64_t (defined modulo 2^64 in C); ">>" on int64_t is the arithmetic shift (gcc and
+ * clang define it so), "/" on int64_t truncates toward zero.
+ *
+ * Readings where the page is silent (each one is listed with its reason in the design
+ * notes):
+ *   r1  (acc - 128*sum) * scale wraps in 64 bits (scale zero-extended), then >> 24.
+ *   r4  Squares for RMS normalization wrap in 64 bits and are summed as u64, the mean is
+ *       the unsigned quotient, the epsilon is added in u64.
+ *   r5  x * weight wraps in 64 bits before the truncating division.
+ *   r7  Rotary pairs are elements (2j, 2j+1) of each head, table entry [position][j].
+ *   r9  Scores: ((q . k) >> 16) * inv_sqrt wraps, then >> 24.
+ *   r10 Weighted values: the sum over positions first, then one >> 24.
+ *   r13 Ties in the maximum pass keep the lowest index.
+ *   r17 The first failing cache store, in program order, ends the turn with error 8.
+ *
+ * Range events: with counting on, every step that the wrap changes (exact integer result
+ * outside int64) is counted, so a workload can show that no reading above mattered.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ range events */
+
+enum {
+  EV_MATROW_ACC = 0,  /* sum (b-128) x outside int64 */
+  EV_MATROW_SCALE,    /* (acc - 128 sum) * scale outside int64 */
+  EV_NORM_SQUARES,    /* sum of squares outside uint64 */
+  EV_NORM_PRODUCT,    /* x * weight outside int64 */
+  EV_ROTARY,          /* a*c - b*s or a*s + b*c outside int64 */
+  EV_SCORE_DOT,       /* q . k outside int64 */
+  EV_SCORE_SCALE,     /* (dot >> 16) * inv outside int64 */
+  EV_SILU_PRODUCT,    /* silu(g) * u outside int64 */
+  EV_RESIDUAL,        /* x + y outside int64 */
+  EV_COUNT
+};
+static uint64_t g_events[EV_COUNT];
+static int g_count_events = 0;
+
+void orc_events_reset(int enable) {
+  memset(g_events, 0, sizeof(g_events));
+  g_count_events = enable;
+}
+void orc_events_get(uint64_t* out) { memcpy(out, g_events, sizeof(g_events)); }
+static void event(int k) {
+#pragma omp atomic
+  g_events[k]++;
+}
+static int outside_i64(__int128 v) { return v > (__int128)INT64_MAX || v < (__int128)INT64_MIN; }
+
+/* ------------------------------------------------------------------ scalar steps */
+
+/* Integer square root, floor(sqrt(v)), by the binary digit-by-digit method.
+ * ("RMS normalization": "integer square root".) */
+uint64_t orc_isqrt(uint64_t v) {
+  uint64_t r = 0, bit = 1ull << 62;
+  while (bit > v) bit >>= 2;
+  while (bit) {
+    if (v >= r + bit) {
+      v -= r + bit;
+      r = (r >> 1) + bit;
+    } else {
+      r >>= 1;
+    }
+    bit >>= 2;
+  }
+  return r;
+}
+
+/* Phase 3, "The forward pass, in order": ((byte - 128) * scale) >> 8 per element. */
+void orc_embed(const uint8_t* row, uint32_t scale, uint32_t n, int64_t* x) {
+  for (uint32_t i = 0; i < n; ++i) x[i] = ((int64_t)row[i] - 128) * (int64_t)scale >> 8;
+}
+
+/* "RMS normalization": rms = isqrt(sum(x*x)/n + 42,950), at least 1;
+ * y = ((x * w) / rms) >> 8 with the division rounding toward zero. */
+void orc_rmsnorm(const int64_t* x, const int32_t* w, uint32_t n, int64_t* y) {
+  uint64_t ss = 0;
+  unsigned __int128 exact = 0;
+  int over = 0;
+  for (uint32_t i = 0; i < n; ++i) {
+    ss += (uint64_t)x[i] * (uint64_t)x[i];
+    if (g_count_events && !over) {
+      unsigned __int128 sq = (unsigned __int128)((__int128)x[i] * x[i]);
+      exact += sq;
+      over = sq > UINT64_MAX || exact > UINT64_MAX;
+    }
+  }
+  if (over) event(EV_NORM_SQUARES);
+  uint64_t mean = ss / n;
+  uint64_t rms = orc_isqrt(mean + 42950u);
+  if (rms < 1) rms = 1;
+  for (uint32_t i = 0; i < n; ++i) {
+    int64_t p = (int64_t)((uint64_t)x[i] * (uint64_t)(int64_t)w[i]);
+    if (g_count_events && outside_i64((__int128)x[i] * w[i])) event(EV_NORM_PRODUCT);
+    int64_t q = p / (int64_t)rms;
+    y[i] = q >> 8;
+  }
+}
+
+/* "A matrix row": sum = x[0] + ... once per vector; acc = sum byte[c] * x[c];
+ * y = ((acc - 128 * sum) * scale) >> 24, products wrapping in 64 bits. */
+void orc_matrow(const uint8_t* W, uint64_t pitch, const uint32_t* scale, uint32_t rows,
+                uint32_t cols, const int64_t* x, int64_t* y) {
+  uint64_t sum = 0;
+  for (uint32_t c = 0; c < cols; ++c) sum += (uint64_t)x[c];
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < (int64_t)rows; ++r) {
+    const uint8_t* row = W + (uint64_t)r * pitch;
+    uint64_t acc = 0;
+    for (uint32_t c = 0; c < cols; ++c) acc += (uint64_t)row[c] * (uint64_t)x[c];
+    uint64_t t = acc - 128u * sum;
+    t *= (uint64_t)scale[r];
+    y[r] = (int64_t)t >> 24;
+    if (g_count_events) {
+      __int128 ex = 0;
+      for (uint32_t c = 0; c < cols; ++c) ex += (__int128)((int)row[c] - 128) * x[c];
+      if (outside_i64(ex)) event(EV_MATROW_ACC);
+      else if (outside_i64(ex * (__int128)scale[r])) event(EV_MATROW_SCALE);
+    }
+  }
+}
+
+/* "The attention cache": a store succeeds when the value fits 32 bits. */
+int orc_fits32(int64_t v) { return v >= INT32_MIN && v <= INT32_MAX; }
+
+/* Phase 8 (reading r7): rotate the pair (a, b) by (cos, sin) with 24 fractional bits. */
+void orc_rotate(int64_t a, int64_t b, int32_t c, int32_t s, int64_t* a2, int64_t* b2) {
+  uint64_t ac = (uint64_t)a * (uint64_t)(int64_t)c, bs = (uint64_t)b * (uint64_t)(int64_t)s;
+  uint64_t as = (uint64_t)a * (uint64_t)(int64_t)s, bc = (uint64_t)b * (uint64_t)(int64_t)c;
+  *a2 = (int64_t)(ac - bs) >> 24;
+  *b2 = (int64_t)(as + bc) >> 24;
+  if (g_count_events && (outside_i64((__int128)a * c - (__int128)b * s) ||
+                         outside_i64((__int128)a * s + (__int128)b * c)))
+    event(EV_ROTARY);
+}
+
+/* Phase 9, "Attention, stage by stage", for one head over p positions.
+ * K and V point at the head's first element of position 0; stride is the distance in
+ * words between positions.  scores receives the exponentials at the end (p entries). */
+void orc_attention_head(const int64_t* q, const int32_t* K, const int32_t* V, uint64_t stride,
+                        uint32_t p, uint32_t hd, uint32_t inv, const uint32_t* exp_tab,
+                        int64_t* scores, int64_t* out) {
+  /* stage 0: scores and the largest score */
+  int64_t m = INT64_MIN;
+  for (uint32_t t = 0; t < p; ++t) {
+    uint64_t dot = 0;
+    __int128 ex = 0;
+    for (uint32_t i = 0; i < hd; ++i) {
+      int64_t k = K[(uint64_t)t * stride + i];
+      dot += (uint64_t)q[i] * (uint64_t)k;
+      if (g_count_events) ex += (__int128)q[i] * k;
+    }
+    int64_t s = (int64_t)dot >> 16;
+    if (g_count_events) {
+      if (outside_i64(ex)) event(EV_SCORE_DOT);
+      else if (outside_i64((__int128)s * inv)) event(EV_SCORE_SCALE);
+    }
+    s = (int64_t)((uint64_t)s * (uint64_t)inv) >> 24;
+    scores[t] = s;
+    if (s > m) m = s;
+  }
+  /* stage 1: exponentials of (largest - score); the exact difference is >= 0 and fits u64 */
+  uint64_t sum = 0;
+  for (uint32_t t = 0; t < p; ++t) {
+    uint64_t d = (uint64_t)m - (uint64_t)scores[t];
+    uint64_t idx = d >> 8;
+    if (idx > 4096) idx = 4096;
+    scores[t] = (int64_t)exp_tab[idx];
+    sum += exp_tab[idx];
+  }
+  /* stage 2: probabilities with 24 fractional bits */
+  for (uint32_t t = 0; t < p; ++t) scores[t] = (int64_t)(((uint64_t)scores[t] << 24) / sum);
+  /* stage 3: weighted values, the sum first, then one shift */
+  for (uint32_t j = 0; j < hd; ++j) {
+    uint64_t acc = 0;
+    for (uint32_t t = 0; t < p; ++t)
+      acc += (uint64_t)scores[t] * (uint64_t)(int64_t)V[(uint64_t)t * stride + j];
+    out[j] = (int64_t)acc >> 24;
+  }
+}
+
+/* "Lookup tables", SiLU: 16 or more returns itself, -16 or less returns zero, otherwise
+ * the entry (x + 16) >> 9 in fixed point. */
+int64_t orc_silu(int64_t g, const int32_t* tab) {
+  const int64_t sixteen = (int64_t)16 << 16;
+  if (g >= sixteen) return g;
+  if (g <= -sixteen) return 0;
+  return tab[(g + sixteen) >> 9];
+}
+
+/* Phase 14: each gate element through the table, times the up element, >> 16. */
+void orc_silu_gate(const int64_t* g, const int64_t* u, uint32_t n, const int32_t* tab, int64_t* h) {
+  for (uint32_t i = 0; i < n; ++i) {
+    int64_t s = orc_silu(g[i], tab);
+    if (g_count_events && outside_i64((__int128)s * u[i])) event(EV_SILU_PRODUCT);
+    h[i] = (int64_t)((uint64_t)s * (uint64_t)u[i]) >> 16;
+  }
+}
+
+/* Phase 19 at temperature zero ("Sampling", maximum pass): the first largest logit. */
+uint32_t orc_argmax(const int64_t* logits, uint32_t n) {
+  uint32_t best = 0;
+  for (uint32_t i = 1; i < n; ++i)
+    if (logits[i] > logits[best]) best = i;
+  return best;
+}
+
+static void residual(int64_t* x, const int64_t* y, uint32_t n) {
+  for (uint32_t i = 0; i < n; ++i) {
+    if (g_count_events && outside_i64((__int128)x[i] + y[i])) event(EV_RESIDUAL);
+    x[i] = (int64_t)((uint64_t)x[i] + (uint64_t)y[i]);
+  }
+}
+
+/* ------------------------------------------------------------------ the state size the
+ * page gives ("The resumable state"): text-mode buffers, each at a multiple of 8 bytes. */
+static uint64_t up8(uint64_t n) { return (n + 7) & ~7ull; }
+
+uint64_t orc_page_state_size(const uint32_t* cfg, uint32_t prompt_bytes, uint32_t max_tokens) {
+  uint64_t dim = cfg[0], hidden = cfg[1], layers = cfg[2], heads = cfg[3], kvh = cfg[4];
+  uint64_t vocab = cfg[5], context = cfg[6];
+  uint64_t kv_dim = dim / heads * kvh;
+  uint64_t cache = (uint64_t)prompt_bytes + max_tokens + 1;
+  if (cache > context) cache = context;
+  uint64_t n = 128;
+  n = up8(n + prompt_bytes);
+  n = up8(n + 4ull * (prompt_bytes + 2));
+  n = up8(n + 4ull * max_tokens);
+  n = up8(n + 128ull * max_tokens);
+  n = up8(n + 4 * 8 * dim);
+  n = up8(n + 2 * 8 * hidden);
+  n = up8(n + 8 * vocab);
+  n = up8(n + 8 * cache);
+  n = up8(n + 4 * layers * cache * kv_dim);
+  n = up8(n + 4 * layers * cache * kv_dim);
+  return n;
+}
+
+/* ------------------------------------------------------------------ model artifact */
+
+typedef struct {
+  const int32_t *attn_norm, *ffn_norm;
+  const uint8_t *wq, *wk, *wv, *wo, *w1, *w3, *w2;
+  const uint32_t *sq, *sk, *sv, *so, *s1, *s3, *s2;
+} orc_layer;
+
+typedef struct {
+  uint32_t dim, hidden, layers, heads, kv_heads, vocab, context;
+  uint32_t head_dim, kv_dim, inv_sqrt, flags;
+  const uint8_t* embed;
+  const uint32_t* embed_scale;
+  const int32_t* final_norm;
+  const uint8_t* cls;
+  const uint32_t* cls_scale;
+  const int32_t* rope;
+  const uint32_t* exp_tab;
+  const int32_t* silu_tab;
+  orc_layer* layer;
+} orc_model;
+
+static uint32_t rd32(const uint8_t* p) { uint32_t v; memcpy(&v, p, 4); return v; }
+static uint64_t rd64(const uint8_t* p) { uint64_t v; memcpy(&v, p, 8); return v; }
+
+/* Parses an artifact (format "CKMODEL1", see the library header).  Returns 0, 1 for an
+ * invalid configuration or 2 for an invalid format; pointers alias the artifact. */
+int orc_model_open(const uint8_t* art, uint64_t len, orc_model** out) {
+  *out = NULL;
+  if (len < 64 || memcmp(art, "CKMODEL1", 8) != 0) return 2;
+  orc_model m;
+  memset(&m, 0, sizeof(m));
+  m.dim = rd32(art + 8); m.hidden = rd32(art + 12); m.layers = rd32(art + 16);
+  m.heads = rd32(art + 20); m.kv_heads = rd32(art + 24); m.vocab = rd32(art + 28);
+  m.context = rd32(art + 32); m.inv_sqrt = rd32(art + 36); m.flags = rd32(art + 40);
+  uint32_t n_tensors = rd32(art + 44);
+  if (!m.dim || !m.hidden || !m.layers || !m.heads || !m.kv_heads || !m.vocab || !m.context) return 1;
+  if (m.dim % m.heads || m.heads % m.kv_heads || (m.dim / m.heads) % 2) return 1;
+  m.head_dim = m.dim / m.heads;
+  m.kv_dim = m.head_dim * m.kv_heads;
+  if (n_tensors != 8 + 16 * m.layers || rd64(art + 48) != len) return 2;
+  if (64 + 16ull * n_tensors > len) return 2;
+  const uint64_t d = m.dim, h = m.hidden, v = m.vocab, kv = m.kv_dim;
+  int tied = m.flags & 1;
+  uint64_t want[8] = {v * d, 4 * v, 4 * d, tied ? 0 : v * d, tied ? 0 : 4 * v,
+                      4ull * m.context * m.head_dim, 4 * 4097, 4 * 4097};
+  uint64_t want_layer[16] = {4 * d, d * d, 4 * d, kv * d, 4 * kv, kv * d, 4 * kv, d * d,
+                             4 * d, 4 * d, h * d, 4 * h, h * d, 4 * h, d * h, 4 * d};
+  if (m.layers > 4096) return 1;
+  const uint8_t** ptr = (const uint8_t**)calloc(n_tensors, sizeof(*ptr));
+  for (uint32_t i = 0; i < n_tensors; ++i) {
+    uint64_t off = rd64(art + 64 + 16 * i), tl = rd64(art + 64 + 16 * i + 8);
+    uint64_t expect = i < 8 ? want[i] : want_layer[(i - 8) % 16];
+    if (tl != expect || (tl && (off > len || tl > len - off || off % 4))) {
+      free(ptr);
+      return 2;
+    }
+    ptr[i] = art + off;
+  }
+  m.embed = ptr[0];
+  m.embed_scale = (const uint32_t*)ptr[1];
+  m.final_norm = (const int32_t*)ptr[2];
+  m.cls = tied ? m.embed : ptr[3];
+  m.cls_scale = tied ? m.embed_scale : (const uint32_t*)ptr[4];
+  m.rope = (const int32_t*)ptr[5];
+  m.exp_tab = (const uint32_t*)ptr[6];
+  m.silu_tab = (const int32_t*)ptr[7];
+  m.layer = (orc_layer*)calloc(m.layers, sizeof(orc_layer));
+  for (uint32_t l = 0; l < m.layers; ++l) {
+    const uint8_t** p = ptr + 8 + 16 * l;
+    orc_layer* L = &m.layer[l];
+    L->attn_norm = (const int32_t*)p[0];
+    L->wq = p[1]; L->sq = (const uint32_t*)p[2];
+    L->wk = p[3]; L->sk = (const uint32_t*)p[4];
+    L->wv = p[5]; L->sv = (const uint32_t*)p[6];
+    L->wo = p[7]; L->so = (const uint32_t*)p[8];
+    L->ffn_norm = (const int32_t*)p[9];
+    L->w1 = p[10]; L->s1 = (const uint32_t*)p[11];
+    L->w3 = p[12]; L->s3 = (const uint32_t*)p[13];
+    L->w2 = p[14]; L->s2 = (const uint32_t*)p[15];
+  }
+  free(ptr);
+  *out = (orc_model*)malloc(sizeof(orc_model));
+  **out = m;
+  return 0;
+}
+
+void orc_model_close(orc_model* m) {
+  if (m) {
+    free(m->layer);
+    free(m);
+  }
+}
+
+/* ------------------------------------------------------------------ state ("CKSTATE1")
+ * The ids-mode state of the library header: a 256-byte header, then the buffers, each at
+ * a multiple of 256 bytes: prompt ids u32[n_prompt], output tokens u32[max_tokens],
+ * x, xb, q, o, y i64[dim], h i64[hidden], logits i64[vocab],
+ * scores i64[heads*cache], K i32[layers*cache*kv_dim], V i32[layers*cache*kv_dim]. */
+
+enum { H_PHASE = 8, H_POSITION = 12, H_NPROMPT = 16, H_MAXTOK = 20, H_CACHE = 24, H_GENERATED = 28,
+       H_FLAGS = 32, H_TEMP = 36, H_ERROR = 40, H_LASTTOK = 44, H_SEED = 48, H_TURNS = 56,
+       H_ERRKEY = 64, H_MAXLOGIT = 72, H_CONFIG = 80 };
+enum { PHASE_RUNNING = 3, PHASE_DONE = 20, PHASE_FAILED = 21 };
+
+typedef struct {
+  uint64_t prompt, out, x, xb, q, o, y, h, logits, scores, k, v, size;
+} orc_layout;
+
+static uint64_t up256(uint64_t n) { return (n + 255) & ~255ull; }
+
+static orc_layout layout_of(const uint32_t* cfg, uint32_t n_prompt, uint32_t max_tokens) {
+  uint64_t dim = cfg[0], hidden = cfg[1], layers = cfg[2], heads = cfg[3], kvh = cfg[4];
+  uint64_t vocab = cfg[5];
+  uint64_t kv_dim = dim / heads * kvh;
+  uint64_t cache = (uint64_t)n_prompt + max_tokens - 1;
+  orc_layout L;
+  uint64_t n = 256;
+  L.prompt = n; n = up256(n + 4ull * n_prompt);
+  L.out = n; n = up256(n + 4ull * max_tokens);
+  L.x = n; n = up256(n + 8 * dim);
+  L.xb = n; n = up256(n + 8 * dim);
+  L.q = n; n = up256(n + 8 * dim);
+  L.o = n; n = up256(n + 8 * dim);
+  L.y = n; n = up256(n + 8 * dim);
+  L.h = n; n = up256(n + 8 * hidden);
+  L.logits = n; n = up256(n + 8 * vocab);
+  L.scores = n; n = up256(n + 8 * heads * cache);
+  L.k = n; n = up256(n + 4 * layers * cache * kv_dim);
+  L.v = n; n = up256(n + 4 * layers * cache * kv_dim);
+  L.size = n;
+  return L;
+}
+
+static void model_cfg(const orc_model* m, uint32_t* cfg) {
+  cfg[0] = m->dim; cfg[1] = m->hidden; cfg[2] = m->layers; cfg[3] = m->heads;
+  cfg[4] = m->kv_heads; cfg[5] = m->vocab; cfg[6] = m->context;
+}
+
+uint64_t orc_state_size(const orc_model* m, uint32_t n_prompt, uint32_t max_tokens) {
+  uint32_t cfg[7];
+  model_cfg(m, cfg);
+  if (n_prompt == 0 || max_tokens == 0) return 0;
+  return layout_of(cfg, n_prompt, max_tokens).size;
+}
+
+static void wr32(uint8_t* p, uint32_t v) { memcpy(p, &v, 4); }
+static void wr64(uint8_t* p, uint64_t v) { memcpy(p, &v, 8); }
+
+/* "The Rust API", init_state, in ids mode: writes a fresh header and the prompt ids.
+ * Errors: 4 wrong length, 3 misaligned, 6 invalid prompt / max tokens / temperature,
+ * 7 prompt plus max tokens less one above the context. */
+int orc_init_state(const orc_model* m, uint8_t* st, uint64_t len, const uint32_t* ids,
+                   uint32_t n_ids, uint32_t max_tokens, uint32_t temperature_q16, uint64_t seed,
+                   uint32_t flags) {
+  if ((uintptr_t)st % 8) return 3;
+  if (n_ids == 0 || max_tokens == 0 || max_tokens > m->context) return 6;
+  if (temperature_q16 != 0) return 6; /* only the maximum pass (temperature zero) is built */
+  for (uint32_t i = 0; i < n_ids; ++i)
+    if (ids[i] >= m->vocab) return 6;
+  if ((uint64_t)n_ids + max_tokens - 1 > m->context) return 7;
+  uint32_t cfg[7];
+  model_cfg(m, cfg);
+  orc_layout L = layout_of(cfg, n_ids, max_tokens);
+  if (len != L.size) return 4;
+  memset(st, 0, len);
+  memcpy(st, "CKSTATE1", 8);
+  wr32(st + H_PHASE, PHASE_RUNNING);
+  wr32(st + H_NPROMPT, n_ids);
+  wr32(st + H_MAXTOK, max_tokens);
+  wr32(st + H_CACHE, n_ids + max_tokens - 1);
+  wr32(st + H_FLAGS, flags);
+  wr32(st + H_TEMP, temperature_q16);
+  wr32(st + H_LASTTOK, 0xFFFFFFFFu);
+  wr64(st + H_SEED, seed);
+  wr64(st + H_ERRKEY, ~0ull);
+  for (int i = 0; i < 7; ++i) wr32(st + H_CONFIG + 4 * i, cfg[i]);
+  memcpy(st + L.prompt, ids, 4ull * n_ids);
+  return 0;
+}
+
+typedef struct {
+  uint32_t complete, generated, generated_this_turn, token, work;
+  uint32_t err_position, err_layer, err_phase, err_element;
+} orc_turn_result;
+
+static uint64_t err_key(uint32_t pos, uint32_t layer, uint32_t phase, uint32_t elem) {
+  return ((uint64_t)pos << 44) | ((uint64_t)layer << 32) | ((uint64_t)phase << 24) | elem;
+}
+
+/* One position, phases 3 to 16 for every layer, then 17 to 19 where a token is generated
+ * ("The forward pass, in order").  Returns 0, or 8 at the first store that does not fit. */
+static int run_position(const orc_model* m, uint8_t* st, const orc_layout* L) {
+  const uint32_t pos = rd32(st + H_POSITION), n_prompt = rd32(st + H_NPROMPT);
+  const uint32_t cache = rd32(st + H_CACHE);
+  const uint32_t* prompt = (const uint32_t*)(st + L->prompt);
+  uint32_t* out = (uint32_t*)(st + L->out);
+  int64_t *x = (int64_t*)(st + L->x), *xb = (int64_t*)(st + L->xb), *q = (int64_t*)(st + L->q);
+  int64_t *o = (int64_t*)(st + L->o), *y = (int64_t*)(st + L->y), *hh = (int64_t*)(st + L->h);
+  int64_t *logits = (int64_t*)(st + L->logits), *scores = (int64_t*)(st + L->scores);
+  int32_t *Kc = (int32_t*)(st + L->k), *Vc = (int32_t*)(st + L->v);
+  const uint32_t d = m->dim, hd = m->head_dim, kvd = m->kv_dim, hid = m->hidden;
+  int64_t* g = (int64_t*)malloc(8ull * hid * 2);
+  int64_t* u = g + hid;
+  int64_t* kv = (int64_t*)malloc(8ull * kvd);
+  int rc = 0;
+
+  /* phase 3: the token of this position is a prompt id or the last generated token */
+  uint32_t tok = pos < n_prompt ? prompt[pos] : out[pos - n_prompt];
+  orc_embed(m->embed + (uint64_t)tok * d, m->embed_scale[tok], d, x);
+
+  for (uint32_t l = 0; l < m->layers && !rc; ++l) {
+    const orc_layer* W = &m->layer[l];
+    int32_t* Kl = Kc + ((uint64_t)l * cache + pos) * kvd;
+    int32_t* Vl = Vc + ((uint64_t)l * cache + pos) * kvd;
+    orc_rmsnorm(x, W->attn_norm, d, xb);                               /* phase 4 */
+    orc_matrow(W->wq, d, W->sq, d, d, xb, q);                          /* phase 5 */
+    orc_matrow(W->wk, d, W->sk, kvd, d, xb, kv);                       /* phase 6 */
+    for (uint32_t j = 0; j < kvd && !rc; ++j) {
+      if (!orc_fits32(kv[j])) { rc = 8; wr64(st + H_ERRKEY, err_key(pos, l, 6, j)); }
+      else Kl[j] = (int32_t)kv[j];
+    }
+    if (rc) break;
+    orc_matrow(W->wv, d, W->sv, kvd, d, xb, kv);                       /* phase 7 */
+    for (uint32_t j = 0; j < kvd && !rc; ++j) {
+      if (!orc_fits32(kv[j])) { rc = 8; wr64(st + H_ERRKEY, err_key(pos, l, 7, j)); }
+      else Vl[j] = (int32_t)kv[j];
+    }
+    if (rc) break;
+    const int32_t* rope = m->rope + (uint64_t)pos * hd;                /* phase 8 */
+    for (uint32_t i = 0; i < d; i += 2) {
+      uint32_t j = (i % hd) / 2;
+      orc_rotate(q[i], q[i + 1], rope[2 * j], rope[2 * j + 1], &q[i], &q[i + 1]);
+    }
+    for (uint32_t i = 0; i < kvd && !rc; i += 2) {
+      uint32_t j = (i % hd) / 2;
+      int64_t a2, b2;
+      orc_rotate(Kl[i], Kl[i + 1], rope[2 * j], rope[2 * j + 1], &a2, &b2);
+      if (!orc_fits32(a2)) { rc = 8; wr64(st + H_ERRKEY, err_key(pos, l, 8, i)); break; }
+      Kl[i] = (int32_t)a2;
+      if (!orc_fits32(b2)) { rc = 8; wr64(st + H_ERRKEY, err_key(pos, l, 8, i + 1)); break; }
+      Kl[i + 1] = (int32_t)b2;
+    }
+    if (rc) break;
+    const uint32_t group = m->heads / m->kv_heads;                     /* phase 9 */
+    for (uint32_t hh_ = 0; hh_ < m->heads; ++hh_) {
+      uint32_t kvh = hh_ / group;
+      const int32_t* K0 = Kc + (uint64_t)l * cache * kvd + (uint64_t)kvh * hd;
+      const int32_t* V0 = Vc + (uint64_t)l * cache * kvd + (uint64_t)kvh * hd;
+      orc_attention_head(q + (uint64_t)hh_ * hd, K0, V0, kvd, pos + 1, hd, m->inv_sqrt, m->exp_tab,
+                         scores + (uint64_t)hh_ * cache, o + (uint64_t)hh_ * hd);
+    }
+    orc_matrow(W->wo, d, W->so, d, d, o, y);                           /* phase 10 */
+    residual(x, y, d);                                                 /* phase 11 */
+    orc_rmsnorm(x, W->ffn_norm, d, xb);
+    orc_matrow(W->w1, d, W->s1, hid, d, xb, g);                        /* phase 12 */
+    orc_matrow(W->w3, d, W->s3, hid, d, xb, u);                        /* phase 13 */
+    orc_silu_gate(g, u, hid, m->silu_tab, hh);                         /* phase 14 */
+    orc_matrow(W->w2, hid, W->s2, d, hid, hh, y);                      /* phase 15 */
+    residual(x, y, d);                                                 /* phase 16 */
+  }
+  free(g);
+  free(kv);
+  if (rc) return rc;
+
+  if (pos + 1 >= n_prompt) {                                           /* a generating position */
+    orc_rmsnorm(x, m->final_norm, d, xb);                              /* phase 17 */
+    orc_matrow(m->cls, d, m->cls_scale, m->vocab, d, xb, logits);      /* phase 18 */
+    uint32_t t = orc_argmax(logits, m->vocab);                         /* phase 19 */
+    uint32_t gen = rd32(st + H_GENERATED);
+    out[gen] = t;
+    wr32(st + H_GENERATED, gen + 1);
+    wr32(st + H_LASTTOK, t);
+    wr64(st + H_MAXLOGIT, (uint64_t)logits[t]);
+    if (gen + 1 == rd32(st + H_MAXTOK) || ((rd32(st + H_FLAGS) & 1) && (t == 1 || t == 2)))
+      wr32(st + H_PHASE, PHASE_DONE);
+  }
+  wr32(st + H_POSITION, pos + 1);
+  return 0;
+}
+
+/* "The Rust API", turn: runs up to n_positions positions of the run.  Errors: 3 for a
+ * state that does not fit the model or is complete, 8 for a cache store that does not
+ * fit (the state is then marked failed). */
+int orc_turn(const orc_model* m, uint8_t* st, uint64_t len, uint32_t n_positions,
+             orc_turn_result* res) {
+  memset(res, 0, sizeof(*res));
+  res->token = 0xFFFFFFFFu;
+  if ((uintptr_t)st % 8 || len < 256 || memcmp(st, "CKSTATE1", 8) != 0) return 3;
+  uint32_t cfg[7];
+  model_cfg(m, cfg);
+  for (int i = 0; i < 7; ++i)
+    if (rd32(st + H_CONFIG + 4 * i) != cfg[i]) return 3;
+  const uint32_t n_prompt = rd32(st + H_NPROMPT), max_tokens = rd32(st + H_MAXTOK);
+  if (!n_prompt || !max_tokens || (uint64_t)n_prompt + max_tokens - 1 > m->context) return 3;
+  orc_layout L = layout_of(cfg, n_prompt, max_tokens);
+  if (len != L.size || rd32(st + H_CACHE) != n_prompt + max_tokens - 1) return 3;
+  if (rd32(st + H_PHASE) != PHASE_RUNNING) return 3;
+  if (rd32(st + H_POSITION) >= n_prompt + max_tokens - 1 || rd32(st + H_GENERATED) >= max_tokens)
+    return 3;
+  int rc = 0;
+  uint32_t gen0 = rd32(st + H_GENERATED);
+  for (uint32_t i = 0; i < n_positions; ++i) {
+    if (rd32(st + H_PHASE) != PHASE_RUNNING) break;
+    uint32_t before = rd32(st + H_GENERATED);
+    rc = run_position(m, st, &L);
+    res->work++;
+    if (rc) {
+      wr32(st + H_PHASE, PHASE_FAILED);
+      wr32(st + H_ERROR, (uint32_t)rc);
+      break;
+    }
+    if (rd32(st + H_GENERATED) != before) res->token = rd32(st + H_LASTTOK);
+  }
+  wr64(st + H_TURNS, rd64(st + H_TURNS) + 1);
+  res->generated = rd32(st + H_GENERATED);
+  res->generated_this_turn = res->generated - gen0;
+  res->complete = rd32(st + H_PHASE) != PHASE_RUNNING;
+  uint64_t key = rd64(st + H_ERRKEY);
+  if (key != ~0ull) {
+    res->err_position = (uint32_t)(key >> 44);
+    res->err_layer = (uint32_t)(key >> 32) & 0xFFF;
+    res->err_phase = (uint32_t)(key >> 24) & 0xFF;
+    res->err_element = (uint32_t)key & 0xFFFFFF;
+  }
+  return rc;
+}
+
+/* Buffer offsets of the state, for the bindings: prompt, out, x, xb, q, o, y, h, logits,
+ * scores, k, v, size (13 values). */
+void orc_state_layout(const orc_model* m, uint32_t n_prompt, uint32_t max_tokens, uint64_t* out13) {
+  uint32_t cfg[7];
+  model_cfg(m, cfg);
+  orc_layout L = layout_of(cfg, n_prompt, max_tokens);
+  memcpy(out13, &L, sizeof(L));
+}

@@ -1,0 +1,173 @@
+"""Whole-model checks of the CPU oracle: invariants and special cases that hold whatever
+the weights are ("The inference core": "The forward pass, in order", "Attention, stage by
+stage", "The resumable state", "Core errors")."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+
+def _model(spec):
+    return oracle.Model(synth.build_artifact(spec))
+
+
+def _buf(m, st, wl, name, dtype, count):
+    lay = m.layout(wl.n_prompt, wl.steps)
+    o = lay[name]
+    return st[o:o + np.dtype(dtype).itemsize * count].view(dtype)
+
+
+@pytest.fixture(scope="module")
+def tiny_ws():
+    wl = synth.WORKLOADS["tiny_ws"]
+    return wl, _model(wl.spec)
+
+
+def test_literal_tiny_config_overflows_the_cache():
+    # the tiny workload as written (row scales ~2^24/8) grows the residual past 2^32 in the
+    # first layer, so layer 2's key store fails on the second position with error 8
+    wl = synth.WORKLOADS["tiny"]
+    m = _model(wl.spec)
+    rc, st = m.init_state(synth.prompt_ids(wl.spec, wl.n_prompt), wl.steps)
+    assert rc == 0
+    oracle.events_reset(True)
+    rc, res = m.turn(st, 100)
+    ev = oracle.events()
+    oracle.events_reset(False)
+    assert rc == 8 and res["complete"] == 1 and res["work"] == 2
+    assert (res["err_position"], res["err_layer"], res["err_phase"]) == (1, 1, 6)
+    assert ev["norm_squares"] > 0          # the 64-bit range really was left
+    h = oracle.header(st)
+    assert h["phase"] == oracle.PHASE_FAILED and h["error"] == 8
+    # a failed state cannot take another turn
+    assert m.turn(st, 1)[0] == 3
+
+
+def test_well_scaled_models_stay_in_range(tiny_ws):
+    wl, m = tiny_ws
+    rc, st = m.init_state(synth.prompt_ids(wl.spec, wl.n_prompt), wl.steps)
+    oracle.events_reset(True)
+    rc, res = m.turn(st, 1000)
+    ev = oracle.events()
+    oracle.events_reset(False)
+    assert rc == 0 and res["complete"] and res["generated"] == wl.steps
+    assert res["work"] == wl.n_prompt + wl.steps - 1
+    assert all(v == 0 for v in ev.values()), ev
+
+
+@pytest.mark.parametrize("name", ["tiny_ws", "gqa"])
+def test_position_zero_attention_returns_the_value_row(name):
+    # with one position the probability is exactly 2^24, so each head's output equals its
+    # key/value head's cached value row; the value head of head h is h / (heads / kv_heads)
+    wl = synth.WORKLOADS[name]
+    spec = wl.spec
+    m = _model(spec)
+    rc, st = m.init_state(synth.prompt_ids(spec, wl.n_prompt), wl.steps)
+    rc, res = m.turn(st, 1)
+    assert rc == 0 and res["work"] == 1
+    cache = wl.n_prompt + wl.steps - 1
+    o = _buf(m, st, wl, "o", "<i8", spec.dim)
+    V = _buf(m, st, wl, "v", "<i4", spec.layers * cache * spec.kv_dim).reshape(spec.layers, cache, spec.kv_dim)
+    hd, group = spec.head_dim, spec.heads // spec.kv_heads
+    for h in range(spec.heads):
+        kvh = h // group
+        assert o[h * hd:(h + 1) * hd].tolist() == V[-1, 0, kvh * hd:(kvh + 1) * hd].astype(np.int64).tolist()
+
+
+def test_turn_split_invariance(tiny_ws):
+    wl, m = tiny_ws
+    ids = synth.prompt_ids(wl.spec, wl.n_prompt)
+    _, a = m.init_state(ids, wl.steps)
+    m.turn(a, 1000)
+    _, b = m.init_state(ids, wl.steps)
+    for n in (1, 2, 3, 5, 1000):
+        if oracle.header(b)["phase"] != oracle.PHASE_RUNNING:
+            break
+        m.turn(b, n)
+    ha, hb = oracle.header(a), oracle.header(b)
+    assert hb["turns"] > ha["turns"]
+    a[56:64] = 0
+    b[56:64] = 0                            # only the turn counter may differ
+    assert np.array_equal(a, b)
+
+
+def test_stop_tokens_end_the_run(tiny_ws):
+    wl, m = tiny_ws
+    ids = synth.prompt_ids(wl.spec, wl.n_prompt)
+    _, full = m.init_state(ids, wl.steps)
+    m.turn(full, 1000)
+    toks = _buf(m, full, wl, "out", "<u4", wl.steps).tolist()
+    first = next(i for i, t in enumerate(toks) if t in (1, 2))   # this seed emits one
+    _, st = m.init_state(ids, wl.steps, flags=oracle.FLAG_STOP_TOKENS)
+    rc, res = m.turn(st, 1000)
+    assert rc == 0 and res["complete"] and res["generated"] == first + 1
+    assert res["token"] == toks[first]
+    assert oracle.header(st)["phase"] == oracle.PHASE_DONE
+    assert _buf(m, st, wl, "out", "<u4", wl.steps).tolist()[:first + 1] == toks[:first + 1]
+
+
+def test_init_state_errors(tiny_ws):
+    wl, m = tiny_ws
+    ids = synth.prompt_ids(wl.spec, 4)
+    ctx = wl.spec.context
+    assert m.init_state(ids, 0)[0] == 6                       # max tokens zero
+    assert m.init_state(ids, ctx + 1)[0] == 6                 # above the context
+    assert m.init_state(np.array([wl.spec.vocab], np.uint32), 2)[0] == 6   # id out of range
+    assert m.init_state(np.array([], np.uint32), 2)[0] == 6   # no prompt id
+    assert m.init_state(ids, 2, temperature_q16=16 * 2**16 + 1)[0] == 6
+    assert m.init_state(ids, ctx - 2)[0] == 7                 # 4 + (ctx-2) - 1 > ctx
+    assert m.init_state(ids, ctx - 3)[0] == 0                 # exactly the context
+    n = m.state_size(4, 5)
+    assert m.init_state(ids, 5, length=n + 8)[0] == 4
+    assert m.init_state(ids, 5, length=n - 8)[0] == 4
+
+
+def test_turn_rejects_foreign_states(tiny_ws):
+    wl, m = tiny_ws
+    ids = synth.prompt_ids(wl.spec, 4)
+    _, st = m.init_state(ids, 5)
+    bad = st.copy()
+    bad[0] ^= 1
+    assert m.turn(bad, 1)[0] == 3                             # tag
+    bad = st.copy()
+    bad[80] ^= 1
+    assert m.turn(bad, 1)[0] == 3                             # configuration echo
+    bad = st.copy()
+    bad[oracle.H_POSITION] = 8                                # cursor past the cache
+    assert m.turn(bad, 1)[0] == 3
+
+
+def test_artifact_errors():
+    art = synth.build_artifact(synth.TINY_WS)
+    bad = art.copy()
+    bad[0] = ord("X")
+    with pytest.raises(ValueError, match="error 2"):
+        oracle.Model(bad)
+    with pytest.raises(ValueError, match="error 2"):
+        oracle.Model(art[:-64].copy())                        # truncated
+    bad = art.copy()
+    bad[8:12] = 0                                             # dim zero
+    with pytest.raises(ValueError, match="error 1"):
+        oracle.Model(bad)
+
+
+def test_tied_classifier_reads_the_embedding():
+    # untying with a classifier that is a copy of the embedding gives the same run
+    spec = synth.GQA_TIED
+    wl = synth.WORKLOADS["gqa_tied"]
+    tied = synth.build_artifact(spec)
+    untied_spec = dataclasses.replace(spec, tied=False)
+    untied = synth.build_artifact(untied_spec)
+    synth.artifact_tensor(untied, synth.T_CLS)[...] = synth.artifact_tensor(tied, synth.T_EMBED)
+    synth.artifact_tensor(untied, synth.T_CLS_SCALE)[...] = synth.artifact_tensor(tied, synth.T_EMBED_SCALE)
+    outs = []
+    for art in (tied, untied):
+        m = oracle.Model(art)
+        rc, st = m.init_state(synth.prompt_ids(spec, wl.n_prompt), wl.steps)
+        rc, res = m.turn(st, 1000)
+        assert rc == 0
+        outs.append(_buf(m, st, wl, "out", "<u4", wl.steps).tolist())
+    assert outs[0] == outs[1]
