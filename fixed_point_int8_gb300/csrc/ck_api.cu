@@ -1,0 +1,805 @@
+// libck host API: artifact loading into HBM, state set-up and the phase sequencer that
+// replays one position's kernels as a CUDA graph ("The inference core": "The forward pass,
+// in order", "The resumable state", "The Rust API", "Core errors").
+#include <climits>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "ck_internal.cuh"
+
+using namespace ck;
+
+struct ck_model {
+  ck_config cfg;
+  uint32_t head_dim, kv_dim, inv_sqrt, flags, pitch_d, pitch_h;
+  int device, num_sms;
+  uint8_t* dev;
+  size_t dev_len;
+  const uint8_t* embed;
+  const uint32_t* embed_scale;
+  const uint8_t* cls;
+  const uint32_t* cls_scale;
+  const int32_t* final_norm;
+  const int32_t* rope;
+  const uint32_t* exp_tab;
+  const int32_t* silu_tab;
+  uint32_t* scratch;  // small device scratch inside dev (ck_argmax result)
+  std::vector<DevLayer> layers;
+  cudaStream_t capture;
+  struct Graph {
+    void* state;
+    size_t len;
+    bool generating;
+    cudaGraphExec_t exec;
+  };
+  std::vector<Graph> graphs;
+};
+
+namespace {
+
+constexpr uint32_t kTable = 4097;
+
+uint32_t rd32(const uint8_t* p) { uint32_t v; memcpy(&v, p, 4); return v; }
+uint64_t rd64(const uint8_t* p) { uint64_t v; memcpy(&v, p, 8); return v; }
+uint32_t pad16(uint32_t n) { return (n + 15u) & ~15u; }
+
+int check_config(const ck_config& c) {
+  if (!c.dim || !c.hidden || !c.layers || !c.heads || !c.kv_heads || !c.vocab || !c.context)
+    return CK_INVALID_CONFIG;
+  if (c.dim % c.heads || c.heads % c.kv_heads) return CK_INVALID_CONFIG;
+  const uint32_t hd = c.dim / c.heads;
+  if (hd < 4 || hd > 128 || (hd & (hd - 1))) return CK_INVALID_CONFIG;
+  if (c.dim > 16384 || c.hidden > 16384 || c.layers > 4095 || c.vocab > (1u << 20) ||
+      c.context > 32768)
+    return CK_INVALID_CONFIG;
+  return CK_OK;
+}
+
+struct Parsed {
+  ck_config cfg;
+  uint32_t inv_sqrt, flags;
+  std::vector<const uint8_t*> t;
+};
+
+int parse_artifact(const void* artifact, size_t len, Parsed* out) {
+  if (!artifact || !out) return CK_INVALID_ARGUMENT;
+  const uint8_t* a = static_cast<const uint8_t*>(artifact);
+  if (len < 64 || memcmp(a, "CKMODEL1", 8) != 0) return CK_INVALID_FORMAT;
+  ck_config c;
+  memcpy(&c, a + 8, sizeof(c));
+  int rc = check_config(c);
+  if (rc) return rc;
+  const uint32_t n = rd32(a + 44);
+  if (n != 8 + 16 * c.layers || rd64(a + 48) != len || 64 + 16ull * n > len) return CK_INVALID_FORMAT;
+  const uint64_t d = c.dim, h = c.hidden, v = c.vocab, kv = (uint64_t)c.dim / c.heads * c.kv_heads;
+  const bool tied = rd32(a + 40) & 1u;
+  const uint64_t glob[8] = {v * d, 4 * v, 4 * d, tied ? 0 : v * d, tied ? 0 : 4 * v,
+                            4ull * c.context * (c.dim / c.heads), 4ull * kTable, 4ull * kTable};
+  const uint64_t lay[16] = {4 * d, d * d, 4 * d, kv * d, 4 * kv, kv * d, 4 * kv, d * d,
+                            4 * d, 4 * d, h * d, 4 * h, h * d, 4 * h, d * h, 4 * d};
+  out->t.assign(n, nullptr);
+  for (uint32_t i = 0; i < n; ++i) {
+    const uint64_t off = rd64(a + 64 + 16ull * i), tl = rd64(a + 64 + 16ull * i + 8);
+    const uint64_t want = i < 8 ? glob[i] : lay[(i - 8) % 16];
+    if (tl != want) return CK_INVALID_FORMAT;
+    if (tl && (off > len || tl > len - off || off % 4)) return CK_INVALID_FORMAT;
+    out->t[i] = a + off;
+  }
+  out->cfg = c;
+  out->inv_sqrt = rd32(a + 36);
+  out->flags = rd32(a + 40);
+  return CK_OK;
+}
+
+// Offsets of the device model layout.
+struct DevPlan {
+  uint64_t embed, embed_scale, cls, cls_scale, final_norm, rope, exp_tab, silu_tab, scratch;
+  struct L { uint64_t wqkv, sqkv, wo, so, w13, s13, w2, s2, an, fn; };
+  std::vector<L> layers;
+  uint64_t total;
+};
+
+DevPlan plan_device(const ck_config& c, bool tied) {
+  DevPlan P;
+  const uint64_t pd = pad16(c.dim), ph = pad16(c.hidden), hd = c.dim / c.heads;
+  const uint64_t kv = hd * c.kv_heads;
+  uint64_t off = 0;
+  auto take = [&](uint64_t bytes) { uint64_t o = off; off = align256(off + bytes); return o; };
+  P.embed = take(c.vocab * pd);
+  P.embed_scale = take(4ull * c.vocab);
+  P.cls = tied ? P.embed : take(c.vocab * pd);
+  P.cls_scale = tied ? P.embed_scale : take(4ull * c.vocab);
+  P.final_norm = take(4ull * c.dim);
+  P.rope = take(4ull * c.context * hd);
+  P.exp_tab = take(4ull * kTable);
+  P.silu_tab = take(4ull * kTable);
+  P.layers.resize(c.layers);
+  for (uint32_t l = 0; l < c.layers; ++l) {
+    DevPlan::L& L = P.layers[l];
+    L.wqkv = take((c.dim + 2 * kv) * pd);
+    L.sqkv = take(4 * (c.dim + 2 * kv));
+    L.wo = take(c.dim * pd);
+    L.so = take(4ull * c.dim);
+    L.w13 = take(2ull * c.hidden * pd);
+    L.s13 = take(8ull * c.hidden);
+    L.w2 = take(c.dim * ph);
+    L.s2 = take(4ull * c.dim);
+    L.an = take(4ull * c.dim);
+    L.fn = take(4ull * c.dim);
+  }
+  P.scratch = take(256);
+  P.total = off;
+  return P;
+}
+
+#define CK_CUDA(call)                          \
+  do {                                         \
+    cudaError_t e_ = (call);                   \
+    if (e_ != cudaSuccess) return CK_CUDA_ERROR; \
+  } while (0)
+
+inline cudaStream_t S(void* s) { return static_cast<cudaStream_t>(s); }
+
+// Copies rows x cols bytes (source pitch cols) to a destination with pitch dpitch.
+cudaError_t copy_rows(uint8_t* dst, size_t dpitch, const uint8_t* src, size_t cols, size_t rows,
+                      cudaStream_t s) {
+  if (!rows || !cols) return cudaSuccess;
+  if (dpitch == cols) return cudaMemcpyAsync(dst, src, rows * cols, cudaMemcpyHostToDevice, s);
+  return cudaMemcpy2DAsync(dst, dpitch, src, cols, cols, rows, cudaMemcpyHostToDevice, s);
+}
+
+// ------------------------------------------------------------------ small kernels
+
+// Phase 3: x[i] = ((byte - 128) * scale) >> 8 over the row of this position's token.
+__global__ void k_embed(uint8_t* st, uint64_t off_prompt, uint64_t off_out, int64_t* x,
+                        const uint8_t* embed, const uint32_t* scale, uint32_t pitch, uint32_t dim,
+                        uint32_t vocab) {
+  if (hdr_ld<uint32_t>(st, kHPhase) != CK_PHASE_RUNNING) return;
+  const uint32_t pos = hdr_ld<uint32_t>(st, kHPosition), np = hdr_ld<uint32_t>(st, kHNPrompt);
+  const uint32_t tok = pos < np ? reinterpret_cast<const uint32_t*>(st + off_prompt)[pos]
+                                : reinterpret_cast<const uint32_t*>(st + off_out)[pos - np];
+  if (tok >= vocab) {  // a state edited outside the library: stop instead of reading past the table
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      hdr<uint32_t>(st, kHError) = CK_INVALID_STATE;
+      hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
+    }
+    return;
+  }
+  const uint8_t* row = embed + (size_t)tok * pitch;
+  const int64_t s = (int64_t)__ldg(scale + tok);
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < dim; i += gridDim.x * blockDim.x)
+    x[i] = ((int64_t)row[i] - 128) * s >> 8;
+}
+
+// End of a prompt position: the last residual (x = xb + y), then the cursor moves on, or
+// the state is marked failed if a cache store did not fit.
+__global__ void k_finish_prompt(uint8_t* st, int64_t* x, const int64_t* xb, const int64_t* y,
+                                uint32_t dim) {
+  if (hdr_ld<uint32_t>(st, kHPhase) != CK_PHASE_RUNNING) return;
+  for (uint32_t i = threadIdx.x; i < dim; i += blockDim.x) x[i] = wadd(xb[i], y[i]);
+  if (threadIdx.x == 0) {
+    if (hdr_ld<uint64_t>(st, kHErrKey) != kNoError) {
+      hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
+      hdr<uint32_t>(st, kHError) = CK_ARITHMETIC;
+    } else {
+      hdr<uint32_t>(st, kHPosition) += 1;
+    }
+  }
+}
+
+constexpr int kArgThreads = 1024;
+
+// First index of the largest logit (strictly greater wins while scanning upward).
+__device__ void block_argmax(const int64_t* l, uint32_t n, long long* best_v, uint32_t* best_i) {
+  __shared__ long long sv[kArgThreads / 32];
+  __shared__ uint32_t si[kArgThreads / 32];
+  long long bv = LLONG_MIN;
+  uint32_t bi = 0xFFFFFFFFu;
+  for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
+    const long long v = l[i];
+    if (bi == 0xFFFFFFFFu || v > bv) {
+      bv = v;
+      bi = i;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const long long ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const uint32_t oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (oi != 0xFFFFFFFFu && (bi == 0xFFFFFFFFu || ov > bv || (ov == bv && oi < bi))) {
+      bv = ov;
+      bi = oi;
+    }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    sv[warp] = bv;
+    si[warp] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x / 32); ++w) {
+      if (si[w] != 0xFFFFFFFFu && (bi == 0xFFFFFFFFu || sv[w] > bv || (sv[w] == bv && si[w] < bi))) {
+        bv = sv[w];
+        bi = si[w];
+      }
+    }
+    *best_v = bv;
+    *best_i = bi;
+  }
+}
+
+// Phase 19 at temperature zero plus the end of a generating position.
+__global__ void __launch_bounds__(kArgThreads) k_sample_finish(uint8_t* st, uint64_t off_out,
+                                                              const int64_t* logits, uint32_t vocab) {
+  if (hdr_ld<uint32_t>(st, kHPhase) != CK_PHASE_RUNNING) return;
+  if (hdr_ld<uint64_t>(st, kHErrKey) != kNoError) {
+    if (threadIdx.x == 0) {
+      hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
+      hdr<uint32_t>(st, kHError) = CK_ARITHMETIC;
+    }
+    return;
+  }
+  long long bv;
+  uint32_t bi;
+  block_argmax(logits, vocab, &bv, &bi);
+  if (threadIdx.x == 0) {
+    const uint32_t gen = hdr_ld<uint32_t>(st, kHGenerated);
+    if (gen >= hdr_ld<uint32_t>(st, kHMaxTok)) {  // unreachable for states the turn validated
+      hdr<uint32_t>(st, kHError) = CK_INVALID_STATE;
+      hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
+      return;
+    }
+    reinterpret_cast<uint32_t*>(st + off_out)[gen] = bi;
+    hdr<uint32_t>(st, kHGenerated) = gen + 1;
+    hdr<uint32_t>(st, kHLastTok) = bi;
+    hdr<long long>(st, kHMaxLogit) = bv;
+    const bool stop = (hdr_ld<uint32_t>(st, kHFlags) & CK_FLAG_STOP_TOKENS) && (bi == 1 || bi == 2);
+    if (gen + 1 == hdr_ld<uint32_t>(st, kHMaxTok) || stop) hdr<uint32_t>(st, kHPhase) = CK_PHASE_DONE;
+    hdr<uint32_t>(st, kHPosition) += 1;
+  }
+}
+
+__global__ void __launch_bounds__(kArgThreads) k_argmax(const int64_t* logits, uint32_t vocab,
+                                                       uint32_t* out) {
+  long long bv;
+  uint32_t bi;
+  block_argmax(logits, vocab, &bv, &bi);
+  if (threadIdx.x == 0) *out = bi;
+}
+
+// ------------------------------------------------------------------ state checks
+
+struct HostHeader {
+  uint8_t b[kHeaderBytes];
+  uint32_t u32(uint32_t off) const { return rd32(b + off); }
+  uint64_t u64(uint32_t off) const { return rd64(b + off); }
+};
+
+int read_header(const void* dev_state, HostHeader* h, cudaStream_t s) {
+  CK_CUDA(cudaMemcpyAsync(h->b, dev_state, kHeaderBytes, cudaMemcpyDeviceToHost, s));
+  CK_CUDA(cudaStreamSynchronize(s));
+  return CK_OK;
+}
+
+// Checks that a state belongs to the model and has a valid cursor ("InvalidState").
+int check_state(const ck_model* m, const void* dev_state, size_t len, const HostHeader& h,
+                StateLayout* lay) {
+  if (memcmp(h.b, "CKSTATE1", 8) != 0) return CK_INVALID_STATE;
+  for (int i = 0; i < 7; ++i)
+    if (h.u32(kHConfig + 4 * i) != (&m->cfg.dim)[i]) return CK_INVALID_STATE;
+  const uint32_t np = h.u32(kHNPrompt), mt = h.u32(kHMaxTok);
+  if (!np || !mt || mt > m->cfg.context || (uint64_t)np + mt - 1 > m->cfg.context) return CK_INVALID_STATE;
+  *lay = state_layout(m->cfg, np, mt);
+  if (len != lay->size || h.u32(kHCache) != lay->cache) return CK_INVALID_STATE;
+  const uint32_t pos = h.u32(kHPosition);
+  if (pos > lay->cache) return CK_INVALID_STATE;
+  // tokens generated so far = generating positions already run
+  const uint32_t gen = pos + 1 > np ? pos + 1 - np : 0;
+  if (h.u32(kHGenerated) != gen) return CK_INVALID_STATE;
+  (void)dev_state;
+  return CK_OK;
+}
+
+int attention_cluster(uint32_t cache) {
+  uint32_t c = (cache + 15) / 16;
+  if (c < 1) c = 1;
+  if (c > 8) c = 8;
+  return (int)c;
+}
+
+// Enqueues one position's kernels (phases 3 to 16 for every layer, then 17 to 19 when the
+// position generates a token).
+int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, bool generating,
+                     cudaStream_t s) {
+  const ck_config& c = m->cfg;
+  int64_t* x = reinterpret_cast<int64_t*>(st + lay.x);
+  int64_t* xb = reinterpret_cast<int64_t*>(st + lay.xb);
+  int64_t* q = reinterpret_cast<int64_t*>(st + lay.q);
+  int64_t* o = reinterpret_cast<int64_t*>(st + lay.o);
+  int64_t* y = reinterpret_cast<int64_t*>(st + lay.y);
+  int64_t* hbuf = reinterpret_cast<int64_t*>(st + lay.h);
+  int64_t* logits = reinterpret_cast<int64_t*>(st + lay.logits);
+  int32_t* K = reinterpret_cast<int32_t*>(st + lay.k);
+  int32_t* V = reinterpret_cast<int32_t*>(st + lay.v);
+  const size_t layer_words = (size_t)lay.cache * m->kv_dim;
+  const int cl = attention_cluster(lay.cache);
+
+  k_embed<<<(c.dim + 255) / 256, 256, 0, s>>>(st, lay.prompt, lay.out, x, m->embed, m->embed_scale,
+                                              m->pitch_d, c.dim, c.vocab);
+  CK_CUDA(cudaGetLastError());
+  int64_t* cur = x;  // the buffer holding the activations
+  for (uint32_t l = 0; l < c.layers; ++l) {
+    const DevLayer& W = m->layers[l];
+    // phases 4-8: residual of the previous layer, attention norm, Q/K/V, cache stores, rotary
+    MatrowParams p = {};
+    p.W = W.wqkv;
+    p.scale = W.sqkv;
+    p.pitch = m->pitch_d;
+    p.rows = c.dim + 2 * m->kv_dim;
+    p.cols = c.dim;
+    p.pro = kProNorm;
+    p.in = cur;
+    p.norm_w = W.attn_norm;
+    if (l > 0) {
+      int64_t* next = cur == x ? xb : x;
+      p.add = y;
+      p.res_out = next;
+      cur = next;
+    }
+    p.epi = kEpiQKV;
+    p.out = q;
+    p.q_rows = c.dim;
+    p.kv_dim = m->kv_dim;
+    p.head_dim = m->head_dim;
+    p.layer = l;
+    p.cache = lay.cache;
+    p.kcache = K + l * layer_words;
+    p.vcache = V + l * layer_words;
+    p.rope = m->rope;
+    p.state = st;
+    CK_CUDA(launch_matrow(p, s, m->num_sms));
+    // phase 9
+    AttnParams a = {};
+    a.state = st;
+    a.q = q;
+    a.o = o;
+    a.kcache = K + l * layer_words;
+    a.vcache = V + l * layer_words;
+    a.exp_tab = m->exp_tab;
+    a.heads = c.heads;
+    a.kv_heads = c.kv_heads;
+    a.head_dim = m->head_dim;
+    a.kv_dim = m->kv_dim;
+    a.inv_sqrt = m->inv_sqrt;
+    a.cache = lay.cache;
+    a.chunk_cap = (lay.cache + cl - 1) / cl;
+    CK_CUDA(launch_attention(a, s, cl));
+    // phase 10
+    MatrowParams po = {};
+    po.W = W.wo;
+    po.scale = W.so;
+    po.pitch = m->pitch_d;
+    po.rows = c.dim;
+    po.cols = c.dim;
+    po.pro = kProPlain;
+    po.in = o;
+    po.epi = kEpiStore;
+    po.out = y;
+    po.state = st;
+    CK_CUDA(launch_matrow(po, s, m->num_sms));
+    // phases 11-14: residual, feed-forward norm, gate and up, SiLU gating
+    int64_t* next = cur == x ? xb : x;
+    MatrowParams pg = {};
+    pg.W = W.w13;
+    pg.scale = W.s13;
+    pg.pitch = m->pitch_d;
+    pg.rows = 2 * c.hidden;
+    pg.cols = c.dim;
+    pg.pro = kProNorm;
+    pg.in = cur;
+    pg.add = y;
+    pg.res_out = next;
+    pg.norm_w = W.ffn_norm;
+    pg.epi = kEpiSiLU;
+    pg.out = hbuf;
+    pg.silu_tab = m->silu_tab;
+    pg.state = st;
+    cur = next;
+    CK_CUDA(launch_matrow(pg, s, m->num_sms));
+    // phase 15 (its residual, phase 16, is added by the next consumer)
+    MatrowParams pd = {};
+    pd.W = W.w2;
+    pd.scale = W.s2;
+    pd.pitch = m->pitch_h;
+    pd.rows = c.dim;
+    pd.cols = c.hidden;
+    pd.pro = kProPlain;
+    pd.in = hbuf;
+    pd.epi = kEpiStore;
+    pd.out = y;
+    pd.state = st;
+    CK_CUDA(launch_matrow(pd, s, m->num_sms));
+  }
+  if (cur != xb) return CK_INVALID_STATE;  // an odd number of residual flips, by construction
+  if (generating) {
+    // phases 16-18: last residual into x, final norm, classifier
+    MatrowParams pc = {};
+    pc.W = m->cls;
+    pc.scale = m->cls_scale;
+    pc.pitch = m->pitch_d;
+    pc.rows = c.vocab;
+    pc.cols = c.dim;
+    pc.pro = kProNorm;
+    pc.in = xb;
+    pc.add = y;
+    pc.res_out = x;
+    pc.norm_w = m->final_norm;
+    pc.epi = kEpiStore;
+    pc.out = logits;
+    pc.state = st;
+    CK_CUDA(launch_matrow(pc, s, m->num_sms));
+    k_sample_finish<<<1, kArgThreads, 0, s>>>(st, lay.out, logits, c.vocab);  // phase 19
+  } else {
+    k_finish_prompt<<<1, 256, 0, s>>>(st, x, xb, y, c.dim);
+  }
+  CK_CUDA(cudaGetLastError());
+  return CK_OK;
+}
+
+int get_graph(ck_model* m, void* dev_state, size_t len, const StateLayout& lay, bool generating,
+              cudaGraphExec_t* out) {
+  for (auto& g : m->graphs)
+    if (g.state == dev_state && g.len == len && g.generating == generating) {
+      *out = g.exec;
+      return CK_OK;
+    }
+  if (m->graphs.size() >= 16) {  // bounded cache: drop the oldest pair
+    cudaGraphExecDestroy(m->graphs.front().exec);
+    m->graphs.erase(m->graphs.begin());
+  }
+  CK_CUDA(cudaStreamBeginCapture(m->capture, cudaStreamCaptureModeThreadLocal));
+  int rc = enqueue_position(m, static_cast<uint8_t*>(dev_state), lay, generating, m->capture);
+  cudaGraph_t graph = nullptr;
+  cudaError_t e = cudaStreamEndCapture(m->capture, &graph);
+  if (rc) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+  }
+  if (e != cudaSuccess) return CK_CUDA_ERROR;
+  cudaGraphExec_t exec;
+  e = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) return CK_CUDA_ERROR;
+  m->graphs.push_back({dev_state, len, generating, exec});
+  *out = exec;
+  return CK_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+const char* ck_version(void) { return "libck 0.1 (sm_103a)"; }
+
+uint64_t ck_host_isqrt(uint64_t v) { return isqrt_u64(v); }
+
+int64_t ck_host_div_trunc(int64_t n, uint32_t d) {
+  if (d == 0) return 0;
+  return sdiv_trunc(n, make_invdiv(d));
+}
+
+int ck_model_size(const void* artifact, size_t len, size_t* dev_bytes) {
+  if (!dev_bytes) return CK_INVALID_ARGUMENT;
+  Parsed P;
+  int rc = parse_artifact(artifact, len, &P);
+  if (rc) return rc;
+  *dev_bytes = plan_device(P.cfg, P.flags & 1u).total;
+  return CK_OK;
+}
+
+int ck_load_model(const void* artifact, size_t len, void* dev_mem, size_t dev_len, void* stream,
+                  ck_model** out) {
+  if (!out || !dev_mem) return CK_INVALID_ARGUMENT;
+  *out = nullptr;
+  if (reinterpret_cast<uintptr_t>(dev_mem) % 256) return CK_INVALID_ARGUMENT;
+  Parsed P;
+  int rc = parse_artifact(artifact, len, &P);
+  if (rc) return rc;
+  const ck_config& c = P.cfg;
+  const bool tied = P.flags & 1u;
+  DevPlan D = plan_device(c, tied);
+  if (dev_len < D.total) return CK_BUFFER_TOO_SMALL;
+  cudaStream_t s = S(stream);
+  uint8_t* dv = static_cast<uint8_t*>(dev_mem);
+  const uint32_t pd = pad16(c.dim), ph = pad16(c.hidden), hd = c.dim / c.heads;
+  const uint32_t kv = hd * c.kv_heads;
+  CK_CUDA(cudaMemsetAsync(dv, 0, D.total, s));
+  auto T = [&](uint32_t i) { return P.t[i]; };
+  CK_CUDA(copy_rows(dv + D.embed, pd, T(0), c.dim, c.vocab, s));
+  CK_CUDA(cudaMemcpyAsync(dv + D.embed_scale, T(1), 4ull * c.vocab, cudaMemcpyHostToDevice, s));
+  if (!tied) {
+    CK_CUDA(copy_rows(dv + D.cls, pd, T(3), c.dim, c.vocab, s));
+    CK_CUDA(cudaMemcpyAsync(dv + D.cls_scale, T(4), 4ull * c.vocab, cudaMemcpyHostToDevice, s));
+  }
+  CK_CUDA(cudaMemcpyAsync(dv + D.final_norm, T(2), 4ull * c.dim, cudaMemcpyHostToDevice, s));
+  CK_CUDA(cudaMemcpyAsync(dv + D.rope, T(5), 4ull * c.context * hd, cudaMemcpyHostToDevice, s));
+  CK_CUDA(cudaMemcpyAsync(dv + D.exp_tab, T(6), 4ull * kTable, cudaMemcpyHostToDevice, s));
+  CK_CUDA(cudaMemcpyAsync(dv + D.silu_tab, T(7), 4ull * kTable, cudaMemcpyHostToDevice, s));
+  for (uint32_t l = 0; l < c.layers; ++l) {
+    const DevPlan::L& L = D.layers[l];
+    const uint32_t b = 8 + 16 * l;
+    CK_CUDA(cudaMemcpyAsync(dv + L.an, T(b + 0), 4ull * c.dim, cudaMemcpyHostToDevice, s));
+    CK_CUDA(copy_rows(dv + L.wqkv, pd, T(b + 1), c.dim, c.dim, s));
+    CK_CUDA(cudaMemcpyAsync(dv + L.sqkv, T(b + 2), 4ull * c.dim, cudaMemcpyHostToDevice, s));
+    CK_CUDA(copy_rows(dv + L.wqkv + (size_t)c.dim * pd, pd, T(b + 3), c.dim, kv, s));
+    CK_CUDA(cudaMemcpyAsync(dv + L.sqkv + 4ull * c.dim, T(b + 4), 4ull * kv, cudaMemcpyHostToDevice, s));
+    CK_CUDA(copy_rows(dv + L.wqkv + (size_t)(c.dim + kv) * pd, pd, T(b + 5), c.dim, kv, s));
+    CK_CUDA(cudaMemcpyAsync(dv + L.sqkv + 4ull * (c.dim + kv), T(b + 6), 4ull * kv,
+                            cudaMemcpyHostToDevice, s));
+    CK_CUDA(copy_rows(dv + L.wo, pd, T(b + 7), c.dim, c.dim, s));
+    CK_CUDA(cudaMemcpyAsync(dv + L.so, T(b + 8), 4ull * c.dim, cudaMemcpyHostToDevice, s));
+    CK_CUDA(cudaMemcpyAsync(dv + L.fn, T(b + 9), 4ull * c.dim, cudaMemcpyHostToDevice, s));
+    // gate rows to even rows, up rows to odd rows (and their scales likewise)
+    CK_CUDA(cudaMemcpy2DAsync(dv + L.w13, 2ull * pd, T(b + 10), c.dim, c.dim, c.hidden,
+                              cudaMemcpyHostToDevice, s));
+    CK_CUDA(cudaMemcpy2DAsync(dv + L.w13 + pd, 2ull * pd, T(b + 12), c.dim, c.dim, c.hidden,
+                              cudaMemcpyHostToDevice, s));
+    CK_CUDA(cudaMemcpy2DAsync(dv + L.s13, 8, T(b + 11), 4, 4, c.hidden, cudaMemcpyHostToDevice, s));
+    CK_CUDA(cudaMemcpy2DAsync(dv + L.s13 + 4, 8, T(b + 13), 4, 4, c.hidden, cudaMemcpyHostToDevice, s));
+    CK_CUDA(copy_rows(dv + L.w2, ph, T(b + 14), c.hidden, c.dim, s));
+    CK_CUDA(cudaMemcpyAsync(dv + L.s2, T(b + 15), 4ull * c.dim, cudaMemcpyHostToDevice, s));
+  }
+  CK_CUDA(cudaStreamSynchronize(s));
+
+  ck_model* m = new (std::nothrow) ck_model();
+  if (!m) return CK_CUDA_ERROR;
+  m->cfg = c;
+  m->head_dim = hd;
+  m->kv_dim = kv;
+  m->inv_sqrt = P.inv_sqrt;
+  m->flags = P.flags;
+  m->pitch_d = pd;
+  m->pitch_h = ph;
+  m->dev = dv;
+  m->dev_len = dev_len;
+  m->embed = dv + D.embed;
+  m->embed_scale = reinterpret_cast<const uint32_t*>(dv + D.embed_scale);
+  m->cls = dv + D.cls;
+  m->cls_scale = reinterpret_cast<const uint32_t*>(dv + D.cls_scale);
+  m->final_norm = reinterpret_cast<const int32_t*>(dv + D.final_norm);
+  m->rope = reinterpret_cast<const int32_t*>(dv + D.rope);
+  m->exp_tab = reinterpret_cast<const uint32_t*>(dv + D.exp_tab);
+  m->silu_tab = reinterpret_cast<const int32_t*>(dv + D.silu_tab);
+  m->scratch = reinterpret_cast<uint32_t*>(dv + D.scratch);
+  m->layers.resize(c.layers);
+  for (uint32_t l = 0; l < c.layers; ++l) {
+    const DevPlan::L& L = D.layers[l];
+    DevLayer& W = m->layers[l];
+    W.wqkv = dv + L.wqkv;
+    W.sqkv = reinterpret_cast<const uint32_t*>(dv + L.sqkv);
+    W.wo = dv + L.wo;
+    W.so = reinterpret_cast<const uint32_t*>(dv + L.so);
+    W.w13 = dv + L.w13;
+    W.s13 = reinterpret_cast<const uint32_t*>(dv + L.s13);
+    W.w2 = dv + L.w2;
+    W.s2 = reinterpret_cast<const uint32_t*>(dv + L.s2);
+    W.attn_norm = reinterpret_cast<const int32_t*>(dv + L.an);
+    W.ffn_norm = reinterpret_cast<const int32_t*>(dv + L.fn);
+  }
+  if (configure_matrow() != cudaSuccess || configure_attention() != cudaSuccess) {
+    delete m;
+    return CK_CUDA_ERROR;
+  }
+  if (cudaGetDevice(&m->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&m->capture, cudaStreamNonBlocking) != cudaSuccess) {
+    delete m;
+    return CK_CUDA_ERROR;
+  }
+  *out = m;
+  return CK_OK;
+}
+
+int ck_model_config(const ck_model* m, ck_config* out) {
+  if (!m || !out) return CK_INVALID_ARGUMENT;
+  *out = m->cfg;
+  return CK_OK;
+}
+
+void ck_free_model(ck_model* m) {
+  if (!m) return;
+  for (auto& g : m->graphs) cudaGraphExecDestroy(g.exec);
+  if (m->capture) cudaStreamDestroy(m->capture);
+  delete m;
+}
+
+int ck_state_size(const ck_model* m, uint32_t n_prompt, uint32_t max_tokens, size_t* out) {
+  if (!m || !out) return CK_INVALID_ARGUMENT;
+  if (!n_prompt || !max_tokens || max_tokens > m->cfg.context) return CK_INVALID_PROMPT;
+  if ((uint64_t)n_prompt + max_tokens - 1 > m->cfg.context) return CK_CONTEXT_EXCEEDED;
+  *out = state_layout(m->cfg, n_prompt, max_tokens).size;
+  return CK_OK;
+}
+
+int ck_init_state(const ck_model* m, void* dev_state, size_t len, const uint32_t* host_ids,
+                  uint32_t n_ids, uint32_t max_tokens, uint32_t temperature_q16, uint64_t seed,
+                  uint32_t flags, void* stream) {
+  if (!m || !dev_state || (n_ids && !host_ids)) return CK_INVALID_ARGUMENT;
+  if (reinterpret_cast<uintptr_t>(dev_state) % 256) return CK_INVALID_STATE;
+  if (!n_ids || !max_tokens || max_tokens > m->cfg.context) return CK_INVALID_PROMPT;
+  if (temperature_q16 != 0) return CK_INVALID_PROMPT;  // only the maximum pass is built
+  for (uint32_t i = 0; i < n_ids; ++i)
+    if (host_ids[i] >= m->cfg.vocab) return CK_INVALID_PROMPT;
+  if ((uint64_t)n_ids + max_tokens - 1 > m->cfg.context) return CK_CONTEXT_EXCEEDED;
+  const StateLayout lay = state_layout(m->cfg, n_ids, max_tokens);
+  if (len != lay.size) return CK_BUFFER_TOO_SMALL;
+  std::vector<uint8_t> h(lay.x, 0);  // header, prompt ids and output tokens
+  memcpy(h.data(), "CKSTATE1", 8);
+  auto w32 = [&](uint32_t off, uint32_t v) { memcpy(h.data() + off, &v, 4); };
+  auto w64 = [&](uint32_t off, uint64_t v) { memcpy(h.data() + off, &v, 8); };
+  w32(kHPhase, CK_PHASE_RUNNING);
+  w32(kHNPrompt, n_ids);
+  w32(kHMaxTok, max_tokens);
+  w32(kHCache, lay.cache);
+  w32(kHFlags, flags);
+  w32(kHTemp, temperature_q16);
+  w32(kHLastTok, 0xFFFFFFFFu);
+  w64(kHSeed, seed);
+  w64(kHErrKey, kNoError);
+  for (int i = 0; i < 7; ++i) w32(kHConfig + 4 * i, (&m->cfg.dim)[i]);
+  memcpy(h.data() + lay.prompt, host_ids, 4ull * n_ids);
+  cudaStream_t s = S(stream);
+  CK_CUDA(cudaMemsetAsync(dev_state, 0, len, s));
+  CK_CUDA(cudaMemcpyAsync(dev_state, h.data(), h.size(), cudaMemcpyHostToDevice, s));
+  CK_CUDA(cudaStreamSynchronize(s));
+  return CK_OK;
+}
+
+int ck_turn(ck_model* m, void* dev_state, size_t len, uint32_t n_positions, void* stream,
+            ck_turn_result* out) {
+  if (!m || !dev_state || !out) return CK_INVALID_ARGUMENT;
+  memset(out, 0, sizeof(*out));
+  out->token = 0xFFFFFFFFu;
+  if (reinterpret_cast<uintptr_t>(dev_state) % 256) return CK_INVALID_STATE;
+  cudaStream_t s = S(stream);
+  HostHeader h0;
+  int rc = read_header(dev_state, &h0, s);
+  if (rc) return rc;
+  StateLayout lay;
+  rc = check_state(m, dev_state, len, h0, &lay);
+  if (rc) return rc;
+  if (h0.u32(kHPhase) != CK_PHASE_RUNNING) return CK_INVALID_STATE;
+  const uint32_t pos0 = h0.u32(kHPosition), np = h0.u32(kHNPrompt);
+  if (pos0 >= lay.cache) return CK_INVALID_STATE;
+  uint32_t n = n_positions;
+  if (n > lay.cache - pos0) n = lay.cache - pos0;
+  for (uint32_t i = 0; i < n; ++i) {
+    const bool generating = pos0 + i + 1 >= np;
+    cudaGraphExec_t exec;
+    rc = get_graph(m, dev_state, len, lay, generating, &exec);
+    if (rc) return rc;
+    CK_CUDA(cudaGraphLaunch(exec, s));
+  }
+  HostHeader h1;
+  rc = read_header(dev_state, &h1, s);
+  if (rc) return rc;
+  const bool failed = h1.u32(kHPhase) == CK_PHASE_FAILED;
+  uint64_t turns = h1.u64(kHTurns) + 1;
+  CK_CUDA(cudaMemcpyAsync(static_cast<uint8_t*>(dev_state) + kHTurns, &turns, 8,
+                          cudaMemcpyHostToDevice, s));
+  CK_CUDA(cudaStreamSynchronize(s));
+  out->generated = h1.u32(kHGenerated);
+  out->generated_this_turn = out->generated - h0.u32(kHGenerated);
+  if (out->generated_this_turn) out->token = h1.u32(kHLastTok);
+  out->work = h1.u32(kHPosition) - pos0 + (failed ? 1u : 0u);
+  out->complete = h1.u32(kHPhase) != CK_PHASE_RUNNING;
+  const uint64_t key = h1.u64(kHErrKey);
+  if (key != kNoError) {
+    out->err_position = (uint32_t)(key >> 44);
+    out->err_layer = (uint32_t)(key >> 32) & 0xFFFu;
+    out->err_phase = (uint32_t)(key >> 24) & 0xFFu;
+    out->err_element = (uint32_t)key & 0xFFFFFFu;
+  }
+  return failed ? (int)h1.u32(kHError) : CK_OK;
+}
+
+int ck_logits(const ck_model* m, const void* dev_state, size_t len, int64_t* host_out, void* stream) {
+  if (!m || !dev_state || !host_out) return CK_INVALID_ARGUMENT;
+  cudaStream_t s = S(stream);
+  HostHeader h;
+  int rc = read_header(dev_state, &h, s);
+  if (rc) return rc;
+  StateLayout lay;
+  rc = check_state(m, dev_state, len, h, &lay);
+  if (rc) return rc;
+  CK_CUDA(cudaMemcpyAsync(host_out, static_cast<const uint8_t*>(dev_state) + lay.logits,
+                          8ull * m->cfg.vocab, cudaMemcpyDeviceToHost, s));
+  CK_CUDA(cudaStreamSynchronize(s));
+  return CK_OK;
+}
+
+int ck_argmax(const ck_model* m, const void* dev_state, size_t len, uint32_t* out, void* stream) {
+  if (!m || !dev_state || !out) return CK_INVALID_ARGUMENT;
+  cudaStream_t s = S(stream);
+  HostHeader h;
+  int rc = read_header(dev_state, &h, s);
+  if (rc) return rc;
+  StateLayout lay;
+  rc = check_state(m, dev_state, len, h, &lay);
+  if (rc) return rc;
+  k_argmax<<<1, kArgThreads, 0, s>>>(
+      reinterpret_cast<const int64_t*>(static_cast<const uint8_t*>(dev_state) + lay.logits),
+      m->cfg.vocab, m->scratch);
+  CK_CUDA(cudaGetLastError());
+  CK_CUDA(cudaMemcpyAsync(out, m->scratch, 4, cudaMemcpyDeviceToHost, s));
+  CK_CUDA(cudaStreamSynchronize(s));
+  return CK_OK;
+}
+
+int ck_output_tokens(const ck_model* m, const void* dev_state, size_t len, uint32_t* host_out,
+                     uint32_t cap, uint32_t* n, void* stream) {
+  if (!m || !dev_state || !n || (cap && !host_out)) return CK_INVALID_ARGUMENT;
+  cudaStream_t s = S(stream);
+  HostHeader h;
+  int rc = read_header(dev_state, &h, s);
+  if (rc) return rc;
+  StateLayout lay;
+  rc = check_state(m, dev_state, len, h, &lay);
+  if (rc) return rc;
+  uint32_t g = h.u32(kHGenerated);
+  if (g > cap) g = cap;
+  if (g) {
+    CK_CUDA(cudaMemcpyAsync(host_out, static_cast<const uint8_t*>(dev_state) + lay.out, 4ull * g,
+                            cudaMemcpyDeviceToHost, s));
+    CK_CUDA(cudaStreamSynchronize(s));
+  }
+  *n = g;
+  return CK_OK;
+}
+
+int ck_state_download(const void* dev_state, size_t len, void* host, void* stream) {
+  if (!dev_state || !host) return CK_INVALID_ARGUMENT;
+  CK_CUDA(cudaMemcpyAsync(host, dev_state, len, cudaMemcpyDeviceToHost, S(stream)));
+  CK_CUDA(cudaStreamSynchronize(S(stream)));
+  return CK_OK;
+}
+
+int ck_state_upload(void* dev_state, const void* host, size_t len, void* stream) {
+  if (!dev_state || !host) return CK_INVALID_ARGUMENT;
+  CK_CUDA(cudaMemcpyAsync(dev_state, host, len, cudaMemcpyHostToDevice, S(stream)));
+  CK_CUDA(cudaStreamSynchronize(S(stream)));
+  return CK_OK;
+}
+
+int ck_matrow(const uint8_t* dev_W, size_t pitch, const uint32_t* dev_scale, uint32_t rows,
+              uint32_t cols, const int64_t* dev_x, int64_t* dev_y, void* stream) {
+  if (!dev_W || !dev_scale || !dev_x || !dev_y) return CK_INVALID_ARGUMENT;
+  if (pitch % 16 || pitch > 16384 || cols < 1 || cols > pitch || rows < 1 || rows > (1u << 24))
+    return CK_INVALID_ARGUMENT;
+  if (reinterpret_cast<uintptr_t>(dev_W) % 16 || reinterpret_cast<uintptr_t>(dev_x) % 8 ||
+      reinterpret_cast<uintptr_t>(dev_y) % 8 || reinterpret_cast<uintptr_t>(dev_scale) % 4)
+    return CK_INVALID_ARGUMENT;
+  int dev = 0, sms = 0;
+  CK_CUDA(configure_matrow());
+  CK_CUDA(cudaGetDevice(&dev));
+  CK_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  MatrowParams p = {};
+  p.W = dev_W;
+  p.scale = dev_scale;
+  p.pitch = (uint32_t)pitch;
+  p.rows = rows;
+  p.cols = cols;
+  p.pro = kProPlain;
+  p.in = dev_x;
+  p.epi = kEpiStore;
+  p.out = dev_y;
+  CK_CUDA(launch_matrow(p, S(stream), sms));
+  return CK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,215 @@
+// Internal definitions shared by the libck translation units (device helpers, the state
+// layout, the device model layout and the kernel parameter blocks).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cmath>
+#include <cuda_runtime.h>
+
+#include "../../include/ck.h"
+
+namespace ck {
+
+// ------------------------------------------------------------------ state header offsets
+constexpr uint32_t kHeaderBytes = 256;
+constexpr uint32_t kHPhase = 8, kHPosition = 12, kHNPrompt = 16, kHMaxTok = 20, kHCache = 24,
+                   kHGenerated = 28, kHFlags = 32, kHTemp = 36, kHError = 40, kHLastTok = 44,
+                   kHSeed = 48, kHTurns = 56, kHErrKey = 64, kHMaxLogit = 72, kHConfig = 80;
+constexpr uint64_t kNoError = ~0ull;
+
+struct StateLayout {
+  uint64_t prompt, out, x, xb, q, o, y, h, logits, scores, k, v, size;
+  uint32_t cache;
+};
+
+inline uint64_t align256(uint64_t n) { return (n + 255) & ~255ull; }
+
+inline StateLayout state_layout(const ck_config& c, uint32_t n_prompt, uint32_t max_tokens) {
+  const uint64_t kv_dim = (uint64_t)c.dim / c.heads * c.kv_heads;
+  const uint64_t cache = (uint64_t)n_prompt + max_tokens - 1;
+  StateLayout s;
+  uint64_t off = kHeaderBytes;
+  auto take = [&](uint64_t bytes) { uint64_t o = off; off = align256(off + bytes); return o; };
+  s.prompt = take(4ull * n_prompt);
+  s.out = take(4ull * max_tokens);
+  s.x = take(8ull * c.dim);
+  s.xb = take(8ull * c.dim);
+  s.q = take(8ull * c.dim);
+  s.o = take(8ull * c.dim);
+  s.y = take(8ull * c.dim);
+  s.h = take(8ull * c.hidden);
+  s.logits = take(8ull * c.vocab);
+  s.scores = take(8ull * c.heads * cache);
+  s.k = take(4ull * c.layers * cache * kv_dim);
+  s.v = take(4ull * c.layers * cache * kv_dim);
+  s.size = off;
+  s.cache = (uint32_t)cache;
+  return s;
+}
+
+// Device-side view of one state header field.
+template <typename T>
+__device__ __forceinline__ T& hdr(uint8_t* st, uint32_t off) {
+  return *reinterpret_cast<T*>(st + off);
+}
+template <typename T>
+__device__ __forceinline__ T hdr_ld(const uint8_t* st, uint32_t off) {
+  return *reinterpret_cast<const T*>(st + off);
+}
+
+__host__ __device__ inline uint64_t err_key(uint32_t pos, uint32_t layer, uint32_t phase,
+                                            uint32_t elem) {
+  return ((uint64_t)pos << 44) | ((uint64_t)layer << 32) | ((uint64_t)phase << 24) | elem;
+}
+
+// ------------------------------------------------------------------ integer helpers
+
+__host__ __device__ inline uint64_t mulhi_u64(uint64_t a, uint64_t b) {
+#ifdef __CUDA_ARCH__
+  return __umul64hi(a, b);
+#else
+  return (uint64_t)(((unsigned __int128)a * b) >> 64);
+#endif
+}
+
+// floor(sqrt(v)) for any u64: a double-precision estimate corrected by exact integer steps.
+__host__ __device__ inline uint64_t isqrt_u64(uint64_t v) {
+  uint64_t r = (uint64_t)sqrt((double)v);
+  if (r > 0xFFFFFFFFull) r = 0xFFFFFFFFull;
+  while (r * r > v) --r;
+  while (r < 0xFFFFFFFFull && (r + 1) * (r + 1) <= v) ++r;
+  return r;
+}
+
+// Division of a u64 by an invariant divisor d (1 <= d < 2^32) with one high multiply,
+// after Granlund and Montgomery, "Division by Invariant Integers using Multiplication"
+// (PLDI 1994), unsigned case with N = 64: l = ceil(log2 d),
+// m = floor(2^64 (2^l - d) / d) + 1, q = (t + ((n - t) >> min(l,1))) >> max(l-1,0) with
+// t = mulhi(m, n).
+struct InvDiv {
+  uint64_t m;
+  uint32_t sh1, sh2;
+};
+
+__host__ __device__ inline InvDiv make_invdiv(uint32_t d) {
+  uint32_t l = 0;
+  while (l < 32 && (1ull << l) < (uint64_t)d) ++l;
+  const uint64_t a = (1ull << l) - d;  // a < d
+  uint64_t q = 0, r = a;               // floor(a * 2^64 / d) by binary long division
+  for (int i = 63; i >= 0; --i) {
+    r <<= 1;                           // r < d < 2^32: never overflows
+    if (r >= d) {
+      r -= d;
+      q |= 1ull << i;
+    }
+  }
+  InvDiv D;
+  D.m = q + 1;
+  D.sh1 = l < 1 ? l : 1;
+  D.sh2 = l > 0 ? l - 1 : 0;
+  return D;
+}
+
+__host__ __device__ inline uint64_t udiv_inv(uint64_t n, const InvDiv& D) {
+  const uint64_t t = mulhi_u64(D.m, n);
+  return (t + ((n - t) >> D.sh1)) >> D.sh2;
+}
+
+// Signed division truncating toward zero.
+__host__ __device__ inline int64_t sdiv_trunc(int64_t n, const InvDiv& D) {
+  const uint64_t mag = n < 0 ? 0 - (uint64_t)n : (uint64_t)n;
+  const uint64_t q = udiv_inv(mag, D);
+  return n < 0 ? (int64_t)(0 - q) : (int64_t)q;
+}
+
+__host__ __device__ inline int64_t wmul(int64_t a, int64_t b) {
+  return (int64_t)((uint64_t)a * (uint64_t)b);
+}
+__host__ __device__ inline int64_t wadd(int64_t a, int64_t b) {
+  return (int64_t)((uint64_t)a + (uint64_t)b);
+}
+
+// The SiLU table lookup ("Lookup tables": 16 or more returns itself, -16 or less zero,
+// otherwise entry (x + 16) >> 9).
+__device__ __forceinline__ int64_t silu_lookup(int64_t g, const int32_t* tab) {
+  const int64_t sixteen = (int64_t)16 << 16;
+  if (g >= sixteen) return g;
+  if (g <= -sixteen) return 0;
+  return (int64_t)__ldg(tab + ((g + sixteen) >> 9));
+}
+
+// dp4a with the first operand's bytes unsigned and the second's signed.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+// ------------------------------------------------------------------ device model
+
+struct DevLayer {
+  const uint8_t* wqkv;   // [dim + 2 kv_dim][pitch_d]: Wq rows, then Wk, then Wv
+  const uint32_t* sqkv;
+  const uint8_t* wo;     // [dim][pitch_d]
+  const uint32_t* so;
+  const uint8_t* w13;    // [2 hidden][pitch_d]: gate row j at 2j, up row j at 2j+1
+  const uint32_t* s13;
+  const uint8_t* w2;     // [dim][pitch_h]
+  const uint32_t* s2;
+  const int32_t* attn_norm;
+  const int32_t* ffn_norm;
+};
+
+// ------------------------------------------------------------------ matrow parameters
+
+enum Prologue : int { kProPlain = 0, kProNorm = 1 };
+enum Epilogue : int { kEpiStore = 0, kEpiQKV = 1, kEpiSiLU = 2 };
+
+struct MatrowParams {
+  const uint8_t* W;
+  const uint32_t* scale;
+  uint32_t pitch;        // bytes per row, multiple of 16
+  uint32_t rows, cols;
+  // prologue: the input vector of `cols` elements
+  int pro;
+  const int64_t* in;     // plain: the vector; norm: the activations
+  const int64_t* add;    // norm: residual addend (nullptr: none)
+  int64_t* res_out;      // norm with addend: where block 0 writes in + add
+  const int32_t* norm_w;
+  // epilogue
+  int epi;
+  int64_t* out;          // store: y[rows]; QKV: rotated queries [q_rows]; SiLU: h[rows / 2]
+  uint32_t q_rows, kv_dim, head_dim, layer, cache;
+  int32_t* kcache;       // this layer's keys, position 0 (i32 [cache][kv_dim])
+  int32_t* vcache;
+  const int32_t* rope;   // [context][head/2][2]
+  const int32_t* silu_tab;
+  uint8_t* state;        // header for position, phase and errors (nullptr: standalone)
+};
+
+struct AttnParams {
+  uint8_t* state;
+  const int64_t* q;      // rotated queries [heads * hd]
+  int64_t* o;            // head outputs [heads * hd]
+  const int32_t* kcache; // this layer, position 0
+  const int32_t* vcache;
+  const uint32_t* exp_tab;
+  uint32_t heads, kv_heads, head_dim, kv_dim, inv_sqrt, cache, chunk_cap;
+};
+
+// Launchers (stream-ordered; return a cudaError_t).
+cudaError_t configure_matrow();     // once per process and device, outside stream capture
+cudaError_t configure_attention();
+cudaError_t launch_matrow(const MatrowParams& p, cudaStream_t s, int num_sms);
+size_t matrow_smem_bytes(uint32_t pitch);
+cudaError_t launch_attention(const AttnParams& p, cudaStream_t s, int cluster);
+
+}  // namespace ck

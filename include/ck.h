@@ -1,0 +1,199 @@
+/* ck.h — C ABI of libck, a GB300 (sm_103a) implementation of curta-core's bit-exact
+ * fixed-point transformer forward pass (phases 3 to 19), as the page "The inference core"
+ * (curta.chat docs) describes it.
+ *
+ * Conventions
+ *   - Every function returns int: 0 on success, otherwise an error number.  1 to 8 are the
+ *     page's core errors (section "Core errors"); 9 and 10 are additions of this library.
+ *   - Pointers named dev_* are device pointers on the current CUDA device; host_* and
+ *     unqualified buffers are host memory.  `stream` is a cudaStream_t (NULL = legacy
+ *     default stream).  All work is enqueued on `stream`; a call returns once its work is
+ *     enqueued unless it says it synchronizes.
+ *   - The library never allocates device memory for models or states: the caller allocates
+ *     them (for example as torch tensors) and passes pointer and length.  The library keeps
+ *     host-side handles and, per state, cached CUDA graphs.
+ *   - Integer formats follow the page's table in "Fixed-point arithmetic": activations,
+ *     queries, logits and scores are int64 with 16 fractional bits; cached keys and values
+ *     int32 with 16; weights are bytes holding weight + 128; row scales uint32 with 24;
+ *     norm weights and rotary cos/sin int32 with 24; probabilities int64 with 24; the
+ *     exponential table uint32 with 30; the SiLU table int32 with 16.
+ */
+#ifndef CK_H
+#define CK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- errors ("Core errors") */
+#define CK_OK 0
+#define CK_INVALID_CONFIG 1     /* a configuration value outside its range (limits below) */
+#define CK_INVALID_FORMAT 2     /* an artifact that does not open with CKMODEL1 or whose
+                                   directory does not fit the file or the configuration */
+#define CK_INVALID_STATE 3      /* a state with the wrong tag, size, alignment, model,
+                                   cursor, or one that is complete or failed */
+#define CK_BUFFER_TOO_SMALL 4   /* ck_init_state given a length other than ck_state_size,
+                                   or a device model buffer shorter than ck_model_size */
+#define CK_MISSING_WEIGHTS 5    /* reserved: a model always holds all its matrices */
+#define CK_INVALID_PROMPT 6     /* no prompt ids, an id >= vocab, max tokens 0 or above the
+                                   context, or a temperature other than 0 */
+#define CK_CONTEXT_EXCEEDED 7   /* prompt ids + max tokens - 1 above the context */
+#define CK_ARITHMETIC 8         /* a key or value that does not fit the cache's 32 bits */
+#define CK_CUDA_ERROR 9         /* a CUDA runtime call failed (library addition) */
+#define CK_INVALID_ARGUMENT 10  /* a null pointer, misaligned pointer or size outside the
+                                   documented limits (library addition) */
+
+/* ---------------------------------------------------------------- configuration
+ * Seven u32 in this order (the page: "the seven u32 values in order"; the order is the
+ * llama2.c header order).  Limits of this library: every field >= 1; dim % heads == 0;
+ * heads % kv_heads == 0; head size dim / heads a power of two from 4 to 128;
+ * dim <= 16384; hidden <= 16384; layers <= 4095; vocab <= 1048576; context <= 32768. */
+typedef struct ck_config {
+  uint32_t dim, hidden, layers, heads, kv_heads, vocab, context;
+} ck_config;
+
+/* ---------------------------------------------------------------- model artifact
+ * Format "CKMODEL1", little-endian; the page's artifact holds the same contents
+ * ("section zero" tables and norms, matrix sections), this is the library's own layout.
+ *   0   8 bytes  "CKMODEL1"
+ *   8   7 x u32  ck_config
+ *   36  u32      one over the square root of the head size, 24 fractional bits
+ *   40  u32      flags: bit 0 = the classifier is the embedding matrix and its row scales
+ *   44  u32      tensor count = 8 + 16 * layers
+ *   48  u64      total artifact length in bytes
+ *   56  u64      reserved (0)
+ *   64  tensor directory: per tensor {u64 offset, u64 length} from the artifact start;
+ *       offsets are multiples of 4; the data of a tensor is contiguous and row-major.
+ * Tensors, in directory order:
+ *   0 embedding       u8  [vocab][dim]       4 classifier scales u32 [vocab] (length 0 if tied)
+ *   1 embedding scales u32 [vocab]           5 rotary  i32 [context][head/2][2] (cos, sin)
+ *   2 final norm      i32 [dim]              6 exponential table u32 [4097]
+ *   3 classifier      u8  [vocab][dim] (length 0 if tied)   7 SiLU table i32 [4097]
+ *   then per layer l, at index 8 + 16 l + j:
+ *   j: 0 attention norm i32[dim]  1 Wq u8[dim][dim]   2 Wq scales u32[dim]
+ *      3 Wk u8[kv_dim][dim] 4 scales   5 Wv u8[kv_dim][dim] 6 scales
+ *      7 Wo u8[dim][dim] 8 scales      9 feed-forward norm i32[dim]
+ *      10 W1 (gate) u8[hidden][dim] 11 scales  12 W3 (up) u8[hidden][dim] 13 scales
+ *      14 W2 (down) u8[dim][hidden] 15 scales
+ *   with kv_dim = dim / heads * kv_heads.  Rotary pair j of a head rotates elements 2j and
+ *   2j+1 of that head by entry [position][j]. */
+
+typedef struct ck_model ck_model;
+
+/* Validates an artifact (host memory) and reports the device bytes ck_load_model needs.
+ * Errors: 2 invalid format, 1 invalid configuration, 10 null pointer. */
+int ck_model_size(const void* artifact, size_t len, size_t* dev_bytes);
+
+/* Copies an artifact into HBM in the library's kernel layout: each matrix row padded to a
+ * multiple of 16 bytes; Wq, Wk, Wv stacked into one matrix; W1 and W3 rows interleaved
+ * (gate row j at 2j, up row j at 2j+1).  dev_mem (256-byte aligned, dev_len >=
+ * ck_model_size bytes) stays owned by the caller and must outlive the model.  The artifact
+ * may be freed when the call returns (it synchronizes `stream`).
+ * Errors: 1, 2, 4 (dev_len too small), 9, 10 (null or misaligned pointer). */
+int ck_load_model(const void* artifact, size_t len, void* dev_mem, size_t dev_len, void* stream,
+                  ck_model** out);
+int ck_model_config(const ck_model* m, ck_config* out);
+/* Frees the host handle and its cached CUDA graphs (not dev_mem). */
+void ck_free_model(ck_model* m);
+
+/* ---------------------------------------------------------------- state ("CKSTATE1")
+ * The page's resumable state ("The resumable state") in ids mode: the run's whole
+ * computation lives in one device buffer, so a state can be copied out and resumed on any
+ * target (the CPU oracle reads the same layout).  Header, 256 bytes:
+ *   0  "CKSTATE1"        8  u32 phase: 3 running, 20 done, 21 failed
+ *   12 u32 position (the next position to run)   16 u32 prompt ids   20 u32 max tokens
+ *   24 u32 cache positions = prompt ids + max tokens - 1          28 u32 generated tokens
+ *   32 u32 flags (bit 0: tokens 1 and 2 complete the run)        36 u32 temperature (0)
+ *   40 u32 error (0 or 8)   44 u32 last generated token (0xFFFFFFFF before the first)
+ *   48 u64 seed   56 u64 turns   64 u64 first error key (all ones if none):
+ *      position << 44 | layer << 32 | phase << 24 | element, phase 6 key store, 7 value
+ *      store, 8 key store after rotary   72 i64 largest logit of the last generating
+ *      position   80 7 x u32 the model's configuration   108..255 zero.
+ * Buffers, each at a multiple of 256 bytes from the state start, in order:
+ *   prompt ids u32[n_prompt], output tokens u32[max_tokens], x (activations) i64[dim],
+ *   four working vectors i64[dim] (xb, q, o, y), h i64[hidden], logits i64[vocab],
+ *   scores i64[heads * cache], keys i32[layers][cache][kv_dim], values likewise.
+ * The working vectors, h and scores are scratch: their contents between turns are
+ * unspecified. */
+#define CK_FLAG_STOP_TOKENS 1u
+#define CK_PHASE_RUNNING 3u
+#define CK_PHASE_DONE 20u
+#define CK_PHASE_FAILED 21u
+
+/* Size in bytes of a state for n_prompt ids and max_tokens.  Errors: 6, 7, 10. */
+int ck_state_size(const ck_model* m, uint32_t n_prompt, uint32_t max_tokens, size_t* out);
+
+/* The page's init_state ("The Rust API") in ids mode: zeroes the state and writes a fresh
+ * header and the prompt ids (host_ids, n_ids entries, the full prompt: no opening token is
+ * added).  dev_state must be 256-byte aligned and exactly ck_state_size bytes.
+ * Errors: 3 misaligned, 4 wrong length, 6, 7, 9, 10. */
+int ck_init_state(const ck_model* m, void* dev_state, size_t len, const uint32_t* host_ids,
+                  uint32_t n_ids, uint32_t max_tokens, uint32_t temperature_q16, uint64_t seed,
+                  uint32_t flags, void* stream);
+
+typedef struct ck_turn_result {
+  uint32_t complete;             /* the run is done or failed */
+  uint32_t generated;            /* tokens generated so far */
+  uint32_t generated_this_turn;
+  uint32_t token;                /* last token sampled this turn, 0xFFFFFFFF if none */
+  uint32_t work;                 /* positions run this turn */
+  uint32_t err_position, err_layer, err_phase, err_element;  /* valid when it returns 8 */
+} ck_turn_result;
+
+/* The page's turn: runs up to n_positions positions (phases 3 to 16 per layer, and 17 to
+ * 19 where a token is generated, "The forward pass, in order").  A turn is the unit of
+ * host synchronisation: the call reads the state header before and after (it
+ * synchronizes `stream`), and all positions in between run as CUDA-graph replays with the
+ * current token kept on the device.  Errors: 3 (state does not belong to the model, is
+ * complete or failed, or is misaligned), 8 (a key or value did not fit 32 bits: the state
+ * is marked failed, err_* name the first failing store), 9, 10. */
+int ck_turn(ck_model* m, void* dev_state, size_t len, uint32_t n_positions, void* stream,
+            ck_turn_result* out);
+
+/* Copies the state's logits (i64[vocab], those of the last generating position) to host
+ * memory; synchronizes `stream`.  Errors: 3, 9, 10. */
+int ck_logits(const ck_model* m, const void* dev_state, size_t len, int64_t* host_out,
+              void* stream);
+
+/* Phase 19 at temperature zero ("Sampling", maximum pass) over the state's logits, run as
+ * a device kernel: the index of the first largest logit.  Synchronizes.  Errors: 3, 9, 10. */
+int ck_argmax(const ck_model* m, const void* dev_state, size_t len, uint32_t* out, void* stream);
+
+/* The page's output_tokens: copies min(generated, cap) token ids to host_out and the count
+ * to *n.  Synchronizes.  Errors: 3, 9, 10. */
+int ck_output_tokens(const ck_model* m, const void* dev_state, size_t len, uint32_t* host_out,
+                     uint32_t cap, uint32_t* n, void* stream);
+
+/* Whole-state copies between device and host (to resume a run on another target).
+ * Synchronize.  Errors: 9, 10. */
+int ck_state_download(const void* dev_state, size_t len, void* host, void* stream);
+int ck_state_upload(void* dev_state, const void* host, size_t len, void* stream);
+
+/* ---------------------------------------------------------------- single matrix row kernel
+ * The page's matrix row ("A matrix row") over a whole matrix on the device:
+ *   sum = x[0] + ... + x[cols-1]; acc_r = sum_c byte[r][c] * x[c] (wrapping in 64 bits);
+ *   y[r] = ((acc_r - 128 * sum) * scale[r]) >> 24, the multiply wrapping in 64 bits and
+ *   the shift arithmetic.
+ * dev_W: rows x pitch bytes, row-major, 16-byte aligned, pitch a multiple of 16 and >= cols
+ * (bytes past cols are ignored); dev_scale u32[rows]; dev_x i64[cols] (8-byte aligned);
+ * dev_y i64[rows].  1 <= cols <= 16384, 1 <= rows <= 2^24.  Errors: 9, 10. */
+int ck_matrow(const uint8_t* dev_W, size_t pitch, const uint32_t* dev_scale, uint32_t rows,
+              uint32_t cols, const int64_t* dev_x, int64_t* dev_y, void* stream);
+
+/* ---------------------------------------------------------------- host-side checks
+ * Host builds of two device routines, for tests without a GPU: floor square root of a u64,
+ * and truncating signed division of n by d (1 <= d < 2^32) through the precomputed
+ * reciprocal the normalization kernels use. */
+uint64_t ck_host_isqrt(uint64_t v);
+int64_t ck_host_div_trunc(int64_t n, uint32_t d);
+
+/* Library version string. */
+const char* ck_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CK_H */

@@ -455,6 +455,11 @@ static int run_position(const orc_model* m, uint8_t* st, const orc_layout* L) {
 
   /* phase 3: the token of this position is a prompt id or the last generated token */
   uint32_t tok = pos < n_prompt ? prompt[pos] : out[pos - n_prompt];
+  if (tok >= m->vocab) { /* a state edited outside init_state and turn */
+    free(g);
+    free(kv);
+    return 3;
+  }
   orc_embed(m->embed + (uint64_t)tok * d, m->embed_scale[tok], d, x);
 
   for (uint32_t l = 0; l < m->layers && !rc; ++l) {
@@ -544,8 +549,10 @@ int orc_turn(const orc_model* m, uint8_t* st, uint64_t len, uint32_t n_positions
   orc_layout L = layout_of(cfg, n_prompt, max_tokens);
   if (len != L.size || rd32(st + H_CACHE) != n_prompt + max_tokens - 1) return 3;
   if (rd32(st + H_PHASE) != PHASE_RUNNING) return 3;
-  if (rd32(st + H_POSITION) >= n_prompt + max_tokens - 1 || rd32(st + H_GENERATED) >= max_tokens)
-    return 3;
+  const uint32_t pos = rd32(st + H_POSITION);
+  if (pos >= n_prompt + max_tokens - 1) return 3;
+  /* tokens generated so far equal the generating positions already run */
+  if (rd32(st + H_GENERATED) != (pos + 1 > n_prompt ? pos + 1 - n_prompt : 0)) return 3;
   int rc = 0;
   uint32_t gen0 = rd32(st + H_GENERATED);
   for (uint32_t i = 0; i < n_positions; ++i) {

@@ -1,0 +1,348 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, element by element,
+bit-exact (integer work, tolerance 0)."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ck():
+    import torch
+    import fixed_point_int8_gb300 as ck
+    from fixed_point_int8_gb300 import build
+    build.build()
+    torch.cuda.init()
+    return ck
+
+
+# ---------------------------------------------------------------- helpers
+
+class Pair:
+    """The same artifact loaded into the oracle and into the GPU library."""
+
+    def __init__(self, ck, spec):
+        self.spec = spec
+        self.art = synth.build_artifact(spec)
+        self.orc = oracle.Model(self.art)
+        rc, self.gpu = ck.Model.load(self.art)
+        assert rc == 0, rc
+
+    def init(self, ck, ids, max_tokens, flags=0):
+        rc, so = self.orc.init_state(ids, max_tokens, flags=flags)
+        assert rc == 0
+        sg = self.gpu.new_state(len(ids), max_tokens)
+        assert self.gpu.init_state(sg, ids, max_tokens, flags=flags) == 0
+        return so, sg
+
+
+def compare_states(orc_model, so, sg_host, n_prompt, max_tokens, what="", turns=True):
+    """Every specified field and buffer of two states (the working vectors are scratch).
+    turns=False skips the turn counter, for runs split into different numbers of turns."""
+    lay = orc_model.layout(n_prompt, max_tokens)
+    assert so.size == sg_host.size == lay["size"]
+    ho, hg = oracle.header(so), oracle.header(sg_host)
+    if not turns:
+        ho.pop("turns"), hg.pop("turns")
+    assert ho == hg, (what, ho, hg)
+    assert np.array_equal(so[:8], sg_host[:8])
+    assert np.array_equal(so[80:108], sg_host[80:108]), what
+    d, v = orc_model.config[0], orc_model.config[5]
+    for name, nbytes in (("prompt", 4 * n_prompt), ("out", 4 * max_tokens), ("x", 8 * d),
+                         ("logits", 8 * v)):
+        o = lay[name]
+        a, b = so[o:o + nbytes], sg_host[o:o + nbytes]
+        if not np.array_equal(a, b):
+            bad = np.flatnonzero(a != b)
+            raise AssertionError(f"{what}: buffer {name} differs at byte {bad[:8]}")
+    for name in ("k", "v"):
+        o, end = lay[name], (lay["v"] if name == "k" else lay["size"])
+        a, b = so[o:end], sg_host[o:end]
+        if not np.array_equal(a, b):
+            bad = np.flatnonzero(a != b)
+            raise AssertionError(f"{what}: cache {name} differs at byte offset {bad[:8]}")
+
+
+# ---------------------------------------------------------------- matrix row
+
+MATROW_CASES = [(1, 1, 16), (3, 15, 16), (5, 17, 32), (7, 172, 176), (64, 64, 64), (130, 300, 304),
+                (1001, 1000, 1008), (257, 4096, 4096), (64, 11008, 11008), (33, 16384, 16384)]
+
+
+def _x_for_limbs(L, cols, seed):
+    rng = np.random.default_rng(seed)
+    if L == 8:
+        x = rng.integers(-2**63, 2**63 - 1, cols, dtype=np.int64)
+        x[:4] = [-2**63, 2**63 - 1, -1, 0][: min(4, cols)]
+        return x
+    lim = 2**(8 * L - 1)
+    x = rng.integers(-lim, lim, cols, dtype=np.int64)     # [-lim, lim - 1]: exactly L limbs
+    x[0] = -lim
+    if cols > 1:
+        x[1] = lim - 1
+    return x
+
+
+@pytest.mark.parametrize("rows,cols,pitch", MATROW_CASES)
+def test_matrow_every_limb_count(ck, rows, cols, pitch):
+    import torch
+    W, s, _ = synth.matrow_case(rows, cols, pitch=pitch)
+    W[0, :cols] = 255
+    if rows > 1:
+        W[1, :cols] = 0
+    Wd = torch.from_numpy(W).cuda()
+    sd = torch.from_numpy(s.view(np.int32)).cuda()
+    for L in range(1, 9):
+        x = _x_for_limbs(L, cols, seed=rows * 31 + L)
+        want = oracle.matrow(W, s, x, cols=cols)
+        rc, y = ck.matrow(Wd, sd, torch.from_numpy(x).cuda(), cols=cols)
+        assert rc == 0
+        got = y.cpu().numpy()
+        assert np.array_equal(got, want), (rows, cols, L, np.flatnonzero(got != want)[:5])
+
+
+def test_matrow_zero_vector_and_extreme_scales(ck):
+    import torch
+    W, s, x = synth.matrow_case(40, 48)
+    s[:4] = [0, 1, 2**32 - 1, 2**31]
+    for vec in (np.zeros(48, np.int64), x):
+        want = oracle.matrow(W, s, vec)
+        rc, y = ck.matrow(torch.from_numpy(W).cuda(), torch.from_numpy(s.view(np.int32)).cuda(),
+                          torch.from_numpy(vec).cuda())
+        assert rc == 0 and np.array_equal(y.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("rows,cols", synth.MATROW_SHAPES)
+def test_matrow_sweep_full_size(ck, rows, cols):
+    """The matrix-row sweep at its full sizes, every output row against the oracle."""
+    import torch
+    W, s, x = synth.matrow_case(rows, cols)
+    want = oracle.matrow(W, s, x)
+    rc, y = ck.matrow(torch.from_numpy(W).cuda(), torch.from_numpy(s.view(np.int32)).cuda(),
+                      torch.from_numpy(x).cuda())
+    assert rc == 0
+    assert np.array_equal(y.cpu().numpy(), want)
+
+
+def test_matrow_rejects_bad_arguments(ck):
+    import torch
+    W = torch.zeros((4, 32), dtype=torch.uint8, device="cuda")
+    s = torch.zeros(4, dtype=torch.int32, device="cuda")
+    x = torch.zeros(32, dtype=torch.int64, device="cuda")
+    assert ck.matrow(W, s, x, cols=33)[0] == 10                    # cols beyond the pitch
+    W2 = torch.zeros((4, 24), dtype=torch.uint8, device="cuda")
+    assert ck.matrow(W2, s, x, cols=24)[0] == 10                   # pitch not a multiple of 16
+    assert ck.matrow(W[:, 1:17], s, x, cols=16)[0] == 10           # misaligned matrix
+
+
+# ---------------------------------------------------------------- whole model
+
+MODELS = {
+    "tiny_ws": synth.WORKLOADS["tiny_ws"],
+    "gqa": synth.WORKLOADS["gqa"],
+    "gqa_tied": synth.WORKLOADS["gqa_tied"],
+}
+
+
+@pytest.fixture(scope="module")
+def pairs(ck):
+    return {name: Pair(ck, wl.spec) for name, wl in MODELS.items()}
+
+
+@pytest.mark.parametrize("name", list(MODELS))
+def test_every_position_matches_the_oracle(ck, pairs, name):
+    wl = MODELS[name]
+    P = pairs[name]
+    ids = synth.prompt_ids(wl.spec, wl.n_prompt)
+    so, sg = P.init(ck, ids, wl.steps)
+    compare_states(P.orc, so, ck.state_download(sg), wl.n_prompt, wl.steps, "after init")
+    for pos in range(wl.n_prompt + wl.steps - 1):
+        rco, reso = P.orc.turn(so, 1)
+        rcg, resg = P.gpu.turn(sg, 1)
+        assert rco == rcg == 0
+        assert reso == resg, (pos, reso, resg)
+        compare_states(P.orc, so, ck.state_download(sg), wl.n_prompt, wl.steps, f"position {pos}")
+    assert oracle.header(so)["phase"] == oracle.PHASE_DONE
+    rc, toks = P.gpu.output_tokens(sg)
+    assert rc == 0 and len(toks) == wl.steps
+
+
+def test_many_positions_in_one_turn(ck, pairs):
+    wl = MODELS["gqa"]
+    P = pairs["gqa"]
+    ids = synth.prompt_ids(wl.spec, wl.n_prompt)
+    so, sg = P.init(ck, ids, wl.steps)
+    rco, reso = P.orc.turn(so, 10_000)
+    splits = [1, 7, 3, 30, 10_000]
+    for n in splits:
+        rc, res = P.gpu.turn(sg, n)
+        assert rc == 0
+        if res["complete"]:
+            break
+    host = ck.state_download(sg)
+    # the turn counter differs (one turn against several); everything else is identical
+    compare_states(P.orc, so, host, wl.n_prompt, wl.steps, "split turns", turns=False)
+    assert P.gpu.turn(sg, 1)[0] == 3                               # complete: InvalidState
+
+
+def test_literal_tiny_workload_fails_like_the_oracle(ck):
+    wl = synth.WORKLOADS["tiny"]
+    P = Pair(ck, wl.spec)
+    ids = synth.prompt_ids(wl.spec, wl.n_prompt)
+    so, sg = P.init(ck, ids, wl.steps)
+    rco, reso = P.orc.turn(so, 100)
+    rcg, resg = P.gpu.turn(sg, 100)
+    assert rco == rcg == 8
+    assert reso == resg
+    ho, hg = oracle.header(so), oracle.header(ck.state_download(sg))
+    for k in ("phase", "error", "err_key", "position", "generated"):
+        assert ho[k] == hg[k], k
+    assert P.gpu.turn(sg, 1)[0] == 3
+
+
+def test_stop_tokens(ck, pairs):
+    wl = MODELS["tiny_ws"]
+    P = pairs["tiny_ws"]
+    ids = synth.prompt_ids(wl.spec, wl.n_prompt)
+    so, sg = P.init(ck, ids, wl.steps, flags=ck.CK_FLAG_STOP_TOKENS)
+    rco, reso = P.orc.turn(so, 1000)
+    rcg, resg = P.gpu.turn(sg, 1000)
+    assert rco == rcg == 0 and reso == resg and resg["complete"]
+    assert resg["generated"] < wl.steps                  # this seed emits a stop token early
+    compare_states(P.orc, so, ck.state_download(sg), wl.n_prompt, wl.steps, "stop tokens")
+
+
+def test_init_state_errors_match_the_oracle(ck, pairs):
+    P = pairs["tiny_ws"]
+    spec = P.spec
+    ids = synth.prompt_ids(spec, 4)
+    ctx = spec.context
+    import torch
+    big = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    cases = [(ids, 0, 0), (ids, ctx + 1, 0), (np.array([spec.vocab], np.uint32), 2, 0),
+             (ids, 2, 16 * 2**16 + 1), (ids, ctx - 2, 0)]
+    for i, mt, temp in cases:
+        rco = P.orc.init_state(i, mt, temperature_q16=temp)[0]
+        rcg = P.gpu.init_state(big, i, mt, temperature_q16=temp)
+        assert rco == rcg != 0, (mt, temp, rco, rcg)
+    rc, n = P.gpu.state_size(4, 5)
+    assert rc == 0
+    assert P.gpu.init_state(big, ids, 5, length=n + 8) == 4
+    assert P.gpu.init_state(big[8:], ids, 5, length=n) == 3          # misaligned
+
+
+def test_turn_rejects_foreign_states(ck, pairs):
+    P = pairs["tiny_ws"]
+    ids = synth.prompt_ids(P.spec, 4)
+    sg = P.gpu.new_state(4, 5)
+    assert P.gpu.init_state(sg, ids, 5) == 0
+    host = ck.state_download(sg)
+    for off, val in ((0, ord("X")), (80, 99), (12, 8)):
+        bad = host.copy()
+        bad[off] = val
+        ck.state_upload(sg, bad)
+        assert P.gpu.turn(sg, 1)[0] == 3
+    other = pairs["gqa"]
+    ck.state_upload(sg, host)
+    assert other.gpu.turn(sg, 1)[0] == 3                            # another model's state
+
+
+def test_cross_target_resume(ck, pairs):
+    """A run continues on either target from the other's state ("The resumable state")."""
+    wl = MODELS["gqa"]
+    P = pairs["gqa"]
+    ids = synth.prompt_ids(wl.spec, wl.n_prompt)
+    ref, _ = P.init(ck, ids, wl.steps)
+    P.orc.turn(ref, 10_000)
+    # GPU first, oracle finishes
+    so, sg = P.init(ck, ids, wl.steps)
+    P.gpu.turn(sg, 20)
+    host = ck.state_download(sg)
+    P.orc.turn(host, 10_000)
+    compare_states(P.orc, ref, host, wl.n_prompt, wl.steps, "gpu then oracle", turns=False)
+    # oracle first, GPU finishes
+    P.orc.turn(so, 25)
+    ck.state_upload(sg, so)
+    rc, res = P.gpu.turn(sg, 10_000)
+    assert rc == 0 and res["complete"]
+    compare_states(P.orc, ref, ck.state_download(sg), wl.n_prompt, wl.steps, "oracle then gpu",
+                   turns=False)
+
+
+def test_argmax_kernel_first_of_ties(ck, pairs):
+    P = pairs["tiny_ws"]
+    spec = P.spec
+    ids = synth.prompt_ids(spec, 3)
+    sg = P.gpu.new_state(3, 4)
+    assert P.gpu.init_state(sg, ids, 4) == 0
+    host = ck.state_download(sg)
+    lay = P.orc.layout(3, 4)
+    rng = np.random.default_rng(3)
+    for case in range(6):
+        logits = rng.integers(-5, 5, spec.vocab).astype(np.int64)
+        if case == 0:
+            logits[:] = -7                                   # all equal: index 0
+        elif case == 1:
+            logits[[17, 300, 511]] = 2**62                   # ties at the top
+        elif case == 2:
+            logits[-1] = 2**63 - 1
+        host[lay["logits"]:lay["logits"] + 8 * spec.vocab] = logits.view(np.uint8)
+        ck.state_upload(sg, host)
+        rc, idx = P.gpu.argmax(sg)
+        assert rc == 0 and idx == oracle.argmax(logits) == int(np.argmax(logits))
+        rc, lg = P.gpu.logits(sg)
+        assert rc == 0 and np.array_equal(lg, logits)
+
+
+def test_model_artifact_errors(ck):
+    art = synth.build_artifact(synth.TINY_WS)
+    bad = art.copy()
+    bad[0] = ord("X")
+    assert ck.Model.load(bad)[0] == 2
+    assert ck.Model.load(art[:-64].copy())[0] == 2
+    bad = art.copy()
+    bad[8:12] = 0
+    assert ck.Model.load(bad)[0] == 1
+
+
+# ---------------------------------------------------------------- full-size sampled positions
+
+def _resume_one(ck, spec, n_prompt, max_tokens, gpu_positions, check_positions):
+    """GPU runs `gpu_positions`, then the oracle and the GPU each run `check_positions` more
+    from that same state; every buffer of the two results must be identical."""
+    P = Pair(ck, spec)
+    ids = synth.prompt_ids(spec, n_prompt)
+    sg = P.gpu.new_state(n_prompt, max_tokens)
+    assert P.gpu.init_state(sg, ids, max_tokens) == 0
+    if gpu_positions:
+        rc, _ = P.gpu.turn(sg, gpu_positions)
+        assert rc == 0
+    host = ck.state_download(sg)
+    rco, reso = P.orc.turn(host, check_positions)
+    rcg, resg = P.gpu.turn(sg, check_positions)
+    assert rco == rcg == 0 and reso["work"] == resg["work"] == check_positions
+    got = ck.state_download(sg)
+    compare_states(P.orc, host, got, n_prompt, max_tokens, f"{spec.name} sampled", turns=False)
+    return oracle.header(got)
+
+
+def test_llama7b_shape_sampled_positions(ck):
+    """7B-shaped model at full size: two prompt positions on the GPU, then the first
+    generating position (classifier and maximum pass included) on both targets."""
+    h = _resume_one(ck, synth.LLAMA7B, n_prompt=3, max_tokens=4, gpu_positions=2, check_positions=1)
+    assert h["generated"] == 1
+
+
+def test_1b_long_context_sampled_position(ck):
+    """1B-shaped model at 8192 context: 7936 prompt ids prefilled on the GPU position by
+    position, then one generating position with attention over 7936 cached positions
+    checked against the oracle."""
+    wl = synth.WORKLOADS["1b_long"]
+    h = _resume_one(ck, wl.spec, n_prompt=wl.n_prompt, max_tokens=wl.steps,
+                    gpu_positions=wl.n_prompt - 1, check_positions=1)
+    assert h["generated"] == 1 and h["position"] == wl.n_prompt

@@ -1,0 +1,84 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every function include/ck.h
+declares; host builds of its integer routines match their definitions.  No GPU needed."""
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ck.h")
+
+
+@pytest.fixture(scope="module")
+def ck():
+    import fixed_point_int8_gb300 as ck
+    from fixed_point_int8_gb300 import build
+    build.build()
+    return ck
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ck_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("ck_load_model", "ck_init_state", "ck_turn", "ck_logits", "ck_argmax", "ck_matrow"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(ck):
+    lib = ctypes.CDLL(ck.build.LIB)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert "sm_103a" in ck.version()
+
+
+def test_library_is_built_for_sm_103a(ck):
+    # the fatbin inside the shared object names the target architecture
+    blob = open(ck.build.LIB, "rb").read()
+    assert b"sm_103a" in blob
+
+
+def test_host_isqrt(ck):
+    rng = np.random.default_rng(21)
+    vals = [0, 1, 2, 3, 42950, 42951, 2**32, 2**32 + 42950, 2**63, 2**64 - 1]
+    for k in list(rng.integers(1, 2**32 - 1, 2000, dtype=np.uint64)) + [2**32 - 1, 2**31]:
+        k = int(k)
+        vals += [k * k - 1, k * k, k * k + 1]
+    vals += [int(v) for v in rng.integers(0, 2**63, 2000, dtype=np.uint64)]
+    for v in vals:
+        assert ck.host_isqrt(v) == math.isqrt(v), v
+
+
+def _trunc_div(n, d):
+    q = abs(n) // d
+    return q if n >= 0 else -q
+
+
+def test_host_division_by_invariant_divisor(ck):
+    rng = np.random.default_rng(22)
+    divisors = [1, 2, 3, 5, 7, 207, 208, 255, 256, 257, 65535, 65536, 65537, 2**31 - 1, 2**31,
+                2**32 - 1] + [int(v) for v in rng.integers(1, 2**32, 300, dtype=np.uint64)]
+    numerators = [0, 1, -1, 2**63 - 1, -2**63, -2**63 + 1, 2**62, -(256 * 207 + 1)]
+    numerators += [int(v) for v in rng.integers(-2**63, 2**63 - 1, 200, dtype=np.int64)]
+    numerators += [int(v) for v in rng.integers(-2**40, 2**40, 200, dtype=np.int64)]
+    for d in divisors:
+        for n in numerators + [d * 12345 - 1, -d * 12345 + 1, d, -d, d - 1, -(d - 1)]:
+            n = max(min(n, 2**63 - 1), -2**63)
+            assert ck.host_div_trunc(n, d) == _trunc_div(n, d), (n, d)
+
+
+def test_library_fails_loudly_without_a_gpu(ck):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # the product path has no CPU fallback: a model cannot be loaded without a device
+    import synth
+    with pytest.raises(Exception):
+        ck.Model.load(synth.build_artifact(synth.TINY_WS))
