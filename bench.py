@@ -1,0 +1,440 @@
+"""Decode benchmark of the fixed-point forward pass on GB300.
+
+Workload: the 7B-shaped fixed-point model (dim 4096, 32 layers, 32 heads x 128, FFN hidden
+11008, vocab 32000, context 2048, ~6.6 GB of int8 weights), seeded synthetic weights, a
+single run: 128 prompt ids prefilled position by position, then greedy decode.  A step is
+one generating position: phases 3 to 19 over all 32 layers and the classifier.
+
+Prints one JSON line:
+  value      decode tokens/s, device-timed (CUDA events on the launching stream) over
+             exactly --steps positions after --warmup untimed ones, max over ranks;
+  e2e        the same metric through the public call a streaming user makes: one
+             ck_turn per token with the token read back on the host every step;
+  roofline   the matrix-row kernel at the decode's largest launch shape (gate and up rows
+             of one layer, 22016 x 4096), timed live with CUDA events, against the measured
+             HBM copy bandwidth;
+  cpu_baseline  the CPU oracle on a bounded sample of the same decode (it continues from
+             the GPU's state after the prefill), whose tokens must equal the GPU's;
+  matrow_sweep  GB/s of the matrix-row kernel on the four sweep shapes.
+``--impl reference`` times the CPU oracle alone on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "decode tokens/s bit-exact vs oracle; matrow HBM GB/s as % of GB300 peak"
+WORKLOAD = ("llama7b_shape fixed-point decode: dim 4096, 32 layers, 32 heads x 128, FFN hidden 11008, "
+            "vocab 32000, context 2048, u8 weights + u32 row scales (6.61 GB/token); 128 prompt ids "
+            "prefilled position by position, then greedy decode; single run per GPU")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def matrow_bytes(rows: int, cols: int) -> int:
+    """Algorithmic bytes of one matrix-row launch: each weight byte, each row scale and
+    output, and the input vector read once."""
+    return rows * cols + 4 * rows + 8 * rows + 8 * cols
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("ck_matrow.cu", "ck_internal.cuh"):
+        with open(os.path.join(ROOT, "fixed_point_int8_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(shape_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
+    kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "matrow_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("kernel_source_hash") == kernel_source_hash() and shape_key in d.get("launches", {}):
+            return int(d["launches"][shape_key]["dram_bytes"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.seek(0)
+        sm, smax, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.file:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    import fixed_point_int8_gb300 as ck
+    from fixed_point_int8_gb300 import build as libbuild
+    import synth
+
+    rank, world, local = dist_setup(args.gpus)
+    libbuild.build()
+    if args.matrow_only:
+        # profiling aid: only the matrix-row timing of one shape, e.g. 22016x4096
+        rows, cols = (int(v) for v in args.matrow_only.split("x"))
+        avg, nb = time_matrow(ck, torch, rows, cols, 5)
+        print(json.dumps({"matrow": args.matrow_only, "us": round(avg * 1e3, 2),
+                          "GB/s": round(nb / (avg * 1e-3) / 1e9, 1)}), flush=True)
+        return
+    spec = synth.LLAMA7B
+    n_prompt = args.prompt_ids
+    K, W = args.steps, args.warmup
+    e2e_steps = min(K, args.e2e_steps)
+    max_tokens = 1 + W + K + e2e_steps
+    assert n_prompt + max_tokens - 1 <= spec.context, "too many steps for the context"
+
+    t0 = time.time()
+    art = synth.build_artifact(spec)
+    ids = synth.prompt_ids(spec, n_prompt, run=rank)
+    rc, model = ck.Model.load(art)
+    assert rc == 0, f"ck_load_model failed: {rc}"
+    state = model.new_state(n_prompt, max_tokens)
+    assert model.init_state(state, ids, max_tokens) == 0
+    stream = torch.cuda.current_stream()
+    setup_s = time.time() - t0
+
+    # prefill: prompt positions 0..126 and position 127, which generates the first token
+    rc, res = model.turn(state, n_prompt)
+    assert rc == 0 and res["generated"] == 1, (rc, res)
+    snapshot = ck.state_download(state) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+
+    # warm-up steps (untimed)
+    rc, res = model.turn(state, W)
+    assert rc == 0 and res["work"] == W
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    with sampler:
+        time.sleep(0.3)
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        rc, res = model.turn(state, K)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        assert rc == 0 and res["work"] == K, (rc, res)
+        dev_ms = ev0.elapsed_time(ev1)
+
+        # e2e: one public ck_turn call per token, its token read back on the host each step
+        torch.cuda.synchronize()
+        e2e_tokens = []
+        t_e = time.perf_counter()
+        for _ in range(e2e_steps):
+            rc, r = model.turn(state, 1)
+            e2e_tokens.append(r["token"])
+        e2e_s = time.perf_counter() - t_e
+        assert rc == 0
+    clocks = sampler.summary()
+
+    ms_max = max_over_ranks(dev_ms, world)
+    value = K * world / (ms_max / 1e3)
+    e2e_max = max_over_ranks(e2e_s, world)
+    e2e_value = e2e_steps * world / e2e_max if e2e_steps else None
+
+    rc, toks = model.output_tokens(state)
+    assert rc == 0
+
+    roof, sweep = matrow_measurements(ck, torch, args)
+
+    cpu = None
+    bitexact = None
+    if snapshot is not None:
+        cpu, bitexact = cpu_baseline(art, snapshot, toks, args.cpu_seconds)
+
+    if rank != 0:
+        return
+    launches_per_step = 1 + 5 * spec.layers + 2
+    weight_bytes = spec.weight_bytes_per_token()
+    hbm, peak_kind = load_peaks()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(ms_max / K, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u8 x i64 (int64 activations, 16 fractional bits)",
+        "data": "synthetic (seeded weights and prompt ids, no checkpoint)",
+        "config": {"workload": WORKLOAD, "prompt_ids": n_prompt, "decode_positions_timed": K,
+                   "l2": "inputs larger than L2: 6.6 GB of weights streamed per step",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "weight_roofline": {"bytes_per_token": weight_bytes,
+                            "tokens_per_s_at_peak": round(hbm * 1e9 / weight_bytes, 1),
+                            "frac": round(value / world / (hbm * 1e9 / weight_bytes), 4),
+                            "peak_gbs": hbm, "peak_kind": peak_kind},
+        "e2e": {"value": round(e2e_value, 2) if e2e_value else None, "unit": "tokens/s",
+                "h2d_bytes_per_step": 8, "d2h_bytes_per_step": 512,
+                "how": "ck_turn(1 position) per token; the call reads the 256-byte state header "
+                       "before and after and writes the 8-byte turn counter"},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "bitexact": bitexact,
+        "matrow_sweep": sweep,
+        "setup_s": round(setup_s, 1),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def time_matrow(ck, torch, rows, cols, iters):
+    """Average duration (ms) of ck_matrow launches of one shape, timed one by one with CUDA
+    events on the current stream; the matrix rotates through copies totalling three times
+    the L2 size so every launch streams from HBM.  Returns (ms, algorithmic bytes)."""
+    import synth
+    stream = torch.cuda.current_stream()
+    l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 128 << 20)
+    W, s, x = synth.matrow_case(rows, cols)
+    nbytes = rows * cols
+    copies = max(2, -(-3 * l2 // nbytes))
+    Wd = torch.from_numpy(W).cuda()
+    Ws = [Wd] + [Wd.clone() for _ in range(copies - 1)]
+    sd = torch.from_numpy(s.view(np.int32)).cuda()
+    xd = torch.from_numpy(x).cuda()
+    y = torch.empty(rows, dtype=torch.int64, device="cuda")
+    for i in range(3):
+        rc, _ = ck.matrow(Ws[i % copies], sd, xd, out=y)
+        assert rc == 0
+    times = []
+    for i in range(iters):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        ck.matrow(Ws[i % copies], sd, xd, out=y)
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in times]
+    del Ws, Wd
+    torch.cuda.empty_cache()
+    return sum(ms) / len(ms), matrow_bytes(rows, cols)
+
+
+def matrow_measurements(ck, torch, args):
+    """Times ck_matrow launches with CUDA events on the current stream; matrices rotate
+    through copies whose total exceeds the L2 cache so every launch streams from HBM."""
+    import synth
+    hbm, peak_kind = load_peaks()
+    time_shape = lambda rows, cols, iters: time_matrow(ck, torch, rows, cols, iters)
+    sweep = {}
+    for rows, cols in synth.MATROW_SHAPES:
+        avg, nb = time_shape(rows, cols, 30)
+        gbs = nb / (avg * 1e-3) / 1e9
+        sweep[f"{rows}x{cols}"] = {"us": round(avg * 1e3, 2), "GB/s": round(gbs, 1),
+                                   "frac_of_peak": round(gbs / hbm, 4)}
+    rows, cols = 2 * 11008, 4096
+    avg, nb = time_shape(rows, cols, 30)
+    achieved = nb / (avg * 1e-3) / 1e9
+    key = f"{rows}x{cols}"
+    traffic = ncu_traffic(key)
+    roof = {"kernel": "k_matrow", "launch": f"{key} (gate and up rows of one 7B layer)",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
+            "traffic": traffic, "algorithmic_bytes": nb, "avg_launch_us": round(avg * 1e3, 2)}
+    return roof, sweep
+
+
+def cpu_baseline(art, snapshot, gpu_tokens, budget_s):
+    """The oracle, as it stands, continues the decode from the GPU's state after the prefill
+    for as many positions as fit in about budget_s seconds; its tokens must equal the GPU's."""
+    import oracle
+    m = oracle.Model(art)
+    st = snapshot.copy()
+    start = oracle.header(st)["generated"]
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        rc, res = m.turn(st, 1)
+        assert rc == 0
+        n += 1
+        el = time.perf_counter() - t0
+        if el > budget_s or n >= 64:
+            break
+    lay = m.layout(oracle.header(st)["n_prompt"], oracle.header(st)["max_tokens"])
+    otoks = st[lay["out"]:lay["out"] + 4 * (start + n)].view("<u4").tolist()
+    same = otoks == gpu_tokens[:start + n]
+    cpu = {"value": round(n / el, 4), "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
+           "sample": f"{n} decode positions of the same 7B-shaped run, continued on the CPU from the "
+                     f"GPU's state after the 128-id prefill (OpenMP over independent matrix rows)"}
+    return cpu, {"checked_tokens": start + n, "equal": bool(same)}
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The CPU oracle as the reference implementation of the same decode: on rank 0 only,
+    it prefills a one-id prompt and times --steps generating positions after --warmup."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    spec = synth.LLAMA7B
+    art = synth.build_artifact(spec)
+    m = oracle.Model(art)
+    K, W = args.steps, args.warmup
+    n_prompt = 1
+    rc, st = m.init_state(synth.prompt_ids(spec, n_prompt), W + K)
+    assert rc == 0
+    rc, _ = m.turn(st, W)
+    assert rc == 0
+    t0 = time.perf_counter()
+    done = 0
+    for _ in range(K):
+        rc, _ = m.turn(st, 1)
+        assert rc == 0
+        done += 1
+        if time.perf_counter() - t0 > args.reference_seconds:
+            break
+    el = time.perf_counter() - t0
+    value = done / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": done, "steps_requested": K,
+        "warmup": W, "ms_per_step": round(el / max(done, 1) * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8 x i64 (int64 activations)",
+        "data": "synthetic (seeded weights and prompt ids, no checkpoint)",
+        "config": {"workload": WORKLOAD.replace("128 prompt ids", "1 prompt id"), "parallelism": "CPU oracle"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
+                         "sample": f"{done} generating positions timed after {W} warm-up positions"},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=253)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=64)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--reference-seconds", type=float, default=150.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prompt-ids", type=int, default=128,
+                    help="prompt length (the workload uses 128; shorter only for profiling)")
+    ap.add_argument("--matrow-only", default="",
+                    help="profiling aid: time ck_matrow on one ROWSxCOLS shape and exit")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -79,6 +79,7 @@ def _lib_():
             "orc_state_layout": ([vp, u32, u32, vp], None),
             "orc_events_reset": ([ctypes.c_int], None),
             "orc_events_get": ([vp], None),
+            "orc_threads": ([], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -165,6 +166,11 @@ def argmax(logits: np.ndarray) -> int:
 def page_state_size(config, prompt_bytes: int, max_tokens: int) -> int:
     cfg = np.array(config, dtype=np.uint32)
     return int(_lib_().orc_page_state_size(cfg.ctypes.data, prompt_bytes, max_tokens))
+
+
+def threads() -> int:
+    """OpenMP threads the oracle's row loops use."""
+    return int(_lib_().orc_threads())
 
 
 def events_reset(enable: bool = True) -> None:
