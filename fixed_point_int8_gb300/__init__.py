@@ -16,6 +16,7 @@ import numpy as np
 from . import build as _build
 
 CK_FLAG_STOP_TOKENS = 1
+PATH_AUTO, PATH_STEP, PATH_KERNELS = 0, 1, 2
 PHASE_RUNNING, PHASE_DONE, PHASE_FAILED = 3, 20, 21
 ERROR_NAMES = {1: "InvalidConfig", 2: "InvalidFormat", 3: "InvalidState", 4: "BufferTooSmall",
                5: "MissingWeights", 6: "InvalidPrompt", 7: "ContextExceeded", 8: "Arithmetic",
@@ -56,6 +57,8 @@ def lib() -> ctypes.CDLL:
             "ck_model_size": ([vp, sz, ctypes.POINTER(sz)], ctypes.c_int),
             "ck_load_model": ([vp, sz, vp, sz, vp, ctypes.POINTER(vp)], ctypes.c_int),
             "ck_model_config": ([vp, ctypes.POINTER(Config)], ctypes.c_int),
+            "ck_set_path": ([vp, ctypes.c_int], ctypes.c_int),
+            "ck_set_step_slots": ([vp, ctypes.c_uint32], ctypes.c_int),
             "ck_free_model": ([vp], None),
             "ck_state_size": ([vp, u32, u32, ctypes.POINTER(sz)], ctypes.c_int),
             "ck_init_state": ([vp, vp, sz, vp, u32, u32, u32, u64, u32, vp], ctypes.c_int),
@@ -135,6 +138,14 @@ class Model:
             self.close()
         except Exception:
             pass
+
+    def set_path(self, path: int) -> int:
+        """PATH_AUTO, PATH_STEP (one persistent kernel per position) or PATH_KERNELS."""
+        return lib().ck_set_path(self._h, path)
+
+    def set_step_slots(self, max_slots: int) -> int:
+        """Cap on the persistent kernel's ring slots (0: as many as fit)."""
+        return lib().ck_set_step_slots(self._h, max_slots)
 
     def state_size(self, n_prompt: int, max_tokens: int) -> tuple[int, int]:
         out = ctypes.c_size_t()

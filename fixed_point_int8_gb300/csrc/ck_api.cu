@@ -26,12 +26,18 @@ struct ck_model {
   const uint32_t* exp_tab;
   const int32_t* silu_tab;
   uint32_t* scratch;  // small device scratch inside dev (ck_argmax result)
+  DevLayer* dev_layers;  // the layer table in device memory (read by the one-position kernel)
+  int path;              // CK_PATH_*
+  uint32_t max_slots;    // cap on the one-position kernel's ring slots (0: as many as fit)
+  int smem_optin;        // largest shared memory a block may opt into
+  size_t step_smem;      // dynamic shared memory available to the one-position kernel
   std::vector<DevLayer> layers;
   cudaStream_t capture;
   struct Graph {
     void* state;
     size_t len;
     bool generating;
+    int path;
     cudaGraphExec_t exec;
   };
   std::vector<Graph> graphs;
@@ -95,7 +101,7 @@ int parse_artifact(const void* artifact, size_t len, Parsed* out) {
 
 // Offsets of the device model layout.
 struct DevPlan {
-  uint64_t embed, embed_scale, cls, cls_scale, final_norm, rope, exp_tab, silu_tab, scratch;
+  uint64_t embed, embed_scale, cls, cls_scale, final_norm, rope, exp_tab, silu_tab, scratch, table;
   struct L { uint64_t wqkv, sqkv, wo, so, w13, s13, w2, s2, an, fn; };
   std::vector<L> layers;
   uint64_t total;
@@ -130,6 +136,7 @@ DevPlan plan_device(const ck_config& c, bool tied) {
     L.fn = take(4ull * c.dim);
   }
   P.scratch = take(256);
+  P.table = take(sizeof(DevLayer) * (uint64_t)c.layers);
   P.total = off;
   return P;
 }
@@ -449,10 +456,72 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
   return CK_OK;
 }
 
+// Launch plan of the one-position kernel for a state, or false when the model or state is
+// outside what it supports (then the phase-by-phase kernels run instead).
+bool plan_step(const ck_model* m, const StateLayout& lay, StepParams* sp, int* grid, size_t* smem) {
+  const ck_config& c = m->cfg;
+  if (m->pitch_d > kStageBytes / 2 || m->pitch_h > kStageBytes || c.heads > 1000) return false;
+  const int G = m->num_sms < 768 ? m->num_sms : 768;
+  const uint32_t gh = c.heads >= (uint32_t)G ? 1u : (uint32_t)G / c.heads;
+  if (c.heads * gh > (uint32_t)G) return false;
+  const uint32_t chunk = (lay.cache + gh - 1) / gh;
+  const uint64_t attn = 8ull * ((uint64_t)m->head_dim * (1 + step_consumer_warps()) +
+                                step_consumer_warps() + chunk);
+  const uint64_t planes = 8ull * (m->pitch_d > m->pitch_h ? m->pitch_d : m->pitch_h);
+  const uint64_t xb = (std::max(attn, planes) + 15) & ~15ull;
+  const uint64_t avail = (uint64_t)m->step_smem;
+  if (avail < xb + 2 * (kStageBytes + 16)) return false;
+  uint64_t ns = (avail - xb) / (kStageBytes + 16);
+  if (ns > 8) ns = 8;
+  if (m->max_slots && ns > m->max_slots) ns = m->max_slots;
+  if (ns < 2) return false;
+  StepParams& p = *sp;
+  p = StepParams{};
+  p.off_prompt = lay.prompt; p.off_out = lay.out; p.off_x = lay.x; p.off_xb = lay.xb; p.off_q = lay.q;
+  p.off_o = lay.o; p.off_y = lay.y; p.off_h = lay.h; p.off_logits = lay.logits;
+  p.off_work = lay.scores; p.off_k = lay.k; p.off_v = lay.v;
+  p.cache = lay.cache;
+  p.dim = c.dim; p.hidden = c.hidden; p.layers = c.layers; p.heads = c.heads; p.kv_heads = c.kv_heads;
+  p.vocab = c.vocab; p.hd = m->head_dim; p.kv_dim = m->kv_dim; p.pitch_d = m->pitch_d;
+  p.pitch_h = m->pitch_h; p.inv_sqrt = m->inv_sqrt;
+  p.gh = gh; p.ns = (uint32_t)ns; p.x_bytes = (uint32_t)xb;
+  p.layers_tab = m->dev_layers;
+  p.embed = m->embed; p.embed_scale = m->embed_scale; p.cls = m->cls; p.cls_scale = m->cls_scale;
+  p.final_norm = m->final_norm; p.rope = m->rope; p.exp_tab = m->exp_tab; p.silu_tab = m->silu_tab;
+  *grid = G;
+  *smem = xb + ns * kStageBytes + 16 * ns;
+  return step_blocks_per_sm(*smem) >= 1;  // every block must be resident for the grid barriers
+}
+
+int enqueue_step(const ck_model* m, uint8_t* st, const StateLayout& lay, bool generating,
+                 cudaStream_t s) {
+  StepParams p;
+  int grid;
+  size_t smem;
+  if (!plan_step(m, lay, &p, &grid, &smem)) return CK_INVALID_ARGUMENT;
+  p.st = st;
+  p.generating = generating ? 1u : 0u;
+  CK_CUDA(cudaMemsetAsync(st + lay.scores, 0, 4096, s));  // grid and head barrier counters
+  CK_CUDA(launch_step(p, s, grid, smem));
+  return CK_OK;
+}
+
+int resolve_path(const ck_model* m, const StateLayout& lay) {
+  if (m->path == CK_PATH_KERNELS) return CK_PATH_KERNELS;
+  StepParams p;
+  int grid;
+  size_t smem;
+  const bool ok = plan_step(m, lay, &p, &grid, &smem);
+  if (m->path == CK_PATH_STEP) return ok ? CK_PATH_STEP : -1;
+  return ok ? CK_PATH_STEP : CK_PATH_KERNELS;
+}
+
 int get_graph(ck_model* m, void* dev_state, size_t len, const StateLayout& lay, bool generating,
               cudaGraphExec_t* out) {
+  const int path = resolve_path(m, lay);
+  if (path < 0) return CK_INVALID_ARGUMENT;
   for (auto& g : m->graphs)
-    if (g.state == dev_state && g.len == len && g.generating == generating) {
+    if (g.state == dev_state && g.len == len && g.generating == generating && g.path == path) {
       *out = g.exec;
       return CK_OK;
     }
@@ -461,7 +530,9 @@ int get_graph(ck_model* m, void* dev_state, size_t len, const StateLayout& lay, 
     m->graphs.erase(m->graphs.begin());
   }
   CK_CUDA(cudaStreamBeginCapture(m->capture, cudaStreamCaptureModeThreadLocal));
-  int rc = enqueue_position(m, static_cast<uint8_t*>(dev_state), lay, generating, m->capture);
+  int rc = path == CK_PATH_STEP
+               ? enqueue_step(m, static_cast<uint8_t*>(dev_state), lay, generating, m->capture)
+               : enqueue_position(m, static_cast<uint8_t*>(dev_state), lay, generating, m->capture);
   cudaGraph_t graph = nullptr;
   cudaError_t e = cudaStreamEndCapture(m->capture, &graph);
   if (rc) {
@@ -473,7 +544,7 @@ int get_graph(ck_model* m, void* dev_state, size_t len, const StateLayout& lay, 
   e = cudaGraphInstantiate(&exec, graph, 0);
   cudaGraphDestroy(graph);
   if (e != cudaSuccess) return CK_CUDA_ERROR;
-  m->graphs.push_back({dev_state, len, generating, exec});
+  m->graphs.push_back({dev_state, len, generating, path, exec});
   *out = exec;
   return CK_OK;
 }
@@ -591,17 +662,43 @@ int ck_load_model(const void* artifact, size_t len, void* dev_mem, size_t dev_le
     W.attn_norm = reinterpret_cast<const int32_t*>(dv + L.an);
     W.ffn_norm = reinterpret_cast<const int32_t*>(dv + L.fn);
   }
+  m->dev_layers = reinterpret_cast<DevLayer*>(dv + D.table);
+  m->path = CK_PATH_AUTO;
+  m->max_slots = 0;
+  if (cudaMemcpyAsync(m->dev_layers, m->layers.data(), sizeof(DevLayer) * c.layers,
+                      cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    delete m;
+    return CK_CUDA_ERROR;
+  }
   if (configure_matrow() != cudaSuccess || configure_attention() != cudaSuccess) {
     delete m;
     return CK_CUDA_ERROR;
   }
   if (cudaGetDevice(&m->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&m->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, m->device) !=
+          cudaSuccess ||
+      configure_step((size_t)m->smem_optin, &m->step_smem) != cudaSuccess ||
       cudaStreamCreateWithFlags(&m->capture, cudaStreamNonBlocking) != cudaSuccess) {
     delete m;
     return CK_CUDA_ERROR;
   }
   *out = m;
+  return CK_OK;
+}
+
+int ck_set_path(ck_model* m, int path) {
+  if (!m || path < CK_PATH_AUTO || path > CK_PATH_KERNELS) return CK_INVALID_ARGUMENT;
+  m->path = path;
+  return CK_OK;
+}
+
+int ck_set_step_slots(ck_model* m, uint32_t max_slots) {
+  if (!m || max_slots == 1 || max_slots > 8) return CK_INVALID_ARGUMENT;
+  m->max_slots = max_slots;
+  for (auto& g : m->graphs) cudaGraphExecDestroy(g.exec);  // plans change: rebuild graphs
+  m->graphs.clear();
   return CK_OK;
 }
 

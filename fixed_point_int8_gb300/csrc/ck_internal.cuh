@@ -3,7 +3,9 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <algorithm>
 #include <cmath>
+#include <climits>
 #include <cuda_runtime.h>
 
 #include "../../include/ck.h"
@@ -39,7 +41,10 @@ inline StateLayout state_layout(const ck_config& c, uint32_t n_prompt, uint32_t 
   s.y = take(8ull * c.dim);
   s.h = take(8ull * c.hidden);
   s.logits = take(8ull * c.vocab);
-  s.scores = take(8ull * c.heads * cache);
+  // attention scores and library scratch: max(heads * cache, 1024 * (head + 2) + 2048) words
+  const uint64_t hd = c.dim / c.heads;
+  const uint64_t words = std::max<uint64_t>((uint64_t)c.heads * cache, 1024 * (hd + 2) + 2048);
+  s.scores = take(8ull * words);
   s.k = take(4ull * c.layers * cache * kv_dim);
   s.v = take(4ull * c.layers * cache * kv_dim);
   s.size = off;
@@ -153,6 +158,20 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   return v;
 }
 
+__device__ __forceinline__ bool fits_i32(int64_t v) { return v >= INT32_MIN && v <= INT32_MAX; }
+
+// First failing cache store wins: the smallest (position, layer, phase, element) key.
+__device__ __forceinline__ void record_error(uint8_t* st, uint64_t key) {
+  atomicMin(reinterpret_cast<unsigned long long*>(st + kHErrKey), (unsigned long long)key);
+}
+
+// Rotation of the pair (a, b) by (cos, sin) with 24 fractional bits, products wrapping.
+__device__ __forceinline__ void rotate_pair(int64_t a, int64_t b, int32_t c, int32_t s, int64_t& a2,
+                                            int64_t& b2) {
+  a2 = (int64_t)((uint64_t)wmul(a, c) - (uint64_t)wmul(b, s)) >> 24;
+  b2 = wadd(wmul(a, s), wmul(b, c)) >> 24;
+}
+
 // ------------------------------------------------------------------ device model
 
 struct DevLayer {
@@ -204,6 +223,36 @@ struct AttnParams {
   const uint32_t* exp_tab;
   uint32_t heads, kv_heads, head_dim, kv_dim, inv_sqrt, cache, chunk_cap;
 };
+
+// The persistent one-position kernel (ck_step.cu).
+constexpr uint32_t kStageBytes = 24576;  // one ring slot: whole rows of one matrix
+
+struct StepParams {
+  uint8_t* st;
+  uint64_t off_prompt, off_out, off_x, off_xb, off_q, off_o, off_y, off_h, off_logits, off_work,
+      off_k, off_v;
+  uint32_t cache;
+  uint32_t dim, hidden, layers, heads, kv_heads, vocab, hd, kv_dim, pitch_d, pitch_h, inv_sqrt;
+  uint32_t generating;  // run phases 17-19 after the layers
+  uint32_t gh;          // CTAs per attention head
+  uint32_t ns;          // ring slots
+  uint32_t x_bytes;     // planes / attention region
+  const DevLayer* layers_tab;
+  const uint8_t* embed;
+  const uint32_t* embed_scale;
+  const uint8_t* cls;
+  const uint32_t* cls_scale;
+  const int32_t* final_norm;
+  const int32_t* rope;
+  const uint32_t* exp_tab;
+  const int32_t* silu_tab;
+};
+
+cudaError_t configure_step(size_t optin, size_t* dynamic_max);
+cudaError_t launch_step(const StepParams& p, cudaStream_t s, int grid, size_t smem);
+int step_threads();
+int step_blocks_per_sm(size_t smem);
+int step_consumer_warps();
 
 // Launchers (stream-ordered; return a cudaError_t).
 cudaError_t configure_matrow();     // once per process and device, outside stream capture

@@ -128,19 +128,6 @@ __device__ int prologue(const MatrowParams& p, uint32_t* planes32, Scratch* sc,
   return L;
 }
 
-__device__ __forceinline__ void record_error(uint8_t* st, uint64_t key) {
-  atomicMin(reinterpret_cast<unsigned long long*>(st + kHErrKey), (unsigned long long)key);
-}
-
-__device__ __forceinline__ bool fits32(int64_t v) { return v >= INT32_MIN && v <= INT32_MAX; }
-
-// Rotation of the pair (a, b) by (cos, sin) with 24 fractional bits, products wrapping.
-__device__ __forceinline__ void rotate(int64_t a, int64_t b, int32_t c, int32_t s, int64_t& a2,
-                                       int64_t& b2) {
-  a2 = (int64_t)((uint64_t)wmul(a, c) - (uint64_t)wmul(b, s)) >> 24;
-  b2 = wadd(wmul(a, s), wmul(b, c)) >> 24;
-}
-
 // Epilogue for the row handled by this lane (lanes 0..kR-1 of the warp, row r0 + lane).
 __device__ __forceinline__ void epilogue(const MatrowParams& p, uint32_t row, int64_t y,
                                          uint32_t pos) {
@@ -159,21 +146,21 @@ __device__ __forceinline__ void epilogue(const MatrowParams& p, uint32_t row, in
       const uint32_t j = (row % p.head_dim) >> 1;
       const int32_t* cs = p.rope + ((size_t)pos * (p.head_dim >> 1) + j) * 2;
       int64_t a2, b2;
-      rotate(a, b, __ldg(cs), __ldg(cs + 1), a2, b2);
+      rotate_pair(a, b, __ldg(cs), __ldg(cs + 1), a2, b2);
       p.out[row] = even ? a2 : b2;
     } else if (row < p.q_rows + p.kv_dim) {
       const uint32_t e = row - p.q_rows;
-      if (!fits32(y)) record_error(p.state, err_key(pos, p.layer, 6, e));
+      if (!fits_i32(y)) record_error(p.state, err_key(pos, p.layer, 6, e));
       const uint32_t j = (e % p.head_dim) >> 1;
       const int32_t* cs = p.rope + ((size_t)pos * (p.head_dim >> 1) + j) * 2;
       int64_t a2, b2;
-      rotate((int64_t)(int32_t)a, (int64_t)(int32_t)b, __ldg(cs), __ldg(cs + 1), a2, b2);
+      rotate_pair((int64_t)(int32_t)a, (int64_t)(int32_t)b, __ldg(cs), __ldg(cs + 1), a2, b2);
       const int64_t mine = even ? a2 : b2;
-      if (!fits32(mine)) record_error(p.state, err_key(pos, p.layer, 8, e));
+      if (!fits_i32(mine)) record_error(p.state, err_key(pos, p.layer, 8, e));
       p.kcache[(size_t)pos * p.kv_dim + e] = (int32_t)mine;
     } else {
       const uint32_t e = row - p.q_rows - p.kv_dim;
-      if (!fits32(y)) record_error(p.state, err_key(pos, p.layer, 7, e));
+      if (!fits_i32(y)) record_error(p.state, err_key(pos, p.layer, 7, e));
       p.vcache[(size_t)pos * p.kv_dim + e] = (int32_t)y;
     }
   }

@@ -96,6 +96,25 @@ int ck_model_size(const void* artifact, size_t len, size_t* dev_bytes);
 int ck_load_model(const void* artifact, size_t len, void* dev_mem, size_t dev_len, void* stream,
                   ck_model** out);
 int ck_model_config(const ck_model* m, ck_config* out);
+
+/* How ck_turn runs a position.  CK_PATH_STEP: one persistent kernel per position (one
+ * block per SM, launched cooperatively): a producer warp streams every matrix of the
+ * position through shared memory with bulk copies while consumer warps compute, with grid
+ * barriers between dependent phases.  CK_PATH_KERNELS: one kernel per phase.  CK_PATH_AUTO
+ * (the default) takes the persistent kernel whenever the model and state fit it (padded
+ * dim <= 12288, padded hidden <= 24576, heads <= 1000, enough shared memory) and the
+ * phase kernels otherwise.  Both compute the same bits.  Errors: 10 for an unknown path;
+ * ck_turn returns 10 when CK_PATH_STEP is forced on a model or state it cannot run. */
+#define CK_PATH_AUTO 0
+#define CK_PATH_STEP 1
+#define CK_PATH_KERNELS 2
+int ck_set_path(ck_model* m, int path);
+
+/* Caps the number of shared-memory ring slots (24 KB each) the one-position kernel uses;
+ * 0 (the default) takes as many as fit, up to 8.  A tuning and testing control: fewer
+ * slots prefetch less weight data across phase boundaries; the results are the same bits.
+ * Drops the model's cached graphs.  Errors: 10 for 1 or more than 8. */
+int ck_set_step_slots(ck_model* m, uint32_t max_slots);
 /* Frees the host handle and its cached CUDA graphs (not dev_mem). */
 void ck_free_model(ck_model* m);
 
@@ -111,13 +130,14 @@ void ck_free_model(ck_model* m);
  *   48 u64 seed   56 u64 turns   64 u64 first error key (all ones if none):
  *      position << 44 | layer << 32 | phase << 24 | element, phase 6 key store, 7 value
  *      store, 8 key store after rotary   72 i64 largest logit of the last generating
- *      position   80 7 x u32 the model's configuration   108..255 zero.
+ *      position   80 7 x u32 the model's configuration   108..127 zero   128..255 scratch.
  * Buffers, each at a multiple of 256 bytes from the state start, in order:
  *   prompt ids u32[n_prompt], output tokens u32[max_tokens], x (activations) i64[dim],
  *   four working vectors i64[dim] (xb, q, o, y), h i64[hidden], logits i64[vocab],
- *   scores i64[heads * cache], keys i32[layers][cache][kv_dim], values likewise.
- * The working vectors, h and scores are scratch: their contents between turns are
- * unspecified. */
+ *   scores/work i64[max(heads * cache, 1024 * (head + 2) + 2048)],
+ *   keys i32[layers][cache][kv_dim], values likewise.
+ * The working vectors, h, scores/work and header bytes 128..255 are scratch: their
+ * contents between turns are unspecified. */
 #define CK_FLAG_STOP_TOKENS 1u
 #define CK_PHASE_RUNNING 3u
 #define CK_PHASE_DONE 20u

@@ -356,7 +356,8 @@ void orc_model_close(orc_model* m) {
  * The ids-mode state of the library header: a 256-byte header, then the buffers, each at
  * a multiple of 256 bytes: prompt ids u32[n_prompt], output tokens u32[max_tokens],
  * x, xb, q, o, y i64[dim], h i64[hidden], logits i64[vocab],
- * scores i64[heads*cache], K i32[layers*cache*kv_dim], V i32[layers*cache*kv_dim]. */
+ * scores (work) i64[max(heads*cache, 1024*(head+2)+2048)], K i32[layers*cache*kv_dim],
+ * V i32[layers*cache*kv_dim]. */
 
 enum { H_PHASE = 8, H_POSITION = 12, H_NPROMPT = 16, H_MAXTOK = 20, H_CACHE = 24, H_GENERATED = 28,
        H_FLAGS = 32, H_TEMP = 36, H_ERROR = 40, H_LASTTOK = 44, H_SEED = 48, H_TURNS = 56,
@@ -385,7 +386,10 @@ static orc_layout layout_of(const uint32_t* cfg, uint32_t n_prompt, uint32_t max
   L.y = n; n = up256(n + 8 * dim);
   L.h = n; n = up256(n + 8 * hidden);
   L.logits = n; n = up256(n + 8 * vocab);
-  L.scores = n; n = up256(n + 8 * heads * cache);
+  /* scores / work region: max(heads * cache, 1024 * (head + 2) + 2048) i64 words */
+  uint64_t hd = dim / heads;
+  uint64_t words = heads * cache > 1024 * (hd + 2) + 2048 ? heads * cache : 1024 * (hd + 2) + 2048;
+  L.scores = n; n = up256(n + 8 * words);
   L.k = n; n = up256(n + 4 * layers * cache * kv_dim);
   L.v = n; n = up256(n + 4 * layers * cache * kv_dim);
   L.size = n;

@@ -23,15 +23,19 @@ def ck():
 
 # ---------------------------------------------------------------- helpers
 
+PATHS = {"step": 1, "kernels": 2}   # one persistent kernel per position / one kernel per phase
+
+
 class Pair:
     """The same artifact loaded into the oracle and into the GPU library."""
 
-    def __init__(self, ck, spec):
+    def __init__(self, ck, spec, path="step"):
         self.spec = spec
         self.art = synth.build_artifact(spec)
         self.orc = oracle.Model(self.art)
         rc, self.gpu = ck.Model.load(self.art)
         assert rc == 0, rc
+        assert self.gpu.set_path(PATHS[path]) == 0
 
     def init(self, ck, ids, max_tokens, flags=0):
         rc, so = self.orc.init_state(ids, max_tokens, flags=flags)
@@ -149,9 +153,30 @@ MODELS = {
 }
 
 
-@pytest.fixture(scope="module")
-def pairs(ck):
-    return {name: Pair(ck, wl.spec) for name, wl in MODELS.items()}
+@pytest.mark.parametrize("slots", [2, 3, 5])
+def test_step_kernel_with_a_small_ring(ck, slots):
+    """The persistent kernel with fewer ring slots than consumer warps: every slot is reused
+    many times within each phase, on a small model, against the oracle position by position."""
+    wl = MODELS["gqa"]
+    P = Pair(ck, wl.spec, "step")
+    assert P.gpu.set_step_slots(slots) == 0
+    ids = synth.prompt_ids(wl.spec, wl.n_prompt)
+    so, sg = P.init(ck, ids, wl.steps)
+    for pos in range(8):
+        rco, reso = P.orc.turn(so, 1)
+        rcg, resg = P.gpu.turn(sg, 1)
+        assert rco == rcg == 0 and reso == resg, (pos, rcg, resg)
+        compare_states(P.orc, so, ck.state_download(sg), wl.n_prompt, wl.steps, f"slots {slots} pos {pos}")
+    rco, _ = P.orc.turn(so, 10_000)
+    rcg, _ = P.gpu.turn(sg, 10_000)
+    assert rco == rcg == 0
+    compare_states(P.orc, so, ck.state_download(sg), wl.n_prompt, wl.steps, f"slots {slots}", turns=False)
+    assert P.gpu.set_step_slots(1) == 10
+
+
+@pytest.fixture(scope="module", params=list(PATHS))
+def pairs(ck, request):
+    return {name: Pair(ck, wl.spec, request.param) for name, wl in MODELS.items()}
 
 
 @pytest.mark.parametrize("name", list(MODELS))
@@ -190,9 +215,10 @@ def test_many_positions_in_one_turn(ck, pairs):
     assert P.gpu.turn(sg, 1)[0] == 3                               # complete: InvalidState
 
 
-def test_literal_tiny_workload_fails_like_the_oracle(ck):
+@pytest.mark.parametrize("path", list(PATHS))
+def test_literal_tiny_workload_fails_like_the_oracle(ck, path):
     wl = synth.WORKLOADS["tiny"]
-    P = Pair(ck, wl.spec)
+    P = Pair(ck, wl.spec, path)
     ids = synth.prompt_ids(wl.spec, wl.n_prompt)
     so, sg = P.init(ck, ids, wl.steps)
     rco, reso = P.orc.turn(so, 100)
@@ -312,10 +338,10 @@ def test_model_artifact_errors(ck):
 
 # ---------------------------------------------------------------- full-size sampled positions
 
-def _resume_one(ck, spec, n_prompt, max_tokens, gpu_positions, check_positions):
+def _resume_one(ck, spec, n_prompt, max_tokens, gpu_positions, check_positions, path="step"):
     """GPU runs `gpu_positions`, then the oracle and the GPU each run `check_positions` more
     from that same state; every buffer of the two results must be identical."""
-    P = Pair(ck, spec)
+    P = Pair(ck, spec, path)
     ids = synth.prompt_ids(spec, n_prompt)
     sg = P.gpu.new_state(n_prompt, max_tokens)
     assert P.gpu.init_state(sg, ids, max_tokens) == 0
@@ -331,18 +357,40 @@ def _resume_one(ck, spec, n_prompt, max_tokens, gpu_positions, check_positions):
     return oracle.header(got)
 
 
-def test_llama7b_shape_sampled_positions(ck):
-    """7B-shaped model at full size: two prompt positions on the GPU, then the first
-    generating position (classifier and maximum pass included) on both targets."""
-    h = _resume_one(ck, synth.LLAMA7B, n_prompt=3, max_tokens=4, gpu_positions=2, check_positions=1)
+@pytest.mark.parametrize("path", list(PATHS))
+def test_llama7b_shape_sampled_positions(ck, path):
+    """7B-shaped model at full size, in the launch configuration bench.py times: two prompt
+    positions on the GPU, then the first generating position (classifier and maximum pass
+    included) on both targets."""
+    h = _resume_one(ck, synth.LLAMA7B, n_prompt=3, max_tokens=4, gpu_positions=2, check_positions=1,
+                    path=path)
     assert h["generated"] == 1
 
 
-def test_1b_long_context_sampled_position(ck):
+@pytest.mark.parametrize("path", list(PATHS))
+def test_1b_long_context_sampled_position(ck, path):
     """1B-shaped model at 8192 context: 7936 prompt ids prefilled on the GPU position by
     position, then one generating position with attention over 7936 cached positions
     checked against the oracle."""
     wl = synth.WORKLOADS["1b_long"]
     h = _resume_one(ck, wl.spec, n_prompt=wl.n_prompt, max_tokens=wl.steps,
-                    gpu_positions=wl.n_prompt - 1, check_positions=1)
+                    gpu_positions=wl.n_prompt - 1, check_positions=1, path=path)
     assert h["generated"] == 1 and h["position"] == wl.n_prompt
+
+
+def test_paths_agree_and_unknown_path_is_rejected(ck):
+    wl = MODELS["gqa"]
+    P = Pair(ck, wl.spec, "step")
+    assert P.gpu.set_path(7) == 10
+    ids = synth.prompt_ids(wl.spec, wl.n_prompt)
+    outs = []
+    for path in PATHS.values():
+        assert P.gpu.set_path(path) == 0
+        sg = P.gpu.new_state(wl.n_prompt, wl.steps)
+        assert P.gpu.init_state(sg, ids, wl.steps) == 0
+        rc, res = P.gpu.turn(sg, 10_000)
+        assert rc == 0 and res["complete"]
+        outs.append(ck.state_download(sg))
+    lay = P.orc.layout(wl.n_prompt, wl.steps)
+    for name, end in (("out", lay["x"]), ("x", lay["xb"]), ("logits", lay["scores"]), ("k", lay["size"])):
+        assert np.array_equal(outs[0][lay[name]:end], outs[1][lay[name]:end]), name
