@@ -63,6 +63,7 @@ def lib() -> ctypes.CDLL:
             "ck_state_size": ([vp, u32, u32, ctypes.POINTER(sz)], ctypes.c_int),
             "ck_init_state": ([vp, vp, sz, vp, u32, u32, u32, u64, u32, vp], ctypes.c_int),
             "ck_turn": ([vp, vp, sz, u32, vp, ctypes.POINTER(TurnResult)], ctypes.c_int),
+            "ck_turn_noalloc": ([vp, vp, sz, vp, ctypes.POINTER(TurnResult)], ctypes.c_int),
             "ck_logits": ([vp, vp, sz, vp, vp], ctypes.c_int),
             "ck_argmax": ([vp, vp, sz, ctypes.POINTER(u32), vp], ctypes.c_int),
             "ck_output_tokens": ([vp, vp, sz, vp, u32, ctypes.POINTER(u32), vp], ctypes.c_int),
@@ -171,6 +172,12 @@ class Model:
         res = TurnResult()
         n = state.numel() if length is None else length
         rc = lib().ck_turn(self._h, _ptr(state), n, n_positions, _stream(stream), ctypes.byref(res))
+        return rc, res.as_dict()
+
+    def turn_noalloc(self, state, stream=None):
+        """One position through ck_turn_noalloc (no device allocation, shared scratch)."""
+        res = TurnResult()
+        rc = lib().ck_turn_noalloc(self._h, _ptr(state), state.numel(), _stream(stream), ctypes.byref(res))
         return rc, res.as_dict()
 
     def logits(self, state, stream=None):

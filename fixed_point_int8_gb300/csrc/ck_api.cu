@@ -805,6 +805,57 @@ int ck_turn(ck_model* m, void* dev_state, size_t len, uint32_t n_positions, void
   return failed ? (int)h1.u32(kHError) : CK_OK;
 }
 
+int ck_turn_noalloc(ck_model* m, void* dev_state, size_t len, void* stream, ck_turn_result* out) {
+  if (!m || !dev_state || !out) return CK_INVALID_ARGUMENT;
+  memset(out, 0, sizeof(*out));
+  out->token = 0xFFFFFFFFu;
+  if (reinterpret_cast<uintptr_t>(dev_state) % 256) return CK_INVALID_STATE;
+  cudaStream_t s = S(stream);
+  HostHeader h0;
+  int rc = read_header(dev_state, &h0, s);
+  if (rc) return rc;
+  StateLayout lay;
+  rc = check_state(m, dev_state, len, h0, &lay);
+  if (rc) return rc;
+  if (h0.u32(kHPhase) != CK_PHASE_RUNNING) return CK_INVALID_STATE;
+  const uint32_t pos0 = h0.u32(kHPosition), np = h0.u32(kHNPrompt);
+  if (pos0 >= lay.cache) return CK_INVALID_STATE;
+  StepParams p;
+  int grid;
+  size_t smem;
+  if (!plan_step(m, lay, &p, &grid, &smem)) return CK_INVALID_ARGUMENT;
+  // scratch this position needs: counters, per-(head, chunk) partials, per-block candidates
+  const size_t need = 4096 + 8ull * p.heads * p.gh * (p.hd + 2) + 16ull * grid;
+  if (need > noalloc_work_bytes()) return CK_INVALID_ARGUMENT;
+  uint8_t* work = nullptr;
+  CK_CUDA(noalloc_setup(m->step_smem, &work));
+  p.st = static_cast<uint8_t*>(dev_state);
+  p.generating = pos0 + 1 >= np ? 1u : 0u;
+  CK_CUDA(cudaMemsetAsync(work, 0, 4096, s));  // the counters must start at zero every call
+  CK_CUDA(launch_step_noalloc(p, work, s, grid, smem));
+  HostHeader h1;
+  rc = read_header(dev_state, &h1, s);
+  if (rc) return rc;
+  const bool failed = h1.u32(kHPhase) == CK_PHASE_FAILED;
+  uint64_t turns = h1.u64(kHTurns) + 1;
+  CK_CUDA(cudaMemcpyAsync(static_cast<uint8_t*>(dev_state) + kHTurns, &turns, 8,
+                          cudaMemcpyHostToDevice, s));
+  CK_CUDA(cudaStreamSynchronize(s));
+  out->generated = h1.u32(kHGenerated);
+  out->generated_this_turn = out->generated - h0.u32(kHGenerated);
+  if (out->generated_this_turn) out->token = h1.u32(kHLastTok);
+  out->work = h1.u32(kHPosition) - pos0 + (failed ? 1u : 0u);
+  out->complete = h1.u32(kHPhase) != CK_PHASE_RUNNING;
+  const uint64_t key = h1.u64(kHErrKey);
+  if (key != kNoError) {
+    out->err_position = (uint32_t)(key >> 44);
+    out->err_layer = (uint32_t)(key >> 32) & 0xFFFu;
+    out->err_phase = (uint32_t)(key >> 24) & 0xFFu;
+    out->err_element = (uint32_t)key & 0xFFFFFFu;
+  }
+  return failed ? (int)h1.u32(kHError) : CK_OK;
+}
+
 int ck_logits(const ck_model* m, const void* dev_state, size_t len, int64_t* host_out, void* stream) {
   if (!m || !dev_state || !host_out) return CK_INVALID_ARGUMENT;
   cudaStream_t s = S(stream);

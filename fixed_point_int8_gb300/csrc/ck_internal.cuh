@@ -251,6 +251,9 @@ struct StepParams {
 cudaError_t configure_step(size_t optin, size_t* dynamic_max);
 cudaError_t launch_step(const StepParams& p, cudaStream_t s, int grid, size_t smem);
 int step_threads();
+size_t noalloc_work_bytes();
+cudaError_t noalloc_setup(size_t dynamic_max, uint8_t** work);
+cudaError_t launch_step_noalloc(const StepParams& p, uint8_t* work, cudaStream_t s, int grid, size_t smem);
 int step_blocks_per_sm(size_t smem);
 int step_consumer_warps();
 

@@ -833,7 +833,112 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepParams p) {
   }
 }
 
+// ------------------------------------------------------------------ allocation-free variant
+// The same position with its scratch (barrier counters, attention partials, classifier
+// candidates) in this file's own device array instead of the state's work region.
+constexpr size_t kNoAllocWorkBytes = 256 * 1024;
+static __device__ __align__(256) uint8_t g_noalloc_work[kNoAllocWorkBytes];
+
+__global__ void __launch_bounds__(kThreads, 1) k_step_noalloc(const StepParams p, uint8_t* work) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ Shared sh;
+  uint8_t* st = p.st;
+  if (hdr_ld<uint32_t>(st, kHPhase) != CK_PHASE_RUNNING) return;
+  Ctx c;
+  c.p = &p;
+  c.st = st;
+  c.work = work;
+  c.gbar = reinterpret_cast<uint32_t*>(c.work + kWBar);
+  c.gabort = reinterpret_cast<uint32_t*>(c.work + kWAbort);
+  c.ns = p.ns;
+  c.G = gridDim.x;
+  c.ring = smem;
+  c.X = smem + (size_t)p.ns * kStageBytes;
+  c.full = reinterpret_cast<uint64_t*>(c.X + p.x_bytes);
+  c.empty = c.full + p.ns;
+  c.pos = hdr_ld<uint32_t>(st, kHPosition);
+  const uint32_t np = hdr_ld<uint32_t>(st, kHNPrompt);
+  c.tok = c.pos < np ? reinterpret_cast<const uint32_t*>(st + p.off_prompt)[c.pos]
+                     : reinterpret_cast<const uint32_t*>(st + p.off_out)[c.pos - np];
+  if (c.tok >= p.vocab) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      hdr<uint32_t>(st, kHError) = CK_INVALID_STATE;
+      hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
+    }
+    return;
+  }
+  if (threadIdx.x == 0) {
+    sh.abort = 0;
+    for (uint32_t s = 0; s < p.ns; ++s) {
+      mbar_init(&c.full[s], 1);
+      mbar_init(&c.empty[s], 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if ((threadIdx.x >> 5) == kNCW) {
+    if ((threadIdx.x & 31) == 0) producer(c);
+    return;
+  }
+  consumers(c, sh);
+  if (!p.generating && blockIdx.x == 0 && !sh.abort) {
+    int64_t* x = reinterpret_cast<int64_t*>(st + p.off_x);
+    const int64_t* xb = reinterpret_cast<const int64_t*>(st + p.off_xb);
+    const int64_t* y = reinterpret_cast<const int64_t*>(st + p.off_y);
+    for (uint32_t i = threadIdx.x; i < p.dim; i += kCT) x[i] = wadd(xb[i], y[i]);
+    if (threadIdx.x == 0) {
+      if (hdr_ld<uint64_t>(st, kHErrKey) != kNoError) {
+        hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
+        hdr<uint32_t>(st, kHError) = CK_ARITHMETIC;
+      } else {
+        hdr<uint32_t>(st, kHPosition) += 1;
+      }
+    }
+  }
+  if (threadIdx.x == 0 && blockIdx.x == 0 && (sh.abort || ld_acquire(c.gabort))) {
+    hdr<uint32_t>(st, kHError) = CK_CUDA_ERROR;
+    hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
+  }
+}
+
 }  // namespace
+
+size_t noalloc_work_bytes() { return kNoAllocWorkBytes; }
+
+// Set-up of the allocation-free variant, once per device, with that device current: the
+// device address of the scratch array (host code only holds a stand-in for the symbol) and
+// the kernel's shared-memory limit.  Later calls on the device reuse the cached address.
+cudaError_t noalloc_setup(size_t dynamic_max, uint8_t** work) {
+  static uint8_t* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!addr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_work);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_step_noalloc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dynamic_max);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<uint8_t*>(ptr);
+  }
+  *work = addr[dev];
+  return cudaSuccess;
+}
+
+cudaError_t launch_step_noalloc(const StepParams& p, uint8_t* work, cudaStream_t s, int grid, size_t smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_step_noalloc, p, work);
+}
 
 // Allows the kernel the largest dynamic shared memory the device offers beside its static
 // shared memory; *dynamic_max receives that size.

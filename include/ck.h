@@ -173,6 +173,25 @@ typedef struct ck_turn_result {
 int ck_turn(ck_model* m, void* dev_state, size_t len, uint32_t n_positions, void* stream,
             ck_turn_result* out);
 
+/* ck_turn_noalloc has no counterpart on the page: it exists for callers that cannot
+ * allocate device memory once they are running, for example a server whose device memory
+ * is carved up in advance into fixed arenas, or a host framework that owns every
+ * allocation and forbids libraries from making their own.  It runs exactly one position,
+ * like ck_turn with n_positions = 1 on the persistent one-position kernel, and gives the
+ * same bits and the same result fields.  It allocates nothing: no cudaMalloc, no
+ * cudaFree, no graph is instantiated; the kernel is launched directly.  Its scratch (the
+ * grid and per-head barrier counters, attention partials and per-block classifier
+ * candidates) lives in one 256 KB array in the library's device memory that every GPU
+ * loading the library holds until the process exits; the state's own work region is not
+ * used.  The first call on a device looks up that array's device address and sets the
+ * kernel's shared-memory limit, so make it before any stream capture.  Every call shares
+ * the array and clears its counters first; calls whose work overlaps on the GPU (other
+ * streams, other threads) race on it and must not be issued.  Errors: those of ck_turn,
+ * and 10 when the persistent kernel cannot run this model or state, or when this position
+ * needs more than 256 KB of scratch (4096 + 8 * heads * blocks per head * (head size + 2)
+ * + 16 * blocks bytes, where the blocks are the GPU's SMs up to 768). */
+int ck_turn_noalloc(ck_model* m, void* dev_state, size_t len, void* stream, ck_turn_result* out);
+
 /* Copies the state's logits (i64[vocab], those of the last generating position) to host
  * memory; synchronizes `stream`.  Errors: 3, 9, 10. */
 int ck_logits(const ck_model* m, const void* dev_state, size_t len, int64_t* host_out,
