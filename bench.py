@@ -59,6 +59,39 @@ def matrow_bytes(rows: int, cols: int) -> int:
     return rows * cols + 4 * rows + 8 * rows + 8 * cols
 
 
+def step_bytes(spec, pos: int) -> int:
+    """Algorithmic bytes of one generating position at `pos`: every weight byte and row
+    scale once, the K and V cache words of the positions 0..pos once each, the new K/V words,
+    and the vectors (negligible, counted as the matrix inputs and outputs)."""
+    d, h, kv, L, V = spec.dim, spec.hidden, spec.kv_dim, spec.layers, spec.vocab
+    rows = L * (d + 2 * kv + d + 2 * h + d) + V
+    weights = spec.weight_bytes_per_token() + 4 * rows
+    kv_read = L * (pos + 1) * kv * 4 * 2
+    kv_write = L * kv * 4 * 2
+    vectors = 8 * (L * (4 * d + 3 * d + 2 * h + h + d) + V + d)
+    return weights + kv_read + kv_write + vectors
+
+
+def step_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("ck_step.cu", "ck_internal.cuh"):
+        with open(os.path.join(ROOT, "fixed_point_int8_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def step_traffic():
+    path = os.path.join(ROOT, "profiles", "step_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("kernel_source_hash") == step_source_hash():
+            return int(d["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for f in ("ck_matrow.cu", "ck_internal.cuh"):
@@ -184,6 +217,9 @@ def run_ours(args):
                           "GB/s": round(nb / (avg * 1e-3) / 1e9, 1)}), flush=True)
         return
     spec = synth.LLAMA7B
+    if args.layers:
+        import dataclasses
+        spec = dataclasses.replace(spec, layers=args.layers)  # profiling aid only
     n_prompt = args.prompt_ids
     K, W = args.steps, args.warmup
     e2e_steps = min(K, args.e2e_steps)
@@ -195,6 +231,8 @@ def run_ours(args):
     ids = synth.prompt_ids(spec, n_prompt, run=rank)
     rc, model = ck.Model.load(art)
     assert rc == 0, f"ck_load_model failed: {rc}"
+    path = {"auto": ck.PATH_AUTO, "step": ck.PATH_STEP, "kernels": ck.PATH_KERNELS}[args.path]
+    assert model.set_path(path) == 0
     state = model.new_state(n_prompt, max_tokens)
     assert model.init_state(state, ids, max_tokens) == 0
     stream = torch.cuda.current_stream()
@@ -243,6 +281,19 @@ def run_ours(args):
     assert rc == 0
 
     roof, sweep = matrow_measurements(ck, torch, args)
+    kernel_path = "kernels" if args.path == "kernels" else "step"
+    if kernel_path == "step":
+        # the one-position kernel is the whole path: one launch per position
+        p0 = n_prompt + W  # first timed position
+        alg = sum(step_bytes(spec, p) for p in range(p0, p0 + K))
+        achieved = alg / (dev_ms * 1e-3) / 1e9
+        hbm_peak, peak_kind = load_peaks()
+        roof_matrow = roof
+        roof = {"kernel": "k_step", "launch": "one decode position (all 32 layers, classifier, maximum pass)",
+                "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
+                "traffic": step_traffic(), "algorithmic_bytes": alg // K,
+                "avg_launch_us": round(dev_ms * 1e3 / K, 2)}
 
     cpu = None
     bitexact = None
@@ -284,6 +335,8 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "bitexact": bitexact,
         "matrow_sweep": sweep,
+        "matrow_roofline": roof_matrow if kernel_path == "step" else None,
+        "path": kernel_path,
         "setup_s": round(setup_s, 1),
     }
     print(json.dumps(line), flush=True)
@@ -423,8 +476,12 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=150.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=("auto", "step", "kernels"), default="auto",
+                    help="one persistent kernel per position (step) or one kernel per phase")
     ap.add_argument("--prompt-ids", type=int, default=128,
                     help="prompt length (the workload uses 128; shorter only for profiling)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling aid: the same model with fewer layers (small ncu captures)")
     ap.add_argument("--matrow-only", default="",
                     help="profiling aid: time ck_matrow on one ROWSxCOLS shape and exit")
     args = ap.parse_args()

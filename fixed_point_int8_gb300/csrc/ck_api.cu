@@ -467,14 +467,27 @@ bool plan_step(const ck_model* m, const StateLayout& lay, StepParams* sp, int* g
   const uint32_t chunk = (lay.cache + gh - 1) / gh;
   const uint64_t attn = 8ull * ((uint64_t)m->head_dim * (1 + step_consumer_warps()) +
                                 step_consumer_warps() + chunk);
-  const uint64_t planes = 8ull * (m->pitch_d > m->pitch_h ? m->pitch_d : m->pitch_h);
-  const uint64_t xb = (std::max(attn, planes) + 15) & ~15ull;
+  const uint64_t max_pitch = m->pitch_d > m->pitch_h ? m->pitch_d : m->pitch_h;
+  // planes of all eight limbs in shared memory when they are small; otherwise four there and
+  // limbs 4..7 (vectors beyond 32 bits, rare) in a global copy in the work region
+  const uint32_t lcap = 8 * max_pitch <= 48 * 1024 ? 8u : 4u;
+  const uint64_t planes = (uint64_t)lcap * max_pitch;
+  // most rows a block takes in one matrix (whole pairs split over the grid), plus slack
+  const uint64_t max_rows = std::max<uint64_t>(
+      std::max<uint64_t>((uint64_t)c.dim + 2 * (uint64_t)m->kv_dim, 2 * (uint64_t)c.hidden),
+      std::max<uint64_t>((uint64_t)c.dim, (uint64_t)c.vocab));
+  const uint64_t scale_cap = 2 * (((max_rows + 1) / 2 + G - 1) / G) + 2;
+  const uint64_t xb = (std::max<uint64_t>(attn, planes + 4 * scale_cap + 4 * (uint64_t)m->head_dim) + 15) & ~15ull;
   const uint64_t avail = (uint64_t)m->step_smem;
   if (avail < xb + 2 * (kStageBytes + 16)) return false;
   uint64_t ns = (avail - xb) / (kStageBytes + 16);
   if (ns > 8) ns = 8;
   if (m->max_slots && ns > m->max_slots) ns = m->max_slots;
   if (ns < 2) return false;
+  // work region: counters and attention partials, per-block candidates, global planes
+  const uint64_t off_gplanes = (4096 + 8ull * c.heads * gh * (m->head_dim + 2) + 16ull * G + 255) & ~255ull;
+  const uint64_t work_bytes = lay.k - lay.scores;
+  if (off_gplanes + (8 - lcap) * max_pitch > work_bytes) return false;
   StepParams& p = *sp;
   p = StepParams{};
   p.off_prompt = lay.prompt; p.off_out = lay.out; p.off_x = lay.x; p.off_xb = lay.xb; p.off_q = lay.q;
@@ -485,6 +498,15 @@ bool plan_step(const ck_model* m, const StateLayout& lay, StepParams* sp, int* g
   p.vocab = c.vocab; p.hd = m->head_dim; p.kv_dim = m->kv_dim; p.pitch_d = m->pitch_d;
   p.pitch_h = m->pitch_h; p.inv_sqrt = m->inv_sqrt;
   p.gh = gh; p.ns = (uint32_t)ns; p.x_bytes = (uint32_t)xb;
+  p.planes_bytes = (uint32_t)planes;
+  p.lcap = lcap;
+  p.off_gplanes = off_gplanes;
+  // warp groups: groups <= slots (parity rule), two slots beyond the groups stay in flight
+  p.ngroups = ns >= 6 ? 4u : (ns >= 4 ? (uint32_t)ns - 2 : 1u);
+  p.wgroup = (uint32_t)step_consumer_warps() / p.ngroups;
+  p.scale_cap = (uint32_t)scale_cap;
+  p.div_dim = make_invdiv(c.dim);
+  p.div_hidden = make_invdiv(c.hidden);
   p.layers_tab = m->dev_layers;
   p.embed = m->embed; p.embed_scale = m->embed_scale; p.cls = m->cls; p.cls_scale = m->cls_scale;
   p.final_norm = m->final_norm; p.rope = m->rope; p.exp_tab = m->exp_tab; p.silu_tab = m->silu_tab;
@@ -825,7 +847,7 @@ int ck_turn_noalloc(ck_model* m, void* dev_state, size_t len, void* stream, ck_t
   size_t smem;
   if (!plan_step(m, lay, &p, &grid, &smem)) return CK_INVALID_ARGUMENT;
   // scratch this position needs: counters, per-(head, chunk) partials, per-block candidates
-  const size_t need = 4096 + 8ull * p.heads * p.gh * (p.hd + 2) + 16ull * grid;
+  const size_t need = p.off_gplanes + (8 - p.lcap) * (size_t)std::max(p.pitch_d, p.pitch_h);
   if (need > noalloc_work_bytes()) return CK_INVALID_ARGUMENT;
   uint8_t* work = nullptr;
   CK_CUDA(noalloc_setup(m->step_smem, &work));

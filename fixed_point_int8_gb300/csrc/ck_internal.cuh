@@ -77,10 +77,19 @@ __host__ __device__ inline uint64_t mulhi_u64(uint64_t a, uint64_t b) {
 #endif
 }
 
-// floor(sqrt(v)) for any u64: a double-precision estimate corrected by exact integer steps.
+// floor(sqrt(v)) for any u64: a single-precision estimate, one Newton step on the exact
+// integer residual, then exact integer corrections (no double precision: it is slow here).
 __host__ __device__ inline uint64_t isqrt_u64(uint64_t v) {
-  uint64_t r = (uint64_t)sqrt((double)v);
+  uint64_t r = (uint64_t)sqrtf((float)v);
   if (r > 0xFFFFFFFFull) r = 0xFFFFFFFFull;
+  if (r > 0) {
+    const int64_t e = (int64_t)(v - r * r);  // |e| < 2^62: r is within 2^-11 of the root
+    const int64_t step = (int64_t)((float)e / (2.0f * (float)r));
+    int64_t t = (int64_t)r + step;
+    if (t < 0) t = 0;
+    if (t > 0xFFFFFFFFll) t = 0xFFFFFFFFll;
+    r = (uint64_t)t;
+  }
   while (r * r > v) --r;
   while (r < 0xFFFFFFFFull && (r + 1) * (r + 1) <= v) ++r;
   return r;
@@ -99,17 +108,13 @@ struct InvDiv {
 __host__ __device__ inline InvDiv make_invdiv(uint32_t d) {
   uint32_t l = 0;
   while (l < 32 && (1ull << l) < (uint64_t)d) ++l;
-  const uint64_t a = (1ull << l) - d;  // a < d
-  uint64_t q = 0, r = a;               // floor(a * 2^64 / d) by binary long division
-  for (int i = 63; i >= 0; --i) {
-    r <<= 1;                           // r < d < 2^32: never overflows
-    if (r >= d) {
-      r -= d;
-      q |= 1ull << i;
-    }
-  }
+  const uint64_t a = (1ull << l) - d;  // a < d < 2^32
+  // floor(a * 2^64 / d) in two 64/32 steps: both partial quotients are below 2^32
+  const uint64_t hi = (a << 32) / d;
+  const uint64_t rem = (a << 32) - hi * d;
+  const uint64_t lo = (rem << 32) / d;
   InvDiv D;
-  D.m = q + 1;
+  D.m = ((hi << 32) | lo) + 1;
   D.sh1 = l < 1 ? l : 1;
   D.sh2 = l > 0 ? l - 1 : 0;
   return D;
@@ -236,7 +241,13 @@ struct StepParams {
   uint32_t generating;  // run phases 17-19 after the layers
   uint32_t gh;          // CTAs per attention head
   uint32_t ns;          // ring slots
-  uint32_t x_bytes;     // planes / attention region
+  uint32_t x_bytes;     // planes, row scales and rotary row / attention region
+  uint32_t planes_bytes;  // lcap * the largest padded row (planes kept in shared memory)
+  uint32_t lcap;          // limbs whose planes fit shared memory (4 or 8); more go to global
+  uint32_t ngroups, wgroup;  // consumer warp groups and warps per group
+  uint64_t off_gplanes;   // global planes lcap..7, from the work region start
+  uint32_t scale_cap;   // most rows any block takes in one matrix
+  InvDiv div_dim, div_hidden;  // for the mean of squares
   const DevLayer* layers_tab;
   const uint8_t* embed;
   const uint32_t* embed_scale;

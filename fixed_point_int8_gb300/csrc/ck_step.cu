@@ -49,7 +49,10 @@ struct MR {
 };
 
 struct Shared {
-  unsigned long long ra[kNCW], rb[kNCW];
+  const uint32_t* scales;  // this block's row scales of the phase (shared memory)
+  const int32_t* rope;     // this position's (cos, sin) pairs (shared memory)
+  uint32_t rb;             // first row of this block in the phase
+  unsigned long long ra[kNCW], rbuf[kNCW];
   long long am_v[kNCW];
   uint32_t am_i[kNCW];
   InvDiv div;
@@ -215,8 +218,7 @@ __device__ bool grid_sync(const Ctx& c, Shared& sh, uint32_t& epoch) {
   consumer_bar();
   ++epoch;
   if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(c.gbar, 1u);
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(c.gbar) : "memory");
     const uint32_t target = epoch * c.G;
     uint32_t i = 0;
     while (ld_acquire(c.gbar) < target) {
@@ -237,8 +239,7 @@ __device__ bool grid_sync(const Ctx& c, Shared& sh, uint32_t& epoch) {
 __device__ bool group_sync(const Ctx& c, Shared& sh, uint32_t* counter, uint32_t target) {
   consumer_bar();
   if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(counter, 1u);
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(counter) : "memory");
     uint32_t i = 0;
     while (ld_acquire(counter) < target) {
       if (++i > kPollLimit || ld_acquire(c.gabort)) {
@@ -272,14 +273,14 @@ __device__ void consumer_sum_or(unsigned long long& s, unsigned long long& o, Sh
   o = warp_or(o);
   if (lane == 0) {
     sh.ra[warp] = s;
-    sh.rb[warp] = o;
+    sh.rbuf[warp] = o;
   }
   consumer_bar();
   if (threadIdx.x == 0) {
     unsigned long long a = 0, b = 0;
     for (int w = 0; w < kNCW; ++w) {
       a += sh.ra[w];
-      b |= sh.rb[w];
+      b |= sh.rbuf[w];
     }
     sh.S = a;
     sh.orv = b;
@@ -289,33 +290,126 @@ __device__ void consumer_sum_or(unsigned long long& s, unsigned long long& o, Sh
   o = sh.orv;
 }
 
-__device__ __forceinline__ int64_t input_elem(const Ctx& c, const MR& m, uint32_t i) {
+constexpr int kPPT = 8;                                  // element pairs per thread per block
+constexpr uint32_t kBlockPairs = (uint32_t)kCT * kPPT;   // 2048 pairs = 4096 elements
+
+// The phase input for element pairs pbase + tid + j*kCT (j < kPPT): the embedding row of the
+// token (phase 3), or in (+ add).  All loads of a block are issued before any is used, so a
+// thread waits for one round trip per block instead of one per element.  Beyond n: zeros.
+__device__ __forceinline__ void load_pairs(const Ctx& c, const MR& m, uint32_t pbase, int64_t (&x)[2 * kPPT]) {
+  const uint32_t n = m.cols;
   if (m.pro == kPEmbedNorm) {
     const StepParams& p = *c.p;
+    const uint8_t* row = p.embed + (size_t)c.tok * p.pitch_d;
     const int64_t s = (int64_t)__ldg(p.embed_scale + c.tok);
-    return ((int64_t)p.embed[(size_t)c.tok * p.pitch_d + i] - 128) * s >> 8;  // phase 3
+#pragma unroll
+    for (int j = 0; j < kPPT; ++j) {
+      const uint32_t i = 2 * (pbase + threadIdx.x + (uint32_t)j * kCT);
+      int64_t a = 0, b = 0;
+      if (i + 1 < n) {
+        const uint16_t w = *reinterpret_cast<const uint16_t*>(row + i);
+        a = ((int64_t)(w & 0xFF) - 128) * s >> 8;
+        b = ((int64_t)(w >> 8) - 128) * s >> 8;
+      } else if (i < n) {
+        a = ((int64_t)row[i] - 128) * s >> 8;
+      }
+      x[2 * j] = a;
+      x[2 * j + 1] = b;
+    }
+    return;
   }
-  int64_t x = m.in[i];
-  if (m.add) x = wadd(x, m.add[i]);
-  return x;
+#pragma unroll
+  for (int j = 0; j < kPPT; ++j) {
+    const uint32_t i = 2 * (pbase + threadIdx.x + (uint32_t)j * kCT);
+    int64_t a = 0, b = 0;
+    if (i + 1 < n) {
+      const longlong2 v = *reinterpret_cast<const longlong2*>(m.in + i);
+      a = v.x;
+      b = v.y;
+    } else if (i < n) {
+      a = m.in[i];
+    }
+    x[2 * j] = a;
+    x[2 * j + 1] = b;
+  }
+  if (m.add) {
+#pragma unroll
+    for (int j = 0; j < kPPT; ++j) {
+      const uint32_t i = 2 * (pbase + threadIdx.x + (uint32_t)j * kCT);
+      if (i + 1 < n) {
+        const longlong2 v = *reinterpret_cast<const longlong2*>(m.add + i);
+        x[2 * j] = wadd(x[2 * j], v.x);
+        x[2 * j + 1] = wadd(x[2 * j + 1], v.y);
+      } else if (i < n) {
+        x[2 * j] = wadd(x[2 * j], m.add[i]);
+      }
+    }
+  }
 }
 
-// Packs the phase's input vector into byte planes; returns the limb count, *S the sum.
+// The norm weights of the same element pairs (zeros beyond n).
+__device__ __forceinline__ void load_weights(const MR& m, uint32_t pbase, int2 (&w)[kPPT]) {
+  const uint32_t n = m.cols;
+#pragma unroll
+  for (int j = 0; j < kPPT; ++j) {
+    const uint32_t i = 2 * (pbase + threadIdx.x + (uint32_t)j * kCT);
+    int2 v = make_int2(0, 0);
+    if (i + 1 < n) v = *reinterpret_cast<const int2*>(m.norm_w + i);
+    else if (i < n) v.x = m.norm_w[i];
+    w[j] = v;
+  }
+}
+
+// Packs the phase's input vector into byte planes (after the residual and the RMS
+// normalization where the phase has them); returns the limb count and *S the wrapping sum.
 __device__ int prologue(const Ctx& c, const MR& m, Shared& sh, unsigned long long* S_out) {
-  const uint32_t n = m.cols, words = m.pitch / 4;
-  uint32_t* planes32 = reinterpret_cast<uint32_t*>(c.X);
+  const uint32_t n = m.cols, half = m.pitch / 2;
+  const uint32_t npairs = (n + 1) / 2;
+  uint16_t* planes16 = reinterpret_cast<uint16_t*>(c.X);
+  const uint32_t lcap = c.p->lcap;
+  uint16_t* gplanes16 = reinterpret_cast<uint16_t*>(c.work + c.p->off_gplanes);
   const bool writer = blockIdx.x == 0;
-  if (m.pro != kPPlain) {
+  const bool norm = m.pro != kPPlain;
+  const bool single = half <= kBlockPairs;  // the whole vector fits one block of registers
+  // this block's row scales (and for Q/K/V the position's rotary row) go to shared memory
+  // so that no epilogue waits on global memory; the loads are issued first and stored last
+  uint32_t rb, re;
+  cta_rows(m, blockIdx.x, c.G, rb, re);
+  uint32_t* sc = reinterpret_cast<uint32_t*>(c.X + c.p->planes_bytes);
+  int32_t* rp = reinterpret_cast<int32_t*>(c.X + c.p->planes_bytes + 4 * c.p->scale_cap);
+  const uint32_t my_row = rb + threadIdx.x;
+  const uint32_t my_scale = my_row < re ? __ldg(m.scale + my_row) : 0u;
+  const bool qkv = m.epi == kEQKV;
+  const int32_t my_rope = (qkv && threadIdx.x < c.p->hd) ? __ldg(c.p->rope + (size_t)c.pos * c.p->hd + threadIdx.x) : 0;
+  int64_t x[2 * kPPT];
+  int2 wv[kPPT];
+  if (norm) {
     // "RMS normalization": rms = isqrt(sum(x*x)/n + 42,950), at least 1
     unsigned long long ss = 0, dummy = 0;
-    for (uint32_t i = threadIdx.x; i < n; i += kCT) {
-      const int64_t x = input_elem(c, m, i);
-      if (writer && m.res_out) m.res_out[i] = x;
-      ss += (unsigned long long)x * (unsigned long long)x;
+    for (uint32_t pb = 0; pb < npairs; pb += kBlockPairs) {
+      load_pairs(c, m, pb, x);
+      if (single) load_weights(m, pb, wv);  // in flight while the sums reduce
+#pragma unroll
+      for (int e = 0; e < 2 * kPPT; ++e) ss += (unsigned long long)x[e] * (unsigned long long)x[e];
+      if (writer && m.res_out) {
+#pragma unroll
+        for (int j = 0; j < kPPT; ++j) {
+          const uint32_t i = 2 * (pb + threadIdx.x + (uint32_t)j * kCT);
+          if (i + 1 < n) {
+            longlong2 v;
+            v.x = x[2 * j];
+            v.y = x[2 * j + 1];
+            *reinterpret_cast<longlong2*>(m.res_out + i) = v;
+          } else if (i < n) {
+            m.res_out[i] = x[2 * j];
+          }
+        }
+      }
     }
     consumer_sum_or(ss, dummy, sh);
     if (threadIdx.x == 0) {
-      uint64_t rms = isqrt_u64(ss / n + 42950ull);
+      const InvDiv& Dn = n == c.p->dim ? c.p->div_dim : c.p->div_hidden;
+      uint64_t rms = isqrt_u64(udiv_inv(ss, Dn) + 42950ull);
       if (rms < 1) rms = 1;
       sh.div = make_invdiv((uint32_t)rms);
     }
@@ -323,56 +417,109 @@ __device__ int prologue(const Ctx& c, const MR& m, Shared& sh, unsigned long lon
   }
   const InvDiv D = sh.div;
   unsigned long long S = 0, orv = 0;
-  for (uint32_t g = threadIdx.x; g < words; g += kCT) {
-    int64_t v[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t i = 4 * g + e;
-      int64_t val = 0;
-      if (i < n) {
-        if (m.pro != kPPlain) {
-          const int64_t prod = wmul(input_elem(c, m, i), (int64_t)m.norm_w[i]);
-          val = sdiv_trunc(prod, D) >> 8;  // division toward zero, then >> 8
-        } else {
-          val = m.in[i];
-        }
-      }
-      v[e] = val;
-      S += (unsigned long long)val;
-      orv |= (unsigned long long)(val ^ (val >> 63));
+  for (uint32_t pb = 0; pb < half; pb += kBlockPairs) {
+    if (!(norm && single)) {  // a single block is still in registers
+      load_pairs(c, m, pb, x);
+      if (norm) load_weights(m, pb, wv);
     }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      uint32_t w = 0;
+    for (int j = 0; j < kPPT; ++j) {
+      const uint32_t pidx = pb + threadIdx.x + (uint32_t)j * kCT;
+      if (pidx >= half) continue;
+      const uint32_t i = 2 * pidx;
+      int64_t v0 = x[2 * j], v1 = x[2 * j + 1];
+      if (norm) {
+        // y = ((x * w) / rms) >> 8, the division truncating toward zero
+        v0 = i < n ? sdiv_trunc(wmul(v0, (int64_t)wv[j].x), D) >> 8 : 0;
+        v1 = i + 1 < n ? sdiv_trunc(wmul(v1, (int64_t)wv[j].y), D) >> 8 : 0;
+      }
+      S += (unsigned long long)v0 + (unsigned long long)v1;
+      orv |= (unsigned long long)(v0 ^ (v0 >> 63)) | (unsigned long long)(v1 ^ (v1 >> 63));
 #pragma unroll
-      for (int e = 0; e < 4; ++e) w |= (uint32_t)(((uint64_t)v[e] >> (8 * k)) & 0xFF) << (8 * e);
-      planes32[k * words + g] = w;
+      for (int k = 0; k < 8; ++k) {
+        if ((uint32_t)k >= lcap) break;
+        planes16[(size_t)k * half + pidx] =
+            (uint16_t)((((uint64_t)v0 >> (8 * k)) & 0xFF) | ((((uint64_t)v1 >> (8 * k)) & 0xFF) << 8));
+      }
     }
   }
-  consumer_sum_or(S, orv, sh);
+  if (my_row < re) sc[threadIdx.x] = my_scale;
+  for (uint32_t r = my_row + kCT; r < re; r += kCT) sc[r - rb] = __ldg(m.scale + r);
+  if (qkv && threadIdx.x < c.p->hd) rp[threadIdx.x] = my_rope;
+  for (uint32_t i = threadIdx.x + kCT; qkv && i < c.p->hd; i += kCT)
+    rp[i] = __ldg(c.p->rope + (size_t)c.pos * c.p->hd + i);
+  if (threadIdx.x == 0) {
+    sh.scales = sc;
+    sh.rb = rb;
+    sh.rope = rp;
+  }
+  consumer_sum_or(S, orv, sh);  // its barriers also publish the scales and the rotary row
   int L = 1;
   while (L < 8 && (orv >> (8 * L - 1)) != 0) ++L;
+  if ((uint32_t)L > lcap) {
+    // A vector beyond 8*lcap bits (rare): its planes lcap..L-1 go to the global copy, which
+    // every block writes with the same bytes; the consumers read them from there.
+    for (uint32_t pb = 0; pb < half; pb += kBlockPairs) {
+      load_pairs(c, m, pb, x);
+      if (norm) load_weights(m, pb, wv);
+#pragma unroll
+      for (int j = 0; j < kPPT; ++j) {
+        const uint32_t pidx = pb + threadIdx.x + (uint32_t)j * kCT;
+        if (pidx >= half) continue;
+        const uint32_t i = 2 * pidx;
+        int64_t v0 = x[2 * j], v1 = x[2 * j + 1];
+        if (norm) {
+          v0 = i < n ? sdiv_trunc(wmul(v0, (int64_t)wv[j].x), D) >> 8 : 0;
+          v1 = i + 1 < n ? sdiv_trunc(wmul(v1, (int64_t)wv[j].y), D) >> 8 : 0;
+        }
+        for (uint32_t k = lcap; k < (uint32_t)L; ++k)
+          gplanes16[(size_t)(k - lcap) * half + pidx] =
+              (uint16_t)((((uint64_t)v0 >> (8 * k)) & 0xFF) | ((((uint64_t)v1 >> (8 * k)) & 0xFF) << 8));
+      }
+    }
+    __threadfence_block();
+    consumer_bar();
+  }
   *S_out = S;
   return L;
 }
 
-// R rows of a stage (lanes along the row); returns in lane r (< R) the 64-bit sum of row r.
-template <int L, int R>
-__device__ __forceinline__ unsigned long long dot_rows(const uint8_t* rows, uint32_t pitch,
-                                                      const uint8_t* planes) {
+// Row r (< 4) of the up to four rows a warp takes at once: the two rows of pair pq, then
+// the two rows of pair pq + wg.
+__device__ __forceinline__ uint32_t stage_row(uint32_t pq, uint32_t wg, uint32_t r) {
+  return 2 * (pq + (r >> 1) * wg) + (r & 1);
+}
+
+// R rows of a stage (lanes along the row), rows stage_row(pq, wg, 0..R) of the stage;
+// returns in lane r (< R) the 64-bit sum of row r.  Planes k < lcap are in shared memory, the others
+// (only when kMixed) in the global copy.
+template <int L, int R, bool kMixed>
+__device__ __forceinline__ unsigned long long dot_rows(const uint8_t* stage, uint32_t pq, uint32_t wg,
+                                                      uint32_t pitch, const uint8_t* planes_s,
+                                                      const uint8_t* planes_g, uint32_t lcap) {
   const int lane = threadIdx.x & 31;
+  const uint8_t* rp[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) rp[r] = stage + (size_t)stage_row(pq, wg, (uint32_t)r) * pitch;
+  const uint8_t* pp[L];
+#pragma unroll
+  for (int k = 0; k < L; ++k)
+    pp[k] = (!kMixed || (uint32_t)k < lcap) ? planes_s + (size_t)k * pitch : planes_g + (size_t)(k - lcap) * pitch;
   uint32_t acc[R][L];
 #pragma unroll
   for (int r = 0; r < R; ++r)
 #pragma unroll
     for (int k = 0; k < L; ++k) acc[r][k] = 0;
+  // Nine warps put three on one of the SM's four register-file quarters, which leaves 168
+  // registers a thread: the column loop stays rolled so the accumulators never spill.
+#pragma unroll 1
   for (uint32_t cc = lane * 16; cc < pitch; cc += 512) {
     uint4 w[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) w[r] = *reinterpret_cast<const uint4*>(rows + (size_t)r * pitch + cc);
+    for (int r = 0; r < R; ++r) w[r] = *reinterpret_cast<const uint4*>(rp[r] + cc);
 #pragma unroll
     for (int k = 0; k < L; ++k) {
-      const uint4 x = *reinterpret_cast<const uint4*>(planes + (size_t)k * pitch + cc);
+      const uint4 x = *reinterpret_cast<const uint4*>(pp[k] + cc);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         if (k < L - 1) {
@@ -409,6 +556,18 @@ __device__ __forceinline__ unsigned long long dot_rows(const uint8_t* rows, uint
   return mine;
 }
 
+template <int L, bool kMixed>
+__device__ __forceinline__ unsigned long long dot_rows_n(uint32_t R, const uint8_t* stage, uint32_t pq, uint32_t wg,
+                                                        uint32_t pitch, const uint8_t* ps, const uint8_t* pg,
+                                                        uint32_t lcap) {
+  switch (R) {
+    case 4: return dot_rows<L, 4, kMixed>(stage, pq, wg, pitch, ps, pg, lcap);
+    case 3: return dot_rows<L, 3, kMixed>(stage, pq, wg, pitch, ps, pg, lcap);
+    case 2: return dot_rows<L, 2, kMixed>(stage, pq, wg, pitch, ps, pg, lcap);
+    default: return dot_rows<L, 1, kMixed>(stage, pq, wg, pitch, ps, pg, lcap);
+  }
+}
+
 struct Best {
   long long v;
   uint32_t i;
@@ -423,7 +582,7 @@ __device__ __forceinline__ void best_update(Best& b, long long v, uint32_t i) {
 
 // Epilogue for the row of this lane (lanes < R), after the partner exchange for pairs.
 __device__ __forceinline__ void epilogue(const Ctx& c, const MR& m, uint32_t layer, uint32_t row,
-                                         bool valid, int64_t y, Best& best) {
+                                         bool valid, int64_t y, Best& best, const int32_t* rope) {
   const int64_t partner = (int64_t)__shfl_xor_sync(0xffffffffu, (unsigned long long)y, 1);
   if (!valid) return;
   const StepParams& p = *c.p;
@@ -440,17 +599,15 @@ __device__ __forceinline__ void epilogue(const Ctx& c, const MR& m, uint32_t lay
     const uint32_t q_rows = p.dim;
     if (row < q_rows) {
       const uint32_t j = (row % p.hd) >> 1;
-      const int32_t* cs = p.rope + ((size_t)c.pos * (p.hd >> 1) + j) * 2;
       int64_t a2, b2;
-      rotate_pair(a, b, __ldg(cs), __ldg(cs + 1), a2, b2);
+      rotate_pair(a, b, rope[2 * j], rope[2 * j + 1], a2, b2);
       m.out[row] = even ? a2 : b2;
     } else if (row < q_rows + p.kv_dim) {
       const uint32_t e = row - q_rows;
       if (!fits_i32(y)) record_error(c.st, err_key(c.pos, layer, 6, e));
       const uint32_t j = (e % p.hd) >> 1;
-      const int32_t* cs = p.rope + ((size_t)c.pos * (p.hd >> 1) + j) * 2;
       int64_t a2, b2;
-      rotate_pair((int64_t)(int32_t)a, (int64_t)(int32_t)b, __ldg(cs), __ldg(cs + 1), a2, b2);
+      rotate_pair((int64_t)(int32_t)a, (int64_t)(int32_t)b, rope[2 * j], rope[2 * j + 1], a2, b2);
       const int64_t mine = even ? a2 : b2;
       if (!fits_i32(mine)) record_error(c.st, err_key(c.pos, layer, 8, e));
       m.kc[(size_t)c.pos * p.kv_dim + e] = (int32_t)mine;
@@ -462,19 +619,23 @@ __device__ __forceinline__ void epilogue(const Ctx& c, const MR& m, uint32_t lay
   }
 }
 
-template <int L>
+template <int L, bool kMixed>
 __device__ void consume_phase(const Ctx& c, const MR& m, uint32_t layer, unsigned long long S,
                               uint32_t gs0, Shared& sh, Best& best) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const StepParams& p = *c.p;
+  // Stages rotate over the warp groups; the warps of a group split each stage's row pairs.
+  // A group's previous stage precedes the slot's previous use (groups <= slots), so its
+  // parity wait can never see a phase two uses old.
+  const uint32_t grp = (uint32_t)warp / p.wgroup, wi = (uint32_t)warp % p.wgroup;
+  if (grp >= p.ngroups) return;
   uint32_t rb, re;
   cta_rows(m, blockIdx.x, c.G, rb, re);
   const uint32_t sr = stage_rows(m.pitch);
+  const uint8_t* pg = c.work + p.off_gplanes;
   uint32_t gs = gs0;
-  // Stages rotate over min(kNCW, ns) owner warps: a warp's previous stage then precedes the
-  // slot's previous use, so its parity wait can never see a phase two uses old.
-  const uint32_t owners = c.ns < (uint32_t)kNCW ? c.ns : (uint32_t)kNCW;
   for (uint32_t r0 = rb; r0 < re; r0 += sr, ++gs) {
-    if (gs % owners != (uint32_t)warp) continue;
+    if (gs % p.ngroups != grp) continue;
     const uint32_t slot = gs % c.ns;
     bool ok = false;
     for (uint32_t i = 0; i < kPollLimit; ++i) {
@@ -490,30 +651,22 @@ __device__ void consume_phase(const Ctx& c, const MR& m, uint32_t layer, unsigne
       return;
     }
     const uint32_t nr = min(sr, re - r0);
+    const uint32_t npairs = (nr + 1) / 2;
     const uint8_t* stage = c.ring + (size_t)slot * kStageBytes;
-    for (uint32_t g = 0; g < nr;) {
-      const uint32_t left = nr - g;
-      unsigned long long acc;
-      uint32_t R;
-      if (left >= 4) {
-        acc = dot_rows<L, 4>(stage + (size_t)g * m.pitch, m.pitch, c.X);
-        R = 4;
-      } else if (left >= 2) {
-        acc = dot_rows<L, 2>(stage + (size_t)g * m.pitch, m.pitch, c.X);
-        R = 2;
-      } else {
-        acc = dot_rows<L, 1>(stage + (size_t)g * m.pitch, m.pitch, c.X);
-        R = 1;
-      }
-      const uint32_t row = r0 + g + lane;
+    // this warp's pairs: wi, wi + wgroup, ... taken two at a time (up to four rows)
+    const uint32_t wg = p.wgroup;
+    for (uint32_t pq = wi; pq < npairs; pq += 2 * wg) {
+      // rows of pair pq, then of pair pq + wg; only the last pair of a stage can be single
+      const uint32_t R = min(2 * pq + 2, nr) - 2 * pq + (pq + wg < npairs ? min(2 * (pq + wg) + 2, nr) - 2 * (pq + wg) : 0);
+      const unsigned long long acc = dot_rows_n<L, kMixed>(R, stage, pq, wg, m.pitch, c.X, pg, p.lcap);
+      const uint32_t row = r0 + stage_row(pq, wg, lane < 4 ? (uint32_t)lane : 0u);
       const bool valid = (uint32_t)lane < R;
       int64_t y = 0;
       if (valid) {
-        const unsigned long long t = (acc - (S << 7)) * (unsigned long long)__ldg(m.scale + row);
+        const unsigned long long t = (acc - (S << 7)) * (unsigned long long)sh.scales[row - sh.rb];
         y = (int64_t)t >> 24;
       }
-      epilogue(c, m, layer, row, valid, y, best);
-      g += R;
+      epilogue(c, m, layer, row, valid, y, best, sh.rope);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&c.empty[slot]);
@@ -694,15 +847,16 @@ __device__ void consumers(const Ctx& c, Shared& sh) {
       const MR m = matrow_of(c, l < p.layers ? l : 0, kind);
       unsigned long long S;
       const int L = prologue(c, m, sh, &S);
+      const bool mixed = (uint32_t)L > p.lcap;
       switch (L) {
-        case 1: consume_phase<1>(c, m, l, S, gs, sh, best); break;
-        case 2: consume_phase<2>(c, m, l, S, gs, sh, best); break;
-        case 3: consume_phase<3>(c, m, l, S, gs, sh, best); break;
-        case 4: consume_phase<4>(c, m, l, S, gs, sh, best); break;
-        case 5: consume_phase<5>(c, m, l, S, gs, sh, best); break;
-        case 6: consume_phase<6>(c, m, l, S, gs, sh, best); break;
-        case 7: consume_phase<7>(c, m, l, S, gs, sh, best); break;
-        default: consume_phase<8>(c, m, l, S, gs, sh, best); break;
+        case 1: consume_phase<1, false>(c, m, l, S, gs, sh, best); break;
+        case 2: consume_phase<2, false>(c, m, l, S, gs, sh, best); break;
+        case 3: consume_phase<3, false>(c, m, l, S, gs, sh, best); break;
+        case 4: consume_phase<4, false>(c, m, l, S, gs, sh, best); break;
+        case 5: mixed ? consume_phase<5, true>(c, m, l, S, gs, sh, best) : consume_phase<5, false>(c, m, l, S, gs, sh, best); break;
+        case 6: mixed ? consume_phase<6, true>(c, m, l, S, gs, sh, best) : consume_phase<6, false>(c, m, l, S, gs, sh, best); break;
+        case 7: mixed ? consume_phase<7, true>(c, m, l, S, gs, sh, best) : consume_phase<7, false>(c, m, l, S, gs, sh, best); break;
+        default: mixed ? consume_phase<8, true>(c, m, l, S, gs, sh, best) : consume_phase<8, false>(c, m, l, S, gs, sh, best); break;
       }
       gs += phase_stages(c, m);
       consumer_bar();  // a warp that gave up returns early: leave together
@@ -801,7 +955,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepParams p) {
     sh.abort = 0;
     for (uint32_t s = 0; s < p.ns; ++s) {
       mbar_init(&c.full[s], 1);
-      mbar_init(&c.empty[s], 1);
+      mbar_init(&c.empty[s], p.wgroup);  // every warp of the owning group releases the slot
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -871,7 +1025,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step_noalloc(const StepParams p
     sh.abort = 0;
     for (uint32_t s = 0; s < p.ns; ++s) {
       mbar_init(&c.full[s], 1);
-      mbar_init(&c.empty[s], 1);
+      mbar_init(&c.empty[s], p.wgroup);  // every warp of the owning group releases the slot
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
