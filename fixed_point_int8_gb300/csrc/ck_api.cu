@@ -5,6 +5,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <thread>
 #include <vector>
 
 #include "ck_internal.cuh"
@@ -29,6 +30,7 @@ struct ck_model {
   DevLayer* dev_layers;  // the layer table in device memory (read by the one-position kernel)
   int path;              // CK_PATH_*
   uint32_t max_slots;    // cap on the one-position kernel's ring slots (0: as many as fit)
+  uint32_t att_full;     // positions every block of a head scores itself (0: default)
   int smem_optin;        // largest shared memory a block may opt into
   size_t step_smem;      // dynamic shared memory available to the one-position kernel
   std::vector<DevLayer> layers;
@@ -49,7 +51,6 @@ constexpr uint32_t kTable = 4097;
 
 uint32_t rd32(const uint8_t* p) { uint32_t v; memcpy(&v, p, 4); return v; }
 uint64_t rd64(const uint8_t* p) { uint64_t v; memcpy(&v, p, 8); return v; }
-uint32_t pad16(uint32_t n) { return (n + 15u) & ~15u; }
 
 int check_config(const ck_config& c) {
   if (!c.dim || !c.hidden || !c.layers || !c.heads || !c.kv_heads || !c.vocab || !c.context)
@@ -109,7 +110,7 @@ struct DevPlan {
 
 DevPlan plan_device(const ck_config& c, bool tied) {
   DevPlan P;
-  const uint64_t pd = pad16(c.dim), ph = pad16(c.hidden), hd = c.dim / c.heads;
+  const uint64_t pd = pad128(c.dim), ph = pad128(c.hidden), hd = c.dim / c.heads;
   const uint64_t kv = hd * c.kv_heads;
   uint64_t off = 0;
   auto take = [&](uint64_t bytes) { uint64_t o = off; off = align256(off + bytes); return o; };
@@ -149,12 +150,46 @@ DevPlan plan_device(const ck_config& c, bool tied) {
 
 inline cudaStream_t S(void* s) { return static_cast<cudaStream_t>(s); }
 
-// Copies rows x cols bytes (source pitch cols) to a destination with pitch dpitch.
-cudaError_t copy_rows(uint8_t* dst, size_t dpitch, const uint8_t* src, size_t cols, size_t rows,
-                      cudaStream_t s) {
-  if (!rows || !cols) return cudaSuccess;
-  if (dpitch == cols) return cudaMemcpyAsync(dst, src, rows * cols, cudaMemcpyHostToDevice, s);
-  return cudaMemcpy2DAsync(dst, dpitch, src, cols, cols, rows, cudaMemcpyHostToDevice, s);
+// Uploads a matrix of `rows` rows of `cols` bytes (row r at row_ptr(r)) to dst in
+// column-group layout with `pitch` columns (a multiple of 128; padding bytes zero).  The
+// host reorders into `stage` with a few threads, then one copy; a copy from pageable
+// memory returns once the bytes are staged, so the buffer may be reused right after.
+template <typename RowFn>
+cudaError_t upload_grouped(uint8_t* dst, uint32_t rows, uint32_t cols, uint32_t pitch, RowFn row_ptr,
+                           std::vector<uint8_t>& stage, cudaStream_t s) {
+  if (!rows) return cudaSuccess;
+  const size_t bytes = (size_t)rows * pitch;
+  if (stage.size() < bytes) stage.resize(bytes);
+  uint8_t* out = stage.data();
+  const uint32_t groups = pitch / kGroupCols;
+  auto work = [&](uint32_t r0, uint32_t r1) {
+    for (uint32_t r = r0; r < r1; ++r) {
+      const uint8_t* src = row_ptr(r);
+      for (uint32_t g = 0; g < groups; ++g) {
+        uint8_t* d = out + ((size_t)g * rows + r) * kGroupCols;
+        for (uint32_t j = 0; j < 8; ++j) {
+          const uint32_t col = g * kGroupCols + 16 * j;
+          uint8_t* chunk = d + ((j ^ (r & 7u)) << 4);
+          const uint32_t n = col >= cols ? 0u : (cols - col < 16 ? cols - col : 16u);
+          if (n) memcpy(chunk, src + col, n);
+          if (n < 16) memset(chunk + n, 0, 16 - n);
+        }
+      }
+    }
+  };
+  unsigned nt = std::thread::hardware_concurrency();
+  if (nt < 1) nt = 1;
+  if (nt > 16) nt = 16;
+  if ((size_t)rows * pitch < (1u << 22) || rows < nt) nt = 1;
+  if (nt == 1) {
+    work(0, rows);
+  } else {
+    std::vector<std::thread> th;
+    for (unsigned t = 0; t < nt; ++t)
+      th.emplace_back(work, (uint32_t)((uint64_t)rows * t / nt), (uint32_t)((uint64_t)rows * (t + 1) / nt));
+    for (auto& t : th) t.join();
+  }
+  return cudaMemcpyAsync(dst, out, bytes, cudaMemcpyHostToDevice, s);
 }
 
 // ------------------------------------------------------------------ small kernels
@@ -174,10 +209,10 @@ __global__ void k_embed(uint8_t* st, uint64_t off_prompt, uint64_t off_out, int6
     }
     return;
   }
-  const uint8_t* row = embed + (size_t)tok * pitch;
+  (void)pitch;
   const int64_t s = (int64_t)__ldg(scale + tok);
   for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < dim; i += gridDim.x * blockDim.x)
-    x[i] = ((int64_t)row[i] - 128) * s >> 8;
+    x[i] = ((int64_t)embed[grouped_offset(vocab, tok, i)] - 128) * s >> 8;
 }
 
 // End of a prompt position: the last residual (x = xb + y), then the cursor moves on, or
@@ -344,6 +379,7 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
     MatrowParams p = {};
     p.W = W.wqkv;
     p.scale = W.sqkv;
+    p.grouped = 1;
     p.pitch = m->pitch_d;
     p.rows = c.dim + 2 * m->kv_dim;
     p.cols = c.dim;
@@ -388,6 +424,7 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
     MatrowParams po = {};
     po.W = W.wo;
     po.scale = W.so;
+    po.grouped = 1;
     po.pitch = m->pitch_d;
     po.rows = c.dim;
     po.cols = c.dim;
@@ -402,6 +439,7 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
     MatrowParams pg = {};
     pg.W = W.w13;
     pg.scale = W.s13;
+    pg.grouped = 1;
     pg.pitch = m->pitch_d;
     pg.rows = 2 * c.hidden;
     pg.cols = c.dim;
@@ -420,6 +458,7 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
     MatrowParams pd = {};
     pd.W = W.w2;
     pd.scale = W.s2;
+    pd.grouped = 1;
     pd.pitch = m->pitch_h;
     pd.rows = c.dim;
     pd.cols = c.hidden;
@@ -436,6 +475,7 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
     MatrowParams pc = {};
     pc.W = m->cls;
     pc.scale = m->cls_scale;
+    pc.grouped = 1;
     pc.pitch = m->pitch_d;
     pc.rows = c.vocab;
     pc.cols = c.dim;
@@ -460,34 +500,44 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
 // outside what it supports (then the phase-by-phase kernels run instead).
 bool plan_step(const ck_model* m, const StateLayout& lay, StepParams* sp, int* grid, size_t* smem) {
   const ck_config& c = m->cfg;
-  if (m->pitch_d > kStageBytes / 2 || m->pitch_h > kStageBytes || c.heads > 1000) return false;
+  if (c.heads > 1000) return false;
   const int G = m->num_sms < 768 ? m->num_sms : 768;
   const uint32_t gh = c.heads >= (uint32_t)G ? 1u : (uint32_t)G / c.heads;
   if (c.heads * gh > (uint32_t)G) return false;
-  const uint32_t chunk = (lay.cache + gh - 1) / gh;
-  const uint64_t attn = 8ull * ((uint64_t)m->head_dim * (1 + step_consumer_warps()) +
-                                step_consumer_warps() + chunk);
-  const uint64_t max_pitch = m->pitch_d > m->pitch_h ? m->pitch_d : m->pitch_h;
-  // planes of all eight limbs in shared memory when they are small; otherwise four there and
-  // limbs 4..7 (vectors beyond 32 bits, rare) in a global copy in the work region
-  const uint32_t lcap = 8 * max_pitch <= 48 * 1024 ? 8u : 4u;
-  const uint64_t planes = (uint64_t)lcap * max_pitch;
+  const uint64_t hd = m->head_dim;
+  // attention: every CTA of a head scores all positions up to att_full (the head's keys are
+  // then read by each of its CTAs, from L2 after the first); beyond, the scoring is split
+  const uint32_t att_def = m->att_full ? m->att_full : (uint32_t)(16384 / hd);
+  const uint32_t att_full = gh == 1 ? lay.cache : std::min<uint32_t>(lay.cache, att_def);
+  const uint64_t chunk = (lay.cache + gh - 1) / gh;
+  const uint64_t nscore = std::max<uint64_t>(chunk, att_full);
+  const uint64_t attn = 8ull * (hd * (1 + kStepWarps) + kStepWarps + nscore);
+  const uint64_t max_pitch = std::max(m->pitch_d, m->pitch_h);
+  // byte planes in shared memory: at least four limbs of the widest input, eight of a
+  // dim-wide one when they fit in 48 KB; planes beyond go to a global copy (rare)
+  const uint64_t planes = std::max<uint64_t>(4 * max_pitch, std::min<uint64_t>(8ull * m->pitch_d, 48 * 1024));
   // most rows a block takes in one matrix (whole pairs split over the grid), plus slack
   const uint64_t max_rows = std::max<uint64_t>(
       std::max<uint64_t>((uint64_t)c.dim + 2 * (uint64_t)m->kv_dim, 2 * (uint64_t)c.hidden),
       std::max<uint64_t>((uint64_t)c.dim, (uint64_t)c.vocab));
   const uint64_t scale_cap = 2 * (((max_rows + 1) / 2 + G - 1) / G) + 2;
-  const uint64_t xb = (std::max<uint64_t>(attn, planes + 4 * scale_cap + 4 * (uint64_t)m->head_dim) + 15) & ~15ull;
+  const uint64_t xb = (std::max<uint64_t>(attn, planes + 4 * scale_cap + 4 * hd) + 15) & ~15ull;
+  const uint64_t red = (uint64_t)step_red_bytes();
   const uint64_t avail = (uint64_t)m->step_smem;
-  if (avail < xb + 2 * (kStageBytes + 16)) return false;
-  uint64_t ns = (avail - xb) / (kStageBytes + 16);
+  if (avail < xb + red + 2 * (kStageBytes + 16)) return false;
+  uint64_t ns = (avail - xb - red) / (kStageBytes + 16);
   if (ns > 8) ns = 8;
   if (m->max_slots && ns > m->max_slots) ns = m->max_slots;
   if (ns < 2) return false;
-  // work region: counters and attention partials, per-block candidates, global planes
-  const uint64_t off_gplanes = (4096 + 8ull * c.heads * gh * (m->head_dim + 2) + 16ull * G + 255) & ~255ull;
+  // work region: counters, attention maxima and sums, classifier candidates, attention
+  // accumulators, global planes
+  const uint64_t off_part = 4096;
+  const uint64_t off_cand = off_part + 16ull * c.heads * gh;
+  const uint64_t off_oacc = (off_cand + 16ull * G + 255) & ~255ull;
+  const uint64_t off_gplanes = (off_oacc + 8ull * c.dim + 255) & ~255ull;
+  const uint64_t lcap_min = std::min<uint64_t>(8, planes / max_pitch);
   const uint64_t work_bytes = lay.k - lay.scores;
-  if (off_gplanes + (8 - lcap) * max_pitch > work_bytes) return false;
+  if (off_gplanes + (8 - lcap_min) * max_pitch > work_bytes) return false;
   StepParams& p = *sp;
   p = StepParams{};
   p.off_prompt = lay.prompt; p.off_out = lay.out; p.off_x = lay.x; p.off_xb = lay.xb; p.off_q = lay.q;
@@ -497,13 +547,10 @@ bool plan_step(const ck_model* m, const StateLayout& lay, StepParams* sp, int* g
   p.dim = c.dim; p.hidden = c.hidden; p.layers = c.layers; p.heads = c.heads; p.kv_heads = c.kv_heads;
   p.vocab = c.vocab; p.hd = m->head_dim; p.kv_dim = m->kv_dim; p.pitch_d = m->pitch_d;
   p.pitch_h = m->pitch_h; p.inv_sqrt = m->inv_sqrt;
-  p.gh = gh; p.ns = (uint32_t)ns; p.x_bytes = (uint32_t)xb;
+  p.gh = gh; p.att_full = att_full; p.ns = (uint32_t)ns; p.x_bytes = (uint32_t)xb;
+  p.owners = std::min<uint32_t>(kStepWarps, (uint32_t)ns);
   p.planes_bytes = (uint32_t)planes;
-  p.lcap = lcap;
-  p.off_gplanes = off_gplanes;
-  // warp groups: groups <= slots (parity rule), two slots beyond the groups stay in flight
-  p.ngroups = ns >= 6 ? 4u : (ns >= 4 ? (uint32_t)ns - 2 : 1u);
-  p.wgroup = (uint32_t)step_consumer_warps() / p.ngroups;
+  p.off_part = off_part; p.off_cand = off_cand; p.off_oacc = off_oacc; p.off_gplanes = off_gplanes;
   p.scale_cap = (uint32_t)scale_cap;
   p.div_dim = make_invdiv(c.dim);
   p.div_hidden = make_invdiv(c.hidden);
@@ -511,8 +558,15 @@ bool plan_step(const ck_model* m, const StateLayout& lay, StepParams* sp, int* g
   p.embed = m->embed; p.embed_scale = m->embed_scale; p.cls = m->cls; p.cls_scale = m->cls_scale;
   p.final_norm = m->final_norm; p.rope = m->rope; p.exp_tab = m->exp_tab; p.silu_tab = m->silu_tab;
   *grid = G;
-  *smem = xb + ns * kStageBytes + 16 * ns;
+  *smem = xb + red + ns * kStageBytes + 16 * ns;
   return step_blocks_per_sm(*smem) >= 1;  // every block must be resident for the grid barriers
+}
+
+// Bytes of the work region the one-position kernel uses for a plan.
+size_t step_work_bytes(const StepParams& p) {
+  const uint64_t max_pitch = std::max(p.pitch_d, p.pitch_h);
+  const uint64_t lcap_min = std::min<uint64_t>(8, p.planes_bytes / max_pitch);
+  return p.off_gplanes + (8 - lcap_min) * max_pitch;
 }
 
 int enqueue_step(const ck_model* m, uint8_t* st, const StateLayout& lay, bool generating,
@@ -609,14 +663,19 @@ int ck_load_model(const void* artifact, size_t len, void* dev_mem, size_t dev_le
   if (dev_len < D.total) return CK_BUFFER_TOO_SMALL;
   cudaStream_t s = S(stream);
   uint8_t* dv = static_cast<uint8_t*>(dev_mem);
-  const uint32_t pd = pad16(c.dim), ph = pad16(c.hidden), hd = c.dim / c.heads;
+  const uint32_t pd = pad128(c.dim), ph = pad128(c.hidden), hd = c.dim / c.heads;
   const uint32_t kv = hd * c.kv_heads;
   CK_CUDA(cudaMemsetAsync(dv, 0, D.total, s));
   auto T = [&](uint32_t i) { return P.t[i]; };
-  CK_CUDA(copy_rows(dv + D.embed, pd, T(0), c.dim, c.vocab, s));
+  std::vector<uint8_t> stage;
+  // a row-major source matrix of `cols`-byte rows
+  auto plain = [](const uint8_t* base, uint32_t cols) {
+    return [base, cols](uint32_t r) { return base + (size_t)r * cols; };
+  };
+  CK_CUDA(upload_grouped(dv + D.embed, c.vocab, c.dim, pd, plain(T(0), c.dim), stage, s));
   CK_CUDA(cudaMemcpyAsync(dv + D.embed_scale, T(1), 4ull * c.vocab, cudaMemcpyHostToDevice, s));
   if (!tied) {
-    CK_CUDA(copy_rows(dv + D.cls, pd, T(3), c.dim, c.vocab, s));
+    CK_CUDA(upload_grouped(dv + D.cls, c.vocab, c.dim, pd, plain(T(3), c.dim), stage, s));
     CK_CUDA(cudaMemcpyAsync(dv + D.cls_scale, T(4), 4ull * c.vocab, cudaMemcpyHostToDevice, s));
   }
   CK_CUDA(cudaMemcpyAsync(dv + D.final_norm, T(2), 4ull * c.dim, cudaMemcpyHostToDevice, s));
@@ -627,24 +686,31 @@ int ck_load_model(const void* artifact, size_t len, void* dev_mem, size_t dev_le
     const DevPlan::L& L = D.layers[l];
     const uint32_t b = 8 + 16 * l;
     CK_CUDA(cudaMemcpyAsync(dv + L.an, T(b + 0), 4ull * c.dim, cudaMemcpyHostToDevice, s));
-    CK_CUDA(copy_rows(dv + L.wqkv, pd, T(b + 1), c.dim, c.dim, s));
+    // Q rows, then K rows, then V rows as one matrix
+    const uint8_t *wq = T(b + 1), *wk = T(b + 3), *wv = T(b + 5);
+    const uint32_t dim = c.dim;
+    CK_CUDA(upload_grouped(dv + L.wqkv, c.dim + 2 * kv, c.dim, pd,
+                           [=](uint32_t r) {
+                             return r < dim ? wq + (size_t)r * dim
+                                            : r < dim + kv ? wk + (size_t)(r - dim) * dim
+                                                           : wv + (size_t)(r - dim - kv) * dim;
+                           },
+                           stage, s));
     CK_CUDA(cudaMemcpyAsync(dv + L.sqkv, T(b + 2), 4ull * c.dim, cudaMemcpyHostToDevice, s));
-    CK_CUDA(copy_rows(dv + L.wqkv + (size_t)c.dim * pd, pd, T(b + 3), c.dim, kv, s));
     CK_CUDA(cudaMemcpyAsync(dv + L.sqkv + 4ull * c.dim, T(b + 4), 4ull * kv, cudaMemcpyHostToDevice, s));
-    CK_CUDA(copy_rows(dv + L.wqkv + (size_t)(c.dim + kv) * pd, pd, T(b + 5), c.dim, kv, s));
     CK_CUDA(cudaMemcpyAsync(dv + L.sqkv + 4ull * (c.dim + kv), T(b + 6), 4ull * kv,
                             cudaMemcpyHostToDevice, s));
-    CK_CUDA(copy_rows(dv + L.wo, pd, T(b + 7), c.dim, c.dim, s));
+    CK_CUDA(upload_grouped(dv + L.wo, c.dim, c.dim, pd, plain(T(b + 7), c.dim), stage, s));
     CK_CUDA(cudaMemcpyAsync(dv + L.so, T(b + 8), 4ull * c.dim, cudaMemcpyHostToDevice, s));
     CK_CUDA(cudaMemcpyAsync(dv + L.fn, T(b + 9), 4ull * c.dim, cudaMemcpyHostToDevice, s));
     // gate rows to even rows, up rows to odd rows (and their scales likewise)
-    CK_CUDA(cudaMemcpy2DAsync(dv + L.w13, 2ull * pd, T(b + 10), c.dim, c.dim, c.hidden,
-                              cudaMemcpyHostToDevice, s));
-    CK_CUDA(cudaMemcpy2DAsync(dv + L.w13 + pd, 2ull * pd, T(b + 12), c.dim, c.dim, c.hidden,
-                              cudaMemcpyHostToDevice, s));
+    const uint8_t *wg = T(b + 10), *wu = T(b + 12);
+    CK_CUDA(upload_grouped(dv + L.w13, 2 * c.hidden, c.dim, pd,
+                           [=](uint32_t r) { return ((r & 1) ? wu : wg) + (size_t)(r >> 1) * dim; },
+                           stage, s));
     CK_CUDA(cudaMemcpy2DAsync(dv + L.s13, 8, T(b + 11), 4, 4, c.hidden, cudaMemcpyHostToDevice, s));
     CK_CUDA(cudaMemcpy2DAsync(dv + L.s13 + 4, 8, T(b + 13), 4, 4, c.hidden, cudaMemcpyHostToDevice, s));
-    CK_CUDA(copy_rows(dv + L.w2, ph, T(b + 14), c.hidden, c.dim, s));
+    CK_CUDA(upload_grouped(dv + L.w2, c.dim, c.hidden, ph, plain(T(b + 14), c.hidden), stage, s));
     CK_CUDA(cudaMemcpyAsync(dv + L.s2, T(b + 15), 4ull * c.dim, cudaMemcpyHostToDevice, s));
   }
   CK_CUDA(cudaStreamSynchronize(s));
@@ -687,6 +753,7 @@ int ck_load_model(const void* artifact, size_t len, void* dev_mem, size_t dev_le
   m->dev_layers = reinterpret_cast<DevLayer*>(dv + D.table);
   m->path = CK_PATH_AUTO;
   m->max_slots = 0;
+  m->att_full = 0;
   if (cudaMemcpyAsync(m->dev_layers, m->layers.data(), sizeof(DevLayer) * c.layers,
                       cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess) {
@@ -720,6 +787,14 @@ int ck_set_step_slots(ck_model* m, uint32_t max_slots) {
   if (!m || max_slots == 1 || max_slots > 8) return CK_INVALID_ARGUMENT;
   m->max_slots = max_slots;
   for (auto& g : m->graphs) cudaGraphExecDestroy(g.exec);  // plans change: rebuild graphs
+  m->graphs.clear();
+  return CK_OK;
+}
+
+int ck_set_attention_split(ck_model* m, uint32_t positions) {
+  if (!m) return CK_INVALID_ARGUMENT;
+  m->att_full = positions;
+  for (auto& g : m->graphs) cudaGraphExecDestroy(g.exec);
   m->graphs.clear();
   return CK_OK;
 }
@@ -846,8 +921,9 @@ int ck_turn_noalloc(ck_model* m, void* dev_state, size_t len, void* stream, ck_t
   int grid;
   size_t smem;
   if (!plan_step(m, lay, &p, &grid, &smem)) return CK_INVALID_ARGUMENT;
-  // scratch this position needs: counters, per-(head, chunk) partials, per-block candidates
-  const size_t need = p.off_gplanes + (8 - p.lcap) * (size_t)std::max(p.pitch_d, p.pitch_h);
+  // scratch this position needs: counters, attention partials and accumulators, per-block
+  // candidates, global planes
+  const size_t need = step_work_bytes(p);
   if (need > noalloc_work_bytes()) return CK_INVALID_ARGUMENT;
   uint8_t* work = nullptr;
   CK_CUDA(noalloc_setup(m->step_smem, &work));
@@ -961,6 +1037,7 @@ int ck_matrow(const uint8_t* dev_W, size_t pitch, const uint32_t* dev_scale, uin
   MatrowParams p = {};
   p.W = dev_W;
   p.scale = dev_scale;
+  p.grouped = 0;
   p.pitch = (uint32_t)pitch;
   p.rows = rows;
   p.cols = cols;

@@ -179,6 +179,23 @@ __device__ __forceinline__ void rotate_pair(int64_t a, int64_t b, int32_t c, int
 
 // ------------------------------------------------------------------ device model
 
+// Device layout of every model matrix ("column groups").  Rows are padded with zero bytes to
+// a multiple of 128 columns, and the columns are cut into groups of 128.  Group g holds, row
+// after row, each row's 128 bytes of that group; within them, the row's 16-byte chunk j
+// (columns 128g + 16j ..) sits at position j ^ (row & 7).  A block of consecutive rows of
+// one group is one contiguous run of memory, so a CTA can copy a rectangle of rows x 128
+// columns with one bulk copy, and the rotation of the chunks by the row index lets 32 lanes
+// that read the same column chunk of 32 consecutive rows from shared memory hit all banks.
+constexpr uint32_t kGroupCols = 128;
+
+__host__ __device__ inline uint32_t pad128(uint32_t n) { return (n + 127u) & ~127u; }
+
+// Byte offset of (row r, column c) in a matrix of `rows` rows in column-group layout.
+__host__ __device__ inline uint64_t grouped_offset(uint32_t rows, uint32_t r, uint32_t c) {
+  const uint32_t g = c >> 7, j = (c >> 4) & 7u;
+  return ((uint64_t)g * rows + r) * kGroupCols + ((j ^ (r & 7u)) << 4) + (c & 15u);
+}
+
 struct DevLayer {
   const uint8_t* wqkv;   // [dim + 2 kv_dim][pitch_d]: Wq rows, then Wk, then Wv
   const uint32_t* sqkv;
@@ -200,7 +217,8 @@ enum Epilogue : int { kEpiStore = 0, kEpiQKV = 1, kEpiSiLU = 2 };
 struct MatrowParams {
   const uint8_t* W;
   const uint32_t* scale;
-  uint32_t pitch;        // bytes per row, multiple of 16
+  uint32_t grouped;      // 1: W in column-group layout (model matrices); 0: row-major
+  uint32_t pitch;        // bytes per row, multiple of 16 (of 128 when grouped)
   uint32_t rows, cols;
   // prologue: the input vector of `cols` elements
   int pro;
@@ -230,7 +248,9 @@ struct AttnParams {
 };
 
 // The persistent one-position kernel (ck_step.cu).
-constexpr uint32_t kStageBytes = 24576;  // one ring slot: whole rows of one matrix
+constexpr uint32_t kStageBytes = 24576;  // one ring slot: column groups of one row panel
+constexpr uint32_t kPanelRows = 96;      // most rows of one panel (three a lane)
+constexpr uint32_t kStepWarps = 8;       // consumer warps
 
 struct StepParams {
   uint8_t* st;
@@ -240,12 +260,16 @@ struct StepParams {
   uint32_t dim, hidden, layers, heads, kv_heads, vocab, hd, kv_dim, pitch_d, pitch_h, inv_sqrt;
   uint32_t generating;  // run phases 17-19 after the layers
   uint32_t gh;          // CTAs per attention head
+  uint32_t att_full;    // up to this many positions every CTA of a head scores all of them
   uint32_t ns;          // ring slots
+  uint32_t owners;      // consumer warps that take ring stages in turn (<= ns)
   uint32_t x_bytes;     // planes, row scales and rotary row / attention region
-  uint32_t planes_bytes;  // lcap * the largest padded row (planes kept in shared memory)
-  uint32_t lcap;          // limbs whose planes fit shared memory (4 or 8); more go to global
-  uint32_t ngroups, wgroup;  // consumer warp groups and warps per group
-  uint64_t off_gplanes;   // global planes lcap..7, from the work region start
+  uint32_t planes_bytes;  // shared memory for byte planes; a phase keeps
+                          // min(8, planes_bytes / pitch) planes there, the rest in global
+  uint64_t off_part;    // from the work region start: attention maxima and sums [heads*gh][2]
+  uint64_t off_cand;    // classifier candidates [grid][2]
+  uint64_t off_oacc;    // attention output accumulators [dim] (u64, before the >> 24)
+  uint64_t off_gplanes; // global byte planes of limbs beyond the shared-memory ones
   uint32_t scale_cap;   // most rows any block takes in one matrix
   InvDiv div_dim, div_hidden;  // for the mean of squares
   const DevLayer* layers_tab;
@@ -267,6 +291,7 @@ cudaError_t noalloc_setup(size_t dynamic_max, uint8_t** work);
 cudaError_t launch_step_noalloc(const StepParams& p, uint8_t* work, cudaStream_t s, int grid, size_t smem);
 int step_blocks_per_sm(size_t smem);
 int step_consumer_warps();
+size_t step_red_bytes();
 
 // Launchers (stream-ordered; return a cudaError_t).
 cudaError_t configure_matrow();     // once per process and device, outside stream capture

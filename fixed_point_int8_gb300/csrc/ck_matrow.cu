@@ -166,7 +166,9 @@ __device__ __forceinline__ void epilogue(const MatrowParams& p, uint32_t row, in
   }
 }
 
-template <int L>
+// Rows of W: row-major with the given pitch, or (kGrouped) the model's column-group layout,
+// where the 16-byte chunk at column c of row r sits at grouped_offset(rows, r, c).
+template <int L, bool kGrouped>
 __device__ void rows_loop(const MatrowParams& p, const uint8_t* planes, unsigned long long S,
                           uint32_t pos) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -176,8 +178,14 @@ __device__ void rows_loop(const MatrowParams& p, const uint8_t* planes, unsigned
   for (uint32_t g = blockIdx.x * kWarps + warp; g < groups; g += nw) {
     const uint32_t r0 = g * kR;
     const uint8_t* wrow[kR];
+    uint32_t rsw[kR];  // grouped: the row's chunk rotation, (row & 7) << 4
 #pragma unroll
-    for (int r = 0; r < kR; ++r) wrow[r] = p.W + (size_t)min(r0 + r, p.rows - 1) * pitch;
+    for (int r = 0; r < kR; ++r) {
+      const uint32_t row = min(r0 + r, p.rows - 1);
+      wrow[r] = kGrouped ? p.W + (size_t)row * kGroupCols : p.W + (size_t)row * pitch;
+      rsw[r] = (row & 7u) << 4;
+    }
+    const size_t gstride = (size_t)p.rows * kGroupCols;  // grouped: bytes between column groups
     uint32_t acc[kR][L];
 #pragma unroll
     for (int r = 0; r < kR; ++r)
@@ -185,8 +193,15 @@ __device__ void rows_loop(const MatrowParams& p, const uint8_t* planes, unsigned
       for (int k = 0; k < L; ++k) acc[r][k] = 0;
     for (uint32_t c = lane * 16; c < pitch; c += 512) {
       uint4 w[kR];
+      if (kGrouped) {
+        const size_t gbase = (size_t)(c >> 7) * gstride;
+        const uint32_t chunk = c & 0x70u;
 #pragma unroll
-      for (int r = 0; r < kR; ++r) w[r] = ld_stream16(wrow[r] + c);
+        for (int r = 0; r < kR; ++r) w[r] = ld_stream16(wrow[r] + gbase + (chunk ^ rsw[r]));
+      } else {
+#pragma unroll
+        for (int r = 0; r < kR; ++r) w[r] = ld_stream16(wrow[r] + c);
+      }
 #pragma unroll
       for (int k = 0; k < L; ++k) {
         const uint4 xk = *reinterpret_cast<const uint4*>(planes + (size_t)k * pitch + c);
@@ -244,15 +259,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_matrow(const MatrowParams p) {
   Scratch* sc = reinterpret_cast<Scratch*>(smem + 8 * (size_t)p.pitch);
   unsigned long long S;
   const int L = prologue(p, reinterpret_cast<uint32_t*>(planes), sc, &S);
-  switch (L) {
-    case 1: rows_loop<1>(p, planes, S, pos); break;
-    case 2: rows_loop<2>(p, planes, S, pos); break;
-    case 3: rows_loop<3>(p, planes, S, pos); break;
-    case 4: rows_loop<4>(p, planes, S, pos); break;
-    case 5: rows_loop<5>(p, planes, S, pos); break;
-    case 6: rows_loop<6>(p, planes, S, pos); break;
-    case 7: rows_loop<7>(p, planes, S, pos); break;
-    default: rows_loop<8>(p, planes, S, pos); break;
+  if (p.grouped) {
+    switch (L) {
+      case 1: rows_loop<1, true>(p, planes, S, pos); break;
+      case 2: rows_loop<2, true>(p, planes, S, pos); break;
+      case 3: rows_loop<3, true>(p, planes, S, pos); break;
+      case 4: rows_loop<4, true>(p, planes, S, pos); break;
+      case 5: rows_loop<5, true>(p, planes, S, pos); break;
+      case 6: rows_loop<6, true>(p, planes, S, pos); break;
+      case 7: rows_loop<7, true>(p, planes, S, pos); break;
+      default: rows_loop<8, true>(p, planes, S, pos); break;
+    }
+  } else {
+    switch (L) {
+      case 1: rows_loop<1, false>(p, planes, S, pos); break;
+      case 2: rows_loop<2, false>(p, planes, S, pos); break;
+      case 3: rows_loop<3, false>(p, planes, S, pos); break;
+      case 4: rows_loop<4, false>(p, planes, S, pos); break;
+      case 5: rows_loop<5, false>(p, planes, S, pos); break;
+      case 6: rows_loop<6, false>(p, planes, S, pos); break;
+      case 7: rows_loop<7, false>(p, planes, S, pos); break;
+      default: rows_loop<8, false>(p, planes, S, pos); break;
+    }
   }
 }
 

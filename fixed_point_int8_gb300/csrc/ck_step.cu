@@ -1,19 +1,27 @@
 // One position of the forward pass ("The inference core", "The forward pass, in order") as
 // one persistent kernel: one CTA per SM, launched cooperatively so every CTA is resident.
 //
-// GB300 design.  Each CTA owns a contiguous slice of the rows of every matrix of the step.
-// A producer warp streams those slices, matrix after matrix and layer after layer, through
-// a ring of shared-memory slots with cp.async.bulk copies completing on mbarriers; it never
-// waits for activations, only for free slots, so HBM keeps streaming across phase
-// boundaries.  Eight consumer warps own ring stages round-robin; for each matrix they pack
-// the phase's input vector into byte planes (after the residual and the RMS
-// normalization where the phase has them), run the dp4a matrix-row loop on the staged rows
-// and apply the fused epilogue.  Phases that depend on each other are separated by a grid
-// barrier among the consumer warps.  Attention splits each head's positions over a few
-// CTAs that exchange their maxima, sums and partial weighted values through the state's
-// work area behind per-head group barriers.  Every wait is bounded: on a timeout the kernel
-// raises an abort flag, stops issuing copies, waits (bounded) for its copies in flight and
-// the state is marked failed with error 9.
+// GB300 design.  Each CTA owns a contiguous slice of the rows of every matrix of the step,
+// cut into panels of at most 96 rows.  The model's matrices sit in HBM in column-group
+// layout (rows of 128-byte groups), so one panel's rows of one column group are a single
+// contiguous run: a producer warp streams them, panel after panel, matrix after matrix and
+// layer after layer, through a ring of shared-memory slots with cp.async.bulk copies that
+// complete on mbarriers.  It never waits for activations, only for free slots, so HBM keeps
+// streaming across phase boundaries.
+//
+// Eight consumer warps take the ring's stages in turn.  Within a stage, lane l accumulates
+// rows l, l + 32, ... of the panel over all the stage's columns, so a lane holds whole dot
+// products and no shuffle reduction is needed: at the end of a panel the warps' partial
+// sums meet in shared memory and one thread per row runs the fused epilogue.  The dot products use byte planes of the input vector: the phase's prologue
+// (residual, RMS normalization) writes plane k = byte k of every element, and each row sum
+// is sum_k 2^(8k) sum_c byte[r][c] * plane_k[c], one dp4a per four bytes and limb.
+//
+// Phases that depend on each other are separated by a grid barrier among the consumer
+// warps.  Attention splits each head's positions over a few CTAs that add their weighted
+// values into 64-bit accumulators in the work area; the CTAs of a head exchange maxima and
+// sums only when the context is long enough to split the scoring.  Every wait is bounded:
+// on a timeout the kernel raises an abort flag, stops issuing copies, waits (bounded) for
+// its copies in flight and the state is marked failed with error 9.
 #include <climits>
 
 #include "ck_internal.cuh"
@@ -21,20 +29,23 @@
 namespace ck {
 namespace {
 
-constexpr int kNCW = 8;                 // consumer warps
+constexpr int kNCW = (int)kStepWarps;   // consumer warps
 constexpr int kCT = 32 * kNCW;          // consumer threads
 constexpr int kThreads = kCT + 32;      // plus one producer warp
 constexpr uint32_t kPollLimit = 1u << 22;
+constexpr int kRMax = (int)(kPanelRows / 32);  // rows a lane accumulates
+constexpr uint32_t kBlockElems = 16u * kCT;     // prologue: 16 consecutive elements a thread
 
-// work area offsets (bytes from the start of the state's scores/work region)
-constexpr uint32_t kWBar = 0, kWAbort = 4, kWHeads = 64, kWPart = 4096;  // [0, 4096) zeroed per launch
+// work area offsets (bytes from the start of the state's scores/work region); [0, 4096) is
+// zeroed before every launch
+constexpr uint32_t kWBar = 0, kWAbort = 4, kWHeads = 64;
 
-enum Pro : int { kPPlain = 0, kPNorm = 1, kPEmbedNorm = 2 };
+enum Pro : int { kPPlain = 0, kPNorm = 1, kPEmbedNorm = 2, kPAcc = 3 };
 enum Epi : int { kEStore = 0, kEQKV = 1, kESiLU = 2, kELogits = 3 };
 enum Kind : int { kQKV = 0, kATT = 1, kO = 2, kGU = 3, kDOWN = 4, kCLS = 5, kEND = 6 };
 
 struct MR {
-  const uint8_t* W;
+  const uint8_t* W;  // column-group layout
   const uint32_t* scale;
   uint32_t pitch, rows, cols;
   int pro;
@@ -49,13 +60,9 @@ struct MR {
 };
 
 struct Shared {
-  const uint32_t* scales;  // this block's row scales of the phase (shared memory)
-  const int32_t* rope;     // this position's (cos, sin) pairs (shared memory)
-  uint32_t rb;             // first row of this block in the phase
   unsigned long long ra[kNCW], rbuf[kNCW];
   long long am_v[kNCW];
   uint32_t am_i[kNCW];
-  InvDiv div;
   unsigned long long S, orv;
   int abort;
 };
@@ -96,83 +103,111 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
 }
 __device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"r"(kCT) : "memory"); }
 
-struct Ctx {
-  const StepParams* p;
-  uint8_t* st;
-  uint8_t* work;
-  uint32_t* gbar;
-  uint32_t* gabort;
-  uint8_t* ring;
-  uint8_t* X;
-  uint64_t* full;
-  uint64_t* empty;
-  uint32_t ns, pos, tok, G;
-};
+// Dynamic shared memory: the ring (ns slots), the X region (byte planes, row scales and
+// rotary row; attention reuses it), the partial row sums [kNCW][kPanelRows] and the ring's
+// full and empty mbarriers.  Everything below is addressed from the kernel's parameter
+// block and this symbol, so the compiler can re-derive addresses instead of keeping them
+// live across phases.
+extern __shared__ __align__(128) uint8_t smem[];
 
-__device__ __forceinline__ int64_t* st64(const Ctx& c, uint64_t off) {
-  return reinterpret_cast<int64_t*>(c.st + off);
+__device__ __forceinline__ uint8_t* ring_of() { return smem; }
+__device__ __forceinline__ uint8_t* xreg(const StepParams& p) { return smem + (size_t)p.ns * kStageBytes; }
+__device__ __forceinline__ unsigned long long* red_of(const StepParams& p) {
+  return reinterpret_cast<unsigned long long*>(xreg(p) + p.x_bytes);
+}
+__device__ __forceinline__ uint64_t* full_of(const StepParams& p) {
+  return reinterpret_cast<uint64_t*>(red_of(p) + kNCW * kPanelRows);
+}
+__device__ __forceinline__ uint64_t* empty_of(const StepParams& p) { return full_of(p) + p.ns; }
+
+// The position's own values: the scratch area (the state's work region, or the
+// allocation-free variant's array), the position and its token.
+struct Pos {
+  uint8_t* work;
+  uint32_t pos, tok;
+};
+__device__ __forceinline__ uint32_t* gbar_of(const Pos& q) { return reinterpret_cast<uint32_t*>(q.work + kWBar); }
+__device__ __forceinline__ uint32_t* gabort_of(const Pos& q) { return reinterpret_cast<uint32_t*>(q.work + kWAbort); }
+
+__device__ __forceinline__ int64_t* st64(const StepParams& p, uint64_t off) {
+  return reinterpret_cast<int64_t*>(p.st + off);
 }
 
-// The matrix-row phase of kind `k` in layer l (see the phase table in the design notes).
-__device__ MR matrow_of(const Ctx& c, uint32_t l, int k) {
-  const StepParams& p = *c.p;
+// The matrix-row phase of kind `k` in layer l:
+//   QKV   attention norm of x (+ y of the previous layer, the sum kept in x), Q/K/V rows,
+//         rotary on Q and K, checked cache stores of K and V
+//   O     the head outputs (accumulators >> 24) times Wo, into y
+//   GU    feed-forward norm of x + y (the sum kept in xb), gate and up rows, SiLU gating, h
+//   DOWN  h times W2, into y
+//   CLS   final norm of xb + y (the sum kept in x), the classifier rows into the logits
+__device__ __forceinline__ MR matrow_of(const StepParams& p, const Pos& q, uint32_t l, int k) {
   MR m = {};
   const DevLayer* W = p.layers_tab + l;
-  int64_t* x = st64(c, p.off_x);
-  int64_t* xb = st64(c, p.off_xb);
-  int64_t* y = st64(c, p.off_y);
+  int64_t* x = st64(p, p.off_x);
+  int64_t* xb = st64(p, p.off_xb);
+  int64_t* y = st64(p, p.off_y);
   if (k == kQKV) {
     m.W = W->wqkv; m.scale = W->sqkv; m.pitch = p.pitch_d; m.rows = p.dim + 2 * p.kv_dim; m.cols = p.dim;
     m.pro = l == 0 ? kPEmbedNorm : kPNorm;
     m.in = xb; m.add = l == 0 ? nullptr : y; m.res_out = x; m.norm_w = W->attn_norm;
-    m.epi = kEQKV; m.out = st64(c, p.off_q);
+    m.epi = kEQKV; m.out = st64(p, p.off_q);
     const size_t lw = (size_t)p.cache * p.kv_dim;
-    m.kc = reinterpret_cast<int32_t*>(c.st + p.off_k) + l * lw;
-    m.vc = reinterpret_cast<int32_t*>(c.st + p.off_v) + l * lw;
+    m.kc = reinterpret_cast<int32_t*>(p.st + p.off_k) + l * lw;
+    m.vc = reinterpret_cast<int32_t*>(p.st + p.off_v) + l * lw;
   } else if (k == kO) {
     m.W = W->wo; m.scale = W->so; m.pitch = p.pitch_d; m.rows = p.dim; m.cols = p.dim;
-    m.pro = kPPlain; m.in = st64(c, p.off_o); m.epi = kEStore; m.out = y;
+    m.pro = kPAcc; m.in = reinterpret_cast<const int64_t*>(q.work + p.off_oacc); m.epi = kEStore; m.out = y;
   } else if (k == kGU) {
     m.W = W->w13; m.scale = W->s13; m.pitch = p.pitch_d; m.rows = 2 * p.hidden; m.cols = p.dim;
     m.pro = kPNorm; m.in = x; m.add = y; m.res_out = xb; m.norm_w = W->ffn_norm;
-    m.epi = kESiLU; m.out = st64(c, p.off_h);
+    m.epi = kESiLU; m.out = st64(p, p.off_h);
   } else if (k == kDOWN) {
     m.W = W->w2; m.scale = W->s2; m.pitch = p.pitch_h; m.rows = p.dim; m.cols = p.hidden;
-    m.pro = kPPlain; m.in = st64(c, p.off_h); m.epi = kEStore; m.out = y;
+    m.pro = kPPlain; m.in = st64(p, p.off_h); m.epi = kEStore; m.out = y;
   } else {  // classifier
     m.W = p.cls; m.scale = p.cls_scale; m.pitch = p.pitch_d; m.rows = p.vocab; m.cols = p.dim;
     m.pro = kPNorm; m.in = xb; m.add = y; m.res_out = x; m.norm_w = p.final_norm;
-    m.epi = kELogits; m.out = st64(c, p.off_logits);
+    m.epi = kELogits; m.out = st64(p, p.off_logits);
   }
   return m;
 }
 
 // This CTA's rows of a matrix: whole pairs, split evenly over the grid.
-__device__ __forceinline__ void cta_rows(const MR& m, uint32_t b, uint32_t G, uint32_t& rb, uint32_t& re) {
-  const uint32_t np = (m.rows + 1) / 2;
+__device__ __forceinline__ void cta_rows(uint32_t rows, uint32_t b, uint32_t G, uint32_t& rb, uint32_t& re) {
+  const uint32_t np = (rows + 1) / 2;
   const uint32_t pb = (uint32_t)((uint64_t)np * b / G), pe = (uint32_t)((uint64_t)np * (b + 1) / G);
-  rb = min(m.rows, 2 * pb);
-  re = min(m.rows, 2 * pe);
+  rb = min(rows, 2 * pb);
+  re = min(rows, 2 * pe);
 }
-__device__ __forceinline__ uint32_t stage_rows(uint32_t pitch) {
-  uint32_t sr = kStageBytes / pitch;
-  if (sr >= 2) sr &= ~1u;
-  return sr < 1 ? 1 : sr;
+__device__ __forceinline__ uint32_t panel_count(uint32_t nr) { return (nr + kPanelRows - 1) / kPanelRows; }
+// Panel i of npan over nr rows: rows [p0, p0 + pn) of the CTA's slice, whole pairs, at most
+// kPanelRows (ceil(nr / 2) <= (kPanelRows / 2) npan pairs, split evenly).
+__device__ __forceinline__ void panel_of(uint32_t nr, uint32_t npan, uint32_t i, uint32_t& p0, uint32_t& pn) {
+  const uint32_t pairs = (nr + 1) / 2;
+  const uint32_t a = pairs * i / npan, b = pairs * (i + 1) / npan;
+  p0 = 2 * a;
+  pn = min(2 * b, nr) - 2 * a;
+}
+// Column groups one ring slot holds for a panel of pn rows (at least one: pn * 128 <= slot).
+__device__ __forceinline__ uint32_t groups_per_stage(uint32_t pn) {
+  const uint32_t g = kStageBytes / (pn * kGroupCols);
+  return g < 1 ? 1 : g;
 }
 
 // ------------------------------------------------------------------ producer
 
-__device__ bool producer_wait_empty(const Ctx& c, uint32_t slot, uint32_t parity) {
+__device__ bool producer_wait_empty(const StepParams& p, const Pos& q, uint32_t slot, uint32_t parity) {
   for (uint32_t i = 0; i < kPollLimit; ++i) {
-    if (mbar_try(&c.empty[slot], parity)) return true;
-    if ((i & 63) == 63 && ld_acquire(c.gabort)) return false;
+    if (mbar_try(&empty_of(p)[slot], parity)) return true;
+    if ((i & 63) == 63 && ld_acquire(gabort_of(q))) return false;
   }
-  atomicExch(c.gabort, 1u);
+  atomicExch(gabort_of(q), 1u);
   return false;
 }
 
-__device__ void producer(const Ctx& c) {
-  const StepParams& p = *c.p;
+__device__ void producer(const StepParams& p, const Pos& q) {
+  uint64_t* full = full_of(p);
+  const uint32_t ns = p.ns;
   uint32_t gs = 0;
   bool ok = true;
   for (uint32_t l = 0; l <= p.layers && ok; ++l) {
@@ -182,74 +217,80 @@ __device__ void producer(const Ctx& c) {
         if (!p.generating || kk > 0) break;
         k = kCLS;
       }
-      const MR m = matrow_of(c, l < p.layers ? l : 0, k);
+      const MR m = matrow_of(p, q, l < p.layers ? l : 0, k);
       uint32_t rb, re;
-      cta_rows(m, blockIdx.x, c.G, rb, re);
-      const uint32_t sr = stage_rows(m.pitch);
-      for (uint32_t r0 = rb; r0 < re; r0 += sr, ++gs) {
-        const uint32_t slot = gs % c.ns;
-        if (gs >= c.ns && !producer_wait_empty(c, slot, ((gs / c.ns) - 1) & 1)) {
-          ok = false;
-          break;
+      cta_rows(m.rows, blockIdx.x, gridDim.x, rb, re);
+      const uint32_t nr = re - rb, npan = panel_count(nr), NG = m.pitch / kGroupCols;
+      for (uint32_t i = 0; i < npan && ok; ++i) {
+        uint32_t p0, pn;
+        panel_of(nr, npan, i, p0, pn);
+        const uint32_t gps = groups_per_stage(pn), run = pn * kGroupCols;
+        const uint8_t* src0 = m.W + (size_t)(rb + p0) * kGroupCols;
+        for (uint32_t g0 = 0; g0 < NG; g0 += gps, ++gs) {
+          const uint32_t slot = gs % ns;
+          if (gs >= ns && !producer_wait_empty(p, q, slot, ((gs / ns) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          if (gs >= ns && !mbar_try(&full[slot], ((gs / ns) - 1) & 1)) {
+            atomicExch(gabort_of(q), 1u);  // the slot's last fill never completed: stop, do not re-arm
+            ok = false;
+            break;
+          }
+          const uint32_t ng = min(gps, NG - g0);
+          mbar_expect_tx(&full[slot], ng * run);
+          uint8_t* dst = ring_of() + (size_t)slot * kStageBytes;
+          for (uint32_t gl = 0; gl < ng; ++gl)
+            bulk_g2s(dst + (size_t)gl * run, src0 + (size_t)(g0 + gl) * m.rows * kGroupCols, run, &full[slot]);
         }
-        if (gs >= c.ns && !mbar_try(&c.full[slot], ((gs / c.ns) - 1) & 1)) {
-          atomicExch(c.gabort, 1u);  // the slot's last fill never completed: stop, do not re-arm
-          ok = false;
-          break;
-        }
-        const uint32_t nr = min(sr, re - r0);
-        mbar_expect_tx(&c.full[slot], nr * m.pitch);
-        bulk_g2s(c.ring + (size_t)slot * kStageBytes, m.W + (size_t)r0 * m.pitch, nr * m.pitch,
-                 &c.full[slot]);
       }
     }
   }
   // wait (bounded) for every copy still in flight before the CTA may exit
-  for (uint32_t j = gs > c.ns ? gs - c.ns : 0; j < gs; ++j) {
+  for (uint32_t j = gs > ns ? gs - ns : 0; j < gs; ++j) {
     for (uint32_t i = 0; i < kPollLimit; ++i)
-      if (mbar_try(&c.full[j % c.ns], (j / c.ns) & 1)) break;
+      if (mbar_try(&full[j % ns], (j / ns) & 1)) break;
   }
 }
 
 // ------------------------------------------------------------------ consumer helpers
 
-// Barrier over the consumer warps of every CTA; `epoch` counts the barriers passed.
-__device__ bool grid_sync(const Ctx& c, Shared& sh, uint32_t& epoch) {
+// Barrier over the consumer warps of every CTA; `epoch` counts the barriers passed.  The
+// release add publishes this CTA's writes (ordered before it by the CTA barrier), and the
+// acquire load that sees every CTA's add orders the others' writes before this CTA's reads.
+__device__ bool grid_sync(const Pos& q, Shared& sh, uint32_t& epoch) {
   consumer_bar();
   ++epoch;
   if (threadIdx.x == 0) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(c.gbar) : "memory");
-    const uint32_t target = epoch * c.G;
+    uint32_t* gbar = gbar_of(q);
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(gbar) : "memory");
+    const uint32_t target = epoch * gridDim.x;
     uint32_t i = 0;
-    while (ld_acquire(c.gbar) < target) {
-      if (++i > kPollLimit || ld_acquire(c.gabort)) {
-        atomicExch(c.gabort, 1u);
+    while (ld_acquire(gbar) < target) {
+      if (++i > kPollLimit || ((i & 255) == 0 && ld_acquire(gabort_of(q)))) {
+        atomicExch(gabort_of(q), 1u);
         sh.abort = 1;
         break;
       }
-      __nanosleep(32);
     }
-    __threadfence();
   }
   consumer_bar();
   return sh.abort == 0;
 }
 
 // Barrier among the gh CTAs of one attention head (monotonic target within a launch).
-__device__ bool group_sync(const Ctx& c, Shared& sh, uint32_t* counter, uint32_t target) {
+__device__ bool group_sync(const Pos& q, Shared& sh, uint32_t* counter, uint32_t target) {
   consumer_bar();
   if (threadIdx.x == 0) {
     asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(counter) : "memory");
     uint32_t i = 0;
     while (ld_acquire(counter) < target) {
-      if (++i > kPollLimit || ld_acquire(c.gabort)) {
-        atomicExch(c.gabort, 1u);
+      if (++i > kPollLimit || ((i & 255) == 0 && ld_acquire(gabort_of(q)))) {
+        atomicExch(gabort_of(q), 1u);
         sh.abort = 1;
         break;
       }
-      __nanosleep(32);
     }
-    __threadfence();
   }
   consumer_bar();
   return sh.abort == 0;
@@ -276,297 +317,234 @@ __device__ void consumer_sum_or(unsigned long long& s, unsigned long long& o, Sh
     sh.rbuf[warp] = o;
   }
   consumer_bar();
-  if (threadIdx.x == 0) {
-    unsigned long long a = 0, b = 0;
-    for (int w = 0; w < kNCW; ++w) {
-      a += sh.ra[w];
-      b |= sh.rbuf[w];
-    }
-    sh.S = a;
-    sh.orv = b;
+  unsigned long long a = 0, b = 0;
+#pragma unroll
+  for (int w = 0; w < kNCW; ++w) {
+    a += sh.ra[w];
+    b |= sh.rbuf[w];
   }
-  consumer_bar();
-  s = sh.S;
-  o = sh.orv;
+  consumer_bar();  // every thread has read the partials before they are reused
+  s = a;
+  o = b;
 }
 
-constexpr int kPPT = 8;                                  // element pairs per thread per block
-constexpr uint32_t kBlockPairs = (uint32_t)kCT * kPPT;   // 2048 pairs = 4096 elements
-
-// The phase input for element pairs pbase + tid + j*kCT (j < kPPT): the embedding row of the
-// token (phase 3), or in (+ add).  All loads of a block are issued before any is used, so a
-// thread waits for one round trip per block instead of one per element.  Beyond n: zeros.
-__device__ __forceinline__ void load_pairs(const Ctx& c, const MR& m, uint32_t pbase, int64_t (&x)[2 * kPPT]) {
+// The phase input for elements e0 .. e0+15 (e0 a multiple of 16): the embedding row of the
+// token (phase 3), the attention accumulators >> 24, or in (+ add).  Zeros at and beyond n.
+__device__ __forceinline__ void load16(const StepParams& p, const Pos& q, const MR& m, uint32_t e0,
+                                       int64_t (&x)[16]) {
   const uint32_t n = m.cols;
   if (m.pro == kPEmbedNorm) {
-    const StepParams& p = *c.p;
-    const uint8_t* row = p.embed + (size_t)c.tok * p.pitch_d;
-    const int64_t s = (int64_t)__ldg(p.embed_scale + c.tok);
+    const int64_t s = (int64_t)__ldg(p.embed_scale + q.tok);
+    uint4 b = make_uint4(0u, 0u, 0u, 0u);
+    if (e0 < n) b = __ldg(reinterpret_cast<const uint4*>(p.embed + grouped_offset(p.vocab, q.tok, e0)));
+    const uint32_t wd[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int j = 0; j < kPPT; ++j) {
-      const uint32_t i = 2 * (pbase + threadIdx.x + (uint32_t)j * kCT);
-      int64_t a = 0, b = 0;
-      if (i + 1 < n) {
-        const uint16_t w = *reinterpret_cast<const uint16_t*>(row + i);
-        a = ((int64_t)(w & 0xFF) - 128) * s >> 8;
-        b = ((int64_t)(w >> 8) - 128) * s >> 8;
-      } else if (i < n) {
-        a = ((int64_t)row[i] - 128) * s >> 8;
-      }
-      x[2 * j] = a;
-      x[2 * j + 1] = b;
+    for (int i = 0; i < 16; ++i) {
+      const int64_t byte = (int64_t)((wd[i >> 2] >> (8 * (i & 3))) & 0xFFu);
+      x[i] = e0 + i < n ? (byte - 128) * s >> 8 : 0;
     }
     return;
   }
+  if (e0 + 16 <= n) {
 #pragma unroll
-  for (int j = 0; j < kPPT; ++j) {
-    const uint32_t i = 2 * (pbase + threadIdx.x + (uint32_t)j * kCT);
-    int64_t a = 0, b = 0;
-    if (i + 1 < n) {
-      const longlong2 v = *reinterpret_cast<const longlong2*>(m.in + i);
-      a = v.x;
-      b = v.y;
-    } else if (i < n) {
-      a = m.in[i];
+    for (int j = 0; j < 8; ++j) {
+      const longlong2 v = *reinterpret_cast<const longlong2*>(m.in + e0 + 2 * j);
+      x[2 * j] = v.x;
+      x[2 * j + 1] = v.y;
     }
-    x[2 * j] = a;
-    x[2 * j + 1] = b;
-  }
-  if (m.add) {
+    if (m.add) {
 #pragma unroll
-    for (int j = 0; j < kPPT; ++j) {
-      const uint32_t i = 2 * (pbase + threadIdx.x + (uint32_t)j * kCT);
-      if (i + 1 < n) {
-        const longlong2 v = *reinterpret_cast<const longlong2*>(m.add + i);
+      for (int j = 0; j < 8; ++j) {
+        const longlong2 v = *reinterpret_cast<const longlong2*>(m.add + e0 + 2 * j);
         x[2 * j] = wadd(x[2 * j], v.x);
         x[2 * j + 1] = wadd(x[2 * j + 1], v.y);
-      } else if (i < n) {
-        x[2 * j] = wadd(x[2 * j], m.add[i]);
       }
     }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      int64_t v = 0;
+      if (e0 + i < n) {
+        v = m.in[e0 + i];
+        if (m.add) v = wadd(v, m.add[e0 + i]);
+      }
+      x[i] = v;
+    }
+  }
+  if (m.pro == kPAcc) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] >>= 24;
   }
 }
 
-// The norm weights of the same element pairs (zeros beyond n).
-__device__ __forceinline__ void load_weights(const MR& m, uint32_t pbase, int2 (&w)[kPPT]) {
+// The norm weights of elements e0 .. e0+15 (zeros beyond n).
+__device__ __forceinline__ void load_w16(const MR& m, uint32_t e0, int32_t (&w)[16]) {
   const uint32_t n = m.cols;
+  if (e0 + 16 <= n) {
 #pragma unroll
-  for (int j = 0; j < kPPT; ++j) {
-    const uint32_t i = 2 * (pbase + threadIdx.x + (uint32_t)j * kCT);
-    int2 v = make_int2(0, 0);
-    if (i + 1 < n) v = *reinterpret_cast<const int2*>(m.norm_w + i);
-    else if (i < n) v.x = m.norm_w[i];
-    w[j] = v;
+    for (int j = 0; j < 4; ++j) {
+      const int4 v = __ldg(reinterpret_cast<const int4*>(m.norm_w + e0 + 4 * j));
+      w[4 * j] = v.x;
+      w[4 * j + 1] = v.y;
+      w[4 * j + 2] = v.z;
+      w[4 * j + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = e0 + i < n ? __ldg(m.norm_w + e0 + i) : 0;
+  }
+}
+
+// Planes k0 .. k1-1 of the 16 values: plane k's bytes (byte k of each value, in element
+// order) are 16 bytes at base + (k - kbase) * pitch + e0.  A 4 x 4 byte transpose of each
+// group of four values gives their four low (or high) plane words.
+__device__ __forceinline__ void store_planes(const int64_t (&y)[16], uint8_t* base, uint32_t pitch,
+                                             uint32_t e0, uint32_t k0, uint32_t k1, uint32_t kbase) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    if ((uint32_t)(4 * half) >= k1 || (uint32_t)(4 * half + 4) <= k0) continue;
+    uint32_t pw[4][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t a = (uint32_t)((uint64_t)y[4 * q] >> (32 * half));
+      const uint32_t b = (uint32_t)((uint64_t)y[4 * q + 1] >> (32 * half));
+      const uint32_t cc = (uint32_t)((uint64_t)y[4 * q + 2] >> (32 * half));
+      const uint32_t d = (uint32_t)((uint64_t)y[4 * q + 3] >> (32 * half));
+      const uint32_t ab0 = __byte_perm(a, b, 0x5140), ab1 = __byte_perm(a, b, 0x7362);
+      const uint32_t cd0 = __byte_perm(cc, d, 0x5140), cd1 = __byte_perm(cc, d, 0x7362);
+      pw[0][q] = __byte_perm(ab0, cd0, 0x5410);
+      pw[1][q] = __byte_perm(ab0, cd0, 0x7632);
+      pw[2][q] = __byte_perm(ab1, cd1, 0x5410);
+      pw[3][q] = __byte_perm(ab1, cd1, 0x7632);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t k = 4 * half + j;
+      if (k < k0 || k >= k1) continue;
+      *reinterpret_cast<uint4*>(base + (size_t)(k - kbase) * pitch + e0) =
+          make_uint4(pw[j][0], pw[j][1], pw[j][2], pw[j][3]);
+    }
   }
 }
 
 // Packs the phase's input vector into byte planes (after the residual and the RMS
-// normalization where the phase has them); returns the limb count and *S the wrapping sum.
-__device__ int prologue(const Ctx& c, const MR& m, Shared& sh, unsigned long long* S_out) {
-  const uint32_t n = m.cols, half = m.pitch / 2;
-  const uint32_t npairs = (n + 1) / 2;
-  uint16_t* planes16 = reinterpret_cast<uint16_t*>(c.X);
-  const uint32_t lcap = c.p->lcap;
-  uint16_t* gplanes16 = reinterpret_cast<uint16_t*>(c.work + c.p->off_gplanes);
+// normalization where the phase has them): planes below *lcap_out in shared memory, the
+// others (only when the vector needs them) in the global copy.  Returns the limb count and
+// *S_out the wrapping sum of the packed vector.  Also stages this CTA's row scales and (for
+// Q/K/V) the position's rotary row in shared memory, and for Q/K/V block 0 clears the
+// attention accumulators that this layer's attention adds into.
+__device__ __forceinline__ int prologue(const StepParams& p, const Pos& q, const MR& m, Shared& sh,
+                                        unsigned long long* S_out, uint32_t* lcap_out) {
+  const uint32_t n = m.cols, pitch = m.pitch;
+  uint8_t* X = xreg(p);
+  const uint32_t nblk = (pitch + kBlockElems - 1) / kBlockElems;
+  uint32_t lcap = p.planes_bytes / pitch;
+  if (lcap > 8) lcap = 8;
   const bool writer = blockIdx.x == 0;
-  const bool norm = m.pro != kPPlain;
-  const bool single = half <= kBlockPairs;  // the whole vector fits one block of registers
-  // this block's row scales (and for Q/K/V the position's rotary row) go to shared memory
-  // so that no epilogue waits on global memory; the loads are issued first and stored last
+  const bool norm = m.pro == kPNorm || m.pro == kPEmbedNorm;
+  const uint32_t tid = threadIdx.x, et = 16 * tid;
   uint32_t rb, re;
-  cta_rows(m, blockIdx.x, c.G, rb, re);
-  uint32_t* sc = reinterpret_cast<uint32_t*>(c.X + c.p->planes_bytes);
-  int32_t* rp = reinterpret_cast<int32_t*>(c.X + c.p->planes_bytes + 4 * c.p->scale_cap);
-  const uint32_t my_row = rb + threadIdx.x;
-  const uint32_t my_scale = my_row < re ? __ldg(m.scale + my_row) : 0u;
+  cta_rows(m.rows, blockIdx.x, gridDim.x, rb, re);
+  uint32_t* sc = reinterpret_cast<uint32_t*>(X + p.planes_bytes);
+  int32_t* rp = reinterpret_cast<int32_t*>(X + p.planes_bytes + 4 * p.scale_cap);
   const bool qkv = m.epi == kEQKV;
-  const int32_t my_rope = (qkv && threadIdx.x < c.p->hd) ? __ldg(c.p->rope + (size_t)c.pos * c.p->hd + threadIdx.x) : 0;
-  int64_t x[2 * kPPT];
-  int2 wv[kPPT];
+  // loads whose results are only stored at the end: in flight during the vector work
+  const uint32_t my_row = rb + tid;
+  const uint32_t my_scale = my_row < re ? __ldg(m.scale + my_row) : 0u;
+  const int32_t my_rope = (qkv && tid < p.hd) ? __ldg(p.rope + (size_t)q.pos * p.hd + tid) : 0;
+  if (qkv && writer) {
+    unsigned long long* acc = reinterpret_cast<unsigned long long*>(q.work + p.off_oacc);
+    for (uint32_t i = tid; i < p.dim; i += kCT) acc[i] = 0ull;
+  }
+  int64_t x[16];
+  int32_t w[16];
+  InvDiv D = {};
   if (norm) {
     // "RMS normalization": rms = isqrt(sum(x*x)/n + 42,950), at least 1
     unsigned long long ss = 0, dummy = 0;
-    for (uint32_t pb = 0; pb < npairs; pb += kBlockPairs) {
-      load_pairs(c, m, pb, x);
-      if (single) load_weights(m, pb, wv);  // in flight while the sums reduce
+    for (uint32_t b = 0; b < nblk; ++b) {
+      const uint32_t e0 = b * kBlockElems + et;
+      if (e0 >= pitch) continue;
+      load16(p, q, m, e0, x);
+      if (nblk == 1) load_w16(m, e0, w);  // in flight while the sums reduce
 #pragma unroll
-      for (int e = 0; e < 2 * kPPT; ++e) ss += (unsigned long long)x[e] * (unsigned long long)x[e];
+      for (int i = 0; i < 16; ++i) ss += (unsigned long long)x[i] * (unsigned long long)x[i];
       if (writer && m.res_out) {
+        if (e0 + 16 <= n) {
 #pragma unroll
-        for (int j = 0; j < kPPT; ++j) {
-          const uint32_t i = 2 * (pb + threadIdx.x + (uint32_t)j * kCT);
-          if (i + 1 < n) {
+          for (int j = 0; j < 8; ++j) {
             longlong2 v;
             v.x = x[2 * j];
             v.y = x[2 * j + 1];
-            *reinterpret_cast<longlong2*>(m.res_out + i) = v;
-          } else if (i < n) {
-            m.res_out[i] = x[2 * j];
+            *reinterpret_cast<longlong2*>(m.res_out + e0 + 2 * j) = v;
           }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (e0 + i < n) m.res_out[e0 + i] = x[i];
         }
       }
     }
     consumer_sum_or(ss, dummy, sh);
-    if (threadIdx.x == 0) {
-      const InvDiv& Dn = n == c.p->dim ? c.p->div_dim : c.p->div_hidden;
-      uint64_t rms = isqrt_u64(udiv_inv(ss, Dn) + 42950ull);
-      if (rms < 1) rms = 1;
-      sh.div = make_invdiv((uint32_t)rms);
-    }
-    consumer_bar();
+    const InvDiv& Dn = n == p.dim ? p.div_dim : p.div_hidden;
+    uint64_t rms = isqrt_u64(udiv_inv(ss, Dn) + 42950ull);
+    if (rms < 1) rms = 1;
+    D = make_invdiv((uint32_t)rms);  // every thread alike: no broadcast needed
   }
-  const InvDiv D = sh.div;
   unsigned long long S = 0, orv = 0;
-  for (uint32_t pb = 0; pb < half; pb += kBlockPairs) {
-    if (!(norm && single)) {  // a single block is still in registers
-      load_pairs(c, m, pb, x);
-      if (norm) load_weights(m, pb, wv);
+  for (uint32_t b = 0; b < nblk; ++b) {
+    const uint32_t e0 = b * kBlockElems + et;
+    if (e0 >= pitch) continue;
+    if (!(norm && nblk == 1)) {  // a single block is still in registers
+      load16(p, q, m, e0, x);
+      if (norm) load_w16(m, e0, w);
+    }
+    if (norm) {
+      // y = ((x * w) / rms) >> 8, the division truncating toward zero (zeros beyond n)
+#pragma unroll
+      for (int i = 0; i < 16; ++i) x[i] = sdiv_trunc(wmul(x[i], (int64_t)w[i]), D) >> 8;
     }
 #pragma unroll
-    for (int j = 0; j < kPPT; ++j) {
-      const uint32_t pidx = pb + threadIdx.x + (uint32_t)j * kCT;
-      if (pidx >= half) continue;
-      const uint32_t i = 2 * pidx;
-      int64_t v0 = x[2 * j], v1 = x[2 * j + 1];
-      if (norm) {
-        // y = ((x * w) / rms) >> 8, the division truncating toward zero
-        v0 = i < n ? sdiv_trunc(wmul(v0, (int64_t)wv[j].x), D) >> 8 : 0;
-        v1 = i + 1 < n ? sdiv_trunc(wmul(v1, (int64_t)wv[j].y), D) >> 8 : 0;
-      }
-      S += (unsigned long long)v0 + (unsigned long long)v1;
-      orv |= (unsigned long long)(v0 ^ (v0 >> 63)) | (unsigned long long)(v1 ^ (v1 >> 63));
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        if ((uint32_t)k >= lcap) break;
-        planes16[(size_t)k * half + pidx] =
-            (uint16_t)((((uint64_t)v0 >> (8 * k)) & 0xFF) | ((((uint64_t)v1 >> (8 * k)) & 0xFF) << 8));
-      }
+    for (int i = 0; i < 16; ++i) {
+      S += (unsigned long long)x[i];
+      orv |= (unsigned long long)(x[i] ^ (x[i] >> 63));
     }
+    store_planes(x, X, pitch, e0, 0, lcap, 0);
   }
-  if (my_row < re) sc[threadIdx.x] = my_scale;
+  if (my_row < re) sc[tid] = my_scale;
   for (uint32_t r = my_row + kCT; r < re; r += kCT) sc[r - rb] = __ldg(m.scale + r);
-  if (qkv && threadIdx.x < c.p->hd) rp[threadIdx.x] = my_rope;
-  for (uint32_t i = threadIdx.x + kCT; qkv && i < c.p->hd; i += kCT)
-    rp[i] = __ldg(c.p->rope + (size_t)c.pos * c.p->hd + i);
-  if (threadIdx.x == 0) {
-    sh.scales = sc;
-    sh.rb = rb;
-    sh.rope = rp;
-  }
-  consumer_sum_or(S, orv, sh);  // its barriers also publish the scales and the rotary row
+  if (qkv && tid < p.hd) rp[tid] = my_rope;
+  for (uint32_t i = tid + kCT; qkv && i < p.hd; i += kCT) rp[i] = __ldg(p.rope + (size_t)q.pos * p.hd + i);
+  consumer_sum_or(S, orv, sh);  // its barriers also publish the planes, scales and rotary row
   int L = 1;
   while (L < 8 && (orv >> (8 * L - 1)) != 0) ++L;
+  if (L > 4) L = 8;  // the consumers run 1, 2, 3, 4 or 8 limbs
   if ((uint32_t)L > lcap) {
     // A vector beyond 8*lcap bits (rare): its planes lcap..L-1 go to the global copy, which
-    // every block writes with the same bytes; the consumers read them from there.
-    for (uint32_t pb = 0; pb < half; pb += kBlockPairs) {
-      load_pairs(c, m, pb, x);
-      if (norm) load_weights(m, pb, wv);
-#pragma unroll
-      for (int j = 0; j < kPPT; ++j) {
-        const uint32_t pidx = pb + threadIdx.x + (uint32_t)j * kCT;
-        if (pidx >= half) continue;
-        const uint32_t i = 2 * pidx;
-        int64_t v0 = x[2 * j], v1 = x[2 * j + 1];
+    // every block writes with the same bytes after the grid barrier that opened the phase.
+    uint8_t* gpl = q.work + p.off_gplanes;
+    for (uint32_t b = 0; b < nblk; ++b) {
+      const uint32_t e0 = b * kBlockElems + et;
+      if (e0 >= pitch) continue;
+      if (nblk > 1) {  // one block is still in registers
+        load16(p, q, m, e0, x);
         if (norm) {
-          v0 = i < n ? sdiv_trunc(wmul(v0, (int64_t)wv[j].x), D) >> 8 : 0;
-          v1 = i + 1 < n ? sdiv_trunc(wmul(v1, (int64_t)wv[j].y), D) >> 8 : 0;
+          load_w16(m, e0, w);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[i] = sdiv_trunc(wmul(x[i], (int64_t)w[i]), D) >> 8;
         }
-        for (uint32_t k = lcap; k < (uint32_t)L; ++k)
-          gplanes16[(size_t)(k - lcap) * half + pidx] =
-              (uint16_t)((((uint64_t)v0 >> (8 * k)) & 0xFF) | ((((uint64_t)v1 >> (8 * k)) & 0xFF) << 8));
       }
+      store_planes(x, gpl, pitch, e0, lcap, (uint32_t)L, lcap);
     }
     __threadfence_block();
     consumer_bar();
   }
   *S_out = S;
+  *lcap_out = lcap;
   return L;
 }
 
-// Row r (< 4) of the up to four rows a warp takes at once: the two rows of pair pq, then
-// the two rows of pair pq + wg.
-__device__ __forceinline__ uint32_t stage_row(uint32_t pq, uint32_t wg, uint32_t r) {
-  return 2 * (pq + (r >> 1) * wg) + (r & 1);
-}
-
-// R rows of a stage (lanes along the row), rows stage_row(pq, wg, 0..R) of the stage;
-// returns in lane r (< R) the 64-bit sum of row r.  Planes k < lcap are in shared memory, the others
-// (only when kMixed) in the global copy.
-template <int L, int R, bool kMixed>
-__device__ __forceinline__ unsigned long long dot_rows(const uint8_t* stage, uint32_t pq, uint32_t wg,
-                                                      uint32_t pitch, const uint8_t* planes_s,
-                                                      const uint8_t* planes_g, uint32_t lcap) {
-  const int lane = threadIdx.x & 31;
-  const uint8_t* rp[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) rp[r] = stage + (size_t)stage_row(pq, wg, (uint32_t)r) * pitch;
-  const uint8_t* pp[L];
-#pragma unroll
-  for (int k = 0; k < L; ++k)
-    pp[k] = (!kMixed || (uint32_t)k < lcap) ? planes_s + (size_t)k * pitch : planes_g + (size_t)(k - lcap) * pitch;
-  uint32_t acc[R][L];
-#pragma unroll
-  for (int r = 0; r < R; ++r)
-#pragma unroll
-    for (int k = 0; k < L; ++k) acc[r][k] = 0;
-  // Nine warps put three on one of the SM's four register-file quarters, which leaves 168
-  // registers a thread: the column loop stays rolled so the accumulators never spill.
-#pragma unroll 1
-  for (uint32_t cc = lane * 16; cc < pitch; cc += 512) {
-    uint4 w[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) w[r] = *reinterpret_cast<const uint4*>(rp[r] + cc);
-#pragma unroll
-    for (int k = 0; k < L; ++k) {
-      const uint4 x = *reinterpret_cast<const uint4*>(pp[k] + cc);
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        if (k < L - 1) {
-          uint32_t a = acc[r][k];
-          a = __dp4a(w[r].x, x.x, a);
-          a = __dp4a(w[r].y, x.y, a);
-          a = __dp4a(w[r].z, x.z, a);
-          a = __dp4a(w[r].w, x.w, a);
-          acc[r][k] = a;
-        } else {
-          int a = (int)acc[r][k];
-          a = dp4a_us(w[r].x, x.x, a);
-          a = dp4a_us(w[r].y, x.y, a);
-          a = dp4a_us(w[r].z, x.z, a);
-          a = dp4a_us(w[r].w, x.w, a);
-          acc[r][k] = (uint32_t)a;
-        }
-      }
-    }
-  }
-  unsigned long long mine = 0;
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    unsigned long long a = 0;
-#pragma unroll
-    for (int k = 0; k < L; ++k) {
-      const unsigned long long t = (k < L - 1) ? (unsigned long long)acc[r][k]
-                                               : (unsigned long long)(long long)(int)acc[r][k];
-      a += t << (8 * k);
-    }
-    a = warp_sum(a);
-    if (lane == r) mine = a;
-  }
-  return mine;
-}
-
-template <int L, bool kMixed>
-__device__ __forceinline__ unsigned long long dot_rows_n(uint32_t R, const uint8_t* stage, uint32_t pq, uint32_t wg,
-                                                        uint32_t pitch, const uint8_t* ps, const uint8_t* pg,
-                                                        uint32_t lcap) {
-  switch (R) {
-    case 4: return dot_rows<L, 4, kMixed>(stage, pq, wg, pitch, ps, pg, lcap);
-    case 3: return dot_rows<L, 3, kMixed>(stage, pq, wg, pitch, ps, pg, lcap);
-    case 2: return dot_rows<L, 2, kMixed>(stage, pq, wg, pitch, ps, pg, lcap);
-    default: return dot_rows<L, 1, kMixed>(stage, pq, wg, pitch, ps, pg, lcap);
-  }
-}
+// ------------------------------------------------------------------ matrix rows
 
 struct Best {
   long long v;
@@ -580,12 +558,12 @@ __device__ __forceinline__ void best_update(Best& b, long long v, uint32_t i) {
   }
 }
 
-// Epilogue for the row of this lane (lanes < R), after the partner exchange for pairs.
-__device__ __forceinline__ void epilogue(const Ctx& c, const MR& m, uint32_t layer, uint32_t row,
-                                         bool valid, int64_t y, Best& best, const int32_t* rope) {
+// Epilogue of one row (threads with valid == false only take part in the partner exchange;
+// the partner of an even row is the next thread).
+__device__ __forceinline__ void epilogue(const StepParams& p, const Pos& q, const MR& m, uint32_t layer,
+                                         uint32_t row, bool valid, int64_t y, Best& best, const int32_t* rope) {
   const int64_t partner = (int64_t)__shfl_xor_sync(0xffffffffu, (unsigned long long)y, 1);
   if (!valid) return;
-  const StepParams& p = *c.p;
   if (m.epi == kEStore) {
     m.out[row] = y;
   } else if (m.epi == kELogits) {
@@ -604,122 +582,271 @@ __device__ __forceinline__ void epilogue(const Ctx& c, const MR& m, uint32_t lay
       m.out[row] = even ? a2 : b2;
     } else if (row < q_rows + p.kv_dim) {
       const uint32_t e = row - q_rows;
-      if (!fits_i32(y)) record_error(c.st, err_key(c.pos, layer, 6, e));
+      if (!fits_i32(y)) record_error(p.st, err_key(q.pos, layer, 6, e));
       const uint32_t j = (e % p.hd) >> 1;
       int64_t a2, b2;
       rotate_pair((int64_t)(int32_t)a, (int64_t)(int32_t)b, rope[2 * j], rope[2 * j + 1], a2, b2);
       const int64_t mine = even ? a2 : b2;
-      if (!fits_i32(mine)) record_error(c.st, err_key(c.pos, layer, 8, e));
-      m.kc[(size_t)c.pos * p.kv_dim + e] = (int32_t)mine;
+      if (!fits_i32(mine)) record_error(p.st, err_key(q.pos, layer, 8, e));
+      m.kc[(size_t)q.pos * p.kv_dim + e] = (int32_t)mine;
     } else {
       const uint32_t e = row - q_rows - p.kv_dim;
-      if (!fits_i32(y)) record_error(c.st, err_key(c.pos, layer, 7, e));
-      m.vc[(size_t)c.pos * p.kv_dim + e] = (int32_t)y;
+      if (!fits_i32(y)) record_error(p.st, err_key(q.pos, layer, 7, e));
+      m.vc[(size_t)q.pos * p.kv_dim + e] = (int32_t)y;
     }
   }
 }
 
-template <int L, bool kMixed>
-__device__ void consume_phase(const Ctx& c, const MR& m, uint32_t layer, unsigned long long S,
-                              uint32_t gs0, Shared& sh, Best& best) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const StepParams& p = *c.p;
-  // Stages rotate over the warp groups; the warps of a group split each stage's row pairs.
-  // A group's previous stage precedes the slot's previous use (groups <= slots), so its
-  // parity wait can never see a phase two uses old.
-  const uint32_t grp = (uint32_t)warp / p.wgroup, wi = (uint32_t)warp % p.wgroup;
-  if (grp >= p.ngroups) return;
-  uint32_t rb, re;
-  cta_rows(m, blockIdx.x, c.G, rb, re);
-  const uint32_t sr = stage_rows(m.pitch);
-  const uint8_t* pg = c.work + p.off_gplanes;
-  uint32_t gs = gs0;
-  for (uint32_t r0 = rb; r0 < re; r0 += sr, ++gs) {
-    if (gs % p.ngroups != grp) continue;
-    const uint32_t slot = gs % c.ns;
-    bool ok = false;
-    for (uint32_t i = 0; i < kPollLimit; ++i) {
-      if (mbar_try(&c.full[slot], (gs / c.ns) & 1)) {
-        ok = true;
-        break;
+// Waits (bounded) for a ring slot's fill; false after a timeout or another CTA's abort.
+__device__ __forceinline__ bool wait_full(const StepParams& p, const Pos& q, uint32_t slot, uint32_t parity) {
+  for (uint32_t i = 0; i < kPollLimit; ++i) {
+    if (mbar_try(&full_of(p)[slot], parity)) return true;
+    if ((i & 63) == 63 && ld_acquire(gabort_of(q))) return false;
+  }
+  atomicExch(gabort_of(q), 1u);
+  return false;
+}
+
+// dp4a of one weight chunk (16 bytes of a row) with one plane chunk into a limb sum: plain
+// u8 x u8 for the low planes, u8 x s8 for the top plane (top is a constant after
+// unrolling).
+__device__ __forceinline__ uint32_t dp16(bool top, const uint4& w, const uint4& x, uint32_t a) {
+  if (top) {
+    int t = dp4a_us(w.x, x.x, (int)a);
+    t = dp4a_us(w.y, x.y, t);
+    t = dp4a_us(w.z, x.z, t);
+    t = dp4a_us(w.w, x.w, t);
+    return (uint32_t)t;
+  }
+  a = __dp4a(w.x, x.x, a);
+  a = __dp4a(w.y, x.y, a);
+  a = __dp4a(w.z, x.z, a);
+  return __dp4a(w.w, x.w, a);
+}
+
+// One ring stage (ng column groups of a panel) owned by this warp, for R row slots and
+// L <= 4 limbs: lane = row slot (rows lane + 32 j of the panel), all eight 16-byte column
+// chunks of every group; acc[j][k] is the u32 sum of row slot j's bytes times plane k (the
+// top plane L-1 signed; all in shared memory, which holds at least four).  `rot` is the
+// lane's chunk rotation (its rows' index in the matrix, modulo 8).
+template <int R, int L>
+__device__ __forceinline__ void stage_narrow(const uint8_t* stage, uint32_t ng, uint32_t run,
+                                             const uint32_t (&roff)[kRMax], uint32_t rot, uint32_t col0,
+                                             const uint8_t* planes, uint32_t pitch,
+                                             uint32_t (&acc)[kRMax][4]) {
+#pragma unroll 1
+  for (uint32_t gl = 0; gl < ng; ++gl) {
+    const uint8_t* base = stage + (size_t)gl * run;
+    const uint8_t* xcol = planes + col0 + gl * kGroupCols;
+#pragma unroll 4
+    for (uint32_t c = 0; c < 8; ++c) {
+      const uint32_t pc = (c ^ rot) << 4;
+      uint4 wv[R];
+#pragma unroll
+      for (int j = 0; j < R; ++j) wv[j] = *reinterpret_cast<const uint4*>(base + roff[j] + pc);
+#pragma unroll
+      for (int k = 0; k < L; ++k) {
+        const uint4 xk = *reinterpret_cast<const uint4*>(xcol + (size_t)k * pitch + 16 * c);
+#pragma unroll
+        for (int j = 0; j < R; ++j) acc[j][k] = dp16(k == L - 1, wv[j], xk, acc[j][k]);
       }
-      if ((i & 63) == 63 && ld_acquire(c.gabort)) break;
     }
-    if (!ok) {
-      atomicExch(c.gabort, 1u);
-      sh.abort = 1;
-      return;
-    }
-    const uint32_t nr = min(sr, re - r0);
-    const uint32_t npairs = (nr + 1) / 2;
-    const uint8_t* stage = c.ring + (size_t)slot * kStageBytes;
-    // this warp's pairs: wi, wi + wgroup, ... taken two at a time (up to four rows)
-    const uint32_t wg = p.wgroup;
-    for (uint32_t pq = wi; pq < npairs; pq += 2 * wg) {
-      // rows of pair pq, then of pair pq + wg; only the last pair of a stage can be single
-      const uint32_t R = min(2 * pq + 2, nr) - 2 * pq + (pq + wg < npairs ? min(2 * (pq + wg) + 2, nr) - 2 * (pq + wg) : 0);
-      const unsigned long long acc = dot_rows_n<L, kMixed>(R, stage, pq, wg, m.pitch, c.X, pg, p.lcap);
-      const uint32_t row = r0 + stage_row(pq, wg, lane < 4 ? (uint32_t)lane : 0u);
-      const bool valid = (uint32_t)lane < R;
-      int64_t y = 0;
-      if (valid) {
-        const unsigned long long t = (acc - (S << 7)) * (unsigned long long)sh.scales[row - sh.rb];
-        y = (int64_t)t >> 24;
-      }
-      epilogue(c, m, layer, row, valid, y, best, sh.rope);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&c.empty[slot]);
   }
 }
 
-__device__ uint32_t phase_stages(const Ctx& c, const MR& m) {
-  uint32_t rb, re;
-  cta_rows(m, blockIdx.x, c.G, rb, re);
-  const uint32_t sr = stage_rows(m.pitch);
-  return re > rb ? (re - rb + sr - 1) / sr : 0;
+// The same for vectors of 5 to 8 limbs (rare): all eight planes (planes above the last are
+// the sign bytes, so the sum with the top plane signed is still exact), each chunk's limb
+// sums folded at once into a wrapping 64-bit sum per row slot kept in acc[j][0] (low word)
+// and acc[j][1] (high word), so that no eight u32 accumulators per row stay live.  Planes
+// k >= lcap come from the global copy.
+template <int R>
+__device__ __forceinline__ void stage_wide(const uint8_t* stage, uint32_t ng, uint32_t run,
+                                           const uint32_t (&roff)[kRMax], uint32_t rot, uint32_t col0,
+                                           const uint8_t* planes, const uint8_t* gpl, uint32_t pitch,
+                                           uint32_t lcap, uint32_t (&acc)[kRMax][4]) {
+  unsigned long long sum[R];
+#pragma unroll
+  for (int j = 0; j < R; ++j) sum[j] = ((unsigned long long)acc[j][1] << 32) | acc[j][0];
+#pragma unroll 1
+  for (uint32_t gl = 0; gl < ng; ++gl) {
+    const uint8_t* base = stage + (size_t)gl * run;
+#pragma unroll 1
+    for (uint32_t c = 0; c < 8; ++c) {
+      const uint32_t col = col0 + gl * kGroupCols + 16 * c;
+      uint4 wv[R];
+#pragma unroll
+      for (int j = 0; j < R; ++j) wv[j] = *reinterpret_cast<const uint4*>(base + roff[j] + ((c ^ rot) << 4));
+#pragma unroll 1
+      for (int k = 0; k < 8; ++k) {
+        uint4 xk;
+        if ((uint32_t)k < lcap) xk = *reinterpret_cast<const uint4*>(planes + (size_t)k * pitch + col);
+        else xk = *reinterpret_cast<const uint4*>(gpl + (size_t)(k - lcap) * pitch + col);  // written in this launch
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          if (k < 7) sum[j] += (unsigned long long)dp16(false, wv[j], xk, 0u) << (8 * k);
+          else sum[j] += (unsigned long long)(long long)(int)dp16(true, wv[j], xk, 0u) << 56;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    acc[j][0] = (uint32_t)sum[j];
+    acc[j][1] = (uint32_t)(sum[j] >> 32);
+  }
 }
 
-// Phase 9 for this CTA's (head, chunk).
-__device__ bool attention(const Ctx& c, uint32_t l, Shared& sh) {
-  const StepParams& p = *c.p;
+// One stage with the body for (R row slots, L limbs), both uniform over the CTA.
+__device__ __forceinline__ void stage_dispatch(uint32_t R, int L, const uint8_t* stage, uint32_t ng,
+                                               uint32_t run, const uint32_t (&roff)[kRMax], uint32_t rot,
+                                               uint32_t col0, const uint8_t* planes, const uint8_t* gpl,
+                                               uint32_t pitch, uint32_t lcap, uint32_t (&acc)[kRMax][4]) {
+#define CK_NARROW(r, l) \
+  case r * 16 + l: stage_narrow<r, l>(stage, ng, run, roff, rot, col0, planes, pitch, acc); break;
+#define CK_ROWS(r)                                                                               \
+  CK_NARROW(r, 1) CK_NARROW(r, 2) CK_NARROW(r, 3) CK_NARROW(r, 4)                               \
+  case r * 16 + 8: stage_wide<r>(stage, ng, run, roff, rot, col0, planes, gpl, pitch, lcap, acc); break;
+  switch (R * 16 + (uint32_t)L) {
+    CK_ROWS(1) CK_ROWS(2) CK_ROWS(3)
+    default: break;
+  }
+#undef CK_ROWS
+#undef CK_NARROW
+}
+
+// One matrix-row phase on this CTA's rows.  The stages rotate over the owner warps (at
+// most as many as ring slots, so that a warp's previous stage always precedes its slot's
+// previous use and a parity wait cannot see a fill two uses old); a warp accumulates the
+// rows of its stages in registers (lane = row), and at the end of each panel the warps'
+// partial sums are added in shared memory and one thread per row applies the correction,
+// the row scale and the epilogue: y = ((sum_c byte * x - 128 * S) * scale) >> 24, wrapping
+// in 64 bits.  A warp that meets a timeout keeps walking the stages without waiting, so
+// that every warp reaches the same CTA barriers; the caller leaves on sh.abort.
+__device__ __forceinline__ void consume_phase(const StepParams& p, const Pos& q, const MR& m, uint32_t layer,
+                                              int L, unsigned long long S, uint32_t lcap, uint32_t& gs,
+                                              Shared& sh, Best& best) {
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  uint32_t rb, re;
+  cta_rows(m.rows, blockIdx.x, gridDim.x, rb, re);
+  const uint32_t nr = re - rb, npan = panel_count(nr), NG = m.pitch / kGroupCols;
+  const uint32_t pitch = m.pitch, owners = p.owners;
+  const uint8_t* planes = xreg(p);
+  const uint8_t* gpl = q.work + p.off_gplanes;
+  const uint32_t* sc = reinterpret_cast<const uint32_t*>(xreg(p) + p.planes_bytes);
+  const int32_t* rope = reinterpret_cast<const int32_t*>(xreg(p) + p.planes_bytes + 4 * p.scale_cap);
+  unsigned long long* red = red_of(p);
+  bool dead = false;
+  for (uint32_t pi = 0; pi < npan; ++pi) {
+    uint32_t p0, pn;
+    panel_of(nr, npan, pi, p0, pn);
+    const uint32_t R = (pn + 31) / 32, gps = groups_per_stage(pn), run = pn * kGroupCols;
+    const uint32_t rot = (rb + p0 + lane) & 7u;
+    uint32_t roff[kRMax];
+#pragma unroll
+    for (int j = 0; j < kRMax; ++j) roff[j] = min(lane + 32u * j, pn - 1) * kGroupCols;
+    uint32_t acc[kRMax][4];
+#pragma unroll
+    for (int j = 0; j < kRMax; ++j)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[j][k] = 0;
+    for (uint32_t g0 = 0; g0 < NG; g0 += gps, ++gs) {
+      if (gs % owners != warp) continue;
+      const uint32_t slot = gs % p.ns;
+      if (!dead && *reinterpret_cast<volatile int*>(&sh.abort)) dead = true;
+      if (!dead && !wait_full(p, q, slot, (gs / p.ns) & 1)) {
+        dead = true;
+        sh.abort = 1;
+      }
+      if (!dead) {
+        const uint32_t ng = min(gps, NG - g0);
+        const uint8_t* stage = ring_of() + (size_t)slot * kStageBytes;
+        stage_dispatch(R, L, stage, ng, run, roff, rot, g0 * kGroupCols, planes, gpl, pitch, lcap, acc);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_of(p)[slot]);
+    }
+    // this warp's partial sums of the panel's rows, limbs combined (zero without stages)
+#pragma unroll
+    for (int j = 0; j < kRMax; ++j) {
+      const uint32_t r = lane + 32u * j;
+      if ((uint32_t)j >= R || r >= pn) continue;
+      unsigned long long a = 0;
+      if (L <= 4) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (k >= L) continue;
+          const unsigned long long t = (k < L - 1) ? (unsigned long long)acc[j][k]
+                                                   : (unsigned long long)(long long)(int)acc[j][k];
+          a += t << (8 * k);
+        }
+      } else {
+        a = ((unsigned long long)acc[j][1] << 32) | acc[j][0];
+      }
+      red[warp * kPanelRows + r] = a;
+    }
+    consumer_bar();
+    const bool valid = tid < pn && !dead;
+    int64_t y = 0;
+    if (valid) {
+      unsigned long long sum = 0;
+#pragma unroll
+      for (int w = 0; w < kNCW; ++w) sum += red[w * kPanelRows + tid];
+      const unsigned long long t = (sum - (S << 7)) * (unsigned long long)sc[p0 + tid];
+      y = (int64_t)t >> 24;
+    }
+    epilogue(p, q, m, layer, rb + p0 + tid, valid, y, best, rope);
+    consumer_bar();  // every thread has read the partial sums before the next panel's
+  }
+}
+
+// ------------------------------------------------------------------ attention
+
+// Phase 9 for this CTA's (head, chunk): "Attention" in four stages over positions 0..pos of
+// the head's cache.  Each CTA adds sum_t P_t * v_t over its chunk of positions into the
+// head's 64-bit accumulators (the O prologue applies the final >> 24).  The maximum and the
+// sum Z need every position: for short contexts each CTA scores all positions itself; for
+// longer ones the CTAs score their own chunks and exchange maxima and sums (two barriers
+// among the head's CTAs).
+__device__ __forceinline__ bool attention(const StepParams& p, const Pos& q, uint32_t l, Shared& sh) {
   const uint32_t b = blockIdx.x, gh = p.gh;
   if (b >= p.heads * gh) return true;
   const uint32_t h = b / gh, ch = b % gh, hd = p.hd;
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int64_t* q_s = reinterpret_cast<int64_t*>(c.X);
+  int64_t* q_s = reinterpret_cast<int64_t*>(xreg(p));
   unsigned long long* part = reinterpret_cast<unsigned long long*>(q_s + hd);  // [kNCW][hd]
   long long* red = reinterpret_cast<long long*>(part + kNCW * hd);             // [kNCW]
-  long long* sc = red + kNCW;                                                  // chunk scores
-  const uint32_t P = c.pos + 1;
+  long long* sc = red + kNCW;                                                  // scores
+  const uint32_t P = q.pos + 1;
+  const bool full = gh == 1 || P <= p.att_full;
   const uint32_t cs = (P + gh - 1) / gh;
-  const uint32_t t0 = min(P, ch * cs), t1 = min(P, t0 + cs), n = t1 - t0;
+  const uint32_t t0 = min(P, ch * cs), t1 = min(P, t0 + cs);
+  const uint32_t s0 = full ? 0u : t0, s1 = full ? P : t1, nsc = s1 - s0;
   const uint32_t kvh = h / (p.heads / p.kv_heads);
   const size_t lw = (size_t)p.cache * p.kv_dim;
-  const int32_t* Kh = reinterpret_cast<const int32_t*>(c.st + p.off_k) + l * lw + (size_t)kvh * hd;
-  const int32_t* Vh = reinterpret_cast<const int32_t*>(c.st + p.off_v) + l * lw + (size_t)kvh * hd;
-  long long* wpart = reinterpret_cast<long long*>(c.work + kWPart) + (size_t)(h * gh + ch) * (hd + 2);
-  uint32_t* hcount = reinterpret_cast<uint32_t*>(c.work + kWHeads) + h;
-  const int64_t* qg = st64(c, p.off_q) + (size_t)h * hd;
+  const int32_t* Kh = reinterpret_cast<const int32_t*>(p.st + p.off_k) + l * lw + (size_t)kvh * hd;
+  const int32_t* Vh = reinterpret_cast<const int32_t*>(p.st + p.off_v) + l * lw + (size_t)kvh * hd;
+  long long* parts = reinterpret_cast<long long*>(q.work + p.off_part) + (size_t)h * gh * 2;  // [gh][2]
+  uint32_t* hcount = reinterpret_cast<uint32_t*>(q.work + kWHeads) + h;
+  const int64_t* qg = st64(p, p.off_q) + (size_t)h * hd;
   for (uint32_t i = tid; i < hd; i += kCT) q_s[i] = qg[i];
   consumer_bar();
   const uint32_t lpp = hd / 4, ppw = 32 / lpp;
   const uint32_t sub = lane % lpp, slot = lane / lpp, e0 = sub * 4;
   const int64_t q0 = q_s[e0], q1 = q_s[e0 + 1], q2 = q_s[e0 + 2], q3 = q_s[e0 + 3];
-  // stage 0: scores ((q . k) >> 16) * inv >> 24 and the chunk maximum
+  // stage 0: scores ((q . k) >> 16) * inv >> 24 and their maximum
   long long lmax = LLONG_MIN;
-  for (uint32_t base = warp * ppw; base < n; base += kNCW * ppw) {
+  for (uint32_t base = warp * ppw; base < nsc; base += kNCW * ppw) {
     const uint32_t tl = base + slot;
     unsigned long long d = 0;
-    if (tl < n) {
-      const int4 k4 = *reinterpret_cast<const int4*>(Kh + (size_t)(t0 + tl) * p.kv_dim + e0);
+    if (tl < nsc) {
+      const int4 k4 = *reinterpret_cast<const int4*>(Kh + (size_t)(s0 + tl) * p.kv_dim + e0);
       d = (unsigned long long)q0 * (unsigned long long)(long long)k4.x +
           (unsigned long long)q1 * (unsigned long long)(long long)k4.y +
           (unsigned long long)q2 * (unsigned long long)(long long)k4.z +
           (unsigned long long)q3 * (unsigned long long)(long long)k4.w;
     }
     for (uint32_t o = lpp >> 1; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-    if (tl < n && sub == 0) {
+    if (tl < nsc && sub == 0) {
       long long s = (long long)d >> 16;
       s = (long long)((unsigned long long)s * (unsigned long long)p.inv_sqrt) >> 24;
       sc[tl] = s;
@@ -735,19 +862,18 @@ __device__ bool attention(const Ctx& c, uint32_t l, Shared& sh) {
   consumer_bar();
   long long m = LLONG_MIN;
   for (int w = 0; w < kNCW; ++w) m = red[w] > m ? red[w] : m;
-  if (gh > 1) {
-    if (tid == 0) wpart[0] = m;
-    if (!group_sync(c, sh, hcount, (3 * l + 1) * gh)) return false;
+  if (!full) {
+    if (tid == 0) parts[2 * ch] = m;
+    if (!group_sync(q, sh, hcount, (2 * l + 1) * gh)) return false;
     m = LLONG_MIN;
     for (uint32_t j = 0; j < gh; ++j) {
-      const long long v = *(volatile long long*)(reinterpret_cast<long long*>(c.work + kWPart) +
-                                                 (size_t)(h * gh + j) * (hd + 2));
+      const long long v = *(volatile long long*)(parts + 2 * j);
       m = v > m ? v : m;
     }
   }
   // stage 1: exponentials EXP[min((m - s) >> 8, 4096)] and their sum
   unsigned long long z = 0;
-  for (uint32_t tl = tid; tl < n; tl += kCT) {
+  for (uint32_t tl = tid; tl < nsc; tl += kCT) {
     unsigned long long idx = ((unsigned long long)m - (unsigned long long)sc[tl]) >> 8;
     if (idx > 4096) idx = 4096;
     const unsigned long long e = __ldg(p.exp_tab + idx);
@@ -760,24 +886,28 @@ __device__ bool attention(const Ctx& c, uint32_t l, Shared& sh) {
   consumer_bar();
   unsigned long long Z = 0;
   for (int w = 0; w < kNCW; ++w) Z += (unsigned long long)red[w];
-  if (gh > 1) {
-    if (tid == 0) wpart[1] = (long long)Z;
-    if (!group_sync(c, sh, hcount, (3 * l + 2) * gh)) return false;
+  if (!full) {
+    if (tid == 0) parts[2 * ch + 1] = (long long)Z;
+    if (!group_sync(q, sh, hcount, (2 * l + 2) * gh)) return false;
     Z = 0;
-    for (uint32_t j = 0; j < gh; ++j)
-      Z += (unsigned long long)*(volatile long long*)(reinterpret_cast<long long*>(c.work + kWPart) +
-                                                      (size_t)(h * gh + j) * (hd + 2) + 1);
+    for (uint32_t j = 0; j < gh; ++j) Z += (unsigned long long)*(volatile long long*)(parts + 2 * j + 1);
   }
-  // stage 2: probabilities (e << 24) / Z
-  for (uint32_t tl = tid; tl < n; tl += kCT) sc[tl] = (long long)(((unsigned long long)sc[tl] << 24) / Z);
+  // stage 2: probabilities (e << 24) / Z over this CTA's chunk [t0, t1)
+  const bool small_z = Z > 0 && Z <= 0xFFFFFFFFull;
+  const InvDiv DZ = make_invdiv(small_z ? (uint32_t)Z : 1u);
+  for (uint32_t t = t0 + tid; t < t1; t += kCT) {
+    const unsigned long long num = (unsigned long long)sc[t - s0] << 24;
+    sc[t - s0] = (long long)(small_z ? udiv_inv(num, DZ) : num / Z);
+  }
   consumer_bar();
-  // stage 3: sum over positions of P * v, then one >> 24
+  // stage 3: sum over the chunk of P * v, added into the head's accumulators
+  const uint32_t nch = t1 - t0;
   unsigned long long a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-  for (uint32_t base = warp * ppw; base < n; base += kNCW * ppw) {
+  for (uint32_t base = warp * ppw; base < nch; base += kNCW * ppw) {
     const uint32_t tl = base + slot;
-    if (tl < n) {
+    if (tl < nch) {
       const int4 v4 = *reinterpret_cast<const int4*>(Vh + (size_t)(t0 + tl) * p.kv_dim + e0);
-      const long long pr = sc[tl];
+      const long long pr = sc[t0 - s0 + tl];
       a0 += (unsigned long long)(pr * (long long)v4.x);
       a1 += (unsigned long long)(pr * (long long)v4.y);
       a2 += (unsigned long long)(pr * (long long)v4.z);
@@ -798,35 +928,22 @@ __device__ bool attention(const Ctx& c, uint32_t l, Shared& sh) {
     dst[3] = a3;
   }
   consumer_bar();
-  int64_t* og = st64(c, p.off_o) + (size_t)h * hd;
-  if (gh == 1) {
+  if (nch) {
+    unsigned long long* acc = reinterpret_cast<unsigned long long*>(q.work + p.off_oacc) + (size_t)h * hd;
     for (uint32_t j = tid; j < hd; j += kCT) {
       unsigned long long s = 0;
       for (int w = 0; w < kNCW; ++w) s += part[(size_t)w * hd + j];
-      og[j] = (int64_t)s >> 24;
-    }
-    return true;
-  }
-  for (uint32_t j = tid; j < hd; j += kCT) {
-    unsigned long long s = 0;
-    for (int w = 0; w < kNCW; ++w) s += part[(size_t)w * hd + j];
-    wpart[2 + j] = (long long)s;
-  }
-  if (!group_sync(c, sh, hcount, (3 * l + 3) * gh)) return false;
-  if (ch == 0) {
-    for (uint32_t j = tid; j < hd; j += kCT) {
-      unsigned long long s = 0;
-      for (uint32_t q = 0; q < gh; ++q)
-        s += (unsigned long long)*(volatile long long*)(reinterpret_cast<long long*>(c.work + kWPart) +
-                                                        (size_t)(h * gh + q) * (hd + 2) + 2 + j);
-      og[j] = (int64_t)s >> 24;
+      if (gh == 1) acc[j] = s;  // the only contributor
+      else atomicAdd(acc + j, s);
     }
   }
   return true;
 }
 
-__device__ void consumers(const Ctx& c, Shared& sh) {
-  const StepParams& p = *c.p;
+// ------------------------------------------------------------------ the position
+
+
+__device__ __forceinline__ void consumers(const StepParams& p, const Pos& q, Shared& sh) {
   uint32_t epoch = 0, gs = 0;
   Best best;
   best.v = LLONG_MIN;
@@ -838,28 +955,18 @@ __device__ void consumers(const Ctx& c, Shared& sh) {
         if (k > kQKV) break;
         kind = p.generating ? kCLS : kEND;
       }
-      if (!(l == 0 && kind == kQKV) && !grid_sync(c, sh, epoch)) return;
+      if (!(l == 0 && kind == kQKV) && !grid_sync(q, sh, epoch)) return;
       if (kind == kEND) return;
       if (kind == kATT) {
-        if (!attention(c, l, sh)) return;
+        if (!attention(p, q, l, sh)) return;
         continue;
       }
-      const MR m = matrow_of(c, l < p.layers ? l : 0, kind);
+      const MR m = matrow_of(p, q, l < p.layers ? l : 0, kind);
       unsigned long long S;
-      const int L = prologue(c, m, sh, &S);
-      const bool mixed = (uint32_t)L > p.lcap;
-      switch (L) {
-        case 1: consume_phase<1, false>(c, m, l, S, gs, sh, best); break;
-        case 2: consume_phase<2, false>(c, m, l, S, gs, sh, best); break;
-        case 3: consume_phase<3, false>(c, m, l, S, gs, sh, best); break;
-        case 4: consume_phase<4, false>(c, m, l, S, gs, sh, best); break;
-        case 5: mixed ? consume_phase<5, true>(c, m, l, S, gs, sh, best) : consume_phase<5, false>(c, m, l, S, gs, sh, best); break;
-        case 6: mixed ? consume_phase<6, true>(c, m, l, S, gs, sh, best) : consume_phase<6, false>(c, m, l, S, gs, sh, best); break;
-        case 7: mixed ? consume_phase<7, true>(c, m, l, S, gs, sh, best) : consume_phase<7, false>(c, m, l, S, gs, sh, best); break;
-        default: mixed ? consume_phase<8, true>(c, m, l, S, gs, sh, best) : consume_phase<8, false>(c, m, l, S, gs, sh, best); break;
-      }
-      gs += phase_stages(c, m);
-      consumer_bar();  // a warp that gave up returns early: leave together
+      uint32_t lcap;
+      const int L = prologue(p, q, m, sh, &S, &lcap);
+      consume_phase(p, q, m, l, L, S, lcap, gs, sh, best);
+      consumer_bar();
       if (sh.abort) return;
       if (kind == kCLS) {
         // this CTA's first largest logit, then the grid's in the last phase
@@ -876,32 +983,29 @@ __device__ void consumers(const Ctx& c, Shared& sh) {
           sh.am_i[warp] = best.i;
         }
         consumer_bar();
+        long long* cand = reinterpret_cast<long long*>(q.work + p.off_cand);
         if (threadIdx.x == 0) {
           Best cb;
           cb.v = LLONG_MIN;
           cb.i = 0xFFFFFFFFu;
           for (int w = 0; w < kNCW; ++w)
             if (sh.am_i[w] != 0xFFFFFFFFu) best_update(cb, sh.am_v[w], sh.am_i[w]);
-          long long* slot = reinterpret_cast<long long*>(c.work + kWPart) +
-                            (size_t)p.heads * p.gh * (p.hd + 2) + 2 * blockIdx.x;
-          slot[0] = cb.v;
-          slot[1] = (long long)cb.i;
+          cand[2 * blockIdx.x] = cb.v;
+          cand[2 * blockIdx.x + 1] = (long long)cb.i;
         }
-        if (!grid_sync(c, sh, epoch)) return;
+        if (!grid_sync(q, sh, epoch)) return;
         if (blockIdx.x != 0) return;
         // phase 19 (maximum pass over the per-CTA candidates) and the end of the position
         if (threadIdx.x == 0) {
           Best g;
           g.v = LLONG_MIN;
           g.i = 0xFFFFFFFFu;
-          const long long* slots = reinterpret_cast<const long long*>(c.work + kWPart) +
-                                   (size_t)p.heads * p.gh * (p.hd + 2);
-          for (uint32_t q = 0; q < c.G; ++q) {
-            const long long v = *(volatile const long long*)(slots + 2 * q);
-            const uint32_t i = (uint32_t) * (volatile const long long*)(slots + 2 * q + 1);
+          for (uint32_t b = 0; b < gridDim.x; ++b) {
+            const long long v = *(volatile const long long*)(cand + 2 * b);
+            const uint32_t i = (uint32_t) * (volatile const long long*)(cand + 2 * b + 1);
             if (i != 0xFFFFFFFFu) best_update(g, v, i);
           }
-          uint8_t* st = c.st;
+          uint8_t* st = p.st;
           if (hdr_ld<uint64_t>(st, kHErrKey) != kNoError) {
             hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
             hdr<uint32_t>(st, kHError) = CK_ARITHMETIC;
@@ -923,28 +1027,17 @@ __device__ void consumers(const Ctx& c, Shared& sh) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) k_step(const StepParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ Shared sh;
+// The whole position for one CTA, with its scratch at `work`.
+__device__ __forceinline__ void step_body(const StepParams& p, uint8_t* work, Shared& sh) {
   uint8_t* st = p.st;
   if (hdr_ld<uint32_t>(st, kHPhase) != CK_PHASE_RUNNING) return;  // every CTA alike
-  Ctx c;
-  c.p = &p;
-  c.st = st;
-  c.work = st + p.off_work;
-  c.gbar = reinterpret_cast<uint32_t*>(c.work + kWBar);
-  c.gabort = reinterpret_cast<uint32_t*>(c.work + kWAbort);
-  c.ns = p.ns;
-  c.G = gridDim.x;
-  c.ring = smem;
-  c.X = smem + (size_t)p.ns * kStageBytes;
-  c.full = reinterpret_cast<uint64_t*>(c.X + p.x_bytes);
-  c.empty = c.full + p.ns;
-  c.pos = hdr_ld<uint32_t>(st, kHPosition);
+  Pos q;
+  q.work = work;
+  q.pos = hdr_ld<uint32_t>(st, kHPosition);
   const uint32_t np = hdr_ld<uint32_t>(st, kHNPrompt);
-  c.tok = c.pos < np ? reinterpret_cast<const uint32_t*>(st + p.off_prompt)[c.pos]
-                     : reinterpret_cast<const uint32_t*>(st + p.off_out)[c.pos - np];
-  if (c.tok >= p.vocab) {  // a state edited outside the library
+  q.tok = q.pos < np ? reinterpret_cast<const uint32_t*>(st + p.off_prompt)[q.pos]
+                     : reinterpret_cast<const uint32_t*>(st + p.off_out)[q.pos - np];
+  if (q.tok >= p.vocab) {  // a state edited outside the library
     if (blockIdx.x == 0 && threadIdx.x == 0) {
       hdr<uint32_t>(st, kHError) = CK_INVALID_STATE;
       hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
@@ -954,17 +1047,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepParams p) {
   if (threadIdx.x == 0) {
     sh.abort = 0;
     for (uint32_t s = 0; s < p.ns; ++s) {
-      mbar_init(&c.full[s], 1);
-      mbar_init(&c.empty[s], p.wgroup);  // every warp of the owning group releases the slot
+      mbar_init(&full_of(p)[s], 1);
+      mbar_init(&empty_of(p)[s], 1);  // the stage's owner warp releases it
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
   if ((threadIdx.x >> 5) == kNCW) {
-    if ((threadIdx.x & 31) == 0) producer(c);
+    if ((threadIdx.x & 31) == 0) producer(p, q);
     return;
   }
-  consumers(c, sh);
+  consumers(p, q, sh);
   // a prompt position ends with the last residual and the cursor (block 0, after the grid
   // barrier the consumers passed on their way out of the last layer)
   if (!p.generating && blockIdx.x == 0 && !sh.abort) {
@@ -981,78 +1074,41 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(const StepParams p) {
       }
     }
   }
-  if (threadIdx.x == 0 && blockIdx.x == 0 && (sh.abort || ld_acquire(c.gabort))) {
+  if (threadIdx.x == 0 && blockIdx.x == 0 && (sh.abort || ld_acquire(gabort_of(q)))) {
     hdr<uint32_t>(st, kHError) = CK_CUDA_ERROR;
     hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
   }
 }
 
+__global__ void __launch_bounds__(kThreads, 1) k_step(const StepParams p) {
+  __shared__ Shared sh;
+  step_body(p, p.st + p.off_work, sh);
+}
+
 // ------------------------------------------------------------------ allocation-free variant
-// The same position with its scratch (barrier counters, attention partials, classifier
-// candidates) in this file's own device array instead of the state's work region.
+// The same position with its scratch (barrier counters, attention partials and
+// accumulators, classifier candidates, global planes) in this file's own device array
+// instead of the state's work region.
 constexpr size_t kNoAllocWorkBytes = 256 * 1024;
 static __device__ __align__(256) uint8_t g_noalloc_work[kNoAllocWorkBytes];
 
 __global__ void __launch_bounds__(kThreads, 1) k_step_noalloc(const StepParams p, uint8_t* work) {
-  extern __shared__ __align__(128) uint8_t smem[];
   __shared__ Shared sh;
-  uint8_t* st = p.st;
-  if (hdr_ld<uint32_t>(st, kHPhase) != CK_PHASE_RUNNING) return;
-  Ctx c;
-  c.p = &p;
-  c.st = st;
-  c.work = work;
-  c.gbar = reinterpret_cast<uint32_t*>(c.work + kWBar);
-  c.gabort = reinterpret_cast<uint32_t*>(c.work + kWAbort);
-  c.ns = p.ns;
-  c.G = gridDim.x;
-  c.ring = smem;
-  c.X = smem + (size_t)p.ns * kStageBytes;
-  c.full = reinterpret_cast<uint64_t*>(c.X + p.x_bytes);
-  c.empty = c.full + p.ns;
-  c.pos = hdr_ld<uint32_t>(st, kHPosition);
-  const uint32_t np = hdr_ld<uint32_t>(st, kHNPrompt);
-  c.tok = c.pos < np ? reinterpret_cast<const uint32_t*>(st + p.off_prompt)[c.pos]
-                     : reinterpret_cast<const uint32_t*>(st + p.off_out)[c.pos - np];
-  if (c.tok >= p.vocab) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-      hdr<uint32_t>(st, kHError) = CK_INVALID_STATE;
-      hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
-    }
-    return;
-  }
-  if (threadIdx.x == 0) {
-    sh.abort = 0;
-    for (uint32_t s = 0; s < p.ns; ++s) {
-      mbar_init(&c.full[s], 1);
-      mbar_init(&c.empty[s], p.wgroup);  // every warp of the owning group releases the slot
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-  if ((threadIdx.x >> 5) == kNCW) {
-    if ((threadIdx.x & 31) == 0) producer(c);
-    return;
-  }
-  consumers(c, sh);
-  if (!p.generating && blockIdx.x == 0 && !sh.abort) {
-    int64_t* x = reinterpret_cast<int64_t*>(st + p.off_x);
-    const int64_t* xb = reinterpret_cast<const int64_t*>(st + p.off_xb);
-    const int64_t* y = reinterpret_cast<const int64_t*>(st + p.off_y);
-    for (uint32_t i = threadIdx.x; i < p.dim; i += kCT) x[i] = wadd(xb[i], y[i]);
-    if (threadIdx.x == 0) {
-      if (hdr_ld<uint64_t>(st, kHErrKey) != kNoError) {
-        hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
-        hdr<uint32_t>(st, kHError) = CK_ARITHMETIC;
-      } else {
-        hdr<uint32_t>(st, kHPosition) += 1;
-      }
-    }
-  }
-  if (threadIdx.x == 0 && blockIdx.x == 0 && (sh.abort || ld_acquire(c.gabort))) {
-    hdr<uint32_t>(st, kHError) = CK_CUDA_ERROR;
-    hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
-  }
+  step_body(p, work, sh);
+}
+
+cudaError_t launch_coop(const void* fn, void** args, cudaStream_t s, int grid, size_t smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 }  // namespace
@@ -1081,17 +1137,10 @@ cudaError_t noalloc_setup(size_t dynamic_max, uint8_t** work) {
 }
 
 cudaError_t launch_step_noalloc(const StepParams& p, uint8_t* work, cudaStream_t s, int grid, size_t smem) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_step_noalloc, p, work);
+  StepParams pc = p;
+  uint8_t* w = work;
+  void* args[2] = {&pc, &w};
+  return launch_coop(reinterpret_cast<const void*>(k_step_noalloc), args, s, grid, smem);
 }
 
 // Allows the kernel the largest dynamic shared memory the device offers beside its static
@@ -1106,17 +1155,9 @@ cudaError_t configure_step(size_t optin, size_t* dynamic_max) {
 }
 
 cudaError_t launch_step(const StepParams& p, cudaStream_t s, int grid, size_t smem) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_step, p);
+  StepParams pc = p;
+  void* args[1] = {&pc};
+  return launch_coop(reinterpret_cast<const void*>(k_step), args, s, grid, smem);
 }
 
 int step_threads() { return kThreads; }
@@ -1127,5 +1168,6 @@ int step_blocks_per_sm(size_t smem) {
   return n;
 }
 int step_consumer_warps() { return kNCW; }
+size_t step_red_bytes() { return (size_t)kNCW * kPanelRows * 8; }
 
 }  // namespace ck

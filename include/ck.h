@@ -101,9 +101,8 @@ int ck_model_config(const ck_model* m, ck_config* out);
  * block per SM, launched cooperatively): a producer warp streams every matrix of the
  * position through shared memory with bulk copies while consumer warps compute, with grid
  * barriers between dependent phases.  CK_PATH_KERNELS: one kernel per phase.  CK_PATH_AUTO
- * (the default) takes the persistent kernel whenever the model and state fit it (padded
- * dim <= 12288, padded hidden <= 24576, heads <= 1000, enough shared memory) and the
- * phase kernels otherwise.  Both compute the same bits.  Errors: 10 for an unknown path;
+ * (the default) takes the persistent kernel whenever the model and state fit it (heads <=
+ * 1000, enough shared memory and state work area) and the phase kernels otherwise.  Both compute the same bits.  Errors: 10 for an unknown path;
  * ck_turn returns 10 when CK_PATH_STEP is forced on a model or state it cannot run. */
 #define CK_PATH_AUTO 0
 #define CK_PATH_STEP 1
@@ -115,6 +114,13 @@ int ck_set_path(ck_model* m, int path);
  * slots prefetch less weight data across phase boundaries; the results are the same bits.
  * Drops the model's cached graphs.  Errors: 10 for 1 or more than 8. */
 int ck_set_step_slots(ck_model* m, uint32_t max_slots);
+
+/* The one-position kernel splits each attention head's positions over a few blocks.  Up to
+ * `positions` positions (0, the default: 16384 / head dimension) every block of a head
+ * scores all of them itself; beyond, the blocks score their own chunks and exchange maxima
+ * and sums.  A tuning and testing control: the results are the same bits.  Drops the
+ * model's cached graphs.  Errors: 10 for a null handle. */
+int ck_set_attention_split(ck_model* m, uint32_t positions);
 /* Frees the host handle and its cached CUDA graphs (not dev_mem). */
 void ck_free_model(ck_model* m);
 

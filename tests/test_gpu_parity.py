@@ -174,6 +174,23 @@ def test_step_kernel_with_a_small_ring(ck, slots):
     assert P.gpu.set_step_slots(1) == 10
 
 
+@pytest.mark.parametrize("name,split", [("gqa", 1), ("gqa", 3), ("tiny_ws", 1), ("gqa_tied", 2)])
+def test_step_kernel_with_split_attention_scoring(ck, name, split):
+    """The persistent kernel with each head's scoring split over its blocks beyond `split`
+    positions (maxima and sums exchanged between the blocks), every position against the
+    oracle."""
+    wl = MODELS[name]
+    P = Pair(ck, wl.spec, "step")
+    assert P.gpu.set_attention_split(split) == 0
+    ids = synth.prompt_ids(wl.spec, wl.n_prompt)
+    so, sg = P.init(ck, ids, wl.steps)
+    for pos in range(wl.n_prompt + wl.steps - 1):
+        rco, reso = P.orc.turn(so, 1)
+        rcg, resg = P.gpu.turn(sg, 1)
+        assert rco == rcg == 0 and reso == resg, (pos, rcg, resg)
+        compare_states(P.orc, so, ck.state_download(sg), wl.n_prompt, wl.steps, f"split {split} pos {pos}")
+
+
 @pytest.fixture(scope="module", params=list(PATHS))
 def pairs(ck, request):
     return {name: Pair(ck, wl.spec, request.param) for name, wl in MODELS.items()}
