@@ -31,6 +31,8 @@ struct ck_model {
   int path;              // CK_PATH_*
   uint32_t max_slots;    // cap on the one-position kernel's ring slots (0: as many as fit)
   uint32_t att_full;     // positions every block of a head scores itself (0: default)
+  uint32_t pf_kb;        // L2 prefetch distance of the one-position kernel, KB per block
+                         // (0: default)
   int smem_optin;        // largest shared memory a block may opt into
   size_t step_smem;      // dynamic shared memory available to the one-position kernel
   std::vector<DevLayer> layers;
@@ -526,7 +528,7 @@ bool plan_step(const ck_model* m, const StateLayout& lay, StepParams* sp, int* g
   const uint64_t avail = (uint64_t)m->step_smem;
   if (avail < xb + red + 2 * (kStageBytes + 16)) return false;
   uint64_t ns = (avail - xb - red) / (kStageBytes + 16);
-  if (ns > 8) ns = 8;
+  if (ns > kMaxSlots) ns = kMaxSlots;
   if (m->max_slots && ns > m->max_slots) ns = m->max_slots;
   if (ns < 2) return false;
   // work region: counters, attention maxima and sums, classifier candidates, attention
@@ -548,7 +550,7 @@ bool plan_step(const ck_model* m, const StateLayout& lay, StepParams* sp, int* g
   p.vocab = c.vocab; p.hd = m->head_dim; p.kv_dim = m->kv_dim; p.pitch_d = m->pitch_d;
   p.pitch_h = m->pitch_h; p.inv_sqrt = m->inv_sqrt;
   p.gh = gh; p.att_full = att_full; p.ns = (uint32_t)ns; p.x_bytes = (uint32_t)xb;
-  p.owners = std::min<uint32_t>(kStepWarps, (uint32_t)ns);
+  p.pf_bytes = m->pf_kb * 1024u;  // 0 (the default): none
   p.planes_bytes = (uint32_t)planes;
   p.off_part = off_part; p.off_cand = off_cand; p.off_oacc = off_oacc; p.off_gplanes = off_gplanes;
   p.scale_cap = (uint32_t)scale_cap;
@@ -754,6 +756,7 @@ int ck_load_model(const void* artifact, size_t len, void* dev_mem, size_t dev_le
   m->path = CK_PATH_AUTO;
   m->max_slots = 0;
   m->att_full = 0;
+  m->pf_kb = 0;
   if (cudaMemcpyAsync(m->dev_layers, m->layers.data(), sizeof(DevLayer) * c.layers,
                       cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess) {
@@ -784,9 +787,17 @@ int ck_set_path(ck_model* m, int path) {
 }
 
 int ck_set_step_slots(ck_model* m, uint32_t max_slots) {
-  if (!m || max_slots == 1 || max_slots > 8) return CK_INVALID_ARGUMENT;
+  if (!m || max_slots == 1 || max_slots > kMaxSlots) return CK_INVALID_ARGUMENT;
   m->max_slots = max_slots;
   for (auto& g : m->graphs) cudaGraphExecDestroy(g.exec);  // plans change: rebuild graphs
+  m->graphs.clear();
+  return CK_OK;
+}
+
+int ck_set_step_prefetch(ck_model* m, uint32_t kb_per_block) {
+  if (!m || kb_per_block > 4096) return CK_INVALID_ARGUMENT;
+  m->pf_kb = kb_per_block;
+  for (auto& g : m->graphs) cudaGraphExecDestroy(g.exec);
   m->graphs.clear();
   return CK_OK;
 }

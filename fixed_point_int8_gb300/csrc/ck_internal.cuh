@@ -248,7 +248,11 @@ struct AttnParams {
 };
 
 // The persistent one-position kernel (ck_step.cu).
-constexpr uint32_t kStageBytes = 24576;  // one ring slot: column groups of one row panel
+// One ring slot: column groups of one row panel.  22 KB holds two groups of panels up to 88
+// rows (or one of 96) and lets eight slots fit beside the planes, so that all eight
+// consumer warps own stages.
+constexpr uint32_t kStageBytes = 22528;
+constexpr uint32_t kMaxSlots = 8;        // ring slots at most
 constexpr uint32_t kPanelRows = 96;      // most rows of one panel (three a lane)
 constexpr uint32_t kStepWarps = 8;       // consumer warps
 
@@ -262,7 +266,7 @@ struct StepParams {
   uint32_t gh;          // CTAs per attention head
   uint32_t att_full;    // up to this many positions every CTA of a head scores all of them
   uint32_t ns;          // ring slots
-  uint32_t owners;      // consumer warps that take ring stages in turn (<= ns)
+  uint32_t pf_bytes;    // how far ahead of the ring fills the producer prefetches into L2
   uint32_t x_bytes;     // planes, row scales and rotary row / attention region
   uint32_t planes_bytes;  // shared memory for byte planes; a phase keeps
                           // min(8, planes_bytes / pitch) planes there, the rest in global

@@ -9,10 +9,11 @@
 // complete on mbarriers.  It never waits for activations, only for free slots, so HBM keeps
 // streaming across phase boundaries.
 //
-// Eight consumer warps take the ring's stages in turn.  Within a stage, lane l accumulates
-// rows l, l + 32, ... of the panel over all the stage's columns, so a lane holds whole dot
-// products and no shuffle reduction is needed: at the end of a panel the warps' partial
-// sums meet in shared memory and one thread per row runs the fused epilogue.  The dot products use byte planes of the input vector: the phase's prologue
+// Eight consumer warps read every slot: warp w takes the 16-byte column chunk w of each
+// column group, and lane l accumulates rows l, l + 32, ... of the panel, so a lane holds
+// whole dot products over its columns and no shuffle reduction is needed: at the end of a
+// panel the warps' partial sums meet in shared memory and one thread per row runs the
+// fused epilogue.  The dot products use byte planes of the input vector: the phase's prologue
 // (residual, RMS normalization) writes plane k = byte k of every element, and each row sum
 // is sum_k 2^(8k) sum_c byte[r][c] * plane_k[c], one dp4a per four bytes and limb.
 //
@@ -205,47 +206,110 @@ __device__ bool producer_wait_empty(const StepParams& p, const Pos& q, uint32_t 
   return false;
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Walks the position's ring stages in order: layer, matrix, panel, column groups.  Stage =
+// ng runs of `run` bytes, run r starting at src + r * gstride.
+struct StageCursor {
+  uint32_t l, kk;        // layer and matrix index (QKV, O, GU, DOWN; the classifier after)
+  uint32_t rb, nr, npan, pi, p0, pn, gps, g0, NG;
+  const uint8_t* W;
+  uint32_t rows;
+  bool done;
+};
+
+// The matrix of (l, kk), or false past the last one.
+__device__ __forceinline__ bool cursor_matrix(const StepParams& p, const Pos& q, StageCursor& c) {
+  for (;;) {
+    if (c.l > p.layers || (c.l == p.layers && (!p.generating || c.kk > 0))) return false;
+    int k = c.kk == 0 ? kQKV : c.kk == 1 ? kO : c.kk == 2 ? kGU : kDOWN;
+    if (c.l == p.layers) k = kCLS;
+    const MR m = matrow_of(p, q, c.l < p.layers ? c.l : 0, k);
+    uint32_t re;
+    cta_rows(m.rows, blockIdx.x, gridDim.x, c.rb, re);
+    c.nr = re - c.rb;
+    c.npan = panel_count(c.nr);
+    c.NG = m.pitch / kGroupCols;
+    c.W = m.W;
+    c.rows = m.rows;
+    c.pi = 0;
+    c.g0 = 0;
+    if (c.npan) {
+      panel_of(c.nr, c.npan, 0, c.p0, c.pn);
+      c.gps = groups_per_stage(c.pn);
+      return true;
+    }
+    if (++c.kk == 4) {
+      c.kk = 0;
+      ++c.l;
+    }
+  }
+}
+__device__ __forceinline__ void cursor_start(const StepParams& p, const Pos& q, StageCursor& c) {
+  c.l = 0;
+  c.kk = 0;
+  c.done = !cursor_matrix(p, q, c);
+}
+__device__ __forceinline__ void cursor_next(const StepParams& p, const Pos& q, StageCursor& c) {
+  c.g0 += c.gps;
+  if (c.g0 < c.NG) return;
+  c.g0 = 0;
+  if (++c.pi < c.npan) {
+    panel_of(c.nr, c.npan, c.pi, c.p0, c.pn);
+    c.gps = groups_per_stage(c.pn);
+    return;
+  }
+  if (++c.kk == 4) {
+    c.kk = 0;
+    ++c.l;
+  }
+  c.done = !cursor_matrix(p, q, c);
+}
+
+// The producer: fills ring slot gs % ns with stage gs once the slot's previous stage is
+// released, and keeps L2 prefetches of the following stages about pf_bytes ahead of the
+// fills, so that HBM keeps streaming while the consumers are in barriers, prologues or
+// attention and the ring is full.
 __device__ void producer(const StepParams& p, const Pos& q) {
   uint64_t* full = full_of(p);
   const uint32_t ns = p.ns;
+  StageCursor fc, pc;
+  cursor_start(p, q, fc);
+  cursor_start(p, q, pc);
+  unsigned long long filled = 0, fetched = 0;  // bytes
   uint32_t gs = 0;
   bool ok = true;
-  for (uint32_t l = 0; l <= p.layers && ok; ++l) {
-    for (int kk = 0; kk < 4 && ok; ++kk) {
-      int k = kk == 0 ? kQKV : kk == 1 ? kO : kk == 2 ? kGU : kDOWN;
-      if (l == p.layers) {
-        if (!p.generating || kk > 0) break;
-        k = kCLS;
-      }
-      const MR m = matrow_of(p, q, l < p.layers ? l : 0, k);
-      uint32_t rb, re;
-      cta_rows(m.rows, blockIdx.x, gridDim.x, rb, re);
-      const uint32_t nr = re - rb, npan = panel_count(nr), NG = m.pitch / kGroupCols;
-      for (uint32_t i = 0; i < npan && ok; ++i) {
-        uint32_t p0, pn;
-        panel_of(nr, npan, i, p0, pn);
-        const uint32_t gps = groups_per_stage(pn), run = pn * kGroupCols;
-        const uint8_t* src0 = m.W + (size_t)(rb + p0) * kGroupCols;
-        for (uint32_t g0 = 0; g0 < NG; g0 += gps, ++gs) {
-          const uint32_t slot = gs % ns;
-          if (gs >= ns && !producer_wait_empty(p, q, slot, ((gs / ns) - 1) & 1)) {
-            ok = false;
-            break;
-          }
-          if (gs >= ns && !mbar_try(&full[slot], ((gs / ns) - 1) & 1)) {
-            atomicExch(gabort_of(q), 1u);  // the slot's last fill never completed: stop, do not re-arm
-            ok = false;
-            break;
-          }
-          const uint32_t ng = min(gps, NG - g0);
-          mbar_expect_tx(&full[slot], ng * run);
-          uint8_t* dst = ring_of() + (size_t)slot * kStageBytes;
-          for (uint32_t gl = 0; gl < ng; ++gl)
-            bulk_g2s(dst + (size_t)gl * run, src0 + (size_t)(g0 + gl) * m.rows * kGroupCols, run, &full[slot]);
-        }
-      }
+  for (; !fc.done; cursor_next(p, q, fc), ++gs) {
+    const uint32_t run = fc.pn * kGroupCols;
+    const uint32_t ng = min(fc.gps, fc.NG - fc.g0);
+    // prefetch ahead (the fill cursor never passes the prefetch cursor)
+    while (p.pf_bytes && !pc.done && fetched < filled + ng * run + p.pf_bytes) {
+      const uint32_t prun = pc.pn * kGroupCols, png = min(pc.gps, pc.NG - pc.g0);
+      const uint8_t* src = pc.W + (size_t)(pc.rb + pc.p0) * kGroupCols + (size_t)pc.g0 * pc.rows * kGroupCols;
+      for (uint32_t gl = 0; gl < png; ++gl) prefetch_l2(src + (size_t)gl * pc.rows * kGroupCols, prun);
+      fetched += (unsigned long long)png * prun;
+      cursor_next(p, q, pc);
     }
+    const uint32_t slot = gs % ns;
+    if (gs >= ns && !producer_wait_empty(p, q, slot, ((gs / ns) - 1) & 1)) {
+      ok = false;
+      break;
+    }
+    if (gs >= ns && !mbar_try(&full[slot], ((gs / ns) - 1) & 1)) {
+      atomicExch(gabort_of(q), 1u);  // the slot's last fill never completed: stop, do not re-arm
+      ok = false;
+      break;
+    }
+    mbar_expect_tx(&full[slot], ng * run);
+    uint8_t* dst = ring_of() + (size_t)slot * kStageBytes;
+    const uint8_t* src = fc.W + (size_t)(fc.rb + fc.p0) * kGroupCols + (size_t)fc.g0 * fc.rows * kGroupCols;
+    for (uint32_t gl = 0; gl < ng; ++gl)
+      bulk_g2s(dst + (size_t)gl * run, src + (size_t)gl * fc.rows * kGroupCols, run, &full[slot]);
+    filled += (unsigned long long)ng * run;
   }
+  (void)ok;
   // wait (bounded) for every copy still in flight before the CTA may exit
   for (uint32_t j = gs > ns ? gs - ns : 0; j < gs; ++j) {
     for (uint32_t i = 0; i < kPollLimit; ++i)
@@ -624,32 +688,30 @@ __device__ __forceinline__ uint32_t dp16(bool top, const uint4& w, const uint4& 
   return __dp4a(w.w, x.w, a);
 }
 
-// One ring stage (ng column groups of a panel) owned by this warp, for R row slots and
-// L <= 4 limbs: lane = row slot (rows lane + 32 j of the panel), all eight 16-byte column
-// chunks of every group; acc[j][k] is the u32 sum of row slot j's bytes times plane k (the
-// top plane L-1 signed; all in shared memory, which holds at least four).  `rot` is the
-// lane's chunk rotation (its rows' index in the matrix, modulo 8).
+// This warp's share of one ring stage (ng column groups of a panel) for R row slots and
+// L <= 4 limbs: lane = row slot (rows lane + 32 j of the panel), warp = 16-byte column
+// chunk of every group; acc[j][k] is the u32 sum of row slot j's bytes times plane k (the
+// top plane L-1 signed; all in shared memory, which holds at least four).  `pc` is the
+// lane's chunk position within a row's 128 bytes (the warp's chunk rotated by the rows'
+// index in the matrix, modulo 8).  (One group at a time: with nine warps a thread has 168
+// registers, and two groups in flight made the compiler spill.)
 template <int R, int L>
 __device__ __forceinline__ void stage_narrow(const uint8_t* stage, uint32_t ng, uint32_t run,
-                                             const uint32_t (&roff)[kRMax], uint32_t rot, uint32_t col0,
+                                             const uint32_t (&roff)[kRMax], uint32_t pc, uint32_t col0,
                                              const uint8_t* planes, uint32_t pitch,
                                              uint32_t (&acc)[kRMax][4]) {
 #pragma unroll 1
   for (uint32_t gl = 0; gl < ng; ++gl) {
-    const uint8_t* base = stage + (size_t)gl * run;
+    const uint8_t* base = stage + (size_t)gl * run + pc;
     const uint8_t* xcol = planes + col0 + gl * kGroupCols;
-#pragma unroll 4
-    for (uint32_t c = 0; c < 8; ++c) {
-      const uint32_t pc = (c ^ rot) << 4;
-      uint4 wv[R];
+    uint4 wv[R];
 #pragma unroll
-      for (int j = 0; j < R; ++j) wv[j] = *reinterpret_cast<const uint4*>(base + roff[j] + pc);
+    for (int j = 0; j < R; ++j) wv[j] = *reinterpret_cast<const uint4*>(base + roff[j]);
 #pragma unroll
-      for (int k = 0; k < L; ++k) {
-        const uint4 xk = *reinterpret_cast<const uint4*>(xcol + (size_t)k * pitch + 16 * c);
+    for (int k = 0; k < L; ++k) {
+      const uint4 xk = *reinterpret_cast<const uint4*>(xcol + (size_t)k * pitch);
 #pragma unroll
-        for (int j = 0; j < R; ++j) acc[j][k] = dp16(k == L - 1, wv[j], xk, acc[j][k]);
-      }
+      for (int j = 0; j < R; ++j) acc[j][k] = dp16(k == L - 1, wv[j], xk, acc[j][k]);
     }
   }
 }
@@ -661,75 +723,87 @@ __device__ __forceinline__ void stage_narrow(const uint8_t* stage, uint32_t ng, 
 // k >= lcap come from the global copy.
 template <int R>
 __device__ __forceinline__ void stage_wide(const uint8_t* stage, uint32_t ng, uint32_t run,
-                                           const uint32_t (&roff)[kRMax], uint32_t rot, uint32_t col0,
+                                           const uint32_t (&roff)[kRMax], uint32_t pc, uint32_t col0,
                                            const uint8_t* planes, const uint8_t* gpl, uint32_t pitch,
                                            uint32_t lcap, uint32_t (&acc)[kRMax][4]) {
-  unsigned long long sum[R];
-#pragma unroll
-  for (int j = 0; j < R; ++j) sum[j] = ((unsigned long long)acc[j][1] << 32) | acc[j][0];
 #pragma unroll 1
   for (uint32_t gl = 0; gl < ng; ++gl) {
-    const uint8_t* base = stage + (size_t)gl * run;
-#pragma unroll 1
-    for (uint32_t c = 0; c < 8; ++c) {
-      const uint32_t col = col0 + gl * kGroupCols + 16 * c;
-      uint4 wv[R];
+    const uint8_t* base = stage + (size_t)gl * run + pc;
+    const uint32_t col = col0 + gl * kGroupCols;
 #pragma unroll
-      for (int j = 0; j < R; ++j) wv[j] = *reinterpret_cast<const uint4*>(base + roff[j] + ((c ^ rot) << 4));
+    for (int j = 0; j < R; ++j) {
+      const uint4 w = *reinterpret_cast<const uint4*>(base + roff[j]);
+      unsigned long long sum = ((unsigned long long)acc[j][1] << 32) | acc[j][0];
 #pragma unroll 1
       for (int k = 0; k < 8; ++k) {
         uint4 xk;
         if ((uint32_t)k < lcap) xk = *reinterpret_cast<const uint4*>(planes + (size_t)k * pitch + col);
         else xk = *reinterpret_cast<const uint4*>(gpl + (size_t)(k - lcap) * pitch + col);  // written in this launch
-#pragma unroll
-        for (int j = 0; j < R; ++j) {
-          if (k < 7) sum[j] += (unsigned long long)dp16(false, wv[j], xk, 0u) << (8 * k);
-          else sum[j] += (unsigned long long)(long long)(int)dp16(true, wv[j], xk, 0u) << 56;
-        }
+        if (k < 7) sum += (unsigned long long)dp16(false, w, xk, 0u) << (8 * k);
+        else sum += (unsigned long long)(long long)(int)dp16(true, w, xk, 0u) << 56;
       }
+      acc[j][0] = (uint32_t)sum;
+      acc[j][1] = (uint32_t)(sum >> 32);
     }
   }
-#pragma unroll
-  for (int j = 0; j < R; ++j) {
-    acc[j][0] = (uint32_t)sum[j];
-    acc[j][1] = (uint32_t)(sum[j] >> 32);
+}
+
+// The consumers' next ring stage: its slot and the parity of the fill it waits for.
+struct RingPos {
+  uint32_t slot, par;
+};
+__device__ __forceinline__ void ring_advance(const StepParams& p, RingPos& r) {
+  if (++r.slot == p.ns) {
+    r.slot = 0;
+    r.par ^= 1u;
   }
 }
 
-// One stage with the body for (R row slots, L limbs), both uniform over the CTA.
-__device__ __forceinline__ void stage_dispatch(uint32_t R, int L, const uint8_t* stage, uint32_t ng,
-                                               uint32_t run, const uint32_t (&roff)[kRMax], uint32_t rot,
-                                               uint32_t col0, const uint8_t* planes, const uint8_t* gpl,
-                                               uint32_t pitch, uint32_t lcap, uint32_t (&acc)[kRMax][4]) {
-#define CK_NARROW(r, l) \
-  case r * 16 + l: stage_narrow<r, l>(stage, ng, run, roff, rot, col0, planes, pitch, acc); break;
-#define CK_ROWS(r)                                                                               \
-  CK_NARROW(r, 1) CK_NARROW(r, 2) CK_NARROW(r, 3) CK_NARROW(r, 4)                               \
-  case r * 16 + 8: stage_wide<r>(stage, ng, run, roff, rot, col0, planes, gpl, pitch, lcap, acc); break;
-  switch (R * 16 + (uint32_t)L) {
-    CK_ROWS(1) CK_ROWS(2) CK_ROWS(3)
-    default: break;
+// Waits for each stage of a panel (NG column groups, gps a stage), runs this warp's share
+// with the body for (R row slots, L limbs) and releases the slot.  A warp that meets a
+// timeout (or sees another's) keeps walking the stages without waiting, so that every warp
+// reaches the same CTA barriers; returns whether it did.
+template <int R, int L>
+__device__ __forceinline__ bool panel_stages(const StepParams& p, const Pos& q, RingPos& rp, uint32_t NG,
+                                             uint32_t gps, uint32_t run, const uint32_t (&roff)[kRMax],
+                                             uint32_t pc, uint32_t col0, const uint8_t* planes,
+                                             const uint8_t* gpl, uint32_t pitch, uint32_t lcap, Shared& sh,
+                                             bool dead, uint32_t (&acc)[kRMax][4]) {
+  const uint32_t lane = threadIdx.x & 31;
+  for (uint32_t g0 = 0; g0 < NG; g0 += gps) {
+    const uint32_t slot = rp.slot;
+    if (!dead && *reinterpret_cast<volatile int*>(&sh.abort)) dead = true;
+    if (!dead && !wait_full(p, q, slot, rp.par)) {
+      dead = true;
+      sh.abort = 1;
+    }
+    if (!dead) {
+      const uint32_t ng = min(gps, NG - g0);
+      const uint8_t* stage = ring_of() + (size_t)slot * kStageBytes;
+      if (L <= 4) stage_narrow<R, (L <= 4 ? L : 4)>(stage, ng, run, roff, pc, col0 + g0 * kGroupCols, planes, pitch, acc);
+      else stage_wide<R>(stage, ng, run, roff, pc, col0 + g0 * kGroupCols, planes, gpl, pitch, lcap, acc);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_of(p)[slot]);
+    ring_advance(p, rp);
   }
-#undef CK_ROWS
-#undef CK_NARROW
+  return dead;
 }
 
-// One matrix-row phase on this CTA's rows.  The stages rotate over the owner warps (at
-// most as many as ring slots, so that a warp's previous stage always precedes its slot's
-// previous use and a parity wait cannot see a fill two uses old); a warp accumulates the
-// rows of its stages in registers (lane = row), and at the end of each panel the warps'
-// partial sums are added in shared memory and one thread per row applies the correction,
-// the row scale and the epilogue: y = ((sum_c byte * x - 128 * S) * scale) >> 24, wrapping
-// in 64 bits.  A warp that meets a timeout keeps walking the stages without waiting, so
+// One matrix-row phase on this CTA's rows.  Every warp reads every stage (warp w: column
+// chunk w of each group) and accumulates the rows in registers (lane = row), so all warps
+// finish a panel together; at the end of each panel the warps' partial sums are added in
+// shared memory and one thread per row applies the correction, the row scale and the
+// epilogue: y = ((sum_c byte * x - 128 * S) * scale) >> 24, wrapping in 64 bits.  A warp that meets a timeout keeps walking the stages without waiting, so
 // that every warp reaches the same CTA barriers; the caller leaves on sh.abort.
 __device__ __forceinline__ void consume_phase(const StepParams& p, const Pos& q, const MR& m, uint32_t layer,
-                                              int L, unsigned long long S, uint32_t lcap, uint32_t& gs,
+                                              int L, unsigned long long S, uint32_t lcap, RingPos& rp,
                                               Shared& sh, Best& best) {
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   uint32_t rb, re;
   cta_rows(m.rows, blockIdx.x, gridDim.x, rb, re);
   const uint32_t nr = re - rb, npan = panel_count(nr), NG = m.pitch / kGroupCols;
-  const uint32_t pitch = m.pitch, owners = p.owners;
+  const uint32_t pitch = m.pitch;
   const uint8_t* planes = xreg(p);
   const uint8_t* gpl = q.work + p.off_gplanes;
   const uint32_t* sc = reinterpret_cast<const uint32_t*>(xreg(p) + p.planes_bytes);
@@ -740,7 +814,7 @@ __device__ __forceinline__ void consume_phase(const StepParams& p, const Pos& q,
     uint32_t p0, pn;
     panel_of(nr, npan, pi, p0, pn);
     const uint32_t R = (pn + 31) / 32, gps = groups_per_stage(pn), run = pn * kGroupCols;
-    const uint32_t rot = (rb + p0 + lane) & 7u;
+    const uint32_t pc = (warp ^ ((rb + p0 + lane) & 7u)) << 4;
     uint32_t roff[kRMax];
 #pragma unroll
     for (int j = 0; j < kRMax; ++j) roff[j] = min(lane + 32u * j, pn - 1) * kGroupCols;
@@ -749,22 +823,19 @@ __device__ __forceinline__ void consume_phase(const StepParams& p, const Pos& q,
     for (int j = 0; j < kRMax; ++j)
 #pragma unroll
       for (int k = 0; k < 4; ++k) acc[j][k] = 0;
-    for (uint32_t g0 = 0; g0 < NG; g0 += gps, ++gs) {
-      if (gs % owners != warp) continue;
-      const uint32_t slot = gs % p.ns;
-      if (!dead && *reinterpret_cast<volatile int*>(&sh.abort)) dead = true;
-      if (!dead && !wait_full(p, q, slot, (gs / p.ns) & 1)) {
-        dead = true;
-        sh.abort = 1;
-      }
-      if (!dead) {
-        const uint32_t ng = min(gps, NG - g0);
-        const uint8_t* stage = ring_of() + (size_t)slot * kStageBytes;
-        stage_dispatch(R, L, stage, ng, run, roff, rot, g0 * kGroupCols, planes, gpl, pitch, lcap, acc);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_of(p)[slot]);
+    const uint32_t col0 = warp * 16;
+#define CK_PANEL(r, l)                                                                              \
+  case r * 16 + l:                                                                                  \
+    dead = panel_stages<r, l>(p, q, rp, NG, gps, run, roff, pc, col0, planes, gpl, pitch, lcap, sh, \
+                              dead, acc);                                                           \
+    break;
+#define CK_PANELS(r) CK_PANEL(r, 1) CK_PANEL(r, 2) CK_PANEL(r, 3) CK_PANEL(r, 4) CK_PANEL(r, 8)
+    switch (R * 16 + (uint32_t)L) {
+      CK_PANELS(1) CK_PANELS(2) CK_PANELS(3)
+      default: break;
     }
+#undef CK_PANELS
+#undef CK_PANEL
     // this warp's partial sums of the panel's rows, limbs combined (zero without stages)
 #pragma unroll
     for (int j = 0; j < kRMax; ++j) {
@@ -944,7 +1015,8 @@ __device__ __forceinline__ bool attention(const StepParams& p, const Pos& q, uin
 
 
 __device__ __forceinline__ void consumers(const StepParams& p, const Pos& q, Shared& sh) {
-  uint32_t epoch = 0, gs = 0;
+  uint32_t epoch = 0;
+  RingPos rp = {0u, 0u};
   Best best;
   best.v = LLONG_MIN;
   best.i = 0xFFFFFFFFu;
@@ -965,7 +1037,7 @@ __device__ __forceinline__ void consumers(const StepParams& p, const Pos& q, Sha
       unsigned long long S;
       uint32_t lcap;
       const int L = prologue(p, q, m, sh, &S, &lcap);
-      consume_phase(p, q, m, l, L, S, lcap, gs, sh, best);
+      consume_phase(p, q, m, l, L, S, lcap, rp, sh, best);
       consumer_bar();
       if (sh.abort) return;
       if (kind == kCLS) {
@@ -1048,7 +1120,7 @@ __device__ __forceinline__ void step_body(const StepParams& p, uint8_t* work, Sh
     sh.abort = 0;
     for (uint32_t s = 0; s < p.ns; ++s) {
       mbar_init(&full_of(p)[s], 1);
-      mbar_init(&empty_of(p)[s], 1);  // the stage's owner warp releases it
+      mbar_init(&empty_of(p)[s], kNCW);  // every consumer warp releases every slot
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }

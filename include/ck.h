@@ -109,7 +109,7 @@ int ck_model_config(const ck_model* m, ck_config* out);
 #define CK_PATH_KERNELS 2
 int ck_set_path(ck_model* m, int path);
 
-/* Caps the number of shared-memory ring slots (24 KB each) the one-position kernel uses;
+/* Caps the number of shared-memory ring slots (22 KB each) the one-position kernel uses;
  * 0 (the default) takes as many as fit, up to 8.  A tuning and testing control: fewer
  * slots prefetch less weight data across phase boundaries; the results are the same bits.
  * Drops the model's cached graphs.  Errors: 10 for 1 or more than 8. */
@@ -121,6 +121,12 @@ int ck_set_step_slots(ck_model* m, uint32_t max_slots);
  * and sums.  A tuning and testing control: the results are the same bits.  Drops the
  * model's cached graphs.  Errors: 10 for a null handle. */
 int ck_set_attention_split(ck_model* m, uint32_t positions);
+
+/* How far ahead of its shared-memory ring each block of the one-position kernel prefetches
+ * weights into L2, in KB (0, the default: none).  Prefetches keep HBM
+ * streaming while the blocks synchronise.  A tuning control: the results are the same
+ * bits.  Drops the model's cached graphs.  Errors: 10 for a null handle or above 4096. */
+int ck_set_step_prefetch(ck_model* m, uint32_t kb_per_block);
 /* Frees the host handle and its cached CUDA graphs (not dev_mem). */
 void ck_free_model(ck_model* m);
 

@@ -172,6 +172,7 @@ def test_step_kernel_with_a_small_ring(ck, slots):
     assert rco == rcg == 0
     compare_states(P.orc, so, ck.state_download(sg), wl.n_prompt, wl.steps, f"slots {slots}", turns=False)
     assert P.gpu.set_step_slots(1) == 10
+    assert P.gpu.set_step_slots(9) == 10
 
 
 @pytest.mark.parametrize("name,split", [("gqa", 1), ("gqa", 3), ("tiny_ws", 1), ("gqa_tied", 2)])
