@@ -523,23 +523,28 @@ bool plan_step(const ck_model* m, const StateLayout& lay, StepParams* sp, int* g
       std::max<uint64_t>((uint64_t)c.dim + 2 * (uint64_t)m->kv_dim, 2 * (uint64_t)c.hidden),
       std::max<uint64_t>((uint64_t)c.dim, (uint64_t)c.vocab));
   const uint64_t scale_cap = 2 * (((max_rows + 1) / 2 + G - 1) / G) + 2;
-  const uint64_t xb = (std::max<uint64_t>(attn, planes + 4 * scale_cap + 4 * hd) + 15) & ~15ull;
+  // X region: planes, row scales, rotary row, residual slice, next norm's weights slice
+  const uint64_t x_vslice = (planes + 4 * scale_cap + 4 * hd + 15) & ~15ull;
+  const uint64_t x_wslice = x_vslice + 8 * scale_cap;
+  const uint64_t xb = (std::max<uint64_t>(attn, x_wslice + 4 * scale_cap) + 15) & ~15ull;
   const uint64_t red = (uint64_t)step_red_bytes();
   const uint64_t avail = (uint64_t)m->step_smem;
-  if (avail < xb + red + 2 * (kStageBytes + 16)) return false;
-  uint64_t ns = (avail - xb - red) / (kStageBytes + 16);
+  if (avail < xb + red + 2 * (kStageBytes + 16) + 16) return false;
+  uint64_t ns = (avail - xb - red - 16) / (kStageBytes + 16);
   if (ns > kMaxSlots) ns = kMaxSlots;
   if (m->max_slots && ns > m->max_slots) ns = m->max_slots;
   if (ns < 2) return false;
-  // work region: counters, attention maxima and sums, classifier candidates, attention
-  // accumulators, global planes
-  const uint64_t off_part = 4096;
+  // work region: cleared counters and sums, attention partials, classifier candidates,
+  // attention accumulators, the three plane buffers of the phase inputs
+  const uint64_t off_hsync = 256, off_hfin = off_hsync + 4ull * c.heads;
+  const uint64_t zero_bytes = (off_hfin + 4ull * c.heads + 255) & ~255ull;
+  const uint64_t off_part = zero_bytes;
   const uint64_t off_cand = off_part + 16ull * c.heads * gh;
   const uint64_t off_oacc = (off_cand + 16ull * G + 255) & ~255ull;
-  const uint64_t off_gplanes = (off_oacc + 8ull * c.dim + 255) & ~255ull;
-  const uint64_t lcap_min = std::min<uint64_t>(8, planes / max_pitch);
+  const uint64_t off_vbuf = (off_oacc + 8ull * c.dim + 255) & ~255ull;
+  const uint64_t work_need = off_vbuf + 3 * 8 * max_pitch;
   const uint64_t work_bytes = lay.k - lay.scores;
-  if (off_gplanes + (8 - lcap_min) * max_pitch > work_bytes) return false;
+  if (work_need > work_bytes) return false;
   StepParams& p = *sp;
   p = StepParams{};
   p.off_prompt = lay.prompt; p.off_out = lay.out; p.off_x = lay.x; p.off_xb = lay.xb; p.off_q = lay.q;
@@ -552,7 +557,10 @@ bool plan_step(const ck_model* m, const StateLayout& lay, StepParams* sp, int* g
   p.gh = gh; p.att_full = att_full; p.ns = (uint32_t)ns; p.x_bytes = (uint32_t)xb;
   p.pf_bytes = m->pf_kb * 1024u;  // 0 (the default): none
   p.planes_bytes = (uint32_t)planes;
-  p.off_part = off_part; p.off_cand = off_cand; p.off_oacc = off_oacc; p.off_gplanes = off_gplanes;
+  p.zero_bytes = (uint32_t)zero_bytes; p.off_hsync = (uint32_t)off_hsync; p.off_hfin = (uint32_t)off_hfin;
+  p.off_part = off_part; p.off_cand = off_cand; p.off_oacc = off_oacc; p.off_vbuf = off_vbuf;
+  p.vbuf_pitch = (uint32_t)max_pitch;
+  p.x_vslice = (uint32_t)x_vslice; p.x_wslice = (uint32_t)x_wslice;
   p.scale_cap = (uint32_t)scale_cap;
   p.div_dim = make_invdiv(c.dim);
   p.div_hidden = make_invdiv(c.hidden);
@@ -560,16 +568,12 @@ bool plan_step(const ck_model* m, const StateLayout& lay, StepParams* sp, int* g
   p.embed = m->embed; p.embed_scale = m->embed_scale; p.cls = m->cls; p.cls_scale = m->cls_scale;
   p.final_norm = m->final_norm; p.rope = m->rope; p.exp_tab = m->exp_tab; p.silu_tab = m->silu_tab;
   *grid = G;
-  *smem = xb + red + ns * kStageBytes + 16 * ns;
+  *smem = xb + red + ns * kStageBytes + 16 * ns + 16;  // + the plane-copy barrier
   return step_blocks_per_sm(*smem) >= 1;  // every block must be resident for the grid barriers
 }
 
 // Bytes of the work region the one-position kernel uses for a plan.
-size_t step_work_bytes(const StepParams& p) {
-  const uint64_t max_pitch = std::max(p.pitch_d, p.pitch_h);
-  const uint64_t lcap_min = std::min<uint64_t>(8, p.planes_bytes / max_pitch);
-  return p.off_gplanes + (8 - lcap_min) * max_pitch;
-}
+size_t step_work_bytes(const StepParams& p) { return p.off_vbuf + 3ull * 8 * p.vbuf_pitch; }
 
 int enqueue_step(const ck_model* m, uint8_t* st, const StateLayout& lay, bool generating,
                  cudaStream_t s) {
@@ -579,7 +583,7 @@ int enqueue_step(const ck_model* m, uint8_t* st, const StateLayout& lay, bool ge
   if (!plan_step(m, lay, &p, &grid, &smem)) return CK_INVALID_ARGUMENT;
   p.st = st;
   p.generating = generating ? 1u : 0u;
-  CK_CUDA(cudaMemsetAsync(st + lay.scores, 0, 4096, s));  // grid and head barrier counters
+  CK_CUDA(cudaMemsetAsync(st + lay.scores, 0, p.zero_bytes, s));  // counters and per-vector sums
   CK_CUDA(launch_step(p, s, grid, smem));
   return CK_OK;
 }
@@ -940,7 +944,7 @@ int ck_turn_noalloc(ck_model* m, void* dev_state, size_t len, void* stream, ck_t
   CK_CUDA(noalloc_setup(m->step_smem, &work));
   p.st = static_cast<uint8_t*>(dev_state);
   p.generating = pos0 + 1 >= np ? 1u : 0u;
-  CK_CUDA(cudaMemsetAsync(work, 0, 4096, s));  // the counters must start at zero every call
+  CK_CUDA(cudaMemsetAsync(work, 0, p.zero_bytes, s));  // counters and sums start at zero every call
   CK_CUDA(launch_step_noalloc(p, work, s, grid, smem));
   HostHeader h1;
   rc = read_header(dev_state, &h1, s);

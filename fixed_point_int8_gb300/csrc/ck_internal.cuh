@@ -270,10 +270,17 @@ struct StepParams {
   uint32_t x_bytes;     // planes, row scales and rotary row / attention region
   uint32_t planes_bytes;  // shared memory for byte planes; a phase keeps
                           // min(8, planes_bytes / pitch) planes there, the rest in global
-  uint64_t off_part;    // from the work region start: attention maxima and sums [heads*gh][2]
+  // work region (offsets from its start); [0, zero_bytes) is cleared before every launch:
+  // barrier and abort words, the per-vector sums and the per-head counters
+  uint32_t zero_bytes;
+  uint32_t off_hsync, off_hfin;  // per-head barrier counters and finish counters
+  uint64_t off_part;    // attention maxima and sums [heads*gh][2]
   uint64_t off_cand;    // classifier candidates [grid][2]
   uint64_t off_oacc;    // attention output accumulators [dim] (u64, before the >> 24)
-  uint64_t off_gplanes; // global byte planes of limbs beyond the shared-memory ones
+  uint64_t off_vbuf;    // byte planes of the phase inputs: three buffers of 8 x vbuf_pitch
+  uint32_t vbuf_pitch;  // bytes per plane slot (the widest padded vector)
+  uint32_t x_vslice, x_wslice;  // X region: this block's residual slice (i64) and the next
+                                // norm's weights for it (i32), scale_cap entries each
   uint32_t scale_cap;   // most rows any block takes in one matrix
   InvDiv div_dim, div_hidden;  // for the mean of squares
   const DevLayer* layers_tab;

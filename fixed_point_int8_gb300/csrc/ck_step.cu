@@ -35,29 +35,26 @@ constexpr int kCT = 32 * kNCW;          // consumer threads
 constexpr int kThreads = kCT + 32;      // plus one producer warp
 constexpr uint32_t kPollLimit = 1u << 22;
 constexpr int kRMax = (int)(kPanelRows / 32);  // rows a lane accumulates
-constexpr uint32_t kBlockElems = 16u * kCT;     // prologue: 16 consecutive elements a thread
 
-// work area offsets (bytes from the start of the state's scores/work region); [0, 4096) is
-// zeroed before every launch
-constexpr uint32_t kWBar = 0, kWAbort = 4, kWHeads = 64;
+// work area offsets (bytes from the start of the state's scores/work region); the first
+// zero_bytes are cleared before every launch
+constexpr uint32_t kWBar = 0, kWAbort = 4;  // then the per-vector sums (8 .. 80)
 
-enum Pro : int { kPPlain = 0, kPNorm = 1, kPEmbedNorm = 2, kPAcc = 3 };
-enum Epi : int { kEStore = 0, kEQKV = 1, kESiLU = 2, kELogits = 3 };
+enum Epi : int { kEResid = 0, kEQKV = 1, kESiLU = 2, kELogits = 3 };
 enum Kind : int { kQKV = 0, kATT = 1, kO = 2, kGU = 3, kDOWN = 4, kCLS = 5, kEND = 6 };
 
 struct MR {
   const uint8_t* W;  // column-group layout
   const uint32_t* scale;
   uint32_t pitch, rows, cols;
-  int pro;
-  const int64_t* in;
-  const int64_t* add;
-  int64_t* res_out;
-  const int32_t* norm_w;
+  uint32_t vin;               // index of the input vector (see "phase inputs")
   int epi;
-  int64_t* out;
-  int32_t* kc;
+  int64_t* out;               // Q/K/V: the rotated queries; classifier: the logits
+  int32_t* kc;                // Q/K/V: this layer's key and value cache
   int32_t* vc;
+  const int64_t* res_in;      // O, DOWN: the residual stream the outputs add to
+  int64_t* res_out;           // O, DOWN: the sum (the next norm's input)
+  const int32_t* next_norm;   // O, DOWN: the next norm's weights (nullptr: none)
 };
 
 struct Shared {
@@ -66,6 +63,7 @@ struct Shared {
   uint32_t am_i[kNCW];
   unsigned long long S, orv;
   int abort;
+  int last;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -134,41 +132,37 @@ __device__ __forceinline__ int64_t* st64(const StepParams& p, uint64_t off) {
   return reinterpret_cast<int64_t*>(p.st + off);
 }
 
-// The matrix-row phase of kind `k` in layer l:
-//   QKV   attention norm of x (+ y of the previous layer, the sum kept in x), Q/K/V rows,
-//         rotary on Q and K, checked cache stores of K and V
-//   O     the head outputs (accumulators >> 24) times Wo, into y
-//   GU    feed-forward norm of x + y (the sum kept in xb), gate and up rows, SiLU gating, h
-//   DOWN  h times W2, into y
-//   CLS   final norm of xb + y (the sum kept in x), the classifier rows into the logits
+// The matrix-row phase of kind `k` in layer l ("The forward pass, in order"):
+//   QKV   the attention norm's output times Wq, Wk, Wv; rotary on Q and K, checked cache
+//         stores of K and V
+//   O     the head outputs times Wo; x + y goes to xb (the feed-forward norm's input)
+//   GU    the feed-forward norm's output times the gate and up rows; SiLU gating gives h
+//   DOWN  h times W2; xb + y goes to x (the next layer's, or the final, norm's input)
+//   CLS   the final norm's output times the classifier rows into the logits
 __device__ __forceinline__ MR matrow_of(const StepParams& p, const Pos& q, uint32_t l, int k) {
   MR m = {};
   const DevLayer* W = p.layers_tab + l;
   int64_t* x = st64(p, p.off_x);
   int64_t* xb = st64(p, p.off_xb);
-  int64_t* y = st64(p, p.off_y);
   if (k == kQKV) {
     m.W = W->wqkv; m.scale = W->sqkv; m.pitch = p.pitch_d; m.rows = p.dim + 2 * p.kv_dim; m.cols = p.dim;
-    m.pro = l == 0 ? kPEmbedNorm : kPNorm;
-    m.in = xb; m.add = l == 0 ? nullptr : y; m.res_out = x; m.norm_w = W->attn_norm;
-    m.epi = kEQKV; m.out = st64(p, p.off_q);
+    m.vin = 4 * l; m.epi = kEQKV; m.out = st64(p, p.off_q);
     const size_t lw = (size_t)p.cache * p.kv_dim;
     m.kc = reinterpret_cast<int32_t*>(p.st + p.off_k) + l * lw;
     m.vc = reinterpret_cast<int32_t*>(p.st + p.off_v) + l * lw;
   } else if (k == kO) {
     m.W = W->wo; m.scale = W->so; m.pitch = p.pitch_d; m.rows = p.dim; m.cols = p.dim;
-    m.pro = kPAcc; m.in = reinterpret_cast<const int64_t*>(q.work + p.off_oacc); m.epi = kEStore; m.out = y;
+    m.vin = 4 * l + 1; m.epi = kEResid; m.res_in = x; m.res_out = xb; m.next_norm = W->ffn_norm;
   } else if (k == kGU) {
     m.W = W->w13; m.scale = W->s13; m.pitch = p.pitch_d; m.rows = 2 * p.hidden; m.cols = p.dim;
-    m.pro = kPNorm; m.in = x; m.add = y; m.res_out = xb; m.norm_w = W->ffn_norm;
-    m.epi = kESiLU; m.out = st64(p, p.off_h);
+    m.vin = 4 * l + 2; m.epi = kESiLU;
   } else if (k == kDOWN) {
     m.W = W->w2; m.scale = W->s2; m.pitch = p.pitch_h; m.rows = p.dim; m.cols = p.hidden;
-    m.pro = kPPlain; m.in = st64(p, p.off_h); m.epi = kEStore; m.out = y;
+    m.vin = 4 * l + 3; m.epi = kEResid; m.res_in = xb; m.res_out = x;
+    m.next_norm = l + 1 < p.layers ? W[1].attn_norm : (p.generating ? p.final_norm : nullptr);
   } else {  // classifier
     m.W = p.cls; m.scale = p.cls_scale; m.pitch = p.pitch_d; m.rows = p.vocab; m.cols = p.dim;
-    m.pro = kPNorm; m.in = xb; m.add = y; m.res_out = x; m.norm_w = p.final_norm;
-    m.epi = kELogits; m.out = st64(p, p.off_logits);
+    m.vin = 4 * p.layers; m.epi = kELogits; m.out = st64(p, p.off_logits);
   }
   return m;
 }
@@ -268,52 +262,63 @@ __device__ __forceinline__ void cursor_next(const StepParams& p, const Pos& q, S
   c.done = !cursor_matrix(p, q, c);
 }
 
-// The producer: fills ring slot gs % ns with stage gs once the slot's previous stage is
-// released, and keeps L2 prefetches of the following stages about pf_bytes ahead of the
-// fills, so that HBM keeps streaming while the consumers are in barriers, prologues or
-// attention and the ring is full.
+// The producer warp: fills ring slot gs % ns with stage gs once the slot's previous stage
+// is released (lane 0 waits and arms the slot's barrier, then lane j issues the bulk copy
+// of the stage's group j), and optionally keeps L2 prefetches of the following stages
+// about pf_bytes ahead of the fills, so that HBM keeps streaming while the consumers are in
+// barriers, prologues or attention and the ring is full.
 __device__ void producer(const StepParams& p, const Pos& q) {
+  const uint32_t lane = threadIdx.x & 31;
   uint64_t* full = full_of(p);
   const uint32_t ns = p.ns;
   StageCursor fc, pc;
   cursor_start(p, q, fc);
   cursor_start(p, q, pc);
   unsigned long long filled = 0, fetched = 0;  // bytes
-  uint32_t gs = 0;
-  bool ok = true;
+  uint32_t gs = 0, slot = 0, epar = 0;  // epar: parity of the slot's previous release
+  bool stop = false;
   for (; !fc.done; cursor_next(p, q, fc), ++gs) {
     const uint32_t run = fc.pn * kGroupCols;
     const uint32_t ng = min(fc.gps, fc.NG - fc.g0);
+    const size_t gstride = (size_t)fc.rows * kGroupCols;
     // prefetch ahead (the fill cursor never passes the prefetch cursor)
     while (p.pf_bytes && !pc.done && fetched < filled + ng * run + p.pf_bytes) {
       const uint32_t prun = pc.pn * kGroupCols, png = min(pc.gps, pc.NG - pc.g0);
       const uint8_t* src = pc.W + (size_t)(pc.rb + pc.p0) * kGroupCols + (size_t)pc.g0 * pc.rows * kGroupCols;
-      for (uint32_t gl = 0; gl < png; ++gl) prefetch_l2(src + (size_t)gl * pc.rows * kGroupCols, prun);
+      for (uint32_t gl = lane; gl < png; gl += 32) prefetch_l2(src + (size_t)gl * pc.rows * kGroupCols, prun);
       fetched += (unsigned long long)png * prun;
       cursor_next(p, q, pc);
     }
-    const uint32_t slot = gs % ns;
-    if (gs >= ns && !producer_wait_empty(p, q, slot, ((gs / ns) - 1) & 1)) {
-      ok = false;
-      break;
+    if (lane == 0) {
+      if (gs >= ns) {
+        if (!producer_wait_empty(p, q, slot, epar)) {
+          stop = true;
+        } else if (!mbar_try(&full[slot], epar)) {
+          atomicExch(gabort_of(q), 1u);  // the slot's last fill never completed: stop, do not re-arm
+          stop = true;
+        }
+      }
+      if (!stop) mbar_expect_tx(&full[slot], ng * run);
     }
-    if (gs >= ns && !mbar_try(&full[slot], ((gs / ns) - 1) & 1)) {
-      atomicExch(gabort_of(q), 1u);  // the slot's last fill never completed: stop, do not re-arm
-      ok = false;
-      break;
+    stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
+    if (stop) break;
+    for (uint32_t gl = lane; gl < ng; gl += 32) {  // small panels put many groups in a stage
+      uint8_t* dst = ring_of() + (size_t)slot * kStageBytes + (size_t)gl * run;
+      const uint8_t* src = fc.W + (size_t)(fc.rb + fc.p0) * kGroupCols + (size_t)(fc.g0 + gl) * gstride;
+      bulk_g2s(dst, src, run, &full[slot]);
     }
-    mbar_expect_tx(&full[slot], ng * run);
-    uint8_t* dst = ring_of() + (size_t)slot * kStageBytes;
-    const uint8_t* src = fc.W + (size_t)(fc.rb + fc.p0) * kGroupCols + (size_t)fc.g0 * fc.rows * kGroupCols;
-    for (uint32_t gl = 0; gl < ng; ++gl)
-      bulk_g2s(dst + (size_t)gl * run, src + (size_t)gl * fc.rows * kGroupCols, run, &full[slot]);
     filled += (unsigned long long)ng * run;
+    if (++slot == ns) {  // stage gs + 1 = k ns: from k = 2 on, each wrap flips the parity
+      slot = 0;
+      if (gs + 1 > ns) epar ^= 1u;
+    }
   }
-  (void)ok;
   // wait (bounded) for every copy still in flight before the CTA may exit
-  for (uint32_t j = gs > ns ? gs - ns : 0; j < gs; ++j) {
-    for (uint32_t i = 0; i < kPollLimit; ++i)
-      if (mbar_try(&full[j % ns], (j / ns) & 1)) break;
+  if (lane == 0) {
+    for (uint32_t j = gs > ns ? gs - ns : 0; j < gs; ++j) {
+      for (uint32_t i = 0; i < kPollLimit; ++i)
+        if (mbar_try(&full[j % ns], (j / ns) & 1)) break;
+    }
   }
 }
 
@@ -392,217 +397,188 @@ __device__ void consumer_sum_or(unsigned long long& s, unsigned long long& o, Sh
   o = b;
 }
 
-// The phase input for elements e0 .. e0+15 (e0 a multiple of 16): the embedding row of the
-// token (phase 3), the attention accumulators >> 24, or in (+ add).  Zeros at and beyond n.
-__device__ __forceinline__ void load16(const StepParams& p, const Pos& q, const MR& m, uint32_t e0,
-                                       int64_t (&x)[16]) {
-  const uint32_t n = m.cols;
-  if (m.pro == kPEmbedNorm) {
-    const int64_t s = (int64_t)__ldg(p.embed_scale + q.tok);
-    uint4 b = make_uint4(0u, 0u, 0u, 0u);
-    if (e0 < n) b = __ldg(reinterpret_cast<const uint4*>(p.embed + grouped_offset(p.vocab, q.tok, e0)));
+// ------------------------------------------------------------------ phase inputs
+// Every matrix phase reads its input vector (index vin: 4l + 0 the attention norm's output,
+// 4l + 1 the head outputs, 4l + 2 the feed-forward norm's output, 4l + 3 h, 4L the final
+// norm's output) as byte planes: plane k holds byte k of every element.  The planes sit in
+// one of three global buffers (vin mod 3), written by the blocks that produce the elements,
+// together with two sums over the vector (the wrapping sum S for the -128 * S correction
+// and the OR of |x| that sets the limb count); a phase starts with one bulk copy of them
+// into shared memory.  Norm inputs also need the wrapping sum of squares SS of the
+// residual they normalise, added up by the blocks that produce the residual.  The sums live
+// in the cleared part of the work region in three slots (vin mod 3); the slot of vin + 2 is
+// cleared while phase vin runs (its last readers finished before that phase's barrier, and
+// its first writers come after the next one).
+constexpr int kSumS = 0, kSumOr = 1, kSumSq = 2;
+__device__ __forceinline__ unsigned long long* vsum(const Pos& q, int kind, uint32_t vin) {
+  return reinterpret_cast<unsigned long long*>(q.work + 8) + 3 * kind + vin % 3;
+}
+__device__ __forceinline__ unsigned long long vsum_ld(const Pos& q, int kind, uint32_t vin) {
+  return *reinterpret_cast<volatile unsigned long long*>(vsum(q, kind, vin));
+}
+__device__ __forceinline__ uint8_t* vbuf(const StepParams& p, const Pos& q, uint32_t vin) {
+  return q.work + p.off_vbuf + (size_t)(vin % 3) * 8 * p.vbuf_pitch;
+}
+__device__ __forceinline__ uint64_t* pbar_of(const StepParams& p) { return empty_of(p) + p.ns; }
+
+// The eight bytes of v into planes 0..7 at column c.
+__device__ __forceinline__ void put_planes(uint8_t* buf, uint32_t pitch, uint32_t c, int64_t v) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) buf[(size_t)k * pitch + c] = (uint8_t)((uint64_t)v >> (8 * k));
+}
+
+// Limb count of a vector from the OR of |x|: 1 to 4, or 8 (the consumers' bodies).
+__device__ __forceinline__ int limbs_of(unsigned long long orv) {
+  int L = 1;
+  while (L < 8 && (orv >> (8 * L - 1)) != 0) ++L;
+  return L > 4 ? 8 : L;
+}
+
+// Adds this block's partial sums of a vector into its slot (one atomic each).
+__device__ void add_vector_sums(const Pos& q, uint32_t vin, unsigned long long s, unsigned long long o,
+                                Shared& sh) {
+  consumer_sum_or(s, o, sh);
+  if (threadIdx.x == 0) {
+    atomicAdd(vsum(q, kSumS, vin), s);
+    atomicOr(vsum(q, kSumOr, vin), o);
+  }
+}
+
+__device__ __forceinline__ void mbar_expect(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes)
+               : "memory");
+}
+
+// "RMS normalization" of this block's slice of a norm input: rms = isqrt(SS/n + 42,950),
+// at least 1, then y = ((x * w) / rms) >> 8 with the division truncating toward zero, from
+// the residual slice and the weights staged in shared memory; the bytes of y go to the
+// vector's planes and the block's sums to its slot.
+__device__ void distribute(const StepParams& p, const Pos& q, uint32_t vin, Shared& sh) {
+  uint32_t rb, re;
+  cta_rows(p.dim, blockIdx.x, gridDim.x, rb, re);
+  const int64_t* vs = reinterpret_cast<const int64_t*>(xreg(p) + p.x_vslice);
+  const int32_t* ws = reinterpret_cast<const int32_t*>(xreg(p) + p.x_wslice);
+  uint64_t rms = isqrt_u64(udiv_inv(vsum_ld(q, kSumSq, vin), p.div_dim) + 42950ull);
+  if (rms < 1) rms = 1;
+  const InvDiv D = make_invdiv((uint32_t)rms);
+  uint8_t* buf = vbuf(p, q, vin);
+  unsigned long long S = 0, orv = 0;
+  for (uint32_t t = threadIdx.x; t < re - rb; t += kCT) {
+    const int64_t y = sdiv_trunc(wmul(vs[t], (int64_t)ws[t]), D) >> 8;
+    put_planes(buf, p.pitch_d, rb + t, y);
+    S += (unsigned long long)y;
+    orv |= (unsigned long long)(y ^ (y >> 63));
+  }
+  add_vector_sums(q, vin, S, orv, sh);
+}
+
+// Vector 0, phase 3 and the first attention norm: every block adds up the squares of the
+// whole embedding row itself (it is only dim bytes), then writes its slice of the residual
+// x = ((byte - 128) * scale) >> 8 and of the normalised planes.
+__device__ void distribute_embed(const StepParams& p, const Pos& q, Shared& sh) {
+  const int64_t s = (int64_t)__ldg(p.embed_scale + q.tok);
+  unsigned long long ss = 0, dummy = 0;
+  for (uint32_t e0 = 16 * threadIdx.x; e0 < p.dim; e0 += 16 * kCT) {
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(p.embed + grouped_offset(p.vocab, q.tok, e0)));
     const uint32_t wd[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const int64_t byte = (int64_t)((wd[i >> 2] >> (8 * (i & 3))) & 0xFFu);
-      x[i] = e0 + i < n ? (byte - 128) * s >> 8 : 0;
-    }
-    return;
-  }
-  if (e0 + 16 <= n) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const longlong2 v = *reinterpret_cast<const longlong2*>(m.in + e0 + 2 * j);
-      x[2 * j] = v.x;
-      x[2 * j + 1] = v.y;
-    }
-    if (m.add) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const longlong2 v = *reinterpret_cast<const longlong2*>(m.add + e0 + 2 * j);
-        x[2 * j] = wadd(x[2 * j], v.x);
-        x[2 * j + 1] = wadd(x[2 * j + 1], v.y);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      int64_t v = 0;
-      if (e0 + i < n) {
-        v = m.in[e0 + i];
-        if (m.add) v = wadd(v, m.add[e0 + i]);
-      }
-      x[i] = v;
+      const int64_t x = ((int64_t)((wd[i >> 2] >> (8 * (i & 3))) & 0xFFu) - 128) * s >> 8;
+      if (e0 + i < p.dim) ss += (unsigned long long)x * (unsigned long long)x;
     }
   }
-  if (m.pro == kPAcc) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] >>= 24;
+  consumer_sum_or(ss, dummy, sh);
+  uint64_t rms = isqrt_u64(udiv_inv(ss, p.div_dim) + 42950ull);
+  if (rms < 1) rms = 1;
+  const InvDiv D = make_invdiv((uint32_t)rms);
+  uint32_t rb, re;
+  cta_rows(p.dim, blockIdx.x, gridDim.x, rb, re);
+  int64_t* x = st64(p, p.off_x);
+  const int32_t* w = p.layers_tab[0].attn_norm;
+  uint8_t* buf = vbuf(p, q, 0);
+  unsigned long long S = 0, orv = 0;
+  for (uint32_t r = rb + threadIdx.x; r < re; r += kCT) {
+    const int64_t xv = ((int64_t)p.embed[grouped_offset(p.vocab, q.tok, r)] - 128) * s >> 8;
+    x[r] = xv;
+    const int64_t y = sdiv_trunc(wmul(xv, (int64_t)__ldg(w + r)), D) >> 8;
+    put_planes(buf, p.pitch_d, r, y);
+    S += (unsigned long long)y;
+    orv |= (unsigned long long)(y ^ (y >> 63));
   }
+  add_vector_sums(q, 0, S, orv, sh);
 }
 
-// The norm weights of elements e0 .. e0+15 (zeros beyond n).
-__device__ __forceinline__ void load_w16(const MR& m, uint32_t e0, int32_t (&w)[16]) {
-  const uint32_t n = m.cols;
-  if (e0 + 16 <= n) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int4 v = __ldg(reinterpret_cast<const int4*>(m.norm_w + e0 + 4 * j));
-      w[4 * j] = v.x;
-      w[4 * j + 1] = v.y;
-      w[4 * j + 2] = v.z;
-      w[4 * j + 3] = v.w;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) w[i] = e0 + i < n ? __ldg(m.norm_w + e0 + i) : 0;
-  }
-}
-
-// Planes k0 .. k1-1 of the 16 values: plane k's bytes (byte k of each value, in element
-// order) are 16 bytes at base + (k - kbase) * pitch + e0.  A 4 x 4 byte transpose of each
-// group of four values gives their four low (or high) plane words.
-__device__ __forceinline__ void store_planes(const int64_t (&y)[16], uint8_t* base, uint32_t pitch,
-                                             uint32_t e0, uint32_t k0, uint32_t k1, uint32_t kbase) {
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    if ((uint32_t)(4 * half) >= k1 || (uint32_t)(4 * half + 4) <= k0) continue;
-    uint32_t pw[4][4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t a = (uint32_t)((uint64_t)y[4 * q] >> (32 * half));
-      const uint32_t b = (uint32_t)((uint64_t)y[4 * q + 1] >> (32 * half));
-      const uint32_t cc = (uint32_t)((uint64_t)y[4 * q + 2] >> (32 * half));
-      const uint32_t d = (uint32_t)((uint64_t)y[4 * q + 3] >> (32 * half));
-      const uint32_t ab0 = __byte_perm(a, b, 0x5140), ab1 = __byte_perm(a, b, 0x7362);
-      const uint32_t cd0 = __byte_perm(cc, d, 0x5140), cd1 = __byte_perm(cc, d, 0x7362);
-      pw[0][q] = __byte_perm(ab0, cd0, 0x5410);
-      pw[1][q] = __byte_perm(ab0, cd0, 0x7632);
-      pw[2][q] = __byte_perm(ab1, cd1, 0x5410);
-      pw[3][q] = __byte_perm(ab1, cd1, 0x7632);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t k = 4 * half + j;
-      if (k < k0 || k >= k1) continue;
-      *reinterpret_cast<uint4*>(base + (size_t)(k - kbase) * pitch + e0) =
-          make_uint4(pw[j][0], pw[j][1], pw[j][2], pw[j][3]);
-    }
-  }
-}
-
-// Packs the phase's input vector into byte planes (after the residual and the RMS
-// normalization where the phase has them): planes below *lcap_out in shared memory, the
-// others (only when the vector needs them) in the global copy.  Returns the limb count and
-// *S_out the wrapping sum of the packed vector.  Also stages this CTA's row scales and (for
-// Q/K/V) the position's rotary row in shared memory, and for Q/K/V block 0 clears the
-// attention accumulators that this layer's attention adds into.
-__device__ __forceinline__ int prologue(const StepParams& p, const Pos& q, const MR& m, Shared& sh,
-                                        unsigned long long* S_out, uint32_t* lcap_out) {
-  const uint32_t n = m.cols, pitch = m.pitch;
-  uint8_t* X = xreg(p);
-  const uint32_t nblk = (pitch + kBlockElems - 1) / kBlockElems;
+// Start of a matrix phase: one bulk copy of the input's planes 0..3 into shared memory
+// (and 4..7 when the vector needs more than four limbs and they fit), the vector's sums,
+// this block's row scales and (Q/K/V) the position's rotary row, and (O, DOWN) the residual
+// slice the outputs add to with the next norm's weights for it.  Block 0 also clears the
+// sums' slot of vector vin + 2 and, for Q/K/V, the attention accumulators.  Returns the
+// limb count; *S_out the wrapping sum, *lcap_out the planes held in shared memory.
+__device__ int fetch_prologue(const StepParams& p, const Pos& q, const MR& m, Shared& sh, uint32_t& ppar,
+                              unsigned long long* S_out, uint32_t* lcap_out) {
+  const uint32_t pitch = m.pitch, tid = threadIdx.x;
   uint32_t lcap = p.planes_bytes / pitch;
   if (lcap > 8) lcap = 8;
-  const bool writer = blockIdx.x == 0;
-  const bool norm = m.pro == kPNorm || m.pro == kPEmbedNorm;
-  const uint32_t tid = threadIdx.x, et = 16 * tid;
   uint32_t rb, re;
   cta_rows(m.rows, blockIdx.x, gridDim.x, rb, re);
+  uint8_t* X = xreg(p);
   uint32_t* sc = reinterpret_cast<uint32_t*>(X + p.planes_bytes);
   int32_t* rp = reinterpret_cast<int32_t*>(X + p.planes_bytes + 4 * p.scale_cap);
+  int64_t* vs = reinterpret_cast<int64_t*>(X + p.x_vslice);
+  int32_t* ws = reinterpret_cast<int32_t*>(X + p.x_wslice);
   const bool qkv = m.epi == kEQKV;
-  // loads whose results are only stored at the end: in flight during the vector work
+  uint64_t* pbar = pbar_of(p);
+  const uint8_t* src = vbuf(p, q, m.vin);
+  if (tid == 0) {
+    // the planes were written by other blocks' generic stores before the grid barrier
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    mbar_expect(pbar, 4 * pitch);
+    bulk_g2s(X, src, 4 * pitch, pbar);
+  }
+  // loads whose results are only stored at the end: in flight during the rest
   const uint32_t my_row = rb + tid;
   const uint32_t my_scale = my_row < re ? __ldg(m.scale + my_row) : 0u;
   const int32_t my_rope = (qkv && tid < p.hd) ? __ldg(p.rope + (size_t)q.pos * p.hd + tid) : 0;
-  if (qkv && writer) {
-    unsigned long long* acc = reinterpret_cast<unsigned long long*>(q.work + p.off_oacc);
-    for (uint32_t i = tid; i < p.dim; i += kCT) acc[i] = 0ull;
+  const unsigned long long S = vsum_ld(q, kSumS, m.vin);
+  const int L = limbs_of(vsum_ld(q, kSumOr, m.vin));
+  if (tid == 0) {
+    if (L > 4 && lcap > 4) {
+      const uint32_t nb = (lcap - 4) * pitch;
+      mbar_expect(pbar, nb);
+      bulk_g2s(X + 4 * pitch, src + 4 * pitch, nb, pbar);
+    }
+    mbar_arrive(pbar);
   }
-  int64_t x[16];
-  int32_t w[16];
-  InvDiv D = {};
-  if (norm) {
-    // "RMS normalization": rms = isqrt(sum(x*x)/n + 42,950), at least 1
-    unsigned long long ss = 0, dummy = 0;
-    for (uint32_t b = 0; b < nblk; ++b) {
-      const uint32_t e0 = b * kBlockElems + et;
-      if (e0 >= pitch) continue;
-      load16(p, q, m, e0, x);
-      if (nblk == 1) load_w16(m, e0, w);  // in flight while the sums reduce
-#pragma unroll
-      for (int i = 0; i < 16; ++i) ss += (unsigned long long)x[i] * (unsigned long long)x[i];
-      if (writer && m.res_out) {
-        if (e0 + 16 <= n) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            longlong2 v;
-            v.x = x[2 * j];
-            v.y = x[2 * j + 1];
-            *reinterpret_cast<longlong2*>(m.res_out + e0 + 2 * j) = v;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (e0 + i < n) m.res_out[e0 + i] = x[i];
-        }
-      }
+  if (blockIdx.x == 0) {
+    if (tid < 3) *vsum(q, (int)tid, m.vin + 2) = 0ull;
+    if (qkv) {
+      unsigned long long* acc = reinterpret_cast<unsigned long long*>(q.work + p.off_oacc);
+      for (uint32_t i = tid; i < p.dim; i += kCT) acc[i] = 0ull;
     }
-    consumer_sum_or(ss, dummy, sh);
-    const InvDiv& Dn = n == p.dim ? p.div_dim : p.div_hidden;
-    uint64_t rms = isqrt_u64(udiv_inv(ss, Dn) + 42950ull);
-    if (rms < 1) rms = 1;
-    D = make_invdiv((uint32_t)rms);  // every thread alike: no broadcast needed
   }
-  unsigned long long S = 0, orv = 0;
-  for (uint32_t b = 0; b < nblk; ++b) {
-    const uint32_t e0 = b * kBlockElems + et;
-    if (e0 >= pitch) continue;
-    if (!(norm && nblk == 1)) {  // a single block is still in registers
-      load16(p, q, m, e0, x);
-      if (norm) load_w16(m, e0, w);
+  if (m.epi == kEResid) {
+    for (uint32_t t = tid; t < re - rb; t += kCT) {
+      vs[t] = m.res_in[rb + t];
+      ws[t] = m.next_norm ? __ldg(m.next_norm + rb + t) : 0;
     }
-    if (norm) {
-      // y = ((x * w) / rms) >> 8, the division truncating toward zero (zeros beyond n)
-#pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = sdiv_trunc(wmul(x[i], (int64_t)w[i]), D) >> 8;
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      S += (unsigned long long)x[i];
-      orv |= (unsigned long long)(x[i] ^ (x[i] >> 63));
-    }
-    store_planes(x, X, pitch, e0, 0, lcap, 0);
   }
   if (my_row < re) sc[tid] = my_scale;
   for (uint32_t r = my_row + kCT; r < re; r += kCT) sc[r - rb] = __ldg(m.scale + r);
   if (qkv && tid < p.hd) rp[tid] = my_rope;
   for (uint32_t i = tid + kCT; qkv && i < p.hd; i += kCT) rp[i] = __ldg(p.rope + (size_t)q.pos * p.hd + i);
-  consumer_sum_or(S, orv, sh);  // its barriers also publish the planes, scales and rotary row
-  int L = 1;
-  while (L < 8 && (orv >> (8 * L - 1)) != 0) ++L;
-  if (L > 4) L = 8;  // the consumers run 1, 2, 3, 4 or 8 limbs
-  if ((uint32_t)L > lcap) {
-    // A vector beyond 8*lcap bits (rare): its planes lcap..L-1 go to the global copy, which
-    // every block writes with the same bytes after the grid barrier that opened the phase.
-    uint8_t* gpl = q.work + p.off_gplanes;
-    for (uint32_t b = 0; b < nblk; ++b) {
-      const uint32_t e0 = b * kBlockElems + et;
-      if (e0 >= pitch) continue;
-      if (nblk > 1) {  // one block is still in registers
-        load16(p, q, m, e0, x);
-        if (norm) {
-          load_w16(m, e0, w);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) x[i] = sdiv_trunc(wmul(x[i], (int64_t)w[i]), D) >> 8;
-        }
-      }
-      store_planes(x, gpl, pitch, e0, lcap, (uint32_t)L, lcap);
+  bool ok = false;
+  for (uint32_t i = 0; i < kPollLimit; ++i) {
+    if (mbar_try(pbar, ppar)) {
+      ok = true;
+      break;
     }
-    __threadfence_block();
-    consumer_bar();
   }
+  ppar ^= 1u;
+  if (!ok) {
+    atomicExch(gabort_of(q), 1u);
+    sh.abort = 1;
+  }
+  consumer_bar();  // the scales, rotary row and slices of the other threads
   *S_out = S;
   *lcap_out = lcap;
   return L;
@@ -622,19 +598,36 @@ __device__ __forceinline__ void best_update(Best& b, long long v, uint32_t i) {
   }
 }
 
+// Per-thread partial sums of the vector an epilogue produces (see "phase inputs").
+struct OutSums {
+  unsigned long long s, o, sq;
+};
+
 // Epilogue of one row (threads with valid == false only take part in the partner exchange;
-// the partner of an even row is the next thread).
+// the partner of an even row is the next thread).  t is the row's index in this CTA's
+// slice.
 __device__ __forceinline__ void epilogue(const StepParams& p, const Pos& q, const MR& m, uint32_t layer,
-                                         uint32_t row, bool valid, int64_t y, Best& best, const int32_t* rope) {
+                                         uint32_t row, uint32_t t, bool valid, int64_t y, Best& best,
+                                         const int32_t* rope, int64_t* vs, OutSums& os) {
   const int64_t partner = (int64_t)__shfl_xor_sync(0xffffffffu, (unsigned long long)y, 1);
   if (!valid) return;
-  if (m.epi == kEStore) {
-    m.out[row] = y;
+  if (m.epi == kEResid) {
+    // the residual: its sum goes on, to be normalised by the next phase
+    const int64_t v = wadd(vs[t], y);
+    m.res_out[row] = v;
+    vs[t] = v;
+    os.sq += (unsigned long long)v * (unsigned long long)v;
   } else if (m.epi == kELogits) {
     m.out[row] = y;
     best_update(best, y, row);
   } else if (m.epi == kESiLU) {
-    if ((row & 1) == 0) m.out[row >> 1] = wmul(silu_lookup(y, p.silu_tab), partner) >> 16;
+    if ((row & 1) == 0) {
+      // h = (silu(gate) * up) >> 16, straight into the planes of DOWN's input
+      const int64_t h = wmul(silu_lookup(y, p.silu_tab), partner) >> 16;
+      put_planes(vbuf(p, q, m.vin + 1), p.pitch_h, row >> 1, h);
+      os.s += (unsigned long long)h;
+      os.o |= (unsigned long long)(h ^ (h >> 63));
+    }
   } else {  // Q/K/V: rotary on Q and K, checked cache stores for K and V
     const bool even = (row & 1) == 0;
     const int64_t a = even ? y : partner, b = even ? partner : y;
@@ -805,10 +798,12 @@ __device__ __forceinline__ void consume_phase(const StepParams& p, const Pos& q,
   const uint32_t nr = re - rb, npan = panel_count(nr), NG = m.pitch / kGroupCols;
   const uint32_t pitch = m.pitch;
   const uint8_t* planes = xreg(p);
-  const uint8_t* gpl = q.work + p.off_gplanes;
+  const uint8_t* gpl = vbuf(p, q, m.vin) + (size_t)lcap * pitch;  // planes lcap.. in global memory
   const uint32_t* sc = reinterpret_cast<const uint32_t*>(xreg(p) + p.planes_bytes);
   const int32_t* rope = reinterpret_cast<const int32_t*>(xreg(p) + p.planes_bytes + 4 * p.scale_cap);
+  int64_t* vs = reinterpret_cast<int64_t*>(xreg(p) + p.x_vslice);
   unsigned long long* red = red_of(p);
+  OutSums os = {0ull, 0ull, 0ull};
   bool dead = false;
   for (uint32_t pi = 0; pi < npan; ++pi) {
     uint32_t p0, pn;
@@ -865,19 +860,131 @@ __device__ __forceinline__ void consume_phase(const StepParams& p, const Pos& q,
       const unsigned long long t = (sum - (S << 7)) * (unsigned long long)sc[p0 + tid];
       y = (int64_t)t >> 24;
     }
-    epilogue(p, q, m, layer, rb + p0 + tid, valid, y, best, rope);
+    epilogue(p, q, m, layer, rb + p0 + tid, p0 + tid, valid, y, best, rope, vs, os);
     consumer_bar();  // every thread has read the partial sums before the next panel's
+  }
+  // this block's share of the sums of the vector the phase produced
+  if (m.epi == kESiLU) {
+    add_vector_sums(q, m.vin + 1, os.s, os.o, sh);
+  } else if (m.epi == kEResid && m.next_norm) {
+    unsigned long long dummy = 0;
+    consumer_sum_or(os.sq, dummy, sh);
+    if (tid == 0) atomicAdd(vsum(q, kSumSq, m.vin + 1), os.sq);
   }
 }
 
 // ------------------------------------------------------------------ attention
 
-// Phase 9 for this CTA's (head, chunk): "Attention" in four stages over positions 0..pos of
-// the head's cache.  Each CTA adds sum_t P_t * v_t over its chunk of positions into the
-// head's 64-bit accumulators (the O prologue applies the final >> 24).  The maximum and the
-// sum Z need every position: for short contexts each CTA scores all positions itself; for
-// longer ones the CTAs score their own chunks and exchange maxima and sums (two barriers
-// among the head's CTAs).
+constexpr int kAB = 8;  // positions a lane group loads at once: one memory round trip each
+
+// Stage 0 over positions [s0, s0 + n): scores ((q . k) >> 16) * inv >> 24 into sc, lanes
+// along the head dimension (hd / 4 lanes a position, four elements each), kAB positions a
+// lane group per round so that all of a round's key loads are in flight together.
+// Returns the thread's largest score (LLONG_MIN if none).
+__device__ __forceinline__ long long att_scores(const StepParams& p, const int32_t* Kh, uint32_t s0, uint32_t n,
+                                                const int64_t* q_s, long long* sc) {
+  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t lpp = p.hd / 4, ppw = 32 / lpp, sub = lane % lpp, slot = lane / lpp, e0 = sub * 4;
+  const int64_t q0 = q_s[e0], q1 = q_s[e0 + 1], q2 = q_s[e0 + 2], q3 = q_s[e0 + 3];
+  long long lmax = LLONG_MIN;
+  const uint32_t round = kNCW * ppw * kAB;
+  for (uint32_t base = 0; base < n; base += round) {
+    int4 k4[kAB];
+#pragma unroll
+    for (int bb = 0; bb < kAB; ++bb) {
+      const uint32_t tl = base + (bb * kNCW + warp) * ppw + slot;
+      k4[bb] = tl < n ? *reinterpret_cast<const int4*>(Kh + (size_t)(s0 + tl) * p.kv_dim + e0) : make_int4(0, 0, 0, 0);
+    }
+    unsigned long long d[kAB];
+#pragma unroll
+    for (int bb = 0; bb < kAB; ++bb)
+      d[bb] = (unsigned long long)q0 * (unsigned long long)(long long)k4[bb].x +
+              (unsigned long long)q1 * (unsigned long long)(long long)k4[bb].y +
+              (unsigned long long)q2 * (unsigned long long)(long long)k4[bb].z +
+              (unsigned long long)q3 * (unsigned long long)(long long)k4[bb].w;
+    for (uint32_t o = lpp >> 1; o > 0; o >>= 1) {
+#pragma unroll
+      for (int bb = 0; bb < kAB; ++bb) d[bb] += __shfl_xor_sync(0xffffffffu, d[bb], o);
+    }
+#pragma unroll
+    for (int bb = 0; bb < kAB; ++bb) {
+      const uint32_t tl = base + (bb * kNCW + warp) * ppw + slot;
+      if (tl < n && sub == 0) {
+        long long sv = (long long)d[bb] >> 16;
+        sv = (long long)((unsigned long long)sv * (unsigned long long)p.inv_sqrt) >> 24;
+        sc[tl] = sv;
+        lmax = sv > lmax ? sv : lmax;
+      }
+    }
+  }
+  return lmax;
+}
+
+// Stage 3 over positions [t0, t0 + n) and dimensions [dlo, dlo + dn) (dn a multiple of 4):
+// the wrapping sums over positions of P_t * v_t, lanes along the dimensions, kAB positions
+// a lane group per round; the warp's sums over its positions end in part[warp][0 .. dn).
+__device__ __forceinline__ void att_values(const StepParams& p, const int32_t* Vh, uint32_t t0, uint32_t n,
+                                           uint32_t dlo, uint32_t dn, const long long* pr,
+                                           unsigned long long* part) {
+  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t lpp = dn / 4, ppw = 32 / lpp, sub = lane % lpp, slot = lane / lpp, e0 = sub * 4;
+  unsigned long long a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+  const uint32_t round = kNCW * ppw * kAB;
+  for (uint32_t base = 0; base < n; base += round) {
+    int4 v4[kAB];
+    long long pb[kAB];
+#pragma unroll
+    for (int bb = 0; bb < kAB; ++bb) {
+      const uint32_t tl = base + (bb * kNCW + warp) * ppw + slot;
+      v4[bb] = tl < n ? *reinterpret_cast<const int4*>(Vh + (size_t)(t0 + tl) * p.kv_dim + dlo + e0)
+                      : make_int4(0, 0, 0, 0);
+      pb[bb] = tl < n ? pr[tl] : 0;
+    }
+#pragma unroll
+    for (int bb = 0; bb < kAB; ++bb) {
+      a0 += (unsigned long long)(pb[bb] * (long long)v4[bb].x);
+      a1 += (unsigned long long)(pb[bb] * (long long)v4[bb].y);
+      a2 += (unsigned long long)(pb[bb] * (long long)v4[bb].z);
+      a3 += (unsigned long long)(pb[bb] * (long long)v4[bb].w);
+    }
+  }
+  for (uint32_t o = 16; o >= lpp && o > 0; o >>= 1) {
+    a0 += __shfl_xor_sync(0xffffffffu, a0, o);
+    a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+    a2 += __shfl_xor_sync(0xffffffffu, a2, o);
+    a3 += __shfl_xor_sync(0xffffffffu, a3, o);
+  }
+  if (slot == 0) {
+    unsigned long long* dst = part + (size_t)warp * dn + e0;
+    dst[0] = a0;
+    dst[1] = a1;
+    dst[2] = a2;
+    dst[3] = a3;
+  }
+}
+
+// O's input elements o = sum >> 24 of head dimensions [c0, c0 + cn): byte planes and this
+// block's part of the vector's sums.
+__device__ __forceinline__ void att_output(const StepParams& p, const Pos& q, uint32_t l, uint32_t c0, uint32_t cn,
+                                           const unsigned long long* sums, Shared& sh) {
+  uint8_t* buf = vbuf(p, q, 4 * l + 1);
+  unsigned long long S = 0, orv = 0;
+  for (uint32_t j = threadIdx.x; j < cn; j += kCT) {
+    const int64_t o = (int64_t)sums[j] >> 24;
+    put_planes(buf, p.pitch_d, c0 + j, o);
+    S += (unsigned long long)o;
+    orv |= (unsigned long long)(o ^ (o >> 63));
+  }
+  add_vector_sums(q, 4 * l + 1, S, orv, sh);
+}
+
+// Phase 9 for this CTA's (head, share): "Attention" in four stages over positions 0..pos
+// of the head's cache.  The maximum and the sum Z need every position.  Short contexts
+// (up to att_full positions): every CTA of the head scores all positions itself and takes
+// a share of the head's dimensions in stage 3, so its outputs are final.  Longer ones: the
+// CTAs score their own chunks of positions, exchange maxima and sums (two barriers among
+// the head's CTAs), add sum_t P_t * v_t over their chunks into the head's 64-bit
+// accumulators, and the last to finish turns them into the outputs.
 __device__ __forceinline__ bool attention(const StepParams& p, const Pos& q, uint32_t l, Shared& sh) {
   const uint32_t b = blockIdx.x, gh = p.gh;
   if (b >= p.heads * gh) return true;
@@ -891,39 +998,18 @@ __device__ __forceinline__ bool attention(const StepParams& p, const Pos& q, uin
   const bool full = gh == 1 || P <= p.att_full;
   const uint32_t cs = (P + gh - 1) / gh;
   const uint32_t t0 = min(P, ch * cs), t1 = min(P, t0 + cs);
-  const uint32_t s0 = full ? 0u : t0, s1 = full ? P : t1, nsc = s1 - s0;
+  const uint32_t s0 = full ? 0u : t0, nsc = (full ? P : t1) - s0;
   const uint32_t kvh = h / (p.heads / p.kv_heads);
   const size_t lw = (size_t)p.cache * p.kv_dim;
   const int32_t* Kh = reinterpret_cast<const int32_t*>(p.st + p.off_k) + l * lw + (size_t)kvh * hd;
   const int32_t* Vh = reinterpret_cast<const int32_t*>(p.st + p.off_v) + l * lw + (size_t)kvh * hd;
   long long* parts = reinterpret_cast<long long*>(q.work + p.off_part) + (size_t)h * gh * 2;  // [gh][2]
-  uint32_t* hcount = reinterpret_cast<uint32_t*>(q.work + kWHeads) + h;
+  uint32_t* hcount = reinterpret_cast<uint32_t*>(q.work + p.off_hsync) + h;
   const int64_t* qg = st64(p, p.off_q) + (size_t)h * hd;
   for (uint32_t i = tid; i < hd; i += kCT) q_s[i] = qg[i];
   consumer_bar();
-  const uint32_t lpp = hd / 4, ppw = 32 / lpp;
-  const uint32_t sub = lane % lpp, slot = lane / lpp, e0 = sub * 4;
-  const int64_t q0 = q_s[e0], q1 = q_s[e0 + 1], q2 = q_s[e0 + 2], q3 = q_s[e0 + 3];
-  // stage 0: scores ((q . k) >> 16) * inv >> 24 and their maximum
-  long long lmax = LLONG_MIN;
-  for (uint32_t base = warp * ppw; base < nsc; base += kNCW * ppw) {
-    const uint32_t tl = base + slot;
-    unsigned long long d = 0;
-    if (tl < nsc) {
-      const int4 k4 = *reinterpret_cast<const int4*>(Kh + (size_t)(s0 + tl) * p.kv_dim + e0);
-      d = (unsigned long long)q0 * (unsigned long long)(long long)k4.x +
-          (unsigned long long)q1 * (unsigned long long)(long long)k4.y +
-          (unsigned long long)q2 * (unsigned long long)(long long)k4.z +
-          (unsigned long long)q3 * (unsigned long long)(long long)k4.w;
-    }
-    for (uint32_t o = lpp >> 1; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-    if (tl < nsc && sub == 0) {
-      long long s = (long long)d >> 16;
-      s = (long long)((unsigned long long)s * (unsigned long long)p.inv_sqrt) >> 24;
-      sc[tl] = s;
-      lmax = s > lmax ? s : lmax;
-    }
-  }
+  // stage 0: scores and their maximum
+  long long lmax = att_scores(p, Kh, s0, nsc, q_s, sc);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const long long t = __shfl_xor_sync(0xffffffffu, lmax, o);
@@ -963,50 +1049,56 @@ __device__ __forceinline__ bool attention(const StepParams& p, const Pos& q, uin
     Z = 0;
     for (uint32_t j = 0; j < gh; ++j) Z += (unsigned long long)*(volatile long long*)(parts + 2 * j + 1);
   }
-  // stage 2: probabilities (e << 24) / Z over this CTA's chunk [t0, t1)
+  // stage 2: probabilities (e << 24) / Z over the positions stage 3 needs
+  const uint32_t v0 = full ? 0u : t0, nv = full ? P : t1 - t0;
   const bool small_z = Z > 0 && Z <= 0xFFFFFFFFull;
   const InvDiv DZ = make_invdiv(small_z ? (uint32_t)Z : 1u);
-  for (uint32_t t = t0 + tid; t < t1; t += kCT) {
-    const unsigned long long num = (unsigned long long)sc[t - s0] << 24;
-    sc[t - s0] = (long long)(small_z ? udiv_inv(num, DZ) : num / Z);
+  for (uint32_t t = tid; t < nv; t += kCT) {
+    const unsigned long long num = (unsigned long long)sc[v0 - s0 + t] << 24;
+    sc[v0 - s0 + t] = (long long)(small_z ? udiv_inv(num, DZ) : num / Z);
   }
   consumer_bar();
-  // stage 3: sum over the chunk of P * v, added into the head's accumulators
-  const uint32_t nch = t1 - t0;
-  unsigned long long a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-  for (uint32_t base = warp * ppw; base < nch; base += kNCW * ppw) {
-    const uint32_t tl = base + slot;
-    if (tl < nch) {
-      const int4 v4 = *reinterpret_cast<const int4*>(Vh + (size_t)(t0 + tl) * p.kv_dim + e0);
-      const long long pr = sc[t0 - s0 + tl];
-      a0 += (unsigned long long)(pr * (long long)v4.x);
-      a1 += (unsigned long long)(pr * (long long)v4.y);
-      a2 += (unsigned long long)(pr * (long long)v4.z);
-      a3 += (unsigned long long)(pr * (long long)v4.w);
+  if (full) {
+    // stage 3 on this CTA's share of the head's dimensions: final outputs
+    const uint32_t nsplit = min(gh, hd / 4), dn = hd / nsplit;
+    if (ch >= nsplit) return true;
+    att_values(p, Vh, 0, P, ch * dn, dn, sc, part);
+    consumer_bar();
+    unsigned long long* fin = reinterpret_cast<unsigned long long*>(q_s);  // [dn]: q is no longer needed
+    for (uint32_t j = tid; j < dn; j += kCT) {
+      unsigned long long v = 0;
+      for (int w = 0; w < kNCW; ++w) v += part[(size_t)w * dn + j];
+      fin[j] = v;
     }
+    consumer_bar();
+    att_output(p, q, l, h * hd + ch * dn, dn, fin, sh);
+    return true;
   }
-  for (uint32_t o = 16; o >= lpp && o > 0; o >>= 1) {
-    a0 += __shfl_xor_sync(0xffffffffu, a0, o);
-    a1 += __shfl_xor_sync(0xffffffffu, a1, o);
-    a2 += __shfl_xor_sync(0xffffffffu, a2, o);
-    a3 += __shfl_xor_sync(0xffffffffu, a3, o);
-  }
-  if (slot == 0) {
-    unsigned long long* dst = part + (size_t)warp * hd + e0;
-    dst[0] = a0;
-    dst[1] = a1;
-    dst[2] = a2;
-    dst[3] = a3;
-  }
+  // stage 3 on this CTA's chunk of positions, added into the head's accumulators
+  att_values(p, Vh, t0, t1 - t0, 0, hd, sc + (t0 - s0), part);
   consumer_bar();
-  if (nch) {
-    unsigned long long* acc = reinterpret_cast<unsigned long long*>(q.work + p.off_oacc) + (size_t)h * hd;
+  unsigned long long* acc = reinterpret_cast<unsigned long long*>(q.work + p.off_oacc) + (size_t)h * hd;
+  if (t1 > t0) {
     for (uint32_t j = tid; j < hd; j += kCT) {
-      unsigned long long s = 0;
-      for (int w = 0; w < kNCW; ++w) s += part[(size_t)w * hd + j];
-      if (gh == 1) acc[j] = s;  // the only contributor
-      else atomicAdd(acc + j, s);
+      unsigned long long v = 0;
+      for (int w = 0; w < kNCW; ++w) v += part[(size_t)w * hd + j];
+      atomicAdd(acc + j, v);
     }
+  }
+  // the head's last CTA to finish turns the accumulators into O's input
+  __threadfence();
+  consumer_bar();
+  if (tid == 0) {
+    uint32_t* fin = reinterpret_cast<uint32_t*>(q.work + p.off_hfin) + h;
+    sh.last = atomicAdd(fin, 1u) == (l + 1) * gh - 1;
+  }
+  consumer_bar();
+  if (sh.last) {
+    __threadfence();
+    unsigned long long* fin = part;  // [hd], reused
+    for (uint32_t j = tid; j < hd; j += kCT) fin[j] = *reinterpret_cast<volatile unsigned long long*>(acc + j);
+    consumer_bar();
+    att_output(p, q, l, h * hd, hd, fin, sh);
   }
   return true;
 }
@@ -1014,89 +1106,88 @@ __device__ __forceinline__ bool attention(const StepParams& p, const Pos& q, uin
 // ------------------------------------------------------------------ the position
 
 
+// One matrix phase: prologue (planes of its input), the rows, the epilogues.  False on abort.
+__device__ __forceinline__ bool matrix_phase(const StepParams& p, const Pos& q, uint32_t l, int kind,
+                                             RingPos& rp, uint32_t& ppar, Shared& sh, Best& best) {
+  const MR m = matrow_of(p, q, l, kind);
+  unsigned long long S;
+  uint32_t lcap;
+  const int L = fetch_prologue(p, q, m, sh, ppar, &S, &lcap);
+  consume_phase(p, q, m, l, L, S, lcap, rp, sh, best);
+  consumer_bar();
+  return sh.abort == 0;
+}
+
+// The consumer warps' sequence for one position (grid barriers between dependent steps):
+//   embedding and first attention norm (every block its slice)
+//   per layer: QKV | attention (+ O's input) | O (+ residual) | norm slices | GU (+ h) |
+//              DOWN (+ residual) | next norm slices
+//   when the position generates: final norm slices | classifier | maximum pass
 __device__ __forceinline__ void consumers(const StepParams& p, const Pos& q, Shared& sh) {
-  uint32_t epoch = 0;
+  uint32_t epoch = 0, ppar = 0;
   RingPos rp = {0u, 0u};
   Best best;
   best.v = LLONG_MIN;
   best.i = 0xFFFFFFFFu;
-  for (uint32_t l = 0; l <= p.layers; ++l) {
-    for (int k = kQKV; k <= kDOWN; ++k) {
-      int kind = k;
-      if (l == p.layers) {
-        if (k > kQKV) break;
-        kind = p.generating ? kCLS : kEND;
-      }
-      if (!(l == 0 && kind == kQKV) && !grid_sync(q, sh, epoch)) return;
-      if (kind == kEND) return;
-      if (kind == kATT) {
-        if (!attention(p, q, l, sh)) return;
-        continue;
-      }
-      const MR m = matrow_of(p, q, l < p.layers ? l : 0, kind);
-      unsigned long long S;
-      uint32_t lcap;
-      const int L = prologue(p, q, m, sh, &S, &lcap);
-      consume_phase(p, q, m, l, L, S, lcap, rp, sh, best);
-      consumer_bar();
-      if (sh.abort) return;
-      if (kind == kCLS) {
-        // this CTA's first largest logit, then the grid's in the last phase
-        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          Best ob;
-          ob.v = __shfl_xor_sync(0xffffffffu, best.v, o);
-          ob.i = __shfl_xor_sync(0xffffffffu, best.i, o);
-          if (ob.i != 0xFFFFFFFFu) best_update(best, ob.v, ob.i);
-        }
-        if (lane == 0) {
-          sh.am_v[warp] = best.v;
-          sh.am_i[warp] = best.i;
-        }
-        consumer_bar();
-        long long* cand = reinterpret_cast<long long*>(q.work + p.off_cand);
-        if (threadIdx.x == 0) {
-          Best cb;
-          cb.v = LLONG_MIN;
-          cb.i = 0xFFFFFFFFu;
-          for (int w = 0; w < kNCW; ++w)
-            if (sh.am_i[w] != 0xFFFFFFFFu) best_update(cb, sh.am_v[w], sh.am_i[w]);
-          cand[2 * blockIdx.x] = cb.v;
-          cand[2 * blockIdx.x + 1] = (long long)cb.i;
-        }
-        if (!grid_sync(q, sh, epoch)) return;
-        if (blockIdx.x != 0) return;
-        // phase 19 (maximum pass over the per-CTA candidates) and the end of the position
-        if (threadIdx.x == 0) {
-          Best g;
-          g.v = LLONG_MIN;
-          g.i = 0xFFFFFFFFu;
-          for (uint32_t b = 0; b < gridDim.x; ++b) {
-            const long long v = *(volatile const long long*)(cand + 2 * b);
-            const uint32_t i = (uint32_t) * (volatile const long long*)(cand + 2 * b + 1);
-            if (i != 0xFFFFFFFFu) best_update(g, v, i);
-          }
-          uint8_t* st = p.st;
-          if (hdr_ld<uint64_t>(st, kHErrKey) != kNoError) {
-            hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
-            hdr<uint32_t>(st, kHError) = CK_ARITHMETIC;
-          } else {
-            const uint32_t gen = hdr_ld<uint32_t>(st, kHGenerated);
-            reinterpret_cast<uint32_t*>(st + p.off_out)[gen] = g.i;
-            hdr<uint32_t>(st, kHGenerated) = gen + 1;
-            hdr<uint32_t>(st, kHLastTok) = g.i;
-            hdr<long long>(st, kHMaxLogit) = g.v;
-            const bool stop =
-                (hdr_ld<uint32_t>(st, kHFlags) & CK_FLAG_STOP_TOKENS) && (g.i == 1 || g.i == 2);
-            if (gen + 1 == hdr_ld<uint32_t>(st, kHMaxTok) || stop) hdr<uint32_t>(st, kHPhase) = CK_PHASE_DONE;
-            hdr<uint32_t>(st, kHPosition) += 1;
-          }
-        }
-        return;
-      }
+  distribute_embed(p, q, sh);
+  if (!grid_sync(q, sh, epoch)) return;
+  for (uint32_t l = 0; l < p.layers; ++l) {
+    if (!matrix_phase(p, q, l, kQKV, rp, ppar, sh, best)) return;
+    if (!grid_sync(q, sh, epoch)) return;
+    if (!attention(p, q, l, sh)) return;
+    if (!grid_sync(q, sh, epoch)) return;
+    if (!matrix_phase(p, q, l, kO, rp, ppar, sh, best)) return;
+    if (!grid_sync(q, sh, epoch)) return;
+    distribute(p, q, 4 * l + 2, sh);
+    if (!grid_sync(q, sh, epoch)) return;
+    if (!matrix_phase(p, q, l, kGU, rp, ppar, sh, best)) return;
+    if (!grid_sync(q, sh, epoch)) return;
+    if (!matrix_phase(p, q, l, kDOWN, rp, ppar, sh, best)) return;
+    if (!grid_sync(q, sh, epoch)) return;
+    if (l + 1 < p.layers || p.generating) {
+      distribute(p, q, 4 * l + 4, sh);
+      if (!grid_sync(q, sh, epoch)) return;
     }
   }
+  if (!p.generating) return;  // a prompt position: x holds the last residual
+  if (!matrix_phase(p, q, 0, kCLS, rp, ppar, sh, best)) return;
+  // this CTA's first largest logit, then the grid's in the last phase
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Best ob;
+    ob.v = __shfl_xor_sync(0xffffffffu, best.v, o);
+    ob.i = __shfl_xor_sync(0xffffffffu, best.i, o);
+    if (ob.i != 0xFFFFFFFFu) best_update(best, ob.v, ob.i);
+  }
+  if (lane == 0) {
+    sh.am_v[warp] = best.v;
+    sh.am_i[warp] = best.i;
+  }
+  consumer_bar();
+  long long* cand = reinterpret_cast<long long*>(q.work + p.off_cand);
+  if (threadIdx.x == 0) {
+    Best cb;
+    cb.v = LLONG_MIN;
+    cb.i = 0xFFFFFFFFu;
+    for (int w = 0; w < kNCW; ++w)
+      if (sh.am_i[w] != 0xFFFFFFFFu) best_update(cb, sh.am_v[w], sh.am_i[w]);
+    cand[2 * blockIdx.x] = cb.v;
+    cand[2 * blockIdx.x + 1] = (long long)cb.i;
+  }
+  if (!grid_sync(q, sh, epoch)) return;
+  if (blockIdx.x != 0 || threadIdx.x != 0) return;
+  // phase 19: maximum pass over the per-CTA candidates
+  Best g;
+  g.v = LLONG_MIN;
+  g.i = 0xFFFFFFFFu;
+  for (uint32_t b = 0; b < gridDim.x; ++b) {
+    const long long v = *(volatile const long long*)(cand + 2 * b);
+    const uint32_t i = (uint32_t) * (volatile const long long*)(cand + 2 * b + 1);
+    if (i != 0xFFFFFFFFu) best_update(g, v, i);
+  }
+  sh.am_v[0] = g.v;
+  sh.am_i[0] = g.i;
 }
 
 // The whole position for one CTA, with its scratch at `work`.
@@ -1122,34 +1213,39 @@ __device__ __forceinline__ void step_body(const StepParams& p, uint8_t* work, Sh
       mbar_init(&full_of(p)[s], 1);
       mbar_init(&empty_of(p)[s], kNCW);  // every consumer warp releases every slot
     }
+    mbar_init(pbar_of(p), 1);  // the phase prologue's plane copy
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
   if ((threadIdx.x >> 5) == kNCW) {
-    if ((threadIdx.x & 31) == 0) producer(p, q);
+    producer(p, q);
     return;
   }
   consumers(p, q, sh);
-  // a prompt position ends with the last residual and the cursor (block 0, after the grid
-  // barrier the consumers passed on their way out of the last layer)
-  if (!p.generating && blockIdx.x == 0 && !sh.abort) {
-    int64_t* x = reinterpret_cast<int64_t*>(st + p.off_x);
-    const int64_t* xb = reinterpret_cast<const int64_t*>(st + p.off_xb);
-    const int64_t* y = reinterpret_cast<const int64_t*>(st + p.off_y);
-    for (uint32_t i = threadIdx.x; i < p.dim; i += kCT) x[i] = wadd(xb[i], y[i]);
-    if (threadIdx.x == 0) {
-      if (hdr_ld<uint64_t>(st, kHErrKey) != kNoError) {
-        hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
-        hdr<uint32_t>(st, kHError) = CK_ARITHMETIC;
-      } else {
-        hdr<uint32_t>(st, kHPosition) += 1;
-      }
-    }
-  }
-  if (threadIdx.x == 0 && blockIdx.x == 0 && (sh.abort || ld_acquire(gabort_of(q)))) {
+  // block 0 ends the position after the last grid barrier: the generated token (phase 19)
+  // or, for a prompt position, only the cursor; a failed cache store fails the state
+  if (blockIdx.x != 0 || threadIdx.x != 0) return;
+  if (sh.abort || ld_acquire(gabort_of(q))) {
     hdr<uint32_t>(st, kHError) = CK_CUDA_ERROR;
     hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
+    return;
   }
+  if (hdr_ld<uint64_t>(st, kHErrKey) != kNoError) {
+    hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
+    hdr<uint32_t>(st, kHError) = CK_ARITHMETIC;
+    return;
+  }
+  if (p.generating) {
+    const uint32_t tok = sh.am_i[0];
+    const uint32_t gen = hdr_ld<uint32_t>(st, kHGenerated);
+    reinterpret_cast<uint32_t*>(st + p.off_out)[gen] = tok;
+    hdr<uint32_t>(st, kHGenerated) = gen + 1;
+    hdr<uint32_t>(st, kHLastTok) = tok;
+    hdr<long long>(st, kHMaxLogit) = sh.am_v[0];
+    const bool stop = (hdr_ld<uint32_t>(st, kHFlags) & CK_FLAG_STOP_TOKENS) && (tok == 1 || tok == 2);
+    if (gen + 1 == hdr_ld<uint32_t>(st, kHMaxTok) || stop) hdr<uint32_t>(st, kHPhase) = CK_PHASE_DONE;
+  }
+  hdr<uint32_t>(st, kHPosition) += 1;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) k_step(const StepParams p) {
