@@ -192,6 +192,23 @@ def test_step_kernel_with_split_attention_scoring(ck, name, split):
         compare_states(P.orc, so, ck.state_download(sg), wl.n_prompt, wl.steps, f"split {split} pos {pos}")
 
 
+def test_step_kernel_with_l2_prefetch(ck):
+    """The persistent kernel with its producer prefetching weights into L2 ahead of a small
+    ring: every position against the oracle; out-of-range settings are rejected."""
+    wl = MODELS["gqa"]
+    P = Pair(ck, wl.spec, "step")
+    assert P.gpu.set_step_prefetch(64) == 0
+    assert P.gpu.set_step_slots(3) == 0
+    ids = synth.prompt_ids(wl.spec, wl.n_prompt)
+    so, sg = P.init(ck, ids, wl.steps)
+    for pos in range(wl.n_prompt + wl.steps - 1):
+        rco, reso = P.orc.turn(so, 1)
+        rcg, resg = P.gpu.turn(sg, 1)
+        assert rco == rcg == 0 and reso == resg, (pos, rcg, resg)
+        compare_states(P.orc, so, ck.state_download(sg), wl.n_prompt, wl.steps, f"prefetch pos {pos}")
+    assert P.gpu.set_step_prefetch(5000) == 10
+
+
 @pytest.fixture(scope="module", params=list(PATHS))
 def pairs(ck, request):
     return {name: Pair(ck, wl.spec, request.param) for name, wl in MODELS.items()}
