@@ -413,6 +413,36 @@ def test_1b_long_context_sampled_position(ck, path):
     assert h["generated"] == 1 and h["position"] == wl.n_prompt
 
 
+def test_1b_sixty_four_runs_sampled(ck):
+    """The 1B-shaped model with 64 independent runs (64 prompt ids each, own state and
+    cache), advanced in turns interleaved like a serving loop; sampled runs then take one
+    generating position on both targets from the same state."""
+    wl = synth.WORKLOADS["1b_x64"]
+    spec = wl.spec
+    art = synth.build_artifact(spec)
+    orc = oracle.Model(art)
+    rc, gpu = ck.Model.load(art)
+    assert rc == 0
+    states = []
+    for r in range(wl.runs):
+        ids = synth.prompt_ids(spec, wl.n_prompt, run=r)
+        sg = gpu.new_state(wl.n_prompt, wl.steps)
+        assert gpu.init_state(sg, ids, wl.steps) == 0
+        states.append(sg)
+    chunk = 16
+    for done in range(0, wl.n_prompt - 1, chunk):  # the prompts, 16 positions a turn per run
+        for sg in states:
+            rc, res = gpu.turn(sg, min(chunk, wl.n_prompt - 1 - done))
+            assert rc == 0, rc
+    for r in (0, 37, wl.runs - 1):
+        host = ck.state_download(states[r])
+        rco, reso = orc.turn(host, 1)
+        rcg, resg = gpu.turn(states[r], 1)
+        assert rco == rcg == 0 and reso == resg, (r, reso, resg)
+        compare_states(orc, host, ck.state_download(states[r]), wl.n_prompt, wl.steps, f"run {r}", turns=False)
+        assert oracle.header(host)["generated"] == 1
+
+
 def test_paths_agree_and_unknown_path_is_rejected(ck):
     wl = MODELS["gqa"]
     P = Pair(ck, wl.spec, "step")
