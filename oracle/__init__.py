@@ -8,7 +8,7 @@ It imports nothing from the GPU library and the library imports nothing from it.
 Pin status (each function is checked in ``tests/test_oracle_pins.py`` against values the
 page fixes, closed forms, textbook routines or brute force):
   isqrt, embed, rmsnorm, matrow, fits32, rotate, attention_head, silu, silu_gate, argmax,
-  page_state_size: pinned.
+  xorshift_next, sample_index, draw_walk, sample, page_state_size: pinned.
   Whole-model token streams: parity unpinned against curta-core itself (the page prints no
   tokens or logits for a model); pinned only through the per-step pins and invariants.
 """
@@ -32,6 +32,7 @@ LAYOUT_NAMES = ("prompt", "out", "x", "xb", "q", "o", "y", "h", "logits", "score
 # header offsets of the ids-mode state (format "CKSTATE1")
 H_PHASE, H_POSITION, H_NPROMPT, H_MAXTOK, H_CACHE, H_GENERATED = 8, 12, 16, 20, 24, 28
 H_FLAGS, H_TEMP, H_ERROR, H_LASTTOK, H_SEED, H_TURNS, H_ERRKEY, H_MAXLOGIT = 32, 36, 40, 44, 48, 56, 64, 72
+H_EXPSUM, H_DRAW = 112, 120
 PHASE_RUNNING, PHASE_DONE, PHASE_FAILED = 3, 20, 21
 FLAG_STOP_TOKENS = 1
 
@@ -70,6 +71,11 @@ def _lib_():
             "orc_silu": ([i64, vp], i64),
             "orc_silu_gate": ([vp, vp, u32, vp, vp], None),
             "orc_argmax": ([vp, u32], u32),
+            "orc_xorshift_next": ([ctypes.POINTER(u64)], u64),
+            "orc_sample_index": ([i64, i64, u32], u32),
+            "orc_draw_walk": ([vp, u32, u64], u32),
+            "orc_sample": ([vp, u32, u32, vp, ctypes.POINTER(u64), ctypes.POINTER(i64),
+                            ctypes.POINTER(u64), ctypes.POINTER(u64)], u32),
             "orc_page_state_size": ([vp, u32, u32], u64),
             "orc_model_open": ([vp, u64, ctypes.POINTER(vp)], ctypes.c_int),
             "orc_model_close": ([vp], None),
@@ -163,6 +169,32 @@ def argmax(logits: np.ndarray) -> int:
     return int(_lib_().orc_argmax(logits.ctypes.data, logits.size))
 
 
+def xorshift_next(state: int) -> tuple[int, int]:
+    """One step of the sampling generator: returns (new state, output)."""
+    s = ctypes.c_uint64(state)
+    out = int(_lib_().orc_xorshift_next(ctypes.byref(s)))
+    return int(s.value), out
+
+
+def sample_index(m: int, l: int, temperature_q16: int) -> int:
+    return int(_lib_().orc_sample_index(m, l, temperature_q16))
+
+
+def draw_walk(e: np.ndarray, r: int) -> int:
+    e = _c(e, np.uint64)
+    return int(_lib_().orc_draw_walk(e.ctypes.data, e.size, r))
+
+
+def sample(logits: np.ndarray, temperature_q16: int, exp_tab: np.ndarray, state: int) -> dict:
+    """Phase 19 on a logit vector: {token, state, max, sum, draw}."""
+    logits, e = _c(logits, np.int64), _c(exp_tab, np.uint32)
+    s, m, z, d = ctypes.c_uint64(state), ctypes.c_int64(), ctypes.c_uint64(), ctypes.c_uint64()
+    tok = _lib_().orc_sample(logits.ctypes.data, logits.size, temperature_q16, e.ctypes.data,
+                             ctypes.byref(s), ctypes.byref(m), ctypes.byref(z), ctypes.byref(d))
+    return {"token": int(tok), "state": int(s.value), "max": int(m.value), "sum": int(z.value),
+            "draw": int(d.value)}
+
+
 def page_state_size(config, prompt_bytes: int, max_tokens: int) -> int:
     cfg = np.array(config, dtype=np.uint32)
     return int(_lib_().orc_page_state_size(cfg.ctypes.data, prompt_bytes, max_tokens))
@@ -239,6 +271,7 @@ def header(state: np.ndarray) -> dict:
     u64 = lambda o: int(state[o:o + 8].view("<u8")[0])
     return {"phase": u32(H_PHASE), "position": u32(H_POSITION), "n_prompt": u32(H_NPROMPT),
             "max_tokens": u32(H_MAXTOK), "cache": u32(H_CACHE), "generated": u32(H_GENERATED),
-            "flags": u32(H_FLAGS), "error": u32(H_ERROR), "last_token": u32(H_LASTTOK),
-            "turns": u64(H_TURNS), "err_key": u64(H_ERRKEY),
+            "flags": u32(H_FLAGS), "temperature": u32(H_TEMP), "error": u32(H_ERROR),
+            "last_token": u32(H_LASTTOK), "generator": u64(H_SEED), "turns": u64(H_TURNS),
+            "err_key": u64(H_ERRKEY), "exp_sum": u64(H_EXPSUM), "draw": u64(H_DRAW),
             "max_logit": int(state[H_MAXLOGIT:H_MAXLOGIT + 8].view("<i8")[0])}

@@ -1,7 +1,8 @@
 /* ORACLE — test infrastructure, not part of the product.
  *
  * A plain, slow, obviously correct CPU restatement of curta-core's integer forward pass
- * (phases 3 to 19 at temperature zero), written from the page "The inference core"
+ * (phases 3 to 19, sampling at temperature zero and above), written from the page "The
+ * inference core"
  * (curta.chat docs).  Only the tests, the smoke check and the benchmark's CPU-baseline leg
  * may load it.  It shares no code with the GPU library: it parses the model artifact and
  * the state layout itself, from the format description.
@@ -21,6 +22,10 @@
  *   r10 Weighted values: the sum over positions first, then one >> 24.
  *   r13 Ties in the maximum pass keep the lowest index.
  *   r17 The first failing cache store, in program order, ends the turn with error 8.
+ *   r20 Sampling divides m - l by the temperature into a value with 16 fractional bits,
+ *       truncating; the exponential-table index is that value >> 8, capped at 4,096.
+ *   r21 The generator state is the seed word (a zero seed stored as its first state); the
+ *       state header records the last sum of exponentials and the last draw.
  *
  * Range events: with counting on, every step that the wrap changes (exact integer result
  * outside int64) is counted, so a workload can show that no reading above mattered.
@@ -227,6 +232,64 @@ uint32_t orc_argmax(const int64_t* logits, uint32_t n) {
   return best;
 }
 
+/* "Sampling", the generator: xorshift64* (shifts 12 right, 25 left, 27 right, then the
+ * product with 0x2545F4914F6CDD1D mod 2^64).  Advances the state once and returns the
+ * output; the shifted value, not the product, is the new state. */
+uint64_t orc_xorshift_next(uint64_t* state) {
+  uint64_t x = *state;
+  x ^= x >> 12;
+  x ^= x << 25;
+  x ^= x >> 27;
+  *state = x;
+  return x * 0x2545F4914F6CDD1Dull;
+}
+
+/* "Sampling", sum pass: the exponential-table index of a logit l below the largest logit m
+ * at temperature t (16 fractional bits, 1 ..= 16 << 16).  The difference m - l, which has
+ * 16 fractional bits and is zero or more, is divided by the temperature, truncating, into a
+ * value that again has 16 fractional bits; the index is that value >> 8, capped at 4,096,
+ * as for every read of the exponential table.  Computed in 128 bits, so nothing wraps. */
+uint32_t orc_sample_index(int64_t m, int64_t l, uint32_t t) {
+  unsigned __int128 d = (unsigned __int128)((__int128)m - (__int128)l);
+  unsigned __int128 scaled = (d << 16) / t;
+  unsigned __int128 idx = scaled >> 8;
+  return idx > 4096 ? 4096u : (uint32_t)idx;
+}
+
+/* "Sampling", draw pass walk: from the remainder r, subtract each entry's exponential in
+ * vocabulary order and take the first entry the remainder falls inside. */
+uint32_t orc_draw_walk(const uint64_t* e, uint32_t n, uint64_t r) {
+  for (uint32_t i = 0; i < n; ++i) {
+    if (r < e[i]) return i;
+    r -= e[i];
+  }
+  return n; /* r was not below the sum: no entry */
+}
+
+/* Phase 19, "Sampling": the maximum pass, and above temperature zero the sum and draw
+ * passes.  gen is the run's generator state (advanced once per draw); m, sum and draw
+ * receive the largest logit, the sum of exponentials and the draw (0 at temperature 0). */
+uint32_t orc_sample(const int64_t* logits, uint32_t n, uint32_t t, const uint32_t* exp_tab,
+                    uint64_t* gen, int64_t* m, uint64_t* sum, uint64_t* draw) {
+  uint32_t best = orc_argmax(logits, n);                       /* maximum pass */
+  *m = logits[best];
+  *sum = 0;
+  *draw = 0;
+  if (t == 0) return best;
+  uint64_t* e = (uint64_t*)malloc(8ull * n);
+  uint64_t z = 0;
+  for (uint32_t i = 0; i < n; ++i) {                            /* sum pass */
+    e[i] = exp_tab[orc_sample_index(*m, logits[i], t)];
+    z += e[i];
+  }
+  uint64_t r = orc_xorshift_next(gen) % z;                      /* draw pass */
+  uint32_t chosen = orc_draw_walk(e, n, r);
+  free(e);
+  *sum = z;
+  *draw = r;
+  return chosen;
+}
+
 static void residual(int64_t* x, const int64_t* y, uint32_t n) {
   for (uint32_t i = 0; i < n; ++i) {
     if (g_count_events && outside_i64((__int128)x[i] + y[i])) event(EV_RESIDUAL);
@@ -361,7 +424,7 @@ void orc_model_close(orc_model* m) {
 
 enum { H_PHASE = 8, H_POSITION = 12, H_NPROMPT = 16, H_MAXTOK = 20, H_CACHE = 24, H_GENERATED = 28,
        H_FLAGS = 32, H_TEMP = 36, H_ERROR = 40, H_LASTTOK = 44, H_SEED = 48, H_TURNS = 56,
-       H_ERRKEY = 64, H_MAXLOGIT = 72, H_CONFIG = 80 };
+       H_ERRKEY = 64, H_MAXLOGIT = 72, H_CONFIG = 80, H_EXPSUM = 112, H_DRAW = 120 };
 enum { PHASE_RUNNING = 3, PHASE_DONE = 20, PHASE_FAILED = 21 };
 
 typedef struct {
@@ -419,7 +482,7 @@ int orc_init_state(const orc_model* m, uint8_t* st, uint64_t len, const uint32_t
                    uint32_t flags) {
   if ((uintptr_t)st % 8) return 3;
   if (n_ids == 0 || max_tokens == 0 || max_tokens > m->context) return 6;
-  if (temperature_q16 != 0) return 6; /* only the maximum pass (temperature zero) is built */
+  if (temperature_q16 > (16u << 16)) return 6; /* a temperature above 16 */
   for (uint32_t i = 0; i < n_ids; ++i)
     if (ids[i] >= m->vocab) return 6;
   if ((uint64_t)n_ids + max_tokens - 1 > m->context) return 7;
@@ -436,7 +499,7 @@ int orc_init_state(const orc_model* m, uint8_t* st, uint64_t len, const uint32_t
   wr32(st + H_FLAGS, flags);
   wr32(st + H_TEMP, temperature_q16);
   wr32(st + H_LASTTOK, 0xFFFFFFFFu);
-  wr64(st + H_SEED, seed);
+  wr64(st + H_SEED, seed ? seed : 0x9E3779B97F4A7C15ull); /* a zero seed's first state */
   wr64(st + H_ERRKEY, ~0ull);
   for (int i = 0; i < 7; ++i) wr32(st + H_CONFIG + 4 * i, cfg[i]);
   memcpy(st + L.prompt, ids, 4ull * n_ids);
@@ -535,12 +598,18 @@ static int run_position(const orc_model* m, uint8_t* st, const orc_layout* L) {
   if (pos + 1 >= n_prompt) {                                           /* a generating position */
     orc_rmsnorm(x, m->final_norm, d, xb);                              /* phase 17 */
     orc_matrow(m->cls, d, m->cls_scale, m->vocab, d, xb, logits);      /* phase 18 */
-    uint32_t t = orc_argmax(logits, m->vocab);                         /* phase 19 */
+    uint64_t state = rd64(st + H_SEED), z, draw;                       /* phase 19 */
+    int64_t mx;
+    uint32_t t = orc_sample(logits, m->vocab, rd32(st + H_TEMP), m->exp_tab, &state, &mx, &z,
+                            &draw);
     uint32_t gen = rd32(st + H_GENERATED);
     out[gen] = t;
     wr32(st + H_GENERATED, gen + 1);
     wr32(st + H_LASTTOK, t);
-    wr64(st + H_MAXLOGIT, (uint64_t)logits[t]);
+    wr64(st + H_MAXLOGIT, (uint64_t)mx);
+    wr64(st + H_SEED, state);
+    wr64(st + H_EXPSUM, z);
+    wr64(st + H_DRAW, draw);
     if (gen + 1 == rd32(st + H_MAXTOK) || ((rd32(st + H_FLAGS) & 1) && (t == 1 || t == 2)))
       wr32(st + H_PHASE, PHASE_DONE);
   }

@@ -118,6 +118,7 @@ def test_init_state_errors(tiny_ws):
     assert m.init_state(np.array([wl.spec.vocab], np.uint32), 2)[0] == 6   # id out of range
     assert m.init_state(np.array([], np.uint32), 2)[0] == 6   # no prompt id
     assert m.init_state(ids, 2, temperature_q16=16 * 2**16 + 1)[0] == 6
+    assert m.init_state(ids, 2, temperature_q16=16 * 2**16)[0] == 0   # 16 is allowed
     assert m.init_state(ids, ctx - 2)[0] == 7                 # 4 + (ctx-2) - 1 > ctx
     assert m.init_state(ids, ctx - 3)[0] == 0                 # exactly the context
     n = m.state_size(4, 5)
@@ -171,3 +172,49 @@ def test_tied_classifier_reads_the_embedding():
         assert rc == 0
         outs.append(_buf(m, st, wl, "out", "<u4", wl.steps).tolist())
     assert outs[0] == outs[1]
+
+
+def test_sampled_run_advances_the_generator_once_per_token(tiny_ws):
+    """"Sampling": above temperature zero each generated token draws once from the run's
+    generator, seeded by the run's seed (a zero seed from the page's constant), and the
+    header keeps the last sum of exponentials and draw, with draw < sum."""
+    wl, m = tiny_ws
+    ids = synth.prompt_ids(wl.spec, wl.n_prompt)
+    f_zero = 0x9E3779B97F4A7C15
+    for seed, temp in ((0, 1 << 16), (12345, 3 << 15), (2**64 - 1, 16 << 16)):
+        rc, st = m.init_state(ids, wl.steps, temperature_q16=temp, seed=seed)
+        assert rc == 0
+        h = oracle.header(st)
+        assert h["generator"] == (seed or f_zero) and h["temperature"] == temp
+        state = seed or f_zero
+        for pos in range(wl.n_prompt + wl.steps - 1):
+            rc, res = m.turn(st, 1)
+            assert rc == 0
+            h = oracle.header(st)
+            if pos + 1 >= wl.n_prompt:
+                tok = int(_buf(m, st, wl, "out", "<u4", wl.steps)[h["generated"] - 1])
+                lg = _buf(m, st, wl, "logits", "<i8", wl.spec.vocab)
+                r = oracle.sample(lg, temp, synth.exp_table(), state)   # from the state before
+                state = oracle.xorshift_next(state)[0]
+                assert r["token"] == tok and r["state"] == state
+                assert (r["sum"], r["draw"]) == (h["exp_sum"], h["draw"])
+                assert 0 <= h["draw"] < h["exp_sum"]
+                assert h["exp_sum"] >= 1 << 30                # the largest logit adds EXP[0]
+                assert h["max_logit"] == int(lg.max())
+            else:
+                assert h["draw"] == 0 and h["exp_sum"] == 0
+            assert h["generator"] == state
+        assert h["phase"] == oracle.PHASE_DONE
+
+
+def test_high_temperature_changes_the_tokens_and_zero_does_not_draw(tiny_ws):
+    wl, m = tiny_ws
+    ids = synth.prompt_ids(wl.spec, wl.n_prompt)
+    _, greedy = m.init_state(ids, wl.steps)
+    m.turn(greedy, 1000)
+    g = _buf(m, greedy, wl, "out", "<u4", wl.steps).tolist()
+    h = oracle.header(greedy)
+    assert h["generator"] == 0x9E3779B97F4A7C15 and h["exp_sum"] == 0   # never advanced
+    _, hot = m.init_state(ids, wl.steps, temperature_q16=16 << 16, seed=7)
+    m.turn(hot, 1000)
+    assert _buf(m, hot, wl, "out", "<u4", wl.steps).tolist() != g

@@ -327,3 +327,144 @@ def test_xorshift64star_generator():
         x, o = step(x)
         want.append(o)
     assert synth.xs64s_sequence(0, 5) == want
+
+
+# ---------------------------------------------------------------- sampling (phase 19 above zero)
+
+def _gf2_apply(cols, v):
+    """The GF(2) matrix with the given column images applied to the 64-bit vector v."""
+    out = 0
+    j = 0
+    while v:
+        if v & 1:
+            out ^= cols[j]
+        v >>= 1
+        j += 1
+    return out
+
+
+def _gf2_mul(a, b):
+    return [_gf2_apply(a, c) for c in b]
+
+
+def _gf2_pow(a, e):
+    r = [1 << j for j in range(64)]
+    while e:
+        if e & 1:
+            r = _gf2_mul(r, a)
+        a = _gf2_mul(a, a)
+        e >>= 1
+    return r
+
+
+def test_sampling_generator_has_the_full_xorshift_period():
+    """The oracle's state step is linear over GF(2) and its matrix has order exactly
+    2^64 - 1, the maximal period Marsaglia's xorshift theorem gives for the triple
+    (12, 25, 27): a wrong shift amount or direction breaks it.  Its output is the state
+    times the page's multiplier, and the zero seed's sequence matches the input generator's
+    (itself pinned to the page above)."""
+    f = facts()["xorshift64star"]
+    mult, zero = int(f["multiplier"], 16), int(f["zero_seed_state"], 16)
+    step = lambda x: oracle.xorshift_next(x)[0]
+    cols = [step(1 << j) for j in range(64)]
+    rng = np.random.default_rng(3)
+    for _ in range(20):
+        a, b = (int(v) for v in rng.integers(0, 2**63, 2, dtype=np.uint64))
+        assert step(a ^ b) == step(a) ^ step(b)
+        assert step(a) == _gf2_apply(cols, a)
+    order = 2**64 - 1
+    ident = [1 << j for j in range(64)]
+    assert _gf2_pow(cols, order) == ident
+    for p in (3, 5, 17, 257, 641, 65537, 6700417):            # the primes of 2^64 - 1
+        assert order % p == 0
+        assert _gf2_pow(cols, order // p) != ident
+    x, outs = zero, []
+    for _ in range(6):
+        x, o = oracle.xorshift_next(x)
+        assert o == (x * mult) % M64
+        outs.append(o)
+    assert outs == synth.xs64s_sequence(0, 6)
+
+
+def test_sample_index_is_the_table_rule_at_temperature_one():
+    """At temperature 1 (1 << 16) the index is the exponential table's own rule, d >> 8
+    capped at 4096; temperature 2 halves the step and 1/2 doubles it; huge differences cap
+    without wrapping."""
+    rng = np.random.default_rng(4)
+    for _ in range(300):
+        m = int(rng.integers(-2**40, 2**40))
+        d = int(rng.integers(0, 2**22))
+        assert oracle.sample_index(m, m - d, 1 << 16) == min(d >> 8, 4096)
+        assert oracle.sample_index(m, m - d, 1 << 17) == min(d >> 9, 4096)
+        assert oracle.sample_index(m, m - d, 1 << 15) == min(d >> 7, 4096)
+    assert oracle.sample_index(2**63 - 1, -2**63, 1) == 4096
+    assert oracle.sample_index(2**63 - 1, -2**63, 16 << 16) == 4096
+    assert oracle.sample_index(5, 5, 1) == 0
+
+
+def test_sample_index_is_exp_of_difference_over_temperature():
+    """Real-valued check: the entry read is e^-(dl / T) to within one table step (1/256 in
+    the exponent) plus the entry's rounding, for temperatures that are not powers of two."""
+    tab = synth.exp_table()
+    rng = np.random.default_rng(5)
+    for _ in range(400):
+        t = int(rng.integers(1, 16 << 16))
+        d = int(rng.integers(0, 17 * t))
+        idx = oracle.sample_index(0, -d, t)
+        x = (d / 65536) / (t / 65536)
+        if x >= 4097 / 256:
+            assert idx == 4096
+            continue
+        assert idx == int(x * 256) or abs(x * 256 - round(x * 256)) < 1e-9
+        got = tab[idx] / 2**30
+        assert math.exp(-x) <= got * math.exp(1 / 256) + 1e-9
+        assert got <= math.exp(-x) * math.exp(1 / 256) + 1e-9
+
+
+def test_draw_walk_takes_the_first_entry_the_remainder_falls_inside():
+    e = np.array([5, 0, 3, 7], dtype=np.uint64)
+    want = {0: 0, 4: 0, 5: 2, 7: 2, 8: 3, 14: 3, 15: 4}
+    for r, i in want.items():
+        assert oracle.draw_walk(e, r) == i, r
+
+
+def test_sample_temperature_zero_is_the_maximum_pass():
+    v = np.array([3, 9, 9, 1], dtype=np.int64)
+    r = oracle.sample(v, 0, synth.exp_table(), 77)
+    assert r == {"token": 1, "state": 77, "max": 9, "sum": 0, "draw": 0}
+
+
+def test_sample_equal_logits_closed_form():
+    """Equal logits: every exponential is EXP[0] = 2^30, the sum is n * 2^30, and the draw
+    picks entry draw // 2^30; the state advances exactly once."""
+    tab = synth.exp_table()
+    for n, t, seed in ((7, 1 << 16, 11), (1000, 3 << 16, 12345), (32000, 1, 2**63 + 9)):
+        v = np.full(n, -42, dtype=np.int64)
+        r = oracle.sample(v, t, tab, seed)
+        out = synth.xs64s_sequence(seed, 1)[0]
+        assert r["sum"] == n << 30
+        assert r["draw"] == out % (n << 30)
+        assert r["token"] == r["draw"] >> 30
+        assert r["state"] == oracle.xorshift_next(seed)[0]
+        assert r["max"] == -42
+
+
+def test_sample_frequencies_follow_the_exponentials():
+    """Many draws from one vector: each entry's frequency is its exponential over the sum
+    (binomial 5-sigma bound).  Logits are spaced on the table's grid at temperature 1."""
+    tab = synth.exp_table()
+    ks = [0, 100, 256, 700, 4096, 5000]
+    v = np.array([-256 * k for k in ks], dtype=np.int64)
+    e = np.array([tab[min(k, 4096)] for k in ks], dtype=np.float64)
+    p = e / e.sum()
+    n = 20000
+    counts = np.zeros(len(ks))
+    state = 99
+    for _ in range(n):
+        r = oracle.sample(v, 1 << 16, tab, state)
+        state = r["state"]
+        counts[r["token"]] += 1
+        assert r["sum"] == int(e.sum())
+    for i in range(len(ks)):
+        sd = math.sqrt(n * p[i] * (1 - p[i])) + 1
+        assert abs(counts[i] - n * p[i]) <= 5 * sd, (i, counts[i], n * p[i])
