@@ -275,9 +275,14 @@ __device__ void block_argmax(const int64_t* l, uint32_t n, long long* best_v, ui
   }
 }
 
-// Phase 19 at temperature zero plus the end of a generating position.
+// Phase 19 ("Sampling": the maximum pass, and above temperature zero the sum and draw
+// passes) plus the end of a generating position.
 __global__ void __launch_bounds__(kArgThreads) k_sample_finish(uint8_t* st, uint64_t off_out,
-                                                              const int64_t* logits, uint32_t vocab) {
+                                                              const int64_t* logits, uint32_t vocab,
+                                                              const uint32_t* exp_tab) {
+  __shared__ unsigned long long gsum[kSampleGroups];
+  __shared__ long long max_v;
+  __shared__ uint32_t max_i;
   if (hdr_ld<uint32_t>(st, kHPhase) != CK_PHASE_RUNNING) return;
   if (hdr_ld<uint64_t>(st, kHErrKey) != kNoError) {
     if (threadIdx.x == 0) {
@@ -290,6 +295,24 @@ __global__ void __launch_bounds__(kArgThreads) k_sample_finish(uint8_t* st, uint
   uint32_t bi;
   block_argmax(logits, vocab, &bv, &bi);
   if (threadIdx.x == 0) {
+    max_v = bv;
+    max_i = bi;
+  }
+  __syncthreads();
+  bv = max_v;
+  bi = max_i;
+  const uint32_t temp = hdr_ld<uint32_t>(st, kHTemp);
+  unsigned long long state = hdr_ld<unsigned long long>(st, kHSeed), z = 0, draw = 0;
+  if (temp != 0) {
+    const SampleOut so = block_sample(reinterpret_cast<const long long*>(logits), vocab, bv, temp,
+                                      exp_tab, state, gsum, kArgThreads / 32,
+                                      [] { __syncthreads(); });
+    bi = so.token;
+    state = so.state;
+    z = so.sum;
+    draw = so.draw;
+  }
+  if (threadIdx.x == 0) {
     const uint32_t gen = hdr_ld<uint32_t>(st, kHGenerated);
     if (gen >= hdr_ld<uint32_t>(st, kHMaxTok)) {  // unreachable for states the turn validated
       hdr<uint32_t>(st, kHError) = CK_INVALID_STATE;
@@ -300,6 +323,9 @@ __global__ void __launch_bounds__(kArgThreads) k_sample_finish(uint8_t* st, uint
     hdr<uint32_t>(st, kHGenerated) = gen + 1;
     hdr<uint32_t>(st, kHLastTok) = bi;
     hdr<long long>(st, kHMaxLogit) = bv;
+    hdr<unsigned long long>(st, kHSeed) = state;
+    hdr<unsigned long long>(st, kHExpSum) = z;
+    hdr<unsigned long long>(st, kHDraw) = draw;
     const bool stop = (hdr_ld<uint32_t>(st, kHFlags) & CK_FLAG_STOP_TOKENS) && (bi == 1 || bi == 2);
     if (gen + 1 == hdr_ld<uint32_t>(st, kHMaxTok) || stop) hdr<uint32_t>(st, kHPhase) = CK_PHASE_DONE;
     hdr<uint32_t>(st, kHPosition) += 1;
@@ -490,7 +516,7 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
     pc.out = logits;
     pc.state = st;
     CK_CUDA(launch_matrow(pc, s, m->num_sms));
-    k_sample_finish<<<1, kArgThreads, 0, s>>>(st, lay.out, logits, c.vocab);  // phase 19
+    k_sample_finish<<<1, kArgThreads, 0, s>>>(st, lay.out, logits, c.vocab, m->exp_tab);  // phase 19
   } else {
     k_finish_prompt<<<1, 256, 0, s>>>(st, x, xb, y, c.dim);
   }
@@ -841,7 +867,7 @@ int ck_init_state(const ck_model* m, void* dev_state, size_t len, const uint32_t
   if (!m || !dev_state || (n_ids && !host_ids)) return CK_INVALID_ARGUMENT;
   if (reinterpret_cast<uintptr_t>(dev_state) % 256) return CK_INVALID_STATE;
   if (!n_ids || !max_tokens || max_tokens > m->cfg.context) return CK_INVALID_PROMPT;
-  if (temperature_q16 != 0) return CK_INVALID_PROMPT;  // only the maximum pass is built
+  if (temperature_q16 > kMaxTemperature) return CK_INVALID_PROMPT;
   for (uint32_t i = 0; i < n_ids; ++i)
     if (host_ids[i] >= m->cfg.vocab) return CK_INVALID_PROMPT;
   if ((uint64_t)n_ids + max_tokens - 1 > m->cfg.context) return CK_CONTEXT_EXCEEDED;
@@ -858,7 +884,7 @@ int ck_init_state(const ck_model* m, void* dev_state, size_t len, const uint32_t
   w32(kHFlags, flags);
   w32(kHTemp, temperature_q16);
   w32(kHLastTok, 0xFFFFFFFFu);
-  w64(kHSeed, seed);
+  w64(kHSeed, seed ? seed : kZeroSeedState);  // the generator's first state
   w64(kHErrKey, kNoError);
   for (int i = 0; i < 7; ++i) w32(kHConfig + 4 * i, (&m->cfg.dim)[i]);
   memcpy(h.data() + lay.prompt, host_ids, 4ull * n_ids);

@@ -16,7 +16,10 @@ namespace ck {
 constexpr uint32_t kHeaderBytes = 256;
 constexpr uint32_t kHPhase = 8, kHPosition = 12, kHNPrompt = 16, kHMaxTok = 20, kHCache = 24,
                    kHGenerated = 28, kHFlags = 32, kHTemp = 36, kHError = 40, kHLastTok = 44,
-                   kHSeed = 48, kHTurns = 56, kHErrKey = 64, kHMaxLogit = 72, kHConfig = 80;
+                   kHSeed = 48, kHTurns = 56, kHErrKey = 64, kHMaxLogit = 72, kHConfig = 80,
+                   kHExpSum = 112, kHDraw = 120;
+constexpr uint32_t kMaxTemperature = 16u << 16;       // 16 with 16 fraction bits
+constexpr unsigned long long kZeroSeedState = 0x9E3779B97F4A7C15ull;
 constexpr uint64_t kNoError = ~0ull;
 
 struct StateLayout {
@@ -293,6 +296,122 @@ struct StepParams {
   const uint32_t* exp_tab;
   const int32_t* silu_tab;
 };
+
+// ------------------------------------------------------------------ phase 19 above zero
+// "Sampling" at a temperature t > 0 (16 fraction bits).  Sum pass: every logit l adds the
+// exponential-table entry at min(((m - l) / t) >> 8, 4096), the difference over the
+// temperature taken with 16 fraction bits and truncated.  Draw pass: the generator's output
+// modulo the sum, walked through the vocabulary in order, subtracting each entry's
+// exponential; the entry it falls inside is the token.
+constexpr uint32_t kSampleGroups = 1024;  // u64 partial sums a sampling block keeps in smem
+
+// floor(floor(d * 2^16 / t) / 2^8) = floor(256 d / t) for d = m - l >= 0; that reaches the
+// cap 4096 exactly when d >= 16 t, and below it 256 d < 2^32.
+__device__ __forceinline__ uint32_t sample_exp_index(long long m, long long l, uint32_t t) {
+  const unsigned long long d = (unsigned long long)m - (unsigned long long)l;
+  if (d >= 16ull * t) return 4096u;
+  return ((uint32_t)d << 8) / t;
+}
+
+// xorshift64*: the state moves by the three shifts; the output is the state times the
+// multiplier modulo 2^64.
+__device__ __forceinline__ unsigned long long sample_next(unsigned long long* state) {
+  unsigned long long x = *state;
+  x ^= x >> 12;
+  x ^= x << 25;
+  x ^= x >> 27;
+  *state = x;
+  return x * 0x2545F4914F6CDD1Dull;
+}
+
+__device__ __forceinline__ unsigned long long warp_inclusive_scan(unsigned long long v, uint32_t lane) {
+#pragma unroll
+  for (uint32_t o = 1; o < 32; o <<= 1) {
+    const unsigned long long w = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += w;
+  }
+  return v;
+}
+
+struct SampleOut {
+  uint32_t token;
+  unsigned long long sum, draw, state;  // state: the generator after the draw
+};
+
+// The sum and draw passes by nwarps warps of one block (every thread of them calls it, with
+// `bar` synchronising exactly those threads).  Logits are read through L2.  The vocabulary is
+// cut into chunks of 32 entries and groups of u chunks (at most kSampleGroups groups); gsum
+// (shared memory, kSampleGroups words) receives each group's sum.  The result is valid in
+// warp 0.
+template <class Bar>
+__device__ SampleOut block_sample(const long long* logits, uint32_t vocab, long long m, uint32_t t,
+                                  const uint32_t* exp_tab, unsigned long long state,
+                                  unsigned long long* gsum, uint32_t nwarps, Bar bar) {
+  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t nchunk = (vocab + 31) / 32;
+  const uint32_t u = (nchunk + kSampleGroups - 1) / kSampleGroups;
+  const uint32_t ngroup = (nchunk + u - 1) / u;
+  for (uint32_t g = warp; g < ngroup; g += nwarps) {
+    unsigned long long s = 0;
+    const uint32_t c1 = min(g * u + u, nchunk);
+    for (uint32_t c = g * u; c < c1; ++c) {
+      const uint32_t i = c * 32 + lane;
+      if (i < vocab) s += __ldg(exp_tab + sample_exp_index(m, __ldcg(logits + i), t));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) gsum[g] = s;
+  }
+  bar();
+  SampleOut out{0u, 0ull, 0ull, state};
+  if (warp != 0) return out;
+  // lane j owns groups [j * seg, (j + 1) * seg)
+  const uint32_t seg = (ngroup + 31) / 32;
+  const uint32_t g0 = min(lane * seg, ngroup), g1 = min(g0 + seg, ngroup);
+  unsigned long long own = 0;
+  for (uint32_t g = g0; g < g1; ++g) own += gsum[g];
+  const unsigned long long inc = warp_inclusive_scan(own, lane);
+  const unsigned long long z = __shfl_sync(0xffffffffu, inc, 31);
+  unsigned long long r = 0;
+  if (lane == 0) {
+    r = sample_next(&state) % z;
+    out.state = state;
+  }
+  r = __shfl_sync(0xffffffffu, r, 0);
+  // the lane whose groups hold the draw, then the group, then the chunk, then the entry
+  const int L = __ffs(__ballot_sync(0xffffffffu, inc > r)) - 1;
+  unsigned long long rem = r - __shfl_sync(0xffffffffu, inc - own, L);
+  uint32_t gsel = g0;
+  if ((int)lane == L) {
+    for (uint32_t g = g0; g < g1; ++g) {
+      if (rem < gsum[g]) {
+        gsel = g;
+        break;
+      }
+      rem -= gsum[g];
+    }
+  }
+  gsel = __shfl_sync(0xffffffffu, gsel, L);
+  rem = __shfl_sync(0xffffffffu, rem, L);
+  uint32_t token = 0;
+  const uint32_t c1 = min(gsel * u + u, nchunk);
+  for (uint32_t c = gsel * u; c < c1; ++c) {
+    const uint32_t i = c * 32 + lane;
+    const unsigned long long e =
+        i < vocab ? (unsigned long long)__ldg(exp_tab + sample_exp_index(m, __ldcg(logits + i), t)) : 0ull;
+    const unsigned long long ci = warp_inclusive_scan(e, lane);
+    const unsigned long long tot = __shfl_sync(0xffffffffu, ci, 31);
+    if (rem < tot) {
+      token = c * 32 + (uint32_t)(__ffs(__ballot_sync(0xffffffffu, ci > rem)) - 1);
+      break;
+    }
+    rem -= tot;
+  }
+  out.token = token;
+  out.sum = z;
+  out.draw = r;
+  return out;
+}
 
 cudaError_t configure_step(size_t optin, size_t* dynamic_max);
 cudaError_t launch_step(const StepParams& p, cudaStream_t s, int grid, size_t smem);

@@ -61,6 +61,7 @@ struct Shared {
   unsigned long long ra[kNCW], rbuf[kNCW];
   long long am_v[kNCW];
   uint32_t am_i[kNCW];
+  unsigned long long smp_state, smp_sum, smp_draw;  // phase 19 above temperature zero
   unsigned long long S, orv;
   int abort;
   int last;
@@ -1176,18 +1177,37 @@ __device__ __forceinline__ void consumers(const StepParams& p, const Pos& q, Sha
     cand[2 * blockIdx.x + 1] = (long long)cb.i;
   }
   if (!grid_sync(q, sh, epoch)) return;
-  if (blockIdx.x != 0 || threadIdx.x != 0) return;
+  if (blockIdx.x != 0) return;
   // phase 19: maximum pass over the per-CTA candidates
-  Best g;
-  g.v = LLONG_MIN;
-  g.i = 0xFFFFFFFFu;
-  for (uint32_t b = 0; b < gridDim.x; ++b) {
-    const long long v = *(volatile const long long*)(cand + 2 * b);
-    const uint32_t i = (uint32_t) * (volatile const long long*)(cand + 2 * b + 1);
-    if (i != 0xFFFFFFFFu) best_update(g, v, i);
+  if (threadIdx.x == 0) {
+    Best g;
+    g.v = LLONG_MIN;
+    g.i = 0xFFFFFFFFu;
+    for (uint32_t b = 0; b < gridDim.x; ++b) {
+      const long long v = *(volatile const long long*)(cand + 2 * b);
+      const uint32_t i = (uint32_t) * (volatile const long long*)(cand + 2 * b + 1);
+      if (i != 0xFFFFFFFFu) best_update(g, v, i);
+    }
+    sh.am_v[0] = g.v;
+    sh.am_i[0] = g.i;
+    sh.smp_state = hdr_ld<unsigned long long>(p.st, kHSeed);
+    sh.smp_sum = 0;
+    sh.smp_draw = 0;
   }
-  sh.am_v[0] = g.v;
-  sh.am_i[0] = g.i;
+  const uint32_t temp = hdr_ld<uint32_t>(p.st, kHTemp);
+  if (temp == 0) return;
+  // sum and draw passes by block 0's consumer warps; the ring's shared memory is free now
+  consumer_bar();
+  const SampleOut so = block_sample(reinterpret_cast<const long long*>(st64(p, p.off_logits)),
+                                    p.vocab, sh.am_v[0], temp, p.exp_tab, sh.smp_state,
+                                    reinterpret_cast<unsigned long long*>(ring_of()), kNCW,
+                                    [] { consumer_bar(); });
+  if (threadIdx.x == 0) {
+    sh.am_i[0] = so.token;
+    sh.smp_state = so.state;
+    sh.smp_sum = so.sum;
+    sh.smp_draw = so.draw;
+  }
 }
 
 // The whole position for one CTA, with its scratch at `work`.
@@ -1242,6 +1262,9 @@ __device__ __forceinline__ void step_body(const StepParams& p, uint8_t* work, Sh
     hdr<uint32_t>(st, kHGenerated) = gen + 1;
     hdr<uint32_t>(st, kHLastTok) = tok;
     hdr<long long>(st, kHMaxLogit) = sh.am_v[0];
+    hdr<unsigned long long>(st, kHSeed) = sh.smp_state;
+    hdr<unsigned long long>(st, kHExpSum) = sh.smp_sum;
+    hdr<unsigned long long>(st, kHDraw) = sh.smp_draw;
     const bool stop = (hdr_ld<uint32_t>(st, kHFlags) & CK_FLAG_STOP_TOKENS) && (tok == 1 || tok == 2);
     if (gen + 1 == hdr_ld<uint32_t>(st, kHMaxTok) || stop) hdr<uint32_t>(st, kHPhase) = CK_PHASE_DONE;
   }

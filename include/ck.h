@@ -39,7 +39,7 @@ extern "C" {
                                    or a device model buffer shorter than ck_model_size */
 #define CK_MISSING_WEIGHTS 5    /* reserved: a model always holds all its matrices */
 #define CK_INVALID_PROMPT 6     /* no prompt ids, an id >= vocab, max tokens 0 or above the
-                                   context, or a temperature other than 0 */
+                                   context, or a temperature above 16 (16 << 16) */
 #define CK_CONTEXT_EXCEEDED 7   /* prompt ids + max tokens - 1 above the context */
 #define CK_ARITHMETIC 8         /* a key or value that does not fit the cache's 32 bits */
 #define CK_CUDA_ERROR 9         /* a CUDA runtime call failed (library addition) */
@@ -137,12 +137,17 @@ void ck_free_model(ck_model* m);
  *   0  "CKSTATE1"        8  u32 phase: 3 running, 20 done, 21 failed
  *   12 u32 position (the next position to run)   16 u32 prompt ids   20 u32 max tokens
  *   24 u32 cache positions = prompt ids + max tokens - 1          28 u32 generated tokens
- *   32 u32 flags (bit 0: tokens 1 and 2 complete the run)        36 u32 temperature (0)
+ *   32 u32 flags (bit 0: tokens 1 and 2 complete the run)
+ *   36 u32 temperature, 16 fraction bits (0: the maximum pass alone)
  *   40 u32 error (0 or 8)   44 u32 last generated token (0xFFFFFFFF before the first)
- *   48 u64 seed   56 u64 turns   64 u64 first error key (all ones if none):
+ *   48 u64 the sampling generator's state: the seed (0x9E3779B97F4A7C15 for a zero seed),
+ *      advanced once per token drawn above temperature zero   56 u64 turns
+ *   64 u64 first error key (all ones if none):
  *      position << 44 | layer << 32 | phase << 24 | element, phase 6 key store, 7 value
  *      store, 8 key store after rotary   72 i64 largest logit of the last generating
- *      position   80 7 x u32 the model's configuration   108..127 zero   128..255 scratch.
+ *      position   80 7 x u32 the model's configuration   108 zero
+ *   112 u64 sum of exponentials and 120 u64 draw of the last token sampled above temperature
+ *      zero (both 0 at temperature zero)   128..255 scratch.
  * Buffers, each at a multiple of 256 bytes from the state start, in order:
  *   prompt ids u32[n_prompt], output tokens u32[max_tokens], x (activations) i64[dim],
  *   four working vectors i64[dim] (xb, q, o, y), h i64[hidden], logits i64[vocab],
@@ -161,6 +166,10 @@ int ck_state_size(const ck_model* m, uint32_t n_prompt, uint32_t max_tokens, siz
 /* The page's init_state ("The Rust API") in ids mode: zeroes the state and writes a fresh
  * header and the prompt ids (host_ids, n_ids entries, the full prompt: no opening token is
  * added).  dev_state must be 256-byte aligned and exactly ck_state_size bytes.
+ * temperature_q16 (0 ..= 16 << 16, 16 fraction bits) and seed select phase 19 ("Sampling"):
+ * at zero the first largest logit; above zero the sum pass over
+ * EXP[min(((max - logit) / temperature) >> 8, 4096)] and a draw from xorshift64* seeded
+ * with seed (a zero seed starts at 0x9E3779B97F4A7C15).
  * Errors: 3 misaligned, 4 wrong length, 6, 7, 9, 10. */
 int ck_init_state(const ck_model* m, void* dev_state, size_t len, const uint32_t* host_ids,
                   uint32_t n_ids, uint32_t max_tokens, uint32_t temperature_q16, uint64_t seed,

@@ -37,11 +37,11 @@ class Pair:
         assert rc == 0, rc
         assert self.gpu.set_path(PATHS[path]) == 0
 
-    def init(self, ck, ids, max_tokens, flags=0):
-        rc, so = self.orc.init_state(ids, max_tokens, flags=flags)
+    def init(self, ck, ids, max_tokens, flags=0, temperature_q16=0, seed=0):
+        rc, so = self.orc.init_state(ids, max_tokens, temperature_q16, seed, flags=flags)
         assert rc == 0
         sg = self.gpu.new_state(len(ids), max_tokens)
-        assert self.gpu.init_state(sg, ids, max_tokens, flags=flags) == 0
+        assert self.gpu.init_state(sg, ids, max_tokens, temperature_q16, seed, flags=flags) == 0
         return so, sg
 
 
@@ -230,6 +230,47 @@ def test_every_position_matches_the_oracle(ck, pairs, name):
     assert oracle.header(so)["phase"] == oracle.PHASE_DONE
     rc, toks = P.gpu.output_tokens(sg)
     assert rc == 0 and len(toks) == wl.steps
+
+
+SAMPLING = [(1 << 16, 0), (16 << 16, 12345), (3 << 14, 2**64 - 1), (1, 99)]
+
+
+@pytest.mark.parametrize("temp,seed", SAMPLING)
+def test_sampled_positions_match_the_oracle(ck, pairs, temp, seed):
+    """Phase 19 above temperature zero (sum pass, draw pass, the generator state, sum and
+    draw in the header): every position of two models against the oracle."""
+    for name in ("gqa", "tiny_ws"):
+        wl = MODELS[name]
+        P = pairs[name]
+        ids = synth.prompt_ids(wl.spec, wl.n_prompt)
+        so, sg = P.init(ck, ids, wl.steps, temperature_q16=temp, seed=seed)
+        for pos in range(wl.n_prompt + wl.steps - 1):
+            rco, reso = P.orc.turn(so, 1)
+            rcg, resg = P.gpu.turn(sg, 1)
+            assert rco == rcg == 0 and reso == resg, (name, pos, reso, resg)
+            compare_states(P.orc, so, ck.state_download(sg), wl.n_prompt, wl.steps,
+                           f"{name} temperature {temp} position {pos}")
+        h = oracle.header(so)
+        assert h["phase"] == oracle.PHASE_DONE and h["exp_sum"] >= 1 << 30
+
+
+WIDE_VOCAB = synth.ModelSpec("wide_vocab", 64, 172, 2, 4, 4, 70001, 64, scale_rule="well", tied=False,
+                             seed=0x5EED0031)
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_sampling_over_a_wide_vocabulary(ck, path):
+    """A vocabulary of 70,001 entries: the sampler's groups hold several 32-entry chunks
+    and the last chunk is ragged; both temperatures against the oracle at every position."""
+    P = Pair(ck, WIDE_VOCAB, path)
+    ids = synth.prompt_ids(WIDE_VOCAB, 6)
+    for temp, seed in ((16 << 16, 5), (1 << 16, 0), (0, 0)):
+        so, sg = P.init(ck, ids, 10, temperature_q16=temp, seed=seed)
+        for pos in range(15):
+            rco, reso = P.orc.turn(so, 1)
+            rcg, resg = P.gpu.turn(sg, 1)
+            assert rco == rcg == 0 and reso == resg, (temp, pos, reso, resg)
+            compare_states(P.orc, so, ck.state_download(sg), 6, 10, f"wide vocab {temp} {pos}")
 
 
 def test_many_positions_in_one_turn(ck, pairs):
