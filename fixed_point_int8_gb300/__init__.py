@@ -61,6 +61,7 @@ def lib() -> ctypes.CDLL:
             "ck_set_step_slots": ([vp, ctypes.c_uint32], ctypes.c_int),
             "ck_set_attention_split": ([vp, ctypes.c_uint32], ctypes.c_int),
             "ck_set_step_prefetch": ([vp, ctypes.c_uint32], ctypes.c_int),
+            "ck_set_prefill": ([vp, ctypes.c_uint32], ctypes.c_int),
             "ck_free_model": ([vp], None),
             "ck_state_size": ([vp, u32, u32, ctypes.POINTER(sz)], ctypes.c_int),
             "ck_init_state": ([vp, vp, sz, vp, u32, u32, u32, u64, u32, vp], ctypes.c_int),
@@ -153,6 +154,10 @@ class Model:
     def set_step_prefetch(self, kb_per_block: int) -> int:
         """L2 prefetch distance of the persistent kernel, KB per block (0: default)."""
         return lib().ck_set_step_prefetch(self._h, kb_per_block)
+
+    def set_prefill(self, positions: int) -> int:
+        """Prompt positions per layer-major prefill chunk (0 or 1: position by position)."""
+        return lib().ck_set_prefill(self._h, positions)
 
     def set_attention_split(self, positions: int) -> int:
         """Positions up to which each block of an attention head scores all of them (0: default)."""

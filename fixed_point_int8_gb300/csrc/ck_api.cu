@@ -36,6 +36,10 @@ struct ck_model {
   int smem_optin;        // largest shared memory a block may opt into
   size_t step_smem;      // dynamic shared memory available to the one-position kernel
   std::vector<DevLayer> layers;
+  uint32_t pf_cap;       // prompt positions per layer-major chunk (0: position by position)
+  uint8_t* pf_work;      // the chunk's device scratch, allocated at first use
+  size_t pf_bytes;
+  bool pf_configured;
   cudaStream_t capture;
   struct Graph {
     void* state;
@@ -50,6 +54,8 @@ struct ck_model {
 namespace {
 
 constexpr uint32_t kTable = 4097;
+constexpr uint32_t kDefaultPrefillChunk = 256;  // prompt positions per layer-major chunk
+constexpr uint32_t kMaxPrefillChunk = 4096;
 
 uint32_t rd32(const uint8_t* p) { uint32_t v; memcpy(&v, p, 4); return v; }
 uint64_t rd64(const uint8_t* p) { uint64_t v; memcpy(&v, p, 8); return v; }
@@ -657,6 +663,45 @@ int get_graph(ck_model* m, void* dev_state, size_t len, const StateLayout& lay, 
   return CK_OK;
 }
 
+PrefillModel prefill_model(const ck_model* m) {
+  PrefillModel pm;
+  pm.cfg = m->cfg;
+  pm.head_dim = m->head_dim;
+  pm.kv_dim = m->kv_dim;
+  pm.inv_sqrt = m->inv_sqrt;
+  pm.pitch_d = m->pitch_d;
+  pm.pitch_h = m->pitch_h;
+  pm.embed = m->embed;
+  pm.embed_scale = m->embed_scale;
+  pm.layers = m->layers.data();
+  pm.rope = m->rope;
+  pm.exp_tab = m->exp_tab;
+  pm.silu_tab = m->silu_tab;
+  return pm;
+}
+
+// Positions pos .. pos+P-1 layer by layer.  CK_INVALID_ARGUMENT: the batched kernels do not
+// handle this model or cache (the caller runs the positions one by one instead).
+int prefill_chunk(ck_model* m, uint8_t* st, const StateLayout& lay, uint32_t pos, uint32_t P,
+                  cudaStream_t s) {
+  const PrefillModel pm = prefill_model(m);
+  if (!prefill_supported(pm, lay.cache, (size_t)m->smem_optin)) return CK_INVALID_ARGUMENT;
+  if (!m->pf_configured) {
+    CK_CUDA(configure_prefill((size_t)m->smem_optin));
+    m->pf_configured = true;
+  }
+  const size_t need = prefill_work_bytes(pm, m->pf_cap);
+  if (m->pf_bytes < need) {
+    if (m->pf_work) CK_CUDA(cudaFree(m->pf_work));
+    m->pf_work = nullptr;
+    m->pf_bytes = 0;
+    CK_CUDA(cudaMalloc(&m->pf_work, need));
+    m->pf_bytes = need;
+  }
+  CK_CUDA(enqueue_prefill(pm, st, lay, pos, P, m->pf_work, m->pf_cap, s));
+  return CK_OK;
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -787,6 +832,10 @@ int ck_load_model(const void* artifact, size_t len, void* dev_mem, size_t dev_le
   m->max_slots = 0;
   m->att_full = 0;
   m->pf_kb = 0;
+  m->pf_cap = kDefaultPrefillChunk;
+  m->pf_work = nullptr;
+  m->pf_bytes = 0;
+  m->pf_configured = false;
   if (cudaMemcpyAsync(m->dev_layers, m->layers.data(), sizeof(DevLayer) * c.layers,
                       cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess) {
@@ -846,8 +895,18 @@ int ck_model_config(const ck_model* m, ck_config* out) {
   return CK_OK;
 }
 
+int ck_set_prefill(ck_model* m, uint32_t positions) {
+  if (!m || positions > kMaxPrefillChunk) return CK_INVALID_ARGUMENT;
+  m->pf_cap = positions;
+  if (m->pf_work) cudaFree(m->pf_work);  // resized at next use
+  m->pf_work = nullptr;
+  m->pf_bytes = 0;
+  return CK_OK;
+}
+
 void ck_free_model(ck_model* m) {
   if (!m) return;
+  if (m->pf_work) cudaFree(m->pf_work);
   for (auto& g : m->graphs) cudaGraphExecDestroy(g.exec);
   if (m->capture) cudaStreamDestroy(m->capture);
   delete m;
@@ -913,12 +972,25 @@ int ck_turn(ck_model* m, void* dev_state, size_t len, uint32_t n_positions, void
   if (pos0 >= lay.cache) return CK_INVALID_STATE;
   uint32_t n = n_positions;
   if (n > lay.cache - pos0) n = lay.cache - pos0;
-  for (uint32_t i = 0; i < n; ++i) {
-    const bool generating = pos0 + i + 1 >= np;
+  for (uint32_t i = 0; i < n;) {
+    const uint32_t pos = pos0 + i;
+    // two or more prompt positions that generate no token: layer-major, in chunks
+    const uint32_t run = pos + 1 < np ? std::min(np - 1 - pos, n - i) : 0u;
+    if (run >= 2 && m->pf_cap >= 2) {
+      const uint32_t P = std::min(run, m->pf_cap);
+      rc = prefill_chunk(m, static_cast<uint8_t*>(dev_state), lay, pos, P, s);
+      if (rc != CK_OK && rc != CK_INVALID_ARGUMENT) return rc;
+      if (rc == CK_OK) {
+        i += P;
+        continue;
+      }
+    }
+    const bool generating = pos + 1 >= np;
     cudaGraphExec_t exec;
     rc = get_graph(m, dev_state, len, lay, generating, &exec);
     if (rc) return rc;
     CK_CUDA(cudaGraphLaunch(exec, s));
+    ++i;
   }
   HostHeader h1;
   rc = read_header(dev_state, &h1, s);

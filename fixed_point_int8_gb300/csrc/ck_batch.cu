@@ -1,0 +1,746 @@
+// Layer-major prefill: the prompt positions of one run go through each layer together
+// ("The inference core", "The forward pass, in order": phases 3 to 16 for every position
+// that generates no token).
+//
+// Position by position, every matrix is read from memory once per position.  Here a chunk
+// of P prompt positions moves through a layer at once, so each matrix is read once per
+// chunk and its matrix rows ("A matrix row") for all P positions become one dense
+// contraction  Y[n][r] = sum_c (byte[r][c] - 128) * x[n][c]  on the tensor cores.
+//
+// Exactness.  When every x of a vector fits 8L signed bits,
+//   x = sum_{k<L-1} 256^k u_k + 256^(L-1) s,   u_k bytes (0..255), s a signed byte,
+// so the contraction splits into L contractions over byte planes.  Every plane value and
+// every (byte - 128) is an integer of at most 8 bits, exact in f16; the warp MMA forms the
+// products exactly and adds them in f32, which is exact while every partial sum stays
+// below 2^24: 512 columns of |(byte - 128) u| <= 128 * 255 = 32,640 reach at most
+// 16,711,680.  So every 512 columns the f32 sums move into i32 accumulators (whole rows stay
+// below 2^31 up to 65,793 columns), and the planes are combined modulo 2^64 with the row
+// scale and the >> 24: the same bits as the wrapping definition, since
+// sum_c byte*x - 128 * sum_c x = sum_c (byte - 128) x  modulo 2^64.
+//
+// The rest of each layer (normalization, rotary, checked cache stores, attention over the
+// run's cache with the causal limit of each position, SiLU gating, residuals) runs per
+// position exactly as in the one-position kernels, P positions per launch.  A cache store
+// that does not fit records the smallest (position, layer, phase, element) key, which is the
+// first failing store in position order, since no position reads a later position's values.
+#include <cuda_fp16.h>
+
+#include "ck_internal.cuh"
+
+namespace ck {
+namespace {
+
+constexpr uint32_t kBM = 128;        // contraction tile: 128 matrix rows
+constexpr uint32_t kBN = 64;         // x 64 plane columns (positions of one plane)
+constexpr uint32_t kBK = 128;        // x 128 columns, one column group
+constexpr int kGemmThreads = 256;    // 8 warps, 4 (rows) x 2 (columns), 32 x 32 each
+constexpr int kStages = 3;
+constexpr uint32_t kATile = kBM * kBK;       // u8 weights, in the matrix's own layout
+constexpr uint32_t kBTile = kBN * kBK * 2;   // f16 planes
+constexpr uint32_t kStageBytesB = kATile + kBTile;
+constexpr uint32_t kFlushGroups = 4;         // column groups between f32 -> i32 moves
+constexpr int kRowThreads = 256;
+
+enum BEpi : int { kBEpiQKV = 0, kBEpiResid = 1, kBEpiSiLU = 2 };
+
+__device__ __forceinline__ bool running(const uint8_t* st) {
+  return hdr_ld<uint32_t>(st, kHPhase) == CK_PHASE_RUNNING;
+}
+
+// Limbs of a vector from the OR of x ^ (x >> 63) over it: the smallest L with every x in
+// 8L signed bits.
+__device__ __forceinline__ int limbs_of_or(unsigned long long orv) {
+  int L = 1;
+  while (L < 8 && (orv >> (8 * L - 1)) != 0) ++L;
+  return L;
+}
+
+__device__ __forceinline__ unsigned long long bwarp_sum(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ unsigned long long bwarp_or(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Block-wide sum (every thread gets it); red holds kRowThreads / 32 words.
+__device__ unsigned long long block_sum(unsigned long long v, unsigned long long* red) {
+  v = bwarp_sum(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  unsigned long long t = 0;
+  for (uint32_t w = 0; w < blockDim.x / 32; ++w) t += red[w];
+  __syncthreads();
+  return t;
+}
+
+// One atomic OR per block of the values' x ^ (x >> 63).
+__device__ void block_or_to(unsigned long long v, unsigned long long* dst, unsigned long long* red) {
+  v = bwarp_or(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long t = 0;
+    for (uint32_t w = 0; w < blockDim.x / 32; ++w) t |= red[w];
+    if (t) atomicOr(dst, t);
+  }
+}
+
+// ------------------------------------------------------------------ phase 3 and norms
+
+// Phase 3 for positions pos0 .. pos0+P-1 (one block each): x = ((byte - 128) * scale) >> 8.
+__global__ void __launch_bounds__(kRowThreads) k_bembed(const uint8_t* st, uint64_t off_prompt,
+                                                         uint32_t pos0, int64_t* X, uint32_t d,
+                                                         const uint8_t* E, const uint32_t* Es,
+                                                         uint32_t vocab, uint32_t* badpos) {
+  if (!running(st)) return;
+  const uint32_t n = blockIdx.x;
+  const uint32_t tok = reinterpret_cast<const uint32_t*>(st + off_prompt)[pos0 + n];
+  int64_t* x = X + (size_t)n * d;
+  if (tok >= vocab) {  // a state edited outside the library: that position fails
+    if (threadIdx.x == 0) atomicMin(badpos, pos0 + n);
+    for (uint32_t i = threadIdx.x; i < d; i += blockDim.x) x[i] = 0;
+    return;
+  }
+  const int64_t s = (int64_t)__ldg(Es + tok);
+  for (uint32_t i = threadIdx.x; i < d; i += blockDim.x)
+    x[i] = ((int64_t)E[grouped_offset(vocab, tok, i)] - 128) * s >> 8;
+}
+
+// "RMS normalization" of each position's row (one block each): rms = max(isqrt(sum x^2 / d
+// + 42,950), 1), y = ((x * w) / rms) >> 8 with the division truncating; ORs the outputs'
+// magnitudes into *orw for the plane count.
+__global__ void __launch_bounds__(kRowThreads) k_bnorm(const uint8_t* st, const int64_t* X,
+                                                        int64_t* XB, const int32_t* w, uint32_t d,
+                                                        unsigned long long* orw) {
+  __shared__ unsigned long long red[kRowThreads / 32];
+  __shared__ InvDiv div;
+  if (!running(st)) return;
+  const int64_t* x = X + (size_t)blockIdx.x * d;
+  int64_t* y = XB + (size_t)blockIdx.x * d;
+  unsigned long long ss = 0;
+  for (uint32_t i = threadIdx.x; i < d; i += blockDim.x)
+    ss += (unsigned long long)x[i] * (unsigned long long)x[i];
+  ss = block_sum(ss, red);
+  if (threadIdx.x == 0) {
+    uint64_t rms = isqrt_u64(ss / d + 42950ull);
+    if (rms < 1) rms = 1;
+    div = make_invdiv((uint32_t)rms);
+  }
+  __syncthreads();
+  const InvDiv D = div;
+  unsigned long long o = 0;
+  for (uint32_t i = threadIdx.x; i < d; i += blockDim.x) {
+    const int64_t v = sdiv_trunc(wmul(x[i], (int64_t)w[i]), D) >> 8;
+    y[i] = v;
+    o |= (unsigned long long)(v ^ (v >> 63));
+  }
+  block_or_to(o, orw, red);
+}
+
+// ------------------------------------------------------------------ byte planes
+
+// Plane layout, read by the contraction one 16 KB tile at a time: plane column
+// n' = k * Npad + n (plane k of position n), tiles of 64 plane columns x 128 columns stored
+// tile after tile (column groups inner), each tile 64 rows of 256 bytes (128 f16), the
+// 16-byte chunk j of row i at j ^ ((i & 7) << 1) so the MMA operand loads hit every bank.
+__device__ __forceinline__ uint64_t plane_offset(uint32_t np, uint32_t KG, uint32_t kg, uint32_t chunk) {
+  const uint32_t nt = np / kBN, nl = np % kBN;
+  return ((uint64_t)nt * KG + kg) * kBTile + (uint64_t)nl * 256 + ((chunk ^ ((nl & 7u) << 1)) << 4);
+}
+
+// Writes planes 0 .. L-1 of the P vectors V (row stride ld, cols used), zero beyond P and
+// cols.  One thread per 8 columns of one plane of one position.
+__global__ void __launch_bounds__(kRowThreads) k_bplanes(const uint8_t* st, const int64_t* V,
+                                                          uint32_t ld, uint32_t P, uint32_t cols,
+                                                          uint32_t Npad, uint32_t KG,
+                                                          const unsigned long long* orw, uint8_t* B) {
+  if (!running(st)) return;
+  const int L = limbs_of_or(*orw);
+  const uint32_t per_row = KG * 16;  // 8-column chunks of a row
+  const uint64_t total = (uint64_t)L * Npad * per_row;
+  for (uint64_t q = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; q < total;
+       q += (uint64_t)gridDim.x * blockDim.x) {
+    const uint32_t k = (uint32_t)(q / ((uint64_t)Npad * per_row));
+    const uint32_t rem = (uint32_t)(q % ((uint64_t)Npad * per_row));
+    const uint32_t n = rem / per_row, cc = rem % per_row;
+    const uint32_t kg = cc >> 4, ch = cc & 15u, c0 = kg * kBK + ch * 8;
+    uint32_t h[4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      int v2[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint32_t c = c0 + e + u;
+        const int64_t x = (n < P && c < cols) ? V[(size_t)n * ld + c] : 0;
+        v2[u] = (k + 1 < (uint32_t)L) ? (int)(((uint64_t)x >> (8 * k)) & 0xFFu)
+                                      : (int)(x >> (8 * k));  // top plane: signed
+      }
+      const __half2 hv = __halves2half2(__int2half_rn(v2[0]), __int2half_rn(v2[1]));
+      h[e >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
+    }
+    *reinterpret_cast<uint4*>(B + plane_offset(k * Npad + n, KG, kg, ch)) = make_uint4(h[0], h[1], h[2], h[3]);
+  }
+}
+
+// ------------------------------------------------------------------ the contraction
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Two weight bytes (selected by sel) as an f16 pair of byte - 128: 0x64XX is the f16 value
+// 1024 + XX exactly, and subtracting 1152 leaves XX - 128, also exact.
+__device__ __forceinline__ uint32_t bytes_to_f16x2(uint32_t w, uint32_t sel) {
+  const uint32_t h = __byte_perm(w, 0x64646464u, sel);
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
+  return r;
+}
+
+__device__ __forceinline__ void mma_f16(float* c, const uint32_t* a, const uint32_t* b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// S[n'][r] = sum_c (W[r][c] - 128) * plane[n'][c] for plane columns n' < L * Npad, one
+// 128 x 64 tile per block.  Within every 16-column step, lane (g, t) presents the physical
+// columns 4t .. 4t+3 of the step as the MMA's k = 2t, 2t+1, 2t+8, 2t+9, for the weights and
+// the planes alike, so each operand is one 32- or 64-bit shared load; the order of the
+// columns inside a sum does not matter.
+__global__ void __launch_bounds__(kGemmThreads, 2) k_bgemm(const uint8_t* st, const uint8_t* W,
+                                                           uint32_t rows, uint32_t KG,
+                                                           const uint8_t* B, uint32_t Npad,
+                                                           const unsigned long long* orw, int32_t* S) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  if (!running(st)) return;
+  const int L = limbs_of_or(*orw);
+  const uint32_t nt = blockIdx.y;
+  if (nt >= (uint32_t)L * (Npad / kBN)) return;
+  const uint32_t m0 = blockIdx.x * kBM;
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t wm = warp & 3u, wn = warp >> 2;
+  const uint32_t g = lane >> 2, t = lane & 3u;
+
+  auto load_stage = [&](uint32_t kg, uint32_t slot) {
+    uint8_t* sa = smem + slot * kStageBytesB;
+    uint8_t* sb = sa + kATile;
+    const uint8_t* ga = W + ((size_t)kg * rows + m0) * kBK;  // rows m0.. of group kg: contiguous
+    const uint8_t* gb = B + ((size_t)nt * KG + kg) * kBTile;
+    for (uint32_t q = tid; q < kATile / 16; q += kGemmThreads) {
+      const bool ok = m0 + (q >> 3) < rows;
+      cp_async16(sa + q * 16, ok ? ga + q * 16 : W, ok ? 16u : 0u);  // rows past the end: zeros
+    }
+    for (uint32_t q = tid; q < kBTile / 16; q += kGemmThreads) cp_async16(sb + q * 16, gb + q * 16, 16u);
+  };
+
+  float acc[2][4][4];
+  int32_t iacc[2][4][4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc[i][j][e] = 0.f;
+        iacc[i][j][e] = 0;
+      }
+
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s) {
+    if ((uint32_t)s < KG) load_stage((uint32_t)s, (uint32_t)s);
+    cp_async_commit();
+  }
+  for (uint32_t kg = 0; kg < KG; ++kg) {
+    cp_async_wait<kStages - 2>();
+    __syncthreads();
+    const uint32_t next = kg + kStages - 1;
+    if (next < KG) load_stage(next, next % kStages);
+    cp_async_commit();
+    const uint8_t* sa = smem + (kg % kStages) * kStageBytesB;
+    const uint8_t* sb = sa + kATile;
+#pragma unroll 2
+    for (uint32_t kk = 0; kk < 8; ++kk) {
+      uint32_t a[2][4], b[4][2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint32_t r0 = wm * 32 + i * 16 + g;  // r0 & 7 == g, and so is (r0 + 8) & 7
+        const uint32_t off = ((kk ^ g) << 4) + 4 * t;
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(sa + r0 * kBK + off);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(sa + (r0 + 8) * kBK + off);
+        a[i][0] = bytes_to_f16x2(w0, 0x5140u);
+        a[i][1] = bytes_to_f16x2(w1, 0x5140u);
+        a[i][2] = bytes_to_f16x2(w0, 0x5342u);
+        a[i][3] = bytes_to_f16x2(w1, 0x5342u);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t nl = wn * 32 + j * 8 + g;  // nl & 7 == g
+        const uint32_t chunk = (2 * kk + (t >> 1)) ^ (g << 1);
+        const uint2 v = *reinterpret_cast<const uint2*>(sb + nl * 256 + (chunk << 4) + 8 * (t & 1u));
+        b[j][0] = v.x;
+        b[j][1] = v.y;
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mma_f16(acc[i][j], a[i], b[j]);
+    }
+    if ((kg + 1) % kFlushGroups == 0 || kg + 1 == KG) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            iacc[i][j][e] += __float2int_rn(acc[i][j][e]);  // an integer below 2^24: exact
+            acc[i][j][e] = 0.f;
+          }
+    }
+  }
+  cp_async_wait<0>();
+  // lane (g, t) holds rows g and g + 8, plane columns 2t and 2t + 1 of each 16 x 8 tile
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t n0 = nt * kBN + wn * 32 + j * 8 + 2 * t;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t r = m0 + wm * 32 + i * 16 + g + (e >= 2 ? 8u : 0u);
+        const uint32_t np = n0 + (e & 1);
+        if (r < rows) S[(size_t)np * rows + r] = iacc[i][j][e];
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ epilogues
+
+struct BEpiParams {
+  const uint8_t* st;
+  const int32_t* S;
+  uint32_t rows, Npad, P, pos0;
+  const unsigned long long* orw;  // the input vector's OR word (its plane count)
+  const uint32_t* scale;
+  int mode;
+  // QKV
+  int64_t* Q;                     // [P][dim] rotated queries
+  int32_t* kc;                    // this layer's keys and values, position 0
+  int32_t* vc;
+  const int32_t* rope;
+  uint32_t dim, kv_dim, head_dim, layer;
+  // residual: X[n][r] += y;  SiLU: H[n][j] = (silu(y_2j) * y_2j+1) >> 16
+  int64_t* X;
+  int64_t* H;
+  uint32_t hidden;
+  const int32_t* silu_tab;
+  unsigned long long* or_out;     // SiLU: the output vector's OR word
+};
+
+// y[n][r] = ((sum_k S_k[n][r] << 8k) * scale[r]) >> 24, wrapping.
+__device__ __forceinline__ int64_t combine(const BEpiParams& p, int L, uint32_t n, uint32_t r) {
+  unsigned long long a = 0;
+  for (int k = 0; k < L; ++k)
+    a += (unsigned long long)(long long)p.S[((size_t)k * p.Npad + n) * p.rows + r] << (8 * k);
+  return (int64_t)(a * (unsigned long long)__ldg(p.scale + r)) >> 24;
+}
+
+// One thread per (position, row pair): rows 2i and 2i+1 are a rotary pair in Q and K and a
+// gate/up pair in the feed-forward matrix.
+__global__ void __launch_bounds__(kRowThreads) k_bepi(const BEpiParams p) {
+  __shared__ unsigned long long red[kRowThreads / 32];
+  if (!running(p.st)) return;
+  const int L = limbs_of_or(*p.orw);
+  const uint32_t pairs = p.rows / 2;
+  unsigned long long o = 0;
+  for (uint64_t idx = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < (uint64_t)p.P * pairs;
+       idx += (uint64_t)gridDim.x * blockDim.x) {
+    const uint32_t n = (uint32_t)(idx / pairs), r = 2 * (uint32_t)(idx % pairs);
+    const int64_t y0 = combine(p, L, n, r), y1 = combine(p, L, n, r + 1);
+    if (p.mode == kBEpiResid) {
+      int64_t* x = p.X + (size_t)n * p.rows + r;
+      x[0] = wadd(x[0], y0);
+      x[1] = wadd(x[1], y1);
+    } else if (p.mode == kBEpiSiLU) {
+      const int64_t h = wmul(silu_lookup(y0, p.silu_tab), y1) >> 16;
+      p.H[(size_t)n * p.hidden + (r >> 1)] = h;
+      o |= (unsigned long long)(h ^ (h >> 63));
+    } else {
+      const uint32_t pos = p.pos0 + n;
+      const int32_t* rope = p.rope + (size_t)pos * p.head_dim;  // [pos][head/2] pairs (cos, sin)
+      if (r < p.dim) {
+        const int32_t* cs = rope + ((r % p.head_dim) & ~1u);
+        int64_t a2, b2;
+        rotate_pair(y0, y1, __ldg(cs), __ldg(cs + 1), a2, b2);
+        p.Q[(size_t)n * p.dim + r] = a2;
+        p.Q[(size_t)n * p.dim + r + 1] = b2;
+      } else if (r < p.dim + p.kv_dim) {
+        const uint32_t e = r - p.dim;
+        if (!fits_i32(y0)) record_error(const_cast<uint8_t*>(p.st), err_key(pos, p.layer, 6, e));
+        if (!fits_i32(y1)) record_error(const_cast<uint8_t*>(p.st), err_key(pos, p.layer, 6, e + 1));
+        const int32_t* cs = rope + ((e % p.head_dim) & ~1u);
+        int64_t a2, b2;
+        rotate_pair((int64_t)(int32_t)y0, (int64_t)(int32_t)y1, __ldg(cs), __ldg(cs + 1), a2, b2);
+        if (!fits_i32(a2)) record_error(const_cast<uint8_t*>(p.st), err_key(pos, p.layer, 8, e));
+        if (!fits_i32(b2)) record_error(const_cast<uint8_t*>(p.st), err_key(pos, p.layer, 8, e + 1));
+        p.kc[(size_t)pos * p.kv_dim + e] = (int32_t)a2;
+        p.kc[(size_t)pos * p.kv_dim + e + 1] = (int32_t)b2;
+      } else {
+        const uint32_t e = r - p.dim - p.kv_dim;
+        if (!fits_i32(y0)) record_error(const_cast<uint8_t*>(p.st), err_key(pos, p.layer, 7, e));
+        if (!fits_i32(y1)) record_error(const_cast<uint8_t*>(p.st), err_key(pos, p.layer, 7, e + 1));
+        p.vc[(size_t)pos * p.kv_dim + e] = (int32_t)y0;
+        p.vc[(size_t)pos * p.kv_dim + e + 1] = (int32_t)y1;
+      }
+    }
+  }
+  if (p.mode == kBEpiSiLU) block_or_to(o, p.or_out, red);
+}
+
+// ------------------------------------------------------------------ attention
+
+struct BAttnParams {
+  const uint8_t* st;
+  const int64_t* Q;     // [P][dim]
+  int64_t* O;           // [P][dim]
+  const int32_t* kc;    // this layer's cache, position 0
+  const int32_t* vc;
+  const uint32_t* exp_tab;
+  uint32_t pos0, dim, heads, kv_heads, head_dim, kv_dim, inv_sqrt;
+  unsigned long long* or_out;
+};
+
+constexpr int kAttnWarps = kRowThreads / 32;
+
+size_t battn_smem(uint32_t hd, uint32_t positions) {
+  return 8 * ((size_t)hd * (1 + kAttnWarps) + kAttnWarps + positions);
+}
+
+// Phase 9 for query position pos0 + blockIdx.y and head blockIdx.x ("Attention, stage by
+// stage"), over the cache positions 0 .. pos: scores and their maximum, exponentials and
+// their sum, probabilities with 24 fraction bits, and the weighted values with one >> 24.
+__global__ void __launch_bounds__(kRowThreads) k_battn(const BAttnParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  if (!running(p.st)) return;
+  const uint32_t hd = p.head_dim, h = blockIdx.x, n = blockIdx.y;
+  const uint32_t pos = p.pos0 + n, np = pos + 1;
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int64_t* q_s = reinterpret_cast<int64_t*>(smem);
+  unsigned long long* part = reinterpret_cast<unsigned long long*>(q_s + hd);  // [warps][hd]
+  long long* red = reinterpret_cast<long long*>(part + (size_t)kAttnWarps * hd);
+  long long* sc = red + kAttnWarps;                                            // [np]
+  const uint32_t kvh = h / (p.heads / p.kv_heads);
+  for (uint32_t i = tid; i < hd; i += kRowThreads) q_s[i] = p.Q[(size_t)n * p.dim + (size_t)h * hd + i];
+  __syncthreads();
+  const int32_t* Kh = p.kc + (size_t)kvh * hd;
+  const int32_t* Vh = p.vc + (size_t)kvh * hd;
+  const uint32_t lpp = hd / 4, ppw = 32 / lpp;  // lanes per position (four elements each)
+  const uint32_t sub = lane % lpp, slot = lane / lpp, e0 = sub * 4;
+  const int64_t q0 = q_s[e0], q1 = q_s[e0 + 1], q2 = q_s[e0 + 2], q3 = q_s[e0 + 3];
+
+  long long lmax = LLONG_MIN;
+  for (uint32_t base = warp * ppw; base < np; base += kAttnWarps * ppw) {
+    const uint32_t tl = base + slot;
+    unsigned long long dsum = 0;
+    if (tl < np) {
+      const int4 k4 = *reinterpret_cast<const int4*>(Kh + (size_t)tl * p.kv_dim + e0);
+      dsum = (unsigned long long)q0 * (unsigned long long)(long long)k4.x +
+             (unsigned long long)q1 * (unsigned long long)(long long)k4.y +
+             (unsigned long long)q2 * (unsigned long long)(long long)k4.z +
+             (unsigned long long)q3 * (unsigned long long)(long long)k4.w;
+    }
+    for (uint32_t o = lpp >> 1; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+    if (tl < np && sub == 0) {
+      long long s = (long long)dsum >> 16;
+      s = (long long)((unsigned long long)s * (unsigned long long)p.inv_sqrt) >> 24;
+      sc[tl] = s;
+      lmax = s > lmax ? s : lmax;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const long long v = __shfl_xor_sync(0xffffffffu, lmax, o);
+    lmax = v > lmax ? v : lmax;
+  }
+  if (lane == 0) red[warp] = lmax;
+  __syncthreads();
+  long long m = red[0];
+  for (int w = 1; w < kAttnWarps; ++w) m = red[w] > m ? red[w] : m;
+  __syncthreads();
+
+  unsigned long long z = 0;
+  for (uint32_t tl = tid; tl < np; tl += kRowThreads) {
+    unsigned long long idx = ((unsigned long long)m - (unsigned long long)sc[tl]) >> 8;
+    if (idx > 4096) idx = 4096;
+    const unsigned long long e = __ldg(p.exp_tab + idx);
+    sc[tl] = (long long)e;
+    z += e;
+  }
+  z = bwarp_sum(z);
+  if (lane == 0) red[warp] = (long long)z;
+  __syncthreads();
+  unsigned long long Z = 0;
+  for (int w = 0; w < kAttnWarps; ++w) Z += (unsigned long long)red[w];
+  for (uint32_t tl = tid; tl < np; tl += kRowThreads)
+    sc[tl] = (long long)(((unsigned long long)sc[tl] << 24) / Z);
+  __syncthreads();
+
+  unsigned long long a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+  for (uint32_t base = warp * ppw; base < np; base += kAttnWarps * ppw) {
+    const uint32_t tl = base + slot;
+    if (tl < np) {
+      const int4 v4 = *reinterpret_cast<const int4*>(Vh + (size_t)tl * p.kv_dim + e0);
+      const long long pr = sc[tl];
+      a0 += (unsigned long long)(pr * (long long)v4.x);
+      a1 += (unsigned long long)(pr * (long long)v4.y);
+      a2 += (unsigned long long)(pr * (long long)v4.z);
+      a3 += (unsigned long long)(pr * (long long)v4.w);
+    }
+  }
+  for (uint32_t o = 16; o >= lpp && o > 0; o >>= 1) {
+    a0 += __shfl_xor_sync(0xffffffffu, a0, o);
+    a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+    a2 += __shfl_xor_sync(0xffffffffu, a2, o);
+    a3 += __shfl_xor_sync(0xffffffffu, a3, o);
+  }
+  if (slot == 0) {
+    unsigned long long* dst = part + (size_t)warp * hd + e0;
+    dst[0] = a0;
+    dst[1] = a1;
+    dst[2] = a2;
+    dst[3] = a3;
+  }
+  __syncthreads();
+  unsigned long long orv = 0;
+  for (uint32_t j = tid; j < hd; j += kRowThreads) {
+    unsigned long long s = 0;
+    for (int w = 0; w < kAttnWarps; ++w) s += part[(size_t)w * hd + j];
+    const long long v = (long long)s >> 24;
+    p.O[(size_t)n * p.dim + (size_t)h * hd + j] = v;
+    orv |= (unsigned long long)(v ^ (v >> 63));
+  }
+  block_or_to(orv, p.or_out, reinterpret_cast<unsigned long long*>(red));
+}
+
+// ------------------------------------------------------------------ end of the chunk
+
+// The chunk's outcome: the first failing position (a cache store that did not fit, error 8,
+// or a prompt id outside the vocabulary, error 3) fails the state there; otherwise the last
+// position's residual becomes the state's x and the cursor moves past the chunk.
+__global__ void __launch_bounds__(kRowThreads) k_bfinish(uint8_t* st, const int64_t* X, int64_t* x,
+                                                         uint32_t d, uint32_t pos0, uint32_t P,
+                                                         const uint32_t* badpos) {
+  if (!running(st)) return;
+  const uint64_t key = hdr_ld<uint64_t>(st, kHErrKey);
+  const uint32_t key_pos = key == kNoError ? 0xFFFFFFFFu : (uint32_t)(key >> 44);
+  const uint32_t bad = *badpos;
+  __syncthreads();  // every thread has read the header before thread 0 writes it
+  if (bad != 0xFFFFFFFFu && bad <= key_pos) {
+    if (threadIdx.x == 0) {
+      hdr<uint64_t>(st, kHErrKey) = kNoError;  // that position stopped before any store
+      hdr<uint32_t>(st, kHError) = CK_INVALID_STATE;
+      hdr<uint32_t>(st, kHPosition) = bad;
+      hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
+    }
+    return;
+  }
+  if (key != kNoError) {
+    if (threadIdx.x == 0) {
+      hdr<uint32_t>(st, kHError) = CK_ARITHMETIC;
+      hdr<uint32_t>(st, kHPosition) = key_pos;
+      hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
+    }
+    return;
+  }
+  for (uint32_t i = threadIdx.x; i < d; i += blockDim.x) x[i] = X[(size_t)(P - 1) * d + i];
+  if (threadIdx.x == 0) hdr<uint32_t>(st, kHPosition) = pos0 + P;
+}
+
+uint32_t pad64(uint32_t n) { return (n + 63u) & ~63u; }
+
+struct WorkLayout {
+  uint64_t X, XB, Q, O, H, B, S, orw, bad, size;
+};
+
+WorkLayout work_layout(const PrefillModel& m, uint32_t cap) {
+  const uint64_t Np = pad64(cap);
+  const uint64_t kg_max = std::max(m.pitch_d, m.pitch_h) / kBK;
+  const uint64_t rows_max = std::max<uint64_t>((uint64_t)m.cfg.dim + 2ull * m.kv_dim, 2ull * m.cfg.hidden);
+  WorkLayout w;
+  uint64_t off = 0;
+  auto take = [&](uint64_t bytes) { uint64_t o = off; off = align256(off + bytes); return o; };
+  w.X = take(8 * Np * m.cfg.dim);
+  w.XB = take(8 * Np * m.cfg.dim);
+  w.Q = take(8 * Np * m.cfg.dim);
+  w.O = take(8 * Np * m.cfg.dim);
+  w.H = take(8 * Np * m.cfg.hidden);
+  w.B = take(8 * (Np / kBN) * kg_max * kBTile);     // up to 8 planes
+  w.S = take(4 * 8 * Np * rows_max);
+  w.orw = take(8ull * 4 * m.cfg.layers);
+  w.bad = take(4);
+  w.size = off;
+  return w;
+}
+
+}  // namespace
+
+size_t prefill_work_bytes(const PrefillModel& m, uint32_t cap) { return work_layout(m, cap).size; }
+
+bool prefill_supported(const PrefillModel& m, uint32_t cache, size_t smem_optin) {
+  const uint32_t hd = m.head_dim;
+  if (hd % 4 || hd > 128 || hd < 4 || (32 % (hd / 4)) != 0) return false;  // attention lane layout
+  if (m.cfg.heads % m.cfg.kv_heads) return false;
+  if (m.pitch_d > 65536 || m.pitch_h > 65536) return false;               // i32 plane sums
+  if (battn_smem(hd, cache) > smem_optin) return false;
+  if ((size_t)kStages * kStageBytesB > smem_optin) return false;
+  return true;
+}
+
+cudaError_t configure_prefill(size_t smem_optin) {
+  cudaError_t e = cudaFuncSetAttribute(k_bgemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kStages * kStageBytesB);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_battn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_optin);
+}
+
+cudaError_t enqueue_prefill(const PrefillModel& m, uint8_t* st, const StateLayout& lay, uint32_t pos0,
+                            uint32_t P, uint8_t* work, uint32_t cap, cudaStream_t s) {
+  if (P == 0 || P > cap) return cudaErrorInvalidValue;
+  const ck_config& c = m.cfg;
+  const WorkLayout w = work_layout(m, cap);
+  const uint32_t Npad = pad64(P);
+  const uint32_t KGd = m.pitch_d / kBK, KGh = m.pitch_h / kBK;
+  int64_t* X = reinterpret_cast<int64_t*>(work + w.X);
+  int64_t* XB = reinterpret_cast<int64_t*>(work + w.XB);
+  int64_t* Q = reinterpret_cast<int64_t*>(work + w.Q);
+  int64_t* O = reinterpret_cast<int64_t*>(work + w.O);
+  int64_t* H = reinterpret_cast<int64_t*>(work + w.H);
+  uint8_t* B = work + w.B;
+  int32_t* S = reinterpret_cast<int32_t*>(work + w.S);
+  unsigned long long* orw = reinterpret_cast<unsigned long long*>(work + w.orw);
+  uint32_t* bad = reinterpret_cast<uint32_t*>(work + w.bad);
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(orw, 0, 8ull * 4 * c.layers, s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(bad, 0xFF, 4, s)) != cudaSuccess) return e;
+  int32_t* K = reinterpret_cast<int32_t*>(st + lay.k);
+  int32_t* V = reinterpret_cast<int32_t*>(st + lay.v);
+  const size_t layer_words = (size_t)lay.cache * m.kv_dim;
+  const size_t gemm_smem = (size_t)kStages * kStageBytesB;
+
+  auto planes = [&](const int64_t* vec, uint32_t ld, uint32_t cols, uint32_t KG,
+                    const unsigned long long* ow) {
+    const uint64_t work_items = 8ull * Npad * KG * 16;
+    const uint32_t blocks = (uint32_t)std::min<uint64_t>((work_items + kRowThreads - 1) / kRowThreads, 4096);
+    k_bplanes<<<blocks, kRowThreads, 0, s>>>(st, vec, ld, P, cols, Npad, KG, ow, B);
+  };
+  auto gemm = [&](const uint8_t* Wm, uint32_t rows, uint32_t KG, const unsigned long long* ow) {
+    const dim3 grid((rows + kBM - 1) / kBM, 8 * Npad / kBN);
+    k_bgemm<<<grid, kGemmThreads, gemm_smem, s>>>(st, Wm, rows, KG, B, Npad, ow, S);
+  };
+  auto epi = [&](BEpiParams p) {
+    p.st = st;
+    p.S = S;
+    p.Npad = Npad;
+    p.P = P;
+    p.pos0 = pos0;
+    const uint64_t items = (uint64_t)P * (p.rows / 2);
+    const uint32_t blocks = (uint32_t)std::min<uint64_t>((items + kRowThreads - 1) / kRowThreads, 8192);
+    k_bepi<<<blocks, kRowThreads, 0, s>>>(p);
+  };
+
+  k_bembed<<<P, kRowThreads, 0, s>>>(st, lay.prompt, pos0, X, c.dim, m.embed, m.embed_scale, c.vocab, bad);
+  for (uint32_t l = 0; l < c.layers; ++l) {
+    const DevLayer& Wl = m.layers[l];
+    unsigned long long* o4 = orw + 4 * l;
+    // phases 4-8: attention norm, Q/K/V rows, checked cache stores, rotary
+    k_bnorm<<<P, kRowThreads, 0, s>>>(st, X, XB, Wl.attn_norm, c.dim, o4 + 0);
+    planes(XB, c.dim, c.dim, KGd, o4 + 0);
+    gemm(Wl.wqkv, c.dim + 2 * m.kv_dim, KGd, o4 + 0);
+    BEpiParams pq = {};
+    pq.rows = c.dim + 2 * m.kv_dim;
+    pq.orw = o4 + 0;
+    pq.scale = Wl.sqkv;
+    pq.mode = kBEpiQKV;
+    pq.Q = Q;
+    pq.kc = K + l * layer_words;
+    pq.vc = V + l * layer_words;
+    pq.rope = m.rope;
+    pq.dim = c.dim;
+    pq.kv_dim = m.kv_dim;
+    pq.head_dim = m.head_dim;
+    pq.layer = l;
+    epi(pq);
+    // phase 9
+    BAttnParams pa = {};
+    pa.st = st;
+    pa.Q = Q;
+    pa.O = O;
+    pa.kc = K + l * layer_words;
+    pa.vc = V + l * layer_words;
+    pa.exp_tab = m.exp_tab;
+    pa.pos0 = pos0;
+    pa.dim = c.dim;
+    pa.heads = c.heads;
+    pa.kv_heads = c.kv_heads;
+    pa.head_dim = m.head_dim;
+    pa.kv_dim = m.kv_dim;
+    pa.inv_sqrt = m.inv_sqrt;
+    pa.or_out = o4 + 1;
+    k_battn<<<dim3(c.heads, P), kRowThreads, battn_smem(m.head_dim, pos0 + P), s>>>(pa);
+    // phases 10-11: output rows and the residual
+    planes(O, c.dim, c.dim, KGd, o4 + 1);
+    gemm(Wl.wo, c.dim, KGd, o4 + 1);
+    BEpiParams po = {};
+    po.rows = c.dim;
+    po.orw = o4 + 1;
+    po.scale = Wl.so;
+    po.mode = kBEpiResid;
+    po.X = X;
+    epi(po);
+    // phases 12-14: feed-forward norm, gate and up rows, SiLU gating
+    k_bnorm<<<P, kRowThreads, 0, s>>>(st, X, XB, Wl.ffn_norm, c.dim, o4 + 2);
+    planes(XB, c.dim, c.dim, KGd, o4 + 2);
+    gemm(Wl.w13, 2 * c.hidden, KGd, o4 + 2);
+    BEpiParams pg = {};
+    pg.rows = 2 * c.hidden;
+    pg.orw = o4 + 2;
+    pg.scale = Wl.s13;
+    pg.mode = kBEpiSiLU;
+    pg.H = H;
+    pg.hidden = c.hidden;
+    pg.silu_tab = m.silu_tab;
+    pg.or_out = o4 + 3;
+    epi(pg);
+    // phases 15-16: down rows and the residual
+    planes(H, c.hidden, c.hidden, KGh, o4 + 3);
+    gemm(Wl.w2, c.dim, KGh, o4 + 3);
+    BEpiParams pd = {};
+    pd.rows = c.dim;
+    pd.orw = o4 + 3;
+    pd.scale = Wl.s2;
+    pd.mode = kBEpiResid;
+    pd.X = X;
+    epi(pd);
+  }
+  k_bfinish<<<1, kRowThreads, 0, s>>>(st, X, reinterpret_cast<int64_t*>(st + lay.x), c.dim, pos0, P, bad);
+  return cudaGetLastError();
+}
+
+}  // namespace ck

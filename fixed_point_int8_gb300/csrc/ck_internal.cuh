@@ -413,6 +413,26 @@ __device__ SampleOut block_sample(const long long* logits, uint32_t vocab, long 
   return out;
 }
 
+// ------------------------------------------------------------------ layer-major prefill
+struct PrefillModel {
+  ck_config cfg;
+  uint32_t head_dim, kv_dim, inv_sqrt, pitch_d, pitch_h;
+  const uint8_t* embed;
+  const uint32_t* embed_scale;
+  const DevLayer* layers;  // host array of the layer table
+  const int32_t* rope;
+  const uint32_t* exp_tab;
+  const int32_t* silu_tab;
+};
+// Device scratch a chunk of up to `cap` positions needs.
+size_t prefill_work_bytes(const PrefillModel& m, uint32_t cap);
+// Whether the batched kernels handle this model and cache length.
+bool prefill_supported(const PrefillModel& m, uint32_t cache, size_t smem_optin);
+cudaError_t configure_prefill(size_t smem_optin);
+// Prompt positions pos0 .. pos0+P-1 (none generating) of the state, layer by layer.
+cudaError_t enqueue_prefill(const PrefillModel& m, uint8_t* st, const StateLayout& lay, uint32_t pos0,
+                            uint32_t P, uint8_t* work, uint32_t cap, cudaStream_t s);
+
 cudaError_t configure_step(size_t optin, size_t* dynamic_max);
 cudaError_t launch_step(const StepParams& p, cudaStream_t s, int grid, size_t smem);
 int step_threads();

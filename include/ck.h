@@ -127,7 +127,20 @@ int ck_set_attention_split(ck_model* m, uint32_t positions);
  * streaming while the blocks synchronise.  A tuning control: the results are the same
  * bits.  Drops the model's cached graphs.  Errors: 10 for a null handle or above 4096. */
 int ck_set_step_prefetch(ck_model* m, uint32_t kb_per_block);
-/* Frees the host handle and its cached CUDA graphs (not dev_mem). */
+
+/* Layer-major prefill ("The forward pass, in order", phases 3 to 16 of prompt positions
+ * that generate no token): when a turn reaches two or more such positions, ck_turn runs up
+ * to `positions` of them (default 256) through each layer together, so every matrix is read
+ * once per chunk and the matrix rows of the chunk are one tensor-core contraction over the
+ * byte planes of the activations (exact: f16 products of 8-bit integers summed in f32 below
+ * 2^24, then in 32-bit and 64-bit integers).  The state, cache and errors are the same bits
+ * as position by position; a cache store that does not fit fails the state at the first
+ * failing position.  The chunk's device scratch (about positions x 40 x dim bytes plus
+ * 16 x positions x the widest matrix's rows) is allocated by the first such turn and kept
+ * until ck_free_model or the next call.  0 or 1 turns it off.  Errors: 10 for a null
+ * handle or above 4096. */
+int ck_set_prefill(ck_model* m, uint32_t positions);
+/* Frees the host handle, its cached CUDA graphs and its prefill scratch (not dev_mem). */
 void ck_free_model(ck_model* m);
 
 /* ---------------------------------------------------------------- state ("CKSTATE1")
@@ -188,7 +201,8 @@ typedef struct ck_turn_result {
  * 19 where a token is generated, "The forward pass, in order").  A turn is the unit of
  * host synchronisation: the call reads the state header before and after (it
  * synchronizes `stream`), and all positions in between run as CUDA-graph replays with the
- * current token kept on the device.  Errors: 3 (state does not belong to the model, is
+ * current token kept on the device, prompt positions in layer-major chunks (see
+ * ck_set_prefill).  Errors: 3 (state does not belong to the model, is
  * complete or failed, or is misaligned), 8 (a key or value did not fit 32 bits: the state
  * is marked failed, err_* name the first failing store), 9, 10. */
 int ck_turn(ck_model* m, void* dev_state, size_t len, uint32_t n_positions, void* stream,

@@ -484,6 +484,117 @@ def test_1b_sixty_four_runs_sampled(ck):
         assert oracle.header(host)["generated"] == 1
 
 
+# ---------------------------------------------------------------- layer-major prefill
+
+MEDIUM = synth.ModelSpec("medium_gqa", 640, 1728, 2, 10, 5, 1000, 600, scale_rule="well", tied=False,
+                         seed=0x5EED0041)
+
+
+@pytest.mark.parametrize("chunk", [256, 7, 2])
+def test_prefill_matches_the_oracle(ck, chunk):
+    """Layer-major prefill of 299 prompt positions in chunks (the last one ragged) on a model
+    whose matrices span several row tiles, more than four column groups (the f32 sums move
+    to integers mid-row) and a padded last group; then the generating positions.  The whole
+    state against the oracle run position by position."""
+    P = Pair(ck, MEDIUM, "step")
+    assert P.gpu.set_prefill(chunk) == 0
+    n_prompt, steps = 300, 4
+    ids = synth.prompt_ids(MEDIUM, n_prompt)
+    so, sg = P.init(ck, ids, steps)
+    rco, reso = P.orc.turn(so, n_prompt - 1)
+    rcg, resg = P.gpu.turn(sg, n_prompt - 1)
+    assert rco == rcg == 0 and reso == resg, (reso, resg)
+    compare_states(P.orc, so, ck.state_download(sg), n_prompt, steps, f"prefill chunk {chunk}")
+    rco, reso = P.orc.turn(so, 100)
+    rcg, resg = P.gpu.turn(sg, 100)
+    assert rco == rcg == 0 and reso == resg
+    compare_states(P.orc, so, ck.state_download(sg), n_prompt, steps, f"after prefill {chunk}")
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_prefill_small_models(ck, path):
+    """Every small model prefilled in one turn, at the default chunk and at chunks of 3,
+    then generated to the end, against the oracle."""
+    for name, wl in MODELS.items():
+        for chunk in (256, 3):
+            P = Pair(ck, wl.spec, path)
+            assert P.gpu.set_prefill(chunk) == 0
+            ids = synth.prompt_ids(wl.spec, wl.n_prompt)
+            so, sg = P.init(ck, ids, wl.steps, temperature_q16=3 << 15, seed=chunk)
+            for n in (wl.n_prompt - 1, 1000):
+                rco, reso = P.orc.turn(so, n)
+                rcg, resg = P.gpu.turn(sg, n)
+                assert rco == rcg == 0 and reso == resg, (name, chunk, reso, resg)
+                compare_states(P.orc, so, ck.state_download(sg), wl.n_prompt, wl.steps,
+                               f"{name} chunk {chunk} after {n}")
+
+
+@pytest.mark.parametrize("chunk", [256, 3])
+def test_prefill_failure_matches_the_oracle(ck, chunk):
+    """The literal tiny workload overflows a key store at position 1 (layer 1): the
+    layer-major prefill fails the state at the same position with the same key."""
+    wl = synth.WORKLOADS["tiny"]
+    P = Pair(ck, wl.spec, "step")
+    assert P.gpu.set_prefill(chunk) == 0
+    ids = synth.prompt_ids(wl.spec, wl.n_prompt)
+    so, sg = P.init(ck, ids, wl.steps)
+    rco, reso = P.orc.turn(so, 100)
+    rcg, resg = P.gpu.turn(sg, 100)
+    assert rco == rcg == 8 and reso == resg, (reso, resg)
+    assert resg["err_position"] == 1
+    ho, hg = oracle.header(so), oracle.header(ck.state_download(sg))
+    for k in ("phase", "error", "err_key", "position", "generated"):
+        assert ho[k] == hg[k], k
+    assert P.gpu.turn(sg, 1)[0] == 3
+    assert P.gpu.set_prefill(4097) == 10
+
+
+def _prefill_sampled(ck, spec, n_prompt, samples, chunk=256):
+    """The GPU prefills n_prompt - 1 positions layer-major; for each sampled position p the
+    oracle recomputes p alone from the GPU's cache below p (the words of p cleared first),
+    and the key and value words of p in every layer must be identical, as must the last
+    prefilled position's residual."""
+    P = Pair(ck, spec, "step")
+    assert P.gpu.set_prefill(chunk) == 0
+    ids = synth.prompt_ids(spec, n_prompt)
+    sg = P.gpu.new_state(n_prompt, 2)
+    assert P.gpu.init_state(sg, ids, 2) == 0
+    rc, res = P.gpu.turn(sg, n_prompt - 1)
+    assert rc == 0 and res["work"] == n_prompt - 1
+    got = ck.state_download(sg)
+    lay = P.orc.layout(n_prompt, 2)
+    cache, kvd = n_prompt + 1, spec.kv_dim
+    for p in samples:
+        host = got.copy()
+        host[oracle.H_POSITION:oracle.H_POSITION + 4] = np.array([p], "<u4").view(np.uint8)
+        words = []
+        for name in ("k", "v"):
+            for l in range(spec.layers):
+                o = lay[name] + 4 * ((l * cache + p) * kvd)
+                host[o:o + 4 * kvd] = 0
+                words.append((name, l, o))
+        rco, reso = P.orc.turn(host, 1)
+        assert rco == 0 and reso["work"] == 1
+        for name, l, o in words:
+            a, b = host[o:o + 4 * kvd], got[o:o + 4 * kvd]
+            assert np.array_equal(a, b), (spec.name, p, name, l, np.flatnonzero(a != b)[:8])
+        if p == n_prompt - 2:
+            d = spec.dim
+            assert np.array_equal(host[lay["x"]:lay["x"] + 8 * d], got[lay["x"]:lay["x"] + 8 * d])
+
+
+def test_prefill_1b_shape_sampled_positions(ck):
+    """1B-shaped model at full size: 299 prompt positions layer-major (chunks of 256 and 43),
+    sampled positions from both chunks recomputed by the oracle."""
+    _prefill_sampled(ck, synth.ONE_B, 300, [0, 131, 255, 256, 298])
+
+
+def test_prefill_llama7b_shape_sampled_positions(ck):
+    """7B-shaped model at full size: 69 prompt positions in one ragged chunk, the first and
+    last recomputed by the oracle."""
+    _prefill_sampled(ck, synth.LLAMA7B, 70, [0, 68])
+
+
 def test_paths_agree_and_unknown_path_is_rejected(ck):
     wl = MODELS["gqa"]
     P = Pair(ck, wl.spec, "step")
