@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
             "ck_state_size": ([vp, u32, u32, ctypes.POINTER(sz)], ctypes.c_int),
             "ck_init_state": ([vp, vp, sz, vp, u32, u32, u32, u64, u32, vp], ctypes.c_int),
             "ck_turn": ([vp, vp, sz, u32, vp, ctypes.POINTER(TurnResult)], ctypes.c_int),
+            "ck_turn_batch": ([vp, vp, vp, u32, vp, vp, vp], ctypes.c_int),
             "ck_turn_noalloc": ([vp, vp, sz, vp, ctypes.POINTER(TurnResult)], ctypes.c_int),
             "ck_logits": ([vp, vp, sz, vp, vp], ctypes.c_int),
             "ck_argmax": ([vp, vp, sz, ctypes.POINTER(u32), vp], ctypes.c_int),
@@ -188,6 +189,18 @@ class Model:
         n = state.numel() if length is None else length
         rc = lib().ck_turn(self._h, _ptr(state), n, n_positions, _stream(stream), ctypes.byref(res))
         return rc, res.as_dict()
+
+    def turn_batch(self, states, lengths=None, stream=None):
+        """One position of each state in one batched pass (ck_turn_batch).
+        Returns (rc, [result dict per state], [rc per state])."""
+        n = len(states)
+        ptrs = (ctypes.c_void_p * max(n, 1))(*[_ptr(t) for t in states])
+        lens = (ctypes.c_size_t * max(n, 1))(*[(t.numel() if lengths is None else lengths[i])
+                                             for i, t in enumerate(states)])
+        res = (TurnResult * max(n, 1))()
+        rcs = (ctypes.c_int * max(n, 1))()
+        rc = lib().ck_turn_batch(self._h, ptrs, lens, n, _stream(stream), res, rcs)
+        return rc, [res[i].as_dict() for i in range(n)], [int(rcs[i]) for i in range(n)]
 
     def turn_noalloc(self, state, stream=None):
         """One position through ck_turn_noalloc (no device allocation, shared scratch)."""

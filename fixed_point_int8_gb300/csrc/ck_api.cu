@@ -1,6 +1,7 @@
 // libck host API: artifact loading into HBM, state set-up and the phase sequencer that
 // replays one position's kernels as a CUDA graph ("The inference core": "The forward pass,
 // in order", "The resumable state", "The Rust API", "Core errors").
+#include <algorithm>
 #include <climits>
 #include <cstdlib>
 #include <cstring>
@@ -37,8 +38,9 @@ struct ck_model {
   size_t step_smem;      // dynamic shared memory available to the one-position kernel
   std::vector<DevLayer> layers;
   uint32_t pf_cap;       // prompt positions per layer-major chunk (0: position by position)
-  uint8_t* pf_work;      // the chunk's device scratch, allocated at first use
+  uint8_t* pf_work;      // device scratch of the batched kernels, allocated at first use
   size_t pf_bytes;
+  uint32_t pf_wcap;      // rows the scratch is laid out for
   bool pf_configured;
   cudaStream_t capture;
   struct Graph {
@@ -677,7 +679,29 @@ PrefillModel prefill_model(const ck_model* m) {
   pm.rope = m->rope;
   pm.exp_tab = m->exp_tab;
   pm.silu_tab = m->silu_tab;
+  pm.cls = m->cls;
+  pm.cls_scale = m->cls_scale;
+  pm.final_norm = m->final_norm;
   return pm;
+}
+
+// The batched kernels' scratch, laid out for at least `rows` rows.
+int ensure_batch_work(ck_model* m, uint32_t rows) {
+  if (!m->pf_configured) {
+    CK_CUDA(configure_prefill((size_t)m->smem_optin));
+    m->pf_configured = true;
+  }
+  if (m->pf_work && m->pf_wcap >= rows) return CK_OK;
+  const uint32_t cap = std::max(rows, m->pf_wcap);
+  const size_t need = prefill_work_bytes(prefill_model(m), cap);
+  if (m->pf_work) CK_CUDA(cudaFree(m->pf_work));
+  m->pf_work = nullptr;
+  m->pf_bytes = 0;
+  m->pf_wcap = 0;
+  CK_CUDA(cudaMalloc(&m->pf_work, need));
+  m->pf_bytes = need;
+  m->pf_wcap = cap;
+  return CK_OK;
 }
 
 // Positions pos .. pos+P-1 layer by layer.  CK_INVALID_ARGUMENT: the batched kernels do not
@@ -686,19 +710,9 @@ int prefill_chunk(ck_model* m, uint8_t* st, const StateLayout& lay, uint32_t pos
                   cudaStream_t s) {
   const PrefillModel pm = prefill_model(m);
   if (!prefill_supported(pm, lay.cache, (size_t)m->smem_optin)) return CK_INVALID_ARGUMENT;
-  if (!m->pf_configured) {
-    CK_CUDA(configure_prefill((size_t)m->smem_optin));
-    m->pf_configured = true;
-  }
-  const size_t need = prefill_work_bytes(pm, m->pf_cap);
-  if (m->pf_bytes < need) {
-    if (m->pf_work) CK_CUDA(cudaFree(m->pf_work));
-    m->pf_work = nullptr;
-    m->pf_bytes = 0;
-    CK_CUDA(cudaMalloc(&m->pf_work, need));
-    m->pf_bytes = need;
-  }
-  CK_CUDA(enqueue_prefill(pm, st, lay, pos, P, m->pf_work, m->pf_cap, s));
+  const int rc = ensure_batch_work(m, m->pf_cap);
+  if (rc) return rc;
+  CK_CUDA(enqueue_prefill(pm, st, lay, pos, P, m->pf_work, m->pf_wcap, s));
   return CK_OK;
 }
 
@@ -835,6 +849,7 @@ int ck_load_model(const void* artifact, size_t len, void* dev_mem, size_t dev_le
   m->pf_cap = kDefaultPrefillChunk;
   m->pf_work = nullptr;
   m->pf_bytes = 0;
+  m->pf_wcap = 0;
   m->pf_configured = false;
   if (cudaMemcpyAsync(m->dev_layers, m->layers.data(), sizeof(DevLayer) * c.layers,
                       cudaMemcpyHostToDevice, s) != cudaSuccess ||
@@ -901,6 +916,7 @@ int ck_set_prefill(ck_model* m, uint32_t positions) {
   if (m->pf_work) cudaFree(m->pf_work);  // resized at next use
   m->pf_work = nullptr;
   m->pf_bytes = 0;
+  m->pf_wcap = 0;
   return CK_OK;
 }
 
@@ -1013,6 +1029,107 @@ int ck_turn(ck_model* m, void* dev_state, size_t len, uint32_t n_positions, void
     out->err_element = (uint32_t)key & 0xFFFFFFu;
   }
   return failed ? (int)h1.u32(kHError) : CK_OK;
+}
+
+int ck_turn_batch(ck_model* m, void* const* dev_states, const size_t* lens, uint32_t n_states,
+                  void* stream, ck_turn_result* out, int* rcs) {
+  if (!m || !dev_states || !lens || !out || !rcs || n_states == 0 || n_states > kMaxPrefillChunk)
+    return CK_INVALID_ARGUMENT;
+  for (uint32_t i = 0; i < n_states; ++i)
+    if (!dev_states[i]) return CK_INVALID_ARGUMENT;
+  {
+    std::vector<void*> sorted(dev_states, dev_states + n_states);
+    std::sort(sorted.begin(), sorted.end());
+    if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end()) return CK_INVALID_ARGUMENT;
+  }
+  for (uint32_t i = 0; i < n_states; ++i) {
+    memset(&out[i], 0, sizeof(out[i]));
+    out[i].token = 0xFFFFFFFFu;
+    rcs[i] = CK_OK;
+  }
+  cudaStream_t s = S(stream);
+  const PrefillModel pm = prefill_model(m);
+  int rc = ensure_batch_work(m, n_states);
+  if (rc) return rc;
+  // the states that can take a position: aligned, this model's, running, with a position left
+  std::vector<uint32_t> idx;
+  std::vector<uint8_t*> ptrs;
+  for (uint32_t i = 0; i < n_states; ++i) {
+    if (reinterpret_cast<uintptr_t>(dev_states[i]) % 256) {
+      rcs[i] = CK_INVALID_STATE;
+      continue;
+    }
+    idx.push_back(i);
+    ptrs.push_back(static_cast<uint8_t*>(dev_states[i]));
+  }
+  std::vector<uint8_t> h0(kHeaderBytes * idx.size() + 1), h1(h0.size());
+  if (!idx.empty())
+    CK_CUDA(batch_gather_headers(pm, ptrs.data(), (uint32_t)idx.size(), m->pf_work, m->pf_wcap, h0.data(), s));
+  std::vector<RowDesc> rows;
+  std::vector<uint32_t> row_of;  // index into dev_states of each row
+  uint32_t max_positions = 1;
+  for (size_t j = 0; j < idx.size(); ++j) {
+    const uint32_t i = idx[j];
+    HostHeader h;
+    memcpy(h.b, h0.data() + kHeaderBytes * j, kHeaderBytes);
+    StateLayout lay;
+    if (check_state(m, dev_states[i], lens[i], h, &lay) != CK_OK || h.u32(kHPhase) != CK_PHASE_RUNNING ||
+        h.u32(kHPosition) >= lay.cache) {
+      rcs[i] = CK_INVALID_STATE;
+      continue;
+    }
+    if (!prefill_supported(pm, lay.cache, (size_t)m->smem_optin)) return CK_INVALID_ARGUMENT;
+    RowDesc r = {};
+    r.st = static_cast<uint8_t*>(dev_states[i]);
+    r.pos = h.u32(kHPosition);
+    r.cache = lay.cache;
+    r.np = h.u32(kHNPrompt);
+    r.generating = r.pos + 1 >= r.np ? 1u : 0u;
+    r.off_prompt = lay.prompt;
+    r.off_out = lay.out;
+    r.off_x = lay.x;
+    r.off_logits = lay.logits;
+    r.off_k = lay.k;
+    r.off_v = lay.v;
+    rows.push_back(r);
+    row_of.push_back(i);
+    max_positions = std::max(max_positions, r.pos + 1);
+    out[i].generated = h.u32(kHGenerated);  // before; replaced below
+  }
+  if (!rows.empty()) {
+    CK_CUDA(enqueue_batch(pm, rows.data(), (uint32_t)rows.size(), max_positions, m->pf_work, m->pf_wcap, s));
+    std::vector<uint8_t*> rptrs;
+    for (const RowDesc& r : rows) rptrs.push_back(r.st);
+    CK_CUDA(batch_gather_headers(pm, rptrs.data(), (uint32_t)rows.size(), m->pf_work, m->pf_wcap, h1.data(), s));
+  }
+  int first = CK_OK;
+  for (size_t j = 0; j < rows.size(); ++j) {
+    const uint32_t i = row_of[j];
+    HostHeader h;
+    memcpy(h.b, h1.data() + kHeaderBytes * j, kHeaderBytes);
+    const bool failed = h.u32(kHPhase) == CK_PHASE_FAILED;
+    ck_turn_result& o = out[i];
+    const uint32_t gen0 = o.generated;
+    o.generated = h.u32(kHGenerated);
+    o.generated_this_turn = o.generated - gen0;
+    if (o.generated_this_turn) o.token = h.u32(kHLastTok);
+    o.work = h.u32(kHPosition) - rows[j].pos + (failed ? 1u : 0u);
+    o.complete = h.u32(kHPhase) != CK_PHASE_RUNNING;
+    const uint64_t key = h.u64(kHErrKey);
+    if (key != kNoError) {
+      o.err_position = (uint32_t)(key >> 44);
+      o.err_layer = (uint32_t)(key >> 32) & 0xFFFu;
+      o.err_phase = (uint32_t)(key >> 24) & 0xFFu;
+      o.err_element = (uint32_t)key & 0xFFFFFFu;
+    }
+    rcs[i] = failed ? (int)h.u32(kHError) : CK_OK;
+  }
+  for (uint32_t i = 0; i < n_states; ++i)
+    if (rcs[i] != CK_OK) {
+      first = rcs[i];
+      break;
+    }
+  return first;
 }
 
 int ck_turn_noalloc(ck_model* m, void* dev_state, size_t len, void* stream, ck_turn_result* out) {

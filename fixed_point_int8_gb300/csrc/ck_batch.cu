@@ -41,10 +41,17 @@ constexpr uint32_t kStageBytesB = kATile + kBTile;
 constexpr uint32_t kFlushGroups = 4;         // column groups between f32 -> i32 moves
 constexpr int kRowThreads = 256;
 
-enum BEpi : int { kBEpiQKV = 0, kBEpiResid = 1, kBEpiSiLU = 2 };
+enum BEpi : int { kBEpiQKV = 0, kBEpiResid = 1, kBEpiSiLU = 2, kBEpiLogits = 3 };
 
-__device__ __forceinline__ bool running(const uint8_t* st) {
-  return hdr_ld<uint32_t>(st, kHPhase) == CK_PHASE_RUNNING;
+// A chunk of one run is gated by that run's state: a position earlier in the same turn
+// that failed it stops the chunk.  A batch of runs has no gate (nullptr).
+__device__ __forceinline__ bool running(const uint8_t* gate) {
+  return gate == nullptr || hdr_ld<uint32_t>(gate, kHPhase) == CK_PHASE_RUNNING;
+}
+
+__device__ __forceinline__ int32_t* layer_cache(const RowDesc& r, uint64_t off, uint32_t layer,
+                                                uint32_t kv_dim) {
+  return reinterpret_cast<int32_t*>(r.st + off) + (size_t)layer * r.cache * kv_dim;
 }
 
 // Limbs of a vector from the OR of x ^ (x >> 63) over it: the smallest L with every x in
@@ -91,17 +98,20 @@ __device__ void block_or_to(unsigned long long v, unsigned long long* dst, unsig
 
 // ------------------------------------------------------------------ phase 3 and norms
 
-// Phase 3 for positions pos0 .. pos0+P-1 (one block each): x = ((byte - 128) * scale) >> 8.
-__global__ void __launch_bounds__(kRowThreads) k_bembed(const uint8_t* st, uint64_t off_prompt,
-                                                         uint32_t pos0, int64_t* X, uint32_t d,
-                                                         const uint8_t* E, const uint32_t* Es,
-                                                         uint32_t vocab, uint32_t* badpos) {
-  if (!running(st)) return;
+// Phase 3 for every row (one block each): the row's token is its run's prompt id at the
+// position, or the token generated there; x = ((byte - 128) * scale) >> 8.
+__global__ void __launch_bounds__(kRowThreads) k_bembed(const uint8_t* gate, const RowDesc* rows,
+                                                         int64_t* X, uint32_t d, const uint8_t* E,
+                                                         const uint32_t* Es, uint32_t vocab,
+                                                         int32_t* rstat) {
+  if (!running(gate)) return;
   const uint32_t n = blockIdx.x;
-  const uint32_t tok = reinterpret_cast<const uint32_t*>(st + off_prompt)[pos0 + n];
+  const RowDesc r = rows[n];
+  const uint32_t tok = r.pos < r.np ? reinterpret_cast<const uint32_t*>(r.st + r.off_prompt)[r.pos]
+                                    : reinterpret_cast<const uint32_t*>(r.st + r.off_out)[r.pos - r.np];
   int64_t* x = X + (size_t)n * d;
   if (tok >= vocab) {  // a state edited outside the library: that position fails
-    if (threadIdx.x == 0) atomicMin(badpos, pos0 + n);
+    if (threadIdx.x == 0) rstat[n] = CK_INVALID_STATE;
     for (uint32_t i = threadIdx.x; i < d; i += blockDim.x) x[i] = 0;
     return;
   }
@@ -113,12 +123,12 @@ __global__ void __launch_bounds__(kRowThreads) k_bembed(const uint8_t* st, uint6
 // "RMS normalization" of each position's row (one block each): rms = max(isqrt(sum x^2 / d
 // + 42,950), 1), y = ((x * w) / rms) >> 8 with the division truncating; ORs the outputs'
 // magnitudes into *orw for the plane count.
-__global__ void __launch_bounds__(kRowThreads) k_bnorm(const uint8_t* st, const int64_t* X,
+__global__ void __launch_bounds__(kRowThreads) k_bnorm(const uint8_t* gate, const int64_t* X,
                                                         int64_t* XB, const int32_t* w, uint32_t d,
                                                         unsigned long long* orw) {
   __shared__ unsigned long long red[kRowThreads / 32];
   __shared__ InvDiv div;
-  if (!running(st)) return;
+  if (!running(gate)) return;
   const int64_t* x = X + (size_t)blockIdx.x * d;
   int64_t* y = XB + (size_t)blockIdx.x * d;
   unsigned long long ss = 0;
@@ -154,11 +164,11 @@ __device__ __forceinline__ uint64_t plane_offset(uint32_t np, uint32_t KG, uint3
 
 // Writes planes 0 .. L-1 of the P vectors V (row stride ld, cols used), zero beyond P and
 // cols.  One thread per 8 columns of one plane of one position.
-__global__ void __launch_bounds__(kRowThreads) k_bplanes(const uint8_t* st, const int64_t* V,
+__global__ void __launch_bounds__(kRowThreads) k_bplanes(const uint8_t* gate, const int64_t* V,
                                                           uint32_t ld, uint32_t P, uint32_t cols,
                                                           uint32_t Npad, uint32_t KG,
                                                           const unsigned long long* orw, uint8_t* B) {
-  if (!running(st)) return;
+  if (!running(gate)) return;
   const int L = limbs_of_or(*orw);
   const uint32_t per_row = KG * 16;  // 8-column chunks of a row
   const uint64_t total = (uint64_t)L * Npad * per_row;
@@ -224,12 +234,12 @@ __device__ __forceinline__ void mma_f16(float* c, const uint32_t* a, const uint3
 // columns 4t .. 4t+3 of the step as the MMA's k = 2t, 2t+1, 2t+8, 2t+9, for the weights and
 // the planes alike, so each operand is one 32- or 64-bit shared load; the order of the
 // columns inside a sum does not matter.
-__global__ void __launch_bounds__(kGemmThreads, 2) k_bgemm(const uint8_t* st, const uint8_t* W,
+__global__ void __launch_bounds__(kGemmThreads, 2) k_bgemm(const uint8_t* gate, const uint8_t* W,
                                                            uint32_t rows, uint32_t KG,
                                                            const uint8_t* B, uint32_t Npad,
                                                            const unsigned long long* orw, int32_t* S) {
   extern __shared__ __align__(128) uint8_t smem[];
-  if (!running(st)) return;
+  if (!running(gate)) return;
   const int L = limbs_of_or(*orw);
   const uint32_t nt = blockIdx.y;
   if (nt >= (uint32_t)L * (Npad / kBN)) return;
@@ -334,16 +344,15 @@ __global__ void __launch_bounds__(kGemmThreads, 2) k_bgemm(const uint8_t* st, co
 // ------------------------------------------------------------------ epilogues
 
 struct BEpiParams {
-  const uint8_t* st;
+  const uint8_t* gate;
+  const RowDesc* rdesc;
   const int32_t* S;
-  uint32_t rows, Npad, P, pos0;
+  uint32_t rows, Npad, P;
   const unsigned long long* orw;  // the input vector's OR word (its plane count)
   const uint32_t* scale;
   int mode;
-  // QKV
+  // QKV (each row's keys and values go to its run's cache, at its position)
   int64_t* Q;                     // [P][dim] rotated queries
-  int32_t* kc;                    // this layer's keys and values, position 0
-  int32_t* vc;
   const int32_t* rope;
   uint32_t dim, kv_dim, head_dim, layer;
   // residual: X[n][r] += y;  SiLU: H[n][j] = (silu(y_2j) * y_2j+1) >> 16
@@ -363,16 +372,25 @@ __device__ __forceinline__ int64_t combine(const BEpiParams& p, int L, uint32_t 
 }
 
 // One thread per (position, row pair): rows 2i and 2i+1 are a rotary pair in Q and K and a
-// gate/up pair in the feed-forward matrix.
+// gate/up pair in the feed-forward matrix.  Logits (an odd count possible) are written to
+// the states of the rows that generate a token.
 __global__ void __launch_bounds__(kRowThreads) k_bepi(const BEpiParams p) {
   __shared__ unsigned long long red[kRowThreads / 32];
-  if (!running(p.st)) return;
+  if (!running(p.gate)) return;
   const int L = limbs_of_or(*p.orw);
-  const uint32_t pairs = p.rows / 2;
+  const uint32_t pairs = (p.rows + 1) / 2;
   unsigned long long o = 0;
   for (uint64_t idx = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < (uint64_t)p.P * pairs;
        idx += (uint64_t)gridDim.x * blockDim.x) {
     const uint32_t n = (uint32_t)(idx / pairs), r = 2 * (uint32_t)(idx % pairs);
+    if (p.mode == kBEpiLogits) {
+      const RowDesc rd = p.rdesc[n];
+      if (!rd.generating) continue;
+      int64_t* lg = reinterpret_cast<int64_t*>(rd.st + rd.off_logits);
+      lg[r] = combine(p, L, n, r);
+      if (r + 1 < p.rows) lg[r + 1] = combine(p, L, n, r + 1);
+      continue;
+    }
     const int64_t y0 = combine(p, L, n, r), y1 = combine(p, L, n, r + 1);
     if (p.mode == kBEpiResid) {
       int64_t* x = p.X + (size_t)n * p.rows + r;
@@ -383,7 +401,9 @@ __global__ void __launch_bounds__(kRowThreads) k_bepi(const BEpiParams p) {
       p.H[(size_t)n * p.hidden + (r >> 1)] = h;
       o |= (unsigned long long)(h ^ (h >> 63));
     } else {
-      const uint32_t pos = p.pos0 + n;
+      const RowDesc rd = p.rdesc[n];
+      const uint32_t pos = rd.pos;
+      uint8_t* st = rd.st;
       const int32_t* rope = p.rope + (size_t)pos * p.head_dim;  // [pos][head/2] pairs (cos, sin)
       if (r < p.dim) {
         const int32_t* cs = rope + ((r % p.head_dim) & ~1u);
@@ -393,21 +413,23 @@ __global__ void __launch_bounds__(kRowThreads) k_bepi(const BEpiParams p) {
         p.Q[(size_t)n * p.dim + r + 1] = b2;
       } else if (r < p.dim + p.kv_dim) {
         const uint32_t e = r - p.dim;
-        if (!fits_i32(y0)) record_error(const_cast<uint8_t*>(p.st), err_key(pos, p.layer, 6, e));
-        if (!fits_i32(y1)) record_error(const_cast<uint8_t*>(p.st), err_key(pos, p.layer, 6, e + 1));
+        if (!fits_i32(y0)) record_error(st, err_key(pos, p.layer, 6, e));
+        if (!fits_i32(y1)) record_error(st, err_key(pos, p.layer, 6, e + 1));
         const int32_t* cs = rope + ((e % p.head_dim) & ~1u);
         int64_t a2, b2;
         rotate_pair((int64_t)(int32_t)y0, (int64_t)(int32_t)y1, __ldg(cs), __ldg(cs + 1), a2, b2);
-        if (!fits_i32(a2)) record_error(const_cast<uint8_t*>(p.st), err_key(pos, p.layer, 8, e));
-        if (!fits_i32(b2)) record_error(const_cast<uint8_t*>(p.st), err_key(pos, p.layer, 8, e + 1));
-        p.kc[(size_t)pos * p.kv_dim + e] = (int32_t)a2;
-        p.kc[(size_t)pos * p.kv_dim + e + 1] = (int32_t)b2;
+        if (!fits_i32(a2)) record_error(st, err_key(pos, p.layer, 8, e));
+        if (!fits_i32(b2)) record_error(st, err_key(pos, p.layer, 8, e + 1));
+        int32_t* kc = layer_cache(rd, rd.off_k, p.layer, p.kv_dim) + (size_t)pos * p.kv_dim;
+        kc[e] = (int32_t)a2;
+        kc[e + 1] = (int32_t)b2;
       } else {
         const uint32_t e = r - p.dim - p.kv_dim;
-        if (!fits_i32(y0)) record_error(const_cast<uint8_t*>(p.st), err_key(pos, p.layer, 7, e));
-        if (!fits_i32(y1)) record_error(const_cast<uint8_t*>(p.st), err_key(pos, p.layer, 7, e + 1));
-        p.vc[(size_t)pos * p.kv_dim + e] = (int32_t)y0;
-        p.vc[(size_t)pos * p.kv_dim + e + 1] = (int32_t)y1;
+        if (!fits_i32(y0)) record_error(st, err_key(pos, p.layer, 7, e));
+        if (!fits_i32(y1)) record_error(st, err_key(pos, p.layer, 7, e + 1));
+        int32_t* vc = layer_cache(rd, rd.off_v, p.layer, p.kv_dim) + (size_t)pos * p.kv_dim;
+        vc[e] = (int32_t)y0;
+        vc[e + 1] = (int32_t)y1;
       }
     }
   }
@@ -417,13 +439,12 @@ __global__ void __launch_bounds__(kRowThreads) k_bepi(const BEpiParams p) {
 // ------------------------------------------------------------------ attention
 
 struct BAttnParams {
-  const uint8_t* st;
+  const uint8_t* gate;
+  const RowDesc* rdesc;
   const int64_t* Q;     // [P][dim]
   int64_t* O;           // [P][dim]
-  const int32_t* kc;    // this layer's cache, position 0
-  const int32_t* vc;
   const uint32_t* exp_tab;
-  uint32_t pos0, dim, heads, kv_heads, head_dim, kv_dim, inv_sqrt;
+  uint32_t layer, dim, heads, kv_heads, head_dim, kv_dim, inv_sqrt;
   unsigned long long* or_out;
 };
 
@@ -433,14 +454,15 @@ size_t battn_smem(uint32_t hd, uint32_t positions) {
   return 8 * ((size_t)hd * (1 + kAttnWarps) + kAttnWarps + positions);
 }
 
-// Phase 9 for query position pos0 + blockIdx.y and head blockIdx.x ("Attention, stage by
-// stage"), over the cache positions 0 .. pos: scores and their maximum, exponentials and
-// their sum, probabilities with 24 fraction bits, and the weighted values with one >> 24.
+// Phase 9 for row blockIdx.y and head blockIdx.x ("Attention, stage by stage"), over its
+// run's cache positions 0 .. pos: scores and their maximum, exponentials and their sum,
+// probabilities with 24 fraction bits, and the weighted values with one >> 24.
 __global__ void __launch_bounds__(kRowThreads) k_battn(const BAttnParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  if (!running(p.st)) return;
+  if (!running(p.gate)) return;
   const uint32_t hd = p.head_dim, h = blockIdx.x, n = blockIdx.y;
-  const uint32_t pos = p.pos0 + n, np = pos + 1;
+  const RowDesc rd = p.rdesc[n];
+  const uint32_t np = rd.pos + 1;
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int64_t* q_s = reinterpret_cast<int64_t*>(smem);
   unsigned long long* part = reinterpret_cast<unsigned long long*>(q_s + hd);  // [warps][hd]
@@ -449,8 +471,8 @@ __global__ void __launch_bounds__(kRowThreads) k_battn(const BAttnParams p) {
   const uint32_t kvh = h / (p.heads / p.kv_heads);
   for (uint32_t i = tid; i < hd; i += kRowThreads) q_s[i] = p.Q[(size_t)n * p.dim + (size_t)h * hd + i];
   __syncthreads();
-  const int32_t* Kh = p.kc + (size_t)kvh * hd;
-  const int32_t* Vh = p.vc + (size_t)kvh * hd;
+  const int32_t* Kh = layer_cache(rd, rd.off_k, p.layer, p.kv_dim) + (size_t)kvh * hd;
+  const int32_t* Vh = layer_cache(rd, rd.off_v, p.layer, p.kv_dim) + (size_t)kvh * hd;
   const uint32_t lpp = hd / 4, ppw = 32 / lpp;  // lanes per position (four elements each)
   const uint32_t sub = lane % lpp, slot = lane / lpp, e0 = sub * 4;
   const int64_t q0 = q_s[e0], q1 = q_s[e0 + 1], q2 = q_s[e0 + 2], q3 = q_s[e0 + 3];
@@ -539,19 +561,37 @@ __global__ void __launch_bounds__(kRowThreads) k_battn(const BAttnParams p) {
   block_or_to(orv, p.or_out, reinterpret_cast<unsigned long long*>(red));
 }
 
-// ------------------------------------------------------------------ end of the chunk
+// ------------------------------------------------------------------ end of a pass
 
-// The chunk's outcome: the first failing position (a cache store that did not fit, error 8,
+// Rows pos0 .. pos0+P-1 of one run.
+__global__ void k_rows_fill(RowDesc* rows, RowDesc tmpl, uint32_t pos0, uint32_t P) {
+  const uint32_t n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= P) return;
+  RowDesc r = tmpl;
+  r.pos = pos0 + n;
+  rows[n] = r;
+}
+
+// A chunk of one run: the first failing position (a cache store that did not fit, error 8,
 // or a prompt id outside the vocabulary, error 3) fails the state there; otherwise the last
 // position's residual becomes the state's x and the cursor moves past the chunk.
 __global__ void __launch_bounds__(kRowThreads) k_bfinish(uint8_t* st, const int64_t* X, int64_t* x,
                                                          uint32_t d, uint32_t pos0, uint32_t P,
-                                                         const uint32_t* badpos) {
+                                                         const int32_t* rstat) {
+  __shared__ uint32_t first_bad;
   if (!running(st)) return;
   const uint64_t key = hdr_ld<uint64_t>(st, kHErrKey);
   const uint32_t key_pos = key == kNoError ? 0xFFFFFFFFu : (uint32_t)(key >> 44);
-  const uint32_t bad = *badpos;
+  if (threadIdx.x == 0) {
+    first_bad = 0xFFFFFFFFu;
+    for (uint32_t n = 0; n < P; ++n)
+      if (rstat[n]) {
+        first_bad = pos0 + n;
+        break;
+      }
+  }
   __syncthreads();  // every thread has read the header before thread 0 writes it
+  const uint32_t bad = first_bad;
   if (bad != 0xFFFFFFFFu && bad <= key_pos) {
     if (threadIdx.x == 0) {
       hdr<uint64_t>(st, kHErrKey) = kNoError;  // that position stopped before any store
@@ -573,16 +613,123 @@ __global__ void __launch_bounds__(kRowThreads) k_bfinish(uint8_t* st, const int6
   if (threadIdx.x == 0) hdr<uint32_t>(st, kHPosition) = pos0 + P;
 }
 
+constexpr int kFinishThreads = 256;
+
+// A batch of runs, one block per row: the end of its position.  A failed store or a token
+// outside the vocabulary fails that run; otherwise the residual becomes its x, and where the
+// position generates, phase 19 ("Sampling": the maximum pass, and above temperature zero
+// the sum and draw passes) chooses the token.  Every run's turn counter advances.
+__global__ void __launch_bounds__(kFinishThreads) k_mfinish(const RowDesc* rows, const int64_t* X,
+                                                            uint32_t d, uint32_t vocab,
+                                                            const uint32_t* exp_tab,
+                                                            const int32_t* rstat) {
+  __shared__ unsigned long long gsum[kSampleGroups];
+  __shared__ long long wv[kFinishThreads / 32];
+  __shared__ uint32_t wi[kFinishThreads / 32];
+  __shared__ long long max_v;
+  __shared__ uint32_t max_i;
+  const uint32_t n = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const RowDesc rd = rows[n];
+  uint8_t* st = rd.st;
+  const uint64_t key = hdr_ld<uint64_t>(st, kHErrKey);
+  const int32_t bad = rstat[n];
+  __syncthreads();  // header read by all before thread 0 writes it
+  if (threadIdx.x == 0) hdr<uint64_t>(st, kHTurns) = hdr_ld<uint64_t>(st, kHTurns) + 1;
+  if (bad || key != kNoError) {
+    if (threadIdx.x == 0) {
+      if (bad) hdr<uint64_t>(st, kHErrKey) = kNoError;  // stopped before any store
+      hdr<uint32_t>(st, kHError) = bad ? (uint32_t)bad : CK_ARITHMETIC;
+      hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
+    }
+    return;
+  }
+  int64_t* x = reinterpret_cast<int64_t*>(st + rd.off_x);
+  for (uint32_t i = threadIdx.x; i < d; i += blockDim.x) x[i] = X[(size_t)n * d + i];
+  if (!rd.generating) {
+    if (threadIdx.x == 0) hdr<uint32_t>(st, kHPosition) = rd.pos + 1;
+    return;
+  }
+  // maximum pass: the first largest logit
+  const long long* lg = reinterpret_cast<const long long*>(st + rd.off_logits);
+  long long bv = LLONG_MIN;
+  uint32_t bi = 0xFFFFFFFFu;
+  for (uint32_t i = threadIdx.x; i < vocab; i += blockDim.x) {
+    const long long v = __ldcg(lg + i);
+    if (bi == 0xFFFFFFFFu || v > bv) {
+      bv = v;
+      bi = i;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const long long ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const uint32_t oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (oi != 0xFFFFFFFFu && (bi == 0xFFFFFFFFu || ov > bv || (ov == bv && oi < bi))) {
+      bv = ov;
+      bi = oi;
+    }
+  }
+  if (lane == 0) {
+    wv[warp] = bv;
+    wi[warp] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kFinishThreads / 32; ++w)
+      if (wi[w] != 0xFFFFFFFFu && (wv[w] > bv || (wv[w] == bv && wi[w] < bi))) {
+        bv = wv[w];
+        bi = wi[w];
+      }
+    max_v = bv;
+    max_i = bi;
+  }
+  __syncthreads();
+  bv = max_v;
+  bi = max_i;
+  const uint32_t temp = hdr_ld<uint32_t>(st, kHTemp);
+  unsigned long long gen_state = hdr_ld<unsigned long long>(st, kHSeed), z = 0, draw = 0;
+  if (temp != 0) {
+    const SampleOut so = block_sample(lg, vocab, bv, temp, exp_tab, gen_state, gsum,
+                                      kFinishThreads / 32, [] { __syncthreads(); });
+    bi = so.token;
+    gen_state = so.state;
+    z = so.sum;
+    draw = so.draw;
+  }
+  if (threadIdx.x == 0) {
+    const uint32_t gen = hdr_ld<uint32_t>(st, kHGenerated);
+    reinterpret_cast<uint32_t*>(st + rd.off_out)[gen] = bi;
+    hdr<uint32_t>(st, kHGenerated) = gen + 1;
+    hdr<uint32_t>(st, kHLastTok) = bi;
+    hdr<long long>(st, kHMaxLogit) = bv;
+    hdr<unsigned long long>(st, kHSeed) = gen_state;
+    hdr<unsigned long long>(st, kHExpSum) = z;
+    hdr<unsigned long long>(st, kHDraw) = draw;
+    const bool stop = (hdr_ld<uint32_t>(st, kHFlags) & CK_FLAG_STOP_TOKENS) && (bi == 1 || bi == 2);
+    if (gen + 1 == hdr_ld<uint32_t>(st, kHMaxTok) || stop) hdr<uint32_t>(st, kHPhase) = CK_PHASE_DONE;
+    hdr<uint32_t>(st, kHPosition) = rd.pos + 1;
+  }
+}
+
+__global__ void k_gather_headers(const uint8_t* const* states, uint32_t n, uint8_t* out) {
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n * (kHeaderBytes / 8);
+       i += gridDim.x * blockDim.x) {
+    const uint32_t s = i / (kHeaderBytes / 8), w = i % (kHeaderBytes / 8);
+    reinterpret_cast<uint64_t*>(out)[i] = reinterpret_cast<const uint64_t*>(states[s])[w];
+  }
+}
+
 uint32_t pad64(uint32_t n) { return (n + 63u) & ~63u; }
 
 struct WorkLayout {
-  uint64_t X, XB, Q, O, H, B, S, orw, bad, size;
+  uint64_t X, XB, Q, O, H, B, S, orw, rows, rstat, ptrs, hdrs, size;
 };
 
 WorkLayout work_layout(const PrefillModel& m, uint32_t cap) {
   const uint64_t Np = pad64(cap);
   const uint64_t kg_max = std::max(m.pitch_d, m.pitch_h) / kBK;
-  const uint64_t rows_max = std::max<uint64_t>((uint64_t)m.cfg.dim + 2ull * m.kv_dim, 2ull * m.cfg.hidden);
+  const uint64_t rows_max = std::max<uint64_t>({(uint64_t)m.cfg.dim + 2ull * m.kv_dim,
+                                                2ull * m.cfg.hidden, (uint64_t)m.cfg.vocab});
   WorkLayout w;
   uint64_t off = 0;
   auto take = [&](uint64_t bytes) { uint64_t o = off; off = align256(off + bytes); return o; };
@@ -593,10 +740,144 @@ WorkLayout work_layout(const PrefillModel& m, uint32_t cap) {
   w.H = take(8 * Np * m.cfg.hidden);
   w.B = take(8 * (Np / kBN) * kg_max * kBTile);     // up to 8 planes
   w.S = take(4 * 8 * Np * rows_max);
-  w.orw = take(8ull * 4 * m.cfg.layers);
-  w.bad = take(4);
+  w.orw = take(8ull * (4 * m.cfg.layers + 1));
+  w.rows = take(sizeof(RowDesc) * Np);
+  w.rstat = take(4 * Np);
+  w.ptrs = take(8 * Np);
+  w.hdrs = take((uint64_t)kHeaderBytes * Np);
   w.size = off;
   return w;
+}
+
+// The layers for P rows (phases 3 to 16), then, with `classify`, the final norm and the
+// classifier rows into the logits of the rows that generate.
+cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkLayout& w,
+                         uint8_t* work, uint32_t P, uint32_t max_positions, bool classify,
+                         cudaStream_t s) {
+  const ck_config& c = m.cfg;
+  const uint32_t Npad = pad64(P);
+  const uint32_t KGd = m.pitch_d / kBK, KGh = m.pitch_h / kBK;
+  int64_t* X = reinterpret_cast<int64_t*>(work + w.X);
+  int64_t* XB = reinterpret_cast<int64_t*>(work + w.XB);
+  int64_t* Q = reinterpret_cast<int64_t*>(work + w.Q);
+  int64_t* O = reinterpret_cast<int64_t*>(work + w.O);
+  int64_t* H = reinterpret_cast<int64_t*>(work + w.H);
+  uint8_t* B = work + w.B;
+  int32_t* S = reinterpret_cast<int32_t*>(work + w.S);
+  unsigned long long* orw = reinterpret_cast<unsigned long long*>(work + w.orw);
+  const RowDesc* rows = reinterpret_cast<const RowDesc*>(work + w.rows);
+  int32_t* rstat = reinterpret_cast<int32_t*>(work + w.rstat);
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(orw, 0, 8ull * (4 * c.layers + 1), s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(rstat, 0, 4ull * P, s)) != cudaSuccess) return e;
+  const size_t gemm_smem = (size_t)kStages * kStageBytesB;
+
+  auto planes = [&](const int64_t* vec, uint32_t ld, uint32_t cols, uint32_t KG,
+                    const unsigned long long* ow) {
+    const uint64_t work_items = 8ull * Npad * KG * 16;
+    const uint32_t blocks = (uint32_t)std::min<uint64_t>((work_items + kRowThreads - 1) / kRowThreads, 4096);
+    k_bplanes<<<blocks, kRowThreads, 0, s>>>(gate, vec, ld, P, cols, Npad, KG, ow, B);
+  };
+  auto gemm = [&](const uint8_t* Wm, uint32_t nrows, uint32_t KG, const unsigned long long* ow) {
+    const dim3 grid((nrows + kBM - 1) / kBM, 8 * Npad / kBN);
+    k_bgemm<<<grid, kGemmThreads, gemm_smem, s>>>(gate, Wm, nrows, KG, B, Npad, ow, S);
+  };
+  auto epi = [&](BEpiParams p) {
+    p.gate = gate;
+    p.rdesc = rows;
+    p.S = S;
+    p.Npad = Npad;
+    p.P = P;
+    const uint64_t items = (uint64_t)P * ((p.rows + 1) / 2);
+    const uint32_t blocks = (uint32_t)std::min<uint64_t>((items + kRowThreads - 1) / kRowThreads, 8192);
+    k_bepi<<<blocks, kRowThreads, 0, s>>>(p);
+  };
+
+  k_bembed<<<P, kRowThreads, 0, s>>>(gate, rows, X, c.dim, m.embed, m.embed_scale, c.vocab, rstat);
+  for (uint32_t l = 0; l < c.layers; ++l) {
+    const DevLayer& Wl = m.layers[l];
+    unsigned long long* o4 = orw + 4 * l;
+    // phases 4-8: attention norm, Q/K/V rows, checked cache stores, rotary
+    k_bnorm<<<P, kRowThreads, 0, s>>>(gate, X, XB, Wl.attn_norm, c.dim, o4 + 0);
+    planes(XB, c.dim, c.dim, KGd, o4 + 0);
+    gemm(Wl.wqkv, c.dim + 2 * m.kv_dim, KGd, o4 + 0);
+    BEpiParams pq = {};
+    pq.rows = c.dim + 2 * m.kv_dim;
+    pq.orw = o4 + 0;
+    pq.scale = Wl.sqkv;
+    pq.mode = kBEpiQKV;
+    pq.Q = Q;
+    pq.rope = m.rope;
+    pq.dim = c.dim;
+    pq.kv_dim = m.kv_dim;
+    pq.head_dim = m.head_dim;
+    pq.layer = l;
+    epi(pq);
+    // phase 9
+    BAttnParams pa = {};
+    pa.gate = gate;
+    pa.rdesc = rows;
+    pa.Q = Q;
+    pa.O = O;
+    pa.exp_tab = m.exp_tab;
+    pa.layer = l;
+    pa.dim = c.dim;
+    pa.heads = c.heads;
+    pa.kv_heads = c.kv_heads;
+    pa.head_dim = m.head_dim;
+    pa.kv_dim = m.kv_dim;
+    pa.inv_sqrt = m.inv_sqrt;
+    pa.or_out = o4 + 1;
+    k_battn<<<dim3(c.heads, P), kRowThreads, battn_smem(m.head_dim, max_positions), s>>>(pa);
+    // phases 10-11: output rows and the residual
+    planes(O, c.dim, c.dim, KGd, o4 + 1);
+    gemm(Wl.wo, c.dim, KGd, o4 + 1);
+    BEpiParams po = {};
+    po.rows = c.dim;
+    po.orw = o4 + 1;
+    po.scale = Wl.so;
+    po.mode = kBEpiResid;
+    po.X = X;
+    epi(po);
+    // phases 12-14: feed-forward norm, gate and up rows, SiLU gating
+    k_bnorm<<<P, kRowThreads, 0, s>>>(gate, X, XB, Wl.ffn_norm, c.dim, o4 + 2);
+    planes(XB, c.dim, c.dim, KGd, o4 + 2);
+    gemm(Wl.w13, 2 * c.hidden, KGd, o4 + 2);
+    BEpiParams pg = {};
+    pg.rows = 2 * c.hidden;
+    pg.orw = o4 + 2;
+    pg.scale = Wl.s13;
+    pg.mode = kBEpiSiLU;
+    pg.H = H;
+    pg.hidden = c.hidden;
+    pg.silu_tab = m.silu_tab;
+    pg.or_out = o4 + 3;
+    epi(pg);
+    // phases 15-16: down rows and the residual
+    planes(H, c.hidden, c.hidden, KGh, o4 + 3);
+    gemm(Wl.w2, c.dim, KGh, o4 + 3);
+    BEpiParams pd = {};
+    pd.rows = c.dim;
+    pd.orw = o4 + 3;
+    pd.scale = Wl.s2;
+    pd.mode = kBEpiResid;
+    pd.X = X;
+    epi(pd);
+  }
+  if (classify) {
+    // phases 17-18: final norm and classifier rows (written only for generating rows)
+    unsigned long long* of = orw + 4 * c.layers;
+    k_bnorm<<<P, kRowThreads, 0, s>>>(gate, X, XB, m.final_norm, c.dim, of);
+    planes(XB, c.dim, c.dim, KGd, of);
+    gemm(m.cls, c.vocab, KGd, of);
+    BEpiParams pc = {};
+    pc.rows = c.vocab;
+    pc.orw = of;
+    pc.scale = m.cls_scale;
+    pc.mode = kBEpiLogits;
+    epi(pc);
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -623,123 +904,54 @@ cudaError_t configure_prefill(size_t smem_optin) {
 cudaError_t enqueue_prefill(const PrefillModel& m, uint8_t* st, const StateLayout& lay, uint32_t pos0,
                             uint32_t P, uint8_t* work, uint32_t cap, cudaStream_t s) {
   if (P == 0 || P > cap) return cudaErrorInvalidValue;
-  const ck_config& c = m.cfg;
   const WorkLayout w = work_layout(m, cap);
-  const uint32_t Npad = pad64(P);
-  const uint32_t KGd = m.pitch_d / kBK, KGh = m.pitch_h / kBK;
-  int64_t* X = reinterpret_cast<int64_t*>(work + w.X);
-  int64_t* XB = reinterpret_cast<int64_t*>(work + w.XB);
-  int64_t* Q = reinterpret_cast<int64_t*>(work + w.Q);
-  int64_t* O = reinterpret_cast<int64_t*>(work + w.O);
-  int64_t* H = reinterpret_cast<int64_t*>(work + w.H);
-  uint8_t* B = work + w.B;
-  int32_t* S = reinterpret_cast<int32_t*>(work + w.S);
-  unsigned long long* orw = reinterpret_cast<unsigned long long*>(work + w.orw);
-  uint32_t* bad = reinterpret_cast<uint32_t*>(work + w.bad);
-  cudaError_t e;
-  if ((e = cudaMemsetAsync(orw, 0, 8ull * 4 * c.layers, s)) != cudaSuccess) return e;
-  if ((e = cudaMemsetAsync(bad, 0xFF, 4, s)) != cudaSuccess) return e;
-  int32_t* K = reinterpret_cast<int32_t*>(st + lay.k);
-  int32_t* V = reinterpret_cast<int32_t*>(st + lay.v);
-  const size_t layer_words = (size_t)lay.cache * m.kv_dim;
-  const size_t gemm_smem = (size_t)kStages * kStageBytesB;
+  RowDesc t = {};
+  t.st = st;
+  t.cache = lay.cache;
+  t.np = 0xFFFFFFFFu;  // every row is a prompt position
+  t.generating = 0;
+  t.off_prompt = lay.prompt;
+  t.off_out = lay.out;
+  t.off_x = lay.x;
+  t.off_logits = lay.logits;
+  t.off_k = lay.k;
+  t.off_v = lay.v;
+  RowDesc* rows = reinterpret_cast<RowDesc*>(work + w.rows);
+  k_rows_fill<<<(P + 255) / 256, 256, 0, s>>>(rows, t, pos0, P);
+  cudaError_t e = enqueue_rows(m, st, w, work, P, pos0 + P, false, s);
+  if (e != cudaSuccess) return e;
+  k_bfinish<<<1, kRowThreads, 0, s>>>(st, reinterpret_cast<const int64_t*>(work + w.X),
+                                      reinterpret_cast<int64_t*>(st + lay.x), m.cfg.dim, pos0, P,
+                                      reinterpret_cast<const int32_t*>(work + w.rstat));
+  return cudaGetLastError();
+}
 
-  auto planes = [&](const int64_t* vec, uint32_t ld, uint32_t cols, uint32_t KG,
-                    const unsigned long long* ow) {
-    const uint64_t work_items = 8ull * Npad * KG * 16;
-    const uint32_t blocks = (uint32_t)std::min<uint64_t>((work_items + kRowThreads - 1) / kRowThreads, 4096);
-    k_bplanes<<<blocks, kRowThreads, 0, s>>>(st, vec, ld, P, cols, Npad, KG, ow, B);
-  };
-  auto gemm = [&](const uint8_t* Wm, uint32_t rows, uint32_t KG, const unsigned long long* ow) {
-    const dim3 grid((rows + kBM - 1) / kBM, 8 * Npad / kBN);
-    k_bgemm<<<grid, kGemmThreads, gemm_smem, s>>>(st, Wm, rows, KG, B, Npad, ow, S);
-  };
-  auto epi = [&](BEpiParams p) {
-    p.st = st;
-    p.S = S;
-    p.Npad = Npad;
-    p.P = P;
-    p.pos0 = pos0;
-    const uint64_t items = (uint64_t)P * (p.rows / 2);
-    const uint32_t blocks = (uint32_t)std::min<uint64_t>((items + kRowThreads - 1) / kRowThreads, 8192);
-    k_bepi<<<blocks, kRowThreads, 0, s>>>(p);
-  };
+cudaError_t batch_gather_headers(const PrefillModel& m, uint8_t* const* host_states, uint32_t n,
+                                 uint8_t* work, uint32_t cap, uint8_t* host_out, cudaStream_t s) {
+  if (n == 0 || n > cap) return cudaErrorInvalidValue;
+  const WorkLayout w = work_layout(m, cap);
+  cudaError_t e = cudaMemcpyAsync(work + w.ptrs, host_states, 8ull * n, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return e;
+  k_gather_headers<<<(n * (kHeaderBytes / 8) + 255) / 256, 256, 0, s>>>(
+      reinterpret_cast<const uint8_t* const*>(work + w.ptrs), n, work + w.hdrs);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = cudaMemcpyAsync(host_out, work + w.hdrs, (size_t)kHeaderBytes * n, cudaMemcpyDeviceToHost, s)) !=
+      cudaSuccess)
+    return e;
+  return cudaStreamSynchronize(s);
+}
 
-  k_bembed<<<P, kRowThreads, 0, s>>>(st, lay.prompt, pos0, X, c.dim, m.embed, m.embed_scale, c.vocab, bad);
-  for (uint32_t l = 0; l < c.layers; ++l) {
-    const DevLayer& Wl = m.layers[l];
-    unsigned long long* o4 = orw + 4 * l;
-    // phases 4-8: attention norm, Q/K/V rows, checked cache stores, rotary
-    k_bnorm<<<P, kRowThreads, 0, s>>>(st, X, XB, Wl.attn_norm, c.dim, o4 + 0);
-    planes(XB, c.dim, c.dim, KGd, o4 + 0);
-    gemm(Wl.wqkv, c.dim + 2 * m.kv_dim, KGd, o4 + 0);
-    BEpiParams pq = {};
-    pq.rows = c.dim + 2 * m.kv_dim;
-    pq.orw = o4 + 0;
-    pq.scale = Wl.sqkv;
-    pq.mode = kBEpiQKV;
-    pq.Q = Q;
-    pq.kc = K + l * layer_words;
-    pq.vc = V + l * layer_words;
-    pq.rope = m.rope;
-    pq.dim = c.dim;
-    pq.kv_dim = m.kv_dim;
-    pq.head_dim = m.head_dim;
-    pq.layer = l;
-    epi(pq);
-    // phase 9
-    BAttnParams pa = {};
-    pa.st = st;
-    pa.Q = Q;
-    pa.O = O;
-    pa.kc = K + l * layer_words;
-    pa.vc = V + l * layer_words;
-    pa.exp_tab = m.exp_tab;
-    pa.pos0 = pos0;
-    pa.dim = c.dim;
-    pa.heads = c.heads;
-    pa.kv_heads = c.kv_heads;
-    pa.head_dim = m.head_dim;
-    pa.kv_dim = m.kv_dim;
-    pa.inv_sqrt = m.inv_sqrt;
-    pa.or_out = o4 + 1;
-    k_battn<<<dim3(c.heads, P), kRowThreads, battn_smem(m.head_dim, pos0 + P), s>>>(pa);
-    // phases 10-11: output rows and the residual
-    planes(O, c.dim, c.dim, KGd, o4 + 1);
-    gemm(Wl.wo, c.dim, KGd, o4 + 1);
-    BEpiParams po = {};
-    po.rows = c.dim;
-    po.orw = o4 + 1;
-    po.scale = Wl.so;
-    po.mode = kBEpiResid;
-    po.X = X;
-    epi(po);
-    // phases 12-14: feed-forward norm, gate and up rows, SiLU gating
-    k_bnorm<<<P, kRowThreads, 0, s>>>(st, X, XB, Wl.ffn_norm, c.dim, o4 + 2);
-    planes(XB, c.dim, c.dim, KGd, o4 + 2);
-    gemm(Wl.w13, 2 * c.hidden, KGd, o4 + 2);
-    BEpiParams pg = {};
-    pg.rows = 2 * c.hidden;
-    pg.orw = o4 + 2;
-    pg.scale = Wl.s13;
-    pg.mode = kBEpiSiLU;
-    pg.H = H;
-    pg.hidden = c.hidden;
-    pg.silu_tab = m.silu_tab;
-    pg.or_out = o4 + 3;
-    epi(pg);
-    // phases 15-16: down rows and the residual
-    planes(H, c.hidden, c.hidden, KGh, o4 + 3);
-    gemm(Wl.w2, c.dim, KGh, o4 + 3);
-    BEpiParams pd = {};
-    pd.rows = c.dim;
-    pd.orw = o4 + 3;
-    pd.scale = Wl.s2;
-    pd.mode = kBEpiResid;
-    pd.X = X;
-    epi(pd);
-  }
-  k_bfinish<<<1, kRowThreads, 0, s>>>(st, X, reinterpret_cast<int64_t*>(st + lay.x), c.dim, pos0, P, bad);
+cudaError_t enqueue_batch(const PrefillModel& m, const RowDesc* host_rows, uint32_t n, uint32_t max_positions,
+                          uint8_t* work, uint32_t cap, cudaStream_t s) {
+  if (n == 0 || n > cap) return cudaErrorInvalidValue;
+  const WorkLayout w = work_layout(m, cap);
+  cudaError_t e = cudaMemcpyAsync(work + w.rows, host_rows, sizeof(RowDesc) * n, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return e;
+  if ((e = enqueue_rows(m, nullptr, w, work, n, max_positions, true, s)) != cudaSuccess) return e;
+  k_mfinish<<<n, kFinishThreads, 0, s>>>(reinterpret_cast<const RowDesc*>(work + w.rows),
+                                         reinterpret_cast<const int64_t*>(work + w.X), m.cfg.dim,
+                                         m.cfg.vocab, m.exp_tab,
+                                         reinterpret_cast<const int32_t*>(work + w.rstat));
   return cudaGetLastError();
 }
 

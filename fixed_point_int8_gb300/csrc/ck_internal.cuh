@@ -413,7 +413,16 @@ __device__ SampleOut block_sample(const long long* logits, uint32_t vocab, long 
   return out;
 }
 
-// ------------------------------------------------------------------ layer-major prefill
+// ------------------------------------------------------------------ rows of many positions
+// The batched kernels (layer-major prefill of one run, or one position of each of many
+// runs) take one descriptor per row: the position it computes and where its run keeps it.
+struct RowDesc {
+  uint8_t* st;                 // the run's state
+  uint32_t pos, cache, np;     // position, cache positions, prompt ids
+  uint32_t generating;         // phases 17-19 follow the layers
+  uint64_t off_prompt, off_out, off_x, off_logits, off_k, off_v;
+};
+
 struct PrefillModel {
   ck_config cfg;
   uint32_t head_dim, kv_dim, inv_sqrt, pitch_d, pitch_h;
@@ -423,6 +432,9 @@ struct PrefillModel {
   const int32_t* rope;
   const uint32_t* exp_tab;
   const int32_t* silu_tab;
+  const uint8_t* cls;
+  const uint32_t* cls_scale;
+  const int32_t* final_norm;
 };
 // Device scratch a chunk of up to `cap` positions needs.
 size_t prefill_work_bytes(const PrefillModel& m, uint32_t cap);
@@ -432,6 +444,13 @@ cudaError_t configure_prefill(size_t smem_optin);
 // Prompt positions pos0 .. pos0+P-1 (none generating) of the state, layer by layer.
 cudaError_t enqueue_prefill(const PrefillModel& m, uint8_t* st, const StateLayout& lay, uint32_t pos0,
                             uint32_t P, uint8_t* work, uint32_t cap, cudaStream_t s);
+// Copies the 256-byte headers of n states (device pointers) to host_out; synchronizes.
+cudaError_t batch_gather_headers(const PrefillModel& m, uint8_t* const* host_states, uint32_t n,
+                                 uint8_t* work, uint32_t cap, uint8_t* host_out, cudaStream_t s);
+// One position of each of n runs (host_rows: their descriptors), with phases 17-19 where a
+// row generates; max_positions bounds every row's pos + 1.
+cudaError_t enqueue_batch(const PrefillModel& m, const RowDesc* host_rows, uint32_t n, uint32_t max_positions,
+                          uint8_t* work, uint32_t cap, cudaStream_t s);
 
 cudaError_t configure_step(size_t optin, size_t* dynamic_max);
 cudaError_t launch_step(const StepParams& p, cudaStream_t s, int grid, size_t smem);

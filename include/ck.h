@@ -208,6 +208,20 @@ typedef struct ck_turn_result {
 int ck_turn(ck_model* m, void* dev_state, size_t len, uint32_t n_positions, void* stream,
             ck_turn_result* out);
 
+/* One position of each of n_states runs of the model, in one batched pass: the matrix rows
+ * of all the runs' positions are one tensor-core contraction per matrix (the layer-major
+ * kernels of ck_set_prefill), attention reads each run's own cache up to its position, and
+ * each generating run samples its token (temperature and generator of its own state).  The
+ * same bits as ck_turn(state, 1) on each state in turn.  dev_states: n_states distinct
+ * device state pointers with their lengths in lens (host arrays); out and rcs (host arrays
+ * of n_states) receive each state's turn result and return code: 0, 3 (misaligned, not
+ * this model's, complete or failed: that state is left untouched), or 8 (a cache store did
+ * not fit: that run is failed).  Synchronizes `stream`.  Returns the first nonzero rcs[i],
+ * else 0; 10 for null arguments, repeated states or n_states of 0 or above 4096 (nothing is
+ * run), 9 for a CUDA error. */
+int ck_turn_batch(ck_model* m, void* const* dev_states, const size_t* lens, uint32_t n_states,
+                  void* stream, ck_turn_result* out, int* rcs);
+
 /* ck_turn_noalloc has no counterpart on the page: it exists for callers that cannot
  * allocate device memory once they are running, for example a server whose device memory
  * is carved up in advance into fixed arenas, or a host framework that owns every

@@ -595,6 +595,97 @@ def test_prefill_llama7b_shape_sampled_positions(ck):
     _prefill_sampled(ck, synth.LLAMA7B, 70, [0, 68])
 
 
+# ---------------------------------------------------------------- many runs in one pass
+
+def test_batched_runs_match_the_oracle(ck):
+    """Five runs of one model with different prompts, lengths, temperatures and seeds,
+    advanced one position each per batched pass from their first position to the end (runs
+    finish at different passes and then drop out); every run's state against the oracle
+    after every pass."""
+    wl = MODELS["gqa"]
+    P = Pair(ck, wl.spec, "step")
+    runs = []
+    for r, (n_prompt, steps, temp, seed) in enumerate([(12, 40, 0, 0), (3, 20, 1 << 16, 9),
+                                                         (30, 8, 16 << 16, 0), (1, 30, 3 << 14, 77),
+                                                         (7, 45, 0, 0)]):
+        ids = synth.prompt_ids(wl.spec, n_prompt, run=r)
+        so, sg = P.init(ck, ids, steps, temperature_q16=temp, seed=seed)
+        runs.append([so, sg, n_prompt, steps])
+    passes = 0
+    while True:
+        live = [r for r in runs if oracle.header(r[0])["phase"] == oracle.PHASE_RUNNING]
+        if not live:
+            break
+        rc, res, rcs = P.gpu.turn_batch([r[1] for r in live])
+        assert rc == 0 and rcs == [0] * len(live), (rc, rcs)
+        for r, got in zip(live, res):
+            rco, reso = P.orc.turn(r[0], 1)
+            assert rco == 0 and reso == got, (passes, reso, got)
+            compare_states(P.orc, r[0], ck.state_download(r[1]), r[2], r[3], f"pass {passes}")
+        passes += 1
+    assert passes == 51
+    # complete states are refused one by one, the others in the same call still run
+    so, sg = P.init(ck, synth.prompt_ids(wl.spec, 4), 3)
+    rc, res, rcs = P.gpu.turn_batch([runs[0][1], sg])
+    assert rc == 3 and rcs == [3, 0] and res[1]["work"] == 1
+    assert P.gpu.turn_batch([sg, sg])[0] == 10                      # the same state twice
+
+
+def test_batched_runs_fail_like_the_oracle(ck):
+    """Literal tiny runs overflow their caches at different positions: each failing run
+    fails alone, with the oracle's key, in the pass that reaches it, while the others go
+    on."""
+    wl = synth.WORKLOADS["tiny"]
+    P = Pair(ck, wl.spec, "step")
+    runs = []
+    for r in range(4):
+        ids = synth.prompt_ids(wl.spec, 2 + r, run=r)
+        so, sg = P.init(ck, ids, 6)
+        runs.append((so, sg))
+    for _ in range(12):
+        live = [r for r in runs if oracle.header(r[0])["phase"] == oracle.PHASE_RUNNING]
+        if not live:
+            break
+        rc, res, rcs = P.gpu.turn_batch([r[1] for r in live])
+        for (so, sg), got, rcg in zip(live, res, rcs):
+            rco, reso = P.orc.turn(so, 1)
+            assert rco == rcg and reso == got, (rco, rcg, reso, got)
+            ho, hg = oracle.header(so), oracle.header(ck.state_download(sg))
+            for k in ("phase", "error", "err_key", "position", "generated", "turns"):
+                assert ho[k] == hg[k], k
+    # this seed: three runs fail (positions 1, 0 and 6) and one completes
+    assert [oracle.header(r[0])["phase"] for r in runs] == [oracle.PHASE_FAILED] * 3 + [oracle.PHASE_DONE]
+
+
+def test_1b_sixty_four_runs_batched_sampled(ck):
+    """The 1B-shaped model with 64 runs: prompts prefilled per run, then generating
+    positions of all 64 runs in batched passes; sampled runs recomputed by the oracle for
+    the last pass from the state before it."""
+    wl = synth.WORKLOADS["1b_x64"]
+    spec = wl.spec
+    art = synth.build_artifact(spec)
+    orc = oracle.Model(art)
+    rc, gpu = ck.Model.load(art)
+    assert rc == 0
+    states = []
+    for r in range(wl.runs):
+        ids = synth.prompt_ids(spec, wl.n_prompt, run=r)
+        sg = gpu.new_state(wl.n_prompt, wl.steps)
+        assert gpu.init_state(sg, ids, wl.steps, temperature_q16=(r % 3) << 15, seed=r) == 0
+        assert gpu.turn(sg, wl.n_prompt - 1)[0] == 0
+        states.append(sg)
+    for _ in range(3):
+        rc, res, rcs = gpu.turn_batch(states)
+        assert rc == 0 and all(x["generated_this_turn"] == 1 for x in res)
+    snaps = {r: ck.state_download(states[r]) for r in (0, 1, 2, 37, wl.runs - 1)}
+    rc, res, rcs = gpu.turn_batch(states)
+    assert rc == 0
+    for r, host in snaps.items():
+        rco, reso = orc.turn(host, 1)
+        assert rco == 0 and reso == res[r], (r, reso, res[r])
+        compare_states(orc, host, ck.state_download(states[r]), wl.n_prompt, wl.steps, f"run {r}", turns=False)
+
+
 def test_paths_agree_and_unknown_path_is_rejected(ck):
     wl = MODELS["gqa"]
     P = Pair(ck, wl.spec, "step")
