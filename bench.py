@@ -15,7 +15,11 @@ Prints one JSON line:
              HBM copy bandwidth;
   cpu_baseline  the CPU oracle on a bounded sample of the same decode (it continues from
              the GPU's state after the prefill), whose tokens must equal the GPU's;
-  matrow_sweep  GB/s of the matrix-row kernel on the four sweep shapes.
+  matrow_sweep  GB/s of the matrix-row kernel on the four sweep shapes;
+  prefill    the 127 prompt positions of the workload, layer-major (device-timed);
+  batched_runs  the 1B-shaped model with 64 independent runs (64 prompt ids each, prefilled
+             per run), generating positions of all 64 advanced together per ck_turn_batch
+             pass, device-timed over --batched-passes passes.
 ``--impl reference`` times the CPU oracle alone on the same workload and metric.
 """
 from __future__ import annotations
@@ -39,7 +43,7 @@ import numpy as np  # noqa: E402
 METRIC = "decode tokens/s bit-exact vs oracle; matrow HBM GB/s as % of GB300 peak"
 WORKLOAD = ("llama7b_shape fixed-point decode: dim 4096, 32 layers, 32 heads x 128, FFN hidden 11008, "
             "vocab 32000, context 2048, u8 weights + u32 row scales (6.61 GB/token); 128 prompt ids "
-            "prefilled position by position, then greedy decode; single run per GPU")
+            "prefilled layer-major, then greedy decode; single run per GPU")
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -212,6 +216,10 @@ def run_ours(args):
 
     rank, world, local = dist_setup(args.gpus)
     libbuild.build()
+    if args.batched_only:
+        # profiling aid: only the 64-run batched measurement
+        print(json.dumps({"batched_runs": batched_runs(ck, torch, synth, args.batched_passes)}), flush=True)
+        return
     if args.matrow_only:
         # profiling aid: only the matrix-row timing of one shape, e.g. 22016x4096
         rows, cols = (int(v) for v in args.matrow_only.split("x"))
@@ -241,8 +249,17 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     setup_s = time.time() - t0
 
-    # prefill: prompt positions 0..126 and position 127, which generates the first token
-    rc, res = model.turn(state, n_prompt)
+    # prefill: prompt positions 0..126 layer-major, then position 127, which generates the
+    # first token
+    torch.cuda.synchronize()
+    pev0, pev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pev0.record(stream)
+    rc, res = model.turn(state, n_prompt - 1)
+    pev1.record(stream)
+    torch.cuda.synchronize()
+    assert rc == 0 and res["work"] == n_prompt - 1, (rc, res)
+    prefill_ms = pev0.elapsed_time(pev1)
+    rc, res = model.turn(state, 1)
     assert rc == 0 and res["generated"] == 1, (rc, res)
     snapshot = ck.state_download(state) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
 
@@ -303,6 +320,11 @@ def run_ours(args):
     bitexact = None
     if snapshot is not None:
         cpu, bitexact = cpu_baseline(art, snapshot, toks, args.cpu_seconds)
+    batched = None
+    if args.batched_passes and rank == 0:
+        del model, state
+        torch.cuda.empty_cache()
+        batched = batched_runs(ck, torch, synth, args.batched_passes)
 
     if rank != 0:
         return
@@ -342,10 +364,62 @@ def run_ours(args):
         "bitexact": bitexact,
         "matrow_sweep": sweep,
         "matrow_roofline": roof_matrow if kernel_path == "step" else None,
+        "prefill": {"value": round((n_prompt - 1) / (prefill_ms * 1e-3), 1), "unit": "prompt positions/s",
+                    "positions": n_prompt - 1, "ms": round(prefill_ms, 3),
+                    "how": "one ck_turn over the prompt positions that generate no token: layer-major "
+                           "chunks, byte-plane f16 MMA contraction (CUDA events on the stream)"},
+        "batched_runs": batched,
         "path": kernel_path,
         "setup_s": round(setup_s, 1),
     }
     print(json.dumps(line), flush=True)
+
+
+def batched_runs(ck, torch, synth, passes):
+    """The 1B-shaped model with 64 runs: each prefilled per run, then `passes` generating
+    passes of ck_turn_batch (one position of every run each), device-timed after three
+    untimed passes."""
+    wl = synth.WORKLOADS["1b_x64"]
+    spec = wl.spec
+    passes = min(passes, wl.steps - 4)
+    rc, m = ck.Model.load(synth.build_artifact(spec))
+    assert rc == 0
+    states = []
+    for r in range(wl.runs):
+        sg = m.new_state(wl.n_prompt, wl.steps)
+        assert m.init_state(sg, synth.prompt_ids(spec, wl.n_prompt, run=r), wl.steps) == 0
+        assert m.turn(sg, wl.n_prompt - 1)[0] == 0
+        states.append(sg)
+    for _ in range(3):
+        rc, res, rcs = m.turn_batch(states)
+        assert rc == 0
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(passes):
+        rc, res, rcs = m.turn_batch(states)
+        assert rc == 0 and all(x["generated_this_turn"] == 1 for x in res)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    value = wl.runs * passes / (ms * 1e-3)
+    macs = spec.weight_bytes_per_token() * wl.runs  # one u8 x i64 multiply-add per weight and run
+    peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak = float(json.load(f)["bf16_tflops"])
+    except Exception:
+        pass
+    tflops = 2 * macs / (ms * 1e-3 / passes) / 1e12
+    return {"value": round(value, 1), "unit": "tokens/s", "runs": wl.runs, "passes": passes,
+            "ms_per_pass": round(ms / passes, 3),
+            "workload": "1b_shape (dim 2048, 22 layers, 32 heads, FFN 5632, vocab 32000), 64 runs x 64 "
+                        "prompt ids, positions 67.. of each run, greedy",
+            "algorithmic_tflops": round(tflops, 1),
+            "algorithmic_frac_of_bf16_peak": round(tflops / peak, 4) if peak else None,
+            "note": "whole pass (all kernels); algorithmic = 2 x weights x runs per pass, the byte "
+                    "planes multiply the tensor work by the plane count (3 here)"}
 
 
 def time_matrow(ck, torch, rows, cols, iters):
@@ -482,6 +556,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=150.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batched-passes", type=int, default=40,
+                    help="passes of the 64-run batched measurement (0: skip it)")
+    ap.add_argument("--batched-only", action="store_true",
+                    help="profiling aid: run only the 64-run batched measurement")
     ap.add_argument("--path", choices=("auto", "step", "kernels"), default="auto",
                     help="one persistent kernel per position (step) or one kernel per phase")
     ap.add_argument("--prompt-ids", type=int, default=128,
