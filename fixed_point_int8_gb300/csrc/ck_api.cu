@@ -682,6 +682,7 @@ PrefillModel prefill_model(const ck_model* m) {
   pm.cls = m->cls;
   pm.cls_scale = m->cls_scale;
   pm.final_norm = m->final_norm;
+  pm.num_sms = m->num_sms;
   return pm;
 }
 

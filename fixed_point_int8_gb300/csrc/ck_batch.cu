@@ -33,11 +33,7 @@ namespace {
 constexpr uint32_t kBM = 128;        // contraction tile: 128 matrix rows
 constexpr uint32_t kBN = 64;         // x 64 plane columns (positions of one plane)
 constexpr uint32_t kBK = 128;        // x 128 columns, one column group
-constexpr int kGemmThreads = 256;    // 8 warps, 4 (rows) x 2 (columns), 32 x 32 each
-constexpr int kStages = 3;
-constexpr uint32_t kATile = kBM * kBK;       // u8 weights, in the matrix's own layout
-constexpr uint32_t kBTile = kBN * kBK * 2;   // f16 planes
-constexpr uint32_t kStageBytesB = kATile + kBTile;
+constexpr uint32_t kBTile = kBN * kBK * 2;   // f16 planes: one 64 x 128 tile
 constexpr uint32_t kFlushGroups = 4;         // column groups between f32 -> i32 moves
 constexpr int kRowThreads = 256;
 
@@ -155,21 +151,32 @@ __global__ void __launch_bounds__(kRowThreads) k_bnorm(const uint8_t* gate, cons
 
 // Plane layout, read by the contraction one 16 KB tile at a time: plane column
 // n' = k * Npad + n (plane k of position n), tiles of 64 plane columns x 128 columns stored
-// tile after tile (column groups inner), each tile 64 rows of 256 bytes (128 f16), the
-// 16-byte chunk j of row i at j ^ ((i & 7) << 1) so the MMA operand loads hit every bank.
+// tile after tile (column groups inner).  A tile is the MMA's K-major operand layout with the
+// 128-byte swizzle: two atom columns of 64 columns each (64 rows of 128 bytes), the 16-byte
+// chunk c of row i at c ^ (i & 7).
 __device__ __forceinline__ uint64_t plane_offset(uint32_t np, uint32_t KG, uint32_t kg, uint32_t chunk) {
   const uint32_t nt = np / kBN, nl = np % kBN;
-  return ((uint64_t)nt * KG + kg) * kBTile + (uint64_t)nl * 256 + ((chunk ^ ((nl & 7u) << 1)) << 4);
+  return ((uint64_t)nt * KG + kg) * kBTile + (chunk >> 3) * (kBN * 128) + (uint64_t)nl * 128 +
+         (((chunk & 7u) ^ (nl & 7u)) << 4);
 }
 
 // Writes planes 0 .. L-1 of the P vectors V (row stride ld, cols used), zero beyond P and
-// cols.  One thread per 8 columns of one plane of one position.
+// cols.  One thread per 8 columns of one plane of one position.  With clear_rows > 0 it also
+// zeroes the next contraction's output S[n'][r] (n' < L * Npad, r < clear_rows), which a
+// contraction split over column ranges adds into.
 __global__ void __launch_bounds__(kRowThreads) k_bplanes(const uint8_t* gate, const int64_t* V,
                                                           uint32_t ld, uint32_t P, uint32_t cols,
                                                           uint32_t Npad, uint32_t KG,
-                                                          const unsigned long long* orw, uint8_t* B) {
+                                                          const unsigned long long* orw, uint8_t* B,
+                                                          int32_t* S, uint32_t clear_rows) {
   if (!running(gate)) return;
   const int L = limbs_of_or(*orw);
+  if (clear_rows) {
+    const uint64_t words = (uint64_t)L * Npad * clear_rows;
+    for (uint64_t q = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; q < words;
+         q += (uint64_t)gridDim.x * blockDim.x)
+      S[q] = 0;
+  }
   const uint32_t per_row = KG * 16;  // 8-column chunks of a row
   const uint64_t total = (uint64_t)L * Npad * per_row;
   for (uint64_t q = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; q < total;
@@ -198,18 +205,93 @@ __global__ void __launch_bounds__(kRowThreads) k_bplanes(const uint8_t* gate, co
 
 // ------------------------------------------------------------------ the contraction
 
+// The 5th-generation tensor cores (tcgen05): one thread issues 128 x N x 16 MMAs whose
+// operands are read from shared memory through matrix descriptors and whose f32
+// accumulators live in tensor memory (TMEM).  Both operands are K-major with the 128-byte
+// swizzle: 8-row atoms of 128-byte rows, row r's 16-byte chunk j at j ^ (r & 7), atoms
+// 1,024 bytes apart.  The weights' column-group layout is that pattern for bytes, so a
+// weight tile arrives with one bulk copy and is widened to f16 in place of layout; the
+// planes are stored in it as f16.
+constexpr uint32_t kTN = 128;                  // most plane columns per block
+constexpr uint32_t kTcConvWarps = 8;           // widen the weights, drain the accumulators
+constexpr int kTcThreads = 32 * (kTcConvWarps + 2);  // + a producer warp and an MMA warp
+constexpr uint32_t kRing = 3;                  // weight-byte and plane stages in flight
+constexpr uint32_t kAu8 = kBM * kBK;           // 16 KB: 128 rows x 128 weight bytes
+constexpr uint32_t kAf16 = 2 * kBM * 128;      // 32 KB: the same as f16, two atom columns
+constexpr uint32_t kBmax = 2 * kTN * 128;      // 32 KB: 128 plane rows x 128 f16 columns
+constexpr uint32_t kTcSmem = kRing * (kAu8 + kBmax) + 2 * kAf16 + 1024;  // + alignment slack
+constexpr uint32_t kTmemCols = 2 * kTN;        // two accumulator buffers
+constexpr uint32_t kTcPoll = 1u << 22;         // bounded waits
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
-               "r"(src_bytes)
+__device__ __forceinline__ void mb_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mb_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ void mb_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
+}
+__device__ __forceinline__ bool mb_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_addr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase with the given parity; gives up after kTcPoll polls, raising *abort.
+__device__ __forceinline__ void mb_wait(uint64_t* b, uint32_t parity, volatile int* abort) {
+  for (uint32_t it = 0; it < kTcPoll; ++it) {
+    if (mb_try(b, parity)) return;
+    if (*abort) return;
+  }
+  *abort = 1;
+}
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+
+struct TcBars {
+  uint64_t full[kRing];     // stage landed (bulk copies)
+  uint64_t empty[kRing];    // stage's MMAs done: the slot may be refilled
+  uint64_t conv[2];         // f16 weights of the stage written (one arrival per converter warp)
+  uint64_t f16free[2];      // MMAs reading an f16 buffer done
+  uint64_t accf[2];         // accumulator group complete
+  uint64_t accfree[2];      // accumulator buffer drained (one arrival per converter warp)
+};
+
+// Shared-memory matrix descriptor: start >> 4, leading offset (unused with the swizzle) 16
+// bytes, 8-row stride 1,024 bytes, descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of kind::f16: f16 operands, f32 accumulator, both K-major,
+// N / 8 at bit 17, M / 16 at bit 24.
+__host__ __device__ constexpr uint32_t mma_idesc(uint32_t n) {
+  return (1u << 4) | ((n >> 3) << 17) | ((kBM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16_ss(uint32_t tmem, uint64_t da, uint64_t db, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
+      ::"r"(tmem), "l"(da), "l"(db), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(smem_addr(bar))
+               : "memory");
 }
 
 // Two weight bytes (selected by sel) as an f16 pair of byte - 128: 0x64XX is the f16 value
@@ -221,124 +303,209 @@ __device__ __forceinline__ uint32_t bytes_to_f16x2(uint32_t w, uint32_t sel) {
   return r;
 }
 
-__device__ __forceinline__ void mma_f16(float* c, const uint32_t* a, const uint32_t* b) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+// Widens a stage's weight bytes (128 rows x 128 columns, column-group layout) to f16
+// (byte - 128) in the two-atom-column layout the MMA reads.  Four 16-byte chunks a thread.
+__device__ __forceinline__ void widen_weights(const uint8_t* src, uint8_t* dst) {
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const uint32_t id = threadIdx.x + e * (32 * kTcConvWarps);  // 1,024 chunks: row id / 8, chunk id % 8
+    const uint32_t r = id >> 3, j = id & 7u;
+    const uint4 w = *reinterpret_cast<const uint4*>(src + r * 128 + ((j ^ (r & 7u)) << 4));
+    uint4 lo, hi;
+    lo.x = bytes_to_f16x2(w.x, 0x5140u);
+    lo.y = bytes_to_f16x2(w.x, 0x5342u);
+    lo.z = bytes_to_f16x2(w.y, 0x5140u);
+    lo.w = bytes_to_f16x2(w.y, 0x5342u);
+    hi.x = bytes_to_f16x2(w.z, 0x5140u);
+    hi.y = bytes_to_f16x2(w.z, 0x5342u);
+    hi.z = bytes_to_f16x2(w.w, 0x5140u);
+    hi.w = bytes_to_f16x2(w.w, 0x5342u);
+    // columns 16j .. 16j+15: atom column j / 4, f16 chunks 2(j % 4) and 2(j % 4) + 1
+    uint8_t* row = dst + (j >> 2) * (kBM * 128) + r * 128;
+    const uint32_t c0 = 2 * (j & 3u);
+    *reinterpret_cast<uint4*>(row + ((c0 ^ (r & 7u)) << 4)) = lo;
+    *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7u)) << 4)) = hi;
+  }
 }
 
-// S[n'][r] = sum_c (W[r][c] - 128) * plane[n'][c] for plane columns n' < L * Npad, one
-// 128 x 64 tile per block.  Within every 16-column step, lane (g, t) presents the physical
-// columns 4t .. 4t+3 of the step as the MMA's k = 2t, 2t+1, 2t+8, 2t+9, for the weights and
-// the planes alike, so each operand is one 32- or 64-bit shared load; the order of the
-// columns inside a sum does not matter.
-__global__ void __launch_bounds__(kGemmThreads, 2) k_bgemm(const uint8_t* gate, const uint8_t* W,
-                                                           uint32_t rows, uint32_t KG,
-                                                           const uint8_t* B, uint32_t Npad,
-                                                           const unsigned long long* orw, int32_t* S) {
-  extern __shared__ __align__(128) uint8_t smem[];
+// Adds the f32 sums of one accumulator buffer (this warp's 32 rows, this warpgroup's half
+// of the N columns) to the integer sums.  Every sum is an integer below 2^24: exact.
+template <uint32_t N>
+__device__ __forceinline__ void drain(uint32_t tmem_buf, int32_t* iacc) {
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t base = tmem_buf + ((32 * (warp & 3u)) << 16) + (warp >> 2) * (N / 2);
+#pragma unroll
+  for (uint32_t c = 0; c < N / 2; c += 16) {
+    uint32_t v[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(base + c));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) iacc[c + i] += __float2int_rn(__uint_as_float(v[i]));
+  }
+}
+
+// S[n'][r] = sum_c (W[r][c] - 128) * plane[n'][c] for the block's 128 rows and N plane
+// columns (N = 128, or 64 for a last tile), over its range of column groups (gridDim.z
+// ranges add their integer sums into S, cleared beforehand).  Warp-specialised, linked by
+// mbarriers only:
+//   producer (warp 8)   copies stage s (a column group's weight bytes and planes) into ring
+//                       slot s % kRing once the MMAs of stage s - kRing are done;
+//   converters (0..7)   widen stage s's weights into f16 buffer s % 2 once the MMAs of
+//                       stage s - 2 are done, and drain each finished accumulator group;
+//   MMA thread (warp 9) issues stage s's eight 16-column MMAs into accumulator buffer g % 2
+//                       of group g (four column groups, 512 columns: every f32 partial sum
+//                       stays below 2^24) once stage s is widened and group g - 2 drained.
+template <uint32_t N>
+__device__ void bgemm_tile(const uint8_t* W, uint32_t rows, uint32_t KG, const uint8_t* B, uint32_t nt,
+                           int32_t* S, int* fault, uint8_t* sm, TcBars& bar, uint32_t tmem,
+                           volatile int* abort) {
+  const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t m0 = blockIdx.x * kBM;
+  const uint32_t kg0 = blockIdx.z * KG / gridDim.z, kg1 = (blockIdx.z + 1) * KG / gridDim.z;
+  const uint32_t ns = kg1 - kg0, ngroups = (ns + kFlushGroups - 1) / kFlushGroups;
+  uint8_t* au8 = sm;
+  uint8_t* bsm = au8 + kRing * kAu8;
+  uint8_t* af16 = bsm + kRing * kBmax;
+  if (warp == kTcConvWarps) {  // producer
+    if (lane != 0) return;
+    const uint32_t a_bytes = min(kBM, rows - m0) * kBK;
+    for (uint32_t s = 0; s < ns; ++s) {
+      const uint32_t slot = s % kRing, kg = kg0 + s;
+      if (s >= kRing) mb_wait(&bar.empty[slot], ((s - kRing) / kRing) & 1u, abort);
+      if (*abort) return;
+      mb_expect_tx(&bar.full[slot], a_bytes + N * 256);
+      bulk_copy(au8 + slot * kAu8, W + ((size_t)kg * rows + m0) * kBK, a_bytes, &bar.full[slot]);
+      // plane tiles of 64 rows: atom column a of tile t -> rows 64 t .. of atom column a
+#pragma unroll
+      for (uint32_t t = 0; t < N / kBN; ++t)
+#pragma unroll
+        for (uint32_t a = 0; a < 2; ++a)
+          bulk_copy(bsm + slot * kBmax + a * (N * 128) + t * (kBN * 128),
+                    B + ((size_t)(nt * (N / kBN) + t) * KG + kg) * kBTile + a * (kBN * 128), kBN * 128,
+                    &bar.full[slot]);
+    }
+    return;
+  }
+  if (warp == kTcConvWarps + 1) {  // MMA issuer
+    if (lane != 0) return;
+    for (uint32_t s = 0; s < ns; ++s) {
+      const uint32_t slot = s % kRing, fb = s & 1u, g = s / kFlushGroups;
+      mb_wait(&bar.full[slot], (s / kRing) & 1u, abort);
+      mb_wait(&bar.conv[fb], (s >> 1) & 1u, abort);
+      if (s % kFlushGroups == 0 && g >= 2) mb_wait(&bar.accfree[g & 1u], ((g - 2) >> 1) & 1u, abort);
+      if (*abort) return;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t abase = smem_addr(af16 + fb * kAf16), bbase = smem_addr(bsm + slot * kBmax);
+      const uint32_t acc_tmem = tmem + (g & 1u) * kTN;
+#pragma unroll
+      for (uint32_t kk = 0; kk < 8; ++kk) {
+        const uint64_t da = smem_desc(abase + (kk >> 2) * (kBM * 128) + (kk & 3u) * 32);
+        const uint64_t db = smem_desc(bbase + (kk >> 2) * (N * 128) + (kk & 3u) * 32);
+        const uint32_t accumulate = (s % kFlushGroups != 0 || kk != 0) ? 1u : 0u;
+        mma_f16_ss(acc_tmem, da, db, mma_idesc(N), accumulate);
+      }
+      mma_commit(&bar.empty[slot]);
+      mma_commit(&bar.f16free[fb]);
+      if ((s + 1) % kFlushGroups == 0 || s + 1 == ns) mma_commit(&bar.accf[g & 1u]);
+    }
+    return;
+  }
+  // converters
+  int32_t iacc[N / 2];
+#pragma unroll
+  for (uint32_t i = 0; i < N / 2; ++i) iacc[i] = 0;
+  uint32_t drained = 0;
+  auto drain_group = [&](uint32_t gg) {
+    mb_wait(&bar.accf[gg & 1u], (gg >> 1) & 1u, abort);
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (!*abort) drain<N>(tmem + (gg & 1u) * kTN, iacc);
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mb_arrive(&bar.accfree[gg & 1u]);
+  };
+  for (uint32_t s = 0; s < ns; ++s) {
+    const uint32_t slot = s % kRing, fb = s & 1u;
+    mb_wait(&bar.full[slot], (s / kRing) & 1u, abort);
+    if (s >= 2) mb_wait(&bar.f16free[fb], ((s - 2) >> 1) & 1u, abort);
+    if (*abort) break;
+    widen_weights(au8 + slot * kAu8, af16 + fb * kAf16);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mb_arrive(&bar.conv[fb]);
+    // group g - 1 finished a stage ago: drain it while group g fills the other buffer
+    const uint32_t g = s / kFlushGroups;
+    if (s % kFlushGroups == 1 && g >= 1 && drained == g - 1) drain_group(drained++);
+  }
+  for (; drained < ngroups && !*abort; ++drained) drain_group(drained);
+  if (*abort) {
+    if (tid == 0) atomicExch(fault, 1);
+    return;
+  }
+  // warp w holds rows 32 (w % 4) + lane, columns of half w / 4
+  const uint32_t r = m0 + 32 * (warp & 3u) + lane;
+  if (r >= rows) return;
+  const uint32_t n0 = nt * N + (warp >> 2) * (N / 2);
+#pragma unroll
+  for (uint32_t i = 0; i < N / 2; ++i) {
+    int32_t* dst = S + (size_t)(n0 + i) * rows + r;
+    if (gridDim.z > 1)
+      atomicAdd(dst, iacc[i]);
+    else
+      *dst = iacc[i];
+  }
+}
+
+// One block: 128 rows of the matrix x up to 128 plane columns (blockIdx.y), tcgen05 MMAs.
+__global__ void __launch_bounds__(kTcThreads, 1) k_bgemm(const uint8_t* gate, const uint8_t* W,
+                                                         uint32_t rows, uint32_t KG, const uint8_t* B,
+                                                         uint32_t Npad, const unsigned long long* orw,
+                                                         int32_t* S, int* fault) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ TcBars bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
   if (!running(gate)) return;
   const int L = limbs_of_or(*orw);
+  const uint32_t cols = (uint32_t)L * Npad;  // plane columns in use (a multiple of 64)
   const uint32_t nt = blockIdx.y;
-  if (nt >= (uint32_t)L * (Npad / kBN)) return;
-  const uint32_t m0 = blockIdx.x * kBM;
-  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t wm = warp & 3u, wn = warp >> 2;
-  const uint32_t g = lane >> 2, t = lane & 3u;
-
-  auto load_stage = [&](uint32_t kg, uint32_t slot) {
-    uint8_t* sa = smem + slot * kStageBytesB;
-    uint8_t* sb = sa + kATile;
-    const uint8_t* ga = W + ((size_t)kg * rows + m0) * kBK;  // rows m0.. of group kg: contiguous
-    const uint8_t* gb = B + ((size_t)nt * KG + kg) * kBTile;
-    for (uint32_t q = tid; q < kATile / 16; q += kGemmThreads) {
-      const bool ok = m0 + (q >> 3) < rows;
-      cp_async16(sa + q * 16, ok ? ga + q * 16 : W, ok ? 16u : 0u);  // rows past the end: zeros
+  if (nt * kTN >= cols) return;
+  const bool narrow = cols - nt * kTN < kTN;  // a last tile of 64 columns
+  uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  if (threadIdx.x == 0) {
+    for (uint32_t i = 0; i < kRing; ++i) {
+      mb_init(&bar.full[i], 1);
+      mb_init(&bar.empty[i], 1);
     }
-    for (uint32_t q = tid; q < kBTile / 16; q += kGemmThreads) cp_async16(sb + q * 16, gb + q * 16, 16u);
-  };
-
-  float acc[2][4][4];
-  int32_t iacc[2][4][4];
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc[i][j][e] = 0.f;
-        iacc[i][j][e] = 0;
-      }
-
-#pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) {
-    if ((uint32_t)s < KG) load_stage((uint32_t)s, (uint32_t)s);
-    cp_async_commit();
+    for (uint32_t i = 0; i < 2; ++i) {
+      mb_init(&bar.conv[i], kTcConvWarps);
+      mb_init(&bar.f16free[i], 1);
+      mb_init(&bar.accf[i], 1);
+      mb_init(&bar.accfree[i], kTcConvWarps);
+    }
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  for (uint32_t kg = 0; kg < KG; ++kg) {
-    cp_async_wait<kStages - 2>();
-    __syncthreads();
-    const uint32_t next = kg + kStages - 1;
-    if (next < KG) load_stage(next, next % kStages);
-    cp_async_commit();
-    const uint8_t* sa = smem + (kg % kStages) * kStageBytesB;
-    const uint8_t* sb = sa + kATile;
-#pragma unroll 2
-    for (uint32_t kk = 0; kk < 8; ++kk) {
-      uint32_t a[2][4], b[4][2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const uint32_t r0 = wm * 32 + i * 16 + g;  // r0 & 7 == g, and so is (r0 + 8) & 7
-        const uint32_t off = ((kk ^ g) << 4) + 4 * t;
-        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(sa + r0 * kBK + off);
-        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(sa + (r0 + 8) * kBK + off);
-        a[i][0] = bytes_to_f16x2(w0, 0x5140u);
-        a[i][1] = bytes_to_f16x2(w1, 0x5140u);
-        a[i][2] = bytes_to_f16x2(w0, 0x5342u);
-        a[i][3] = bytes_to_f16x2(w1, 0x5342u);
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t nl = wn * 32 + j * 8 + g;  // nl & 7 == g
-        const uint32_t chunk = (2 * kk + (t >> 1)) ^ (g << 1);
-        const uint2 v = *reinterpret_cast<const uint2*>(sb + nl * 256 + (chunk << 4) + 8 * (t & 1u));
-        b[j][0] = v.x;
-        b[j][1] = v.y;
-      }
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) mma_f16(acc[i][j], a[i], b[j]);
-    }
-    if ((kg + 1) % kFlushGroups == 0 || kg + 1 == KG) {
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            iacc[i][j][e] += __float2int_rn(acc[i][j][e]);  // an integer below 2^24: exact
-            acc[i][j][e] = 0.f;
-          }
-    }
+  if ((threadIdx.x >> 5) == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_addr(&tmem_slot)), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  cp_async_wait<0>();
-  // lane (g, t) holds rows g and g + 8, plane columns 2t and 2t + 1 of each 16 x 8 tile
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t n0 = nt * kBN + wn * 32 + j * 8 + 2 * t;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t r = m0 + wm * 32 + i * 16 + g + (e >= 2 ? 8u : 0u);
-        const uint32_t np = n0 + (e & 1);
-        if (r < rows) S[(size_t)np * rows + r] = iacc[i][j][e];
-      }
-    }
-  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = tmem_slot;
+  if (narrow)
+    bgemm_tile<kBN>(W, rows, KG, B, nt * (kTN / kBN), S, fault, sm, bar, tmem, &abort_flag);
+  else
+    bgemm_tile<kTN>(W, rows, KG, B, nt, S, fault, sm, bar, tmem, &abort_flag);
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if ((threadIdx.x >> 5) == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
 // ------------------------------------------------------------------ epilogues
@@ -577,9 +744,17 @@ __global__ void k_rows_fill(RowDesc* rows, RowDesc tmpl, uint32_t pos0, uint32_t
 // position's residual becomes the state's x and the cursor moves past the chunk.
 __global__ void __launch_bounds__(kRowThreads) k_bfinish(uint8_t* st, const int64_t* X, int64_t* x,
                                                          uint32_t d, uint32_t pos0, uint32_t P,
-                                                         const int32_t* rstat) {
+                                                         const int32_t* rstat, const int* fault) {
   __shared__ uint32_t first_bad;
   if (!running(st)) return;
+  if (*fault) {  // a contraction's wait ran out: nothing of the chunk is trusted
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      hdr<uint32_t>(st, kHError) = CK_CUDA_ERROR;
+      hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
+    }
+    return;
+  }
   const uint64_t key = hdr_ld<uint64_t>(st, kHErrKey);
   const uint32_t key_pos = key == kNoError ? 0xFFFFFFFFu : (uint32_t)(key >> 44);
   if (threadIdx.x == 0) {
@@ -622,7 +797,7 @@ constexpr int kFinishThreads = 256;
 __global__ void __launch_bounds__(kFinishThreads) k_mfinish(const RowDesc* rows, const int64_t* X,
                                                             uint32_t d, uint32_t vocab,
                                                             const uint32_t* exp_tab,
-                                                            const int32_t* rstat) {
+                                                            const int32_t* rstat, const int* fault) {
   __shared__ unsigned long long gsum[kSampleGroups];
   __shared__ long long wv[kFinishThreads / 32];
   __shared__ uint32_t wi[kFinishThreads / 32];
@@ -632,12 +807,12 @@ __global__ void __launch_bounds__(kFinishThreads) k_mfinish(const RowDesc* rows,
   const RowDesc rd = rows[n];
   uint8_t* st = rd.st;
   const uint64_t key = hdr_ld<uint64_t>(st, kHErrKey);
-  const int32_t bad = rstat[n];
+  const int32_t bad = *fault ? CK_CUDA_ERROR : rstat[n];  // a contraction that gave up fails all
   __syncthreads();  // header read by all before thread 0 writes it
   if (threadIdx.x == 0) hdr<uint64_t>(st, kHTurns) = hdr_ld<uint64_t>(st, kHTurns) + 1;
   if (bad || key != kNoError) {
     if (threadIdx.x == 0) {
-      if (bad) hdr<uint64_t>(st, kHErrKey) = kNoError;  // stopped before any store
+      if (bad == CK_INVALID_STATE) hdr<uint64_t>(st, kHErrKey) = kNoError;  // stopped before any store
       hdr<uint32_t>(st, kHError) = bad ? (uint32_t)bad : CK_ARITHMETIC;
       hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
     }
@@ -722,7 +897,7 @@ __global__ void k_gather_headers(const uint8_t* const* states, uint32_t n, uint8
 uint32_t pad64(uint32_t n) { return (n + 63u) & ~63u; }
 
 struct WorkLayout {
-  uint64_t X, XB, Q, O, H, B, S, orw, rows, rstat, ptrs, hdrs, size;
+  uint64_t X, XB, Q, O, H, B, S, orw, rows, rstat, ptrs, hdrs, fault, size;
 };
 
 WorkLayout work_layout(const PrefillModel& m, uint32_t cap) {
@@ -745,6 +920,7 @@ WorkLayout work_layout(const PrefillModel& m, uint32_t cap) {
   w.rstat = take(4 * Np);
   w.ptrs = take(8 * Np);
   w.hdrs = take((uint64_t)kHeaderBytes * Np);
+  w.fault = take(4);
   w.size = off;
   return w;
 }
@@ -767,20 +943,30 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
   unsigned long long* orw = reinterpret_cast<unsigned long long*>(work + w.orw);
   const RowDesc* rows = reinterpret_cast<const RowDesc*>(work + w.rows);
   int32_t* rstat = reinterpret_cast<int32_t*>(work + w.rstat);
+  int* fault = reinterpret_cast<int*>(work + w.fault);
   cudaError_t e;
   if ((e = cudaMemsetAsync(orw, 0, 8ull * (4 * c.layers + 1), s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(rstat, 0, 4ull * P, s)) != cudaSuccess) return e;
-  const size_t gemm_smem = (size_t)kStages * kStageBytesB;
+  if ((e = cudaMemsetAsync(fault, 0, 4, s)) != cudaSuccess) return e;
 
+  // column-range split of a contraction: about one block per SM, assuming the usual three
+  // planes (more planes only add blocks), each range at least one group of four column groups
+  auto splits_for = [&](uint32_t nrows, uint32_t KG) {
+    const uint32_t base = ((nrows + kBM - 1) / kBM) * ((3 * Npad + kTN - 1) / kTN);
+    uint32_t z = ((uint32_t)m.num_sms + base - 1) / base;
+    return std::max(1u, std::min(z, KG / kFlushGroups));
+  };
+  // the planes of a vector, clearing the output of the contraction that follows when it splits
   auto planes = [&](const int64_t* vec, uint32_t ld, uint32_t cols, uint32_t KG,
-                    const unsigned long long* ow) {
+                    const unsigned long long* ow, uint32_t next_rows, uint32_t next_KG) {
     const uint64_t work_items = 8ull * Npad * KG * 16;
     const uint32_t blocks = (uint32_t)std::min<uint64_t>((work_items + kRowThreads - 1) / kRowThreads, 4096);
-    k_bplanes<<<blocks, kRowThreads, 0, s>>>(gate, vec, ld, P, cols, Npad, KG, ow, B);
+    const uint32_t clear = splits_for(next_rows, next_KG) > 1 ? next_rows : 0u;
+    k_bplanes<<<blocks, kRowThreads, 0, s>>>(gate, vec, ld, P, cols, Npad, KG, ow, B, S, clear);
   };
   auto gemm = [&](const uint8_t* Wm, uint32_t nrows, uint32_t KG, const unsigned long long* ow) {
-    const dim3 grid((nrows + kBM - 1) / kBM, 8 * Npad / kBN);
-    k_bgemm<<<grid, kGemmThreads, gemm_smem, s>>>(gate, Wm, nrows, KG, B, Npad, ow, S);
+    const dim3 grid((nrows + kBM - 1) / kBM, (8 * Npad + kTN - 1) / kTN, splits_for(nrows, KG));
+    k_bgemm<<<grid, kTcThreads, kTcSmem, s>>>(gate, Wm, nrows, KG, B, Npad, ow, S, fault);
   };
   auto epi = [&](BEpiParams p) {
     p.gate = gate;
@@ -799,7 +985,7 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
     unsigned long long* o4 = orw + 4 * l;
     // phases 4-8: attention norm, Q/K/V rows, checked cache stores, rotary
     k_bnorm<<<P, kRowThreads, 0, s>>>(gate, X, XB, Wl.attn_norm, c.dim, o4 + 0);
-    planes(XB, c.dim, c.dim, KGd, o4 + 0);
+    planes(XB, c.dim, c.dim, KGd, o4 + 0, c.dim + 2 * m.kv_dim, KGd);
     gemm(Wl.wqkv, c.dim + 2 * m.kv_dim, KGd, o4 + 0);
     BEpiParams pq = {};
     pq.rows = c.dim + 2 * m.kv_dim;
@@ -830,7 +1016,7 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
     pa.or_out = o4 + 1;
     k_battn<<<dim3(c.heads, P), kRowThreads, battn_smem(m.head_dim, max_positions), s>>>(pa);
     // phases 10-11: output rows and the residual
-    planes(O, c.dim, c.dim, KGd, o4 + 1);
+    planes(O, c.dim, c.dim, KGd, o4 + 1, c.dim, KGd);
     gemm(Wl.wo, c.dim, KGd, o4 + 1);
     BEpiParams po = {};
     po.rows = c.dim;
@@ -841,7 +1027,7 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
     epi(po);
     // phases 12-14: feed-forward norm, gate and up rows, SiLU gating
     k_bnorm<<<P, kRowThreads, 0, s>>>(gate, X, XB, Wl.ffn_norm, c.dim, o4 + 2);
-    planes(XB, c.dim, c.dim, KGd, o4 + 2);
+    planes(XB, c.dim, c.dim, KGd, o4 + 2, 2 * c.hidden, KGd);
     gemm(Wl.w13, 2 * c.hidden, KGd, o4 + 2);
     BEpiParams pg = {};
     pg.rows = 2 * c.hidden;
@@ -854,7 +1040,7 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
     pg.or_out = o4 + 3;
     epi(pg);
     // phases 15-16: down rows and the residual
-    planes(H, c.hidden, c.hidden, KGh, o4 + 3);
+    planes(H, c.hidden, c.hidden, KGh, o4 + 3, c.dim, KGh);
     gemm(Wl.w2, c.dim, KGh, o4 + 3);
     BEpiParams pd = {};
     pd.rows = c.dim;
@@ -868,7 +1054,7 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
     // phases 17-18: final norm and classifier rows (written only for generating rows)
     unsigned long long* of = orw + 4 * c.layers;
     k_bnorm<<<P, kRowThreads, 0, s>>>(gate, X, XB, m.final_norm, c.dim, of);
-    planes(XB, c.dim, c.dim, KGd, of);
+    planes(XB, c.dim, c.dim, KGd, of, c.vocab, KGd);
     gemm(m.cls, c.vocab, KGd, of);
     BEpiParams pc = {};
     pc.rows = c.vocab;
@@ -890,13 +1076,12 @@ bool prefill_supported(const PrefillModel& m, uint32_t cache, size_t smem_optin)
   if (m.cfg.heads % m.cfg.kv_heads) return false;
   if (m.pitch_d > 65536 || m.pitch_h > 65536) return false;               // i32 plane sums
   if (battn_smem(hd, cache) > smem_optin) return false;
-  if ((size_t)kStages * kStageBytesB > smem_optin) return false;
+  if ((size_t)kTcSmem > smem_optin) return false;
   return true;
 }
 
 cudaError_t configure_prefill(size_t smem_optin) {
-  cudaError_t e = cudaFuncSetAttribute(k_bgemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kStages * kStageBytesB);
+  cudaError_t e = cudaFuncSetAttribute(k_bgemm, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(k_battn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_optin);
 }
@@ -922,7 +1107,8 @@ cudaError_t enqueue_prefill(const PrefillModel& m, uint8_t* st, const StateLayou
   if (e != cudaSuccess) return e;
   k_bfinish<<<1, kRowThreads, 0, s>>>(st, reinterpret_cast<const int64_t*>(work + w.X),
                                       reinterpret_cast<int64_t*>(st + lay.x), m.cfg.dim, pos0, P,
-                                      reinterpret_cast<const int32_t*>(work + w.rstat));
+                                      reinterpret_cast<const int32_t*>(work + w.rstat),
+                                      reinterpret_cast<const int*>(work + w.fault));
   return cudaGetLastError();
 }
 
@@ -951,7 +1137,8 @@ cudaError_t enqueue_batch(const PrefillModel& m, const RowDesc* host_rows, uint3
   k_mfinish<<<n, kFinishThreads, 0, s>>>(reinterpret_cast<const RowDesc*>(work + w.rows),
                                          reinterpret_cast<const int64_t*>(work + w.X), m.cfg.dim,
                                          m.cfg.vocab, m.exp_tab,
-                                         reinterpret_cast<const int32_t*>(work + w.rstat));
+                                         reinterpret_cast<const int32_t*>(work + w.rstat),
+                                         reinterpret_cast<const int*>(work + w.fault));
   return cudaGetLastError();
 }
 

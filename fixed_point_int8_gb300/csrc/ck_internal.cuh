@@ -435,6 +435,7 @@ struct PrefillModel {
   const uint8_t* cls;
   const uint32_t* cls_scale;
   const int32_t* final_norm;
+  int num_sms;
 };
 // Device scratch a chunk of up to `cap` positions needs.
 size_t prefill_work_bytes(const PrefillModel& m, uint32_t cap);
