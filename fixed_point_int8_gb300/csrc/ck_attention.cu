@@ -62,8 +62,8 @@ __global__ void __launch_bounds__(kThreads) k_attention(const AttnParams p) {
   for (uint32_t i = tid; i < hd; i += kThreads) q_s[i] = p.q[(size_t)h * hd + i];
   __syncthreads();
 
-  const int32_t* Kh = p.kcache + (size_t)kvh * hd;
-  const int32_t* Vh = p.vcache + (size_t)kvh * hd;
+  const int32_t* Kh = p.kcache + (size_t)kvh * p.cache * hd;  // the head's positions, contiguous
+  const int32_t* Vh = p.vcache + (size_t)kvh * p.cache * hd;
   const uint32_t lpp = hd / 4;       // lanes per position, four elements each
   const uint32_t ppw = 32 / lpp;     // positions per warp step
   const uint32_t sub = lane % lpp, slot = lane / lpp, e0 = sub * 4;
@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kThreads) k_attention(const AttnParams p) {
     const uint32_t tl = base + slot;
     unsigned long long d = 0;
     if (tl < n) {
-      const int4 k4 = *reinterpret_cast<const int4*>(Kh + (size_t)(t0 + tl) * p.kv_dim + e0);
+      const int4 k4 = *reinterpret_cast<const int4*>(Kh + (size_t)(t0 + tl) * hd + e0);
       d = (unsigned long long)q0 * (unsigned long long)(long long)k4.x +
           (unsigned long long)q1 * (unsigned long long)(long long)k4.y +
           (unsigned long long)q2 * (unsigned long long)(long long)k4.z +
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kThreads) k_attention(const AttnParams p) {
   for (uint32_t base = warp * ppw; base < n; base += kWarps * ppw) {
     const uint32_t tl = base + slot;
     if (tl < n) {
-      const int4 v4 = *reinterpret_cast<const int4*>(Vh + (size_t)(t0 + tl) * p.kv_dim + e0);
+      const int4 v4 = *reinterpret_cast<const int4*>(Vh + (size_t)(t0 + tl) * hd + e0);
       const long long pr = sc[tl];
       a0 += (unsigned long long)(pr * (long long)v4.x);
       a1 += (unsigned long long)(pr * (long long)v4.y);

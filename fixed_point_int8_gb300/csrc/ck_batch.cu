@@ -587,16 +587,16 @@ __global__ void __launch_bounds__(kRowThreads) k_bepi(const BEpiParams p) {
         rotate_pair((int64_t)(int32_t)y0, (int64_t)(int32_t)y1, __ldg(cs), __ldg(cs + 1), a2, b2);
         if (!fits_i32(a2)) record_error(st, err_key(pos, p.layer, 8, e));
         if (!fits_i32(b2)) record_error(st, err_key(pos, p.layer, 8, e + 1));
-        int32_t* kc = layer_cache(rd, rd.off_k, p.layer, p.kv_dim) + (size_t)pos * p.kv_dim;
-        kc[e] = (int32_t)a2;
-        kc[e + 1] = (int32_t)b2;
+        int32_t* kc = layer_cache(rd, rd.off_k, p.layer, p.kv_dim);
+        kc[cache_word(e, pos, p.head_dim, rd.cache)] = (int32_t)a2;
+        kc[cache_word(e + 1, pos, p.head_dim, rd.cache)] = (int32_t)b2;
       } else {
         const uint32_t e = r - p.dim - p.kv_dim;
         if (!fits_i32(y0)) record_error(st, err_key(pos, p.layer, 7, e));
         if (!fits_i32(y1)) record_error(st, err_key(pos, p.layer, 7, e + 1));
-        int32_t* vc = layer_cache(rd, rd.off_v, p.layer, p.kv_dim) + (size_t)pos * p.kv_dim;
-        vc[e] = (int32_t)y0;
-        vc[e + 1] = (int32_t)y1;
+        int32_t* vc = layer_cache(rd, rd.off_v, p.layer, p.kv_dim);
+        vc[cache_word(e, pos, p.head_dim, rd.cache)] = (int32_t)y0;
+        vc[cache_word(e + 1, pos, p.head_dim, rd.cache)] = (int32_t)y1;
       }
     }
   }
@@ -638,8 +638,8 @@ __global__ void __launch_bounds__(kRowThreads) k_battn(const BAttnParams p) {
   const uint32_t kvh = h / (p.heads / p.kv_heads);
   for (uint32_t i = tid; i < hd; i += kRowThreads) q_s[i] = p.Q[(size_t)n * p.dim + (size_t)h * hd + i];
   __syncthreads();
-  const int32_t* Kh = layer_cache(rd, rd.off_k, p.layer, p.kv_dim) + (size_t)kvh * hd;
-  const int32_t* Vh = layer_cache(rd, rd.off_v, p.layer, p.kv_dim) + (size_t)kvh * hd;
+  const int32_t* Kh = layer_cache(rd, rd.off_k, p.layer, p.kv_dim) + (size_t)kvh * rd.cache * hd;
+  const int32_t* Vh = layer_cache(rd, rd.off_v, p.layer, p.kv_dim) + (size_t)kvh * rd.cache * hd;
   const uint32_t lpp = hd / 4, ppw = 32 / lpp;  // lanes per position (four elements each)
   const uint32_t sub = lane % lpp, slot = lane / lpp, e0 = sub * 4;
   const int64_t q0 = q_s[e0], q1 = q_s[e0 + 1], q2 = q_s[e0 + 2], q3 = q_s[e0 + 3];
@@ -649,7 +649,7 @@ __global__ void __launch_bounds__(kRowThreads) k_battn(const BAttnParams p) {
     const uint32_t tl = base + slot;
     unsigned long long dsum = 0;
     if (tl < np) {
-      const int4 k4 = *reinterpret_cast<const int4*>(Kh + (size_t)tl * p.kv_dim + e0);
+      const int4 k4 = *reinterpret_cast<const int4*>(Kh + (size_t)tl * hd + e0);
       dsum = (unsigned long long)q0 * (unsigned long long)(long long)k4.x +
              (unsigned long long)q1 * (unsigned long long)(long long)k4.y +
              (unsigned long long)q2 * (unsigned long long)(long long)k4.z +
@@ -695,7 +695,7 @@ __global__ void __launch_bounds__(kRowThreads) k_battn(const BAttnParams p) {
   for (uint32_t base = warp * ppw; base < np; base += kAttnWarps * ppw) {
     const uint32_t tl = base + slot;
     if (tl < np) {
-      const int4 v4 = *reinterpret_cast<const int4*>(Vh + (size_t)tl * p.kv_dim + e0);
+      const int4 v4 = *reinterpret_cast<const int4*>(Vh + (size_t)tl * hd + e0);
       const long long pr = sc[tl];
       a0 += (unsigned long long)(pr * (long long)v4.x);
       a1 += (unsigned long long)(pr * (long long)v4.y);

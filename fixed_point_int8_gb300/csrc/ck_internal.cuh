@@ -168,6 +168,13 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 
 __device__ __forceinline__ bool fits_i32(int64_t v) { return v >= INT32_MIN && v <= INT32_MAX; }
 
+// Word of element e (0 <= e < kv_dim) of position pos's key or value vector in one layer's
+// cache of `cache` positions: head-major, [kv head][position][head element], so one head's
+// keys over all positions are one contiguous run.
+__host__ __device__ inline size_t cache_word(uint32_t e, uint32_t pos, uint32_t hd, uint32_t cache) {
+  return ((size_t)(e / hd) * cache + pos) * hd + e % hd;
+}
+
 // First failing cache store wins: the smallest (position, layer, phase, element) key.
 __device__ __forceinline__ void record_error(uint8_t* st, uint64_t key) {
   atomicMin(reinterpret_cast<unsigned long long*>(st + kHErrKey), (unsigned long long)key);

@@ -157,11 +157,11 @@ __device__ __forceinline__ void epilogue(const MatrowParams& p, uint32_t row, in
       rotate_pair((int64_t)(int32_t)a, (int64_t)(int32_t)b, __ldg(cs), __ldg(cs + 1), a2, b2);
       const int64_t mine = even ? a2 : b2;
       if (!fits_i32(mine)) record_error(p.state, err_key(pos, p.layer, 8, e));
-      p.kcache[(size_t)pos * p.kv_dim + e] = (int32_t)mine;
+      p.kcache[cache_word(e, pos, p.head_dim, p.cache)] = (int32_t)mine;
     } else {
       const uint32_t e = row - p.q_rows - p.kv_dim;
       if (!fits_i32(y)) record_error(p.state, err_key(pos, p.layer, 7, e));
-      p.vcache[(size_t)pos * p.kv_dim + e] = (int32_t)y;
+      p.vcache[cache_word(e, pos, p.head_dim, p.cache)] = (int32_t)y;
     }
   }
 }

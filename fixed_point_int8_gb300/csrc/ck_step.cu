@@ -646,11 +646,11 @@ __device__ __forceinline__ void epilogue(const StepParams& p, const Pos& q, cons
       rotate_pair((int64_t)(int32_t)a, (int64_t)(int32_t)b, rope[2 * j], rope[2 * j + 1], a2, b2);
       const int64_t mine = even ? a2 : b2;
       if (!fits_i32(mine)) record_error(p.st, err_key(q.pos, layer, 8, e));
-      m.kc[(size_t)q.pos * p.kv_dim + e] = (int32_t)mine;
+      m.kc[cache_word(e, q.pos, p.hd, p.cache)] = (int32_t)mine;
     } else {
       const uint32_t e = row - q_rows - p.kv_dim;
       if (!fits_i32(y)) record_error(p.st, err_key(q.pos, layer, 7, e));
-      m.vc[(size_t)q.pos * p.kv_dim + e] = (int32_t)y;
+      m.vc[cache_word(e, q.pos, p.hd, p.cache)] = (int32_t)y;
     }
   }
 }
@@ -894,7 +894,7 @@ __device__ __forceinline__ long long att_scores(const StepParams& p, const int32
 #pragma unroll
     for (int bb = 0; bb < kAB; ++bb) {
       const uint32_t tl = base + (bb * kNCW + warp) * ppw + slot;
-      k4[bb] = tl < n ? *reinterpret_cast<const int4*>(Kh + (size_t)(s0 + tl) * p.kv_dim + e0) : make_int4(0, 0, 0, 0);
+      k4[bb] = tl < n ? *reinterpret_cast<const int4*>(Kh + (size_t)(s0 + tl) * p.hd + e0) : make_int4(0, 0, 0, 0);
     }
     unsigned long long d[kAB];
 #pragma unroll
@@ -937,7 +937,7 @@ __device__ __forceinline__ void att_values(const StepParams& p, const int32_t* V
 #pragma unroll
     for (int bb = 0; bb < kAB; ++bb) {
       const uint32_t tl = base + (bb * kNCW + warp) * ppw + slot;
-      v4[bb] = tl < n ? *reinterpret_cast<const int4*>(Vh + (size_t)(t0 + tl) * p.kv_dim + dlo + e0)
+      v4[bb] = tl < n ? *reinterpret_cast<const int4*>(Vh + (size_t)(t0 + tl) * p.hd + dlo + e0)
                       : make_int4(0, 0, 0, 0);
       pb[bb] = tl < n ? pr[tl] : 0;
     }
@@ -1002,8 +1002,9 @@ __device__ __forceinline__ bool attention(const StepParams& p, const Pos& q, uin
   const uint32_t s0 = full ? 0u : t0, nsc = (full ? P : t1) - s0;
   const uint32_t kvh = h / (p.heads / p.kv_heads);
   const size_t lw = (size_t)p.cache * p.kv_dim;
-  const int32_t* Kh = reinterpret_cast<const int32_t*>(p.st + p.off_k) + l * lw + (size_t)kvh * hd;
-  const int32_t* Vh = reinterpret_cast<const int32_t*>(p.st + p.off_v) + l * lw + (size_t)kvh * hd;
+  // the head's positions are one contiguous run of the head-major cache
+  const int32_t* Kh = reinterpret_cast<const int32_t*>(p.st + p.off_k) + l * lw + (size_t)kvh * p.cache * hd;
+  const int32_t* Vh = reinterpret_cast<const int32_t*>(p.st + p.off_v) + l * lw + (size_t)kvh * p.cache * hd;
   long long* parts = reinterpret_cast<long long*>(q.work + p.off_part) + (size_t)h * gh * 2;  // [gh][2]
   uint32_t* hcount = reinterpret_cast<uint32_t*>(q.work + p.off_hsync) + h;
   const int64_t* qg = st64(p, p.off_q) + (size_t)h * hd;

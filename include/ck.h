@@ -165,7 +165,8 @@ void ck_free_model(ck_model* m);
  *   prompt ids u32[n_prompt], output tokens u32[max_tokens], x (activations) i64[dim],
  *   four working vectors i64[dim] (xb, q, o, y), h i64[hidden], logits i64[vocab],
  *   scores/work i64[max(heads * cache, 1024 * (head + 2) + 2048)],
- *   keys i32[layers][cache][kv_dim], values likewise.
+ *   keys i32[layers][kv_heads][cache][head] (head-major: a head's keys for all positions are
+ *   contiguous), values likewise.
  * The working vectors, h, scores/work and header bytes 128..255 are scratch: their
  * contents between turns are unspecified. */
 #define CK_FLAG_STOP_TOKENS 1u

@@ -22,6 +22,8 @@
  *   r10 Weighted values: the sum over positions first, then one >> 24.
  *   r13 Ties in the maximum pass keep the lowest index.
  *   r17 The first failing cache store, in program order, ends the turn with error 8.
+ *   r23 The cache keeps each key/value head's words for all positions together:
+ *       [layer][kv head][position][head element]; the page fixes no order inside it.
  *   r20 Sampling divides m - l by the temperature into a value with 16 fractional bits,
  *       truncating; the exponential-table index is that value >> 8, capped at 4,096.
  *   r21 The generator state is the seed word (a zero seed stored as its first state); the
@@ -419,8 +421,8 @@ void orc_model_close(orc_model* m) {
  * The ids-mode state of the library header: a 256-byte header, then the buffers, each at
  * a multiple of 256 bytes: prompt ids u32[n_prompt], output tokens u32[max_tokens],
  * x, xb, q, o, y i64[dim], h i64[hidden], logits i64[vocab],
- * scores (work) i64[max(heads*cache, 1024*(head+2)+2048)], K i32[layers*cache*kv_dim],
- * V i32[layers*cache*kv_dim]. */
+ * scores (work) i64[max(heads*cache, 1024*(head+2)+2048)], K i32[layers][kv heads][cache][head],
+ * V i32 likewise (head-major, reading r23). */
 
 enum { H_PHASE = 8, H_POSITION = 12, H_NPROMPT = 16, H_MAXTOK = 20, H_CACHE = 24, H_GENERATED = 28,
        H_FLAGS = 32, H_TEMP = 36, H_ERROR = 40, H_LASTTOK = 44, H_SEED = 48, H_TURNS = 56,
@@ -515,6 +517,13 @@ static uint64_t err_key(uint32_t pos, uint32_t layer, uint32_t phase, uint32_t e
   return ((uint64_t)pos << 44) | ((uint64_t)layer << 32) | ((uint64_t)phase << 24) | elem;
 }
 
+/* Index of element j (0 <= j < kv_dim) of position pos's key or value vector in layer l's
+ * cache: head-major, [layer][kv head][position][head element] (reading r23). */
+static uint64_t cache_index(uint32_t l, uint32_t cache, uint32_t pos, uint32_t j, uint32_t hd,
+                            uint32_t kvd) {
+  return (uint64_t)l * cache * kvd + ((uint64_t)(j / hd) * cache + pos) * hd + j % hd;
+}
+
 /* One position, phases 3 to 16 for every layer, then 17 to 19 where a token is generated
  * ("The forward pass, in order").  Returns 0, or 8 at the first store that does not fit. */
 static int run_position(const orc_model* m, uint8_t* st, const orc_layout* L) {
@@ -543,20 +552,20 @@ static int run_position(const orc_model* m, uint8_t* st, const orc_layout* L) {
 
   for (uint32_t l = 0; l < m->layers && !rc; ++l) {
     const orc_layer* W = &m->layer[l];
-    int32_t* Kl = Kc + ((uint64_t)l * cache + pos) * kvd;
-    int32_t* Vl = Vc + ((uint64_t)l * cache + pos) * kvd;
+    /* element j of this position's key or value vector (reading r23: head-major cache) */
+#define KV_AT(C, j) ((C)[cache_index(l, cache, pos, (j), hd, kvd)])
     orc_rmsnorm(x, W->attn_norm, d, xb);                               /* phase 4 */
     orc_matrow(W->wq, d, W->sq, d, d, xb, q);                          /* phase 5 */
     orc_matrow(W->wk, d, W->sk, kvd, d, xb, kv);                       /* phase 6 */
     for (uint32_t j = 0; j < kvd && !rc; ++j) {
       if (!orc_fits32(kv[j])) { rc = 8; wr64(st + H_ERRKEY, err_key(pos, l, 6, j)); }
-      else Kl[j] = (int32_t)kv[j];
+      else KV_AT(Kc, j) = (int32_t)kv[j];
     }
     if (rc) break;
     orc_matrow(W->wv, d, W->sv, kvd, d, xb, kv);                       /* phase 7 */
     for (uint32_t j = 0; j < kvd && !rc; ++j) {
       if (!orc_fits32(kv[j])) { rc = 8; wr64(st + H_ERRKEY, err_key(pos, l, 7, j)); }
-      else Vl[j] = (int32_t)kv[j];
+      else KV_AT(Vc, j) = (int32_t)kv[j];
     }
     if (rc) break;
     const int32_t* rope = m->rope + (uint64_t)pos * hd;                /* phase 8 */
@@ -567,21 +576,22 @@ static int run_position(const orc_model* m, uint8_t* st, const orc_layout* L) {
     for (uint32_t i = 0; i < kvd && !rc; i += 2) {
       uint32_t j = (i % hd) / 2;
       int64_t a2, b2;
-      orc_rotate(Kl[i], Kl[i + 1], rope[2 * j], rope[2 * j + 1], &a2, &b2);
+      orc_rotate(KV_AT(Kc, i), KV_AT(Kc, i + 1), rope[2 * j], rope[2 * j + 1], &a2, &b2);
       if (!orc_fits32(a2)) { rc = 8; wr64(st + H_ERRKEY, err_key(pos, l, 8, i)); break; }
-      Kl[i] = (int32_t)a2;
+      KV_AT(Kc, i) = (int32_t)a2;
       if (!orc_fits32(b2)) { rc = 8; wr64(st + H_ERRKEY, err_key(pos, l, 8, i + 1)); break; }
-      Kl[i + 1] = (int32_t)b2;
+      KV_AT(Kc, i + 1) = (int32_t)b2;
     }
     if (rc) break;
     const uint32_t group = m->heads / m->kv_heads;                     /* phase 9 */
     for (uint32_t hh_ = 0; hh_ < m->heads; ++hh_) {
       uint32_t kvh = hh_ / group;
-      const int32_t* K0 = Kc + (uint64_t)l * cache * kvd + (uint64_t)kvh * hd;
-      const int32_t* V0 = Vc + (uint64_t)l * cache * kvd + (uint64_t)kvh * hd;
-      orc_attention_head(q + (uint64_t)hh_ * hd, K0, V0, kvd, pos + 1, hd, m->inv_sqrt, m->exp_tab,
+      const int32_t* K0 = Kc + cache_index(l, cache, 0, kvh * hd, hd, kvd);
+      const int32_t* V0 = Vc + cache_index(l, cache, 0, kvh * hd, hd, kvd);
+      orc_attention_head(q + (uint64_t)hh_ * hd, K0, V0, hd, pos + 1, hd, m->inv_sqrt, m->exp_tab,
                          scores + (uint64_t)hh_ * cache, o + (uint64_t)hh_ * hd);
     }
+#undef KV_AT
     orc_matrow(W->wo, d, W->so, d, d, o, y);                           /* phase 10 */
     residual(x, y, d);                                                 /* phase 11 */
     orc_rmsnorm(x, W->ffn_norm, d, xb);

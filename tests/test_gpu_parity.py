@@ -563,20 +563,21 @@ def _prefill_sampled(ck, spec, n_prompt, samples, chunk=256):
     assert rc == 0 and res["work"] == n_prompt - 1
     got = ck.state_download(sg)
     lay = P.orc.layout(n_prompt, 2)
-    cache, kvd = n_prompt + 1, spec.kv_dim
+    cache, hd = n_prompt + 1, spec.head_dim
     for p in samples:
         host = got.copy()
         host[oracle.H_POSITION:oracle.H_POSITION + 4] = np.array([p], "<u4").view(np.uint8)
         words = []
         for name in ("k", "v"):
             for l in range(spec.layers):
-                o = lay[name] + 4 * ((l * cache + p) * kvd)
-                host[o:o + 4 * kvd] = 0
-                words.append((name, l, o))
+                for kvh in range(spec.kv_heads):  # head-major: [layer][kv head][position][element]
+                    o = lay[name] + 4 * (((l * spec.kv_heads + kvh) * cache + p) * hd)
+                    host[o:o + 4 * hd] = 0
+                    words.append((name, l, o))
         rco, reso = P.orc.turn(host, 1)
         assert rco == 0 and reso["work"] == 1
         for name, l, o in words:
-            a, b = host[o:o + 4 * kvd], got[o:o + 4 * kvd]
+            a, b = host[o:o + 4 * hd], got[o:o + 4 * hd]
             assert np.array_equal(a, b), (spec.name, p, name, l, np.flatnonzero(a != b)[:8])
         if p == n_prompt - 2:
             d = spec.dim

@@ -70,11 +70,13 @@ def test_position_zero_attention_returns_the_value_row(name):
     assert rc == 0 and res["work"] == 1
     cache = wl.n_prompt + wl.steps - 1
     o = _buf(m, st, wl, "o", "<i8", spec.dim)
-    V = _buf(m, st, wl, "v", "<i4", spec.layers * cache * spec.kv_dim).reshape(spec.layers, cache, spec.kv_dim)
     hd, group = spec.head_dim, spec.heads // spec.kv_heads
+    # the cache is head-major: [layer][kv head][position][head element]
+    V = _buf(m, st, wl, "v", "<i4", spec.layers * cache * spec.kv_dim).reshape(
+        spec.layers, spec.kv_heads, cache, hd)
     for h in range(spec.heads):
         kvh = h // group
-        assert o[h * hd:(h + 1) * hd].tolist() == V[-1, 0, kvh * hd:(kvh + 1) * hd].astype(np.int64).tolist()
+        assert o[h * hd:(h + 1) * hd].tolist() == V[-1, kvh, 0].astype(np.int64).tolist()
 
 
 def test_turn_split_invariance(tiny_ws):
