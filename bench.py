@@ -19,7 +19,9 @@ Prints one JSON line:
   prefill    the 127 prompt positions of the workload, layer-major (device-timed);
   batched_runs  the 1B-shaped model with 64 independent runs (64 prompt ids each, prefilled
              per run), generating positions of all 64 advanced together per ck_turn_batch
-             pass, device-timed over --batched-passes passes.
+             pass, device-timed over --batched-passes passes;
+  long_context  the 1B-shaped model at 8,192 context: 7,936 prompt ids prefilled layer-major,
+             then --long-steps generating positions (~position 7,940), device-timed.
 ``--impl reference`` times the CPU oracle alone on the same workload and metric.
 """
 from __future__ import annotations
@@ -220,6 +222,11 @@ def run_ours(args):
         # profiling aid: only the 64-run batched measurement
         print(json.dumps({"batched_runs": batched_runs(ck, torch, synth, args.batched_passes)}), flush=True)
         return
+    if args.long_only:
+        # profiling aid: only the long-context measurement (optionally cut to fewer layers)
+        print(json.dumps({"long_context": long_context(ck, torch, synth, args.long_steps, args.long_layers)}),
+              flush=True)
+        return
     if args.matrow_only:
         # profiling aid: only the matrix-row timing of one shape, e.g. 22016x4096
         rows, cols = (int(v) for v in args.matrow_only.split("x"))
@@ -321,10 +328,15 @@ def run_ours(args):
     if snapshot is not None:
         cpu, bitexact = cpu_baseline(art, snapshot, toks, args.cpu_seconds)
     batched = None
-    if args.batched_passes and rank == 0:
+    longc = None
+    if (args.batched_passes or args.long_steps) and rank == 0:
         del model, state
         torch.cuda.empty_cache()
-        batched = batched_runs(ck, torch, synth, args.batched_passes)
+        if args.batched_passes:
+            batched = batched_runs(ck, torch, synth, args.batched_passes)
+            torch.cuda.empty_cache()
+        if args.long_steps:
+            longc = long_context(ck, torch, synth, args.long_steps, 0)
 
     if rank != 0:
         return
@@ -369,6 +381,7 @@ def run_ours(args):
                     "how": "one ck_turn over the prompt positions that generate no token: layer-major "
                            "chunks, byte-plane f16 MMA contraction (CUDA events on the stream)"},
         "batched_runs": batched,
+        "long_context": longc,
         "path": kernel_path,
         "setup_s": round(setup_s, 1),
     }
@@ -420,6 +433,45 @@ def batched_runs(ck, torch, synth, passes):
             "algorithmic_frac_of_bf16_peak": round(tflops / peak, 4) if peak else None,
             "note": "whole pass (all kernels); algorithmic = 2 x weights x runs per pass, the byte "
                     "planes multiply the tensor work by the plane count (3 here)"}
+
+
+def long_context(ck, torch, synth, steps, layers):
+    """The 1B-shaped model at 8,192 context: 7,936 prompt ids prefilled layer-major (one
+    ck_turn), then `steps` generating positions in one ck_turn, both device-timed."""
+    import dataclasses
+    wl = synth.WORKLOADS["1b_long"]
+    spec = wl.spec if not layers else dataclasses.replace(wl.spec, layers=layers)
+    steps = max(1, min(steps, wl.steps - 4))
+    rc, m = ck.Model.load(synth.build_artifact(spec))
+    assert rc == 0
+    st = m.new_state(wl.n_prompt, wl.steps)
+    assert m.init_state(st, synth.prompt_ids(spec, wl.n_prompt), wl.steps) == 0
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    rc, res = m.turn(st, wl.n_prompt - 1)
+    ev[1].record(stream)
+    assert rc == 0 and res["work"] == wl.n_prompt - 1
+    rc, res = m.turn(st, 3)  # the first generating positions, untimed
+    assert rc == 0
+    ev[2].record(stream)
+    rc, res = m.turn(st, steps)
+    ev[3].record(stream)
+    torch.cuda.synchronize()
+    assert rc == 0 and res["work"] == steps
+    pre_ms, dec_ms = ev[0].elapsed_time(ev[1]), ev[2].elapsed_time(ev[3])
+    pos = wl.n_prompt + 2
+    kv = spec.layers * (pos + steps // 2 + 1) * spec.kv_dim * 4 * 2
+    per_token = spec.weight_bytes_per_token() + kv
+    return {"decode": {"value": round(steps / (dec_ms * 1e-3), 1), "unit": "tokens/s",
+                       "positions": f"{pos}..{pos + steps - 1}",
+                       "bytes_per_token": per_token,
+                       "achieved_gbs": round(per_token / (dec_ms * 1e-3 / steps) / 1e9, 1)},
+            "prefill": {"value": round((wl.n_prompt - 1) / (pre_ms * 1e-3), 1), "unit": "prompt positions/s",
+                        "positions": wl.n_prompt - 1, "ms": round(pre_ms, 1)},
+            "workload": f"1b_shape{' cut to %d layers' % layers if layers else ''}, context 8192, "
+                        f"{wl.n_prompt} prompt ids, greedy"}
 
 
 def time_matrow(ck, torch, rows, cols, iters):
@@ -560,6 +612,12 @@ def main():
                     help="passes of the 64-run batched measurement (0: skip it)")
     ap.add_argument("--batched-only", action="store_true",
                     help="profiling aid: run only the 64-run batched measurement")
+    ap.add_argument("--long-steps", type=int, default=40,
+                    help="generating positions of the 8K-context measurement (0: skip it)")
+    ap.add_argument("--long-only", action="store_true",
+                    help="profiling aid: run only the 8K-context measurement")
+    ap.add_argument("--long-layers", type=int, default=0,
+                    help="profiling aid: cut the 8K-context model to this many layers")
     ap.add_argument("--path", choices=("auto", "step", "kernels"), default="auto",
                     help="one persistent kernel per position (step) or one kernel per phase")
     ap.add_argument("--prompt-ids", type=int, default=128,
