@@ -621,9 +621,38 @@ size_t battn_smem(uint32_t hd, uint32_t positions) {
   return 8 * ((size_t)hd * (1 + kAttnWarps) + kAttnWarps + positions);
 }
 
+constexpr int kAttnBatch = 8;  // positions a lane group loads at once
+
+// Division of a u64 by an invariant divisor 1 <= d < 2^64 (Granlund and Montgomery,
+// "Division by Invariant Integers using Multiplication", PLDI 1994, unsigned case with
+// N = 64): l = ceil(log2 d), m = floor(2^64 (2^l - d) / d) + 1,
+// q = (t + ((n - t) >> min(l, 1))) >> max(l - 1, 0) with t = mulhi(m, n).
+struct InvDiv64 {
+  unsigned long long m;
+  uint32_t sh1, sh2;
+};
+__device__ InvDiv64 make_invdiv64(unsigned long long d) {
+  uint32_t l = 0;
+  while (l < 64 && (l == 64 ? false : (1ull << l) < d)) ++l;
+  const unsigned __int128 two_l = (unsigned __int128)1 << l;
+  const unsigned __int128 num = (two_l - d) << 64;
+  InvDiv64 D;
+  D.m = (unsigned long long)(num / d) + 1;
+  D.sh1 = l < 1 ? l : 1;
+  D.sh2 = l > 0 ? l - 1 : 0;
+  return D;
+}
+__device__ __forceinline__ unsigned long long udiv64(unsigned long long n, const InvDiv64& D) {
+  const unsigned long long t = __umul64hi(D.m, n);
+  return (t + ((n - t) >> D.sh1)) >> D.sh2;
+}
+
 // Phase 9 for row blockIdx.y and head blockIdx.x ("Attention, stage by stage"), over its
 // run's cache positions 0 .. pos: scores and their maximum, exponentials and their sum,
-// probabilities with 24 fraction bits, and the weighted values with one >> 24.
+// probabilities with 24 fraction bits, and the weighted values with one >> 24.  Each lane
+// group loads kAttnBatch positions a round.  When every query element fits 32 signed bits,
+// each product q * k is exact in one 32 x 32 -> 64-bit multiply-add (the same low 64 bits
+// as the wrapping product), and so is every P * v (P <= 2^24).
 __global__ void __launch_bounds__(kRowThreads) k_battn(const BAttnParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   if (!running(p.gate)) return;
@@ -636,31 +665,54 @@ __global__ void __launch_bounds__(kRowThreads) k_battn(const BAttnParams p) {
   long long* red = reinterpret_cast<long long*>(part + (size_t)kAttnWarps * hd);
   long long* sc = red + kAttnWarps;                                            // [np]
   const uint32_t kvh = h / (p.heads / p.kv_heads);
-  for (uint32_t i = tid; i < hd; i += kRowThreads) q_s[i] = p.Q[(size_t)n * p.dim + (size_t)h * hd + i];
-  __syncthreads();
+  int wide = 0;
+  for (uint32_t i = tid; i < hd; i += kRowThreads) {
+    const int64_t v = p.Q[(size_t)n * p.dim + (size_t)h * hd + i];
+    q_s[i] = v;
+    wide |= ((v ^ (v >> 63)) >> 31) != 0;
+  }
+  const bool q32 = !__syncthreads_or(wide);
   const int32_t* Kh = layer_cache(rd, rd.off_k, p.layer, p.kv_dim) + (size_t)kvh * rd.cache * hd;
   const int32_t* Vh = layer_cache(rd, rd.off_v, p.layer, p.kv_dim) + (size_t)kvh * rd.cache * hd;
   const uint32_t lpp = hd / 4, ppw = 32 / lpp;  // lanes per position (four elements each)
   const uint32_t sub = lane % lpp, slot = lane / lpp, e0 = sub * 4;
   const int64_t q0 = q_s[e0], q1 = q_s[e0 + 1], q2 = q_s[e0 + 2], q3 = q_s[e0 + 3];
+  const int32_t n0 = (int32_t)q0, n1 = (int32_t)q1, n2 = (int32_t)q2, n3 = (int32_t)q3;
+  const uint32_t round = kAttnWarps * ppw * kAttnBatch;
 
   long long lmax = LLONG_MIN;
-  for (uint32_t base = warp * ppw; base < np; base += kAttnWarps * ppw) {
-    const uint32_t tl = base + slot;
-    unsigned long long dsum = 0;
-    if (tl < np) {
-      const int4 k4 = *reinterpret_cast<const int4*>(Kh + (size_t)tl * hd + e0);
-      dsum = (unsigned long long)q0 * (unsigned long long)(long long)k4.x +
-             (unsigned long long)q1 * (unsigned long long)(long long)k4.y +
-             (unsigned long long)q2 * (unsigned long long)(long long)k4.z +
-             (unsigned long long)q3 * (unsigned long long)(long long)k4.w;
+  for (uint32_t base = 0; base < np; base += round) {
+    int4 k4[kAttnBatch];
+#pragma unroll
+    for (int bb = 0; bb < kAttnBatch; ++bb) {
+      const uint32_t tl = base + (bb * kAttnWarps + warp) * ppw + slot;
+      k4[bb] = tl < np ? *reinterpret_cast<const int4*>(Kh + (size_t)tl * hd + e0) : make_int4(0, 0, 0, 0);
     }
-    for (uint32_t o = lpp >> 1; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
-    if (tl < np && sub == 0) {
-      long long s = (long long)dsum >> 16;
-      s = (long long)((unsigned long long)s * (unsigned long long)p.inv_sqrt) >> 24;
-      sc[tl] = s;
-      lmax = s > lmax ? s : lmax;
+    unsigned long long d[kAttnBatch];
+#pragma unroll
+    for (int bb = 0; bb < kAttnBatch; ++bb) {
+      if (q32)
+        d[bb] = (unsigned long long)((long long)n0 * k4[bb].x) + (unsigned long long)((long long)n1 * k4[bb].y) +
+                (unsigned long long)((long long)n2 * k4[bb].z) + (unsigned long long)((long long)n3 * k4[bb].w);
+      else
+        d[bb] = (unsigned long long)q0 * (unsigned long long)(long long)k4[bb].x +
+                (unsigned long long)q1 * (unsigned long long)(long long)k4[bb].y +
+                (unsigned long long)q2 * (unsigned long long)(long long)k4[bb].z +
+                (unsigned long long)q3 * (unsigned long long)(long long)k4[bb].w;
+    }
+    for (uint32_t o = lpp >> 1; o > 0; o >>= 1) {
+#pragma unroll
+      for (int bb = 0; bb < kAttnBatch; ++bb) d[bb] += __shfl_xor_sync(0xffffffffu, d[bb], o);
+    }
+#pragma unroll
+    for (int bb = 0; bb < kAttnBatch; ++bb) {
+      const uint32_t tl = base + (bb * kAttnWarps + warp) * ppw + slot;
+      if (tl < np && sub == 0) {
+        long long sv = (long long)d[bb] >> 16;
+        sv = (long long)((unsigned long long)sv * (unsigned long long)p.inv_sqrt) >> 24;
+        sc[tl] = sv;
+        lmax = sv > lmax ? sv : lmax;
+      }
     }
   }
 #pragma unroll
@@ -687,20 +739,30 @@ __global__ void __launch_bounds__(kRowThreads) k_battn(const BAttnParams p) {
   __syncthreads();
   unsigned long long Z = 0;
   for (int w = 0; w < kAttnWarps; ++w) Z += (unsigned long long)red[w];
+  __shared__ InvDiv64 divz;
+  if (tid == 0) divz = make_invdiv64(Z);  // Z >= EXP[0] > 0: the largest score adds 2^30
+  __syncthreads();
+  const InvDiv64 DZ = divz;
   for (uint32_t tl = tid; tl < np; tl += kRowThreads)
-    sc[tl] = (long long)(((unsigned long long)sc[tl] << 24) / Z);
+    sc[tl] = (long long)udiv64((unsigned long long)sc[tl] << 24, DZ);
   __syncthreads();
 
   unsigned long long a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-  for (uint32_t base = warp * ppw; base < np; base += kAttnWarps * ppw) {
-    const uint32_t tl = base + slot;
-    if (tl < np) {
-      const int4 v4 = *reinterpret_cast<const int4*>(Vh + (size_t)tl * hd + e0);
-      const long long pr = sc[tl];
-      a0 += (unsigned long long)(pr * (long long)v4.x);
-      a1 += (unsigned long long)(pr * (long long)v4.y);
-      a2 += (unsigned long long)(pr * (long long)v4.z);
-      a3 += (unsigned long long)(pr * (long long)v4.w);
+  for (uint32_t base = 0; base < np; base += round) {
+    int4 v4[kAttnBatch];
+    int32_t pb[kAttnBatch];
+#pragma unroll
+    for (int bb = 0; bb < kAttnBatch; ++bb) {
+      const uint32_t tl = base + (bb * kAttnWarps + warp) * ppw + slot;
+      v4[bb] = tl < np ? *reinterpret_cast<const int4*>(Vh + (size_t)tl * hd + e0) : make_int4(0, 0, 0, 0);
+      pb[bb] = tl < np ? (int32_t)sc[tl] : 0;  // P <= 2^24
+    }
+#pragma unroll
+    for (int bb = 0; bb < kAttnBatch; ++bb) {
+      a0 += (unsigned long long)((long long)pb[bb] * v4[bb].x);
+      a1 += (unsigned long long)((long long)pb[bb] * v4[bb].y);
+      a2 += (unsigned long long)((long long)pb[bb] * v4[bb].z);
+      a3 += (unsigned long long)((long long)pb[bb] * v4[bb].w);
     }
   }
   for (uint32_t o = 16; o >= lpp && o > 0; o >>= 1) {
@@ -1066,6 +1128,13 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
   return cudaGetLastError();
 }
 
+// The attention kernel's dynamic shared memory may use what its static variables leave.
+size_t battn_dynamic_max(size_t smem_optin) {
+  cudaFuncAttributes a;
+  if (cudaFuncGetAttributes(&a, k_battn) != cudaSuccess) return 0;
+  return smem_optin > a.sharedSizeBytes ? smem_optin - a.sharedSizeBytes : 0;
+}
+
 }  // namespace
 
 size_t prefill_work_bytes(const PrefillModel& m, uint32_t cap) { return work_layout(m, cap).size; }
@@ -1075,7 +1144,7 @@ bool prefill_supported(const PrefillModel& m, uint32_t cache, size_t smem_optin)
   if (hd % 4 || hd > 128 || hd < 4 || (32 % (hd / 4)) != 0) return false;  // attention lane layout
   if (m.cfg.heads % m.cfg.kv_heads) return false;
   if (m.pitch_d > 65536 || m.pitch_h > 65536) return false;               // i32 plane sums
-  if (battn_smem(hd, cache) > smem_optin) return false;
+  if (battn_smem(hd, cache) > battn_dynamic_max(smem_optin)) return false;
   if ((size_t)kTcSmem > smem_optin) return false;
   return true;
 }
@@ -1083,7 +1152,8 @@ bool prefill_supported(const PrefillModel& m, uint32_t cache, size_t smem_optin)
 cudaError_t configure_prefill(size_t smem_optin) {
   cudaError_t e = cudaFuncSetAttribute(k_bgemm, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_battn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_optin);
+  return cudaFuncSetAttribute(k_battn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)battn_dynamic_max(smem_optin));
 }
 
 cudaError_t enqueue_prefill(const PrefillModel& m, uint8_t* st, const StateLayout& lay, uint32_t pos0,
