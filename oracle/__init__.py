@@ -8,7 +8,8 @@ It imports nothing from the GPU library and the library imports nothing from it.
 Pin status (each function is checked in ``tests/test_oracle_pins.py`` against values the
 page fixes, closed forms, textbook routines or brute force):
   isqrt, embed, rmsnorm, matrow, fits32, rotate, attention_head, silu, silu_gate, argmax,
-  xorshift_next, sample_index, draw_walk, sample, page_state_size: pinned.
+  xorshift_next, sample_index, draw_walk, sample, page_state_size, Vocab (tokenizer phases
+  0 to 2 and token text): pinned.
   Whole-model token streams: parity unpinned against curta-core itself (the page prints no
   tokens or logits for a model); pinned only through the per-step pins and invariants.
 """
@@ -86,6 +87,11 @@ def _lib_():
             "orc_events_reset": ([ctypes.c_int], None),
             "orc_events_get": ([vp], None),
             "orc_threads": ([], ctypes.c_int),
+            "orc_vocab_open": ([vp, u64, u32, ctypes.POINTER(vp)], ctypes.c_int),
+            "orc_vocab_close": ([vp], None),
+            "orc_vocab_lookup": ([vp, vp, u32], i64),
+            "orc_encode": ([vp, vp, u32, vp, u32, ctypes.POINTER(u32)], ctypes.c_int),
+            "orc_decode_piece": ([vp, u32, u32, vp, u32], u32),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -264,6 +270,52 @@ class Model:
         res = TurnResult()
         rc = _lib_().orc_turn(self._h, state.ctypes.data, state.size, n_positions, ctypes.byref(res))
         return rc, res.as_dict()
+
+
+class Vocab:
+    """A tokenizer vocabulary (llama2.c's tokenizer file layout) of n tokens."""
+
+    def __init__(self, blob: bytes, n: int):
+        self.blob = np.frombuffer(bytes(blob), dtype=np.uint8).copy()
+        h = ctypes.c_void_p()
+        rc = _lib_().orc_vocab_open(self.blob.ctypes.data, self.blob.size, n, ctypes.byref(h))
+        if rc:
+            raise ValueError(f"oracle: vocabulary rejected with error {rc}")
+        self._h = h
+        self.n = n
+
+    def __del__(self):
+        try:
+            if self._h:
+                _lib_().orc_vocab_close(self._h)
+        except Exception:
+            pass
+
+    def lookup(self, s: bytes) -> int:
+        b = np.frombuffer(bytes(s) or b"\0", dtype=np.uint8)
+        return int(_lib_().orc_vocab_lookup(self._h, b.ctypes.data, len(s)))
+
+    def encode(self, text: bytes):
+        """Phases 0 to 2.  Returns (rc, ids)."""
+        t = np.frombuffer(bytes(text) or b"\0", dtype=np.uint8)
+        cap = len(text) + 2
+        ids = np.zeros(cap, dtype=np.uint32)
+        n = ctypes.c_uint32()
+        rc = _lib_().orc_encode(self._h, t.ctypes.data, len(text), ids.ctypes.data, cap, ctypes.byref(n))
+        return rc, ids[:n.value].tolist() if rc == 0 else []
+
+    def piece(self, prev: int, tok: int) -> bytes:
+        out = np.zeros(1024, dtype=np.uint8)
+        n = _lib_().orc_decode_piece(self._h, prev, tok, out.ctypes.data, out.size)
+        return out[:n].tobytes()
+
+    def decode(self, ids, prev: int = 0) -> bytes:
+        """The text of the tokens ids, each after the one before it (prev before the first)."""
+        out = b""
+        for t in ids:
+            out += self.piece(prev, int(t))
+            prev = int(t)
+        return out
 
 
 def header(state: np.ndarray) -> dict:

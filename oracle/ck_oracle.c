@@ -1,8 +1,8 @@
 /* ORACLE — test infrastructure, not part of the product.
  *
  * A plain, slow, obviously correct CPU restatement of curta-core's integer forward pass
- * (phases 3 to 19, sampling at temperature zero and above), written from the page "The
- * inference core"
+ * (phases 3 to 19, sampling at temperature zero and above, and the tokenizer of phases 0
+ * to 2 with the text of generated tokens), written from the page "The inference core"
  * (curta.chat docs).  Only the tests, the smoke check and the benchmark's CPU-baseline leg
  * may load it.  It shares no code with the GPU library: it parses the model artifact and
  * the state layout itself, from the format description.
@@ -22,6 +22,8 @@
  *   r10 Weighted values: the sum over positions first, then one >> 24.
  *   r13 Ties in the maximum pass keep the lowest index.
  *   r17 The first failing cache store, in program order, ends the turn with error 8.
+ *   r24 Merges of equal score: the leftmost pair merges.
+ *   r25 The merge scan looks up every adjacent pair, the opening token's included.
  *   r23 The cache keeps each key/value head's words for all positions together:
  *       [layer][kv head][position][head element]; the page fixes no order inside it.
  *   r20 Sampling divides m - l by the temperature into a value with 16 fractional bits,
@@ -683,4 +685,195 @@ void orc_state_layout(const orc_model* m, uint32_t n_prompt, uint32_t max_tokens
   model_cfg(m, cfg);
   orc_layout L = layout_of(cfg, n_prompt, max_tokens);
   memcpy(out13, &L, sizeof(L));
+}
+
+/* ------------------------------------------------------------------ tokenizer
+ * "The forward pass, in order", phases 0 to 2, and the text of a generated token
+ * ("Sampling", last paragraph), over a vocabulary in llama2.c's tokenizer file layout:
+ * u32 longest token length, then per token f32 score, i32 byte length, the bytes.
+ * Readings: r24 ties between merges of equal score go to the leftmost pair; r25 every
+ * adjacent pair is looked up, the opening token's included. */
+
+typedef struct {
+  uint32_t n, max_len;
+  float* score;
+  uint32_t* len;
+  const uint8_t** str;
+  uint32_t* sorted; /* token ids in byte-string order, for the binary search */
+  uint8_t* blob;
+} orc_vocab;
+
+static int bytes_cmp(const uint8_t* a, uint32_t la, const uint8_t* b, uint32_t lb) {
+  uint32_t m = la < lb ? la : lb;
+  int c = memcmp(a, b, m);
+  if (c) return c;
+  return la < lb ? -1 : la > lb ? 1 : 0;
+}
+
+static const orc_vocab* g_sort_vocab;
+static int sort_cmp(const void* x, const void* y) {
+  uint32_t a = *(const uint32_t*)x, b = *(const uint32_t*)y;
+  const orc_vocab* v = g_sort_vocab;
+  return bytes_cmp(v->str[a], v->len[a], v->str[b], v->len[b]);
+}
+
+/* Opens a vocabulary of n tokens.  Returns 0, or 2 for a blob that does not hold them. */
+int orc_vocab_open(const uint8_t* blob, uint64_t blob_len, uint32_t n, orc_vocab** out) {
+  *out = NULL;
+  if (blob_len < 4 || n == 0) return 2;
+  orc_vocab* v = (orc_vocab*)calloc(1, sizeof(orc_vocab));
+  v->n = n;
+  v->blob = (uint8_t*)malloc(blob_len);
+  memcpy(v->blob, blob, blob_len);
+  v->score = (float*)malloc(4ull * n);
+  v->len = (uint32_t*)malloc(4ull * n);
+  v->str = (const uint8_t**)malloc(sizeof(uint8_t*) * n);
+  v->sorted = (uint32_t*)malloc(4ull * n);
+  uint64_t off = 4;
+  for (uint32_t i = 0; i < n; ++i) {
+    int32_t l;
+    if (off + 8 > blob_len) goto bad;
+    memcpy(&v->score[i], v->blob + off, 4);
+    memcpy(&l, v->blob + off + 4, 4);
+    off += 8;
+    if (l < 0 || off + (uint64_t)l > blob_len) goto bad;
+    v->len[i] = (uint32_t)l;
+    if ((uint32_t)l > v->max_len) v->max_len = (uint32_t)l;
+    v->str[i] = v->blob + off;
+    off += (uint64_t)l;
+    v->sorted[i] = i;
+  }
+  g_sort_vocab = v;
+  qsort(v->sorted, n, 4, sort_cmp);
+  *out = v;
+  return 0;
+bad:
+  free(v->blob); free(v->score); free(v->len); free(v->str); free(v->sorted); free(v);
+  return 2;
+}
+
+void orc_vocab_close(orc_vocab* v) {
+  if (!v) return;
+  free(v->blob); free(v->score); free(v->len); free(v->str); free(v->sorted); free(v);
+}
+
+/* "A lookup is a binary search over the sorted token ids": the id of the token whose
+ * bytes are s, or -1. */
+int64_t orc_vocab_lookup(const orc_vocab* v, const uint8_t* s, uint32_t len) {
+  uint32_t lo = 0, hi = v->n;
+  while (lo < hi) {
+    uint32_t mid = (lo + hi) / 2, t = v->sorted[mid];
+    int c = bytes_cmp(v->str[t], v->len[t], s, len);
+    if (c == 0) return t;
+    if (c < 0) lo = mid + 1; else hi = mid;
+  }
+  return -1;
+}
+
+/* Byte length of the UTF-8 character starting at s (at most left bytes), 0 if not a valid
+ * character (bad lead byte, truncated, bad continuation, overlong or surrogate). */
+static uint32_t utf8_char(const uint8_t* s, uint32_t left) {
+  uint8_t c = s[0];
+  uint32_t n;
+  uint32_t cp;
+  if (c < 0x80) return 1;
+  if ((c & 0xE0) == 0xC0) { n = 2; cp = c & 0x1F; }
+  else if ((c & 0xF0) == 0xE0) { n = 3; cp = c & 0x0F; }
+  else if ((c & 0xF8) == 0xF0) { n = 4; cp = c & 0x07; }
+  else return 0;
+  if (n > left) return 0;
+  for (uint32_t i = 1; i < n; ++i) {
+    if ((s[i] & 0xC0) != 0x80) return 0;
+    cp = (cp << 6) | (s[i] & 0x3F);
+  }
+  if ((n == 2 && cp < 0x80) || (n == 3 && cp < 0x800) || (n == 4 && cp < 0x10000)) return 0;
+  if (cp > 0x10FFFF || (cp >= 0xD800 && cp <= 0xDFFF)) return 0;
+  return n;
+}
+
+/* Phases 0 to 2 on a prompt of len bytes: the opening token 1, the token of a single space
+ * when the prompt has text, one token per character (or per byte, id byte + 3, for a
+ * character with no token), then the merges.  Writes at most cap ids.  Returns 0, 6 for a
+ * prompt over 1,024 bytes, with a zero byte or not UTF-8, or 4 when cap is too small. */
+int orc_encode(const orc_vocab* v, const uint8_t* text, uint32_t len, uint32_t* ids, uint32_t cap,
+               uint32_t* n_out) {
+  *n_out = 0;
+  if (len > 1024) return 6;
+  for (uint32_t i = 0; i < len;) {
+    if (text[i] == 0) return 6;
+    uint32_t k = utf8_char(text + i, len - i);
+    if (!k) return 6;
+    i += k;
+  }
+  uint32_t* t = (uint32_t*)malloc(4ull * (len + 2));
+  uint32_t n = 0;
+  t[n++] = 1;                                                  /* phase 0 */
+  if (len) {
+    const uint8_t sp = ' ';
+    int64_t id = orc_vocab_lookup(v, &sp, 1);
+    t[n++] = id >= 0 ? (uint32_t)id : (uint32_t)sp + 3;
+  }
+  for (uint32_t i = 0; i < len;) {                             /* phase 1 */
+    uint32_t k = utf8_char(text + i, len - i);
+    int64_t id = orc_vocab_lookup(v, text + i, k);
+    if (id >= 0) t[n++] = (uint32_t)id;
+    else for (uint32_t b = 0; b < k; ++b) t[n++] = (uint32_t)text[i + b] + 3;
+    i += k;
+  }
+  uint8_t* buf = (uint8_t*)malloc(2ull * v->max_len + 2);       /* phase 2 */
+  for (;;) {
+    float best = 0;
+    int64_t best_id = -1;
+    uint32_t best_i = 0;
+    for (uint32_t i = 0; i + 1 < n; ++i) {
+      uint32_t la = v->len[t[i]], lb = v->len[t[i + 1]];
+      memcpy(buf, v->str[t[i]], la);
+      memcpy(buf + la, v->str[t[i + 1]], lb);
+      int64_t id = orc_vocab_lookup(v, buf, la + lb);
+      if (id >= 0 && (best_id < 0 || v->score[id] > best)) {
+        best = v->score[id];
+        best_id = id;
+        best_i = i;
+      }
+    }
+    if (best_id < 0) break;
+    t[best_i] = (uint32_t)best_id;
+    memmove(t + best_i + 1, t + best_i + 2, 4ull * (n - best_i - 2));
+    --n;
+  }
+  free(buf);
+  int rc = 0;
+  if (n > cap) rc = 4;
+  else memcpy(ids, t, 4ull * n);
+  *n_out = n;
+  free(t);
+  return rc;
+}
+
+/* The text of token tok generated after token prev ("Sampling"): the token's bytes, a
+ * leading space dropped right after the opening token, <0xXX> as that one byte, nothing
+ * for tokens 1 and 2.  Writes at most cap bytes; returns the byte count. */
+uint32_t orc_decode_piece(const orc_vocab* v, uint32_t prev, uint32_t tok, uint8_t* out, uint32_t cap) {
+  if (tok >= v->n || tok == 1 || tok == 2) return 0;
+  const uint8_t* s = v->str[tok];
+  uint32_t l = v->len[tok];
+  if (prev == 1 && l && s[0] == ' ') { ++s; --l; }
+  if (l == 6 && s[0] == '<' && s[1] == '0' && s[2] == 'x' && s[5] == '>') {
+    unsigned val = 0;
+    int ok = 1;
+    for (int i = 3; i < 5; ++i) {
+      uint8_t c = s[i];
+      unsigned d = c >= '0' && c <= '9' ? c - '0' : c >= 'A' && c <= 'F' ? c - 'A' + 10 :
+                   c >= 'a' && c <= 'f' ? c - 'a' + 10 : 16;
+      if (d == 16) ok = 0;
+      val = val * 16 + d;
+    }
+    if (ok) {
+      if (cap) out[0] = (uint8_t)val;
+      return 1;
+    }
+  }
+  uint32_t w = l < cap ? l : cap;
+  memcpy(out, s, w);
+  return w;
 }

@@ -324,3 +324,76 @@ def matrow_case(rows: int, cols: int, seed: int = MATROW_SEED, pitch: int | None
     s = random_u32(rows, seed, STREAM_MATRIX + 1 + rows * 7 + cols, 2**20, 2**24)
     x = random_i64(cols, seed, STREAM_VECTOR + rows * 7 + cols, -8 * 2**16, 8 * 2**16)
     return w, s, x
+
+
+# ---------------------------------------------------------------- synthetic tokenizer
+
+STREAM_VOCAB = 4_000_000
+STREAM_TEXT = 5_000_000
+_VOCAB_CHARS = [bytes([c]) for c in range(0x20, 0x7F)] + [c.encode() for c in "éüñöç—€"]
+_TEXT_CHARS = "abcdefghijklmnopqrstuvwxyz      ETAONISRH.,;:!?'-0123456789éüñöç—€日本"
+
+
+def tokenizer_blob(vocab: int, seed: int) -> bytes:
+    """A synthetic vocabulary of `vocab` tokens in llama2.c's tokenizer file layout (u32
+    longest token, then per token f32 score, i32 length, bytes): <unk>, the opening and
+    closing tokens, the 256 byte tokens <0x00>..<0xFF>, the printable ASCII characters and a
+    few 2- and 3-byte characters, then merged tokens, each the concatenation of two earlier
+    text tokens drawn from the seeded stream (at most 16 bytes, no repeats), with scores
+    falling by 0.25 a token so earlier merges win.  Characters of the prompts it cannot
+    spell (two CJK characters) fall back to byte tokens."""
+    import struct
+    toks = [(b"<unk>", 0.0), (b"\n<s>\n", 0.0), (b"\n</s>\n", 0.0)]
+    toks += [(("<0x%02X>" % i).encode(), 0.0) for i in range(256)]
+    text = [(c, -1e6) for c in _VOCAB_CHARS]
+    toks += text[: max(0, vocab - len(toks))]
+    seen = {t for t, _ in toks}
+    pool = [t for t, _ in text]
+    draws = xs64s_sequence(seed ^ STREAM_VOCAB, 8 * max(vocab, 64))
+    k = 0
+    score = -1.0
+    while len(toks) < vocab and k + 1 < len(draws):
+        a, b = pool[draws[k] % len(pool)], pool[draws[k + 1] % len(pool)]
+        k += 2
+        s = a + b
+        if len(s) > 16 or s in seen:
+            continue
+        seen.add(s)
+        toks.append((s, score))
+        pool.append(s)
+        score -= 0.25
+    while len(toks) < vocab:  # draws ran out: filler tokens that no text spells
+        s = ("<f%d>" % len(toks)).encode()
+        toks.append((s, -1e9))
+    out = struct.pack("<I", max(len(t) for t, _ in toks))
+    for t, sc in toks:
+        out += struct.pack("<fi", sc, len(t)) + t
+    return out
+
+
+def vocab_pieces(blob: bytes) -> list[bytes]:
+    """The byte strings of a vocabulary in the tokenizer file layout."""
+    import struct
+    out, off = [], 4
+    while off + 8 <= len(blob):
+        _, n = struct.unpack_from("<fi", blob, off)
+        out.append(blob[off + 8: off + 8 + n])
+        off += 8 + n
+    return out
+
+
+def prompt_text(n_pieces: int, seed: int, run: int = 0, blob: bytes | None = None) -> bytes:
+    """A seeded prompt: n_pieces pieces, each a single character (lower-case letters,
+    spaces, capitals, digits, punctuation, 2- and 3-byte characters, two of them outside the
+    synthetic vocabulary) or, with a vocabulary blob, half of the time one of its merged
+    tokens, so that encoding it has merges to find."""
+    d = xs64s_sequence(seed ^ STREAM_TEXT ^ (run << 20), 2 * n_pieces)
+    merged = [t for t in vocab_pieces(blob)[259:] if len(t) > 1 and not t.startswith(b"<")] if blob else []
+    out = b""
+    for i in range(n_pieces):
+        a, b = d[2 * i], d[2 * i + 1]
+        if merged and a % 2:
+            out += merged[b % len(merged)]
+        else:
+            out += _TEXT_CHARS[b % len(_TEXT_CHARS)].encode()
+    return out

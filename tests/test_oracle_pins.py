@@ -468,3 +468,91 @@ def test_sample_frequencies_follow_the_exponentials():
     for i in range(len(ks)):
         sd = math.sqrt(n * p[i] * (1 - p[i])) + 1
         assert abs(counts[i] - n * p[i]) <= 5 * sd, (i, counts[i], n * p[i])
+
+
+# ---------------------------------------------------------------- tokenizer (phases 0 to 2)
+
+def _blob(extra):
+    """A vocabulary in the tokenizer file layout: the 3 specials, the 256 byte tokens, then
+    `extra` (bytes, score) pairs."""
+    import struct
+    toks = [(b"<unk>", 0.0), (b"\n<s>\n", 0.0), (b"\n</s>\n", 0.0)]
+    toks += [(("<0x%02X>" % i).encode(), 0.0) for i in range(256)] + list(extra)
+    out = struct.pack("<I", max(len(t) for t, _ in toks))
+    for t, sc in toks:
+        out += struct.pack("<fi", sc, len(t)) + t
+    return out, len(toks)
+
+
+def _vocab(extra):
+    blob, n = _blob(extra)
+    v = oracle.Vocab(blob, n)
+    ids = {t: i for i, (t, _) in enumerate(extra, start=259)}
+    return v, ids
+
+
+def test_encode_opening_token_and_space():
+    """Phase 0: token 1, then the single-space token when the prompt has text."""
+    v, ids = _vocab([(b" ", -1.0), (b"a", -1.0)])
+    assert v.encode(b"") == (0, [1])
+    assert v.encode(b"a") == (0, [1, ids[b" "], ids[b"a"]])
+    v2, ids2 = _vocab([(b"a", -1.0)])                      # no space token: its byte token
+    assert v2.encode(b"a") == (0, [1, 0x20 + 3, ids2[b"a"]])
+
+
+def test_encode_byte_fallback():
+    """Phase 1: a character with no token becomes one token per byte, id byte + 3."""
+    v, ids = _vocab([(b" ", -1.0), (b"x", -1.0), ("é".encode(), -1.0)])
+    rc, t = v.encode("x日é".encode())
+    assert rc == 0
+    assert t == [1, ids[b" "], ids[b"x"], 0xE6 + 3, 0x97 + 3, 0xA5 + 3, ids["é".encode()]]
+
+
+def test_encode_merges_take_the_highest_score():
+    """Phase 2: of all adjacent pairs whose joined text is a token, the best score merges
+    first; merges repeat on the result."""
+    v, ids = _vocab([(b" ", -1.0), (b"a", -1.0), (b"b", -1.0), (b"c", -1.0), (b"ab", -5.0), (b"bc", -1.0)])
+    assert v.encode(b"abc") == (0, [1, ids[b" "], ids[b"a"], ids[b"bc"]])
+    v, ids = _vocab([(b" ", -1.0), (b"a", -1.0), (b"b", -1.0), (b"c", -1.0), (b"ab", -1.0), (b"abc", -2.0)])
+    assert v.encode(b"abc") == (0, [1, ids[b" "], ids[b"abc"]])
+    v, ids = _vocab([(b" ", -1.0), (b"a", -1.0), (b"aa", -1.0), (b" a", -9.0)])
+    # "aaa": the two (a, a) pairs tie, the leftmost merges (r24); then " a" is not
+    # reachable because the space now precedes "aa"
+    assert v.encode(b"aaa") == (0, [1, ids[b" "], ids[b"aa"], ids[b"a"]])
+
+
+def test_encode_rejects_bad_prompts():
+    v, _ = _vocab([(b" ", -1.0)])
+    assert v.encode(b"a\x00b")[0] == 6                     # a zero byte
+    assert v.encode(b"\xff")[0] == 6                       # not UTF-8
+    assert v.encode(b"\xc3")[0] == 6                       # truncated character
+    assert v.encode(b"\xc0\x80")[0] == 6                   # overlong
+    assert v.encode(b"a" * 1025)[0] == 6                   # over 1,024 bytes
+    assert v.encode(b"a" * 1024)[0] == 0
+
+
+def test_token_text_rules():
+    """Token text: the bytes, a leading space dropped right after the opening token, <0xXX>
+    as one byte, nothing for tokens 1 and 2."""
+    v, ids = _vocab([(b" hi", -1.0)])
+    assert v.piece(1, ids[b" hi"]) == b"hi"
+    assert v.piece(7, ids[b" hi"]) == b" hi"
+    assert v.piece(5, 0x41 + 3) == b"A"
+    assert v.piece(5, 1) == b"" and v.piece(5, 2) == b""
+    assert v.decode([1, ids[b" hi"], ids[b" hi"], 2]) == b"hi hi"
+
+
+def test_encode_fixed_point_and_round_trip_on_synthetic_vocabularies():
+    """For seeded prompts: decoding the encoding gives the prompt back, and no adjacent pair
+    of the result joins into a token (the merges ran to the end)."""
+    for n, seed in ((512, 0x5EED0011), (32000, 0x5EED0003)):
+        blob = synth.tokenizer_blob(n, seed)
+        v = oracle.Vocab(blob, n)
+        pieces = synth.vocab_pieces(blob)
+        for run in range(6):
+            text = synth.prompt_text(80, seed, run, blob)
+            rc, ids = v.encode(text)
+            assert rc == 0
+            assert v.decode(ids) == text
+            for a, b in zip(ids, ids[1:]):
+                assert v.lookup(pieces[a] + pieces[b]) < 0
