@@ -67,6 +67,10 @@ def lib() -> ctypes.CDLL:
             "ck_init_state": ([vp, vp, sz, vp, u32, u32, u32, u64, u32, vp], ctypes.c_int),
             "ck_turn": ([vp, vp, sz, u32, vp, ctypes.POINTER(TurnResult)], ctypes.c_int),
             "ck_turn_batch": ([vp, vp, vp, u32, vp, vp, vp], ctypes.c_int),
+            "ck_tokenizer_load": ([vp, sz, u32, ctypes.POINTER(vp)], ctypes.c_int),
+            "ck_tokenizer_free": ([vp], None),
+            "ck_encode": ([vp, vp, sz, vp, u32, ctypes.POINTER(u32)], ctypes.c_int),
+            "ck_decode": ([vp, u32, vp, u32, vp, sz, ctypes.POINTER(sz)], ctypes.c_int),
             "ck_turn_noalloc": ([vp, vp, sz, vp, ctypes.POINTER(TurnResult)], ctypes.c_int),
             "ck_logits": ([vp, vp, sz, vp, vp], ctypes.c_int),
             "ck_argmax": ([vp, vp, sz, ctypes.POINTER(u32), vp], ctypes.c_int),
@@ -225,6 +229,47 @@ class Model:
         rc = lib().ck_output_tokens(self._h, _ptr(state), state.numel(), out.ctypes.data, cap,
                                     ctypes.byref(n), _stream(stream))
         return rc, out[:n.value].tolist()
+
+
+class Tokenizer:
+    """A vocabulary for phases 0 to 2 and token text (host code in the library)."""
+
+    def __init__(self, handle):
+        self._h = handle
+
+    @classmethod
+    def load(cls, blob: bytes, vocab: int):
+        """Returns (rc, Tokenizer or None)."""
+        b = np.frombuffer(bytes(blob), dtype=np.uint8)
+        h = ctypes.c_void_p()
+        rc = lib().ck_tokenizer_load(b.ctypes.data, b.size, vocab, ctypes.byref(h))
+        return rc, (cls(h) if rc == 0 else None)
+
+    def __del__(self):
+        try:
+            if self._h:
+                lib().ck_tokenizer_free(self._h)
+        except Exception:
+            pass
+
+    def encode(self, text: bytes):
+        """Returns (rc, ids)."""
+        t = np.frombuffer(bytes(text) or b"\0", dtype=np.uint8)
+        cap = len(text) + 2
+        ids = np.zeros(cap, dtype=np.uint32)
+        n = ctypes.c_uint32()
+        rc = lib().ck_encode(self._h, t.ctypes.data, len(text), ids.ctypes.data, cap, ctypes.byref(n))
+        return rc, (ids[:n.value].copy() if rc == 0 else np.zeros(0, np.uint32))
+
+    def decode(self, ids, prev: int = 0):
+        """Returns (rc, text bytes)."""
+        a = np.ascontiguousarray(np.asarray(ids, dtype=np.uint32))
+        n = ctypes.c_size_t()
+        cap = 256 * max(a.size, 1)
+        out = np.zeros(cap, dtype=np.uint8)
+        rc = lib().ck_decode(self._h, prev, a.ctypes.data if a.size else None, a.size, out.ctypes.data, cap,
+                             ctypes.byref(n))
+        return rc, out[:n.value].tobytes()
 
 
 def state_download(state, stream=None) -> np.ndarray:

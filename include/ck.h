@@ -251,6 +251,32 @@ int ck_logits(const ck_model* m, const void* dev_state, size_t len, int64_t* hos
  * a device kernel: the index of the first largest logit.  Synchronizes.  Errors: 3, 9, 10. */
 int ck_argmax(const ck_model* m, const void* dev_state, size_t len, uint32_t* out, void* stream);
 
+/* ---------------------------------------------------------------- tokenizer
+ * Phases 0 to 2 ("The forward pass, in order") and the text of generated tokens
+ * ("Sampling"), on the host: a prompt is tokenized once per run, before its positions.
+ * The vocabulary is in llama2.c's tokenizer file layout: u32 longest token length, then per
+ * token an f32 score, an i32 byte length and the bytes; token 1 opens a run, tokens 1 and 2
+ * have no text, tokens 3..258 are the bytes 0..255. */
+typedef struct ck_tokenizer ck_tokenizer;
+/* Reads `vocab` tokens from blob (the model's vocabulary size).  Errors: 2 (the blob does
+ * not hold them, or repeats a string), 10. */
+int ck_tokenizer_load(const void* blob, size_t len, uint32_t vocab, ck_tokenizer** out);
+void ck_tokenizer_free(ck_tokenizer* t);
+/* Phases 0 to 2 on a prompt of len bytes: token 1, the token of a single space when there
+ * is text, one token per UTF-8 character (or, for a character with no token, one per byte,
+ * id byte + 3), then, while any adjacent pair's joined text is a token, the pair whose
+ * token has the highest score merges (the leftmost of equals).  Writes the ids (*n of
+ * them) for ck_init_state.  Errors: 6 (over 1,024 bytes, a zero byte, not UTF-8), 4 (cap
+ * below *n), 10. */
+int ck_encode(const ck_tokenizer* t, const uint8_t* text, size_t len, uint32_t* ids, uint32_t cap,
+              uint32_t* n);
+/* The text of ids[0..n), each after the one before it (prev before the first, e.g. the
+ * last prompt id): the token's bytes, a leading space dropped right after token 1, a token
+ * written <0xXX> as that one byte, nothing for tokens 1 and 2.  Writes at most cap bytes;
+ * *n_bytes is the full count.  Errors: 4 (cap below *n_bytes), 10. */
+int ck_decode(const ck_tokenizer* t, uint32_t prev, const uint32_t* ids, uint32_t n, uint8_t* out,
+              size_t cap, size_t* n_bytes);
+
 /* The page's output_tokens: copies min(generated, cap) token ids to host_out and the count
  * to *n.  Synchronizes.  Errors: 3, 9, 10. */
 int ck_output_tokens(const ck_model* m, const void* dev_state, size_t len, uint32_t* host_out,

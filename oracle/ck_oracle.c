@@ -717,7 +717,8 @@ static int sort_cmp(const void* x, const void* y) {
   return bytes_cmp(v->str[a], v->len[a], v->str[b], v->len[b]);
 }
 
-/* Opens a vocabulary of n tokens.  Returns 0, or 2 for a blob that does not hold them. */
+/* Opens a vocabulary of n tokens.  Returns 0, or 2 for a blob that does not hold them or
+ * that repeats a string. */
 int orc_vocab_open(const uint8_t* blob, uint64_t blob_len, uint32_t n, orc_vocab** out) {
   *out = NULL;
   if (blob_len < 4 || n == 0) return 2;
@@ -745,6 +746,8 @@ int orc_vocab_open(const uint8_t* blob, uint64_t blob_len, uint32_t n, orc_vocab
   }
   g_sort_vocab = v;
   qsort(v->sorted, n, 4, sort_cmp);
+  for (uint32_t i = 1; i < n; ++i) /* repeated strings would make a lookup ambiguous */
+    if (sort_cmp(&v->sorted[i - 1], &v->sorted[i]) == 0) goto bad;
   *out = v;
   return 0;
 bad:

@@ -687,6 +687,35 @@ def test_1b_sixty_four_runs_batched_sampled(ck):
         compare_states(orc, host, ck.state_download(states[r]), wl.n_prompt, wl.steps, f"run {r}", turns=False)
 
 
+# ---------------------------------------------------------------- text in, text out
+
+@pytest.mark.parametrize("temp", [0, 3 << 15])
+def test_text_prompt_to_text_output(ck, temp):
+    """A text prompt through the library's tokenizer (phases 0 to 2), the GPU run, and the
+    text of the generated tokens, against the oracle's tokenizer, run and text."""
+    wl = MODELS["gqa"]
+    spec = wl.spec
+    blob = synth.tokenizer_blob(spec.vocab, spec.seed)
+    rc, tok = ck.Tokenizer.load(blob, spec.vocab)
+    assert rc == 0
+    v = oracle.Vocab(blob, spec.vocab)
+    text = synth.prompt_text(20, spec.seed, 3, blob)
+    rcg, ids = tok.encode(text)
+    rco, ids_o = v.encode(text)
+    assert rcg == rco == 0 and ids.tolist() == ids_o
+    P = Pair(ck, spec, "step")
+    steps = 24
+    so, sg = P.init(ck, ids, steps, temperature_q16=temp, seed=5)
+    rco, reso = P.orc.turn(so, 10_000)
+    rcg, resg = P.gpu.turn(sg, 10_000)
+    assert rco == rcg == 0 and reso == resg
+    compare_states(P.orc, so, ck.state_download(sg), len(ids), steps, "text run")
+    rc, out = P.gpu.output_tokens(sg)
+    assert rc == 0 and len(out) == steps
+    rc, got = tok.decode(out, prev=int(ids[-1]))
+    assert rc == 0 and got == v.decode(list(out), prev=int(ids[-1]))
+
+
 def test_paths_agree_and_unknown_path_is_rejected(ck):
     wl = MODELS["gqa"]
     P = Pair(ck, wl.spec, "step")

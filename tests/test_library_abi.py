@@ -82,3 +82,37 @@ def test_library_fails_loudly_without_a_gpu(ck):
     import synth
     with pytest.raises(Exception):
         ck.Model.load(synth.build_artifact(synth.TINY_WS))
+
+
+# ---------------------------------------------------------------- tokenizer (host code)
+
+def test_library_tokenizer_matches_the_oracle():
+    """The library's phases 0 to 2 and token text against the oracle's, on seeded prompts
+    over synthetic vocabularies (host code: no GPU needed)."""
+    import fixed_point_int8_gb300 as ck
+    import oracle
+    import synth
+    for n, seed in ((512, 0x5EED0011), (32000, 0x5EED0003)):
+        blob = synth.tokenizer_blob(n, seed)
+        rc, tok = ck.Tokenizer.load(blob, n)
+        assert rc == 0
+        v = oracle.Vocab(blob, n)
+        for run in range(8):
+            text = synth.prompt_text(120, seed, run, blob)
+            rco, want = v.encode(text)
+            rcg, got = tok.encode(text)
+            assert rco == rcg == 0 and got.tolist() == want, run
+            rc, back = tok.decode(got)
+            assert rc == 0 and back == v.decode(want) == text
+            ids = [int(x) for x in synth.random_u32(40, seed, 77 + run, 0, n - 1)]
+            assert tok.decode(ids, prev=1)[1] == v.decode(ids, prev=1)
+        for bad in (b"a\x00b", b"\xff", b"\xed\xa0\x80", b"x" * 1025):   # zero, bad lead, surrogate, long
+            assert tok.encode(bad)[0] == v.encode(bad)[0] == 6
+        assert tok.encode(b"")[1].tolist() == v.encode(b"")[1] == [1]
+    blob = synth.tokenizer_blob(512, 1)
+    assert ck.Tokenizer.load(blob[:100], 512)[0] == 2                     # truncated
+    import struct
+    dup = struct.pack("<I", 1) + struct.pack("<fi", 0.0, 1) + b"a" + struct.pack("<fi", 0.0, 1) + b"a"
+    assert ck.Tokenizer.load(dup, 2)[0] == 2                               # a repeated string
+    with pytest.raises(ValueError):
+        oracle.Vocab(dup, 2)
