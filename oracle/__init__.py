@@ -92,6 +92,10 @@ def _lib_():
             "orc_vocab_lookup": ([vp, vp, u32], i64),
             "orc_encode": ([vp, vp, u32, vp, u32, ctypes.POINTER(u32)], ctypes.c_int),
             "orc_decode_piece": ([vp, u32, u32, vp, u32], u32),
+            "orc_page_size": ([vp, u32, u32], u64),
+            "orc_page_layout_of": ([vp, u32, u32, vp], None),
+            "orc_page_init": ([vp, vp, u64, vp, u32, u32, u32, u64], ctypes.c_int),
+            "orc_page_turn": ([vp, vp, vp, u64, u32, ctypes.POINTER(u32)], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -316,6 +320,43 @@ class Vocab:
             out += self.piece(prev, int(t))
             prev = int(t)
         return out
+
+
+PAGE_LAYOUT_NAMES = ("prompt", "ptok", "out", "text", "x", "w0", "w1", "w2", "gate", "up", "logits",
+                     "scores", "k", "v", "size", "cache")
+
+
+def page_new(model: "Model", prompt: bytes, max_tokens: int, temperature_q16: int = 0, seed: int = 0):
+    """A fresh page state ("CURTAST2") for a text prompt.  Returns (rc, state bytes)."""
+    n = int(_lib_().orc_page_size(model._h, len(prompt), max_tokens))
+    st = np.zeros(n, dtype=np.uint8)
+    p = np.frombuffer(bytes(prompt) or b"\0", dtype=np.uint8)
+    rc = _lib_().orc_page_init(model._h, st.ctypes.data, n, p.ctypes.data, len(prompt), max_tokens,
+                               temperature_q16, seed)
+    return rc, st
+
+
+def page_layout(model: "Model", prompt_bytes: int, max_tokens: int) -> dict:
+    out = np.zeros(16, dtype=np.uint64)
+    _lib_().orc_page_layout_of(model._h, prompt_bytes, max_tokens, out.ctypes.data)
+    return {k: int(v) for k, v in zip(PAGE_LAYOUT_NAMES, out)}
+
+
+def page_turn(model: "Model", vocab: "Vocab", state: np.ndarray, n_steps: int):
+    """Up to n_steps phase steps in place.  Returns (rc, steps run)."""
+    steps = ctypes.c_uint32()
+    rc = _lib_().orc_page_turn(model._h, vocab._h, state.ctypes.data, state.size, n_steps, ctypes.byref(steps))
+    return rc, int(steps.value)
+
+
+def page_header(state: np.ndarray) -> dict:
+    u32 = lambda o: int(state[o:o + 4].view("<u4")[0])
+    u64 = lambda o: int(state[o:o + 8].view("<u8")[0])
+    return {"phase": u32(8), "layer": u32(12), "row": u32(16), "position": u32(20), "token": u32(24),
+            "prompt_bytes": u32(28), "prompt_tokens": u32(32), "max_tokens": u32(36), "temperature": u32(40),
+            "generated": u32(44), "text_bytes": u32(48), "generator": u64(72), "turns": u64(80),
+            "max_score": int(state[88:96].view("<i8")[0]), "chosen": u32(96), "exp_sum": u64(104),
+            "draw": u64(112), "att_stage": u32(120), "att_index": u32(124)}
 
 
 def header(state: np.ndarray) -> dict:

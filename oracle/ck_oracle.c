@@ -880,3 +880,232 @@ uint32_t orc_decode_piece(const orc_vocab* v, uint32_t prev, uint32_t tok, uint8
   memcpy(out, s, w);
   return w;
 }
+
+/* ------------------------------------------------------------------ the page's state
+ * "The resumable state": the CURTAST2 state (a 128-byte header and text-mode buffers) and
+ * the phases of "The forward pass, in order" run one step at a time, a step being one
+ * phase of one layer of one position (phase 9 one head a step, the row field naming the
+ * head), so that a turn can stop at any phase boundary, mid-layer included, and another
+ * target can go on from the bytes.  Readings: r27 the working vectors between phases
+ * (activations x; w0 the normalised vector, then the output rows before their residual;
+ * w1 the queries; w2 the heads' outputs; gate and up, then SiLU's output in gate); r28 the
+ * tokenizer phases 0 to 2 are one step; r29 a step is all or nothing: a store that does
+ * not fit leaves the state as it was before the step and the turn returns 8. */
+
+enum { P_PHASE = 8, P_LAYER = 12, P_ROW = 16, P_POS = 20, P_TOKEN = 24, P_PBYTES = 28, P_NPTOK = 32,
+       P_MAXTOK = 36, P_TEMP = 40, P_GEN = 44, P_TEXTLEN = 48, P_SEED = 72, P_TURNS = 80,
+       P_MAXSCORE = 88, P_CHOSEN = 96, P_SPASS = 100, P_SUM = 104, P_DRAW = 112, P_ASTAGE = 120,
+       P_AINDEX = 124 };
+
+typedef struct {
+  uint64_t prompt, ptok, out, text, x, w0, w1, w2, gate, up, logits, scores, k, v, size;
+  uint32_t cache;
+} orc_page_layout;
+
+static orc_page_layout page_layout(const orc_model* m, uint32_t prompt_bytes, uint32_t max_tokens) {
+  orc_page_layout L;
+  uint64_t cache = (uint64_t)prompt_bytes + max_tokens + 1;
+  if (cache > m->context) cache = m->context;
+  uint64_t n = 128;
+  L.prompt = n; n = up8(n + prompt_bytes);
+  L.ptok = n; n = up8(n + 4ull * (prompt_bytes + 2));
+  L.out = n; n = up8(n + 4ull * max_tokens);
+  L.text = n; n = up8(n + 128ull * max_tokens);
+  L.x = n; L.w0 = n + 8ull * m->dim; L.w1 = n + 16ull * m->dim; L.w2 = n + 24ull * m->dim;
+  n = up8(n + 32ull * m->dim);
+  L.gate = n; L.up = n + 8ull * m->hidden; n = up8(n + 16ull * m->hidden);
+  L.logits = n; n = up8(n + 8ull * m->vocab);
+  L.scores = n; n = up8(n + 8 * cache);
+  L.k = n; n = up8(n + 4ull * m->layers * cache * m->kv_dim);
+  L.v = n; n = up8(n + 4ull * m->layers * cache * m->kv_dim);
+  L.size = n;
+  L.cache = (uint32_t)cache;
+  return L;
+}
+
+uint64_t orc_page_size(const orc_model* m, uint32_t prompt_bytes, uint32_t max_tokens) {
+  return page_layout(m, prompt_bytes, max_tokens).size;
+}
+
+/* Buffer offsets, for the bindings: prompt, ptok, out, text, x, w0, w1, w2, gate, up,
+ * logits, scores, k, v, size (15 values) and the cache positions. */
+void orc_page_layout_of(const orc_model* m, uint32_t prompt_bytes, uint32_t max_tokens, uint64_t* out16) {
+  orc_page_layout L = page_layout(m, prompt_bytes, max_tokens);
+  memcpy(out16, &L, 15 * 8);
+  out16[15] = L.cache;
+}
+
+/* "The Rust API", init_state: a fresh header and the prompt.  Errors: 4 wrong length, 6
+ * max tokens 0 or above the context, a temperature above 16, a prompt over 1,024 bytes. */
+int orc_page_init(const orc_model* m, uint8_t* st, uint64_t len, const uint8_t* prompt, uint32_t plen,
+                  uint32_t max_tokens, uint32_t temperature_q16, uint64_t seed) {
+  if (max_tokens == 0 || max_tokens > m->context || temperature_q16 > (16u << 16) || plen > 1024) return 6;
+  orc_page_layout L = page_layout(m, plen, max_tokens);
+  if (len != L.size) return 4;
+  memset(st, 0, len);
+  memcpy(st, "CURTAST2", 8);
+  wr32(st + P_PBYTES, plen);
+  wr32(st + P_MAXTOK, max_tokens);
+  wr32(st + P_TEMP, temperature_q16);
+  wr64(st + P_SEED, seed ? seed : 0x9E3779B97F4A7C15ull);
+  memcpy(st + L.prompt, prompt, plen);
+  return 0;
+}
+
+static int store_fit(int32_t* dst, const int64_t* src, uint32_t n) {
+  for (uint32_t j = 0; j < n; ++j)
+    if (!orc_fits32(src[j])) return (int)j;
+  for (uint32_t j = 0; j < n; ++j) dst[j] = (int32_t)src[j];
+  return -1;
+}
+
+/* One step from the state's cursor.  Returns 0, or an error (3 finished or foreign state,
+ * 6 bad prompt, 7 context exceeded, 8 a store that does not fit: nothing changed). */
+static int page_step(const orc_model* m, const orc_vocab* voc, uint8_t* st, const orc_page_layout* L) {
+  const uint32_t phase = rd32(st + P_PHASE), l = rd32(st + P_LAYER), pos = rd32(st + P_POS);
+  const uint32_t d = m->dim, hd = m->head_dim, kvd = m->kv_dim, hid = m->hidden, cache = L->cache;
+  const uint32_t np = rd32(st + P_NPTOK);
+  int64_t *x = (int64_t*)(st + L->x), *w0 = (int64_t*)(st + L->w0), *w1 = (int64_t*)(st + L->w1);
+  int64_t *w2 = (int64_t*)(st + L->w2), *g = (int64_t*)(st + L->gate), *u = (int64_t*)(st + L->up);
+  int64_t* logits = (int64_t*)(st + L->logits);
+  int32_t *K = (int32_t*)(st + L->k), *V = (int32_t*)(st + L->v);
+  uint32_t* ptok = (uint32_t*)(st + L->ptok);
+  uint32_t* out = (uint32_t*)(st + L->out);
+  const orc_layer* W = l < m->layers ? &m->layer[l] : NULL;
+  int32_t* Kp = K + ((uint64_t)l * cache + pos) * kvd; /* the page's order: [layer][position][kv] */
+  int32_t* Vp = V + ((uint64_t)l * cache + pos) * kvd;
+  switch (phase) {
+    case 0: { /* phases 0 to 2: the prompt's tokens */
+      uint32_t n = 0, plen = rd32(st + P_PBYTES);
+      int rc = orc_encode(voc, st + L->prompt, plen, ptok, plen + 2, &n);
+      if (rc) return rc;
+      if ((uint64_t)n + rd32(st + P_MAXTOK) > cache) return 7;
+      wr32(st + P_NPTOK, n);
+      wr32(st + P_POS, 0);
+      wr32(st + P_TOKEN, ptok[0]);
+      wr32(st + P_PHASE, 3);
+      return 0;
+    }
+    case 3: {
+      uint32_t tok = rd32(st + P_TOKEN);
+      if (tok >= m->vocab) return 3;
+      orc_embed(m->embed + (uint64_t)tok * d, m->embed_scale[tok], d, x);
+      wr32(st + P_LAYER, 0);
+      wr32(st + P_PHASE, 4);
+      return 0;
+    }
+    case 4: orc_rmsnorm(x, W->attn_norm, d, w0); break;
+    case 5: orc_matrow(W->wq, d, W->sq, d, d, w0, w1); break;
+    case 6: case 7: {
+      int64_t* tmp = (int64_t*)malloc(8ull * kvd);
+      orc_matrow(phase == 6 ? W->wk : W->wv, d, phase == 6 ? W->sk : W->sv, kvd, d, w0, tmp);
+      int bad = store_fit(phase == 6 ? Kp : Vp, tmp, kvd);
+      free(tmp);
+      if (bad >= 0) return 8;
+      break;
+    }
+    case 8: {
+      const int32_t* rope = m->rope + (uint64_t)pos * hd;
+      int32_t* kk = (int32_t*)malloc(4ull * kvd);
+      for (uint32_t i = 0; i < kvd; i += 2) {
+        uint32_t j = (i % hd) / 2;
+        int64_t a2, b2;
+        orc_rotate(Kp[i], Kp[i + 1], rope[2 * j], rope[2 * j + 1], &a2, &b2);
+        if (!orc_fits32(a2) || !orc_fits32(b2)) { free(kk); return 8; }
+        kk[i] = (int32_t)a2;
+        kk[i + 1] = (int32_t)b2;
+      }
+      memcpy(Kp, kk, 4ull * kvd);
+      free(kk);
+      for (uint32_t i = 0; i < d; i += 2) {
+        uint32_t j = (i % hd) / 2;
+        orc_rotate(w1[i], w1[i + 1], rope[2 * j], rope[2 * j + 1], &w1[i], &w1[i + 1]);
+      }
+      wr32(st + P_ROW, 0);
+      wr32(st + P_ASTAGE, 0);
+      wr32(st + P_AINDEX, 0);
+      break;
+    }
+    case 9: { /* one head a step */
+      uint32_t h = rd32(st + P_ROW);
+      uint32_t kvh = h / (m->heads / m->kv_heads);
+      const int32_t* K0 = K + (uint64_t)l * cache * kvd + (uint64_t)kvh * hd;
+      const int32_t* V0 = V + (uint64_t)l * cache * kvd + (uint64_t)kvh * hd;
+      orc_attention_head(w1 + (uint64_t)h * hd, K0, V0, kvd, pos + 1, hd, m->inv_sqrt, m->exp_tab,
+                         (int64_t*)(st + L->scores), w2 + (uint64_t)h * hd);
+      if (h + 1 < m->heads) {
+        wr32(st + P_ROW, h + 1);
+        return 0;
+      }
+      wr32(st + P_ROW, 0);
+      break;
+    }
+    case 10: orc_matrow(W->wo, d, W->so, d, d, w2, w0); break;
+    case 11: residual(x, w0, d); orc_rmsnorm(x, W->ffn_norm, d, w0); break;
+    case 12: orc_matrow(W->w1, d, W->s1, hid, d, w0, g); break;
+    case 13: orc_matrow(W->w3, d, W->s3, hid, d, w0, u); break;
+    case 14: orc_silu_gate(g, u, hid, m->silu_tab, g); break;
+    case 15: orc_matrow(W->w2, hid, W->s2, d, hid, g, w0); break;
+    case 16: {
+      residual(x, w0, d);
+      if (l + 1 < m->layers) {
+        wr32(st + P_LAYER, l + 1);
+        wr32(st + P_PHASE, 4);
+      } else if (pos + 1 < np) {                          /* the next prompt position */
+        wr32(st + P_POS, pos + 1);
+        wr32(st + P_TOKEN, ptok[pos + 1]);
+        wr32(st + P_PHASE, 3);
+      } else {
+        wr32(st + P_PHASE, 17);
+      }
+      return 0;
+    }
+    case 17: orc_rmsnorm(x, m->final_norm, d, w0); break;
+    case 18: orc_matrow(m->cls, d, m->cls_scale, m->vocab, d, w0, logits); break;
+    case 19: {
+      uint64_t state = rd64(st + P_SEED), z, draw;
+      int64_t mx;
+      uint32_t t = orc_sample(logits, m->vocab, rd32(st + P_TEMP), m->exp_tab, &state, &mx, &z, &draw);
+      uint32_t gen = rd32(st + P_GEN), tl = rd32(st + P_TEXTLEN);
+      uint32_t prev = pos < np ? ptok[pos] : out[gen - 1];
+      out[gen] = t;
+      tl += orc_decode_piece(voc, prev, t, st + L->text + tl, 128);
+      wr32(st + P_GEN, gen + 1);
+      wr32(st + P_TEXTLEN, tl);
+      wr64(st + P_SEED, state);
+      wr64(st + P_MAXSCORE, (uint64_t)mx);
+      wr32(st + P_CHOSEN, t);
+      wr64(st + P_SUM, z);
+      wr64(st + P_DRAW, draw);
+      if (t == 1 || t == 2 || gen + 1 == rd32(st + P_MAXTOK)) {
+        wr32(st + P_PHASE, 20);
+      } else {
+        wr32(st + P_POS, pos + 1);
+        wr32(st + P_TOKEN, t);
+        wr32(st + P_PHASE, 3);
+      }
+      return 0;
+    }
+    default: return 3;
+  }
+  wr32(st + P_PHASE, phase + 1);
+  return 0;
+}
+
+/* "The Rust API", turn, at step granularity: up to n_steps steps.  Returns 0 or the error
+ * of the step that failed (that step changed nothing); *steps receives the steps run. */
+int orc_page_turn(const orc_model* m, const orc_vocab* voc, uint8_t* st, uint64_t len, uint32_t n_steps,
+                  uint32_t* steps) {
+  *steps = 0;
+  if (len < 128 || memcmp(st, "CURTAST2", 8) != 0) return 3;
+  orc_page_layout L = page_layout(m, rd32(st + P_PBYTES), rd32(st + P_MAXTOK));
+  if (len != L.size) return 3;
+  int rc = 0;
+  for (uint32_t i = 0; i < n_steps && rd32(st + P_PHASE) != 20; ++i) {
+    rc = page_step(m, voc, st, &L);
+    if (rc) break;
+    ++*steps;
+  }
+  wr64(st + P_TURNS, rd64(st + P_TURNS) + 1);
+  return rc;
+}

@@ -220,3 +220,69 @@ def test_high_temperature_changes_the_tokens_and_zero_does_not_draw(tiny_ws):
     _, hot = m.init_state(ids, wl.steps, temperature_q16=16 << 16, seed=7)
     m.turn(hot, 1000)
     assert _buf(m, hot, wl, "out", "<u4", wl.steps).tolist() != g
+
+
+# ---------------------------------------------------------------- the page's state (CURTAST2)
+
+def _page_case(temp=0):
+    wl = synth.WORKLOADS["gqa"]
+    spec = wl.spec
+    m = _model(spec)
+    blob = synth.tokenizer_blob(spec.vocab, spec.seed)
+    v = oracle.Vocab(blob, spec.vocab)
+    text = synth.prompt_text(12, spec.seed, 1, blob)
+    return spec, m, v, text
+
+
+def test_page_sizes_agree_with_the_printed_sizes_rule():
+    spec, m, v, text = _page_case()
+    for pb, mt in ((16, 12), (0, 30), (100, 7)):
+        assert oracle.page_layout(m, pb, mt)["size"] == oracle.page_state_size(spec.config(), pb, mt)
+
+
+def test_page_run_stops_anywhere_and_matches_the_ids_run():
+    """The page state run step by step with stops every k steps (mid-layer and mid-attention
+    included) ends in the same bytes as one uninterrupted turn, and its tokens, activations,
+    logits and cache equal those of the ids-mode run of the same prompt ids."""
+    spec, m, v, text = _page_case()
+    steps = 9
+    rc, ref = oracle.page_new(m, text, steps, 3 << 15, 11)
+    assert rc == 0
+    rc, n = oracle.page_turn(m, v, ref, 10**9)
+    assert rc == 0 and oracle.page_header(ref)["phase"] == 20
+    for k in (1, 5, 23):
+        rc, st = oracle.page_new(m, text, steps, 3 << 15, 11)
+        turns = 0
+        while oracle.page_header(st)["phase"] != 20:
+            rc, ran = oracle.page_turn(m, v, st, k)
+            assert rc == 0 and ran >= 1
+            turns += 1
+        assert turns > 1
+        a, b = ref.copy(), st.copy()
+        a[80:88] = 0
+        b[80:88] = 0                                           # the turn counters differ
+        assert np.array_equal(a, b), k
+    # the ids-mode oracle on the page's prompt tokens
+    pl = oracle.page_layout(m, len(text), steps)
+    h = oracle.page_header(ref)
+    ids = ref[pl["ptok"]:pl["ptok"] + 4 * h["prompt_tokens"]].view("<u4")
+    assert ids.tolist() == v.encode(text)[1]
+    rc, so = m.init_state(ids, steps, 3 << 15, 11)
+    rco, _ = m.turn(so, 10**6)
+    assert rco == 0
+    lay = m.layout(len(ids), steps)
+    assert ref[pl["out"]:pl["out"] + 4 * steps].tobytes() == so[lay["out"]:lay["out"] + 4 * steps].tobytes()
+    for name in ("x", "logits"):
+        nb = 8 * (spec.dim if name == "x" else spec.vocab)
+        assert ref[pl[name]:pl[name] + nb].tobytes() == so[lay[name]:lay[name] + nb].tobytes(), name
+    # caches: the page keeps [layer][position][kv], the ids state [layer][kv head][position][head]
+    cache_o = len(ids) + steps - 1
+    hd, kvh = spec.head_dim, spec.kv_heads
+    for name in ("k", "v"):
+        page = ref[pl[name]:pl[name] + 4 * spec.layers * pl["cache"] * spec.kv_dim].view("<i4").reshape(
+            spec.layers, pl["cache"], spec.kv_dim)[:, :cache_o]
+        mine = so[lay[name]:lay[name] + 4 * spec.layers * cache_o * spec.kv_dim].view("<i4").reshape(
+            spec.layers, kvh, cache_o, hd).transpose(0, 2, 1, 3).reshape(spec.layers, cache_o, spec.kv_dim)
+        assert np.array_equal(page, mine), name
+    text_out = ref[pl["text"]:pl["text"] + h["text_bytes"]].tobytes()
+    assert text_out == v.decode(ref[pl["out"]:pl["out"] + 4 * steps].view("<u4").tolist(), prev=int(ids[-1]))
