@@ -71,6 +71,9 @@ def lib() -> ctypes.CDLL:
             "ck_tokenizer_free": ([vp], None),
             "ck_encode": ([vp, vp, sz, vp, u32, ctypes.POINTER(u32)], ctypes.c_int),
             "ck_decode": ([vp, u32, vp, u32, vp, sz, ctypes.POINTER(sz)], ctypes.c_int),
+            "ck_page_size": ([vp, u32, u32, ctypes.POINTER(sz)], ctypes.c_int),
+            "ck_state_to_page": ([vp, vp, vp, sz, vp, sz, vp, sz], ctypes.c_int),
+            "ck_state_from_page": ([vp, vp, sz, vp, sz], ctypes.c_int),
             "ck_turn_noalloc": ([vp, vp, sz, vp, ctypes.POINTER(TurnResult)], ctypes.c_int),
             "ck_logits": ([vp, vp, sz, vp, vp], ctypes.c_int),
             "ck_argmax": ([vp, vp, sz, ctypes.POINTER(u32), vp], ctypes.c_int),
@@ -205,6 +208,30 @@ class Model:
         rcs = (ctypes.c_int * max(n, 1))()
         rc = lib().ck_turn_batch(self._h, ptrs, lens, n, _stream(stream), res, rcs)
         return rc, [res[i].as_dict() for i in range(n)], [int(rcs[i]) for i in range(n)]
+
+    def state_to_page(self, tokenizer, host_state, prompt: bytes):
+        """This library's state (host bytes) into the page's CURTAST2 state.  Returns (rc, page)."""
+        n = ctypes.c_size_t()
+        rc = lib().ck_page_size(self._h, len(prompt), int(host_state[20:24].view("<u4")[0]), ctypes.byref(n))
+        if rc:
+            return rc, None
+        page = np.zeros(n.value, dtype=np.uint8)
+        p = np.frombuffer(bytes(prompt) or b"\0", dtype=np.uint8)
+        hs = np.ascontiguousarray(host_state)
+        rc = lib().ck_state_to_page(self._h, tokenizer._h, hs.ctypes.data, hs.size, p.ctypes.data, len(prompt),
+                                    page.ctypes.data, page.size)
+        return rc, page
+
+    def state_from_page(self, page, n_prompt: int, max_tokens: int):
+        """A page state at a position boundary into this library's state (host bytes).
+        Returns (rc, state)."""
+        rc, n = self.state_size(n_prompt, max_tokens)
+        if rc:
+            return rc, None
+        st = np.zeros(n, dtype=np.uint8)
+        pg = np.ascontiguousarray(page)
+        rc = lib().ck_state_from_page(self._h, pg.ctypes.data, pg.size, st.ctypes.data, st.size)
+        return rc, st
 
     def turn_noalloc(self, state, stream=None):
         """One position through ck_turn_noalloc (no device allocation, shared scratch)."""

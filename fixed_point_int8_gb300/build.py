@@ -11,7 +11,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libck.so")
-SOURCES = ["ck_api.cu", "ck_matrow.cu", "ck_attention.cu", "ck_step.cu", "ck_batch.cu", "ck_token.cu"]
+SOURCES = ["ck_api.cu", "ck_matrow.cu", "ck_attention.cu", "ck_step.cu", "ck_batch.cu", "ck_token.cu", "ck_page.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr"]

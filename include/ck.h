@@ -277,6 +277,27 @@ int ck_encode(const ck_tokenizer* t, const uint8_t* text, size_t len, uint32_t* 
 int ck_decode(const ck_tokenizer* t, uint32_t prev, const uint32_t* ids, uint32_t n, uint8_t* out,
               size_t cap, size_t* n_bytes);
 
+/* ---------------------------------------------------------------- the page's state
+ * The page's resumable state ("The resumable state": CURTAST2, a 128-byte header, the
+ * prompt's bytes and tokens, output tokens and text, activations, working vectors, logits,
+ * scores, and the caches in [layer][position][kv_dim] order), which its core runs one chunk
+ * at a time and can stop at any phase boundary, mid-layer included.  These convert between
+ * it and this library's state at position boundaries (host copies of both). */
+/* Size of a page state for prompt_bytes bytes of prompt and max_tokens.  Errors: 10. */
+int ck_page_size(const ck_model* m, uint32_t prompt_bytes, uint32_t max_tokens, size_t* out);
+/* This library's state (running or done, made with CK_FLAG_STOP_TOKENS since the page's runs
+ * end at tokens 1 and 2, its prompt ids the encoding of `prompt` by t) into a page state at
+ * the start of its next position (phase 3), or done (phase 20); the output text is decoded
+ * with t.  Errors: 3 (not such a state), 4 (page_len not ck_page_size), 6 (prompt), 7 (the
+ * page's cache would be smaller), 10. */
+int ck_state_to_page(const ck_model* m, const ck_tokenizer* t, const void* host_state, size_t len,
+                     const uint8_t* prompt, size_t prompt_len, void* host_page, size_t page_len);
+/* A page state at a position boundary (phase 3 at layer 0, or 20) into this library's
+ * state (len = ck_state_size for its prompt tokens and max tokens).  Errors: 3 (not such a
+ * page state, or one stopped mid-position: run it on to the next position first), 4, 10. */
+int ck_state_from_page(const ck_model* m, const void* host_page, size_t page_len, void* host_state,
+                       size_t len);
+
 /* The page's output_tokens: copies min(generated, cap) token ids to host_out and the count
  * to *n.  Synchronizes.  Errors: 3, 9, 10. */
 int ck_output_tokens(const ck_model* m, const void* dev_state, size_t len, uint32_t* host_out,

@@ -1054,6 +1054,7 @@ static int page_step(const orc_model* m, const orc_vocab* voc, uint8_t* st, cons
       } else if (pos + 1 < np) {                          /* the next prompt position */
         wr32(st + P_POS, pos + 1);
         wr32(st + P_TOKEN, ptok[pos + 1]);
+        wr32(st + P_LAYER, 0);
         wr32(st + P_PHASE, 3);
       } else {
         wr32(st + P_PHASE, 17);
@@ -1082,6 +1083,7 @@ static int page_step(const orc_model* m, const orc_vocab* voc, uint8_t* st, cons
       } else {
         wr32(st + P_POS, pos + 1);
         wr32(st + P_TOKEN, t);
+        wr32(st + P_LAYER, 0);
         wr32(st + P_PHASE, 3);
       }
       return 0;

@@ -716,6 +716,68 @@ def test_text_prompt_to_text_output(ck, temp):
     assert rc == 0 and got == v.decode(list(out), prev=int(ids[-1]))
 
 
+@pytest.mark.parametrize("stride", [7, 1])
+def test_page_state_round_trip_with_mid_layer_stops(ck, stride):
+    """A text prompt run on the GPU into its generating positions; the state converted into
+    the page's CURTAST2 state; the oracle's page executor runs it on in stops of `stride`
+    steps (mid-layer and mid-attention) for two more positions; converted back at a position
+    boundary, the GPU finishes the run.  Every byte equals the oracle's ids-mode run."""
+    wl = MODELS["gqa"]
+    spec = wl.spec
+    blob = synth.tokenizer_blob(spec.vocab, spec.seed)
+    rc, tok = ck.Tokenizer.load(blob, spec.vocab)
+    assert rc == 0
+    v = oracle.Vocab(blob, spec.vocab)
+    text = synth.prompt_text(10, spec.seed, 2, blob)
+    rc, ids = tok.encode(text)
+    assert rc == 0
+    steps = 12
+    P = Pair(ck, spec, "step")
+    so, sg = P.init(ck, ids, steps, flags=ck.CK_FLAG_STOP_TOKENS, temperature_q16=3 << 15, seed=21)
+    rco, _ = P.orc.turn(so, 10**6)
+    assert rco == 0
+    rc, _ = P.gpu.turn(sg, len(ids))                  # the prompt and the first token
+    assert rc == 0
+    rc, page = P.gpu.state_to_page(tok, ck.state_download(sg), text)
+    assert rc == 0
+    h0 = oracle.page_header(page)
+    assert h0["phase"] == 3 and h0["position"] == len(ids)
+    stops = 0
+    while True:
+        h = oracle.page_header(page)
+        if h["phase"] == 20 or (h["phase"] == 3 and h["position"] >= h0["position"] + 2):
+            break
+        near = h["phase"] >= 17 and h["position"] == h0["position"] + 1
+        rc, ran = oracle.page_turn(P.orc, v, page, 1 if near else stride)
+        assert rc == 0 and ran >= 1
+        stops += 1
+        if stops % 5 == 2:
+            assert h["phase"] in range(3, 20)            # really mid-position
+    assert stops > 10
+    rc, back = P.gpu.state_from_page(page, len(ids), steps)
+    assert rc == 0
+    ck.state_upload(sg, back)
+    rc, _ = P.gpu.turn(sg, 10**6)
+    assert rc == 0
+    compare_states(P.orc, so, ck.state_download(sg), len(ids), steps, "page round trip", turns=False)
+    # the page's output text is the decoded output
+    hp = oracle.page_header(page)
+    pl = oracle.page_layout(P.orc, len(text), steps)
+    out = page[pl["out"]:pl["out"] + 4 * hp["generated"]].view("<u4").tolist()
+    assert page[pl["text"]:pl["text"] + hp["text_bytes"]].tobytes() == tok.decode(out, prev=int(ids[-1]))[1]
+    # not a position boundary: refused
+    rc, page2 = P.gpu.state_to_page(tok, ck.state_download(sg), text)
+    oracle.page_turn(P.orc, v, page2, 0)
+    assert P.gpu.state_from_page(page2, len(ids), steps)[0] == 0          # done: a boundary
+    rc, sg2 = P.init(ck, ids, steps, flags=ck.CK_FLAG_STOP_TOKENS)
+    rc, page3 = P.gpu.state_to_page(tok, ck.state_download(sg2), text)
+    assert rc == 0
+    oracle.page_turn(P.orc, v, page3, 2)                # into position 0's layer 0
+    assert P.gpu.state_from_page(page3, len(ids), steps)[0] == 3
+    so4, sg4 = P.init(ck, ids, steps)                   # without the stop-token flag
+    assert P.gpu.state_to_page(tok, ck.state_download(sg4), text)[0] == 3
+
+
 def test_paths_agree_and_unknown_path_is_rejected(ck):
     wl = MODELS["gqa"]
     P = Pair(ck, wl.spec, "step")

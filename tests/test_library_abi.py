@@ -116,3 +116,12 @@ def test_library_tokenizer_matches_the_oracle():
     assert ck.Tokenizer.load(dup, 2)[0] == 2                               # a repeated string
     with pytest.raises(ValueError):
         oracle.Vocab(dup, 2)
+
+
+# ---------------------------------------------------------------- the page's state (host code)
+
+def test_page_converters_reject_wrong_inputs():
+    import fixed_point_int8_gb300 as ck
+    lib = ck.lib()
+    assert lib.ck_page_size(None, 1, 1, None) == 10
+    assert lib.ck_state_from_page(None, None, 0, None, 0) == 10
