@@ -42,6 +42,7 @@ sys.path.insert(0, ROOT)
 
 import numpy as np  # noqa: E402
 
+PATHS = {"auto": 0, "step": 1, "kernels": 2}  # ck_set_path values (CK_PATH_AUTO, _STEP, _KERNELS)
 METRIC = "decode tokens/s bit-exact vs oracle; matrow HBM GB/s as % of GB300 peak"
 WORKLOAD = ("llama7b_shape fixed-point decode: dim 4096, 32 layers, 32 heads x 128, FFN hidden 11008, "
             "vocab 32000, context 2048, u8 weights + u32 row scales (6.61 GB/token); 128 prompt ids "
@@ -225,15 +226,16 @@ def run_ours(args):
         return
     if args.long_only:
         # profiling aid: only the long-context measurement (optionally cut to fewer layers)
-        print(json.dumps({"long_context": long_context(ck, torch, synth, args.long_steps, args.long_layers)}),
+        print(json.dumps({"long_context": long_context(ck, torch, synth, args.long_steps, args.long_layers, PATHS[args.path])}),
               flush=True)
         return
     if args.matrow_only:
         # profiling aid: only the matrix-row timing of one shape, e.g. 22016x4096
         rows, cols = (int(v) for v in args.matrow_only.split("x"))
-        avg, nb = time_matrow(ck, torch, rows, cols, 5)
+        avg, nb, alone = time_matrow(ck, torch, rows, cols, 5)
         print(json.dumps({"matrow": args.matrow_only, "us": round(avg * 1e3, 2),
-                          "GB/s": round(nb / (avg * 1e-3) / 1e9, 1)}), flush=True)
+                          "GB/s": round(nb / (avg * 1e-3) / 1e9, 1), "us_one_by_one": round(alone * 1e3, 2)}),
+              flush=True)
         return
     spec = synth.LLAMA7B
     if args.layers:
@@ -250,7 +252,7 @@ def run_ours(args):
     ids = synth.prompt_ids(spec, n_prompt, run=rank)
     rc, model = ck.Model.load(art)
     assert rc == 0, f"ck_load_model failed: {rc}"
-    path = {"auto": ck.PATH_AUTO, "step": ck.PATH_STEP, "kernels": ck.PATH_KERNELS}[args.path]
+    path = PATHS[args.path]
     assert model.set_path(path) == 0
     state = model.new_state(n_prompt, max_tokens)
     assert model.init_state(state, ids, max_tokens) == 0
@@ -337,7 +339,7 @@ def run_ours(args):
             batched = batched_runs(ck, torch, synth, args.batched_passes)
             torch.cuda.empty_cache()
         if args.long_steps:
-            longc = long_context(ck, torch, synth, args.long_steps, 0)
+            longc = long_context(ck, torch, synth, args.long_steps, 0, path)
 
     if rank != 0:
         return
@@ -436,15 +438,17 @@ def batched_runs(ck, torch, synth, passes):
                     "planes multiply the tensor work by the plane count (3 here)"}
 
 
-def long_context(ck, torch, synth, steps, layers):
+def long_context(ck, torch, synth, steps, layers, path=0):
     """The 1B-shaped model at 8,192 context: 7,936 prompt ids prefilled layer-major (one
-    ck_turn), then `steps` generating positions in one ck_turn, both device-timed."""
+    ck_turn), then `steps` generating positions in one ck_turn, both device-timed; `path`
+    is the ck_set_path choice for the generating positions."""
     import dataclasses
     wl = synth.WORKLOADS["1b_long"]
     spec = wl.spec if not layers else dataclasses.replace(wl.spec, layers=layers)
     steps = max(1, min(steps, wl.steps - 4))
     rc, m = ck.Model.load(synth.build_artifact(spec))
     assert rc == 0
+    assert m.set_path(path) == 0
     st = m.new_state(wl.n_prompt, wl.steps)
     assert m.init_state(st, synth.prompt_ids(spec, wl.n_prompt), wl.steps) == 0
     stream = torch.cuda.current_stream()
@@ -476,9 +480,12 @@ def long_context(ck, torch, synth, steps, layers):
 
 
 def time_matrow(ck, torch, rows, cols, iters):
-    """Average duration (ms) of ck_matrow launches of one shape, timed one by one with CUDA
-    events on the current stream; the matrix rotates through copies totalling three times
-    the L2 size so every launch streams from HBM.  Returns (ms, algorithmic bytes)."""
+    """Average duration (ms) of ck_matrow launches of one shape.  The launches run back to back
+    on the current stream between one pair of CUDA events, queued behind a device-side wait so
+    that host-side call overhead never leaves the GPU idle inside the timed region; the matrix
+    rotates through copies totalling three times the L2 size so every launch streams from HBM.
+    Also returns the average of the same launches timed one by one (an event pair around each).
+    Returns (ms back to back, algorithmic bytes, ms one by one)."""
     import synth
     stream = torch.cuda.current_stream()
     l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 128 << 20)
@@ -493,6 +500,15 @@ def time_matrow(ck, torch, rows, cols, iters):
     for i in range(3):
         rc, _ = ck.matrow(Ws[i % copies], sd, xd, out=y)
         assert rc == 0
+    torch.cuda.synchronize()
+    torch.cuda._sleep(4_000_000)  # about 2 ms of device time while the host queues the launches
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(iters):
+        ck.matrow(Ws[i % copies], sd, xd, out=y)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms_run = a.elapsed_time(b) / iters
     times = []
     for i in range(iters):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -501,33 +517,36 @@ def time_matrow(ck, torch, rows, cols, iters):
         b.record(stream)
         times.append((a, b))
     torch.cuda.synchronize()
-    ms = [a.elapsed_time(b) for a, b in times]
+    ms_alone = sum(a.elapsed_time(b) for a, b in times) / iters
     del Ws, Wd
     torch.cuda.empty_cache()
-    return sum(ms) / len(ms), matrow_bytes(rows, cols)
+    return ms_run, matrow_bytes(rows, cols), ms_alone
 
 
 def matrow_measurements(ck, torch, args):
-    """Times ck_matrow launches with CUDA events on the current stream; matrices rotate
-    through copies whose total exceeds the L2 cache so every launch streams from HBM."""
+    """Times ck_matrow launches with CUDA events on the current stream, back to back (the
+    reported figure) and one by one (context: each then also pays the launch and event
+    latency); matrices rotate through copies whose total exceeds the L2 cache so every
+    launch streams from HBM."""
     import synth
     hbm, peak_kind = load_peaks()
-    time_shape = lambda rows, cols, iters: time_matrow(ck, torch, rows, cols, iters)
     sweep = {}
     for rows, cols in synth.MATROW_SHAPES:
-        avg, nb = time_shape(rows, cols, 30)
+        avg, nb, alone = time_matrow(ck, torch, rows, cols, 30)
         gbs = nb / (avg * 1e-3) / 1e9
         sweep[f"{rows}x{cols}"] = {"us": round(avg * 1e3, 2), "GB/s": round(gbs, 1),
-                                   "frac_of_peak": round(gbs / hbm, 4)}
+                                   "frac_of_peak": round(gbs / hbm, 4), "us_one_by_one": round(alone * 1e3, 2)}
     rows, cols = 2 * 11008, 4096
-    avg, nb = time_shape(rows, cols, 30)
+    avg, nb, alone = time_matrow(ck, torch, rows, cols, 30)
     achieved = nb / (avg * 1e-3) / 1e9
     key = f"{rows}x{cols}"
     traffic = ncu_traffic(key)
     roof = {"kernel": "k_matrow", "launch": f"{key} (gate and up rows of one 7B layer)",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
             "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
-            "traffic": traffic, "algorithmic_bytes": nb, "avg_launch_us": round(avg * 1e3, 2)}
+            "traffic": traffic, "algorithmic_bytes": nb, "avg_launch_us": round(avg * 1e3, 2),
+            "timing": "30 launches back to back between one event pair",
+            "avg_launch_us_one_by_one": round(alone * 1e3, 2)}
     return roof, sweep
 
 

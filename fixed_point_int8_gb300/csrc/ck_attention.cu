@@ -21,6 +21,16 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kU = 8;  // warp steps whose cache loads are in flight together
+
+// A 16-byte cache load that bypasses L1: each cache word is read once per position.
+__device__ __forceinline__ int4 ld_nc_int4(const int32_t* p) {
+  int4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
 
 __device__ __forceinline__ long long warp_max(long long v) {
 #pragma unroll
@@ -38,6 +48,10 @@ __device__ __forceinline__ unsigned long long warp_sum(unsigned long long v) {
 
 __global__ void __launch_bounds__(kThreads) k_attention(const AttnParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
+  // launched with programmatic dependent launch: wait for the kernels before this one on the
+  // stream (the queries and the cache words they wrote), then let the next kernel start early
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (hdr_ld<uint32_t>(p.state, kHPhase) != CK_PHASE_RUNNING) return;  // whole cluster alike
   cg::cluster_group cluster = cg::this_cluster();
   const uint32_t hd = p.head_dim;
@@ -69,24 +83,31 @@ __global__ void __launch_bounds__(kThreads) k_attention(const AttnParams p) {
   const uint32_t sub = lane % lpp, slot = lane / lpp, e0 = sub * 4;
   const int64_t q0 = q_s[e0], q1 = q_s[e0 + 1], q2 = q_s[e0 + 2], q3 = q_s[e0 + 3];
 
-  // stage 0: s_t = (((q . k_t) >> 16) * inv) >> 24, products and sums wrapping; keep the max
+  // stage 0: s_t = (((q . k_t) >> 16) * inv) >> 24, products and sums wrapping; keep the max.
+  // A warp takes kU steps of ppw positions at once, so that kU loads a lane are in flight.
+  const uint32_t step = kWarps * ppw;  // positions the CTA covers per warp step
   long long lmax = LLONG_MIN;
-  for (uint32_t base = warp * ppw; base < n; base += kWarps * ppw) {
-    const uint32_t tl = base + slot;
-    unsigned long long d = 0;
-    if (tl < n) {
-      const int4 k4 = *reinterpret_cast<const int4*>(Kh + (size_t)(t0 + tl) * hd + e0);
-      d = (unsigned long long)q0 * (unsigned long long)(long long)k4.x +
-          (unsigned long long)q1 * (unsigned long long)(long long)k4.y +
-          (unsigned long long)q2 * (unsigned long long)(long long)k4.z +
-          (unsigned long long)q3 * (unsigned long long)(long long)k4.w;
+  for (uint32_t base = warp * ppw; base < n; base += kU * step) {
+    int4 k4[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const uint32_t tl = base + u * step + slot;
+      k4[u] = tl < n ? ld_nc_int4(Kh + (size_t)(t0 + tl) * hd + e0) : make_int4(0, 0, 0, 0);
     }
-    for (uint32_t o = lpp >> 1; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-    if (tl < n && sub == 0) {
-      long long s = (long long)d >> 16;
-      s = (long long)((unsigned long long)s * (unsigned long long)p.inv_sqrt) >> 24;
-      sc[tl] = s;
-      lmax = s > lmax ? s : lmax;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const uint32_t tl = base + u * step + slot;
+      unsigned long long d = (unsigned long long)q0 * (unsigned long long)(long long)k4[u].x +
+                             (unsigned long long)q1 * (unsigned long long)(long long)k4[u].y +
+                             (unsigned long long)q2 * (unsigned long long)(long long)k4[u].z +
+                             (unsigned long long)q3 * (unsigned long long)(long long)k4[u].w;
+      for (uint32_t o = lpp >> 1; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+      if (tl < n && sub == 0) {
+        long long s = (long long)d >> 16;
+        s = (long long)((unsigned long long)s * (unsigned long long)p.inv_sqrt) >> 24;
+        sc[tl] = s;
+        lmax = s > lmax ? s : lmax;
+      }
     }
   }
   lmax = warp_max(lmax);
@@ -132,15 +153,21 @@ __global__ void __launch_bounds__(kThreads) k_attention(const AttnParams p) {
 
   // stage 3: sum over positions of P_t * v_t[j] (exact: |sum| < 2^55), then one >> 24
   unsigned long long a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-  for (uint32_t base = warp * ppw; base < n; base += kWarps * ppw) {
-    const uint32_t tl = base + slot;
-    if (tl < n) {
-      const int4 v4 = *reinterpret_cast<const int4*>(Vh + (size_t)(t0 + tl) * hd + e0);
-      const long long pr = sc[tl];
-      a0 += (unsigned long long)(pr * (long long)v4.x);
-      a1 += (unsigned long long)(pr * (long long)v4.y);
-      a2 += (unsigned long long)(pr * (long long)v4.z);
-      a3 += (unsigned long long)(pr * (long long)v4.w);
+  for (uint32_t base = warp * ppw; base < n; base += kU * step) {
+    int4 v4[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const uint32_t tl = base + u * step + slot;
+      v4[u] = tl < n ? ld_nc_int4(Vh + (size_t)(t0 + tl) * hd + e0) : make_int4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const uint32_t tl = base + u * step + slot;
+      const long long pr = tl < n ? sc[tl] : 0;
+      a0 += (unsigned long long)(pr * (long long)v4[u].x);
+      a1 += (unsigned long long)(pr * (long long)v4[u].y);
+      a2 += (unsigned long long)(pr * (long long)v4[u].z);
+      a3 += (unsigned long long)(pr * (long long)v4[u].w);
     }
   }
   for (uint32_t o = 16; o >= lpp && o > 0; o >>= 1) {
@@ -191,13 +218,15 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t s, int cluster) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = (unsigned)cluster;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, k_attention, p);
 }
 

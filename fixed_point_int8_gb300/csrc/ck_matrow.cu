@@ -1,8 +1,12 @@
 // The matrix-row kernel: y[r] = ((sum_c byte[r][c] * x[c] - 128 * sum_c x[c]) * scale[r]) >> 24
 // with every product and sum wrapping in 64 bits ("The inference core", "A matrix row").
 //
-// GB300 design.  One CTA per SM streams whole rows with 16-byte non-allocating loads.
-// Before the rows, every CTA packs the input vector into shared memory as byte planes:
+// GB300 design.  One CTA per SM (at most) takes an even-aligned share of the rows, so every
+// SM streams even for 4,096-row matrices and both rows of a gate/up or rotary pair finish in
+// the same CTA.  Its warps stream work items of 8 rows by a 512-byte column slice with 16-byte
+// non-allocating loads, loading the next item while they work on the current one; the first
+// item is requested before the vector is packed.  Before the rows, every CTA packs the input
+// vector into shared memory as byte planes:
 // plane k holds byte k of every x[c].  A vector whose values all fit in 8L signed bits is
 // exactly sum_{k<L-1} plane_k 2^(8k) + signed(plane_{L-1}) 2^(8(L-1)), so
 //   sum_c byte[r][c] * x[c] = sum_k 2^(8k) sum_c byte[r][c] * plane_k[c]
@@ -18,7 +22,9 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kR = 4;  // rows a warp accumulates at once
+constexpr int kG = 8;                 // rows of one work item
+constexpr uint32_t kSlice = 512;      // bytes of a row in one work item, 16 a lane
+constexpr uint32_t kChunkRows = 256;  // rows a CTA finishes at once
 
 struct Scratch {
   unsigned long long red[kWarps];
@@ -26,7 +32,15 @@ struct Scratch {
   InvDiv div;
   unsigned long long S;
   unsigned long long orv;
+  unsigned long long tot[kChunkRows];  // row totals of the current chunk
 };
+
+// Programmatic dependent launch.  wait_prior_grids returns once the kernels before this one
+// on the stream have completed and their writes are visible (at once when the launch did not
+// allow an early start); allow_next_grid lets the next such kernel start its own independent
+// prologue on SMs this grid frees.
+__device__ __forceinline__ void wait_prior_grids() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ unsigned long long warp_sum(unsigned long long v) {
 #pragma unroll
@@ -128,12 +142,10 @@ __device__ int prologue(const MatrowParams& p, uint32_t* planes32, Scratch* sc,
   return L;
 }
 
-// Epilogue for the row handled by this lane (lanes 0..kR-1 of the warp, row r0 + lane).
+// Epilogue of one finished row: y is its scaled sum, partner that of row ^ 1 (the other half
+// of a gate/up or rotary pair; unused for plain stores).
 __device__ __forceinline__ void epilogue(const MatrowParams& p, uint32_t row, int64_t y,
-                                         uint32_t pos) {
-  const int lane = threadIdx.x & 31;
-  const int64_t partner = (int64_t)__shfl_xor_sync(0xffffffffu, (unsigned long long)y, 1);
-  if (lane >= kR || row >= p.rows) return;
+                                         int64_t partner, uint32_t pos) {
   if (p.epi == kEpiStore) {
     p.out[row] = y;
   } else if (p.epi == kEpiSiLU) {
@@ -166,120 +178,212 @@ __device__ __forceinline__ void epilogue(const MatrowParams& p, uint32_t row, in
   }
 }
 
+// The rows of a CTA: an even-aligned share of the row pairs, so that both rows of a gate/up
+// or rotary pair finish in the same CTA.
+__device__ __forceinline__ void cta_rows(const MatrowParams& p, uint32_t& rb, uint32_t& re) {
+  const uint32_t pairs = (p.rows + 1) / 2;
+  rb = 2 * (uint32_t)((uint64_t)blockIdx.x * pairs / gridDim.x);
+  re = min(2 * (uint32_t)((uint64_t)(blockIdx.x + 1) * pairs / gridDim.x), p.rows);
+}
+
+// Loads work item `it` of the chunk [c0, c1) into w: rows c0 + kG * (it / ns) onwards (at
+// most kG, not past c1) over the 512-byte column slice it % ns, 16 bytes a lane.  Rows past the
+// chunk, columns past the pitch and items past the last read as zero bytes.
+template <bool kGrouped>
+__device__ __forceinline__ void load_item(const MatrowParams& p, uint32_t c0, uint32_t c1,
+                                          uint32_t ns, uint32_t it, uint32_t items, uint4 (&w)[kG]) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t g = it / ns, s = it - g * ns;
+  const uint32_t r0 = c0 + g * kG, c = s * kSlice + lane * 16;
+  const bool live = it < items && c < p.pitch;
+  const size_t gstride = (size_t)p.rows * kGroupCols;  // grouped: bytes between column groups
+#pragma unroll
+  for (int r = 0; r < kG; ++r) {
+    const uint32_t row = r0 + r;
+    w[r] = make_uint4(0u, 0u, 0u, 0u);
+    if (live && row < c1) {
+      w[r] = kGrouped ? ld_stream16(p.W + (size_t)row * kGroupCols + (size_t)(c >> 7) * gstride +
+                                    ((c & 0x70u) ^ ((row & 7u) << 4)))
+                      : ld_stream16(p.W + (size_t)row * p.pitch + c);
+    }
+  }
+}
+
+// Sums the eight per-lane values v[0..7] over the warp: afterwards every lane holds the
+// total of row (lane >> 2).  Each exchange step halves the values a lane carries, so the
+// whole reduction takes nine 64-bit shuffles instead of eight full butterflies.
+__device__ __forceinline__ unsigned long long reduce_rows8(const unsigned long long (&v)[kG]) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long u[4], t[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const unsigned long long keep = b4 ? v[j + 4] : v[j], send = b4 ? v[j] : v[j + 4];
+    u[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const unsigned long long keep = b3 ? u[j + 2] : u[j], send = b3 ? u[j] : u[j + 2];
+    t[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  unsigned long long s = (b2 ? t[1] : t[0]) + __shfl_xor_sync(0xffffffffu, b2 ? t[0] : t[1], 4);
+  s += __shfl_xor_sync(0xffffffffu, s, 2);
+  s += __shfl_xor_sync(0xffffffffu, s, 1);
+  return s;
+}
+
+// Accumulates rows [h, h + H) of an item: byte-plane dp4a runs, then each row's planes
+// recombined into one 64-bit partial (the top plane signed).
+template <int L, int H>
+__device__ __forceinline__ void item_rows(const uint4 (&w)[kG], const uint8_t* xp, uint32_t pitch,
+                                          int h, unsigned long long (&sums)[kG]) {
+  uint32_t acc[H][L];
+#pragma unroll
+  for (int r = 0; r < H; ++r)
+#pragma unroll
+    for (int k = 0; k < L; ++k) acc[r][k] = 0;
+#pragma unroll
+  for (int k = 0; k < L; ++k) {
+    const uint4 xk = *reinterpret_cast<const uint4*>(xp + (size_t)k * pitch);
+#pragma unroll
+    for (int r = 0; r < H; ++r) {
+      const uint4 wr = w[h + r];
+      if (k < L - 1) {
+        uint32_t a = acc[r][k];
+        a = __dp4a(wr.x, xk.x, a);
+        a = __dp4a(wr.y, xk.y, a);
+        a = __dp4a(wr.z, xk.z, a);
+        a = __dp4a(wr.w, xk.w, a);
+        acc[r][k] = a;
+      } else {
+        int a = (int)acc[r][k];
+        a = dp4a_us(wr.x, xk.x, a);
+        a = dp4a_us(wr.y, xk.y, a);
+        a = dp4a_us(wr.z, xk.z, a);
+        a = dp4a_us(wr.w, xk.w, a);
+        acc[r][k] = (uint32_t)a;
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < H; ++r) {
+    unsigned long long a = 0;
+#pragma unroll
+    for (int k = 0; k < L; ++k) {
+      const unsigned long long t = (k < L - 1) ? (unsigned long long)acc[r][k]
+                                               : (unsigned long long)(long long)(int)acc[r][k];
+      a += t << (8 * k);
+    }
+    sums[h + r] = a;
+  }
+}
+
+// Rows [rb, re) of W, in chunks of at most kChunkRows.  A chunk's work items (kG rows by one
+// 512-byte slice) go round-robin to the warps, each warp loading its next item while it works
+// on the current one; each item's per-row partials add into the chunk's row totals in shared
+// memory, and once all items are in, one thread per row applies the -128 * sum(x) correction,
+// the row scale and the epilogue.  wn holds the warp's first item of the first chunk, loaded
+// before the vector was packed.
 // Rows of W: row-major with the given pitch, or (kGrouped) the model's column-group layout,
 // where the 16-byte chunk at column c of row r sits at grouped_offset(rows, r, c).
 template <int L, bool kGrouped>
-__device__ void rows_loop(const MatrowParams& p, const uint8_t* planes, unsigned long long S,
-                          uint32_t pos) {
+__device__ void rows_loop(const MatrowParams& p, const uint8_t* planes, Scratch* sc,
+                          unsigned long long S, uint32_t pos, uint32_t rb, uint32_t re,
+                          uint4 (&wn)[kG]) {
+  constexpr int H = L <= 4 ? kG / 2 : kG / 4;  // rows accumulated at once (register budget)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t pitch = p.pitch;
-  const uint32_t groups = (p.rows + kR - 1) / kR;
-  const uint32_t nw = gridDim.x * kWarps;
-  for (uint32_t g = blockIdx.x * kWarps + warp; g < groups; g += nw) {
-    const uint32_t r0 = g * kR;
-    const uint8_t* wrow[kR];
-    uint32_t rsw[kR];  // grouped: the row's chunk rotation, (row & 7) << 4
+  const uint32_t pitch = p.pitch, ns = (pitch + kSlice - 1) / kSlice;
+  for (uint32_t c0 = rb; c0 < re; c0 += kChunkRows) {
+    const uint32_t c1 = min(c0 + kChunkRows, re);
+    const uint32_t items = (c1 - c0 + kG - 1) / kG * ns;
+    if (c0 != rb) load_item<kGrouped>(p, c0, c1, ns, warp, items, wn);
+    // the finishing thread's row scales, fetched while the items stream
+    const uint32_t frow = c0 + threadIdx.x, fprow = frow ^ 1u;
+    const uint32_t fscale = frow < c1 ? __ldg(p.scale + frow) : 0u;
+    const uint32_t fpscale = frow < c1 && fprow < c1 ? __ldg(p.scale + fprow) : 0u;
+    for (uint32_t it = warp; it < items; it += kWarps) {
+      uint4 w[kG];
 #pragma unroll
-    for (int r = 0; r < kR; ++r) {
-      const uint32_t row = min(r0 + r, p.rows - 1);
-      wrow[r] = kGrouped ? p.W + (size_t)row * kGroupCols : p.W + (size_t)row * pitch;
-      rsw[r] = (row & 7u) << 4;
-    }
-    const size_t gstride = (size_t)p.rows * kGroupCols;  // grouped: bytes between column groups
-    uint32_t acc[kR][L];
+      for (int r = 0; r < kG; ++r) w[r] = wn[r];
+      load_item<kGrouped>(p, c0, c1, ns, it + kWarps, items, wn);
+      const uint32_t g = it / ns, s = it - g * ns;
+      const uint32_t r0 = c0 + g * kG;
+      const uint32_t c = s * kSlice + lane * 16;
+      unsigned long long sums[kG];
+      if (c < pitch) {
+        const uint8_t* xp = planes + c;
 #pragma unroll
-    for (int r = 0; r < kR; ++r)
-#pragma unroll
-      for (int k = 0; k < L; ++k) acc[r][k] = 0;
-    for (uint32_t c = lane * 16; c < pitch; c += 512) {
-      uint4 w[kR];
-      if (kGrouped) {
-        const size_t gbase = (size_t)(c >> 7) * gstride;
-        const uint32_t chunk = c & 0x70u;
-#pragma unroll
-        for (int r = 0; r < kR; ++r) w[r] = ld_stream16(wrow[r] + gbase + (chunk ^ rsw[r]));
+        for (int h = 0; h < kG; h += H) item_rows<L, H>(w, xp, pitch, h, sums);
       } else {
 #pragma unroll
-        for (int r = 0; r < kR; ++r) w[r] = ld_stream16(wrow[r] + c);
+        for (int r = 0; r < kG; ++r) sums[r] = 0;
       }
-#pragma unroll
-      for (int k = 0; k < L; ++k) {
-        const uint4 xk = *reinterpret_cast<const uint4*>(planes + (size_t)k * pitch + c);
-#pragma unroll
-        for (int r = 0; r < kR; ++r) {
-          if (k < L - 1) {
-            uint32_t a = acc[r][k];
-            a = __dp4a(w[r].x, xk.x, a);
-            a = __dp4a(w[r].y, xk.y, a);
-            a = __dp4a(w[r].z, xk.z, a);
-            a = __dp4a(w[r].w, xk.w, a);
-            acc[r][k] = a;
-          } else {
-            int a = (int)acc[r][k];
-            a = dp4a_us(w[r].x, xk.x, a);
-            a = dp4a_us(w[r].y, xk.y, a);
-            a = dp4a_us(w[r].z, xk.z, a);
-            a = dp4a_us(w[r].w, xk.w, a);
-            acc[r][k] = (uint32_t)a;
-          }
-        }
-      }
+      const unsigned long long tot = reduce_rows8(sums);
+      const uint32_t rl = r0 - c0 + (uint32_t)(lane >> 2);
+      if ((lane & 3) == 0 && c0 + rl < c1) atomicAdd(&sc->tot[rl], tot);
     }
-    unsigned long long sums[kR];
-#pragma unroll
-    for (int r = 0; r < kR; ++r) {
-      unsigned long long a = 0;
-#pragma unroll
-      for (int k = 0; k < L; ++k) {
-        const unsigned long long t = (k < L - 1) ? (unsigned long long)acc[r][k]
-                                                 : (unsigned long long)(long long)(int)acc[r][k];
-        a += t << (8 * k);
-      }
-      sums[r] = warp_sum(a);
+    __syncthreads();
+    if (frow < c1) {
+      const uint32_t t = threadIdx.x;
+      const int64_t y = (int64_t)((sc->tot[t] - (S << 7)) * (unsigned long long)fscale) >> 24;
+      const int64_t partner =
+          fprow < c1 ? (int64_t)((sc->tot[t ^ 1u] - (S << 7)) * (unsigned long long)fpscale) >> 24 : 0;
+      epilogue(p, frow, y, partner, pos);
     }
-    unsigned long long mine = sums[0];
-#pragma unroll
-    for (int r = 1; r < kR; ++r)
-      if (lane == r) mine = sums[r];
-    const uint32_t row = r0 + (uint32_t)lane;
-    int64_t y = 0;
-    if (lane < kR && row < p.rows) {
-      const unsigned long long t = (mine - (S << 7)) * (unsigned long long)__ldg(p.scale + row);
-      y = (int64_t)t >> 24;
-    }
-    epilogue(p, row, y, pos);
+    __syncthreads();
+    for (uint32_t t = threadIdx.x; t < kChunkRows; t += kThreads) sc->tot[t] = 0;
+    __syncthreads();
   }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) k_matrow(const MatrowParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
+  uint32_t rb, re;
+  cta_rows(p, rb, re);
+  // The warp's first weights are requested before anything else: weights are never written,
+  // so this may run while the previous kernel on the stream is still finishing (the launch
+  // allows programmatic dependent launch).  Everything that reads what earlier kernels wrote
+  // (the state header, the vector) waits for their completion first.
+  uint4 wn[kG];
+  if (rb < re) {
+    const uint32_t ns = (p.pitch + kSlice - 1) / kSlice, c1 = min(rb + kChunkRows, re);
+    const uint32_t items = (c1 - rb + kG - 1) / kG * ns;
+    if (p.grouped)
+      load_item<true>(p, rb, c1, ns, threadIdx.x >> 5, items, wn);
+    else
+      load_item<false>(p, rb, c1, ns, threadIdx.x >> 5, items, wn);
+  }
+  wait_prior_grids();
+  allow_next_grid();
+  if (rb >= re) return;
   if (p.state && hdr_ld<uint32_t>(p.state, kHPhase) != CK_PHASE_RUNNING) return;
   const uint32_t pos = p.state ? hdr_ld<uint32_t>(p.state, kHPosition) : 0u;
   uint8_t* planes = smem;
   Scratch* sc = reinterpret_cast<Scratch*>(smem + 8 * (size_t)p.pitch);
+  for (uint32_t t = threadIdx.x; t < kChunkRows; t += kThreads) sc->tot[t] = 0;
   unsigned long long S;
   const int L = prologue(p, reinterpret_cast<uint32_t*>(planes), sc, &S);
   if (p.grouped) {
     switch (L) {
-      case 1: rows_loop<1, true>(p, planes, S, pos); break;
-      case 2: rows_loop<2, true>(p, planes, S, pos); break;
-      case 3: rows_loop<3, true>(p, planes, S, pos); break;
-      case 4: rows_loop<4, true>(p, planes, S, pos); break;
-      case 5: rows_loop<5, true>(p, planes, S, pos); break;
-      case 6: rows_loop<6, true>(p, planes, S, pos); break;
-      case 7: rows_loop<7, true>(p, planes, S, pos); break;
-      default: rows_loop<8, true>(p, planes, S, pos); break;
+      case 1: rows_loop<1, true>(p, planes, sc, S, pos, rb, re, wn); break;
+      case 2: rows_loop<2, true>(p, planes, sc, S, pos, rb, re, wn); break;
+      case 3: rows_loop<3, true>(p, planes, sc, S, pos, rb, re, wn); break;
+      case 4: rows_loop<4, true>(p, planes, sc, S, pos, rb, re, wn); break;
+      case 5: rows_loop<5, true>(p, planes, sc, S, pos, rb, re, wn); break;
+      case 6: rows_loop<6, true>(p, planes, sc, S, pos, rb, re, wn); break;
+      case 7: rows_loop<7, true>(p, planes, sc, S, pos, rb, re, wn); break;
+      default: rows_loop<8, true>(p, planes, sc, S, pos, rb, re, wn); break;
     }
   } else {
     switch (L) {
-      case 1: rows_loop<1, false>(p, planes, S, pos); break;
-      case 2: rows_loop<2, false>(p, planes, S, pos); break;
-      case 3: rows_loop<3, false>(p, planes, S, pos); break;
-      case 4: rows_loop<4, false>(p, planes, S, pos); break;
-      case 5: rows_loop<5, false>(p, planes, S, pos); break;
-      case 6: rows_loop<6, false>(p, planes, S, pos); break;
-      case 7: rows_loop<7, false>(p, planes, S, pos); break;
-      default: rows_loop<8, false>(p, planes, S, pos); break;
+      case 1: rows_loop<1, false>(p, planes, sc, S, pos, rb, re, wn); break;
+      case 2: rows_loop<2, false>(p, planes, sc, S, pos, rb, re, wn); break;
+      case 3: rows_loop<3, false>(p, planes, sc, S, pos, rb, re, wn); break;
+      case 4: rows_loop<4, false>(p, planes, sc, S, pos, rb, re, wn); break;
+      case 5: rows_loop<5, false>(p, planes, sc, S, pos, rb, re, wn); break;
+      case 6: rows_loop<6, false>(p, planes, sc, S, pos, rb, re, wn); break;
+      case 7: rows_loop<7, false>(p, planes, sc, S, pos, rb, re, wn); break;
+      default: rows_loop<8, false>(p, planes, sc, S, pos, rb, re, wn); break;
     }
   }
 }
@@ -296,12 +400,20 @@ cudaError_t configure_matrow() {
 cudaError_t launch_matrow(const MatrowParams& p, cudaStream_t s, int num_sms) {
   const size_t smem = matrow_smem_bytes(p.pitch);
   if (p.pitch > 16384) return cudaErrorInvalidValue;
-  const uint32_t groups = (p.rows + kR - 1) / kR;
-  uint32_t blocks = (groups + kWarps - 1) / kWarps;
-  if (blocks > (uint32_t)num_sms) blocks = (uint32_t)num_sms;
+  const uint32_t pairs = (p.rows + 1) / 2;
+  uint32_t blocks = pairs < (uint32_t)num_sms ? pairs : (uint32_t)num_sms;
   if (blocks < 1) blocks = 1;
-  k_matrow<<<blocks, kThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_matrow, p);
 }
 
 }  // namespace ck
