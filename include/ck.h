@@ -100,10 +100,13 @@ int ck_model_config(const ck_model* m, ck_config* out);
 /* How ck_turn runs a position.  CK_PATH_STEP: one persistent kernel per position (one
  * block per SM, launched cooperatively): a producer warp streams every matrix of the
  * position through shared memory with bulk copies while consumer warps compute, with grid
- * barriers between dependent phases.  CK_PATH_KERNELS: one kernel per phase.  CK_PATH_AUTO
- * (the default) takes the persistent kernel whenever the model and state fit it (heads <=
- * 1000, enough shared memory and state work area) and the phase kernels otherwise.  Both compute the same bits.  Errors: 10 for an unknown path;
- * ck_turn returns 10 when CK_PATH_STEP is forced on a model or state it cannot run. */
+ * barriers between dependent phases.  CK_PATH_KERNELS: one kernel per phase, launched with
+ * programmatic dependent launch so that each kernel's weight loads start while the previous
+ * one finishes.  CK_PATH_AUTO (the default) takes the phase kernels, the faster of the two on
+ * every model measured; CK_PATH_STEP runs only where the model and state fit it (heads <=
+ * 1000, enough shared memory and state work area).  Both compute the same bits.  Errors: 10
+ * for an unknown path; ck_turn returns 10 when CK_PATH_STEP is forced on a model or state it
+ * cannot run. */
 #define CK_PATH_AUTO 0
 #define CK_PATH_STEP 1
 #define CK_PATH_KERNELS 2

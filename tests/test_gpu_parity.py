@@ -454,6 +454,22 @@ def test_1b_long_context_sampled_position(ck, path):
     assert h["generated"] == 1 and h["position"] == wl.n_prompt
 
 
+# (dim, heads, kv_heads): head sizes 128, 32 (grouped), 16, 8 and 4
+LONG_ATTENTION = [(256, 2, 2), (256, 8, 4), (64, 4, 4), (64, 8, 8), (64, 16, 16)]
+
+
+@pytest.mark.parametrize("dim,heads,kv_heads", LONG_ATTENTION)
+def test_long_cache_attention_kernel(ck, dim, heads, kv_heads):
+    """The per-phase path on states whose cache gives each attention CTA more than 128
+    positions (the long-cache attention kernel): 1059 prompt positions on the GPU, then the
+    generating position over 1060 cached positions against the oracle, every buffer."""
+    spec = synth.ModelSpec(f"long_attention_{dim}_{heads}_{kv_heads}", dim, 172, 2, heads, kv_heads, 512,
+                           1100, scale_rule="well", tied=False, seed=0x5EED0031)
+    h = _resume_one(ck, spec, n_prompt=1060, max_tokens=8, gpu_positions=1059, check_positions=1,
+                    path="kernels")
+    assert h["generated"] == 1
+
+
 def test_1b_sixty_four_runs_sampled(ck):
     """The 1B-shaped model with 64 independent runs (64 prompt ids each, own state and
     cache), advanced in turns interleaved like a serving loop; sampled runs then take one
