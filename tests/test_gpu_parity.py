@@ -460,9 +460,9 @@ LONG_ATTENTION = [(256, 2, 2), (256, 8, 4), (64, 4, 4), (64, 8, 8), (64, 16, 16)
 
 @pytest.mark.parametrize("dim,heads,kv_heads", LONG_ATTENTION)
 def test_long_cache_attention_kernel(ck, dim, heads, kv_heads):
-    """The per-phase path on states whose cache gives each attention CTA more than 128
-    positions (the long-cache attention kernel): 1059 prompt positions on the GPU, then the
-    generating position over 1060 cached positions against the oracle, every buffer."""
+    """The per-phase attention kernel over 1060 cached positions (each cluster CTA walks about
+    133 of them, several unrolled load batches): 1059 prompt positions on the GPU, then the
+    generating position against the oracle, every buffer, at head sizes 128 to 4."""
     spec = synth.ModelSpec(f"long_attention_{dim}_{heads}_{kv_heads}", dim, 172, 2, heads, kv_heads, 512,
                            1100, scale_rule="well", tied=False, seed=0x5EED0031)
     h = _resume_one(ck, spec, n_prompt=1060, max_tokens=8, gpu_positions=1059, check_positions=1,
