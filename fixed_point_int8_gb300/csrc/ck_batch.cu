@@ -45,6 +45,14 @@ __device__ __forceinline__ bool running(const uint8_t* gate) {
   return gate == nullptr || hdr_ld<uint32_t>(gate, kHPhase) == CK_PHASE_RUNNING;
 }
 
+// Programmatic dependent launch: the per-layer kernels are launched so that their blocks may
+// be scheduled while the previous kernel on the stream finishes; each waits here, before its
+// first global read or write, until that kernel has completed and its writes are visible.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ int32_t* layer_cache(const RowDesc& r, uint64_t off, uint32_t layer,
                                                 uint32_t kv_dim) {
   return reinterpret_cast<int32_t*>(r.st + off) + (size_t)layer * r.cache * kv_dim;
@@ -124,6 +132,7 @@ __global__ void __launch_bounds__(kRowThreads) k_bnorm(const uint8_t* gate, cons
                                                         unsigned long long* orw) {
   __shared__ unsigned long long red[kRowThreads / 32];
   __shared__ InvDiv div;
+  pdl_enter();
   if (!running(gate)) return;
   const int64_t* x = X + (size_t)blockIdx.x * d;
   int64_t* y = XB + (size_t)blockIdx.x * d;
@@ -169,6 +178,7 @@ __global__ void __launch_bounds__(kRowThreads) k_bplanes(const uint8_t* gate, co
                                                           uint32_t Npad, uint32_t KG,
                                                           const unsigned long long* orw, uint8_t* B,
                                                           int32_t* S, uint32_t clear_rows) {
+  pdl_enter();
   if (!running(gate)) return;
   const int L = limbs_of_or(*orw);
   if (clear_rows) {
@@ -468,6 +478,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_bgemm(const uint8_t* gate, co
   __shared__ TcBars bar;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  pdl_enter();
   if (!running(gate)) return;
   const int L = limbs_of_or(*orw);
   const uint32_t cols = (uint32_t)L * Npad;  // plane columns in use (a multiple of 64)
@@ -543,6 +554,7 @@ __device__ __forceinline__ int64_t combine(const BEpiParams& p, int L, uint32_t 
 // the states of the rows that generate a token.
 __global__ void __launch_bounds__(kRowThreads) k_bepi(const BEpiParams p) {
   __shared__ unsigned long long red[kRowThreads / 32];
+  pdl_enter();
   if (!running(p.gate)) return;
   const int L = limbs_of_or(*p.orw);
   const uint32_t pairs = (p.rows + 1) / 2;
@@ -655,6 +667,7 @@ __device__ __forceinline__ unsigned long long udiv64(unsigned long long n, const
 // as the wrapping product), and so is every P * v (P <= 2^24).
 __global__ void __launch_bounds__(kRowThreads) k_battn(const BAttnParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
+  pdl_enter();
   if (!running(p.gate)) return;
   const uint32_t hd = p.head_dim, h = blockIdx.x, n = blockIdx.y;
   const RowDesc rd = p.rdesc[n];
@@ -987,6 +1000,24 @@ WorkLayout work_layout(const PrefillModel& m, uint32_t cap) {
   return w;
 }
 
+// Launches one of the per-layer kernels with programmatic stream serialization allowed (the
+// kernel begins with pdl_enter).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // The layers for P rows (phases 3 to 16), then, with `classify`, the final norm and the
 // classifier rows into the logits of the rows that generate.
 cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkLayout& w,
@@ -1024,11 +1055,11 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
     const uint64_t work_items = 8ull * Npad * KG * 16;
     const uint32_t blocks = (uint32_t)std::min<uint64_t>((work_items + kRowThreads - 1) / kRowThreads, 4096);
     const uint32_t clear = splits_for(next_rows, next_KG) > 1 ? next_rows : 0u;
-    k_bplanes<<<blocks, kRowThreads, 0, s>>>(gate, vec, ld, P, cols, Npad, KG, ow, B, S, clear);
+    launch_pdl(k_bplanes, dim3(blocks), dim3(kRowThreads), 0, s, gate, vec, ld, P, cols, Npad, KG, ow, B, S, clear);
   };
   auto gemm = [&](const uint8_t* Wm, uint32_t nrows, uint32_t KG, const unsigned long long* ow) {
     const dim3 grid((nrows + kBM - 1) / kBM, (8 * Npad + kTN - 1) / kTN, splits_for(nrows, KG));
-    k_bgemm<<<grid, kTcThreads, kTcSmem, s>>>(gate, Wm, nrows, KG, B, Npad, ow, S, fault);
+    launch_pdl(k_bgemm, grid, dim3(kTcThreads), kTcSmem, s, gate, Wm, nrows, KG, (const uint8_t*)B, Npad, ow, S, fault);
   };
   auto epi = [&](BEpiParams p) {
     p.gate = gate;
@@ -1038,7 +1069,7 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
     p.P = P;
     const uint64_t items = (uint64_t)P * ((p.rows + 1) / 2);
     const uint32_t blocks = (uint32_t)std::min<uint64_t>((items + kRowThreads - 1) / kRowThreads, 8192);
-    k_bepi<<<blocks, kRowThreads, 0, s>>>(p);
+    launch_pdl(k_bepi, dim3(blocks), dim3(kRowThreads), 0, s, p);
   };
 
   k_bembed<<<P, kRowThreads, 0, s>>>(gate, rows, X, c.dim, m.embed, m.embed_scale, c.vocab, rstat);
@@ -1046,7 +1077,7 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
     const DevLayer& Wl = m.layers[l];
     unsigned long long* o4 = orw + 4 * l;
     // phases 4-8: attention norm, Q/K/V rows, checked cache stores, rotary
-    k_bnorm<<<P, kRowThreads, 0, s>>>(gate, X, XB, Wl.attn_norm, c.dim, o4 + 0);
+    launch_pdl(k_bnorm, dim3(P), dim3(kRowThreads), 0, s, gate, (const int64_t*)X, XB, Wl.attn_norm, c.dim, o4 + 0);
     planes(XB, c.dim, c.dim, KGd, o4 + 0, c.dim + 2 * m.kv_dim, KGd);
     gemm(Wl.wqkv, c.dim + 2 * m.kv_dim, KGd, o4 + 0);
     BEpiParams pq = {};
@@ -1076,7 +1107,7 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
     pa.kv_dim = m.kv_dim;
     pa.inv_sqrt = m.inv_sqrt;
     pa.or_out = o4 + 1;
-    k_battn<<<dim3(c.heads, P), kRowThreads, battn_smem(m.head_dim, max_positions), s>>>(pa);
+    launch_pdl(k_battn, dim3(c.heads, P), dim3(kRowThreads), battn_smem(m.head_dim, max_positions), s, pa);
     // phases 10-11: output rows and the residual
     planes(O, c.dim, c.dim, KGd, o4 + 1, c.dim, KGd);
     gemm(Wl.wo, c.dim, KGd, o4 + 1);
@@ -1088,7 +1119,7 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
     po.X = X;
     epi(po);
     // phases 12-14: feed-forward norm, gate and up rows, SiLU gating
-    k_bnorm<<<P, kRowThreads, 0, s>>>(gate, X, XB, Wl.ffn_norm, c.dim, o4 + 2);
+    launch_pdl(k_bnorm, dim3(P), dim3(kRowThreads), 0, s, gate, (const int64_t*)X, XB, Wl.ffn_norm, c.dim, o4 + 2);
     planes(XB, c.dim, c.dim, KGd, o4 + 2, 2 * c.hidden, KGd);
     gemm(Wl.w13, 2 * c.hidden, KGd, o4 + 2);
     BEpiParams pg = {};
@@ -1115,7 +1146,7 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
   if (classify) {
     // phases 17-18: final norm and classifier rows (written only for generating rows)
     unsigned long long* of = orw + 4 * c.layers;
-    k_bnorm<<<P, kRowThreads, 0, s>>>(gate, X, XB, m.final_norm, c.dim, of);
+    launch_pdl(k_bnorm, dim3(P), dim3(kRowThreads), 0, s, gate, (const int64_t*)X, XB, m.final_norm, c.dim, of);
     planes(XB, c.dim, c.dim, KGd, of, c.vocab, KGd);
     gemm(m.cls, c.vocab, KGd, of);
     BEpiParams pc = {};
