@@ -74,8 +74,12 @@ def compare_states(orc_model, so, sg_host, n_prompt, max_tokens, what="", turns=
 
 # ---------------------------------------------------------------- matrix row
 
+# (rows, cols, pitch).  Past 38,912 rows a CTA finishes its share in several 256-row chunks
+# (80,001: odd, three chunks a CTA); a pitch that is not a multiple of 512 leaves a partial
+# last slice.
 MATROW_CASES = [(1, 1, 16), (3, 15, 16), (5, 17, 32), (7, 172, 176), (64, 64, 64), (130, 300, 304),
-                (1001, 1000, 1008), (257, 4096, 4096), (64, 11008, 11008), (33, 16384, 16384)]
+                (1001, 1000, 1008), (257, 4096, 4096), (64, 11008, 11008), (33, 16384, 16384),
+                (80001, 48, 64), (40000, 130, 144)]
 
 
 def _x_for_limbs(L, cols, seed):
