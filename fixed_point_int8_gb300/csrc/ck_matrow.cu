@@ -30,6 +30,7 @@ struct Scratch {
   unsigned long long red[kWarps];
   unsigned long long red2[kWarps];
   InvDiv div;
+  InvDiv divn;  // the vector length's reciprocal (norm prologue)
   unsigned long long S;
   unsigned long long orv;
   unsigned long long tot[kChunkRows];  // row totals of the current chunk
@@ -85,54 +86,114 @@ __device__ __forceinline__ int64_t load_x(const MatrowParams& p, uint32_t i) {
   return x;
 }
 
+// The prologue packs 4-element word groups: thread t takes groups t, t + kThreads, ...  Up to
+// kPG groups a thread (8 elements: vectors of up to 4,096 elements at 512 threads) stay in
+// registers from the sum of squares to the packing, and their norm weights are loaded before
+// the kernel waits for the previous one (they are model data).
+constexpr int kPG = 2;
+
+struct NormWeights {
+  int32_t w[kPG][4];
+};
+
+// The reciprocal of d as make_invdiv builds it, with l = ceil(log2 d) from a count of
+// leading zeros instead of a loop.
+__device__ __forceinline__ InvDiv make_invdiv_clz(uint32_t d) {
+  const uint32_t l = d <= 1 ? 0u : 64u - (uint32_t)__clzll((long long)(d - 1));
+  const uint64_t a = (1ull << l) - d;  // a < d < 2^32
+  const uint64_t hi = (a << 32) / d;
+  const uint64_t rem = (a << 32) - hi * d;
+  const uint64_t lo = (rem << 32) / d;
+  InvDiv D;
+  D.m = ((hi << 32) | lo) + 1;
+  D.sh1 = l < 1 ? l : 1;
+  D.sh2 = l > 0 ? l - 1 : 0;
+  return D;
+}
+
+// Before the wait: the thread's first norm weights, and the vector length's reciprocal.
+__device__ __forceinline__ void prologue_early(const MatrowParams& p, Scratch* sc, NormWeights& nw) {
+  const uint32_t n = p.cols, words = p.pitch / 4;
+  const bool norm = p.pro == kProNorm;
+#pragma unroll
+  for (int j = 0; j < kPG; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t g = threadIdx.x + j * kThreads, i = 4 * g + e;
+      nw.w[j][e] = norm && g < words && i < n ? __ldg(p.norm_w + i) : 0;
+    }
+  if (norm && threadIdx.x == 32) sc->divn = make_invdiv_clz(n);
+}
+
 // Packs the input vector (optionally residual-added and RMS-normalised) into byte planes.
 // Returns the wrapping sum of the vector in *S and the limb count.
 __device__ int prologue(const MatrowParams& p, uint32_t* planes32, Scratch* sc,
-                        unsigned long long* S_out) {
+                        unsigned long long* S_out, const NormWeights& nw) {
   const uint32_t n = p.cols, words = p.pitch / 4;
-  if (p.pro == kProNorm) {
+  const bool norm = p.pro == kProNorm;
+  const bool held = words <= (uint32_t)kPG * kThreads;  // one batch: values stay in registers
+  int64_t xv[kPG][4];
+  if (norm) {
     // "RMS normalization": rms = isqrt(sum(x*x) / n + 42,950), at least 1.
     unsigned long long ss = 0, dummy = 0;
-    for (uint32_t i = threadIdx.x; i < n; i += kThreads) {
-      const int64_t x = load_x(p, i);
-      if (p.res_out && blockIdx.x == 0) p.res_out[i] = x;
-      ss += (unsigned long long)x * (unsigned long long)x;
+    for (uint32_t g0 = threadIdx.x; g0 < words; g0 += kPG * kThreads) {
+#pragma unroll
+      for (int j = 0; j < kPG; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t g = g0 + j * kThreads, i = 4 * g + e;
+          xv[j][e] = g < words && i < n ? load_x(p, i) : 0;
+        }
+#pragma unroll
+      for (int j = 0; j < kPG; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t g = g0 + j * kThreads, i = 4 * g + e;
+          if (g < words && i < n && p.res_out && blockIdx.x == 0) p.res_out[i] = xv[j][e];
+          ss += (unsigned long long)xv[j][e] * (unsigned long long)xv[j][e];
+        }
     }
     block_sum_or(ss, dummy, sc);
     if (threadIdx.x == 0) {
-      uint64_t rms = isqrt_u64(ss / n + 42950ull);
+      uint64_t rms = isqrt_u64(udiv_inv(ss, sc->divn) + 42950ull);  // floor(ss / n)
       if (rms < 1) rms = 1;
-      sc->div = make_invdiv((uint32_t)rms);
+      sc->div = make_invdiv_clz((uint32_t)rms);
     }
     __syncthreads();
   }
   const InvDiv D = sc->div;
   unsigned long long S = 0, orv = 0;
-  for (uint32_t g = threadIdx.x; g < words; g += kThreads) {
-    int64_t v[4];
+  for (uint32_t g0 = threadIdx.x; g0 < words; g0 += kPG * kThreads) {
+    int32_t wv[kPG][4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t i = 4 * g + e;
-      int64_t val = 0;
-      if (i < n) {
-        if (p.pro == kProNorm) {
-          // y = ((x * w) / rms) >> 8, the division truncating toward zero
-          const int64_t prod = wmul(load_x(p, i), (int64_t)p.norm_w[i]);
-          val = sdiv_trunc(prod, D) >> 8;
-        } else {
-          val = p.in[i];
-        }
+    for (int j = 0; j < kPG; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t g = g0 + j * kThreads, i = 4 * g + e;
+        const bool ok = g < words && i < n;
+        if (!(norm && held)) xv[j][e] = ok ? (norm ? load_x(p, i) : p.in[i]) : 0;
+        wv[j][e] = !norm ? 0 : held ? nw.w[j][e] : ok ? __ldg(p.norm_w + i) : 0;
       }
-      v[e] = val;
-      S += (unsigned long long)val;
-      orv |= (unsigned long long)(val ^ (val >> 63));
-    }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      uint32_t w = 0;
+    for (int j = 0; j < kPG; ++j) {
+      const uint32_t g = g0 + j * kThreads;
+      if (g >= words) break;
+      int64_t v[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) w |= (uint32_t)(((uint64_t)v[e] >> (8 * k)) & 0xFF) << (8 * e);
-      planes32[k * words + g] = w;
+      for (int e = 0; e < 4; ++e) {
+        // norm: y = ((x * w) / rms) >> 8, the division truncating toward zero
+        const int64_t val = norm ? sdiv_trunc(wmul(xv[j][e], (int64_t)wv[j][e]), D) >> 8 : xv[j][e];
+        v[e] = val;
+        S += (unsigned long long)val;
+        orv |= (unsigned long long)(val ^ (val >> 63));
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        uint32_t w = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w |= (uint32_t)(((uint64_t)v[e] >> (8 * k)) & 0xFF) << (8 * e);
+        planes32[k * words + g] = w;
+      }
     }
   }
   block_sum_or(S, orv, sc);
@@ -353,16 +414,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_matrow(const MatrowParams p) {
     else
       load_item<false>(p, rb, c1, ns, threadIdx.x >> 5, items, wn);
   }
+  uint8_t* planes = smem;
+  Scratch* sc = reinterpret_cast<Scratch*>(smem + 8 * (size_t)p.pitch);
+  NormWeights nw;
+  prologue_early(p, sc, nw);
   wait_prior_grids();
   allow_next_grid();
   if (rb >= re) return;
   if (p.state && hdr_ld<uint32_t>(p.state, kHPhase) != CK_PHASE_RUNNING) return;
   const uint32_t pos = p.state ? hdr_ld<uint32_t>(p.state, kHPosition) : 0u;
-  uint8_t* planes = smem;
-  Scratch* sc = reinterpret_cast<Scratch*>(smem + 8 * (size_t)p.pitch);
   for (uint32_t t = threadIdx.x; t < kChunkRows; t += kThreads) sc->tot[t] = 0;
   unsigned long long S;
-  const int L = prologue(p, reinterpret_cast<uint32_t*>(planes), sc, &S);
+  const int L = prologue(p, reinterpret_cast<uint32_t*>(planes), sc, &S, nw);
   if (p.grouped) {
     switch (L) {
       case 1: rows_loop<1, true>(p, planes, sc, S, pos, rb, re, wn); break;
