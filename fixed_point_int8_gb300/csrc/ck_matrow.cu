@@ -111,6 +111,17 @@ __device__ __forceinline__ InvDiv make_invdiv_clz(uint32_t d) {
   return D;
 }
 
+// out[k] gets byte k of in[0..3] as its bytes 0..3: a 4 x 4 byte transpose in eight byte
+// permutes (pairs interleaved by byte, then by byte pair).
+__device__ __forceinline__ void transpose_bytes4(const uint32_t (&in)[4], uint32_t* out) {
+  const uint32_t ab_lo = __byte_perm(in[0], in[1], 0x5140), ab_hi = __byte_perm(in[0], in[1], 0x7362);
+  const uint32_t cd_lo = __byte_perm(in[2], in[3], 0x5140), cd_hi = __byte_perm(in[2], in[3], 0x7362);
+  out[0] = __byte_perm(ab_lo, cd_lo, 0x5410);
+  out[1] = __byte_perm(ab_lo, cd_lo, 0x7632);
+  out[2] = __byte_perm(ab_hi, cd_hi, 0x5410);
+  out[3] = __byte_perm(ab_hi, cd_hi, 0x7632);
+}
+
 // Before the wait: the thread's first norm weights, and the vector length's reciprocal.
 __device__ __forceinline__ void prologue_early(const MatrowParams& p, Scratch* sc, NormWeights& nw) {
   const uint32_t n = p.cols, words = p.pitch / 4;
@@ -187,13 +198,16 @@ __device__ int prologue(const MatrowParams& p, uint32_t* planes32, Scratch* sc,
         S += (unsigned long long)val;
         orv |= (unsigned long long)(val ^ (val >> 63));
       }
+      // plane k's word g holds byte k of the four values: a 4 x 4 byte transpose of their
+      // low and of their high halves
+      const uint32_t lo[4] = {(uint32_t)v[0], (uint32_t)v[1], (uint32_t)v[2], (uint32_t)v[3]};
+      const uint32_t hi[4] = {(uint32_t)((uint64_t)v[0] >> 32), (uint32_t)((uint64_t)v[1] >> 32),
+                              (uint32_t)((uint64_t)v[2] >> 32), (uint32_t)((uint64_t)v[3] >> 32)};
+      uint32_t pl[8];
+      transpose_bytes4(lo, pl);
+      transpose_bytes4(hi, pl + 4);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        uint32_t w = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) w |= (uint32_t)(((uint64_t)v[e] >> (8 * k)) & 0xFF) << (8 * e);
-        planes32[k * words + g] = w;
-      }
+      for (int k = 0; k < 8; ++k) planes32[k * words + g] = pl[k];
     }
   }
   block_sum_or(S, orv, sc);
