@@ -43,11 +43,6 @@ __device__ __forceinline__ unsigned long long warp_sum(unsigned long long v) {
 // of the previous kernel (deeper unrolling costs registers and measured slower).
 __global__ void __launch_bounds__(kThreads) k_attention(const AttnParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
-  // launched with programmatic dependent launch: wait for the kernels before this one on the
-  // stream (the queries and the cache words they wrote), then let the next kernel start early
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (hdr_ld<uint32_t>(p.state, kHPhase) != CK_PHASE_RUNNING) return;  // whole cluster alike
   cg::cluster_group cluster = cg::this_cluster();
   const uint32_t hd = p.head_dim;
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -59,33 +54,52 @@ __global__ void __launch_bounds__(kThreads) k_attention(const AttnParams p) {
   long long* red = reinterpret_cast<long long*>(csum + 1);                      // [kWarps]
   long long* sc = red + kWarps;                                                 // [chunk_cap]
 
+  // Launched with programmatic dependent launch.  Before the wait this kernel reads only what
+  // was written before the previous kernel started: the position (set by the previous
+  // position's last kernel) and the cache rows of earlier positions.  The queries and the
+  // newest cache row come from the kernel just before: after the wait.
   const uint32_t pos = hdr_ld<uint32_t>(p.state, kHPosition);
   const uint32_t P = pos + 1;  // positions so far, the current one included
+  const uint32_t older = min(pos, p.cache);  // rows below this were written at earlier positions
   const uint32_t h = blockIdx.x;
   const uint32_t rank = cluster.block_rank(), CL = cluster.num_blocks();
   const uint32_t kvh = h / (p.heads / p.kv_heads);  // "head h reads key/value head h/(heads/kvHeads)"
   const uint32_t cs = (P + CL - 1) / CL;
   const uint32_t t0 = min(P, rank * cs), t1 = min(P, t0 + cs);
   const uint32_t n = t1 - t0;
-
-  for (uint32_t i = tid; i < hd; i += kThreads) q_s[i] = p.q[(size_t)h * hd + i];
-  __syncthreads();
-
   const int32_t* Kh = p.kcache + (size_t)kvh * p.cache * hd;  // the head's positions, contiguous
   const int32_t* Vh = p.vcache + (size_t)kvh * p.cache * hd;
   const uint32_t lpp = hd / 4;       // lanes per position, four elements each
   const uint32_t ppw = 32 / lpp;     // positions per warp step
   const uint32_t sub = lane % lpp, slot = lane / lpp, e0 = sub * 4;
+  const uint32_t base0 = warp * ppw;
+  int4 k4[kUnroll];  // the warp's first batch of keys
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const uint32_t tl = base0 + u * kWarps * ppw + slot;
+    k4[u] = tl < n && t0 + tl < older ? *reinterpret_cast<const int4*>(Kh + (size_t)(t0 + tl) * hd + e0)
+                                      : make_int4(0, 0, 0, 0);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (hdr_ld<uint32_t>(p.state, kHPhase) != CK_PHASE_RUNNING) return;  // whole cluster alike
+
+  for (uint32_t i = tid; i < hd; i += kThreads) q_s[i] = p.q[(size_t)h * hd + i];
+  __syncthreads();
+
   const int64_t q0 = q_s[e0], q1 = q_s[e0 + 1], q2 = q_s[e0 + 2], q3 = q_s[e0 + 3];
 
   // stage 0: s_t = (((q . k_t) >> 16) * inv) >> 24, products and sums wrapping; keep the max
   long long lmax = LLONG_MIN;
-  for (uint32_t base = warp * ppw; base < n; base += kUnroll * kWarps * ppw) {
-    int4 k4[kUnroll];
+  for (uint32_t base = base0; base < n; base += kUnroll * kWarps * ppw) {
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const uint32_t tl = base + u * kWarps * ppw + slot;
-      k4[u] = tl < n ? *reinterpret_cast<const int4*>(Kh + (size_t)(t0 + tl) * hd + e0) : make_int4(0, 0, 0, 0);
+      // the first batch has all but the newest row already
+      if (tl < n && (base != base0 || t0 + tl >= older))
+        k4[u] = *reinterpret_cast<const int4*>(Kh + (size_t)(t0 + tl) * hd + e0);
+      else if (base != base0)
+        k4[u] = make_int4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
