@@ -91,6 +91,7 @@ __device__ __forceinline__ int64_t load_x(const MatrowParams& p, uint32_t i) {
 // registers from the sum of squares to the packing, and their norm weights are loaded before
 // the kernel waits for the previous one (they are model data).
 constexpr int kPG = 2;
+constexpr int kPGP = 3;  // plain prologue: groups a thread loads at once (measured best of 2, 3, 6)
 
 struct NormWeights {
   int32_t w[kPG][4];
@@ -172,9 +173,40 @@ __device__ int prologue(const MatrowParams& p, uint32_t* planes32, Scratch* sc,
     }
     __syncthreads();
   }
-  const InvDiv D = sc->div;
   unsigned long long S = 0, orv = 0;
-  for (uint32_t g0 = threadIdx.x; g0 < words; g0 += kPG * kThreads) {
+  if (!norm) {
+    // plain: kPGP groups a thread load at once
+    for (uint32_t g0 = threadIdx.x; g0 < words; g0 += kPGP * kThreads) {
+      int64_t pv[kPGP][4];
+#pragma unroll
+      for (int j = 0; j < kPGP; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t g = g0 + j * kThreads, i = 4 * g + e;
+          pv[j][e] = g < words && i < n ? p.in[i] : 0;
+        }
+#pragma unroll
+      for (int j = 0; j < kPGP; ++j) {
+        const uint32_t g = g0 + j * kThreads;
+        if (g >= words) break;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          S += (unsigned long long)pv[j][e];
+          orv |= (unsigned long long)(pv[j][e] ^ (pv[j][e] >> 63));
+        }
+        const uint32_t lo[4] = {(uint32_t)pv[j][0], (uint32_t)pv[j][1], (uint32_t)pv[j][2], (uint32_t)pv[j][3]};
+        const uint32_t hi[4] = {(uint32_t)((uint64_t)pv[j][0] >> 32), (uint32_t)((uint64_t)pv[j][1] >> 32),
+                                (uint32_t)((uint64_t)pv[j][2] >> 32), (uint32_t)((uint64_t)pv[j][3] >> 32)};
+        uint32_t pl[8];
+        transpose_bytes4(lo, pl);
+        transpose_bytes4(hi, pl + 4);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) planes32[k * words + g] = pl[k];
+      }
+    }
+  }
+  const InvDiv D = sc->div;
+  for (uint32_t g0 = threadIdx.x; norm && g0 < words; g0 += kPG * kThreads) {
     int32_t wv[kPG][4];
 #pragma unroll
     for (int j = 0; j < kPG; ++j)
