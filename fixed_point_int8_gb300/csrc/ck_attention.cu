@@ -23,7 +23,6 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kUnroll = 4;  // warp steps whose cache loads are in flight together
 
-
 __device__ __forceinline__ long long warp_max(long long v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
