@@ -249,11 +249,23 @@ __device__ void block_argmax(const int64_t* l, uint32_t n, long long* best_v, ui
   __shared__ uint32_t si[kArgThreads / 32];
   long long bv = LLONG_MIN;
   uint32_t bi = 0xFFFFFFFFu;
-  for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
-    const long long v = l[i];
-    if (bi == 0xFFFFFFFFu || v > bv) {
-      bv = v;
-      bi = i;
+  // eight loads a thread in flight, then compared in index order (the first of equal
+  // maxima stays)
+  constexpr int kU = 8;
+  for (uint32_t i0 = threadIdx.x; i0 < n; i0 += kU * blockDim.x) {
+    long long v[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const uint32_t i = i0 + u * blockDim.x;
+      v[u] = i < n ? l[i] : LLONG_MIN;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const uint32_t i = i0 + u * blockDim.x;
+      if (i < n && (bi == 0xFFFFFFFFu || v[u] > bv)) {
+        bv = v[u];
+        bi = i;
+      }
     }
   }
 #pragma unroll
