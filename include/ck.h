@@ -318,7 +318,10 @@ int ck_state_upload(void* dev_state, const void* host, size_t len, void* stream)
  *   the shift arithmetic.
  * dev_W: rows x pitch bytes, row-major, 16-byte aligned, pitch a multiple of 16 and >= cols
  * (bytes past cols are ignored); dev_scale u32[rows]; dev_x i64[cols] (8-byte aligned);
- * dev_y i64[rows].  1 <= cols <= 16384, 1 <= rows <= 2^24.  Errors: 9, 10. */
+ * dev_y i64[rows].  1 <= cols <= 16384, 1 <= rows <= 2^24.  The launch allows programmatic
+ * dependent launch: its weight loads may start while the previous kernel on `stream`
+ * finishes, and it reads dev_x (and writes dev_y) only once that kernel has completed, so
+ * stream order holds as for any launch.  Errors: 9, 10. */
 int ck_matrow(const uint8_t* dev_W, size_t pitch, const uint32_t* dev_scale, uint32_t rows,
               uint32_t cols, const int64_t* dev_x, int64_t* dev_y, void* stream);
 
