@@ -81,9 +81,11 @@ __global__ void __launch_bounds__(kThreads) k_attention(const AttnParams p) {
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (hdr_ld<uint32_t>(p.state, kHPhase) != CK_PHASE_RUNNING) return;  // whole cluster alike
-
+  // the phase is tested after the queries are requested (the whole cluster reads the same
+  // header word and returns alike)
+  const bool running = hdr_ld<uint32_t>(p.state, kHPhase) == CK_PHASE_RUNNING;
   for (uint32_t i = tid; i < hd; i += kThreads) q_s[i] = p.q[(size_t)h * hd + i];
+  if (!running) return;
   __syncthreads();
 
   const int64_t q0 = q_s[e0], q1 = q_s[e0 + 1], q2 = q_s[e0 + 2], q3 = q_s[e0 + 3];

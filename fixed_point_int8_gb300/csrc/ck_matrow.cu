@@ -140,7 +140,7 @@ __device__ __forceinline__ void prologue_early(const MatrowParams& p, Scratch* s
 // Packs the input vector (optionally residual-added and RMS-normalised) into byte planes.
 // Returns the wrapping sum of the vector in *S and the limb count.
 __device__ int prologue(const MatrowParams& p, uint32_t* planes32, Scratch* sc,
-                        unsigned long long* S_out, const NormWeights& nw) {
+                        unsigned long long* S_out, const NormWeights& nw, bool running) {
   const uint32_t n = p.cols, words = p.pitch / 4;
   const bool norm = p.pro == kProNorm;
   const bool held = words <= (uint32_t)kPG * kThreads;  // one batch: values stay in registers
@@ -161,7 +161,7 @@ __device__ int prologue(const MatrowParams& p, uint32_t* planes32, Scratch* sc,
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const uint32_t g = g0 + j * kThreads, i = 4 * g + e;
-          if (g < words && i < n && p.res_out && blockIdx.x == 0) p.res_out[i] = xv[j][e];
+          if (running && g < words && i < n && p.res_out && blockIdx.x == 0) p.res_out[i] = xv[j][e];
           ss += (unsigned long long)xv[j][e] * (unsigned long long)xv[j][e];
         }
     }
@@ -467,11 +467,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_matrow(const MatrowParams p) {
   wait_prior_grids();
   allow_next_grid();
   if (rb >= re) return;
-  if (p.state && hdr_ld<uint32_t>(p.state, kHPhase) != CK_PHASE_RUNNING) return;
+  // The state's phase is read here but tested only after the prologue, so that its vector
+  // loads need not wait for it: for a failed state the prologue skips its one kind of global
+  // store (the residual copy) and the kernel returns after it.  Every thread reads the same
+  // header word, which nothing writes while this kernel runs.
+  const bool running = !p.state || hdr_ld<uint32_t>(p.state, kHPhase) == CK_PHASE_RUNNING;
   const uint32_t pos = p.state ? hdr_ld<uint32_t>(p.state, kHPosition) : 0u;
   for (uint32_t t = threadIdx.x; t < kChunkRows; t += kThreads) sc->tot[t] = 0;
   unsigned long long S;
-  const int L = prologue(p, reinterpret_cast<uint32_t*>(planes), sc, &S, nw);
+  const int L = prologue(p, reinterpret_cast<uint32_t*>(planes), sc, &S, nw, running);
+  if (!running) return;
   if (p.grouped) {
     switch (L) {
       case 1: rows_loop<1, true>(p, planes, sc, S, pos, rb, re, wn); break;
