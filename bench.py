@@ -46,7 +46,8 @@ PATHS = {"auto": 0, "step": 1, "kernels": 2}  # ck_set_path values (CK_PATH_AUTO
 METRIC = "decode tokens/s bit-exact vs oracle; matrow HBM GB/s as % of GB300 peak"
 WORKLOAD = ("llama7b_shape fixed-point decode: dim 4096, 32 layers, 32 heads x 128, FFN hidden 11008, "
             "vocab 32000, context 2048, u8 weights + u32 row scales (6.61 GB/token); 128 prompt ids "
-            "prefilled layer-major, then greedy decode; single run per GPU")
+            "prefilled, then greedy decode; single run per GPU")
+WORKLOAD_TOKENS = 256  # tokens a run of the workload generates
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -210,6 +211,27 @@ def max_over_ranks(v: float, world: int) -> float:
     return float(t.item())
 
 
+# ---------------------------------------------------------------- the workload
+
+def workload_spec(args):
+    import synth
+    spec = synth.LLAMA7B
+    if args.layers:
+        import dataclasses
+        spec = dataclasses.replace(spec, layers=args.layers)  # profiling and test aid only
+    return spec
+
+
+def workload_config(args, n_prompt: int, timed: int, parallelism: str) -> dict:
+    wl = WORKLOAD if not args.layers else WORKLOAD + f" (cut to {args.layers} layers)"
+    if n_prompt != 128:
+        wl = wl.replace("128 prompt ids", f"{n_prompt} prompt ids")
+    return {"workload": wl, "prompt_ids": n_prompt, "decode_positions_timed": timed,
+            "first_timed_position": n_prompt + args.warmup,
+            "l2": "inputs larger than L2: 6.6 GB of weights streamed per step",
+            "parallelism": parallelism}
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args):
@@ -222,7 +244,8 @@ def run_ours(args):
     libbuild.build()
     if args.batched_only:
         # profiling aid: only the 64-run batched measurement
-        print(json.dumps({"batched_runs": batched_runs(ck, torch, synth, args.batched_passes)}), flush=True)
+        print(json.dumps({"batched_runs": batched_runs(ck, torch, synth, args.batched_passes, args.batched_layers)}),
+              flush=True)
         return
     if args.long_only:
         # profiling aid: only the long-context measurement (optionally cut to fewer layers)
@@ -237,14 +260,13 @@ def run_ours(args):
                           "GB/s": round(nb / (avg * 1e-3) / 1e9, 1), "us_one_by_one": round(alone * 1e3, 2)}),
               flush=True)
         return
-    spec = synth.LLAMA7B
-    if args.layers:
-        import dataclasses
-        spec = dataclasses.replace(spec, layers=args.layers)  # profiling aid only
+    spec = workload_spec(args)
     n_prompt = args.prompt_ids
     K, W = args.steps, args.warmup
     e2e_steps = min(K, args.e2e_steps)
-    max_tokens = 1 + W + K + e2e_steps
+    # the state holds the workload's whole run (256 generated tokens), or more when the
+    # requested steps need them; the CPU baseline continues the same run
+    max_tokens = max(WORKLOAD_TOKENS, 1 + W + K + e2e_steps)
     assert n_prompt + max_tokens - 1 <= spec.context, "too many steps for the context"
 
     t0 = time.time()
@@ -342,10 +364,10 @@ def run_ours(args):
         del model, state
         torch.cuda.empty_cache()
         if args.batched_passes:
-            batched = batched_runs(ck, torch, synth, args.batched_passes)
+            batched = batched_runs(ck, torch, synth, args.batched_passes, args.batched_layers)
             torch.cuda.empty_cache()
         if args.long_steps:
-            longc = long_context(ck, torch, synth, args.long_steps, 0, path)
+            longc = long_context(ck, torch, synth, args.long_steps, args.long_layers, path)
 
     if rank != 0:
         return
@@ -367,9 +389,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "u8 x i64 (int64 activations, 16 fractional bits)",
         "data": "synthetic (seeded weights and prompt ids, no checkpoint)",
-        "config": {"workload": WORKLOAD, "prompt_ids": n_prompt, "decode_positions_timed": K,
-                   "l2": "inputs larger than L2: 6.6 GB of weights streamed per step",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": workload_config(args, n_prompt, K, "replicas" if world > 1 else "single GPU"),
         "roofline": roof,
         "weight_roofline": {"bytes_per_token": weight_bytes,
                             "tokens_per_s_at_peak": round(hbm * 1e9 / weight_bytes, 1),
@@ -398,12 +418,13 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
-def batched_runs(ck, torch, synth, passes):
+def batched_runs(ck, torch, synth, passes, layers=0):
     """The 1B-shaped model with 64 runs: each prefilled per run, then `passes` generating
     passes of ck_turn_batch (one position of every run each), device-timed after three
-    untimed passes."""
+    untimed passes.  `layers` cuts the model (a test aid; 0: the whole model)."""
+    import dataclasses
     wl = synth.WORKLOADS["1b_x64"]
-    spec = wl.spec
+    spec = wl.spec if not layers else dataclasses.replace(wl.spec, layers=layers)
     passes = min(passes, wl.steps - 4)
     rc, m = ck.Model.load(synth.build_artifact(spec))
     assert rc == 0
@@ -437,8 +458,8 @@ def batched_runs(ck, torch, synth, passes):
     tflops = 2 * macs / (ms * 1e-3 / passes) / 1e12
     return {"value": round(value, 1), "unit": "tokens/s", "runs": wl.runs, "passes": passes,
             "ms_per_pass": round(ms / passes, 3),
-            "workload": "1b_shape (dim 2048, 22 layers, 32 heads, FFN 5632, vocab 32000), 64 runs x 64 "
-                        "prompt ids, positions 67.. of each run, greedy",
+            "workload": f"1b_shape (dim 2048, {spec.layers} layers, 32 heads, FFN 5632, vocab 32000), 64 runs "
+                        f"x 64 prompt ids, positions 67.. of each run, greedy",
             "algorithmic_tflops": round(tflops, 1),
             "algorithmic_frac_of_bf16_peak": round(tflops / peak, 4) if peak else None,
             "note": "whole pass (all kernels); algorithmic = 2 x weights x runs per pass, the byte "
@@ -559,46 +580,61 @@ def matrow_measurements(ck, torch, args):
 
 def cpu_baseline(art, snapshot, gpu_tokens, budget_s):
     """The oracle, as it stands, continues the decode from the GPU's state after the prefill
-    for as many positions as fit in about budget_s seconds; its tokens must equal the GPU's."""
+    for as many positions as fit in about budget_s seconds, never past the run's last token
+    (the state's max tokens); its tokens must equal the GPU's."""
     import oracle
     m = oracle.Model(art)
     st = snapshot.copy()
-    start = oracle.header(st)["generated"]
+    h = oracle.header(st)
+    start = h["generated"]
+    room = min(h["max_tokens"] - start, len(gpu_tokens) - start)
     t0 = time.perf_counter()
-    n = 0
-    while True:
+    n, rc, el = 0, 0, 0.0
+    while n < room:
         rc, res = m.turn(st, 1)
-        assert rc == 0
-        n += 1
         el = time.perf_counter() - t0
-        if el > budget_s or n >= 64:
+        if rc != 0 or res["generated_this_turn"] != 1:
             break
-    lay = m.layout(oracle.header(st)["n_prompt"], oracle.header(st)["max_tokens"])
+        n += 1
+        if el > budget_s:
+            break
+    if n == 0:
+        return None, {"checked_tokens": start, "equal": False, "oracle_rc": rc}
+    lay = m.layout(h["n_prompt"], h["max_tokens"])
     otoks = st[lay["out"]:lay["out"] + 4 * (start + n)].view("<u4").tolist()
-    same = otoks == gpu_tokens[:start + n]
+    same = otoks == list(gpu_tokens[:start + n])
     cpu = {"value": round(n / el, 4), "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
            "sample": f"{n} decode positions of the same 7B-shaped run, continued on the CPU from the "
-                     f"GPU's state after the 128-id prefill (OpenMP over independent matrix rows)"}
-    return cpu, {"checked_tokens": start + n, "equal": bool(same)}
+                     f"GPU's state after the prefill and the first token (OpenMP over independent matrix "
+                     f"rows)"}
+    return cpu, {"checked_tokens": start + n, "equal": bool(same), "oracle_rc": rc}
 
 
 # ---------------------------------------------------------------- reference arm
 
 def run_reference(args):
-    """The CPU oracle as the reference implementation of the same decode: on rank 0 only,
-    it prefills a one-id prompt and times --steps generating positions after --warmup."""
+    """The CPU oracle as the reference implementation of the same decode, on rank 0 only:
+    it runs the workload's prompt ids (the positions that generate nothing, then the one
+    that generates the first token), --warmup generating positions untimed, then times up
+    to --steps generating positions, the same positions the GPU arm times, stopping early
+    after --reference-seconds."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     import oracle
     import synth
-    spec = synth.LLAMA7B
+    spec = workload_spec(args)
     art = synth.build_artifact(spec)
     m = oracle.Model(art)
     K, W = args.steps, args.warmup
-    n_prompt = 1
-    rc, st = m.init_state(synth.prompt_ids(spec, n_prompt), W + K)
+    n_prompt = args.prompt_ids
+    max_tokens = max(WORKLOAD_TOKENS, 1 + W + K)
+    rc, st = m.init_state(synth.prompt_ids(spec, n_prompt), max_tokens)
     assert rc == 0
+    t_pre = time.perf_counter()
+    rc, res = m.turn(st, n_prompt)  # the prompt positions and the first generated token
+    pre_s = time.perf_counter() - t_pre
+    assert rc == 0 and res["generated"] == 1, (rc, res)
     rc, _ = m.turn(st, W)
     assert rc == 0
     t0 = time.perf_counter()
@@ -615,11 +651,13 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": done, "steps_requested": K,
         "warmup": W, "ms_per_step": round(el / max(done, 1) * 1e3, 2), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "u8 x i64 (int64 activations)",
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8 x i64 (int64 activations, 16 fractional bits)",
         "data": "synthetic (seeded weights and prompt ids, no checkpoint)",
-        "config": {"workload": WORKLOAD.replace("128 prompt ids", "1 prompt id"), "parallelism": "CPU oracle"},
+        "config": workload_config(args, n_prompt, done, "CPU oracle"),
         "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
-                         "sample": f"{done} generating positions timed after {W} warm-up positions"},
+                         "sample": f"generating positions {n_prompt + W}..{n_prompt + W + done - 1} of the "
+                                   f"workload's run ({done} timed after {W} warm-up positions; the "
+                                   f"{n_prompt} prompt positions took {pre_s:.1f} s, untimed)"},
         "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -639,6 +677,8 @@ def main():
                     help="passes of the 64-run batched measurement (0: skip it)")
     ap.add_argument("--batched-only", action="store_true",
                     help="profiling aid: run only the 64-run batched measurement")
+    ap.add_argument("--batched-layers", type=int, default=0,
+                    help="test aid: cut the 64-run model to this many layers")
     ap.add_argument("--long-steps", type=int, default=40,
                     help="generating positions of the 8K-context measurement (0: skip it)")
     ap.add_argument("--long-only", action="store_true",

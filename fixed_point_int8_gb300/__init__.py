@@ -61,6 +61,7 @@ def lib() -> ctypes.CDLL:
             "ck_set_step_slots": ([vp, ctypes.c_uint32], ctypes.c_int),
             "ck_set_attention_split": ([vp, ctypes.c_uint32], ctypes.c_int),
             "ck_set_step_prefetch": ([vp, ctypes.c_uint32], ctypes.c_int),
+            "ck_set_step_wait_limit": ([vp, ctypes.c_uint32], ctypes.c_int),
             "ck_set_prefill": ([vp, ctypes.c_uint32], ctypes.c_int),
             "ck_free_model": ([vp], None),
             "ck_state_size": ([vp, u32, u32, ctypes.POINTER(sz)], ctypes.c_int),
@@ -158,6 +159,10 @@ class Model:
     def set_step_slots(self, max_slots: int) -> int:
         """Cap on the persistent kernel's ring slots (0: as many as fit)."""
         return lib().ck_set_step_slots(self._h, max_slots)
+
+    def set_step_wait_limit(self, polls: int) -> int:
+        """Polls of the one-position kernel's barriers before they give up (0: default)."""
+        return lib().ck_set_step_wait_limit(self._h, polls)
 
     def set_step_prefetch(self, kb_per_block: int) -> int:
         """L2 prefetch distance of the persistent kernel, KB per block (0: default)."""

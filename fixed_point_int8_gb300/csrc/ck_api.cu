@@ -33,6 +33,7 @@ struct ck_model {
   uint32_t max_slots;    // cap on the one-position kernel's ring slots (0: as many as fit)
   uint32_t att_full;     // positions every block of a head scores itself (0: default)
   uint32_t pf_kb;        // L2 prefetch distance of the one-position kernel, KB per block
+  uint32_t sync_polls;   // polls of the one-position kernel's barriers (0: the default)
                          // (0: default)
   int smem_optin;        // largest shared memory a block may opt into
   size_t step_smem;      // dynamic shared memory available to the one-position kernel
@@ -545,8 +546,11 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
 }
 
 // Launch plan of the one-position kernel for a state, or false when the model or state is
-// outside what it supports (then the phase-by-phase kernels run instead).
-bool plan_step(const ck_model* m, const StateLayout& lay, StepParams* sp, int* grid, size_t* smem) {
+// outside what it supports (then the phase-by-phase kernels run instead).  state_work: the
+// kernel's scratch is the state's work region, which must then hold it (the allocation-free
+// entry keeps its scratch elsewhere and checks its own limit).
+bool plan_step(const ck_model* m, const StateLayout& lay, StepParams* sp, int* grid, size_t* smem,
+               bool state_work = true) {
   const ck_config& c = m->cfg;
   if (c.heads > 1000) return false;
   const int G = m->num_sms < 768 ? m->num_sms : 768;
@@ -590,7 +594,7 @@ bool plan_step(const ck_model* m, const StateLayout& lay, StepParams* sp, int* g
   const uint64_t off_vbuf = (off_oacc + 8ull * c.dim + 255) & ~255ull;
   const uint64_t work_need = off_vbuf + 3 * 8 * max_pitch;
   const uint64_t work_bytes = lay.k - lay.scores;
-  if (work_need > work_bytes) return false;
+  if (state_work && work_need > work_bytes) return false;
   StepParams& p = *sp;
   p = StepParams{};
   p.off_prompt = lay.prompt; p.off_out = lay.out; p.off_x = lay.x; p.off_xb = lay.xb; p.off_q = lay.q;
@@ -602,6 +606,7 @@ bool plan_step(const ck_model* m, const StateLayout& lay, StepParams* sp, int* g
   p.pitch_h = m->pitch_h; p.inv_sqrt = m->inv_sqrt;
   p.gh = gh; p.att_full = att_full; p.ns = (uint32_t)ns; p.x_bytes = (uint32_t)xb;
   p.pf_bytes = m->pf_kb * 1024u;  // 0 (the default): none
+  p.sync_polls = m->sync_polls;   // 0 (the default): the kernel's own limit
   p.planes_bytes = (uint32_t)planes;
   p.zero_bytes = (uint32_t)zero_bytes; p.off_hsync = (uint32_t)off_hsync; p.off_hfin = (uint32_t)off_hfin;
   p.off_part = off_part; p.off_cand = off_cand; p.off_oacc = off_oacc; p.off_vbuf = off_vbuf;
@@ -902,6 +907,14 @@ int ck_set_step_slots(ck_model* m, uint32_t max_slots) {
   return CK_OK;
 }
 
+int ck_set_step_wait_limit(ck_model* m, uint32_t polls) {
+  if (!m) return CK_INVALID_ARGUMENT;
+  m->sync_polls = polls;
+  for (auto& g : m->graphs) cudaGraphExecDestroy(g.exec);  // plans change: rebuild graphs
+  m->graphs.clear();
+  return CK_OK;
+}
+
 int ck_set_step_prefetch(ck_model* m, uint32_t kb_per_block) {
   if (!m || kb_per_block > 4096) return CK_INVALID_ARGUMENT;
   m->pf_kb = kb_per_block;
@@ -1164,7 +1177,7 @@ int ck_turn_noalloc(ck_model* m, void* dev_state, size_t len, void* stream, ck_t
   StepParams p;
   int grid;
   size_t smem;
-  if (!plan_step(m, lay, &p, &grid, &smem)) return CK_INVALID_ARGUMENT;
+  if (!plan_step(m, lay, &p, &grid, &smem, false)) return CK_INVALID_ARGUMENT;
   // scratch this position needs: counters, attention partials and accumulators, per-block
   // candidates, global planes
   const size_t need = step_work_bytes(p);

@@ -277,6 +277,8 @@ struct StepParams {
   uint32_t att_full;    // up to this many positions every CTA of a head scores all of them
   uint32_t ns;          // ring slots
   uint32_t pf_bytes;    // how far ahead of the ring fills the producer prefetches into L2
+  uint32_t sync_polls;  // polls of a grid or head-group barrier before it gives up (0: the
+                        // default limit); waits on the CTA's own copies keep the default
   uint32_t x_bytes;     // planes, row scales and rotary row / attention region
   uint32_t planes_bytes;  // shared memory for byte planes; a phase keeps
                           // min(8, planes_bytes / pitch) planes there, the rest in global

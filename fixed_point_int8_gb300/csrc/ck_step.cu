@@ -24,6 +24,7 @@
 // on a timeout the kernel raises an abort flag, stops issuing copies, waits (bounded) for
 // its copies in flight and the state is marked failed with error 9.
 #include <climits>
+#include <mutex>
 
 #include "ck_internal.cuh"
 
@@ -125,6 +126,7 @@ __device__ __forceinline__ uint64_t* empty_of(const StepParams& p) { return full
 struct Pos {
   uint8_t* work;
   uint32_t pos, tok;
+  uint32_t sync_polls;  // polls of a grid or head-group barrier before it gives up
 };
 __device__ __forceinline__ uint32_t* gbar_of(const Pos& q) { return reinterpret_cast<uint32_t*>(q.work + kWBar); }
 __device__ __forceinline__ uint32_t* gabort_of(const Pos& q) { return reinterpret_cast<uint32_t*>(q.work + kWAbort); }
@@ -337,7 +339,7 @@ __device__ bool grid_sync(const Pos& q, Shared& sh, uint32_t& epoch) {
     const uint32_t target = epoch * gridDim.x;
     uint32_t i = 0;
     while (ld_acquire(gbar) < target) {
-      if (++i > kPollLimit || ((i & 255) == 0 && ld_acquire(gabort_of(q)))) {
+      if (++i > q.sync_polls || ((i & 255) == 0 && ld_acquire(gabort_of(q)))) {
         atomicExch(gabort_of(q), 1u);
         sh.abort = 1;
         break;
@@ -355,7 +357,7 @@ __device__ bool group_sync(const Pos& q, Shared& sh, uint32_t* counter, uint32_t
     asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(counter) : "memory");
     uint32_t i = 0;
     while (ld_acquire(counter) < target) {
-      if (++i > kPollLimit || ((i & 255) == 0 && ld_acquire(gabort_of(q)))) {
+      if (++i > q.sync_polls || ((i & 255) == 0 && ld_acquire(gabort_of(q)))) {
         atomicExch(gabort_of(q), 1u);
         sh.abort = 1;
         break;
@@ -1217,6 +1219,7 @@ __device__ __forceinline__ void step_body(const StepParams& p, uint8_t* work, Sh
   if (hdr_ld<uint32_t>(st, kHPhase) != CK_PHASE_RUNNING) return;  // every CTA alike
   Pos q;
   q.work = work;
+  q.sync_polls = p.sync_polls ? p.sync_polls : kPollLimit;
   q.pos = hdr_ld<uint32_t>(st, kHPosition);
   const uint32_t np = hdr_ld<uint32_t>(st, kHNPrompt);
   q.tok = q.pos < np ? reinterpret_cast<const uint32_t*>(st + p.off_prompt)[q.pos]
@@ -1310,12 +1313,16 @@ size_t noalloc_work_bytes() { return kNoAllocWorkBytes; }
 // Set-up of the allocation-free variant, once per device, with that device current: the
 // device address of the scratch array (host code only holds a stand-in for the symbol) and
 // the kernel's shared-memory limit.  Later calls on the device reuse the cached address.
+// A mutex makes the first call on a device run the set-up once even when several host
+// threads make it at the same time.
 cudaError_t noalloc_setup(size_t dynamic_max, uint8_t** work) {
+  static std::mutex mu;
   static uint8_t* addr[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
   if (!addr[dev]) {
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_noalloc_work);

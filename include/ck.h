@@ -131,6 +131,16 @@ int ck_set_attention_split(ck_model* m, uint32_t positions);
  * bits.  Drops the model's cached graphs.  Errors: 10 for a null handle or above 4096. */
 int ck_set_step_prefetch(ck_model* m, uint32_t kb_per_block);
 
+/* A testing control of the one-position kernel's error path: how many times each of its
+ * grid and head-group barriers polls before it gives up (0, the default: about four
+ * million polls, far beyond any wait a healthy position has).  A barrier that gives up
+ * raises the kernel's abort word: every block stops at its next poll, its producer stops
+ * issuing copies and waits for those already in flight, and the turn marks the state
+ * failed and returns 9.  Waits on a block's own copies keep the default limit whatever
+ * this is set to, so no copy is left in flight.  Drops the model's cached graphs.
+ * Errors: 10 for a null handle. */
+int ck_set_step_wait_limit(ck_model* m, uint32_t polls);
+
 /* Layer-major prefill ("The forward pass, in order", phases 3 to 16 of prompt positions
  * that generate no token): when a turn reaches two or more such positions, ck_turn runs up
  * to `positions` of them (default 256) through each layer together, so every matrix is read
@@ -241,8 +251,12 @@ int ck_turn_batch(ck_model* m, void* const* dev_states, const size_t* lens, uint
  * the array and clears its counters first; calls whose work overlaps on the GPU (other
  * streams, other threads) race on it and must not be issued.  Errors: those of ck_turn,
  * and 10 when the persistent kernel cannot run this model or state, or when this position
- * needs more than 256 KB of scratch (4096 + 8 * heads * blocks per head * (head size + 2)
- * + 16 * blocks bytes, where the blocks are the GPU's SMs up to 768). */
+ * needs more than 256 KB of scratch.  With G blocks (the GPU's SMs, at most 768),
+ * gh = G / heads blocks a head (at least 1) and P the widest padded input (dim or hidden
+ * rounded up to a multiple of 128), the scratch is, each part rounded up to 256 bytes:
+ * 256 + 8 * heads (cleared counters), then 16 * heads * gh + 16 * G (attention maxima and
+ * sums, per-block classifier candidates), then 8 * dim (attention accumulators), then
+ * 24 * P (three byte-plane buffers).  The state is still sized by ck_state_size. */
 int ck_turn_noalloc(ck_model* m, void* dev_state, size_t len, void* stream, ck_turn_result* out);
 
 /* Copies the state's logits (i64[vocab], those of the last generating position) to host

@@ -31,6 +31,7 @@ class Pair:
 
     def __init__(self, ck, spec, path="step"):
         self.spec = spec
+        self.path = path
         self.art = synth.build_artifact(spec)
         self.orc = oracle.Model(self.art)
         rc, self.gpu = ck.Model.load(self.art)
@@ -45,9 +46,17 @@ class Pair:
         return so, sg
 
 
-def compare_states(orc_model, so, sg_host, n_prompt, max_tokens, what="", turns=True):
-    """Every specified field and buffer of two states (the working vectors are scratch).
-    turns=False skips the turn counter, for runs split into different numbers of turns."""
+# Working vectors (scratch in the state format) that a path leaves with the oracle's
+# contents after a position it runs alone: the phase kernels write the last layer's rotated
+# queries, head outputs, down-row output and SiLU output where the oracle does; the
+# persistent kernel writes only the queries there.
+VECTORS = {"kernels": ("q", "o", "y", "h"), "step": ("q",)}
+
+
+def compare_states(orc_model, so, sg_host, n_prompt, max_tokens, what="", turns=True, vectors=()):
+    """Every specified field and buffer of two states (the working vectors are scratch,
+    except those named in `vectors`).  turns=False skips the turn counter, for runs split
+    into different numbers of turns."""
     lay = orc_model.layout(n_prompt, max_tokens)
     assert so.size == sg_host.size == lay["size"]
     ho, hg = oracle.header(so), oracle.header(sg_host)
@@ -64,6 +73,13 @@ def compare_states(orc_model, so, sg_host, n_prompt, max_tokens, what="", turns=
         if not np.array_equal(a, b):
             bad = np.flatnonzero(a != b)
             raise AssertionError(f"{what}: buffer {name} differs at byte {bad[:8]}")
+    hidden = orc_model.config[1]
+    for name in vectors:
+        o, nbytes = lay[name], 8 * (hidden if name == "h" else d)
+        a, b = so[o:o + nbytes], sg_host[o:o + nbytes]
+        if not np.array_equal(a, b):
+            bad = np.flatnonzero(a != b)
+            raise AssertionError(f"{what}: working vector {name} differs at byte {bad[:8]}")
     for name in ("k", "v"):
         o, end = lay[name], (lay["v"] if name == "k" else lay["size"])
         a, b = so[o:end], sg_host[o:end]
@@ -213,6 +229,36 @@ def test_step_kernel_with_l2_prefetch(ck):
     assert P.gpu.set_step_prefetch(5000) == 10
 
 
+def test_step_kernel_barrier_timeout_fails_the_state_with_error_9(ck):
+    """The persistent kernel's timeout path, driven without a fault: with its barrier waits
+    cut to one poll, the first grid barrier gives up in the blocks that arrive before the
+    last; every block leaves (each producer first waits for its own copies in flight), the
+    turn returns 9 and the state is failed with error 9, the stream is idle afterwards, and
+    the allocation-free entry fails the same way.  Back at the default limit, a fresh state
+    on the same model runs bit-exact against the oracle."""
+    import torch
+    wl = MODELS["gqa"]
+    P = Pair(ck, wl.spec, "step")
+    ids = synth.prompt_ids(wl.spec, wl.n_prompt)
+    assert P.gpu.set_step_wait_limit(1) == 0
+    for entry in ("turn", "noalloc"):
+        so, sg = P.init(ck, ids, wl.steps)
+        rc, res = P.gpu.turn(sg, 1) if entry == "turn" else P.gpu.turn_noalloc(sg)
+        torch.cuda.current_stream().synchronize()
+        assert rc == 9 and res["complete"] == 1, (entry, rc, res)
+        h = oracle.header(ck.state_download(sg))
+        assert h["phase"] == oracle.PHASE_FAILED and h["error"] == 9 and h["position"] == 0, (entry, h)
+        assert P.gpu.turn(sg, 1)[0] == 3                       # a failed state is refused
+    assert P.gpu.set_step_wait_limit(0) == 0
+    so, sg = P.init(ck, ids, wl.steps)
+    for pos in range(wl.n_prompt + 2):
+        rco, reso = P.orc.turn(so, 1)
+        rcg, resg = P.gpu.turn(sg, 1)
+        assert rco == rcg == 0 and reso == resg, (pos, rcg, resg)
+        compare_states(P.orc, so, ck.state_download(sg), wl.n_prompt, wl.steps, f"after timeout pos {pos}",
+                       vectors=VECTORS["step"])
+
+
 @pytest.fixture(scope="module", params=list(PATHS))
 def pairs(ck, request):
     return {name: Pair(ck, wl.spec, request.param) for name, wl in MODELS.items()}
@@ -230,7 +276,8 @@ def test_every_position_matches_the_oracle(ck, pairs, name):
         rcg, resg = P.gpu.turn(sg, 1)
         assert rco == rcg == 0
         assert reso == resg, (pos, reso, resg)
-        compare_states(P.orc, so, ck.state_download(sg), wl.n_prompt, wl.steps, f"position {pos}")
+        compare_states(P.orc, so, ck.state_download(sg), wl.n_prompt, wl.steps, f"position {pos}",
+                       vectors=VECTORS[P.path])
     assert oracle.header(so)["phase"] == oracle.PHASE_DONE
     rc, toks = P.gpu.output_tokens(sg)
     assert rc == 0 and len(toks) == wl.steps
@@ -253,7 +300,7 @@ def test_sampled_positions_match_the_oracle(ck, pairs, temp, seed):
             rcg, resg = P.gpu.turn(sg, 1)
             assert rco == rcg == 0 and reso == resg, (name, pos, reso, resg)
             compare_states(P.orc, so, ck.state_download(sg), wl.n_prompt, wl.steps,
-                           f"{name} temperature {temp} position {pos}")
+                           f"{name} temperature {temp} position {pos}", vectors=VECTORS[P.path])
         h = oracle.header(so)
         assert h["phase"] == oracle.PHASE_DONE and h["exp_sum"] >= 1 << 30
 
@@ -445,6 +492,33 @@ def test_llama7b_shape_sampled_positions(ck, path):
     h = _resume_one(ck, synth.LLAMA7B, n_prompt=3, max_tokens=4, gpu_positions=2, check_positions=1,
                     path=path)
     assert h["generated"] == 1
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_llama7b_bench_positions(ck, path):
+    """The benchmark's own run at full size: the 7B-shaped model, its 128 prompt ids run on
+    the GPU as bench.py runs them (127 layer-major, then the position that generates the
+    first token), the state sized for the workload's 256 tokens; then generating positions
+    128 and 129 on both targets from the GPU's state, every buffer and the working vectors
+    the path writes compared after each."""
+    spec = synth.LLAMA7B
+    n_prompt, max_tokens = 128, 256
+    P = Pair(ck, spec, path)
+    ids = synth.prompt_ids(spec, n_prompt, run=0)
+    sg = P.gpu.new_state(n_prompt, max_tokens)
+    assert P.gpu.init_state(sg, ids, max_tokens) == 0
+    rc, res = P.gpu.turn(sg, n_prompt - 1)
+    assert rc == 0 and res["work"] == n_prompt - 1
+    rc, res = P.gpu.turn(sg, 1)
+    assert rc == 0 and res["generated"] == 1
+    host = ck.state_download(sg)
+    for pos in (n_prompt, n_prompt + 1):
+        rco, reso = P.orc.turn(host, 1)
+        rcg, resg = P.gpu.turn(sg, 1)
+        assert rco == rcg == 0 and reso == resg, (pos, reso, resg)
+        compare_states(P.orc, host, ck.state_download(sg), n_prompt, max_tokens, f"7B position {pos}",
+                       vectors=VECTORS[path])
+    assert oracle.header(host)["generated"] == 3
 
 
 @pytest.mark.parametrize("path", list(PATHS))
