@@ -206,10 +206,13 @@ cudaError_t upload_grouped(uint8_t* dst, uint32_t rows, uint32_t cols, uint32_t 
 // ------------------------------------------------------------------ small kernels
 
 // Phase 3: x[i] = ((byte - 128) * scale) >> 8 over the row of this position's token.
+// It also clears the position's sums of squares (nslots words at `slots`), which the
+// kernels producing each residual add into.
 __global__ void k_embed(uint8_t* st, uint64_t off_prompt, uint64_t off_out, int64_t* x,
                         const uint8_t* embed, const uint32_t* scale, uint32_t pitch, uint32_t dim,
-                        uint32_t vocab) {
+                        uint32_t vocab, unsigned long long* slots, uint32_t nslots) {
   if (hdr_ld<uint32_t>(st, kHPhase) != CK_PHASE_RUNNING) return;
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < nslots; i += gridDim.x * blockDim.x) slots[i] = 0;
   const uint32_t pos = hdr_ld<uint32_t>(st, kHPosition), np = hdr_ld<uint32_t>(st, kHNPrompt);
   const uint32_t tok = pos < np ? reinterpret_cast<const uint32_t*>(st + off_prompt)[pos]
                                 : reinterpret_cast<const uint32_t*>(st + off_out)[pos - np];
@@ -226,12 +229,10 @@ __global__ void k_embed(uint8_t* st, uint64_t off_prompt, uint64_t off_out, int6
     x[i] = ((int64_t)embed[grouped_offset(vocab, tok, i)] - 128) * s >> 8;
 }
 
-// End of a prompt position: the last residual (x = xb + y), then the cursor moves on, or
-// the state is marked failed if a cache store did not fit.
-__global__ void k_finish_prompt(uint8_t* st, int64_t* x, const int64_t* xb, const int64_t* y,
-                                uint32_t dim) {
+// End of a prompt position (its last residual is already in x): the cursor moves on, or the
+// state is marked failed if a cache store did not fit.
+__global__ void k_finish_prompt(uint8_t* st) {
   if (hdr_ld<uint32_t>(st, kHPhase) != CK_PHASE_RUNNING) return;
-  for (uint32_t i = threadIdx.x; i < dim; i += blockDim.x) x[i] = wadd(xb[i], y[i]);
   if (threadIdx.x == 0) {
     if (hdr_ld<uint64_t>(st, kHErrKey) != kNoError) {
       hdr<uint32_t>(st, kHPhase) = CK_PHASE_FAILED;
@@ -418,13 +419,18 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
   const size_t layer_words = (size_t)lay.cache * m->kv_dim;
   const int cl = attention_cluster(lay.cache);
 
+  // sums of squares of the residuals: slot 2l feeds layer l's attention norm (l >= 1),
+  // 2l + 1 its feed-forward norm, 2 layers the final norm; each is added up by the kernel that
+  // produces the residual (O and DOWN epilogues) and read whole by the normalizing kernel
+  unsigned long long* ss = reinterpret_cast<unsigned long long*>(st + lay.scores);
+  const uint32_t nslots = 2 * c.layers + 1;
   k_embed<<<(c.dim + 255) / 256, 256, 0, s>>>(st, lay.prompt, lay.out, x, m->embed, m->embed_scale,
-                                              m->pitch_d, c.dim, c.vocab);
+                                              m->pitch_d, c.dim, c.vocab, ss, nslots);
   CK_CUDA(cudaGetLastError());
-  int64_t* cur = x;  // the buffer holding the activations
+  int64_t* cur = x;  // the buffer holding the activations (x and xb take turns)
   for (uint32_t l = 0; l < c.layers; ++l) {
     const DevLayer& W = m->layers[l];
-    // phases 4-8: residual of the previous layer, attention norm, Q/K/V, cache stores, rotary
+    // phases 4-8: attention norm, Q/K/V, cache stores, rotary
     MatrowParams p = {};
     p.W = W.wqkv;
     p.scale = W.sqkv;
@@ -435,12 +441,7 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
     p.pro = kProNorm;
     p.in = cur;
     p.norm_w = W.attn_norm;
-    if (l > 0) {
-      int64_t* next = cur == x ? xb : x;
-      p.add = y;
-      p.res_out = next;
-      cur = next;
-    }
+    if (l > 0) p.ss_in = ss + 2 * l;  // layer 0's embedding: the prologue adds its squares up
     p.epi = kEpiQKV;
     p.out = q;
     p.q_rows = c.dim;
@@ -469,7 +470,8 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
     a.cache = lay.cache;
     a.chunk_cap = (lay.cache + cl - 1) / cl;
     CK_CUDA(launch_attention(a, s, cl));
-    // phase 10
+    // phases 10-11: output rows, residual (and its squares for the feed-forward norm)
+    int64_t* next = cur == x ? xb : x;
     MatrowParams po = {};
     po.W = W.wo;
     po.scale = W.so;
@@ -481,10 +483,13 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
     po.in = o;
     po.epi = kEpiStore;
     po.out = y;
+    po.resid_in = cur;
+    po.resid_out = next;
+    po.ss_out = ss + 2 * l + 1;
     po.state = st;
     CK_CUDA(launch_matrow(po, s, m->num_sms));
-    // phases 11-14: residual, feed-forward norm, gate and up, SiLU gating
-    int64_t* next = cur == x ? xb : x;
+    cur = next;
+    // phases 12-14: feed-forward norm, gate and up, SiLU gating
     MatrowParams pg = {};
     pg.W = W.w13;
     pg.scale = W.s13;
@@ -494,16 +499,15 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
     pg.cols = c.dim;
     pg.pro = kProNorm;
     pg.in = cur;
-    pg.add = y;
-    pg.res_out = next;
+    pg.ss_in = ss + 2 * l + 1;
     pg.norm_w = W.ffn_norm;
     pg.epi = kEpiSiLU;
     pg.out = hbuf;
     pg.silu_tab = m->silu_tab;
     pg.state = st;
-    cur = next;
     CK_CUDA(launch_matrow(pg, s, m->num_sms));
-    // phase 15 (its residual, phase 16, is added by the next consumer)
+    // phases 15-16: down rows, residual (and its squares for the next norm)
+    next = cur == x ? xb : x;
     MatrowParams pd = {};
     pd.W = W.w2;
     pd.scale = W.s2;
@@ -515,12 +519,16 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
     pd.in = hbuf;
     pd.epi = kEpiStore;
     pd.out = y;
+    pd.resid_in = cur;
+    pd.resid_out = next;
+    pd.ss_out = ss + 2 * (l + 1);
     pd.state = st;
     CK_CUDA(launch_matrow(pd, s, m->num_sms));
+    cur = next;
   }
-  if (cur != xb) return CK_INVALID_STATE;  // an odd number of residual flips, by construction
+  if (cur != x) return CK_INVALID_STATE;  // an even number of residual flips, by construction
   if (generating) {
-    // phases 16-18: last residual into x, final norm, classifier
+    // phases 17-18: final norm, classifier
     MatrowParams pc = {};
     pc.W = m->cls;
     pc.scale = m->cls_scale;
@@ -529,9 +537,8 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
     pc.rows = c.vocab;
     pc.cols = c.dim;
     pc.pro = kProNorm;
-    pc.in = xb;
-    pc.add = y;
-    pc.res_out = x;
+    pc.in = x;
+    pc.ss_in = ss + 2 * c.layers;
     pc.norm_w = m->final_norm;
     pc.epi = kEpiStore;
     pc.out = logits;
@@ -539,7 +546,7 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
     CK_CUDA(launch_matrow(pc, s, m->num_sms));
     k_sample_finish<<<1, kArgThreads, 0, s>>>(st, lay.out, logits, c.vocab, m->exp_tab);  // phase 19
   } else {
-    k_finish_prompt<<<1, 256, 0, s>>>(st, x, xb, y, c.dim);
+    k_finish_prompt<<<1, 32, 0, s>>>(st);
   }
   CK_CUDA(cudaGetLastError());
   return CK_OK;

@@ -236,9 +236,17 @@ struct MatrowParams {
   const int64_t* add;    // norm: residual addend (nullptr: none)
   int64_t* res_out;      // norm with addend: where block 0 writes in + add
   const int32_t* norm_w;
+  // norm: the sum of the squares of `in`, complete (added up by the kernel that produced
+  // `in`); nullptr: the prologue adds it up itself
+  const unsigned long long* ss_in;
   // epilogue
   int epi;
   int64_t* out;          // store: y[rows]; QKV: rotated queries [q_rows]; SiLU: h[rows / 2]
+  // store with a residual (the page's phases 11 and 16 moved into the producing kernel):
+  // resid_out[r] = resid_in[r] + y[r], and the squares of resid_out added into *ss_out
+  const int64_t* resid_in;
+  int64_t* resid_out;
+  unsigned long long* ss_out;
   uint32_t q_rows, kv_dim, head_dim, layer, cache;
   int32_t* kcache;       // this layer's keys, position 0 (i32 [cache][kv_dim])
   int32_t* vcache;

@@ -34,6 +34,7 @@ struct Scratch {
   unsigned long long S;
   unsigned long long orv;
   unsigned long long tot[kChunkRows];  // row totals of the current chunk
+  long long res[kChunkRows];           // residual inputs of the chunk's rows (store epilogue)
 };
 
 // Programmatic dependent launch.  wait_prior_grids returns once the kernels before this one
@@ -42,6 +43,15 @@ struct Scratch {
 // prologue on SMs this grid frees.
 __device__ __forceinline__ void wait_prior_grids() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// 8-byte asynchronous copy from global to shared memory, and the wait for all of this
+// thread's copies.
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(src) : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ unsigned long long warp_sum(unsigned long long v) {
 #pragma unroll
@@ -134,7 +144,7 @@ __device__ __forceinline__ void prologue_early(const MatrowParams& p, Scratch* s
       const uint32_t g = threadIdx.x + j * kThreads, i = 4 * g + e;
       nw.w[j][e] = norm && g < words && i < n ? __ldg(p.norm_w + i) : 0;
     }
-  if (norm && threadIdx.x == 32) sc->divn = make_invdiv_clz(n);
+  if (norm && threadIdx.x == (p.ss_in ? 0 : 32)) sc->divn = make_invdiv_clz(n);
 }
 
 // Packs the input vector (optionally residual-added and RMS-normalised) into byte planes.
@@ -145,7 +155,26 @@ __device__ int prologue(const MatrowParams& p, uint32_t* planes32, Scratch* sc,
   const bool norm = p.pro == kProNorm;
   const bool held = words <= (uint32_t)kPG * kThreads;  // one batch: values stay in registers
   int64_t xv[kPG][4];
-  if (norm) {
+  if (norm && p.ss_in) {
+    // the producer added up the squares: the values load while thread 0 forms the RMS
+    // reciprocal, then one pass normalises and packs
+    if (held) {
+#pragma unroll
+      for (int j = 0; j < kPG; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t g = threadIdx.x + j * kThreads, i = 4 * g + e;
+          xv[j][e] = g < words && i < n ? p.in[i] : 0;
+        }
+    }
+    if (threadIdx.x == 0) {
+      const unsigned long long ss = *reinterpret_cast<const volatile unsigned long long*>(p.ss_in);
+      uint64_t rms = isqrt_u64(udiv_inv(ss, sc->divn) + 42950ull);  // floor(ss / n)
+      if (rms < 1) rms = 1;
+      sc->div = make_invdiv_clz((uint32_t)rms);
+    }
+    __syncthreads();
+  } else if (norm) {
     // "RMS normalization": rms = isqrt(sum(x*x) / n + 42,950), at least 1.
     unsigned long long ss = 0, dummy = 0;
     for (uint32_t g0 = threadIdx.x; g0 < words; g0 += kPG * kThreads) {
@@ -408,6 +437,8 @@ __device__ void rows_loop(const MatrowParams& p, const uint8_t* planes, Scratch*
     const uint32_t frow = c0 + threadIdx.x, fprow = frow ^ 1u;
     const uint32_t fscale = frow < c1 ? __ldg(p.scale + frow) : 0u;
     const uint32_t fpscale = frow < c1 && fprow < c1 ? __ldg(p.scale + fprow) : 0u;
+    // the residual inputs of the chunk's rows, copied into shared memory while the items stream
+    if (p.resid_out && frow < c1) cp_async8(&sc->res[threadIdx.x], p.resid_in + frow);
     for (uint32_t it = warp; it < items; it += kWarps) {
       uint4 w[kG];
 #pragma unroll
@@ -429,13 +460,25 @@ __device__ void rows_loop(const MatrowParams& p, const uint8_t* planes, Scratch*
       const uint32_t rl = r0 - c0 + (uint32_t)(lane >> 2);
       if ((lane & 3) == 0 && c0 + rl < c1) atomicAdd(&sc->tot[rl], tot);
     }
+    if (p.resid_out) cp_async_wait_all();
     __syncthreads();
+    unsigned long long sq = 0;
     if (frow < c1) {
       const uint32_t t = threadIdx.x;
       const int64_t y = (int64_t)((sc->tot[t] - (S << 7)) * (unsigned long long)fscale) >> 24;
       const int64_t partner =
           fprow < c1 ? (int64_t)((sc->tot[t ^ 1u] - (S << 7)) * (unsigned long long)fpscale) >> 24 : 0;
       epilogue(p, frow, y, partner, pos);
+      if (p.resid_out) {
+        // the residual (phases 11 and 16) and its square for the next normalization
+        const int64_t xr = wadd(sc->res[t], y);
+        p.resid_out[frow] = xr;
+        sq = (unsigned long long)xr * (unsigned long long)xr;
+      }
+    }
+    if (p.resid_out && (threadIdx.x & ~31u) < c1 - c0) {
+      sq = warp_sum(sq);
+      if ((threadIdx.x & 31) == 0) atomicAdd(p.ss_out, sq);
     }
     __syncthreads();
     for (uint32_t t = threadIdx.x; t < kChunkRows; t += kThreads) sc->tot[t] = 0;
