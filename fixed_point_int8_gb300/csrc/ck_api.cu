@@ -424,8 +424,15 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
   // produces the residual (O and DOWN epilogues) and read whole by the normalizing kernel
   unsigned long long* ss = reinterpret_cast<unsigned long long*>(st + lay.scores);
   const uint32_t nslots = 2 * c.layers + 1;
+  // after them (256-byte aligned), where the work region holds it: the attention outputs'
+  // sums before their >> 24, added into by every attention CTA, read by the O kernel and
+  // cleared by the gate/up kernel for the next layer
+  const uint32_t oacc_word = (nslots + 31) & ~31u;
+  const bool use_oacc = 8ull * ((uint64_t)oacc_word + c.dim) <= lay.k - lay.scores;
+  unsigned long long* oacc = use_oacc ? ss + oacc_word : nullptr;
   k_embed<<<(c.dim + 255) / 256, 256, 0, s>>>(st, lay.prompt, lay.out, x, m->embed, m->embed_scale,
-                                              m->pitch_d, c.dim, c.vocab, ss, nslots);
+                                              m->pitch_d, c.dim, c.vocab, ss,
+                                              use_oacc ? oacc_word + c.dim : nslots);
   CK_CUDA(cudaGetLastError());
   int64_t* cur = x;  // the buffer holding the activations (x and xb take turns)
   for (uint32_t l = 0; l < c.layers; ++l) {
@@ -469,6 +476,7 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
     a.inv_sqrt = m->inv_sqrt;
     a.cache = lay.cache;
     a.chunk_cap = (lay.cache + cl - 1) / cl;
+    a.o_acc = oacc;
     CK_CUDA(launch_attention(a, s, cl));
     // phases 10-11: output rows, residual (and its squares for the feed-forward norm)
     int64_t* next = cur == x ? xb : x;
@@ -481,6 +489,8 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
     po.cols = c.dim;
     po.pro = kProPlain;
     po.in = o;
+    po.in_acc = oacc;  // when set: o is written from the sums by block 0
+    po.in_out = o;
     po.epi = kEpiStore;
     po.out = y;
     po.resid_in = cur;
@@ -504,6 +514,8 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
     pg.epi = kEpiSiLU;
     pg.out = hbuf;
     pg.silu_tab = m->silu_tab;
+    pg.acc_clear = oacc;
+    pg.acc_words = c.dim;
     pg.state = st;
     CK_CUDA(launch_matrow(pg, s, m->num_sms));
     // phases 15-16: down rows, residual (and its squares for the next norm)

@@ -37,10 +37,29 @@ __device__ __forceinline__ unsigned long long warp_sum(unsigned long long v) {
   return v;
 }
 
+// Shared memory: queries, per-warp and per-CTA partials, maximum, sum, reduction slots, the
+// chunk's scores, then (16-byte aligned) the first batch of value rows.
+__host__ __device__ inline size_t attn_vpre_offset(uint32_t hd, uint32_t chunk_cap) {
+  return (8 * ((size_t)hd * (2 + kWarps) + 2 + kWarps + chunk_cap) + 15) & ~(size_t)15;
+}
+
+// 16-byte asynchronous copy from global to shared memory (zeros and no read when not valid),
+// and the wait for all of this thread's copies.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n\tcp.async.commit_group;" ::"r"(d), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // Lanes per position = hd / 4, four elements a lane; a warp issues kUnroll steps' cache loads
-// before it uses them.  64 registers a thread, so that several CTAs fit an SM beside the tail
-// of the previous kernel (deeper unrolling costs registers and measured slower).
-__global__ void __launch_bounds__(kThreads) k_attention(const AttnParams p) {
+// before it uses them.  The first batch of key rows of earlier positions is loaded into
+// registers before the dependency wait, the first batch of value rows into shared memory
+// (each lane copies what it reads back itself), the newest rows together with the queries
+// after it.  64 registers a thread, so that four CTAs fit an SM: a head's cluster of eight
+// is placed as soon as two SMs are free of the previous kernel.
+__global__ void __launch_bounds__(kThreads, 4) k_attention(const AttnParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   cg::cluster_group cluster = cg::this_cluster();
   const uint32_t hd = p.head_dim;
@@ -52,11 +71,12 @@ __global__ void __launch_bounds__(kThreads) k_attention(const AttnParams p) {
   unsigned long long* csum = reinterpret_cast<unsigned long long*>(cmax + 1);   // [1]
   long long* red = reinterpret_cast<long long*>(csum + 1);                      // [kWarps]
   long long* sc = red + kWarps;                                                 // [chunk_cap]
+  int4* vpre = reinterpret_cast<int4*>(smem + attn_vpre_offset(hd, p.chunk_cap));  // [kUnroll][kThreads]
 
   // Launched with programmatic dependent launch.  Before the wait this kernel reads only what
   // was written before the previous kernel started: the position (set by the previous
   // position's last kernel) and the cache rows of earlier positions.  The queries and the
-  // newest cache row come from the kernel just before: after the wait.
+  // newest cache rows come from the kernel just before: after the wait.
   const uint32_t pos = hdr_ld<uint32_t>(p.state, kHPosition);
   const uint32_t P = pos + 1;  // positions so far, the current one included
   const uint32_t older = min(pos, p.cache);  // rows below this were written at earlier positions
@@ -72,20 +92,32 @@ __global__ void __launch_bounds__(kThreads) k_attention(const AttnParams p) {
   const uint32_t ppw = 32 / lpp;     // positions per warp step
   const uint32_t sub = lane % lpp, slot = lane / lpp, e0 = sub * 4;
   const uint32_t base0 = warp * ppw;
-  int4 k4[kUnroll];  // the warp's first batch of keys
+  int4 k4[kUnroll];  // the warp's first batch of keys (its values wait in vpre)
 #pragma unroll
   for (int u = 0; u < kUnroll; ++u) {
     const uint32_t tl = base0 + u * kWarps * ppw + slot;
-    k4[u] = tl < n && t0 + tl < older ? *reinterpret_cast<const int4*>(Kh + (size_t)(t0 + tl) * hd + e0)
-                                      : make_int4(0, 0, 0, 0);
+    const bool early = tl < n && t0 + tl < older;
+    k4[u] = early ? *reinterpret_cast<const int4*>(Kh + (size_t)(t0 + tl) * hd + e0) : make_int4(0, 0, 0, 0);
+    if (early) cp_async16(vpre + u * kThreads + tid, Vh + (size_t)(t0 + tl) * hd + e0, true);
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // the phase is tested after the queries are requested (the whole cluster reads the same
-  // header word and returns alike)
+  // the newest rows of the first batch and the queries, requested together; the phase is
+  // tested after them (the whole cluster reads the same header word and returns alike)
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const uint32_t tl = base0 + u * kWarps * ppw + slot;
+    if (tl < n && t0 + tl >= older) {
+      k4[u] = *reinterpret_cast<const int4*>(Kh + (size_t)(t0 + tl) * hd + e0);
+      cp_async16(vpre + u * kThreads + tid, Vh + (size_t)(t0 + tl) * hd + e0, true);
+    }
+  }
   const bool running = hdr_ld<uint32_t>(p.state, kHPhase) == CK_PHASE_RUNNING;
   for (uint32_t i = tid; i < hd; i += kThreads) q_s[i] = p.q[(size_t)h * hd + i];
-  if (!running) return;
+  if (!running) {
+    cp_async_wait_all();  // no copy into shared memory outlives the CTA
+    return;
+  }
   __syncthreads();
 
   const int64_t q0 = q_s[e0], q1 = q_s[e0 + 1], q2 = q_s[e0 + 2], q3 = q_s[e0 + 3];
@@ -93,14 +125,12 @@ __global__ void __launch_bounds__(kThreads) k_attention(const AttnParams p) {
   // stage 0: s_t = (((q . k_t) >> 16) * inv) >> 24, products and sums wrapping; keep the max
   long long lmax = LLONG_MIN;
   for (uint32_t base = base0; base < n; base += kUnroll * kWarps * ppw) {
+    if (base != base0) {
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const uint32_t tl = base + u * kWarps * ppw + slot;
-      // the first batch has all but the newest row already
-      if (tl < n && (base != base0 || t0 + tl >= older))
-        k4[u] = *reinterpret_cast<const int4*>(Kh + (size_t)(t0 + tl) * hd + e0);
-      else if (base != base0)
-        k4[u] = make_int4(0, 0, 0, 0);
+      for (int u = 0; u < kUnroll; ++u) {
+        const uint32_t tl = base + u * kWarps * ppw + slot;
+        k4[u] = tl < n ? *reinterpret_cast<const int4*>(Kh + (size_t)(t0 + tl) * hd + e0) : make_int4(0, 0, 0, 0);
+      }
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
@@ -153,6 +183,10 @@ __global__ void __launch_bounds__(kThreads) k_attention(const AttnParams p) {
   cluster.sync();
   unsigned long long Z = 0;
   for (uint32_t r = 0; r < CL; ++r) Z += *cluster.map_shared_rank(csum, r);
+  // this CTA has read its peers' maxima and sums: it arrives on the cluster barrier now and
+  // waits on it only before it leaves (or exchanges again), so no CTA's shared memory goes
+  // while a peer may still read it
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 
   // stage 2: P_t = (e_t << 24) / Z, 24 fractional bits
   for (uint32_t tl = tid; tl < n; tl += kThreads)
@@ -161,12 +195,16 @@ __global__ void __launch_bounds__(kThreads) k_attention(const AttnParams p) {
 
   // stage 3: sum over positions of P_t * v_t[j] (exact: |sum| < 2^55), then one >> 24
   unsigned long long a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-  for (uint32_t base = warp * ppw; base < n; base += kUnroll * kWarps * ppw) {
+  cp_async_wait_all();  // the first batch of values
+  for (uint32_t base = base0; base < n; base += kUnroll * kWarps * ppw) {
     int4 v4[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const uint32_t tl = base + u * kWarps * ppw + slot;
-      v4[u] = tl < n ? *reinterpret_cast<const int4*>(Vh + (size_t)(t0 + tl) * hd + e0) : make_int4(0, 0, 0, 0);
+      // first batch: slots past the chunk were never written, and their probability is 0
+      v4[u] = base == base0 ? vpre[u * kThreads + tid]
+              : tl < n      ? *reinterpret_cast<const int4*>(Vh + (size_t)(t0 + tl) * hd + e0)
+                            : make_int4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
@@ -192,11 +230,23 @@ __global__ void __launch_bounds__(kThreads) k_attention(const AttnParams p) {
     dst[3] = a3;
   }
   __syncthreads();
+  if (p.o_acc) {
+    // the CTA's partial sums go straight into the head's accumulators (wrapping adds, so the
+    // order of the CTAs changes no bit); the next kernel applies the >> 24
+    for (uint32_t j = tid; j < hd; j += kThreads) {
+      unsigned long long s = 0;
+      for (int w = 0; w < kWarps; ++w) s += part[(size_t)w * hd + j];
+      atomicAdd(p.o_acc + (size_t)h * hd + j, s);
+    }
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    return;
+  }
   for (uint32_t j = tid; j < hd; j += kThreads) {
     unsigned long long s = 0;
     for (int w = 0; w < kWarps; ++w) s += part[(size_t)w * hd + j];
     cpart[j] = s;
   }
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   cluster.sync();
   if (rank == 0) {
     for (uint32_t j = tid; j < hd; j += kThreads) {
@@ -209,7 +259,7 @@ __global__ void __launch_bounds__(kThreads) k_attention(const AttnParams p) {
 }
 
 size_t attn_smem(uint32_t hd, uint32_t chunk_cap) {
-  return 8 * ((size_t)hd * (2 + kWarps) + 2 + kWarps + chunk_cap);
+  return attn_vpre_offset(hd, chunk_cap) + (size_t)kUnroll * kThreads * 16;
 }
 
 }  // namespace

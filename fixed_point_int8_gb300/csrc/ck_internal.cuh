@@ -233,12 +233,20 @@ struct MatrowParams {
   // prologue: the input vector of `cols` elements
   int pro;
   const int64_t* in;     // plain: the vector; norm: the activations
+  // plain, instead of `in`: wrapping sums whose arithmetic >> 24 is the vector (the attention
+  // outputs before their shift); block 0 writes the shifted vector to in_out
+  const unsigned long long* in_acc;
+  int64_t* in_out;
   const int64_t* add;    // norm: residual addend (nullptr: none)
   int64_t* res_out;      // norm with addend: where block 0 writes in + add
   const int32_t* norm_w;
   // norm: the sum of the squares of `in`, complete (added up by the kernel that produced
   // `in`); nullptr: the prologue adds it up itself
   const unsigned long long* ss_in;
+  // acc_words words to zero after the wait, split over the CTAs (the attention sums the
+  // previous kernel has read, for their next use), or nullptr
+  unsigned long long* acc_clear;
+  uint32_t acc_words;
   // epilogue
   int epi;
   int64_t* out;          // store: y[rows]; QKV: rotated queries [q_rows]; SiLU: h[rows / 2]
@@ -258,7 +266,10 @@ struct MatrowParams {
 struct AttnParams {
   uint8_t* state;
   const int64_t* q;      // rotated queries [heads * hd]
-  int64_t* o;            // head outputs [heads * hd]
+  int64_t* o;            // head outputs [heads * hd] (when o_acc is null)
+  // not null: every CTA adds its partial weighted sums of values (before the >> 24) into
+  // these zeroed words [heads * hd] instead, and the next kernel applies the shift
+  unsigned long long* o_acc;
   const int32_t* kcache; // this layer, position 0
   const int32_t* vcache;
   const uint32_t* exp_tab;

@@ -212,7 +212,7 @@ __device__ int prologue(const MatrowParams& p, uint32_t* planes32, Scratch* sc,
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const uint32_t g = g0 + j * kThreads, i = 4 * g + e;
-          pv[j][e] = g < words && i < n ? p.in[i] : 0;
+          pv[j][e] = g < words && i < n ? (p.in_acc ? (int64_t)p.in_acc[i] >> 24 : p.in[i]) : 0;
         }
 #pragma unroll
       for (int j = 0; j < kPGP; ++j) {
@@ -220,6 +220,8 @@ __device__ int prologue(const MatrowParams& p, uint32_t* planes32, Scratch* sc,
         if (g >= words) break;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
+          // the shifted attention outputs, kept in the state by block 0
+          if (p.in_acc && running && blockIdx.x == 0 && 4 * g + e < n) p.in_out[4 * g + e] = pv[j][e];
           S += (unsigned long long)pv[j][e];
           orv |= (unsigned long long)(pv[j][e] ^ (pv[j][e] >> 63));
         }
@@ -509,6 +511,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_matrow(const MatrowParams p) {
   prologue_early(p, sc, nw);
   wait_prior_grids();
   allow_next_grid();
+  if (p.acc_clear) {  // the previous kernel has read these sums: clear them for their next use
+    const uint32_t w0 = (uint32_t)((uint64_t)blockIdx.x * p.acc_words / gridDim.x);
+    const uint32_t w1 = (uint32_t)((uint64_t)(blockIdx.x + 1) * p.acc_words / gridDim.x);
+    for (uint32_t i = w0 + threadIdx.x; i < w1; i += kThreads) p.acc_clear[i] = 0;
+  }
   if (rb >= re) return;
   // The state's phase is read here but tested only after the prologue, so that its vector
   // loads need not wait for it: for a failed state the prologue skips its one kind of global
