@@ -766,7 +766,7 @@ uint64_t ck_host_isqrt(uint64_t v) { return isqrt_u64(v); }
 
 int64_t ck_host_div_trunc(int64_t n, uint32_t d) {
   if (d == 0) return 0;
-  return sdiv_trunc(n, make_invdiv(d));
+  return sdiv_trunc(n, make_invdiv_fast(d));
 }
 
 int ck_model_size(const void* artifact, size_t len, size_t* dev_bytes) {

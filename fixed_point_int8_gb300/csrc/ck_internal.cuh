@@ -123,6 +123,42 @@ __host__ __device__ inline InvDiv make_invdiv(uint32_t d) {
   return D;
 }
 
+// floor(n / d) for 1 <= d < 2^32 and n < d * 2^32 (the quotient fits 32 bits): an estimate
+// from a single-precision reciprocal, one refinement on the exact remainder, then exact
+// integer corrections (both remainders are taken modulo 2^64 and read as signed: their true
+// values are far inside the signed range).  Two of these build the reciprocal below in a few
+// dozen operations instead of two 64-bit divisions.
+__host__ __device__ inline uint64_t div_small_quotient(uint64_t n, uint32_t d) {
+  const float rcp = 1.0f / (float)d;
+  uint64_t q = (uint64_t)((float)n * rcp);      // within about 2^10 of the quotient
+  if (q > 0xFFFFFFFFull) q = 0xFFFFFFFFull;
+  int64_t r = (int64_t)(n - q * d);             // |r| < 2^43
+  q = (uint64_t)((int64_t)q + (int64_t)floorf((float)r * rcp));
+  r = (int64_t)(n - q * d);                     // within a few d of [0, d)
+  while (r < 0) { --q; r += d; }
+  while (r >= (int64_t)d) { ++q; r -= d; }
+  return q;
+}
+
+// make_invdiv with the two 64-by-32 steps done by div_small_quotient and l = ceil(log2 d)
+// from a count of leading zeros.
+__host__ __device__ inline InvDiv make_invdiv_fast(uint32_t d) {
+#ifdef __CUDA_ARCH__
+  const uint32_t l = d <= 1 ? 0u : 32u - (uint32_t)__clz((int)(d - 1));
+#else
+  const uint32_t l = d <= 1 ? 0u : 32u - (uint32_t)__builtin_clz(d - 1);
+#endif
+  const uint64_t a = (1ull << l) - d;  // a < d < 2^32
+  const uint64_t hi = div_small_quotient(a << 32, d);
+  const uint64_t rem = (a << 32) - hi * d;
+  const uint64_t lo = div_small_quotient(rem << 32, d);
+  InvDiv D;
+  D.m = ((hi << 32) | lo) + 1;
+  D.sh1 = l < 1 ? l : 1;
+  D.sh2 = l > 0 ? l - 1 : 0;
+  return D;
+}
+
 __host__ __device__ inline uint64_t udiv_inv(uint64_t n, const InvDiv& D) {
   const uint64_t t = mulhi_u64(D.m, n);
   return (t + ((n - t) >> D.sh1)) >> D.sh2;

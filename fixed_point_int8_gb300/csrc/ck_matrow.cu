@@ -107,21 +107,6 @@ struct NormWeights {
   int32_t w[kPG][4];
 };
 
-// The reciprocal of d as make_invdiv builds it, with l = ceil(log2 d) from a count of
-// leading zeros instead of a loop.
-__device__ __forceinline__ InvDiv make_invdiv_clz(uint32_t d) {
-  const uint32_t l = d <= 1 ? 0u : 64u - (uint32_t)__clzll((long long)(d - 1));
-  const uint64_t a = (1ull << l) - d;  // a < d < 2^32
-  const uint64_t hi = (a << 32) / d;
-  const uint64_t rem = (a << 32) - hi * d;
-  const uint64_t lo = (rem << 32) / d;
-  InvDiv D;
-  D.m = ((hi << 32) | lo) + 1;
-  D.sh1 = l < 1 ? l : 1;
-  D.sh2 = l > 0 ? l - 1 : 0;
-  return D;
-}
-
 // out[k] gets byte k of in[0..3] as its bytes 0..3: a 4 x 4 byte transpose in eight byte
 // permutes (pairs interleaved by byte, then by byte pair).
 __device__ __forceinline__ void transpose_bytes4(const uint32_t (&in)[4], uint32_t* out) {
@@ -144,7 +129,7 @@ __device__ __forceinline__ void prologue_early(const MatrowParams& p, Scratch* s
       const uint32_t g = threadIdx.x + j * kThreads, i = 4 * g + e;
       nw.w[j][e] = norm && g < words && i < n ? __ldg(p.norm_w + i) : 0;
     }
-  if (norm && threadIdx.x == (p.ss_in ? 0 : 32)) sc->divn = make_invdiv_clz(n);
+  if (norm && threadIdx.x == (p.ss_in ? 0 : 32)) sc->divn = make_invdiv_fast(n);
 }
 
 // Packs the input vector (optionally residual-added and RMS-normalised) into byte planes.
@@ -171,7 +156,7 @@ __device__ int prologue(const MatrowParams& p, uint32_t* planes32, Scratch* sc,
       const unsigned long long ss = *reinterpret_cast<const volatile unsigned long long*>(p.ss_in);
       uint64_t rms = isqrt_u64(udiv_inv(ss, sc->divn) + 42950ull);  // floor(ss / n)
       if (rms < 1) rms = 1;
-      sc->div = make_invdiv_clz((uint32_t)rms);
+      sc->div = make_invdiv_fast((uint32_t)rms);
     }
     __syncthreads();
   } else if (norm) {
@@ -198,7 +183,7 @@ __device__ int prologue(const MatrowParams& p, uint32_t* planes32, Scratch* sc,
     if (threadIdx.x == 0) {
       uint64_t rms = isqrt_u64(udiv_inv(ss, sc->divn) + 42950ull);  // floor(ss / n)
       if (rms < 1) rms = 1;
-      sc->div = make_invdiv_clz((uint32_t)rms);
+      sc->div = make_invdiv_fast((uint32_t)rms);
     }
     __syncthreads();
   }

@@ -74,6 +74,19 @@ def test_host_division_by_invariant_divisor(ck):
             assert ck.host_div_trunc(n, d) == _trunc_div(n, d), (n, d)
 
 
+def test_host_division_reciprocal_for_every_small_divisor_and_near_powers_of_two(ck):
+    """The reciprocal the normalization builds from two estimated 64-by-32 divisions: every
+    divisor up to 5,000 and those next to each power of two, each against numerators at the
+    quotient boundaries and the extremes."""
+    divisors = list(range(1, 5001))
+    for k in range(1, 33):
+        divisors += [v for v in (2**k - 1, 2**k, 2**k + 1) if 1 <= v < 2**32]
+    for d in divisors:
+        for n in (0, d - 1, d, 2**63 - 1, -2**63, d * (2**31 // d) - 1, 12345 * d + d - 1, -(d + 1)):
+            n = max(min(n, 2**63 - 1), -2**63)
+            assert ck.host_div_trunc(n, d) == _trunc_div(n, d), (n, d)
+
+
 def test_library_fails_loudly_without_a_gpu(ck):
     import torch
     if torch.cuda.is_available():
