@@ -132,14 +132,23 @@ __global__ void __launch_bounds__(kThreads, 4) k_attention(const AttnParams p) {
         k4[u] = tl < n ? *reinterpret_cast<const int4*>(Kh + (size_t)(t0 + tl) * hd + e0) : make_int4(0, 0, 0, 0);
       }
     }
+    // the kUnroll positions' products, then their sums over the position's lanes level by
+    // level, all positions at once (independent shuffles in flight together)
+    unsigned long long dd[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      dd[u] = (unsigned long long)q0 * (unsigned long long)(long long)k4[u].x +
+              (unsigned long long)q1 * (unsigned long long)(long long)k4[u].y +
+              (unsigned long long)q2 * (unsigned long long)(long long)k4[u].z +
+              (unsigned long long)q3 * (unsigned long long)(long long)k4[u].w;
+    for (uint32_t o = lpp >> 1; o > 0; o >>= 1) {
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) dd[u] += __shfl_xor_sync(0xffffffffu, dd[u], o);
+    }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const uint32_t tl = base + u * kWarps * ppw + slot;
-      unsigned long long d = (unsigned long long)q0 * (unsigned long long)(long long)k4[u].x +
-          (unsigned long long)q1 * (unsigned long long)(long long)k4[u].y +
-          (unsigned long long)q2 * (unsigned long long)(long long)k4[u].z +
-          (unsigned long long)q3 * (unsigned long long)(long long)k4[u].w;
-      for (uint32_t o = lpp >> 1; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+      const unsigned long long d = dd[u];
       if (tl < n && sub == 0) {
         long long s = (long long)d >> 16;
         s = (long long)((unsigned long long)s * (unsigned long long)p.inv_sqrt) >> 24;
@@ -262,18 +271,352 @@ size_t attn_smem(uint32_t hd, uint32_t chunk_cap) {
   return attn_vpre_offset(hd, chunk_cap) + (size_t)kUnroll * kThreads * 16;
 }
 
-}  // namespace
+// ------------------------------------------------------------------ long caches
+// k_attention_long: the same four stages for caches whose chunks span many batches.  A copy
+// warp streams the CTA's chunk of key rows, then of value rows, through a ring of
+// shared-memory slots by bulk copies (a chunk of one head is one contiguous run: the cache is
+// head-major), batch by batch, as soon as the consumers free a slot, so each SM has the ring's
+// bytes in flight instead of the loads its threads can hold.  A batch is kLBatch bytes:
+// 4096 / hd positions, kUnroll warp steps of the eight consumer warps.  Only the batch holding
+// the newest row (written by the kernel just before) waits for that kernel; older rows stream
+// at once.  The copy warp joins the two cluster exchanges between the keys and the values.
+#ifndef CK_LSLOTS
+#define CK_LSLOTS 8
+#endif
+#ifndef CK_LCLUSTER
+#define CK_LCLUSTER 4
+#endif
+#ifndef CK_LLATE
+#define CK_LLATE 1
+#endif
+constexpr uint32_t kLBatch = 16384;
+constexpr uint32_t kLSlots = CK_LSLOTS;
+constexpr int kLCluster = CK_LCLUSTER;  // CTAs a head: few enough that every cluster is resident at once
+constexpr int kLThreads = kThreads + 32;
+constexpr uint32_t kLPoll = 1u << 22;
 
-cudaError_t configure_attention() {
-  return cudaFuncSetAttribute(k_attention, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+__device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void lbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void lbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void lbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
+}
+__device__ __forceinline__ bool lbar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(saddr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void lbulk(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(saddr(dst)),
+      "l"(src), "r"(bytes), "r"(saddr(bar))
+      : "memory");
 }
 
-cudaError_t launch_attention(const AttnParams& p, cudaStream_t s, int cluster) {
-  const size_t smem = attn_smem(p.head_dim, p.chunk_cap);
-  if (smem > 96 * 1024) return cudaErrorInvalidValue;
+// Shared memory of the long kernel: the ring, then the per-CTA region as k_attention lays it
+// out (queries, partials, maximum, sum, reduction slots, scores), then the ring's barriers
+// and the failure flag.
+__host__ __device__ inline size_t lattn_region(uint32_t hd, uint32_t chunk_cap) {
+  return 8 * ((size_t)hd * (2 + kWarps) + 2 + kWarps + chunk_cap);
+}
+__host__ __device__ inline size_t lattn_bars(uint32_t hd, uint32_t chunk_cap) {
+  return ((size_t)kLSlots * kLBatch + lattn_region(hd, chunk_cap) + 15) & ~(size_t)15;
+}
+__host__ __device__ inline size_t lattn_smem(uint32_t hd, uint32_t chunk_cap) {
+  return lattn_bars(hd, chunk_cap) + 2 * kLSlots * 8 + 16;
+}
+
+// A wait of the long kernel that ran out: the state is failed with error 9; the caller goes
+// on without waiting, so that every thread reaches the same barriers.
+__device__ __forceinline__ void lattn_fail(const AttnParams& p, volatile uint32_t* flag) {
+  *flag = 1u;
+  hdr<uint32_t>(p.state, kHError) = CK_CUDA_ERROR;
+  hdr<uint32_t>(p.state, kHPhase) = CK_PHASE_FAILED;
+}
+
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+__global__ void __launch_bounds__(kLThreads, 2) k_attention_long(const AttnParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  cg::cluster_group cluster = cg::this_cluster();
+  const uint32_t hd = p.head_dim;
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint8_t* ring = smem;
+  int64_t* q_s = reinterpret_cast<int64_t*>(smem + (size_t)kLSlots * kLBatch);
+  unsigned long long* part = reinterpret_cast<unsigned long long*>(q_s + hd);  // [kWarps][hd]
+  unsigned long long* cpart = part + kWarps * hd;                               // [hd]
+  long long* cmax = reinterpret_cast<long long*>(cpart + hd);                   // [1]
+  unsigned long long* csum = reinterpret_cast<unsigned long long*>(cmax + 1);   // [1]
+  long long* red = reinterpret_cast<long long*>(csum + 1);                      // [kWarps]
+  long long* sc = red + kWarps;                                                 // [chunk_cap]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + lattn_bars(hd, p.chunk_cap));
+  uint64_t* empty = full + kLSlots;
+  volatile uint32_t* flag = reinterpret_cast<volatile uint32_t*>(empty + kLSlots);
+
+  const uint32_t pos = hdr_ld<uint32_t>(p.state, kHPosition);
+  const uint32_t P = pos + 1;
+  const uint32_t older = min(pos, p.cache);  // rows below this were written at earlier positions
+  const uint32_t h = blockIdx.x;
+  const uint32_t rank = cluster.block_rank(), CL = cluster.num_blocks();
+  const uint32_t kvh = h / (p.heads / p.kv_heads);  // "head h reads key/value head h/(heads/kvHeads)"
+  const uint32_t cs = (P + CL - 1) / CL;
+  const uint32_t t0 = min(P, rank * cs), t1 = min(P, t0 + cs);
+  const uint32_t n = t1 - t0;
+  const int32_t* Kh = p.kcache + (size_t)kvh * p.cache * hd;
+  const int32_t* Vh = p.vcache + (size_t)kvh * p.cache * hd;
+  const uint32_t bp = kLBatch / (hd * 4);  // positions of a batch
+  const uint32_t nb = (n + bp - 1) / bp;   // batches of keys (and of values)
+
+  if (tid == 0) {
+    for (uint32_t i = 0; i < kLSlots; ++i) {
+      lbar_init(&full[i], 1);
+      lbar_init(&empty[i], kWarps);
+    }
+    *flag = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == kWarps) {
+    // the copy warp: key batches, then value batches, into slot g % kLSlots for the g-th batch
+    if (!CK_LLATE) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    uint32_t g = 0;
+    bool waited = false, halt = false;
+    auto issue = [&](const int32_t* base, uint32_t b) {
+      const uint32_t slot = g % kLSlots;
+      if (g >= kLSlots) {
+        const uint32_t par = ((g / kLSlots) - 1) & 1u;
+        uint32_t i = 0;
+        while (!lbar_try(&empty[slot], par)) {
+          if (*flag || ++i > kLPoll) {
+            if (!*flag) lattn_fail(p, flag);
+            halt = true;
+            return;
+          }
+        }
+      }
+      const uint32_t r0 = b * bp, rows = min(bp, n - r0);
+      if (!waited && t0 + r0 + rows > older) {  // the newest row: written by the kernel just before
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        waited = true;
+      }
+      lbar_expect_tx(&full[slot], rows * hd * 4);
+      lbulk(ring + (size_t)slot * kLBatch, base + (size_t)(t0 + r0) * hd, rows * hd * 4, &full[slot]);
+      ++g;
+    };
+    if (lane == 0) {
+      for (uint32_t b = 0; b < nb && !halt; ++b) issue(Kh, b);
+      for (uint32_t b = 0; b < min(nb, kLSlots) && !halt; ++b) issue(Vh, b);  // slots the last keys free
+    }
+    __syncwarp();
+    cluster.sync();  // the consumers' exchange of maxima
+    cluster.sync();  // and of sums
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    if (lane == 0) {
+      for (uint32_t b = min(nb, kLSlots); b < nb && !halt; ++b) issue(Vh, b);
+      // no copy outlives the CTA: the last kLSlots batches started have landed
+      for (uint32_t j = g > kLSlots ? g - kLSlots : 0; j < g; ++j)
+        for (uint32_t i = 0; i < kLPoll; ++i)
+          if (lbar_try(&full[j % kLSlots], (j / kLSlots) & 1u)) break;
+    }
+    __syncwarp();
+    if (CK_LLATE) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    return;
+  }
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (!CK_LLATE) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const bool running = hdr_ld<uint32_t>(p.state, kHPhase) == CK_PHASE_RUNNING;
+  for (uint32_t i = tid; i < hd; i += kThreads) q_s[i] = p.q[(size_t)h * hd + i];
+  consumers_sync();
+  const uint32_t lpp = hd / 4, ppw = 32 / lpp;
+  const uint32_t sub = lane % lpp, pslot = lane / lpp, e0 = sub * 4;
+  const int64_t q0 = q_s[e0], q1 = q_s[e0 + 1], q2 = q_s[e0 + 2], q3 = q_s[e0 + 3];
+  bool dead = false;
+  // a batch's slot, once its copies have landed (bounded; on a timeout the state fails)
+  auto await = [&](uint32_t g) {
+    if (dead) return;
+    for (uint32_t i = 0; i < kLPoll; ++i) {
+      if (lbar_try(&full[g % kLSlots], (g / kLSlots) & 1u)) return;
+      if ((i & 63) == 63 && *flag) break;
+    }
+    if (!*flag) lattn_fail(p, flag);
+    dead = true;
+  };
+
+  // stage 0: s_t = (((q . k_t) >> 16) * inv) >> 24, products and sums wrapping; keep the max
+  long long lmax = LLONG_MIN;
+  for (uint32_t b = 0; b < nb; ++b) {
+    await(b);
+    const int32_t* Kb = reinterpret_cast<const int32_t*>(ring + (size_t)(b % kLSlots) * kLBatch);
+    unsigned long long dd[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t tb = (u * kWarps + warp) * ppw + pslot, tl = b * bp + tb;
+      const int4 k = !dead && tl < n ? *reinterpret_cast<const int4*>(Kb + (size_t)tb * hd + e0) : make_int4(0, 0, 0, 0);
+      dd[u] = (unsigned long long)q0 * (unsigned long long)(long long)k.x +
+              (unsigned long long)q1 * (unsigned long long)(long long)k.y +
+              (unsigned long long)q2 * (unsigned long long)(long long)k.z +
+              (unsigned long long)q3 * (unsigned long long)(long long)k.w;
+    }
+    for (uint32_t o = lpp >> 1; o > 0; o >>= 1) {  // all positions' lane sums at once
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) dd[u] += __shfl_xor_sync(0xffffffffu, dd[u], o);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t tb = (u * kWarps + warp) * ppw + pslot, tl = b * bp + tb;
+      const unsigned long long d = dd[u];
+      if (tl < n && sub == 0) {
+        long long sv = (long long)d >> 16;
+        sv = (long long)((unsigned long long)sv * (unsigned long long)p.inv_sqrt) >> 24;
+        sc[tl] = sv;
+        lmax = sv > lmax ? sv : lmax;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) lbar_arrive(&empty[b % kLSlots]);
+  }
+  lmax = warp_max(lmax);
+  if (lane == 0) red[warp] = lmax;
+  consumers_sync();
+  if (tid == 0) {
+    long long m = red[0];
+    for (int w = 1; w < kWarps; ++w) m = red[w] > m ? red[w] : m;
+    *cmax = m;
+  }
+  cluster.sync();
+  long long m = LLONG_MIN;
+  for (uint32_t r = 0; r < CL; ++r) {
+    const long long v = *cluster.map_shared_rank(cmax, r);
+    m = v > m ? v : m;
+  }
+
+  // stage 1: e_t = EXP[min((m - s_t) >> 8, 4096)]; the exact difference is >= 0 and fits u64
+  unsigned long long z = 0;
+  for (uint32_t tl = tid; tl < n; tl += kThreads) {
+    unsigned long long idx = ((unsigned long long)m - (unsigned long long)sc[tl]) >> 8;
+    if (idx > 4096) idx = 4096;
+    const unsigned long long e = __ldg(p.exp_tab + idx);
+    sc[tl] = (long long)e;
+    z += e;
+  }
+  z = warp_sum(z);
+  if (lane == 0) red[warp] = (long long)z;
+  consumers_sync();
+  if (tid == 0) {
+    unsigned long long t = 0;
+    for (int w = 0; w < kWarps; ++w) t += (unsigned long long)red[w];
+    *csum = t;
+  }
+  cluster.sync();
+  unsigned long long Z = 0;
+  for (uint32_t r = 0; r < CL; ++r) Z += *cluster.map_shared_rank(csum, r);
+  // the peers' maxima and sums are read: arrive now, wait before leaving
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+
+  // stage 2: P_t = (e_t << 24) / Z, 24 fractional bits
+  for (uint32_t tl = tid; tl < n; tl += kThreads)
+    sc[tl] = (long long)(((unsigned long long)sc[tl] << 24) / Z);
+  consumers_sync();
+
+  // stage 3: sum over positions of P_t * v_t[j] (exact: |sum| < 2^55), then one >> 24
+  unsigned long long a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+  for (uint32_t b = 0; b < nb; ++b) {
+    const uint32_t g = nb + b;
+    await(g);
+    const int32_t* Vb = reinterpret_cast<const int32_t*>(ring + (size_t)(g % kLSlots) * kLBatch);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t tb = (u * kWarps + warp) * ppw + pslot, tl = b * bp + tb;
+      if (!dead && tl < n) {
+        const int4 v = *reinterpret_cast<const int4*>(Vb + (size_t)tb * hd + e0);
+        const long long pr = sc[tl];
+        a0 += (unsigned long long)(pr * (long long)v.x);
+        a1 += (unsigned long long)(pr * (long long)v.y);
+        a2 += (unsigned long long)(pr * (long long)v.z);
+        a3 += (unsigned long long)(pr * (long long)v.w);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) lbar_arrive(&empty[g % kLSlots]);
+  }
+  for (uint32_t o = 16; o >= lpp && o > 0; o >>= 1) {
+    a0 += __shfl_xor_sync(0xffffffffu, a0, o);
+    a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+    a2 += __shfl_xor_sync(0xffffffffu, a2, o);
+    a3 += __shfl_xor_sync(0xffffffffu, a3, o);
+  }
+  if (pslot == 0) {
+    unsigned long long* dst = part + (size_t)warp * hd + e0;
+    dst[0] = a0;
+    dst[1] = a1;
+    dst[2] = a2;
+    dst[3] = a3;
+  }
+  consumers_sync();
+  // the next kernel's CTAs may start once this one's are finishing: launched earlier they
+  // would hold SMs that clusters of this grid still wait for
+  if (CK_LLATE) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the CTA's partial sums go straight into the head's accumulators (wrapping adds, so the
+  // order of the CTAs changes no bit); the next kernel applies the >> 24
+  if (running && *flag == 0u) {
+    for (uint32_t j = tid; j < hd; j += kThreads) {
+      unsigned long long sum = 0;
+      for (int w = 0; w < kWarps; ++w) sum += part[(size_t)w * hd + j];
+      atomicAdd(p.o_acc + (size_t)h * hd + j, sum);
+    }
+  }
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+}  // namespace
+
+int g_lattn_smem = 0;  // the opt-in shared memory of this device
+
+cudaError_t configure_attention() {
+  cudaError_t e = cudaFuncSetAttribute(k_attention, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+  int dev = 0, optin = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attention_long, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (e == cudaSuccess) g_lattn_smem = optin;
+  return e;
+}
+
+#ifndef CK_LONG_BATCHES
+#define CK_LONG_BATCHES 2
+#endif
+// The long-cache kernel takes heads whose chunks (over kLCluster CTAs) span more than this
+// many batches, when the accumulator path is on and its shared memory fits.
+uint32_t long_chunk(const AttnParams& p) { return (p.cache + kLCluster - 1) / kLCluster; }
+bool attention_long(const AttnParams& p) {
+  const uint32_t bp = kLBatch / (p.head_dim * 4);
+  return p.o_acc && long_chunk(p) > CK_LONG_BATCHES * bp &&
+         lattn_smem(p.head_dim, long_chunk(p)) <= (size_t)g_lattn_smem;
+}
+
+cudaError_t launch_attention(const AttnParams& p_in, cudaStream_t s, int cluster) {
+  const bool lng = attention_long(p_in);
+  AttnParams p = p_in;
+  if (lng) {
+    cluster = kLCluster;
+    p.chunk_cap = long_chunk(p_in);
+  }
+  const size_t smem = lng ? lattn_smem(p.head_dim, p.chunk_cap) : attn_smem(p.head_dim, p.chunk_cap);
+  if (!lng && smem > 96 * 1024) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.heads, (unsigned)cluster, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(lng ? kLThreads : kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -285,7 +628,7 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t s, int cluster) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_attention, p);
+  return lng ? cudaLaunchKernelEx(&cfg, k_attention_long, p) : cudaLaunchKernelEx(&cfg, k_attention, p);
 }
 
 }  // namespace ck
