@@ -277,7 +277,7 @@ size_t attn_smem(uint32_t hd, uint32_t chunk_cap) {
 // shared-memory slots by bulk copies (a chunk of one head is one contiguous run: the cache is
 // head-major), batch by batch, as soon as the consumers free a slot, so each SM has the ring's
 // bytes in flight instead of the loads its threads can hold.  A batch is kLBatch bytes:
-// 4096 / hd positions, kUnroll warp steps of the eight consumer warps.  Only the batch holding
+// 4096 / hd positions, kLUnroll warp steps of the sixteen consumer warps.  Only the batch holding
 // the newest row (written by the kernel just before) waits for that kernel; older rows stream
 // at once.  The copy warp joins the two cluster exchanges between the keys and the values.
 #ifndef CK_LSLOTS
@@ -292,7 +292,10 @@ size_t attn_smem(uint32_t hd, uint32_t chunk_cap) {
 constexpr uint32_t kLBatch = 16384;
 constexpr uint32_t kLSlots = CK_LSLOTS;
 constexpr int kLCluster = CK_LCLUSTER;  // CTAs a head: few enough that every cluster is resident at once
-constexpr int kLThreads = kThreads + 32;
+constexpr int kLWarps = 16;                    // consumer warps
+constexpr int kLUnroll = 2;                    // warp steps of a batch
+constexpr int kLCons = kLWarps * 32;           // consumer threads
+constexpr int kLThreads = kLCons + 32;         // + the copy warp
 constexpr uint32_t kLPoll = 1u << 22;
 
 __device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -325,7 +328,7 @@ __device__ __forceinline__ void lbulk(void* dst, const void* src, uint32_t bytes
 // out (queries, partials, maximum, sum, reduction slots, scores), then the ring's barriers
 // and the failure flag.
 __host__ __device__ inline size_t lattn_region(uint32_t hd, uint32_t chunk_cap) {
-  return 8 * ((size_t)hd * (2 + kWarps) + 2 + kWarps + chunk_cap);
+  return 8 * ((size_t)hd * (2 + kLWarps) + 2 + kLWarps + chunk_cap);
 }
 __host__ __device__ inline size_t lattn_bars(uint32_t hd, uint32_t chunk_cap) {
   return ((size_t)kLSlots * kLBatch + lattn_region(hd, chunk_cap) + 15) & ~(size_t)15;
@@ -342,21 +345,21 @@ __device__ __forceinline__ void lattn_fail(const AttnParams& p, volatile uint32_
   hdr<uint32_t>(p.state, kHPhase) = CK_PHASE_FAILED;
 }
 
-__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kLCons) : "memory"); }
 
-__global__ void __launch_bounds__(kLThreads, 2) k_attention_long(const AttnParams p) {
+__global__ void __launch_bounds__(kLThreads, 1) k_attention_long(const AttnParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   cg::cluster_group cluster = cg::this_cluster();
   const uint32_t hd = p.head_dim;
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint8_t* ring = smem;
   int64_t* q_s = reinterpret_cast<int64_t*>(smem + (size_t)kLSlots * kLBatch);
-  unsigned long long* part = reinterpret_cast<unsigned long long*>(q_s + hd);  // [kWarps][hd]
-  unsigned long long* cpart = part + kWarps * hd;                               // [hd]
+  unsigned long long* part = reinterpret_cast<unsigned long long*>(q_s + hd);  // [kLWarps][hd]
+  unsigned long long* cpart = part + kLWarps * hd;                               // [hd]
   long long* cmax = reinterpret_cast<long long*>(cpart + hd);                   // [1]
   unsigned long long* csum = reinterpret_cast<unsigned long long*>(cmax + 1);   // [1]
-  long long* red = reinterpret_cast<long long*>(csum + 1);                      // [kWarps]
-  long long* sc = red + kWarps;                                                 // [chunk_cap]
+  long long* red = reinterpret_cast<long long*>(csum + 1);                      // [kLWarps]
+  long long* sc = red + kLWarps;                                                 // [chunk_cap]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lattn_bars(hd, p.chunk_cap));
   uint64_t* empty = full + kLSlots;
   volatile uint32_t* flag = reinterpret_cast<volatile uint32_t*>(empty + kLSlots);
@@ -378,14 +381,14 @@ __global__ void __launch_bounds__(kLThreads, 2) k_attention_long(const AttnParam
   if (tid == 0) {
     for (uint32_t i = 0; i < kLSlots; ++i) {
       lbar_init(&full[i], 1);
-      lbar_init(&empty[i], kWarps);
+      lbar_init(&empty[i], kLWarps);
     }
     *flag = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
-  if (warp == kWarps) {
+  if (warp == kLWarps) {
     // the copy warp: key batches, then value batches, into slot g % kLSlots for the g-th batch
     if (!CK_LLATE) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     uint32_t g = 0;
@@ -436,7 +439,7 @@ __global__ void __launch_bounds__(kLThreads, 2) k_attention_long(const AttnParam
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (!CK_LLATE) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const bool running = hdr_ld<uint32_t>(p.state, kHPhase) == CK_PHASE_RUNNING;
-  for (uint32_t i = tid; i < hd; i += kThreads) q_s[i] = p.q[(size_t)h * hd + i];
+  for (uint32_t i = tid; i < hd; i += kLCons) q_s[i] = p.q[(size_t)h * hd + i];
   consumers_sync();
   const uint32_t lpp = hd / 4, ppw = 32 / lpp;
   const uint32_t sub = lane % lpp, pslot = lane / lpp, e0 = sub * 4;
@@ -458,10 +461,10 @@ __global__ void __launch_bounds__(kLThreads, 2) k_attention_long(const AttnParam
   for (uint32_t b = 0; b < nb; ++b) {
     await(b);
     const int32_t* Kb = reinterpret_cast<const int32_t*>(ring + (size_t)(b % kLSlots) * kLBatch);
-    unsigned long long dd[kUnroll];
+    unsigned long long dd[kLUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const uint32_t tb = (u * kWarps + warp) * ppw + pslot, tl = b * bp + tb;
+    for (int u = 0; u < kLUnroll; ++u) {
+      const uint32_t tb = (u * kLWarps + warp) * ppw + pslot, tl = b * bp + tb;
       const int4 k = !dead && tl < n ? *reinterpret_cast<const int4*>(Kb + (size_t)tb * hd + e0) : make_int4(0, 0, 0, 0);
       dd[u] = (unsigned long long)q0 * (unsigned long long)(long long)k.x +
               (unsigned long long)q1 * (unsigned long long)(long long)k.y +
@@ -470,11 +473,11 @@ __global__ void __launch_bounds__(kLThreads, 2) k_attention_long(const AttnParam
     }
     for (uint32_t o = lpp >> 1; o > 0; o >>= 1) {  // all positions' lane sums at once
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) dd[u] += __shfl_xor_sync(0xffffffffu, dd[u], o);
+      for (int u = 0; u < kLUnroll; ++u) dd[u] += __shfl_xor_sync(0xffffffffu, dd[u], o);
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const uint32_t tb = (u * kWarps + warp) * ppw + pslot, tl = b * bp + tb;
+    for (int u = 0; u < kLUnroll; ++u) {
+      const uint32_t tb = (u * kLWarps + warp) * ppw + pslot, tl = b * bp + tb;
       const unsigned long long d = dd[u];
       if (tl < n && sub == 0) {
         long long sv = (long long)d >> 16;
@@ -491,7 +494,7 @@ __global__ void __launch_bounds__(kLThreads, 2) k_attention_long(const AttnParam
   consumers_sync();
   if (tid == 0) {
     long long m = red[0];
-    for (int w = 1; w < kWarps; ++w) m = red[w] > m ? red[w] : m;
+    for (int w = 1; w < kLWarps; ++w) m = red[w] > m ? red[w] : m;
     *cmax = m;
   }
   cluster.sync();
@@ -503,7 +506,7 @@ __global__ void __launch_bounds__(kLThreads, 2) k_attention_long(const AttnParam
 
   // stage 1: e_t = EXP[min((m - s_t) >> 8, 4096)]; the exact difference is >= 0 and fits u64
   unsigned long long z = 0;
-  for (uint32_t tl = tid; tl < n; tl += kThreads) {
+  for (uint32_t tl = tid; tl < n; tl += kLCons) {
     unsigned long long idx = ((unsigned long long)m - (unsigned long long)sc[tl]) >> 8;
     if (idx > 4096) idx = 4096;
     const unsigned long long e = __ldg(p.exp_tab + idx);
@@ -515,7 +518,7 @@ __global__ void __launch_bounds__(kLThreads, 2) k_attention_long(const AttnParam
   consumers_sync();
   if (tid == 0) {
     unsigned long long t = 0;
-    for (int w = 0; w < kWarps; ++w) t += (unsigned long long)red[w];
+    for (int w = 0; w < kLWarps; ++w) t += (unsigned long long)red[w];
     *csum = t;
   }
   cluster.sync();
@@ -525,7 +528,7 @@ __global__ void __launch_bounds__(kLThreads, 2) k_attention_long(const AttnParam
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 
   // stage 2: P_t = (e_t << 24) / Z, 24 fractional bits
-  for (uint32_t tl = tid; tl < n; tl += kThreads)
+  for (uint32_t tl = tid; tl < n; tl += kLCons)
     sc[tl] = (long long)(((unsigned long long)sc[tl] << 24) / Z);
   consumers_sync();
 
@@ -536,8 +539,8 @@ __global__ void __launch_bounds__(kLThreads, 2) k_attention_long(const AttnParam
     await(g);
     const int32_t* Vb = reinterpret_cast<const int32_t*>(ring + (size_t)(g % kLSlots) * kLBatch);
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const uint32_t tb = (u * kWarps + warp) * ppw + pslot, tl = b * bp + tb;
+    for (int u = 0; u < kLUnroll; ++u) {
+      const uint32_t tb = (u * kLWarps + warp) * ppw + pslot, tl = b * bp + tb;
       if (!dead && tl < n) {
         const int4 v = *reinterpret_cast<const int4*>(Vb + (size_t)tb * hd + e0);
         const long long pr = sc[tl];
@@ -570,9 +573,9 @@ __global__ void __launch_bounds__(kLThreads, 2) k_attention_long(const AttnParam
   // the CTA's partial sums go straight into the head's accumulators (wrapping adds, so the
   // order of the CTAs changes no bit); the next kernel applies the >> 24
   if (running && *flag == 0u) {
-    for (uint32_t j = tid; j < hd; j += kThreads) {
+    for (uint32_t j = tid; j < hd; j += kLCons) {
       unsigned long long sum = 0;
-      for (int w = 0; w < kWarps; ++w) sum += part[(size_t)w * hd + j];
+      for (int w = 0; w < kLWarps; ++w) sum += part[(size_t)w * hd + j];
       atomicAdd(p.o_acc + (size_t)h * hd + j, sum);
     }
   }
