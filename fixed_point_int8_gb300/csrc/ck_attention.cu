@@ -276,12 +276,14 @@ size_t attn_smem(uint32_t hd, uint32_t chunk_cap) {
 // warp streams the CTA's chunk of key rows, then of value rows, through a ring of
 // shared-memory slots by bulk copies (a chunk of one head is one contiguous run: the cache is
 // head-major), batch by batch, as soon as the consumers free a slot, so each SM has the ring's
-// bytes in flight instead of the loads its threads can hold.  A batch is kLBatch bytes:
-// 4096 / hd positions, kLUnroll warp steps of the sixteen consumer warps.  Only the batch holding
+// bytes in flight instead of the loads its threads can hold.  A batch is kLBatch bytes: 8192 /
+// hd positions.  Scoring gives each lane NC chunks of 16 bytes of a key row (16 elements for
+// heads of 16 or more), so a position's lane sums take few shuffle levels; the weighted sum of
+// values gives each lane 4 elements (it needs no per-position sums).  Only the batch holding
 // the newest row (written by the kernel just before) waits for that kernel; older rows stream
 // at once.  The copy warp joins the two cluster exchanges between the keys and the values.
 #ifndef CK_LSLOTS
-#define CK_LSLOTS 8
+#define CK_LSLOTS 4
 #endif
 #ifndef CK_LCLUSTER
 #define CK_LCLUSTER 4
@@ -289,11 +291,11 @@ size_t attn_smem(uint32_t hd, uint32_t chunk_cap) {
 #ifndef CK_LLATE
 #define CK_LLATE 1
 #endif
-constexpr uint32_t kLBatch = 16384;
+constexpr uint32_t kLBatch = 32768;
 constexpr uint32_t kLSlots = CK_LSLOTS;
 constexpr int kLCluster = CK_LCLUSTER;  // CTAs a head: few enough that every cluster is resident at once
 constexpr int kLWarps = 16;                    // consumer warps
-constexpr int kLUnroll = 2;                    // warp steps of a batch
+constexpr int kLUnroll = 4;                    // warp steps of a value batch
 constexpr int kLCons = kLWarps * 32;           // consumer threads
 constexpr int kLThreads = kLCons + 32;         // + the copy warp
 constexpr uint32_t kLPoll = 1u << 22;
@@ -347,6 +349,7 @@ __device__ __forceinline__ void lattn_fail(const AttnParams& p, volatile uint32_
 
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kLCons) : "memory"); }
 
+template <int NC>
 __global__ void __launch_bounds__(kLThreads, 1) k_attention_long(const AttnParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   cg::cluster_group cluster = cg::this_cluster();
@@ -375,7 +378,8 @@ __global__ void __launch_bounds__(kLThreads, 1) k_attention_long(const AttnParam
   const uint32_t n = t1 - t0;
   const int32_t* Kh = p.kcache + (size_t)kvh * p.cache * hd;
   const int32_t* Vh = p.vcache + (size_t)kvh * p.cache * hd;
-  const uint32_t bp = kLBatch / (hd * 4);  // positions of a batch
+  const uint32_t bp = kLBatch / (hd * 4);  // positions of a batch: SK warp steps of the keys,
+                                           // kLUnroll of the values
   const uint32_t nb = (n + bp - 1) / bp;   // batches of keys (and of values)
 
   if (tid == 0) {
@@ -441,9 +445,22 @@ __global__ void __launch_bounds__(kLThreads, 1) k_attention_long(const AttnParam
   const bool running = hdr_ld<uint32_t>(p.state, kHPhase) == CK_PHASE_RUNNING;
   for (uint32_t i = tid; i < hd; i += kLCons) q_s[i] = p.q[(size_t)h * hd + i];
   consumers_sync();
+  // scoring: lane chunks j = 0..NC-1 of its 4 NC elements at rotated places, so that eight
+  // consecutive lanes read eight different bank groups; the queries are permuted alike
+  constexpr uint32_t E = 4 * NC, SH = NC == 4 ? 1 : NC == 2 ? 2 : 3, SK = 4 / NC;
+  const uint32_t lppk = hd / E, ppwk = 32 / lppk;
+  const uint32_t subk = lane % lppk, pslk = lane / lppk;
+  uint32_t koff[NC];
+  int64_t qp[NC][4];
+#pragma unroll
+  for (uint32_t j = 0; j < NC; ++j) {
+    koff[j] = subk * E + 4 * ((j + (lane >> SH)) % NC);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) qp[j][e] = q_s[koff[j] + e];
+  }
+  // weighted values: four elements a lane
   const uint32_t lpp = hd / 4, ppw = 32 / lpp;
   const uint32_t sub = lane % lpp, pslot = lane / lpp, e0 = sub * 4;
-  const int64_t q0 = q_s[e0], q1 = q_s[e0 + 1], q2 = q_s[e0 + 2], q3 = q_s[e0 + 3];
   bool dead = false;
   // a batch's slot, once its copies have landed (bounded; on a timeout the state fails)
   auto await = [&](uint32_t g) {
@@ -461,25 +478,31 @@ __global__ void __launch_bounds__(kLThreads, 1) k_attention_long(const AttnParam
   for (uint32_t b = 0; b < nb; ++b) {
     await(b);
     const int32_t* Kb = reinterpret_cast<const int32_t*>(ring + (size_t)(b % kLSlots) * kLBatch);
-    unsigned long long dd[kLUnroll];
+    unsigned long long dd[SK];
 #pragma unroll
-    for (int u = 0; u < kLUnroll; ++u) {
-      const uint32_t tb = (u * kLWarps + warp) * ppw + pslot, tl = b * bp + tb;
-      const int4 k = !dead && tl < n ? *reinterpret_cast<const int4*>(Kb + (size_t)tb * hd + e0) : make_int4(0, 0, 0, 0);
-      dd[u] = (unsigned long long)q0 * (unsigned long long)(long long)k.x +
-              (unsigned long long)q1 * (unsigned long long)(long long)k.y +
-              (unsigned long long)q2 * (unsigned long long)(long long)k.z +
-              (unsigned long long)q3 * (unsigned long long)(long long)k.w;
+    for (uint32_t u = 0; u < SK; ++u) {
+      const uint32_t tb = (u * kLWarps + warp) * ppwk + pslk, tl = b * bp + tb;
+      unsigned long long a = 0;
+#pragma unroll
+      for (uint32_t j = 0; j < NC; ++j) {
+        const int4 k = !dead && tl < n ? *reinterpret_cast<const int4*>(Kb + (size_t)tb * hd + koff[j])
+                                       : make_int4(0, 0, 0, 0);
+        a += (unsigned long long)qp[j][0] * (unsigned long long)(long long)k.x +
+             (unsigned long long)qp[j][1] * (unsigned long long)(long long)k.y +
+             (unsigned long long)qp[j][2] * (unsigned long long)(long long)k.z +
+             (unsigned long long)qp[j][3] * (unsigned long long)(long long)k.w;
+      }
+      dd[u] = a;
     }
-    for (uint32_t o = lpp >> 1; o > 0; o >>= 1) {  // all positions' lane sums at once
+    for (uint32_t o = lppk >> 1; o > 0; o >>= 1) {  // all positions' lane sums at once
 #pragma unroll
-      for (int u = 0; u < kLUnroll; ++u) dd[u] += __shfl_xor_sync(0xffffffffu, dd[u], o);
+      for (uint32_t u = 0; u < SK; ++u) dd[u] += __shfl_xor_sync(0xffffffffu, dd[u], o);
     }
 #pragma unroll
-    for (int u = 0; u < kLUnroll; ++u) {
-      const uint32_t tb = (u * kLWarps + warp) * ppw + pslot, tl = b * bp + tb;
+    for (uint32_t u = 0; u < SK; ++u) {
+      const uint32_t tb = (u * kLWarps + warp) * ppwk + pslk, tl = b * bp + tb;
       const unsigned long long d = dd[u];
-      if (tl < n && sub == 0) {
+      if (tl < n && subk == 0) {
         long long sv = (long long)d >> 16;
         sv = (long long)((unsigned long long)sv * (unsigned long long)p.inv_sqrt) >> 24;
         sc[tl] = sv;
@@ -591,7 +614,9 @@ cudaError_t configure_attention() {
   int dev = 0, optin = 0;
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attention_long, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attention_long<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attention_long<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attention_long<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
   if (e == cudaSuccess) g_lattn_smem = optin;
   return e;
 }
@@ -631,7 +656,10 @@ cudaError_t launch_attention(const AttnParams& p_in, cudaStream_t s, int cluster
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return lng ? cudaLaunchKernelEx(&cfg, k_attention_long, p) : cudaLaunchKernelEx(&cfg, k_attention, p);
+  if (!lng) return cudaLaunchKernelEx(&cfg, k_attention, p);
+  if (p.head_dim >= 16) return cudaLaunchKernelEx(&cfg, k_attention_long<4>, p);
+  if (p.head_dim == 8) return cudaLaunchKernelEx(&cfg, k_attention_long<2>, p);
+  return cudaLaunchKernelEx(&cfg, k_attention_long<1>, p);
 }
 
 }  // namespace ck
