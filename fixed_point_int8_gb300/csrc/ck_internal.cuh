@@ -80,19 +80,44 @@ __host__ __device__ inline uint64_t mulhi_u64(uint64_t a, uint64_t b) {
 #endif
 }
 
-// floor(sqrt(v)) for any u64: a single-precision estimate, one Newton step on the exact
-// integer residual, then exact integer corrections (no double precision: it is slow here).
+// Single-precision approximations of 1/x and 1/sqrt(x) (a few units in the last place; the
+// hardware's approximate instructions on the device).  The integer routines below only use
+// them as estimates and correct every result exactly.
+__host__ __device__ inline float rcp_estimate(float x) {
+#ifdef __CUDA_ARCH__
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+#else
+  return 1.0f / x;
+#endif
+}
+__host__ __device__ inline float rsqrt_estimate(float x) {
+#ifdef __CUDA_ARCH__
+  float r;
+  asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+#else
+  return 1.0f / sqrtf(x);
+#endif
+}
+
+// floor(sqrt(v)) for any u64: an estimate r = v / sqrt(v) in single precision (within about
+// 2^-21 of the root, so within 2^11 of it), one Newton step on the exact residual v - r^2
+// (a 64-bit value that fits: |v - r^2| < 2^44), then exact integer corrections.  A short
+// dependent chain: it sits on the normalization's critical path.
 __host__ __device__ inline uint64_t isqrt_u64(uint64_t v) {
-  uint64_t r = (uint64_t)sqrtf((float)v);
+  if (v == 0) return 0;
+  const float fv = (float)v, y = rsqrt_estimate(fv);
+  float fr = fv * y;
+  if (fr > 4294967295.0f) fr = 4294967295.0f;
+  uint64_t r = (uint64_t)fr;
   if (r > 0xFFFFFFFFull) r = 0xFFFFFFFFull;
-  if (r > 0) {
-    const int64_t e = (int64_t)(v - r * r);  // |e| < 2^62: r is within 2^-11 of the root
-    const int64_t step = (int64_t)((float)e / (2.0f * (float)r));
-    int64_t t = (int64_t)r + step;
-    if (t < 0) t = 0;
-    if (t > 0xFFFFFFFFll) t = 0xFFFFFFFFll;
-    r = (uint64_t)t;
-  }
+  const int64_t e = (int64_t)(v - r * r);
+  int64_t t = (int64_t)r + (int64_t)((float)e * (0.5f * y));
+  if (t < 0) t = 0;
+  if (t > 0xFFFFFFFFll) t = 0xFFFFFFFFll;
+  r = (uint64_t)t;
   while (r * r > v) --r;
   while (r < 0xFFFFFFFFull && (r + 1) * (r + 1) <= v) ++r;
   return r;
@@ -129,7 +154,7 @@ __host__ __device__ inline InvDiv make_invdiv(uint32_t d) {
 // values are far inside the signed range).  Two of these build the reciprocal below in a few
 // dozen operations instead of two 64-bit divisions.
 __host__ __device__ inline uint64_t div_small_quotient(uint64_t n, uint32_t d) {
-  const float rcp = 1.0f / (float)d;
+  const float rcp = rcp_estimate((float)d);
   uint64_t q = (uint64_t)((float)n * rcp);      // within about 2^10 of the quotient
   if (q > 0xFFFFFFFFull) q = 0xFFFFFFFFull;
   int64_t r = (int64_t)(n - q * d);             // |r| < 2^43
