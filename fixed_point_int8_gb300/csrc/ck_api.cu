@@ -430,6 +430,15 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
   const uint32_t oacc_word = (nslots + 31) & ~31u;
   const bool use_oacc = 8ull * ((uint64_t)oacc_word + c.dim) <= lay.k - lay.scores;
   unsigned long long* oacc = use_oacc ? ss + oacc_word : nullptr;
+  // after them, where the region holds it: the SiLU outputs as byte planes with the gate/up
+  // CTAs' partial sums and ORs, written by the gate/up epilogue for the down kernel's prologue
+  const uint32_t gu_grid = std::min<uint32_t>(c.hidden, (uint32_t)m->num_sms);
+  const uint64_t off_hplanes = align256(8ull * ((uint64_t)oacc_word + c.dim));
+  const uint64_t off_hparts = align256(off_hplanes + 8ull * m->pitch_h);
+  const bool use_hplanes = use_oacc && off_hparts + 16ull * gu_grid <= lay.k - lay.scores;
+  uint8_t* hplanes = use_hplanes ? st + lay.scores + off_hplanes : nullptr;
+  unsigned long long* hparts =
+      use_hplanes ? reinterpret_cast<unsigned long long*>(st + lay.scores + off_hparts) : nullptr;
   k_embed<<<(c.dim + 255) / 256, 256, 0, s>>>(st, lay.prompt, lay.out, x, m->embed, m->embed_scale,
                                               m->pitch_d, c.dim, c.vocab, ss,
                                               use_oacc ? oacc_word + c.dim : nslots);
@@ -516,6 +525,9 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
     pg.silu_tab = m->silu_tab;
     pg.acc_clear = oacc;
     pg.acc_words = c.dim;
+    pg.planes_out = hplanes;
+    pg.planes_pitch = m->pitch_h;
+    pg.parts_out = hparts;
     pg.state = st;
     CK_CUDA(launch_matrow(pg, s, m->num_sms));
     // phases 15-16: down rows, residual (and its squares for the next norm)
@@ -529,6 +541,9 @@ int enqueue_position(const ck_model* m, uint8_t* st, const StateLayout& lay, boo
     pd.cols = c.hidden;
     pd.pro = kProPlain;
     pd.in = hbuf;
+    pd.in_planes = hplanes;  // when set: the planes and partials replace reading hbuf
+    pd.parts_in = hparts;
+    pd.nparts = gu_grid;
     pd.epi = kEpiStore;
     pd.out = y;
     pd.resid_in = cur;

@@ -298,6 +298,12 @@ struct MatrowParams {
   // outputs before their shift); block 0 writes the shifted vector to in_out
   const unsigned long long* in_acc;
   int64_t* in_out;
+  // plain, instead of `in`: the vector already as eight byte planes (plane k at k * pitch)
+  // with per-CTA partial {wrapping sum, OR of |x|} pairs [nparts][2] of the kernel that
+  // wrote them; the prologue copies only the planes the vector needs
+  const uint8_t* in_planes;
+  const unsigned long long* parts_in;
+  uint32_t nparts;
   const int64_t* add;    // norm: residual addend (nullptr: none)
   int64_t* res_out;      // norm with addend: where block 0 writes in + add
   const int32_t* norm_w;
@@ -311,6 +317,11 @@ struct MatrowParams {
   // epilogue
   int epi;
   int64_t* out;          // store: y[rows]; QKV: rotated queries [q_rows]; SiLU: h[rows / 2]
+  // SiLU, besides `out`: h as eight byte planes (plane k at k * planes_pitch) and this
+  // CTA's {wrapping sum, OR of |h|} at parts_out[2 * blockIdx.x], for the next kernel
+  uint8_t* planes_out;
+  uint32_t planes_pitch;
+  unsigned long long* parts_out;
   // store with a residual (the page's phases 11 and 16 moved into the producing kernel):
   // resid_out[r] = resid_in[r] + y[r], and the squares of resid_out added into *ss_out
   const int64_t* resid_in;

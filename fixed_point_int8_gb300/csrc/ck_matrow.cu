@@ -44,8 +44,13 @@ struct Scratch {
 __device__ __forceinline__ void wait_prior_grids() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// 8-byte asynchronous copy from global to shared memory, and the wait for all of this
-// thread's copies.
+// 16- and 8-byte asynchronous copies from global to shared memory, and the wait for all of
+// this thread's copies.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
 __device__ __forceinline__ void cp_async8(void* dst, const void* src) {
   const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(src) : "memory");
@@ -140,6 +145,29 @@ __device__ int prologue(const MatrowParams& p, uint32_t* planes32, Scratch* sc,
   const bool norm = p.pro == kProNorm;
   const bool held = words <= (uint32_t)kPG * kThreads;  // one batch: values stay in registers
   int64_t xv[kPG][4];
+  if (!norm && p.in_planes) {
+    // the producer wrote the planes: copy the first four into shared memory while the
+    // partial sums and ORs are added up, then the rest if the vector needs more limbs
+    const uint32_t pbytes = p.pitch;  // bytes of one plane
+    for (uint32_t k = 0; k < 4; ++k)
+      for (uint32_t o = 16 * threadIdx.x; o < pbytes; o += 16 * kThreads)
+        cp_async16(reinterpret_cast<uint8_t*>(planes32) + (size_t)k * pbytes + o, p.in_planes + (size_t)k * pbytes + o);
+    unsigned long long S = 0, orv = 0;
+    for (uint32_t i = threadIdx.x; i < p.nparts; i += kThreads) {
+      S += p.parts_in[2 * i];
+      orv |= p.parts_in[2 * i + 1];
+    }
+    block_sum_or(S, orv, sc);
+    int L = 1;
+    while (L < 8 && (orv >> (8 * L - 1)) != 0) ++L;
+    for (uint32_t k = 4; k < (uint32_t)L; ++k)
+      for (uint32_t o = 16 * threadIdx.x; o < pbytes; o += 16 * kThreads)
+        cp_async16(reinterpret_cast<uint8_t*>(planes32) + (size_t)k * pbytes + o, p.in_planes + (size_t)k * pbytes + o);
+    cp_async_wait_all();
+    __syncthreads();
+    *S_out = S;
+    return L;
+  }
   if (norm && p.ss_in) {
     // the producer added up the squares: the values load while thread 0 forms the RMS
     // reciprocal, then one pass normalises and packs
@@ -416,6 +444,7 @@ __device__ void rows_loop(const MatrowParams& p, const uint8_t* planes, Scratch*
   constexpr int H = L <= 4 ? kG / 2 : kG / 4;  // rows accumulated at once (register budget)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t pitch = p.pitch, ns = (pitch + kSlice - 1) / kSlice;
+  unsigned long long hs = 0, ho = 0;  // the CTA's SiLU outputs: wrapping sum, OR of |h|
   for (uint32_t c0 = rb; c0 < re; c0 += kChunkRows) {
     const uint32_t c1 = min(c0 + kChunkRows, re);
     const uint32_t items = (c1 - c0 + kG - 1) / kG * ns;
@@ -456,6 +485,15 @@ __device__ void rows_loop(const MatrowParams& p, const uint8_t* planes, Scratch*
       const int64_t partner =
           fprow < c1 ? (int64_t)((sc->tot[t ^ 1u] - (S << 7)) * (unsigned long long)fpscale) >> 24 : 0;
       epilogue(p, frow, y, partner, pos);
+      if (p.planes_out && (frow & 1u) == 0) {
+        // the SiLU output h_j (as the epilogue stored it) as byte planes for the next kernel
+        const int64_t hv = wmul(silu_lookup(y, p.silu_tab), partner) >> 16;
+        const uint32_t j = frow >> 1;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) p.planes_out[(size_t)k * p.planes_pitch + j] = (uint8_t)((uint64_t)hv >> (8 * k));
+        hs += (unsigned long long)hv;
+        ho |= (unsigned long long)(hv ^ (hv >> 63));
+      }
       if (p.resid_out) {
         // the residual (phases 11 and 16) and its square for the next normalization
         const int64_t xr = wadd(sc->res[t], y);
@@ -470,6 +508,13 @@ __device__ void rows_loop(const MatrowParams& p, const uint8_t* planes, Scratch*
     __syncthreads();
     for (uint32_t t = threadIdx.x; t < kChunkRows; t += kThreads) sc->tot[t] = 0;
     __syncthreads();
+  }
+  if (p.planes_out) {
+    block_sum_or(hs, ho, sc);
+    if (threadIdx.x == 0) {
+      p.parts_out[2 * blockIdx.x] = hs;
+      p.parts_out[2 * blockIdx.x + 1] = ho;
+    }
   }
 }
 
