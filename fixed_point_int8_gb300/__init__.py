@@ -84,6 +84,7 @@ def lib() -> ctypes.CDLL:
             "ck_matrow": ([vp, sz, vp, u32, u32, vp, vp, vp], ctypes.c_int),
             "ck_host_isqrt": ([u64], u64),
             "ck_host_div_trunc": ([i64, u32], i64),
+            "ck_host_probability": ([u64, u64], u64),
             "ck_version": ([], ctypes.c_char_p),
         }
         for name, (args, res) in sig.items():
@@ -337,6 +338,11 @@ def host_isqrt(v: int) -> int:
 
 def host_div_trunc(n: int, d: int) -> int:
     return int(lib().ck_host_div_trunc(n, d))
+
+
+def host_probability(e: int, z: int) -> int:
+    """Host build of the attention kernels' floor((e << 24) / z)."""
+    return int(lib().ck_host_probability(e, z))
 
 
 def version() -> str:

@@ -779,6 +779,11 @@ const char* ck_version(void) { return "libck 0.1 (sm_103a)"; }
 
 uint64_t ck_host_isqrt(uint64_t v) { return isqrt_u64(v); }
 
+uint64_t ck_host_probability(uint64_t e, uint64_t z) {
+  if (z == 0) return 0;
+  return div_by_estimate(e << 24, z, rcp_estimate((float)z));
+}
+
 int64_t ck_host_div_trunc(int64_t n, uint32_t d) {
   if (d == 0) return 0;
   return sdiv_trunc(n, make_invdiv_fast(d));

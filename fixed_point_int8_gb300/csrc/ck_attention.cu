@@ -198,8 +198,9 @@ __global__ void __launch_bounds__(kThreads, 4) k_attention(const AttnParams p) {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 
   // stage 2: P_t = (e_t << 24) / Z, 24 fractional bits
+  const float rz = rcp_estimate((float)Z);  // Z >= 2^30: the largest score's entry is 2^30
   for (uint32_t tl = tid; tl < n; tl += kThreads)
-    sc[tl] = (long long)(((unsigned long long)sc[tl] << 24) / Z);
+    sc[tl] = (long long)div_by_estimate((unsigned long long)sc[tl] << 24, Z, rz);
   __syncthreads();
 
   // stage 3: sum over positions of P_t * v_t[j] (exact: |sum| < 2^55), then one >> 24
@@ -551,8 +552,9 @@ __global__ void __launch_bounds__(kLThreads, 1) k_attention_long(const AttnParam
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 
   // stage 2: P_t = (e_t << 24) / Z, 24 fractional bits
+  const float rz = rcp_estimate((float)Z);  // Z >= 2^30: the largest score's entry is 2^30
   for (uint32_t tl = tid; tl < n; tl += kLCons)
-    sc[tl] = (long long)(((unsigned long long)sc[tl] << 24) / Z);
+    sc[tl] = (long long)div_by_estimate((unsigned long long)sc[tl] << 24, Z, rz);
   consumers_sync();
 
   // stage 3: sum over positions of P_t * v_t[j] (exact: |sum| < 2^55), then one >> 24

@@ -165,6 +165,21 @@ __host__ __device__ inline uint64_t div_small_quotient(uint64_t n, uint32_t d) {
   return q;
 }
 
+// floor(num / z) for 1 <= z and a quotient below 2^32 (the probabilities: num = e << 24 with
+// e <= z), from rz, an estimate of 1 / z: two estimated steps on exact remainders, then exact
+// corrections.  The remainders are taken modulo 2^64 and read as signed; they stay far inside
+// that range while num < 2^62.
+__host__ __device__ inline uint64_t div_by_estimate(uint64_t num, uint64_t z, float rz) {
+  uint64_t q = (uint64_t)((float)num * rz);
+  if (q > 0xFFFFFFFFull) q = 0xFFFFFFFFull;
+  int64_t r = (int64_t)(num - q * z);
+  q = (uint64_t)((int64_t)q + (int64_t)floorf((float)r * rz));
+  r = (int64_t)(num - q * z);
+  while (r < 0) { --q; r += (int64_t)z; }
+  while (r >= (int64_t)z) { ++q; r -= (int64_t)z; }
+  return q;
+}
+
 // make_invdiv with the two 64-by-32 steps done by div_small_quotient and l = ceil(log2 d)
 // from a count of leading zeros.
 __host__ __device__ inline InvDiv make_invdiv_fast(uint32_t d) {

@@ -340,11 +340,15 @@ int ck_matrow(const uint8_t* dev_W, size_t pitch, const uint32_t* dev_scale, uin
               uint32_t cols, const int64_t* dev_x, int64_t* dev_y, void* stream);
 
 /* ---------------------------------------------------------------- host-side checks
- * Host builds of two device routines, for tests without a GPU: floor square root of a u64,
+ * Host builds of device routines, for tests without a GPU: floor square root of a u64,
  * and truncating signed division of n by d (1 <= d < 2^32) through the precomputed
  * reciprocal the normalization kernels use. */
 uint64_t ck_host_isqrt(uint64_t v);
 int64_t ck_host_div_trunc(int64_t n, uint32_t d);
+/* A third host build: the attention probability floor((e << 24) / z) ("Attention, stage by
+ * stage", stage 2) as the attention kernels form it from an estimate of 1 / z, for an
+ * exponential 0 <= e <= min(z, 2^30) and a sum 2^30 <= z < 2^46. */
+uint64_t ck_host_probability(uint64_t e, uint64_t z);
 
 /* Library version string. */
 const char* ck_version(void);

@@ -87,6 +87,23 @@ def test_host_division_reciprocal_for_every_small_divisor_and_near_powers_of_two
             assert ck.host_div_trunc(n, d) == _trunc_div(n, d), (n, d)
 
 
+def test_host_probability_from_a_reciprocal_estimate(ck):
+    """The attention probability floor((e << 24) / z) as the kernels form it: sums from one
+    table entry (2^30) to 2^46 - 1, exponentials (table entries, at most 2^30 and at most the
+    sum) from 0 up, at the quotient boundaries."""
+    rng = np.random.default_rng(23)
+    sums = [2**30, 2**30 + 1, 2**31 - 1, 2**31, 3 * 2**30 + 7, 2**40 - 1, 2**43, 2**46 - 1]
+    sums += [int(v) for v in rng.integers(2**30, 2**46, 300, dtype=np.uint64)]
+    for z in sums:
+        top = min(z, 2**30)  # an exponential is one table entry, at most 2^30
+        es = [0, 1, top, top - 1] + [int(v) for v in rng.integers(0, top + 1, 20)]
+        for k in (1, 2, 3, 1000):  # just below and at multiples of z / 2^24
+            q = k * z >> 24
+            es += [e for e in ((q * z + 2**24 - 1) >> 24, (q * z) >> 24) if 0 <= e <= min(z, 2**30)]
+        for e in es:
+            assert ck.host_probability(e, z) == (e << 24) // z, (e, z)
+
+
 def test_library_fails_loudly_without_a_gpu(ck):
     import torch
     if torch.cuda.is_available():
