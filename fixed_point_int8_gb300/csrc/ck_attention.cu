@@ -284,7 +284,7 @@ size_t attn_smem(uint32_t hd, uint32_t chunk_cap) {
 // the newest row (written by the kernel just before) waits for that kernel; older rows stream
 // at once.  The copy warp joins the two cluster exchanges between the keys and the values.
 #ifndef CK_LSLOTS
-#define CK_LSLOTS 4
+#define CK_LSLOTS 5
 #endif
 #ifndef CK_LCLUSTER
 #define CK_LCLUSTER 4
