@@ -77,7 +77,7 @@ __device__ __forceinline__ unsigned long long bwarp_or(unsigned long long v) {
   return v;
 }
 
-// Block-wide sum (every thread gets it); red holds kRowThreads / 32 words.
+// Block-wide sum (every thread gets it); red holds blockDim.x / 32 words.
 __device__ unsigned long long block_sum(unsigned long long v, unsigned long long* red) {
   v = bwarp_sum(v);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
@@ -126,11 +126,13 @@ __global__ void __launch_bounds__(kRowThreads) k_bembed(const uint8_t* gate, con
 
 // "RMS normalization" of each position's row (one block each): rms = max(isqrt(sum x^2 / d
 // + 42,950), 1), y = ((x * w) / rms) >> 8 with the division truncating; ORs the outputs'
-// magnitudes into *orw for the plane count.
-__global__ void __launch_bounds__(kRowThreads) k_bnorm(const uint8_t* gate, const int64_t* X,
-                                                        int64_t* XB, const int32_t* w, uint32_t d,
-                                                        unsigned long long* orw) {
-  __shared__ unsigned long long red[kRowThreads / 32];
+// magnitudes into *orw for the plane count.  A block of kNormThreads: a row's loads go out
+// at once (the kernel is a chain of dependent steps over a few rows).
+constexpr int kNormThreads = 1024;
+__global__ void __launch_bounds__(kNormThreads) k_bnorm(const uint8_t* gate, const int64_t* X,
+                                                         int64_t* XB, const int32_t* w, uint32_t d,
+                                                         unsigned long long* orw) {
+  __shared__ unsigned long long red[kNormThreads / 32];
   __shared__ InvDiv div;
   pdl_enter();
   if (!running(gate)) return;
@@ -1077,7 +1079,7 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
     const DevLayer& Wl = m.layers[l];
     unsigned long long* o4 = orw + 4 * l;
     // phases 4-8: attention norm, Q/K/V rows, checked cache stores, rotary
-    launch_pdl(k_bnorm, dim3(P), dim3(kRowThreads), 0, s, gate, (const int64_t*)X, XB, Wl.attn_norm, c.dim, o4 + 0);
+    launch_pdl(k_bnorm, dim3(P), dim3(kNormThreads), 0, s, gate, (const int64_t*)X, XB, Wl.attn_norm, c.dim, o4 + 0);
     planes(XB, c.dim, c.dim, KGd, o4 + 0, c.dim + 2 * m.kv_dim, KGd);
     gemm(Wl.wqkv, c.dim + 2 * m.kv_dim, KGd, o4 + 0);
     BEpiParams pq = {};
@@ -1119,7 +1121,7 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
     po.X = X;
     epi(po);
     // phases 12-14: feed-forward norm, gate and up rows, SiLU gating
-    launch_pdl(k_bnorm, dim3(P), dim3(kRowThreads), 0, s, gate, (const int64_t*)X, XB, Wl.ffn_norm, c.dim, o4 + 2);
+    launch_pdl(k_bnorm, dim3(P), dim3(kNormThreads), 0, s, gate, (const int64_t*)X, XB, Wl.ffn_norm, c.dim, o4 + 2);
     planes(XB, c.dim, c.dim, KGd, o4 + 2, 2 * c.hidden, KGd);
     gemm(Wl.w13, 2 * c.hidden, KGd, o4 + 2);
     BEpiParams pg = {};
@@ -1146,7 +1148,7 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
   if (classify) {
     // phases 17-18: final norm and classifier rows (written only for generating rows)
     unsigned long long* of = orw + 4 * c.layers;
-    launch_pdl(k_bnorm, dim3(P), dim3(kRowThreads), 0, s, gate, (const int64_t*)X, XB, m.final_norm, c.dim, of);
+    launch_pdl(k_bnorm, dim3(P), dim3(kNormThreads), 0, s, gate, (const int64_t*)X, XB, m.final_norm, c.dim, of);
     planes(XB, c.dim, c.dim, KGd, of, c.vocab, KGd);
     gemm(m.cls, c.vocab, KGd, of);
     BEpiParams pc = {};
