@@ -2,8 +2,9 @@
 
 Workload: the 7B-shaped fixed-point model (dim 4096, 32 layers, 32 heads x 128, FFN hidden
 11008, vocab 32000, context 2048, ~6.6 GB of int8 weights), seeded synthetic weights, a
-single run: 128 prompt ids prefilled position by position, then greedy decode.  A step is
-one generating position: phases 3 to 19 over all 32 layers and the classifier.
+single run: 128 prompt ids (the 127 that generate nothing prefilled layer-major), then
+greedy decode.  A step is one generating position: phases 3 to 19 over all 32 layers and
+the classifier.
 
 Prints one JSON line:
   value      decode tokens/s, device-timed (CUDA events on the launching stream) over
@@ -14,7 +15,8 @@ Prints one JSON line:
              of one layer, 22016 x 4096), timed live with CUDA events, against the measured
              HBM copy bandwidth;
   cpu_baseline  the CPU oracle on a bounded sample of the same decode (it continues from
-             the GPU's state after the prefill), whose tokens must equal the GPU's;
+             the GPU's state after the prefill and the first token, never past the run's
+             last token), whose tokens must equal the GPU's (bitexact);
   matrow_sweep  GB/s of the matrix-row kernel on the four sweep shapes;
   prefill    the 127 prompt positions of the workload, layer-major (device-timed);
   batched_runs  the 1B-shaped model with 64 independent runs (64 prompt ids each, prefilled
@@ -22,7 +24,7 @@ Prints one JSON line:
              pass, device-timed over --batched-passes passes;
   long_context  the 1B-shaped model at 8,192 context: 7,936 prompt ids prefilled layer-major,
              then --long-steps generating positions (~position 7,940), device-timed.
-``--impl reference`` times the CPU oracle alone on the same workload and metric.
+``--impl reference`` times the CPU oracle alone on the same workload, prompt and positions.
 """
 from __future__ import annotations
 
