@@ -37,10 +37,11 @@ __device__ __forceinline__ unsigned long long warp_sum(unsigned long long v) {
   return v;
 }
 
-// Shared memory: queries, per-warp and per-CTA partials, maximum, sum, reduction slots, the
-// chunk's scores, then (16-byte aligned) the first batch of value rows.
+// Shared memory: queries, per-warp and per-CTA partials, the cluster's chunk maxima and sums
+// (slot r written by rank r), reduction slots, the chunk's scores, then (16-byte aligned) the
+// first batch of value rows.
 __host__ __device__ inline size_t attn_vpre_offset(uint32_t hd, uint32_t chunk_cap) {
-  return (8 * ((size_t)hd * (2 + kWarps) + 2 + kWarps + chunk_cap) + 15) & ~(size_t)15;
+  return (8 * ((size_t)hd * (2 + kWarps) + 16 + kWarps + chunk_cap) + 15) & ~(size_t)15;
 }
 
 // 16-byte asynchronous copy from global to shared memory (zeros and no read when not valid),
@@ -67,11 +68,14 @@ __global__ void __launch_bounds__(kThreads, 4) k_attention(const AttnParams p) {
   int64_t* q_s = reinterpret_cast<int64_t*>(smem);
   unsigned long long* part = reinterpret_cast<unsigned long long*>(q_s + hd);  // [kWarps][hd]
   unsigned long long* cpart = part + kWarps * hd;                               // [hd]
-  long long* cmax = reinterpret_cast<long long*>(cpart + hd);                   // [1]
-  unsigned long long* csum = reinterpret_cast<unsigned long long*>(cmax + 1);   // [1]
-  long long* red = reinterpret_cast<long long*>(csum + 1);                      // [kWarps]
+  long long* cmax = reinterpret_cast<long long*>(cpart + hd);                   // [8]
+  unsigned long long* csum = reinterpret_cast<unsigned long long*>(cmax + 8);   // [8]
+  long long* red = reinterpret_cast<long long*>(csum + 8);                      // [kWarps]
   long long* sc = red + kWarps;                                                 // [chunk_cap]
   int4* vpre = reinterpret_cast<int4*>(smem + attn_vpre_offset(hd, p.chunk_cap));  // [kUnroll][kThreads]
+  // every CTA of the cluster has started before any writes into a peer's shared memory: the
+  // arrival here, the wait just before the first such write
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
   // Launched with programmatic dependent launch.  Before the wait this kernel reads only what
   // was written before the previous kernel started: the position (set by the previous
@@ -160,17 +164,17 @@ __global__ void __launch_bounds__(kThreads, 4) k_attention(const AttnParams p) {
   lmax = warp_max(lmax);
   if (lane == 0) red[warp] = lmax;
   __syncthreads();
-  if (tid == 0) {
-    long long m = red[0];
-    for (int w = 1; w < kWarps; ++w) m = red[w] > m ? red[w] : m;
-    *cmax = m;
+  // the CTA's maximum goes into slot `rank` of every peer (thread r writes peer r), so that
+  // after the cluster barrier each CTA reads the maxima from its own shared memory
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  if (tid < CL) {
+    long long mm = red[0];
+    for (int w = 1; w < kWarps; ++w) mm = red[w] > mm ? red[w] : mm;
+    *cluster.map_shared_rank(cmax + rank, tid) = mm;
   }
   cluster.sync();
   long long m = LLONG_MIN;
-  for (uint32_t r = 0; r < CL; ++r) {
-    const long long v = *cluster.map_shared_rank(cmax, r);
-    m = v > m ? v : m;
-  }
+  for (uint32_t r = 0; r < CL; ++r) m = cmax[r] > m ? cmax[r] : m;
 
   // stage 1: e_t = EXP[min((m - s_t) >> 8, 4096)]; the exact difference is >= 0 and fits u64
   unsigned long long z = 0;
@@ -184,18 +188,16 @@ __global__ void __launch_bounds__(kThreads, 4) k_attention(const AttnParams p) {
   z = warp_sum(z);
   if (lane == 0) red[warp] = (long long)z;
   __syncthreads();
-  if (tid == 0) {
+  if (tid < CL) {
     unsigned long long t = 0;
     for (int w = 0; w < kWarps; ++w) t += (unsigned long long)red[w];
-    *csum = t;
+    *cluster.map_shared_rank(csum + rank, tid) = t;
   }
+  // after this barrier no CTA touches a peer's shared memory again (except in the exchange of
+  // partial sums below, which has barriers of its own)
   cluster.sync();
   unsigned long long Z = 0;
-  for (uint32_t r = 0; r < CL; ++r) Z += *cluster.map_shared_rank(csum, r);
-  // this CTA has read its peers' maxima and sums: it arrives on the cluster barrier now and
-  // waits on it only before it leaves (or exchanges again), so no CTA's shared memory goes
-  // while a peer may still read it
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  for (uint32_t r = 0; r < CL; ++r) Z += csum[r];
 
   // stage 2: P_t = (e_t << 24) / Z, 24 fractional bits
   const float rz = rcp_estimate((float)Z);  // Z >= 2^30: the largest score's entry is 2^30
@@ -248,7 +250,6 @@ __global__ void __launch_bounds__(kThreads, 4) k_attention(const AttnParams p) {
       for (int w = 0; w < kWarps; ++w) s += part[(size_t)w * hd + j];
       atomicAdd(p.o_acc + (size_t)h * hd + j, s);
     }
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     return;
   }
   for (uint32_t j = tid; j < hd; j += kThreads) {
@@ -256,7 +257,6 @@ __global__ void __launch_bounds__(kThreads, 4) k_attention(const AttnParams p) {
     for (int w = 0; w < kWarps; ++w) s += part[(size_t)w * hd + j];
     cpart[j] = s;
   }
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   cluster.sync();
   if (rank == 0) {
     for (uint32_t j = tid; j < hd; j += kThreads) {
