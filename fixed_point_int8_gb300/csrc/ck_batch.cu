@@ -631,40 +631,29 @@ struct BAttnParams {
 
 constexpr int kAttnWarps = kRowThreads / 32;
 
-size_t battn_smem(uint32_t hd, uint32_t positions) {
-  return 8 * ((size_t)hd * (1 + kAttnWarps) + kAttnWarps + positions);
-}
-
 constexpr int kAttnBatch = 8;  // positions a lane group loads at once
 
-// Division of a u64 by an invariant divisor 1 <= d < 2^64 (Granlund and Montgomery,
-// "Division by Invariant Integers using Multiplication", PLDI 1994, unsigned case with
-// N = 64): l = ceil(log2 d), m = floor(2^64 (2^l - d) / d) + 1,
-// q = (t + ((n - t) >> min(l, 1))) >> max(l - 1, 0) with t = mulhi(m, n).
-struct InvDiv64 {
-  unsigned long long m;
-  uint32_t sh1, sh2;
-};
-__device__ InvDiv64 make_invdiv64(unsigned long long d) {
-  uint32_t l = 0;
-  while (l < 64 && (l == 64 ? false : (1ull << l) < d)) ++l;
-  const unsigned __int128 two_l = (unsigned __int128)1 << l;
-  const unsigned __int128 num = (two_l - d) << 64;
-  InvDiv64 D;
-  D.m = (unsigned long long)(num / d) + 1;
-  D.sh1 = l < 1 ? l : 1;
-  D.sh2 = l > 0 ? l - 1 : 0;
-  return D;
+// Shared memory: the first round of value rows (each thread's kAttnBatch 16-byte chunks,
+// copied when the kernel starts), then queries, per-warp partials, reduction slots and the
+// row's scores.
+constexpr size_t kAttnVpre = (size_t)kAttnBatch * kRowThreads * 16;
+size_t battn_smem(uint32_t hd, uint32_t positions) {
+  return kAttnVpre + 8 * ((size_t)hd * (1 + kAttnWarps) + kAttnWarps + positions);
 }
-__device__ __forceinline__ unsigned long long udiv64(unsigned long long n, const InvDiv64& D) {
-  const unsigned long long t = __umul64hi(D.m, n);
-  return (t + ((n - t) >> D.sh1)) >> D.sh2;
+
+__device__ __forceinline__ void battn_cp16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n\tcp.async.commit_group;" ::"r"(smem_addr(dst)),
+               "l"(src)
+               : "memory");
 }
 
 // Phase 9 for row blockIdx.y and head blockIdx.x ("Attention, stage by stage"), over its
 // run's cache positions 0 .. pos: scores and their maximum, exponentials and their sum,
 // probabilities with 24 fraction bits, and the weighted values with one >> 24.  Each lane
-// group loads kAttnBatch positions a round.  When every query element fits 32 signed bits,
+// group loads kAttnBatch positions a round; the first round's values are copied into shared
+// memory together with its keys, so that they have arrived when the probabilities are known.
+// The probabilities (e << 24) / Z come from a single-precision estimate of 1 / Z and exact
+// corrections (e <= Z, Z below 2^46).  When every query element fits 32 signed bits,
 // each product q * k is exact in one 32 x 32 -> 64-bit multiply-add (the same low 64 bits
 // as the wrapping product), and so is every P * v (P <= 2^24).
 __global__ void __launch_bounds__(kRowThreads) k_battn(const BAttnParams p) {
@@ -675,11 +664,25 @@ __global__ void __launch_bounds__(kRowThreads) k_battn(const BAttnParams p) {
   const RowDesc rd = p.rdesc[n];
   const uint32_t np = rd.pos + 1;
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int64_t* q_s = reinterpret_cast<int64_t*>(smem);
+  int4* vpre = reinterpret_cast<int4*>(smem);                                  // [kAttnBatch][threads]
+  int64_t* q_s = reinterpret_cast<int64_t*>(smem + kAttnVpre);
   unsigned long long* part = reinterpret_cast<unsigned long long*>(q_s + hd);  // [warps][hd]
   long long* red = reinterpret_cast<long long*>(part + (size_t)kAttnWarps * hd);
   long long* sc = red + kAttnWarps;                                            // [np]
   const uint32_t kvh = h / (p.heads / p.kv_heads);
+  const int32_t* Kh = layer_cache(rd, rd.off_k, p.layer, p.kv_dim) + (size_t)kvh * rd.cache * hd;
+  const int32_t* Vh = layer_cache(rd, rd.off_v, p.layer, p.kv_dim) + (size_t)kvh * rd.cache * hd;
+  const uint32_t lpp = hd / 4, ppw = 32 / lpp;  // lanes per position (four elements each)
+  const uint32_t sub = lane % lpp, slot = lane / lpp, e0 = sub * 4;
+  const uint32_t round = kAttnWarps * ppw * kAttnBatch;
+  // the first round: keys into registers, values into shared memory, before the queries
+  int4 k4[kAttnBatch];
+#pragma unroll
+  for (int bb = 0; bb < kAttnBatch; ++bb) {
+    const uint32_t tl = (bb * kAttnWarps + warp) * ppw + slot;
+    k4[bb] = tl < np ? *reinterpret_cast<const int4*>(Kh + (size_t)tl * hd + e0) : make_int4(0, 0, 0, 0);
+    if (tl < np) battn_cp16(vpre + bb * kRowThreads + tid, Vh + (size_t)tl * hd + e0);
+  }
   int wide = 0;
   for (uint32_t i = tid; i < hd; i += kRowThreads) {
     const int64_t v = p.Q[(size_t)n * p.dim + (size_t)h * hd + i];
@@ -687,21 +690,17 @@ __global__ void __launch_bounds__(kRowThreads) k_battn(const BAttnParams p) {
     wide |= ((v ^ (v >> 63)) >> 31) != 0;
   }
   const bool q32 = !__syncthreads_or(wide);
-  const int32_t* Kh = layer_cache(rd, rd.off_k, p.layer, p.kv_dim) + (size_t)kvh * rd.cache * hd;
-  const int32_t* Vh = layer_cache(rd, rd.off_v, p.layer, p.kv_dim) + (size_t)kvh * rd.cache * hd;
-  const uint32_t lpp = hd / 4, ppw = 32 / lpp;  // lanes per position (four elements each)
-  const uint32_t sub = lane % lpp, slot = lane / lpp, e0 = sub * 4;
   const int64_t q0 = q_s[e0], q1 = q_s[e0 + 1], q2 = q_s[e0 + 2], q3 = q_s[e0 + 3];
   const int32_t n0 = (int32_t)q0, n1 = (int32_t)q1, n2 = (int32_t)q2, n3 = (int32_t)q3;
-  const uint32_t round = kAttnWarps * ppw * kAttnBatch;
 
   long long lmax = LLONG_MIN;
   for (uint32_t base = 0; base < np; base += round) {
-    int4 k4[kAttnBatch];
+    if (base != 0) {
 #pragma unroll
-    for (int bb = 0; bb < kAttnBatch; ++bb) {
-      const uint32_t tl = base + (bb * kAttnWarps + warp) * ppw + slot;
-      k4[bb] = tl < np ? *reinterpret_cast<const int4*>(Kh + (size_t)tl * hd + e0) : make_int4(0, 0, 0, 0);
+      for (int bb = 0; bb < kAttnBatch; ++bb) {
+        const uint32_t tl = base + (bb * kAttnWarps + warp) * ppw + slot;
+        k4[bb] = tl < np ? *reinterpret_cast<const int4*>(Kh + (size_t)tl * hd + e0) : make_int4(0, 0, 0, 0);
+      }
     }
     unsigned long long d[kAttnBatch];
 #pragma unroll
@@ -754,13 +753,11 @@ __global__ void __launch_bounds__(kRowThreads) k_battn(const BAttnParams p) {
   __syncthreads();
   unsigned long long Z = 0;
   for (int w = 0; w < kAttnWarps; ++w) Z += (unsigned long long)red[w];
-  __shared__ InvDiv64 divz;
-  if (tid == 0) divz = make_invdiv64(Z);  // Z >= EXP[0] > 0: the largest score adds 2^30
-  __syncthreads();
-  const InvDiv64 DZ = divz;
+  const float rz = rcp_estimate((float)Z);  // Z >= 2^30: the largest score's entry is 2^30
   for (uint32_t tl = tid; tl < np; tl += kRowThreads)
-    sc[tl] = (long long)udiv64((unsigned long long)sc[tl] << 24, DZ);
+    sc[tl] = (long long)div_by_estimate((unsigned long long)sc[tl] << 24, Z, rz);
   __syncthreads();
+  asm volatile("cp.async.wait_group 0;" ::: "memory");  // this thread's first-round values
 
   unsigned long long a0 = 0, a1 = 0, a2 = 0, a3 = 0;
   for (uint32_t base = 0; base < np; base += round) {
@@ -769,7 +766,9 @@ __global__ void __launch_bounds__(kRowThreads) k_battn(const BAttnParams p) {
 #pragma unroll
     for (int bb = 0; bb < kAttnBatch; ++bb) {
       const uint32_t tl = base + (bb * kAttnWarps + warp) * ppw + slot;
-      v4[bb] = tl < np ? *reinterpret_cast<const int4*>(Vh + (size_t)tl * hd + e0) : make_int4(0, 0, 0, 0);
+      v4[bb] = tl >= np     ? make_int4(0, 0, 0, 0)
+               : base == 0 ? vpre[bb * kRowThreads + tid]
+                           : *reinterpret_cast<const int4*>(Vh + (size_t)tl * hd + e0);
       pb[bb] = tl < np ? (int32_t)sc[tl] : 0;  // P <= 2^24
     }
 #pragma unroll
