@@ -127,31 +127,58 @@ __global__ void __launch_bounds__(kRowThreads) k_bembed(const uint8_t* gate, con
 // "RMS normalization" of each position's row (one block each): rms = max(isqrt(sum x^2 / d
 // + 42,950), 1), y = ((x * w) / rms) >> 8 with the division truncating; ORs the outputs'
 // magnitudes into *orw for the plane count.  A block of kNormThreads: a row's loads go out
-// at once (the kernel is a chain of dependent steps over a few rows).
+// at once (the kernel is a chain of dependent steps over a few rows).  The first kNormPer
+// elements a thread stay in registers between the two passes, their norm weights are loaded
+// before the wait (model data), and both divisions by invariant divisors (d, then rms) use
+// reciprocals built from single-precision estimates with exact corrections.
 constexpr int kNormThreads = 1024;
+constexpr int kNormPer = 4;  // elements a thread keeps (rows up to 4,096)
 __global__ void __launch_bounds__(kNormThreads) k_bnorm(const uint8_t* gate, const int64_t* X,
                                                          int64_t* XB, const int32_t* w, uint32_t d,
                                                          unsigned long long* orw) {
   __shared__ unsigned long long red[kNormThreads / 32];
   __shared__ InvDiv div;
+  int32_t wv[kNormPer];
+#pragma unroll
+  for (int j = 0; j < kNormPer; ++j) {
+    const uint32_t i = threadIdx.x + j * kNormThreads;
+    wv[j] = i < d ? __ldg(w + i) : 0;
+  }
+  const InvDiv Dd = make_invdiv_fast(d);  // floor(ss / d) by a multiply
   pdl_enter();
   if (!running(gate)) return;
   const int64_t* x = X + (size_t)blockIdx.x * d;
   int64_t* y = XB + (size_t)blockIdx.x * d;
+  int64_t xv[kNormPer];
   unsigned long long ss = 0;
-  for (uint32_t i = threadIdx.x; i < d; i += blockDim.x)
+#pragma unroll
+  for (int j = 0; j < kNormPer; ++j) {
+    const uint32_t i = threadIdx.x + j * kNormThreads;
+    xv[j] = i < d ? x[i] : 0;
+    ss += (unsigned long long)xv[j] * (unsigned long long)xv[j];
+  }
+  for (uint32_t i = threadIdx.x + kNormPer * kNormThreads; i < d; i += kNormThreads)
     ss += (unsigned long long)x[i] * (unsigned long long)x[i];
   ss = block_sum(ss, red);
   if (threadIdx.x == 0) {
-    uint64_t rms = isqrt_u64(ss / d + 42950ull);
+    uint64_t rms = isqrt_u64(udiv_inv(ss, Dd) + 42950ull);
     if (rms < 1) rms = 1;
-    div = make_invdiv((uint32_t)rms);
+    div = make_invdiv_fast((uint32_t)rms);
   }
   __syncthreads();
   const InvDiv D = div;
   unsigned long long o = 0;
-  for (uint32_t i = threadIdx.x; i < d; i += blockDim.x) {
-    const int64_t v = sdiv_trunc(wmul(x[i], (int64_t)w[i]), D) >> 8;
+#pragma unroll
+  for (int j = 0; j < kNormPer; ++j) {
+    const uint32_t i = threadIdx.x + j * kNormThreads;
+    if (i < d) {
+      const int64_t v = sdiv_trunc(wmul(xv[j], (int64_t)wv[j]), D) >> 8;
+      y[i] = v;
+      o |= (unsigned long long)(v ^ (v >> 63));
+    }
+  }
+  for (uint32_t i = threadIdx.x + kNormPer * kNormThreads; i < d; i += kNormThreads) {
+    const int64_t v = sdiv_trunc(wmul(x[i], (int64_t)__ldg(w + i)), D) >> 8;
     y[i] = v;
     o |= (unsigned long long)(v ^ (v >> 63));
   }
@@ -172,9 +199,9 @@ __device__ __forceinline__ uint64_t plane_offset(uint32_t np, uint32_t KG, uint3
 }
 
 // Writes planes 0 .. L-1 of the P vectors V (row stride ld, cols used), zero beyond P and
-// cols.  One thread per 8 columns of one plane of one position.  With clear_rows > 0 it also
-// zeroes the next contraction's output S[n'][r] (n' < L * Npad, r < clear_rows), which a
-// contraction split over column ranges adds into.
+// cols.  One thread per 8 columns of one position: it loads the 8 values once and writes
+// their L planes.  With clear_rows > 0 it also zeroes the next contraction's output S[n'][r]
+// (n' < L * Npad, r < clear_rows), which a contraction split over column ranges adds into.
 __global__ void __launch_bounds__(kRowThreads) k_bplanes(const uint8_t* gate, const int64_t* V,
                                                           uint32_t ld, uint32_t P, uint32_t cols,
                                                           uint32_t Npad, uint32_t KG,
@@ -190,28 +217,30 @@ __global__ void __launch_bounds__(kRowThreads) k_bplanes(const uint8_t* gate, co
       S[q] = 0;
   }
   const uint32_t per_row = KG * 16;  // 8-column chunks of a row
-  const uint64_t total = (uint64_t)L * Npad * per_row;
-  for (uint64_t q = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; q < total;
-       q += (uint64_t)gridDim.x * blockDim.x) {
-    const uint32_t k = (uint32_t)(q / ((uint64_t)Npad * per_row));
-    const uint32_t rem = (uint32_t)(q % ((uint64_t)Npad * per_row));
-    const uint32_t n = rem / per_row, cc = rem % per_row;
+  const uint32_t total = Npad * per_row;
+  for (uint32_t q = blockIdx.x * blockDim.x + threadIdx.x; q < total; q += gridDim.x * blockDim.x) {
+    const uint32_t n = q / per_row, cc = q - n * per_row;
     const uint32_t kg = cc >> 4, ch = cc & 15u, c0 = kg * kBK + ch * 8;
-    uint32_t h[4];
+    int64_t xv[8];
 #pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-      int v2[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const uint32_t c = c0 + e + u;
-        const int64_t x = (n < P && c < cols) ? V[(size_t)n * ld + c] : 0;
-        v2[u] = (k + 1 < (uint32_t)L) ? (int)(((uint64_t)x >> (8 * k)) & 0xFFu)
-                                      : (int)(x >> (8 * k));  // top plane: signed
-      }
-      const __half2 hv = __halves2half2(__int2half_rn(v2[0]), __int2half_rn(v2[1]));
-      h[e >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t c = c0 + e;
+      xv[e] = (n < P && c < cols) ? V[(size_t)n * ld + c] : 0;
     }
-    *reinterpret_cast<uint4*>(B + plane_offset(k * Npad + n, KG, kg, ch)) = make_uint4(h[0], h[1], h[2], h[3]);
+    for (int k = 0; k < L; ++k) {
+      uint32_t h[4];
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        int v2[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+          v2[u] = (k + 1 < L) ? (int)(((uint64_t)xv[e + u] >> (8 * k)) & 0xFFu)
+                              : (int)(xv[e + u] >> (8 * k));  // top plane: signed
+        const __half2 hv = __halves2half2(__int2half_rn(v2[0]), __int2half_rn(v2[1]));
+        h[e >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
+      }
+      *reinterpret_cast<uint4*>(B + plane_offset(k * Npad + n, KG, kg, ch)) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
   }
 }
 
@@ -1053,9 +1082,11 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
   // the planes of a vector, clearing the output of the contraction that follows when it splits
   auto planes = [&](const int64_t* vec, uint32_t ld, uint32_t cols, uint32_t KG,
                     const unsigned long long* ow, uint32_t next_rows, uint32_t next_KG) {
-    const uint64_t work_items = 8ull * Npad * KG * 16;
-    const uint32_t blocks = (uint32_t)std::min<uint64_t>((work_items + kRowThreads - 1) / kRowThreads, 4096);
     const uint32_t clear = splits_for(next_rows, next_KG) > 1 ? next_rows : 0u;
+    // a thread per 8 columns of a position; at least a thread per 4 words of the clearing
+    // (sized for the usual three planes)
+    const uint64_t work_items = std::max<uint64_t>((uint64_t)Npad * KG * 16, 3ull * Npad * clear / 4);
+    const uint32_t blocks = (uint32_t)std::min<uint64_t>((work_items + kRowThreads - 1) / kRowThreads, 4096);
     launch_pdl(k_bplanes, dim3(blocks), dim3(kRowThreads), 0, s, gate, vec, ld, P, cols, Npad, KG, ow, B, S, clear);
   };
   auto gemm = [&](const uint8_t* Wm, uint32_t nrows, uint32_t KG, const unsigned long long* ow) {
