@@ -274,6 +274,10 @@ __device__ __forceinline__ void mb_expect_tx(uint64_t* b, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes)
                : "memory");
 }
+// Adds to the transaction bytes the current phase waits for, without an arrival.
+__device__ __forceinline__ void mb_expect_only(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void mb_arrive(uint64_t* b) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
 }
@@ -403,7 +407,7 @@ __device__ __forceinline__ void drain(uint32_t tmem_buf, int32_t* iacc) {
 template <uint32_t N>
 __device__ void bgemm_tile(const uint8_t* W, uint32_t rows, uint32_t KG, const uint8_t* B, uint32_t nt,
                            int32_t* S, int* fault, uint8_t* sm, TcBars& bar, uint32_t tmem,
-                           volatile int* abort) {
+                           volatile int* abort, uint32_t pre) {
   const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t m0 = blockIdx.x * kBM;
   const uint32_t kg0 = blockIdx.z * KG / gridDim.z, kg1 = (blockIdx.z + 1) * KG / gridDim.z;
@@ -418,8 +422,9 @@ __device__ void bgemm_tile(const uint8_t* W, uint32_t rows, uint32_t KG, const u
       const uint32_t slot = s % kRing, kg = kg0 + s;
       if (s >= kRing) mb_wait(&bar.empty[slot], ((s - kRing) / kRing) & 1u, abort);
       if (*abort) return;
-      mb_expect_tx(&bar.full[slot], a_bytes + N * 256);
-      bulk_copy(au8 + slot * kAu8, W + ((size_t)kg * rows + m0) * kBK, a_bytes, &bar.full[slot]);
+      // the first `pre` stages' weight bytes were requested before the wait
+      mb_expect_tx(&bar.full[slot], (s < pre ? 0u : a_bytes) + N * 256);
+      if (s >= pre) bulk_copy(au8 + slot * kAu8, W + ((size_t)kg * rows + m0) * kBK, a_bytes, &bar.full[slot]);
       // plane tiles of 64 rows: atom column a of tile t -> rows 64 t .. of atom column a
 #pragma unroll
       for (uint32_t t = 0; t < N / kBN; ++t)
@@ -501,6 +506,10 @@ __device__ void bgemm_tile(const uint8_t* W, uint32_t rows, uint32_t KG, const u
 }
 
 // One block: 128 rows of the matrix x up to 128 plane columns (blockIdx.y), tcgen05 MMAs.
+// Before the dependency wait (nothing of it reads what the previous kernel writes): the
+// barriers, the tensor memory, and, in the blocks of the first two plane tiles (the ones the
+// usual three planes use), the weight bytes of the first kRing stages (model data).  A block
+// that turns out to have no plane columns waits for those copies before it leaves.
 __global__ void __launch_bounds__(kTcThreads, 1) k_bgemm(const uint8_t* gate, const uint8_t* W,
                                                          uint32_t rows, uint32_t KG, const uint8_t* B,
                                                          uint32_t Npad, const unsigned long long* orw,
@@ -509,15 +518,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_bgemm(const uint8_t* gate, co
   __shared__ TcBars bar;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  pdl_enter();
-  if (!running(gate)) return;
-  const int L = limbs_of_or(*orw);
-  const uint32_t cols = (uint32_t)L * Npad;  // plane columns in use (a multiple of 64)
-  const uint32_t nt = blockIdx.y;
-  if (nt * kTN >= cols) return;
-  const bool narrow = cols - nt * kTN < kTN;  // a last tile of 64 columns
+  const uint32_t tid = threadIdx.x, warp = tid >> 5;
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  if (threadIdx.x == 0) {
+  const uint32_t nt = blockIdx.y;
+  const uint32_t m0 = blockIdx.x * kBM;
+  const uint32_t kg0 = blockIdx.z * KG / gridDim.z, kg1 = (blockIdx.z + 1) * KG / gridDim.z;
+  const uint32_t pre = nt < 2 ? min(kRing, kg1 - kg0) : 0u;  // stages whose weights go out early
+  if (tid == 0) {
     for (uint32_t i = 0; i < kRing; ++i) {
       mb_init(&bar.full[i], 1);
       mb_init(&bar.empty[i], 1);
@@ -530,8 +537,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_bgemm(const uint8_t* gate, co
     }
     abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const uint32_t a_bytes = min(kBM, rows - m0) * kBK;
+    for (uint32_t s = 0; s < pre; ++s) {
+      mb_expect_only(&bar.full[s], a_bytes);
+      bulk_copy(sm + s * kAu8, W + ((size_t)(kg0 + s) * rows + m0) * kBK, a_bytes, &bar.full[s]);
+    }
   }
-  if ((threadIdx.x >> 5) == 0) {
+  if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  ::"r"(smem_addr(&tmem_slot)), "r"(kTmemCols) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -540,13 +552,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_bgemm(const uint8_t* gate, co
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = tmem_slot;
-  if (narrow)
-    bgemm_tile<kBN>(W, rows, KG, B, nt * (kTN / kBN), S, fault, sm, bar, tmem, &abort_flag);
-  else
-    bgemm_tile<kTN>(W, rows, KG, B, nt, S, fault, sm, bar, tmem, &abort_flag);
+  pdl_enter();
+  const int L = running(gate) ? limbs_of_or(*orw) : 0;
+  const uint32_t cols = (uint32_t)L * Npad;  // plane columns in use (a multiple of 64)
+  if (nt * kTN >= cols) {
+    // nothing to compute: the early copies complete on their barriers' arrivals before the
+    // block leaves (a wait that runs out leaves it all the same)
+    if (tid == 0) {
+      for (uint32_t s = 0; s < pre; ++s) {
+        mb_arrive(&bar.full[s]);
+        mb_wait(&bar.full[s], 0, &abort_flag);
+      }
+    }
+  } else if (cols - nt * kTN < kTN) {  // a last tile of 64 columns
+    bgemm_tile<kBN>(W, rows, KG, B, nt * (kTN / kBN), S, fault, sm, bar, tmem, &abort_flag, pre);
+  } else {
+    bgemm_tile<kTN>(W, rows, KG, B, nt, S, fault, sm, bar, tmem, &abort_flag, pre);
+  }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  if ((threadIdx.x >> 5) == 0)
+  if (warp == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
@@ -1072,11 +1097,12 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
   if ((e = cudaMemsetAsync(rstat, 0, 4ull * P, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(fault, 0, 4, s)) != cudaSuccess) return e;
 
-  // column-range split of a contraction: about one block per SM, assuming the usual three
-  // planes (more planes only add blocks), each range at least one group of four column groups
+  // column-range split of a contraction: as many ranges as keep the blocks (one an SM, for
+  // the usual three planes) within one wave, each range at least one group of four column
+  // groups; a second wave of a few blocks would double the launch
   auto splits_for = [&](uint32_t nrows, uint32_t KG) {
     const uint32_t base = ((nrows + kBM - 1) / kBM) * ((3 * Npad + kTN - 1) / kTN);
-    uint32_t z = ((uint32_t)m.num_sms + base - 1) / base;
+    uint32_t z = (uint32_t)m.num_sms / base;
     return std::max(1u, std::min(z, KG / kFlushGroups));
   };
   // the planes of a vector, clearing the output of the contraction that follows when it splits
