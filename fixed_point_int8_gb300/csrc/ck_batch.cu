@@ -253,15 +253,20 @@ __global__ void __launch_bounds__(kRowThreads) k_bplanes(const uint8_t* gate, co
 // 1,024 bytes apart.  The weights' column-group layout is that pattern for bytes, so a
 // weight tile arrives with one bulk copy and is widened to f16 in place of layout; the
 // planes are stored in it as f16.
-constexpr uint32_t kTN = 128;                  // most plane columns per block
+constexpr uint32_t kTN = 192;                  // most plane columns per block (three planes of 64)
 constexpr uint32_t kTcConvWarps = 8;           // widen the weights, drain the accumulators
 constexpr int kTcThreads = 32 * (kTcConvWarps + 2);  // + a producer warp and an MMA warp
-constexpr uint32_t kRing = 3;                  // weight-byte and plane stages in flight
+constexpr uint32_t kRing = 3;                  // weight-byte and plane stages in flight (tiles up to
+                                               // 128 plane columns; 2 for wider ones)
 constexpr uint32_t kAu8 = kBM * kBK;           // 16 KB: 128 rows x 128 weight bytes
 constexpr uint32_t kAf16 = 2 * kBM * 128;      // 32 KB: the same as f16, two atom columns
-constexpr uint32_t kBmax = 2 * kTN * 128;      // 32 KB: 128 plane rows x 128 f16 columns
-constexpr uint32_t kTcSmem = kRing * (kAu8 + kBmax) + 2 * kAf16 + 1024;  // + alignment slack
-constexpr uint32_t kTmemCols = 2 * kTN;        // two accumulator buffers
+__host__ __device__ constexpr uint32_t ring_of(uint32_t n) { return n > 128 ? 2u : kRing; }
+__host__ __device__ constexpr uint32_t tile_smem(uint32_t n) {  // ring of weight bytes and planes, f16 weights
+  return ring_of(n) * (kAu8 + 2 * n * 128) + 2 * kAf16;
+}
+constexpr uint32_t kTcSmem = (tile_smem(128) > tile_smem(kTN) ? tile_smem(128) : tile_smem(kTN)) + 1024;
+constexpr uint32_t kTmemCols = 512;            // two accumulator buffers of up to kTN columns
+constexpr uint32_t kAccCols = 256;             // columns between the two buffers
 constexpr uint32_t kTcPoll = 1u << 22;         // bounded waits
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -394,7 +399,8 @@ __device__ __forceinline__ void drain(uint32_t tmem_buf, int32_t* iacc) {
 }
 
 // S[n'][r] = sum_c (W[r][c] - 128) * plane[n'][c] for the block's 128 rows and N plane
-// columns (N = 128, or 64 for a last tile), over its range of column groups (gridDim.z
+// columns (N = 192, or 128 or 64 for a last tile; plane tiles from pt0 on), over its range
+// of column groups (gridDim.z
 // ranges add their integer sums into S, cleared beforehand).  Warp-specialised, linked by
 // mbarriers only:
 //   producer (warp 8)   copies stage s (a column group's weight bytes and planes) into ring
@@ -405,22 +411,23 @@ __device__ __forceinline__ void drain(uint32_t tmem_buf, int32_t* iacc) {
 //                       of group g (four column groups, 512 columns: every f32 partial sum
 //                       stays below 2^24) once stage s is widened and group g - 2 drained.
 template <uint32_t N>
-__device__ void bgemm_tile(const uint8_t* W, uint32_t rows, uint32_t KG, const uint8_t* B, uint32_t nt,
+__device__ void bgemm_tile(const uint8_t* W, uint32_t rows, uint32_t KG, const uint8_t* B, uint32_t pt0,
                            int32_t* S, int* fault, uint8_t* sm, TcBars& bar, uint32_t tmem,
                            volatile int* abort, uint32_t pre) {
+  constexpr uint32_t R = ring_of(N), kB = 2 * N * 128;  // ring slots, plane bytes of a stage
   const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t m0 = blockIdx.x * kBM;
   const uint32_t kg0 = blockIdx.z * KG / gridDim.z, kg1 = (blockIdx.z + 1) * KG / gridDim.z;
   const uint32_t ns = kg1 - kg0, ngroups = (ns + kFlushGroups - 1) / kFlushGroups;
   uint8_t* au8 = sm;
-  uint8_t* bsm = au8 + kRing * kAu8;
-  uint8_t* af16 = bsm + kRing * kBmax;
+  uint8_t* bsm = au8 + R * kAu8;
+  uint8_t* af16 = bsm + R * kB;
   if (warp == kTcConvWarps) {  // producer
     if (lane != 0) return;
     const uint32_t a_bytes = min(kBM, rows - m0) * kBK;
     for (uint32_t s = 0; s < ns; ++s) {
-      const uint32_t slot = s % kRing, kg = kg0 + s;
-      if (s >= kRing) mb_wait(&bar.empty[slot], ((s - kRing) / kRing) & 1u, abort);
+      const uint32_t slot = s % R, kg = kg0 + s;
+      if (s >= R) mb_wait(&bar.empty[slot], ((s - R) / R) & 1u, abort);
       if (*abort) return;
       // the first `pre` stages' weight bytes were requested before the wait
       mb_expect_tx(&bar.full[slot], (s < pre ? 0u : a_bytes) + N * 256);
@@ -430,8 +437,8 @@ __device__ void bgemm_tile(const uint8_t* W, uint32_t rows, uint32_t KG, const u
       for (uint32_t t = 0; t < N / kBN; ++t)
 #pragma unroll
         for (uint32_t a = 0; a < 2; ++a)
-          bulk_copy(bsm + slot * kBmax + a * (N * 128) + t * (kBN * 128),
-                    B + ((size_t)(nt * (N / kBN) + t) * KG + kg) * kBTile + a * (kBN * 128), kBN * 128,
+          bulk_copy(bsm + slot * kB + a * (N * 128) + t * (kBN * 128),
+                    B + ((size_t)(pt0 + t) * KG + kg) * kBTile + a * (kBN * 128), kBN * 128,
                     &bar.full[slot]);
     }
     return;
@@ -439,14 +446,14 @@ __device__ void bgemm_tile(const uint8_t* W, uint32_t rows, uint32_t KG, const u
   if (warp == kTcConvWarps + 1) {  // MMA issuer
     if (lane != 0) return;
     for (uint32_t s = 0; s < ns; ++s) {
-      const uint32_t slot = s % kRing, fb = s & 1u, g = s / kFlushGroups;
-      mb_wait(&bar.full[slot], (s / kRing) & 1u, abort);
+      const uint32_t slot = s % R, fb = s & 1u, g = s / kFlushGroups;
+      mb_wait(&bar.full[slot], (s / R) & 1u, abort);
       mb_wait(&bar.conv[fb], (s >> 1) & 1u, abort);
       if (s % kFlushGroups == 0 && g >= 2) mb_wait(&bar.accfree[g & 1u], ((g - 2) >> 1) & 1u, abort);
       if (*abort) return;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t abase = smem_addr(af16 + fb * kAf16), bbase = smem_addr(bsm + slot * kBmax);
-      const uint32_t acc_tmem = tmem + (g & 1u) * kTN;
+      const uint32_t abase = smem_addr(af16 + fb * kAf16), bbase = smem_addr(bsm + slot * kB);
+      const uint32_t acc_tmem = tmem + (g & 1u) * kAccCols;
 #pragma unroll
       for (uint32_t kk = 0; kk < 8; ++kk) {
         const uint64_t da = smem_desc(abase + (kk >> 2) * (kBM * 128) + (kk & 3u) * 32);
@@ -468,14 +475,14 @@ __device__ void bgemm_tile(const uint8_t* W, uint32_t rows, uint32_t KG, const u
   auto drain_group = [&](uint32_t gg) {
     mb_wait(&bar.accf[gg & 1u], (gg >> 1) & 1u, abort);
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (!*abort) drain<N>(tmem + (gg & 1u) * kTN, iacc);
+    if (!*abort) drain<N>(tmem + (gg & 1u) * kAccCols, iacc);
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncwarp();
     if (lane == 0) mb_arrive(&bar.accfree[gg & 1u]);
   };
   for (uint32_t s = 0; s < ns; ++s) {
-    const uint32_t slot = s % kRing, fb = s & 1u;
-    mb_wait(&bar.full[slot], (s / kRing) & 1u, abort);
+    const uint32_t slot = s % R, fb = s & 1u;
+    mb_wait(&bar.full[slot], (s / R) & 1u, abort);
     if (s >= 2) mb_wait(&bar.f16free[fb], ((s - 2) >> 1) & 1u, abort);
     if (*abort) break;
     widen_weights(au8 + slot * kAu8, af16 + fb * kAf16);
@@ -494,7 +501,7 @@ __device__ void bgemm_tile(const uint8_t* W, uint32_t rows, uint32_t KG, const u
   // warp w holds rows 32 (w % 4) + lane, columns of half w / 4
   const uint32_t r = m0 + 32 * (warp & 3u) + lane;
   if (r >= rows) return;
-  const uint32_t n0 = nt * N + (warp >> 2) * (N / 2);
+  const uint32_t n0 = pt0 * kBN + (warp >> 2) * (N / 2);
 #pragma unroll
   for (uint32_t i = 0; i < N / 2; ++i) {
     int32_t* dst = S + (size_t)(n0 + i) * rows + r;
@@ -505,11 +512,11 @@ __device__ void bgemm_tile(const uint8_t* W, uint32_t rows, uint32_t KG, const u
   }
 }
 
-// One block: 128 rows of the matrix x up to 128 plane columns (blockIdx.y), tcgen05 MMAs.
+// One block: 128 rows of the matrix x up to kTN plane columns (blockIdx.y), tcgen05 MMAs.
 // Before the dependency wait (nothing of it reads what the previous kernel writes): the
-// barriers, the tensor memory, and, in the blocks of the first two plane tiles (the ones the
-// usual three planes use), the weight bytes of the first kRing stages (model data).  A block
-// that turns out to have no plane columns waits for those copies before it leaves.
+// barriers, the tensor memory, and, in the blocks of the first plane tile (the one the usual
+// three planes fill), the weight bytes of the first two stages (model data).  A block that
+// turns out to have no plane columns waits for those copies before it leaves.
 __global__ void __launch_bounds__(kTcThreads, 1) k_bgemm(const uint8_t* gate, const uint8_t* W,
                                                          uint32_t rows, uint32_t KG, const uint8_t* B,
                                                          uint32_t Npad, const unsigned long long* orw,
@@ -523,7 +530,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_bgemm(const uint8_t* gate, co
   const uint32_t nt = blockIdx.y;
   const uint32_t m0 = blockIdx.x * kBM;
   const uint32_t kg0 = blockIdx.z * KG / gridDim.z, kg1 = (blockIdx.z + 1) * KG / gridDim.z;
-  const uint32_t pre = nt < 2 ? min(kRing, kg1 - kg0) : 0u;  // stages whose weights go out early
+  const uint32_t pre = nt == 0 ? min(2u, kg1 - kg0) : 0u;  // stages whose weights go out early
   if (tid == 0) {
     for (uint32_t i = 0; i < kRing; ++i) {
       mb_init(&bar.full[i], 1);
@@ -564,10 +571,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_bgemm(const uint8_t* gate, co
         mb_wait(&bar.full[s], 0, &abort_flag);
       }
     }
-  } else if (cols - nt * kTN < kTN) {  // a last tile of 64 columns
+  } else if (cols - nt * kTN <= kBN) {  // a last tile of 64 columns
     bgemm_tile<kBN>(W, rows, KG, B, nt * (kTN / kBN), S, fault, sm, bar, tmem, &abort_flag, pre);
+  } else if (cols - nt * kTN <= 2 * kBN) {  // of 128
+    bgemm_tile<2 * kBN>(W, rows, KG, B, nt * (kTN / kBN), S, fault, sm, bar, tmem, &abort_flag, pre);
   } else {
-    bgemm_tile<kTN>(W, rows, KG, B, nt, S, fault, sm, bar, tmem, &abort_flag, pre);
+    bgemm_tile<kTN>(W, rows, KG, B, nt * (kTN / kBN), S, fault, sm, bar, tmem, &abort_flag, pre);
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
