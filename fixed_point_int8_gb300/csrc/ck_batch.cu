@@ -256,17 +256,21 @@ __global__ void __launch_bounds__(kRowThreads) k_bplanes(const uint8_t* gate, co
 constexpr uint32_t kTN = 192;                  // most plane columns per block (three planes of 64)
 constexpr uint32_t kTcConvWarps = 8;           // widen the weights, drain the accumulators
 constexpr int kTcThreads = 32 * (kTcConvWarps + 2);  // + a producer warp and an MMA warp
-constexpr uint32_t kRing = 3;                  // weight-byte and plane stages in flight (tiles up to
-                                               // 128 plane columns; 2 for wider ones)
+constexpr uint32_t kRing = 4;                  // weight-byte and plane stages in flight (tiles up to
+                                               // 128 plane columns; 3 for wider ones)
 constexpr uint32_t kAu8 = kBM * kBK;           // 16 KB: 128 rows x 128 weight bytes
-constexpr uint32_t kAf16 = 2 * kBM * 128;      // 32 KB: the same as f16, two atom columns
-__host__ __device__ constexpr uint32_t ring_of(uint32_t n) { return n > 128 ? 2u : kRing; }
-__host__ __device__ constexpr uint32_t tile_smem(uint32_t n) {  // ring of weight bytes and planes, f16 weights
-  return ring_of(n) * (kAu8 + 2 * n * 128) + 2 * kAf16;
+__host__ __device__ constexpr uint32_t ring_of(uint32_t n) { return n > 128 ? 3u : kRing; }
+__host__ __device__ constexpr uint32_t tile_smem(uint32_t n) {  // ring of weight bytes and planes
+  return ring_of(n) * (kAu8 + 2 * n * 128);
 }
 constexpr uint32_t kTcSmem = (tile_smem(128) > tile_smem(kTN) ? tile_smem(128) : tile_smem(kTN)) + 1024;
-constexpr uint32_t kTmemCols = 512;            // two accumulator buffers of up to kTN columns
-constexpr uint32_t kAccCols = 256;             // columns between the two buffers
+// Tensor memory (512 columns of 128 lanes): two accumulator buffers of up to kTN columns at
+// columns 0 and 256, and the widened weights of two stages (128 rows x 128 f16, 64 columns
+// each: lane = row, two consecutive columns' values a 32-bit column) in the gaps after them.
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = 256;             // columns between the two accumulator buffers
+constexpr uint32_t kAColA = kTN, kAColB = kAccCols + kTN;  // the two weight buffers
+static_assert(kTN + 64 <= kAccCols && kAccCols + kTN + 64 <= kTmemCols, "tensor memory layout");
 constexpr uint32_t kTcPoll = 1u << 22;         // bounded waits
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -312,8 +316,8 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t b
 struct TcBars {
   uint64_t full[kRing];     // stage landed (bulk copies)
   uint64_t empty[kRing];    // stage's MMAs done: the slot may be refilled
-  uint64_t conv[2];         // f16 weights of the stage written (one arrival per converter warp)
-  uint64_t f16free[2];      // MMAs reading an f16 buffer done
+  uint64_t conv[2];         // f16 weights of the stage in tensor memory (one arrival per converter warp)
+  uint64_t f16free[2];      // MMAs reading an f16 weight buffer done
   uint64_t accf[2];         // accumulator group complete
   uint64_t accfree[2];      // accumulator buffer drained (one arrival per converter warp)
 };
@@ -331,11 +335,12 @@ __host__ __device__ constexpr uint32_t mma_idesc(uint32_t n) {
   return (1u << 4) | ((n >> 3) << 17) | ((kBM >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_f16_ss(uint32_t tmem, uint64_t da, uint64_t db, uint32_t idesc,
+// One MMA with A (the widened weights) in tensor memory and B (planes) in shared memory.
+__device__ __forceinline__ void mma_f16_ts(uint32_t tmem, uint32_t ta, uint64_t db, uint32_t idesc,
                                            uint32_t accumulate) {
   asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
-      ::"r"(tmem), "l"(da), "l"(db), "r"(idesc), "r"(accumulate)
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }"
+      ::"r"(tmem), "r"(ta), "l"(db), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -354,28 +359,35 @@ __device__ __forceinline__ uint32_t bytes_to_f16x2(uint32_t w, uint32_t sel) {
 }
 
 // Widens a stage's weight bytes (128 rows x 128 columns, column-group layout) to f16
-// (byte - 128) in the two-atom-column layout the MMA reads.  Four 16-byte chunks a thread.
-__device__ __forceinline__ void widen_weights(const uint8_t* src, uint8_t* dst) {
+// (byte - 128) into tensor memory: warp w takes rows 32 (w % 4) + lane (its lane quarter) and
+// columns 64 (w / 4) .. + 63, four 16-byte chunks of its row, 32 f16 pairs stored at once.
+__device__ __forceinline__ void widen_to_tmem(const uint8_t* src, uint32_t ta) {
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t r = 32 * (warp & 3u) + lane, j0 = 4 * (warp >> 2);
+  uint32_t v[32];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const uint32_t id = threadIdx.x + e * (32 * kTcConvWarps);  // 1,024 chunks: row id / 8, chunk id % 8
-    const uint32_t r = id >> 3, j = id & 7u;
+  for (uint32_t e = 0; e < 4; ++e) {
+    const uint32_t j = j0 + e;
     const uint4 w = *reinterpret_cast<const uint4*>(src + r * 128 + ((j ^ (r & 7u)) << 4));
-    uint4 lo, hi;
-    lo.x = bytes_to_f16x2(w.x, 0x5140u);
-    lo.y = bytes_to_f16x2(w.x, 0x5342u);
-    lo.z = bytes_to_f16x2(w.y, 0x5140u);
-    lo.w = bytes_to_f16x2(w.y, 0x5342u);
-    hi.x = bytes_to_f16x2(w.z, 0x5140u);
-    hi.y = bytes_to_f16x2(w.z, 0x5342u);
-    hi.z = bytes_to_f16x2(w.w, 0x5140u);
-    hi.w = bytes_to_f16x2(w.w, 0x5342u);
-    // columns 16j .. 16j+15: atom column j / 4, f16 chunks 2(j % 4) and 2(j % 4) + 1
-    uint8_t* row = dst + (j >> 2) * (kBM * 128) + r * 128;
-    const uint32_t c0 = 2 * (j & 3u);
-    *reinterpret_cast<uint4*>(row + ((c0 ^ (r & 7u)) << 4)) = lo;
-    *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7u)) << 4)) = hi;
+    v[8 * e + 0] = bytes_to_f16x2(w.x, 0x5140u);
+    v[8 * e + 1] = bytes_to_f16x2(w.x, 0x5342u);
+    v[8 * e + 2] = bytes_to_f16x2(w.y, 0x5140u);
+    v[8 * e + 3] = bytes_to_f16x2(w.y, 0x5342u);
+    v[8 * e + 4] = bytes_to_f16x2(w.z, 0x5140u);
+    v[8 * e + 5] = bytes_to_f16x2(w.z, 0x5342u);
+    v[8 * e + 6] = bytes_to_f16x2(w.w, 0x5140u);
+    v[8 * e + 7] = bytes_to_f16x2(w.w, 0x5342u);
   }
+  const uint32_t addr = ta + ((32 * (warp & 3u)) << 16) + 32 * (warp >> 2);
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      ::"r"(addr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+        "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Adds the f32 sums of one accumulator buffer (this warp's 32 rows, this warpgroup's half
@@ -404,9 +416,10 @@ __device__ __forceinline__ void drain(uint32_t tmem_buf, int32_t* iacc) {
 // ranges add their integer sums into S, cleared beforehand).  Warp-specialised, linked by
 // mbarriers only:
 //   producer (warp 8)   copies stage s (a column group's weight bytes and planes) into ring
-//                       slot s % kRing once the MMAs of stage s - kRing are done;
-//   converters (0..7)   widen stage s's weights into f16 buffer s % 2 once the MMAs of
-//                       stage s - 2 are done, and drain each finished accumulator group;
+//                       slot s % R once the MMAs of stage s - R are done;
+//   converters (0..7)   widen stage s's weights into the tensor-memory f16 buffer s % 2 once
+//                       the MMAs of stage s - 2 are done, and drain each finished
+//                       accumulator group;
 //   MMA thread (warp 9) issues stage s's eight 16-column MMAs into accumulator buffer g % 2
 //                       of group g (four column groups, 512 columns: every f32 partial sum
 //                       stays below 2^24) once stage s is widened and group g - 2 drained.
@@ -421,7 +434,6 @@ __device__ void bgemm_tile(const uint8_t* W, uint32_t rows, uint32_t KG, const u
   const uint32_t ns = kg1 - kg0, ngroups = (ns + kFlushGroups - 1) / kFlushGroups;
   uint8_t* au8 = sm;
   uint8_t* bsm = au8 + R * kAu8;
-  uint8_t* af16 = bsm + R * kB;
   if (warp == kTcConvWarps) {  // producer
     if (lane != 0) return;
     const uint32_t a_bytes = min(kBM, rows - m0) * kBK;
@@ -452,14 +464,13 @@ __device__ void bgemm_tile(const uint8_t* W, uint32_t rows, uint32_t KG, const u
       if (s % kFlushGroups == 0 && g >= 2) mb_wait(&bar.accfree[g & 1u], ((g - 2) >> 1) & 1u, abort);
       if (*abort) return;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t abase = smem_addr(af16 + fb * kAf16), bbase = smem_addr(bsm + slot * kB);
+      const uint32_t ta = tmem + (fb ? kAColB : kAColA), bbase = smem_addr(bsm + slot * kB);
       const uint32_t acc_tmem = tmem + (g & 1u) * kAccCols;
 #pragma unroll
-      for (uint32_t kk = 0; kk < 8; ++kk) {
-        const uint64_t da = smem_desc(abase + (kk >> 2) * (kBM * 128) + (kk & 3u) * 32);
+      for (uint32_t kk = 0; kk < 8; ++kk) {  // K 16 kk .. : eight columns of A, 32 bytes of B rows
         const uint64_t db = smem_desc(bbase + (kk >> 2) * (N * 128) + (kk & 3u) * 32);
         const uint32_t accumulate = (s % kFlushGroups != 0 || kk != 0) ? 1u : 0u;
-        mma_f16_ss(acc_tmem, da, db, mma_idesc(N), accumulate);
+        mma_f16_ts(acc_tmem, ta + 8 * kk, db, mma_idesc(N), accumulate);
       }
       mma_commit(&bar.empty[slot]);
       mma_commit(&bar.f16free[fb]);
@@ -485,8 +496,9 @@ __device__ void bgemm_tile(const uint8_t* W, uint32_t rows, uint32_t KG, const u
     mb_wait(&bar.full[slot], (s / R) & 1u, abort);
     if (s >= 2) mb_wait(&bar.f16free[fb], ((s - 2) >> 1) & 1u, abort);
     if (*abort) break;
-    widen_weights(au8 + slot * kAu8, af16 + fb * kAf16);
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    widen_to_tmem(au8 + slot * kAu8, tmem + (fb ? kAColB : kAColA));
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncwarp();
     if (lane == 0) mb_arrive(&bar.conv[fb]);
     // group g - 1 finished a stage ago: drain it while group g fills the other buffer
@@ -515,7 +527,7 @@ __device__ void bgemm_tile(const uint8_t* W, uint32_t rows, uint32_t KG, const u
 // One block: 128 rows of the matrix x up to kTN plane columns (blockIdx.y), tcgen05 MMAs.
 // Before the dependency wait (nothing of it reads what the previous kernel writes): the
 // barriers, the tensor memory, and, in the blocks of the first plane tile (the one the usual
-// three planes fill), the weight bytes of the first two stages (model data).  A block that
+// three planes fill), the weight bytes of the first three stages (model data).  A block that
 // turns out to have no plane columns waits for those copies before it leaves.
 __global__ void __launch_bounds__(kTcThreads, 1) k_bgemm(const uint8_t* gate, const uint8_t* W,
                                                          uint32_t rows, uint32_t KG, const uint8_t* B,
@@ -530,7 +542,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_bgemm(const uint8_t* gate, co
   const uint32_t nt = blockIdx.y;
   const uint32_t m0 = blockIdx.x * kBM;
   const uint32_t kg0 = blockIdx.z * KG / gridDim.z, kg1 = (blockIdx.z + 1) * KG / gridDim.z;
-  const uint32_t pre = nt == 0 ? min(2u, kg1 - kg0) : 0u;  // stages whose weights go out early
+  const uint32_t pre = nt == 0 ? min(3u, kg1 - kg0) : 0u;  // stages whose weights go out early
   if (tid == 0) {
     for (uint32_t i = 0; i < kRing; ++i) {
       mb_init(&bar.full[i], 1);
