@@ -618,12 +618,29 @@ struct BEpiParams {
   unsigned long long* or_out;     // SiLU: the output vector's OR word
 };
 
-// y[n][r] = ((sum_k S_k[n][r] << 8k) * scale[r]) >> 24, wrapping.
-__device__ __forceinline__ int64_t combine(const BEpiParams& p, int L, uint32_t n, uint32_t r) {
-  unsigned long long a = 0;
-  for (int k = 0; k < L; ++k)
-    a += (unsigned long long)(long long)p.S[((size_t)k * p.Npad + n) * p.rows + r] << (8 * k);
-  return (int64_t)(a * (unsigned long long)__ldg(p.scale + r)) >> 24;
+// y[n][r] = ((sum_k S_k[n][r] << 8k) * scale[r]) >> 24, wrapping, for rows r and r + 1 (r
+// even; r + 1 only when it exists): every plane's pair of sums is requested before any is
+// used, so the loads overlap instead of following one another.
+__device__ __forceinline__ void combine_pair(const BEpiParams& p, int L, uint32_t n, uint32_t r, int64_t& y0,
+                                             int64_t& y1) {
+  const bool two = r + 1 < p.rows, paired = two && (p.rows & 1u) == 0;  // 8-byte aligned pairs
+  int2 v[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int32_t* src = p.S + ((size_t)k * p.Npad + n) * p.rows + r;
+    v[k] = k >= L   ? make_int2(0, 0)
+           : paired ? *reinterpret_cast<const int2*>(src)
+                    : make_int2(src[0], two ? src[1] : 0);
+  }
+  const uint32_t s0 = __ldg(p.scale + r), s1 = two ? __ldg(p.scale + r + 1) : 0u;
+  unsigned long long a0 = 0, a1 = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    a0 += (unsigned long long)(long long)v[k].x << (8 * k);
+    a1 += (unsigned long long)(long long)v[k].y << (8 * k);
+  }
+  y0 = (int64_t)(a0 * (unsigned long long)s0) >> 24;
+  y1 = (int64_t)(a1 * (unsigned long long)s1) >> 24;
 }
 
 // One thread per (position, row pair): rows 2i and 2i+1 are a rotary pair in Q and K and a
@@ -634,20 +651,22 @@ __global__ void __launch_bounds__(kRowThreads) k_bepi(const BEpiParams p) {
   pdl_enter();
   if (!running(p.gate)) return;
   const int L = limbs_of_or(*p.orw);
-  const uint32_t pairs = (p.rows + 1) / 2;
+  const uint32_t pairs = (p.rows + 1) / 2, items = p.P * pairs;  // below 2^32
   unsigned long long o = 0;
-  for (uint64_t idx = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < (uint64_t)p.P * pairs;
-       idx += (uint64_t)gridDim.x * blockDim.x) {
-    const uint32_t n = (uint32_t)(idx / pairs), r = 2 * (uint32_t)(idx % pairs);
+  for (uint32_t idx = blockIdx.x * blockDim.x + threadIdx.x; idx < items; idx += gridDim.x * blockDim.x) {
+    const uint32_t n = idx / pairs, r = 2 * (idx - n * pairs);
     if (p.mode == kBEpiLogits) {
       const RowDesc rd = p.rdesc[n];
       if (!rd.generating) continue;
       int64_t* lg = reinterpret_cast<int64_t*>(rd.st + rd.off_logits);
-      lg[r] = combine(p, L, n, r);
-      if (r + 1 < p.rows) lg[r + 1] = combine(p, L, n, r + 1);
+      int64_t y0, y1;
+      combine_pair(p, L, n, r, y0, y1);
+      lg[r] = y0;
+      if (r + 1 < p.rows) lg[r + 1] = y1;
       continue;
     }
-    const int64_t y0 = combine(p, L, n, r), y1 = combine(p, L, n, r + 1);
+    int64_t y0, y1;
+    combine_pair(p, L, n, r, y0, y1);
     if (p.mode == kBEpiResid) {
       int64_t* x = p.X + (size_t)n * p.rows + r;
       x[0] = wadd(x[0], y0);
