@@ -38,10 +38,10 @@ __device__ __forceinline__ unsigned long long warp_sum(unsigned long long v) {
 }
 
 // Shared memory: queries, per-warp and per-CTA partials, the cluster's chunk maxima and sums
-// (slot r written by rank r), reduction slots, the chunk's scores, then (16-byte aligned) the
-// first batch of value rows.
+// (slot r written by rank r), the two barriers those writes complete on, reduction slots, the
+// chunk's scores, then (16-byte aligned) the first batch of value rows.
 __host__ __device__ inline size_t attn_vpre_offset(uint32_t hd, uint32_t chunk_cap) {
-  return (8 * ((size_t)hd * (2 + kWarps) + 16 + kWarps + chunk_cap) + 15) & ~(size_t)15;
+  return (8 * ((size_t)hd * (2 + kWarps) + 18 + kWarps + chunk_cap) + 15) & ~(size_t)15;
 }
 
 // 16-byte asynchronous copy from global to shared memory (zeros and no read when not valid),
@@ -53,6 +53,56 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
                : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Shared-memory barriers (mbarrier) and bulk copies into shared memory that complete on them.
+__device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void lbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void lbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void lbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
+}
+__device__ __forceinline__ bool lbar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(saddr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void lbulk(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(saddr(dst)),
+      "l"(src), "r"(bytes), "r"(saddr(bar))
+      : "memory");
+}
+
+// An eight-byte store into the same shared-memory variable of cluster peer `peer`, completing
+// on that peer's barrier `bar` (the receiving CTA counts the bytes).
+__device__ __forceinline__ void st_async_peer(void* local, unsigned long long v, uint64_t* bar, uint32_t peer) {
+  uint32_t ra, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(saddr(local)), "r"(peer));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(saddr(bar)), "r"(peer));
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(ra), "l"(v),
+               "r"(rb)
+               : "memory");
+}
+// Waits for an exchange's barrier (phase 0); a wait that runs out fails the state with error 9
+// and the kernel goes on, so that every thread reaches the same barriers.
+constexpr uint32_t kXPoll = 1u << 22;
+__device__ __forceinline__ void exchange_wait(uint64_t* bar, uint8_t* state) {
+  uint32_t i = 0;
+  while (!lbar_try(bar, 0) && ++i < kXPoll) {
+  }
+  if (i >= kXPoll) {
+    hdr<uint32_t>(state, kHError) = CK_CUDA_ERROR;
+    hdr<uint32_t>(state, kHPhase) = CK_PHASE_FAILED;
+  }
+}
 
 // Lanes per position = hd / 4, four elements a lane; a warp issues kUnroll steps' cache loads
 // before it uses them.  The first batch of key rows of earlier positions is loaded into
@@ -70,12 +120,23 @@ __global__ void __launch_bounds__(kThreads, 4) k_attention(const AttnParams p) {
   unsigned long long* cpart = part + kWarps * hd;                               // [hd]
   long long* cmax = reinterpret_cast<long long*>(cpart + hd);                   // [8]
   unsigned long long* csum = reinterpret_cast<unsigned long long*>(cmax + 8);   // [8]
-  long long* red = reinterpret_cast<long long*>(csum + 8);                      // [kWarps]
+  uint64_t* xbar = reinterpret_cast<uint64_t*>(csum + 8);                        // [2]
+  long long* red = reinterpret_cast<long long*>(xbar + 2);                      // [kWarps]
   long long* sc = red + kWarps;                                                 // [chunk_cap]
   int4* vpre = reinterpret_cast<int4*>(smem + attn_vpre_offset(hd, p.chunk_cap));  // [kUnroll][kThreads]
-  // every CTA of the cluster has started before any writes into a peer's shared memory: the
-  // arrival here, the wait just before the first such write
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  // The maxima and sums reach the peers as asynchronous remote stores that complete on the
+  // receiving CTA's barrier (eight bytes from each CTA of the cluster).  Every CTA has set up
+  // its barriers before any peer writes into it: the arrival here, the wait just before the
+  // first such write.
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      lbar_init(&xbar[i], 1);
+      lbar_expect_tx(&xbar[i], 8 * cluster.num_blocks());
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 
   // Launched with programmatic dependent launch.  Before the wait this kernel reads only what
   // was written before the previous kernel started: the position (set by the previous
@@ -164,15 +225,15 @@ __global__ void __launch_bounds__(kThreads, 4) k_attention(const AttnParams p) {
   lmax = warp_max(lmax);
   if (lane == 0) red[warp] = lmax;
   __syncthreads();
-  // the CTA's maximum goes into slot `rank` of every peer (thread r writes peer r), so that
-  // after the cluster barrier each CTA reads the maxima from its own shared memory
+  // the CTA's maximum goes into slot `rank` of every peer (thread r writes peer r); each CTA
+  // then reads the maxima from its own shared memory once all have arrived
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   if (tid < CL) {
     long long mm = red[0];
     for (int w = 1; w < kWarps; ++w) mm = red[w] > mm ? red[w] : mm;
-    *cluster.map_shared_rank(cmax + rank, tid) = mm;
+    st_async_peer(cmax + rank, (unsigned long long)mm, &xbar[0], tid);
   }
-  cluster.sync();
+  exchange_wait(&xbar[0], p.state);
   long long m = LLONG_MIN;
   for (uint32_t r = 0; r < CL; ++r) m = cmax[r] > m ? cmax[r] : m;
 
@@ -191,11 +252,11 @@ __global__ void __launch_bounds__(kThreads, 4) k_attention(const AttnParams p) {
   if (tid < CL) {
     unsigned long long t = 0;
     for (int w = 0; w < kWarps; ++w) t += (unsigned long long)red[w];
-    *cluster.map_shared_rank(csum + rank, tid) = t;
+    st_async_peer(csum + rank, t, &xbar[1], tid);
   }
-  // after this barrier no CTA touches a peer's shared memory again (except in the exchange of
-  // partial sums below, which has barriers of its own)
-  cluster.sync();
+  // once this CTA's sums are in, nothing writes into its shared memory again (except in the
+  // exchange of partial sums below, which has cluster barriers of its own)
+  exchange_wait(&xbar[1], p.state);
   unsigned long long Z = 0;
   for (uint32_t r = 0; r < CL; ++r) Z += csum[r];
 
@@ -300,32 +361,6 @@ constexpr int kLUnroll = 4;                    // warp steps of a value batch
 constexpr int kLCons = kLWarps * 32;           // consumer threads
 constexpr int kLThreads = kLCons + 32;         // + the copy warp
 constexpr uint32_t kLPoll = 1u << 22;
-
-__device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ void lbar_init(uint64_t* b, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void lbar_expect_tx(uint64_t* b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void lbar_arrive(uint64_t* b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
-}
-__device__ __forceinline__ bool lbar_try(uint64_t* b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok)
-      : "r"(saddr(b)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ void lbulk(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(saddr(dst)),
-      "l"(src), "r"(bytes), "r"(saddr(bar))
-      : "memory");
-}
 
 // Shared memory of the long kernel: the ring, then the per-CTA region as k_attention lays it
 // out (queries, partials, maximum, sum, reduction slots, scores), then the ring's barriers
