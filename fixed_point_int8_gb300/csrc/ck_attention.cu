@@ -343,7 +343,8 @@ size_t attn_smem(uint32_t hd, uint32_t chunk_cap) {
 // heads of 16 or more), so a position's lane sums take few shuffle levels; the weighted sum of
 // values gives each lane 4 elements (it needs no per-position sums).  Only the batch holding
 // the newest row (written by the kernel just before) waits for that kernel; older rows stream
-// at once.  The copy warp joins the two cluster exchanges between the keys and the values.
+// at once.  The consumers exchange maxima and sums as in k_attention (remote stores that
+// complete on the receiver's barrier); the copy warp takes no part and keeps streaming.
 #ifndef CK_LSLOTS
 #define CK_LSLOTS 5
 #endif
@@ -366,7 +367,7 @@ constexpr uint32_t kLPoll = 1u << 22;
 // out (queries, partials, maximum, sum, reduction slots, scores), then the ring's barriers
 // and the failure flag.
 __host__ __device__ inline size_t lattn_region(uint32_t hd, uint32_t chunk_cap) {
-  return 8 * ((size_t)hd * (2 + kLWarps) + 2 + kLWarps + chunk_cap);
+  return 8 * ((size_t)hd * (2 + kLWarps) + 18 + kLWarps + chunk_cap);
 }
 __host__ __device__ inline size_t lattn_bars(uint32_t hd, uint32_t chunk_cap) {
   return ((size_t)kLSlots * kLBatch + lattn_region(hd, chunk_cap) + 15) & ~(size_t)15;
@@ -395,9 +396,10 @@ __global__ void __launch_bounds__(kLThreads, 1) k_attention_long(const AttnParam
   int64_t* q_s = reinterpret_cast<int64_t*>(smem + (size_t)kLSlots * kLBatch);
   unsigned long long* part = reinterpret_cast<unsigned long long*>(q_s + hd);  // [kLWarps][hd]
   unsigned long long* cpart = part + kLWarps * hd;                               // [hd]
-  long long* cmax = reinterpret_cast<long long*>(cpart + hd);                   // [1]
-  unsigned long long* csum = reinterpret_cast<unsigned long long*>(cmax + 1);   // [1]
-  long long* red = reinterpret_cast<long long*>(csum + 1);                      // [kLWarps]
+  long long* cmax = reinterpret_cast<long long*>(cpart + hd);                   // [8], slot r from rank r
+  unsigned long long* csum = reinterpret_cast<unsigned long long*>(cmax + 8);   // [8]
+  uint64_t* xbar = reinterpret_cast<uint64_t*>(csum + 8);                        // [2]
+  long long* red = reinterpret_cast<long long*>(xbar + 2);                      // [kLWarps]
   long long* sc = red + kLWarps;                                                 // [chunk_cap]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lattn_bars(hd, p.chunk_cap));
   uint64_t* empty = full + kLSlots;
@@ -423,10 +425,17 @@ __global__ void __launch_bounds__(kLThreads, 1) k_attention_long(const AttnParam
       lbar_init(&full[i], 1);
       lbar_init(&empty[i], kLWarps);
     }
+    for (int i = 0; i < 2; ++i) {  // the exchanges of maxima and sums: eight bytes from each CTA
+      lbar_init(&xbar[i], 1);
+      lbar_expect_tx(&xbar[i], 8 * CL);
+    }
     *flag = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  // every CTA has set up its barriers before a peer's first remote store into it (the
+  // consumers wait on this arrival just before theirs)
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 
   if (warp == kLWarps) {
     // the copy warp: key batches, then value batches, into slot g % kLSlots for the g-th batch
@@ -457,14 +466,7 @@ __global__ void __launch_bounds__(kLThreads, 1) k_attention_long(const AttnParam
     };
     if (lane == 0) {
       for (uint32_t b = 0; b < nb && !halt; ++b) issue(Kh, b);
-      for (uint32_t b = 0; b < min(nb, kLSlots) && !halt; ++b) issue(Vh, b);  // slots the last keys free
-    }
-    __syncwarp();
-    cluster.sync();  // the consumers' exchange of maxima
-    cluster.sync();  // and of sums
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    if (lane == 0) {
-      for (uint32_t b = min(nb, kLSlots); b < nb && !halt; ++b) issue(Vh, b);
+      for (uint32_t b = 0; b < nb && !halt; ++b) issue(Vh, b);  // as the consumers free slots
       // no copy outlives the CTA: the last kLSlots batches started have landed
       for (uint32_t j = g > kLSlots ? g - kLSlots : 0; j < g; ++j)
         for (uint32_t i = 0; i < kLPoll; ++i)
@@ -472,7 +474,6 @@ __global__ void __launch_bounds__(kLThreads, 1) k_attention_long(const AttnParam
     }
     __syncwarp();
     if (CK_LLATE) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     return;
   }
 
@@ -503,6 +504,15 @@ __global__ void __launch_bounds__(kLThreads, 1) k_attention_long(const AttnParam
     if (dead) return;
     for (uint32_t i = 0; i < kLPoll; ++i) {
       if (lbar_try(&full[g % kLSlots], (g / kLSlots) & 1u)) return;
+      if ((i & 63) == 63 && *flag) break;
+    }
+    if (!*flag) lattn_fail(p, flag);
+    dead = true;
+  };
+  // an exchange's values, once the cluster's eight bytes a CTA have landed (bounded likewise)
+  auto xwait = [&](uint64_t* bar) {
+    for (uint32_t i = 0; i < kLPoll; ++i) {
+      if (lbar_try(bar, 0)) return;
       if ((i & 63) == 63 && *flag) break;
     }
     if (!*flag) lattn_fail(p, flag);
@@ -551,17 +561,17 @@ __global__ void __launch_bounds__(kLThreads, 1) k_attention_long(const AttnParam
   lmax = warp_max(lmax);
   if (lane == 0) red[warp] = lmax;
   consumers_sync();
-  if (tid == 0) {
-    long long m = red[0];
-    for (int w = 1; w < kLWarps; ++w) m = red[w] > m ? red[w] : m;
-    *cmax = m;
+  // the CTA's maximum into slot `rank` of every peer (thread r writes peer r) by remote stores
+  // that complete on the peer's barrier; the maxima are then read locally
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  if (tid < CL) {
+    long long mm = red[0];
+    for (int w = 1; w < kLWarps; ++w) mm = red[w] > mm ? red[w] : mm;
+    st_async_peer(cmax + rank, (unsigned long long)mm, &xbar[0], tid);
   }
-  cluster.sync();
+  xwait(&xbar[0]);
   long long m = LLONG_MIN;
-  for (uint32_t r = 0; r < CL; ++r) {
-    const long long v = *cluster.map_shared_rank(cmax, r);
-    m = v > m ? v : m;
-  }
+  for (uint32_t r = 0; r < CL; ++r) m = cmax[r] > m ? cmax[r] : m;
 
   // stage 1: e_t = EXP[min((m - s_t) >> 8, 4096)]; the exact difference is >= 0 and fits u64
   unsigned long long z = 0;
@@ -575,16 +585,14 @@ __global__ void __launch_bounds__(kLThreads, 1) k_attention_long(const AttnParam
   z = warp_sum(z);
   if (lane == 0) red[warp] = (long long)z;
   consumers_sync();
-  if (tid == 0) {
+  if (tid < CL) {
     unsigned long long t = 0;
     for (int w = 0; w < kLWarps; ++w) t += (unsigned long long)red[w];
-    *csum = t;
+    st_async_peer(csum + rank, t, &xbar[1], tid);
   }
-  cluster.sync();
+  xwait(&xbar[1]);  // after this nothing writes into this CTA's shared memory from outside
   unsigned long long Z = 0;
-  for (uint32_t r = 0; r < CL; ++r) Z += *cluster.map_shared_rank(csum, r);
-  // the peers' maxima and sums are read: arrive now, wait before leaving
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  for (uint32_t r = 0; r < CL; ++r) Z += csum[r];
 
   // stage 2: P_t = (e_t << 24) / Z, 24 fractional bits
   const float rz = rcp_estimate((float)Z);  // Z >= 2^30: the largest score's entry is 2^30
@@ -639,7 +647,6 @@ __global__ void __launch_bounds__(kLThreads, 1) k_attention_long(const AttnParam
       atomicAdd(p.o_acc + (size_t)h * hd + j, sum);
     }
   }
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 }  // namespace
