@@ -52,6 +52,13 @@ struct ck_model {
     cudaGraphExec_t exec;
   };
   std::vector<Graph> graphs;
+  struct BatchGraph {  // a batched pass's kernels for a row count and position bound
+    uint32_t n, max_positions;
+    uint8_t* work;
+    uint32_t cap;
+    cudaGraphExec_t exec;
+  };
+  std::vector<BatchGraph> bgraphs;
 };
 
 namespace {
@@ -738,6 +745,11 @@ PrefillModel prefill_model(const ck_model* m) {
   return pm;
 }
 
+void drop_batch_graphs(ck_model* m) {
+  for (auto& g : m->bgraphs) cudaGraphExecDestroy(g.exec);
+  m->bgraphs.clear();
+}
+
 // The batched kernels' scratch, laid out for at least `rows` rows.
 int ensure_batch_work(ck_model* m, uint32_t rows) {
   if (!m->pf_configured) {
@@ -747,6 +759,7 @@ int ensure_batch_work(ck_model* m, uint32_t rows) {
   if (m->pf_work && m->pf_wcap >= rows) return CK_OK;
   const uint32_t cap = std::max(rows, m->pf_wcap);
   const size_t need = prefill_work_bytes(prefill_model(m), cap);
+  drop_batch_graphs(m);  // they point into the scratch
   if (m->pf_work) CK_CUDA(cudaFree(m->pf_work));
   m->pf_work = nullptr;
   m->pf_bytes = 0;
@@ -754,6 +767,37 @@ int ensure_batch_work(ck_model* m, uint32_t rows) {
   CK_CUDA(cudaMalloc(&m->pf_work, need));
   m->pf_bytes = need;
   m->pf_wcap = cap;
+  return CK_OK;
+}
+
+// The batched pass's kernels for n rows and a position bound, as a CUDA graph (captured at
+// first use, kept in a small cache): one launch per pass instead of one per kernel.
+int get_batch_graph(ck_model* m, uint32_t n, uint32_t max_positions, cudaGraphExec_t* out) {
+  for (auto& g : m->bgraphs)
+    if (g.n == n && g.max_positions == max_positions && g.work == m->pf_work && g.cap == m->pf_wcap) {
+      *out = g.exec;
+      return CK_OK;
+    }
+  if (m->bgraphs.size() >= 8) {
+    cudaGraphExecDestroy(m->bgraphs.front().exec);
+    m->bgraphs.erase(m->bgraphs.begin());
+  }
+  CK_CUDA(cudaStreamBeginCapture(m->capture, cudaStreamCaptureModeThreadLocal));
+  const cudaError_t ek = enqueue_batch_kernels(prefill_model(m), n, max_positions, m->pf_work, m->pf_wcap,
+                                               m->capture);
+  cudaGraph_t graph = nullptr;
+  cudaError_t e = cudaStreamEndCapture(m->capture, &graph);
+  if (ek != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    return CK_CUDA_ERROR;
+  }
+  if (e != cudaSuccess) return CK_CUDA_ERROR;
+  cudaGraphExec_t exec;
+  e = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) return CK_CUDA_ERROR;
+  m->bgraphs.push_back({n, max_positions, m->pf_work, m->pf_wcap, exec});
+  *out = exec;
   return CK_OK;
 }
 
@@ -979,6 +1023,7 @@ int ck_model_config(const ck_model* m, ck_config* out) {
 int ck_set_prefill(ck_model* m, uint32_t positions) {
   if (!m || positions > kMaxPrefillChunk) return CK_INVALID_ARGUMENT;
   m->pf_cap = positions;
+  drop_batch_graphs(m);
   if (m->pf_work) cudaFree(m->pf_work);  // resized at next use
   m->pf_work = nullptr;
   m->pf_bytes = 0;
@@ -988,6 +1033,7 @@ int ck_set_prefill(ck_model* m, uint32_t positions) {
 
 void ck_free_model(ck_model* m) {
   if (!m) return;
+  drop_batch_graphs(m);
   if (m->pf_work) cudaFree(m->pf_work);
   for (auto& g : m->graphs) cudaGraphExecDestroy(g.exec);
   if (m->capture) cudaStreamDestroy(m->capture);
@@ -1133,7 +1179,7 @@ int ck_turn_batch(ck_model* m, void* const* dev_states, const size_t* lens, uint
     CK_CUDA(batch_gather_headers(pm, ptrs.data(), (uint32_t)idx.size(), m->pf_work, m->pf_wcap, h0.data(), s));
   std::vector<RowDesc> rows;
   std::vector<uint32_t> row_of;  // index into dev_states of each row
-  uint32_t max_positions = 1;
+  uint32_t max_positions = 1, max_cache = 1;
   for (size_t j = 0; j < idx.size(); ++j) {
     const uint32_t i = idx[j];
     HostHeader h;
@@ -1160,10 +1206,19 @@ int ck_turn_batch(ck_model* m, void* const* dev_states, const size_t* lens, uint
     rows.push_back(r);
     row_of.push_back(i);
     max_positions = std::max(max_positions, r.pos + 1);
+    max_cache = std::max(max_cache, r.cache);
     out[i].generated = h.u32(kHGenerated);  // before; replaced below
   }
   if (!rows.empty()) {
-    CK_CUDA(enqueue_batch(pm, rows.data(), (uint32_t)rows.size(), max_positions, m->pf_work, m->pf_wcap, s));
+    // the position bound rounded up to a multiple of 128 (within the largest cache: the
+    // attention's shared memory is checked for every row's cache), so that one graph serves
+    // many passes
+    const uint32_t bound = std::min(max_cache, (max_positions + 127) / 128 * 128);
+    CK_CUDA(upload_batch_rows(pm, rows.data(), (uint32_t)rows.size(), m->pf_work, m->pf_wcap, s));
+    cudaGraphExec_t exec;
+    rc = get_batch_graph(m, (uint32_t)rows.size(), bound, &exec);
+    if (rc) return rc;
+    CK_CUDA(cudaGraphLaunch(exec, s));
     std::vector<uint8_t*> rptrs;
     for (const RowDesc& r : rows) rptrs.push_back(r.st);
     CK_CUDA(batch_gather_headers(pm, rptrs.data(), (uint32_t)rows.size(), m->pf_work, m->pf_wcap, h1.data(), s));

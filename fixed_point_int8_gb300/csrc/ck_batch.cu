@@ -1326,12 +1326,25 @@ cudaError_t batch_gather_headers(const PrefillModel& m, uint8_t* const* host_sta
   return cudaStreamSynchronize(s);
 }
 
-cudaError_t enqueue_batch(const PrefillModel& m, const RowDesc* host_rows, uint32_t n, uint32_t max_positions,
-                          uint8_t* work, uint32_t cap, cudaStream_t s) {
+cudaError_t upload_batch_rows(const PrefillModel& m, const RowDesc* host_rows, uint32_t n, uint8_t* work,
+                              uint32_t cap, cudaStream_t s) {
   if (n == 0 || n > cap) return cudaErrorInvalidValue;
   const WorkLayout w = work_layout(m, cap);
-  cudaError_t e = cudaMemcpyAsync(work + w.rows, host_rows, sizeof(RowDesc) * n, cudaMemcpyHostToDevice, s);
+  return cudaMemcpyAsync(work + w.rows, host_rows, sizeof(RowDesc) * n, cudaMemcpyHostToDevice, s);
+}
+
+cudaError_t enqueue_batch(const PrefillModel& m, const RowDesc* host_rows, uint32_t n, uint32_t max_positions,
+                          uint8_t* work, uint32_t cap, cudaStream_t s) {
+  cudaError_t e = upload_batch_rows(m, host_rows, n, work, cap, s);
   if (e != cudaSuccess) return e;
+  return enqueue_batch_kernels(m, n, max_positions, work, cap, s);
+}
+
+cudaError_t enqueue_batch_kernels(const PrefillModel& m, uint32_t n, uint32_t max_positions, uint8_t* work,
+                                  uint32_t cap, cudaStream_t s) {
+  if (n == 0 || n > cap) return cudaErrorInvalidValue;
+  const WorkLayout w = work_layout(m, cap);
+  cudaError_t e;
   if ((e = enqueue_rows(m, nullptr, w, work, n, max_positions, true, s)) != cudaSuccess) return e;
   k_mfinish<<<n, kFinishThreads, 0, s>>>(reinterpret_cast<const RowDesc*>(work + w.rows),
                                          reinterpret_cast<const int64_t*>(work + w.X), m.cfg.dim,

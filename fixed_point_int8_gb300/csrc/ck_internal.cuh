@@ -567,6 +567,13 @@ cudaError_t batch_gather_headers(const PrefillModel& m, uint8_t* const* host_sta
 // row generates; max_positions bounds every row's pos + 1.
 cudaError_t enqueue_batch(const PrefillModel& m, const RowDesc* host_rows, uint32_t n, uint32_t max_positions,
                           uint8_t* work, uint32_t cap, cudaStream_t s);
+// The same in two parts: the descriptors' copy into the scratch, then the kernels (which read
+// every per-row value from the descriptors, so that one capture serves many passes of the
+// same row count and position bound).
+cudaError_t upload_batch_rows(const PrefillModel& m, const RowDesc* host_rows, uint32_t n, uint8_t* work,
+                              uint32_t cap, cudaStream_t s);
+cudaError_t enqueue_batch_kernels(const PrefillModel& m, uint32_t n, uint32_t max_positions, uint8_t* work,
+                                  uint32_t cap, cudaStream_t s);
 
 cudaError_t configure_step(size_t optin, size_t* dynamic_max);
 cudaError_t launch_step(const StepParams& p, cudaStream_t s, int grid, size_t smem);
