@@ -726,6 +726,41 @@ def test_batched_runs_match_the_oracle(ck):
     assert P.gpu.turn_batch([sg, sg])[0] == 10                      # the same state twice
 
 
+def test_batched_pass_graphs_across_bounds_counts_and_scratch_changes(ck):
+    """The batched pass replays a CUDA graph captured per row count and position bound (the
+    largest position rounded up to a multiple of 128): runs whose positions cross 128,
+    passes that alternate between all runs and two of them, and a change of the prefill
+    chunk (which frees the scratch the graphs point into) between passes; every run's state
+    against the oracle after every pass it takes part in."""
+    wl = MODELS["gqa"]
+    P = Pair(ck, wl.spec, "kernels")
+    runs = []
+    for r, (n_prompt, steps) in enumerate([(120, 24), (100, 40), (126, 12)]):
+        ids = synth.prompt_ids(wl.spec, n_prompt, run=r)
+        so, sg = P.init(ck, ids, steps)
+        rco, _ = P.orc.turn(so, n_prompt - 1)
+        rcg, _ = P.gpu.turn(sg, n_prompt - 1)
+        assert rco == rcg == 0
+        runs.append([so, sg, n_prompt, steps])
+    positions = set()
+    for i in range(30):
+        live = [r for r in runs if oracle.header(r[0])["phase"] == oracle.PHASE_RUNNING]
+        if not live:
+            break
+        if i % 3 == 1:
+            live = live[:2]
+        if i == 12:
+            assert P.gpu.set_prefill(64) == 0
+        rc, res, rcs = P.gpu.turn_batch([r[1] for r in live])
+        assert rc == 0 and rcs == [0] * len(live), (i, rc, rcs)
+        for r, got in zip(live, res):
+            positions.add(oracle.header(r[0])["position"])
+            rco, reso = P.orc.turn(r[0], 1)
+            assert rco == 0 and reso == got, (i, reso, got)
+            compare_states(P.orc, r[0], ck.state_download(r[1]), r[2], r[3], f"pass {i}")
+    assert min(positions) < 128 <= max(positions)
+
+
 def test_batched_runs_fail_like_the_oracle(ck):
     """Literal tiny runs overflow their caches at different positions: each failing run
     fails alone, with the oracle's key, in the pass that reaches it, while the others go
