@@ -246,13 +246,13 @@ __global__ void __launch_bounds__(kRowThreads) k_bplanes(const uint8_t* gate, co
 
 // ------------------------------------------------------------------ the contraction
 
-// The 5th-generation tensor cores (tcgen05): one thread issues 128 x N x 16 MMAs whose
-// operands are read from shared memory through matrix descriptors and whose f32
-// accumulators live in tensor memory (TMEM).  Both operands are K-major with the 128-byte
-// swizzle: 8-row atoms of 128-byte rows, row r's 16-byte chunk j at j ^ (r & 7), atoms
-// 1,024 bytes apart.  The weights' column-group layout is that pattern for bytes, so a
-// weight tile arrives with one bulk copy and is widened to f16 in place of layout; the
-// planes are stored in it as f16.
+// The 5th-generation tensor cores (tcgen05): one thread issues 128 x N x 16 MMAs whose f32
+// accumulators live in tensor memory (TMEM); A (the weights widened to f16) is read from
+// tensor memory, B (the planes) from shared memory through a matrix descriptor: K-major with
+// the 128-byte swizzle, 8-row atoms of 128-byte rows, row r's 16-byte chunk j at j ^ (r & 7),
+// atoms 1,024 bytes apart.  The weights' column-group layout is that pattern for bytes, so
+// a weight tile arrives with one bulk copy and each row is found at a fixed place to widen;
+// the planes are stored in the pattern as f16.
 constexpr uint32_t kTN = 192;                  // most plane columns per block (three planes of 64)
 constexpr uint32_t kTcConvWarps = 8;           // widen the weights, drain the accumulators
 constexpr int kTcThreads = 32 * (kTcConvWarps + 2);  // + a producer warp and an MMA warp
