@@ -230,9 +230,12 @@ int ck_turn(ck_model* m, void* dev_state, size_t len, uint32_t n_positions, void
  * device state pointers with their lengths in lens (host arrays); out and rcs (host arrays
  * of n_states) receive each state's turn result and return code: 0, 3 (misaligned, not
  * this model's, complete or failed: that state is left untouched), or 8 (a cache store did
- * not fit: that run is failed).  Synchronizes `stream`.  Returns the first nonzero rcs[i],
- * else 0; 10 for null arguments, repeated states or n_states of 0 or above 4096 (nothing is
- * run), 9 for a CUDA error. */
+ * not fit: that run is failed).  Synchronizes `stream`.  The pass's kernels run as one
+ * CUDA-graph replay; the graphs (one per number of runs taking part and bound on their
+ * positions, in steps of 128) are kept with the model, at most eight, and dropped by
+ * ck_set_prefill and ck_free_model.  Returns the first nonzero rcs[i], else 0; 10 for null
+ * arguments, repeated states or n_states of 0 or above 4096 (nothing is run), 9 for a CUDA
+ * error. */
 int ck_turn_batch(ck_model* m, void* const* dev_states, const size_t* lens, uint32_t n_states,
                   void* stream, ck_turn_result* out, int* rcs);
 
