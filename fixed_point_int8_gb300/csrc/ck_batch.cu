@@ -615,7 +615,10 @@ struct BEpiParams {
   int64_t* H;
   uint32_t hidden;
   const int32_t* silu_tab;
-  unsigned long long* or_out;     // SiLU: the output vector's OR word
+  unsigned long long* or_out;     // SiLU, residual with norm: the output vector's OR word
+  // residual followed by the next RMS normalization (k_bresnorm): its weights and output
+  int64_t* XB;
+  const int32_t* norm_w;
 };
 
 // y[n][r] = ((sum_k S_k[n][r] << 8k) * scale[r]) >> 24, wrapping, for rows r and r + 1 (r
@@ -709,6 +712,87 @@ __global__ void __launch_bounds__(kRowThreads) k_bepi(const BEpiParams p) {
     }
   }
   if (p.mode == kBEpiSiLU) block_or_to(o, p.or_out, red);
+}
+
+// Phases 11/16 and the normalization after them in one launch, one block per position row
+// (kNormThreads threads): the residual X[n][r] += y[n][r] from the contraction's plane sums
+// (as k_bepi's residual mode), then "RMS normalization" of the updated row into XB exactly as
+// k_bnorm, the outputs' magnitudes ORed into *or_out.  Thread t takes the row pairs t,
+// t + kNormThreads, ...; the first kNormPer / 2 of them stay in registers between the sum of
+// squares and the division, the rest (rows beyond 4,096) are read back.
+__global__ void __launch_bounds__(kNormThreads) k_bresnorm(const BEpiParams p) {
+  __shared__ unsigned long long red[kNormThreads / 32];
+  __shared__ InvDiv div;
+  constexpr int kPairs = kNormPer / 2;
+  const uint32_t d = p.rows, n = blockIdx.x;
+  int32_t wv[kNormPer];
+#pragma unroll
+  for (int j = 0; j < kNormPer; ++j) {
+    const uint32_t e = 2 * (threadIdx.x + (j >> 1) * kNormThreads) + (j & 1);
+    wv[j] = e < d ? __ldg(p.norm_w + e) : 0;
+  }
+  const InvDiv Dd = make_invdiv_fast(d);  // floor(ss / d) by a multiply
+  pdl_enter();
+  if (!running(p.gate)) return;
+  const int L = limbs_of_or(*p.orw);
+  int64_t* x = p.X + (size_t)n * d;
+  int64_t* y = p.XB + (size_t)n * d;
+  int64_t xv[kNormPer];
+  unsigned long long ss = 0;
+#pragma unroll
+  for (int j = 0; j < kPairs; ++j) {
+    const uint32_t r = 2 * (threadIdx.x + j * kNormThreads);
+    xv[2 * j] = xv[2 * j + 1] = 0;
+    if (r < d) {
+      int64_t y0, y1;
+      combine_pair(p, L, n, r, y0, y1);
+      xv[2 * j] = wadd(x[r], y0);
+      x[r] = xv[2 * j];
+      if (r + 1 < d) {
+        xv[2 * j + 1] = wadd(x[r + 1], y1);
+        x[r + 1] = xv[2 * j + 1];
+      }
+    }
+    ss += (unsigned long long)xv[2 * j] * (unsigned long long)xv[2 * j] +
+          (unsigned long long)xv[2 * j + 1] * (unsigned long long)xv[2 * j + 1];
+  }
+  for (uint32_t r = 2 * (threadIdx.x + kPairs * kNormThreads); r < d; r += 2 * kNormThreads) {
+    int64_t y0, y1;
+    combine_pair(p, L, n, r, y0, y1);
+    const int64_t a = wadd(x[r], y0);
+    x[r] = a;
+    ss += (unsigned long long)a * (unsigned long long)a;
+    if (r + 1 < d) {
+      const int64_t b = wadd(x[r + 1], y1);
+      x[r + 1] = b;
+      ss += (unsigned long long)b * (unsigned long long)b;
+    }
+  }
+  ss = block_sum(ss, red);  // (its barriers also order the residual stores before the reads below)
+  if (threadIdx.x == 0) {
+    uint64_t rms = isqrt_u64(udiv_inv(ss, Dd) + 42950ull);
+    if (rms < 1) rms = 1;
+    div = make_invdiv_fast((uint32_t)rms);
+  }
+  __syncthreads();
+  const InvDiv D = div;
+  unsigned long long o = 0;
+#pragma unroll
+  for (int j = 0; j < kNormPer; ++j) {
+    const uint32_t e = 2 * (threadIdx.x + (j >> 1) * kNormThreads) + (j & 1);
+    if (e < d) {
+      const int64_t v = sdiv_trunc(wmul(xv[j], (int64_t)wv[j]), D) >> 8;
+      y[e] = v;
+      o |= (unsigned long long)(v ^ (v >> 63));
+    }
+  }
+  for (uint32_t e = 2 * (threadIdx.x + kPairs * kNormThreads); e < d; e += 2 * kNormThreads)
+    for (uint32_t u = 0; u < 2 && e + u < d; ++u) {
+      const int64_t v = sdiv_trunc(wmul(x[e + u], (int64_t)__ldg(p.norm_w + e + u)), D) >> 8;
+      y[e + u] = v;
+      o |= (unsigned long long)(v ^ (v >> 63));
+    }
+  block_or_to(o, p.or_out, red);
 }
 
 // ------------------------------------------------------------------ attention
@@ -1159,6 +1243,18 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
     const dim3 grid((nrows + kBM - 1) / kBM, (8 * Npad + kTN - 1) / kTN, splits_for(nrows, KG));
     launch_pdl(k_bgemm, grid, dim3(kTcThreads), kTcSmem, s, gate, Wm, nrows, KG, (const uint8_t*)B, Npad, ow, S, fault);
   };
+  // a residual epilogue together with the normalization that follows it (one block a row)
+  auto resnorm = [&](BEpiParams p, const int32_t* norm_w, unsigned long long* or_out) {
+    p.gate = gate;
+    p.rdesc = rows;
+    p.S = S;
+    p.Npad = Npad;
+    p.P = P;
+    p.XB = XB;
+    p.norm_w = norm_w;
+    p.or_out = or_out;
+    launch_pdl(k_bresnorm, dim3(P), dim3(kNormThreads), 0, s, p);
+  };
   auto epi = [&](BEpiParams p) {
     p.gate = gate;
     p.rdesc = rows;
@@ -1174,8 +1270,10 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
   for (uint32_t l = 0; l < c.layers; ++l) {
     const DevLayer& Wl = m.layers[l];
     unsigned long long* o4 = orw + 4 * l;
-    // phases 4-8: attention norm, Q/K/V rows, checked cache stores, rotary
-    launch_pdl(k_bnorm, dim3(P), dim3(kNormThreads), 0, s, gate, (const int64_t*)X, XB, Wl.attn_norm, c.dim, o4 + 0);
+    // phases 4-8: attention norm (after layer 0 done by the previous layer's last launch),
+    // Q/K/V rows, checked cache stores, rotary
+    if (l == 0)
+      launch_pdl(k_bnorm, dim3(P), dim3(kNormThreads), 0, s, gate, (const int64_t*)X, XB, Wl.attn_norm, c.dim, o4 + 0);
     planes(XB, c.dim, c.dim, KGd, o4 + 0, c.dim + 2 * m.kv_dim, KGd);
     gemm(Wl.wqkv, c.dim + 2 * m.kv_dim, KGd, o4 + 0);
     BEpiParams pq = {};
@@ -1215,9 +1313,8 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
     po.scale = Wl.so;
     po.mode = kBEpiResid;
     po.X = X;
-    epi(po);
-    // phases 12-14: feed-forward norm, gate and up rows, SiLU gating
-    launch_pdl(k_bnorm, dim3(P), dim3(kNormThreads), 0, s, gate, (const int64_t*)X, XB, Wl.ffn_norm, c.dim, o4 + 2);
+    // phases 12-14: feed-forward norm (in the residual's launch), gate and up rows, SiLU gating
+    resnorm(po, Wl.ffn_norm, o4 + 2);
     planes(XB, c.dim, c.dim, KGd, o4 + 2, 2 * c.hidden, KGd);
     gemm(Wl.w13, 2 * c.hidden, KGd, o4 + 2);
     BEpiParams pg = {};
@@ -1239,12 +1336,16 @@ cudaError_t enqueue_rows(const PrefillModel& m, const uint8_t* gate, const WorkL
     pd.scale = Wl.s2;
     pd.mode = kBEpiResid;
     pd.X = X;
-    epi(pd);
+    if (l + 1 < c.layers)  // with the next layer's attention norm
+      resnorm(pd, m.layers[l + 1].attn_norm, orw + 4 * (l + 1));
+    else if (classify)     // with the final norm
+      resnorm(pd, m.final_norm, orw + 4 * c.layers);
+    else
+      epi(pd);
   }
   if (classify) {
     // phases 17-18: final norm and classifier rows (written only for generating rows)
-    unsigned long long* of = orw + 4 * c.layers;
-    launch_pdl(k_bnorm, dim3(P), dim3(kNormThreads), 0, s, gate, (const int64_t*)X, XB, m.final_norm, c.dim, of);
+    unsigned long long* of = orw + 4 * c.layers;  // the final norm ran with the last residual
     planes(XB, c.dim, c.dim, KGd, of, c.vocab, KGd);
     gemm(m.cls, c.vocab, KGd, of);
     BEpiParams pc = {};
