@@ -1434,13 +1434,6 @@ cudaError_t upload_batch_rows(const PrefillModel& m, const RowDesc* host_rows, u
   return cudaMemcpyAsync(work + w.rows, host_rows, sizeof(RowDesc) * n, cudaMemcpyHostToDevice, s);
 }
 
-cudaError_t enqueue_batch(const PrefillModel& m, const RowDesc* host_rows, uint32_t n, uint32_t max_positions,
-                          uint8_t* work, uint32_t cap, cudaStream_t s) {
-  cudaError_t e = upload_batch_rows(m, host_rows, n, work, cap, s);
-  if (e != cudaSuccess) return e;
-  return enqueue_batch_kernels(m, n, max_positions, work, cap, s);
-}
-
 cudaError_t enqueue_batch_kernels(const PrefillModel& m, uint32_t n, uint32_t max_positions, uint8_t* work,
                                   uint32_t cap, cudaStream_t s) {
   if (n == 0 || n > cap) return cudaErrorInvalidValue;

@@ -563,13 +563,10 @@ cudaError_t enqueue_prefill(const PrefillModel& m, uint8_t* st, const StateLayou
 // Copies the 256-byte headers of n states (device pointers) to host_out; synchronizes.
 cudaError_t batch_gather_headers(const PrefillModel& m, uint8_t* const* host_states, uint32_t n,
                                  uint8_t* work, uint32_t cap, uint8_t* host_out, cudaStream_t s);
-// One position of each of n runs (host_rows: their descriptors), with phases 17-19 where a
-// row generates; max_positions bounds every row's pos + 1.
-cudaError_t enqueue_batch(const PrefillModel& m, const RowDesc* host_rows, uint32_t n, uint32_t max_positions,
-                          uint8_t* work, uint32_t cap, cudaStream_t s);
-// The same in two parts: the descriptors' copy into the scratch, then the kernels (which read
-// every per-row value from the descriptors, so that one capture serves many passes of the
-// same row count and position bound).
+// One position of each of n runs, with phases 17-19 where a row generates, in two parts: the
+// descriptors' copy (host_rows) into the scratch, then the kernels, which read every per-row
+// value from the descriptors, so that one capture serves many passes of the same row count;
+// max_positions bounds every row's pos + 1.
 cudaError_t upload_batch_rows(const PrefillModel& m, const RowDesc* host_rows, uint32_t n, uint8_t* work,
                               uint32_t cap, cudaStream_t s);
 cudaError_t enqueue_batch_kernels(const PrefillModel& m, uint32_t n, uint32_t max_positions, uint8_t* work,
